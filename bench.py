@@ -1,0 +1,407 @@
+"""Benchmark of the quantized-KV decode path on GB300.
+
+Workload (the headline configuration): GQA decode, batch 8, 32 query heads over 8 KV heads,
+head dim 128, context 32768, bf16 K/V with Student-t(3) coordinates scaled to unit variance,
+N(0,1) queries; schemes Plain-KV, TQ-KV, KQV and QKQV at n = 4 bits per coordinate.
+One step = for each scheme: quantize-append one new token per (batch, KV head) at position
+T-1 (the cache is pre-filled with T-1 tokens) and decode attention of every query head over the
+T cached tokens.  Each scheme's cache (285-294 MB) is larger than L2 (129 MB) and the four are
+visited in turn, so every step streams its caches from HBM.
+
+Metric: cache-tokens/s = sum over schemes of B * H_kv * T / step time (one cache token = one
+(batch, KV head, token) record with its K and V).  The roofline object reports the decode
+kernels' algorithmic packed bytes / measured decode time against the measured HBM peak.
+
+``--impl reference`` times the float64 CPU oracle on the host cores on a bounded sample of the
+same workload (one slab per scheme per step).  Under torchrun every rank runs the full workload
+on its own GPU (independent batches, no collective): weak scaling.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attention cache-tokens/s and HBM GB/s (% peak); append tok/s"
+UNIT = "cache-tokens/s"
+WORKLOAD = ("GQA decode B=8 Hq=32 Hkv=8 d=128 T=32768, bf16 Student-t(3) K/V; "
+            "Plain-KV, TQ-KV, KQV, QKQV at n=4; step = per scheme: append 1 token per slab + decode")
+SCHEMES = [("plain", 4), ("tq", 4), ("kqv", 4), ("qkqv", 4)]
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def record_bytes(scheme, n, d=128, m=128):
+    """Packed bytes of one cache record (K and V of one token of one slab)."""
+    from turboquant_quantized_kv_tq_gb300.binding import SCHEMES as S, tq_config, tq_config_from_scheme
+    c = tq_config()
+    tq_config_from_scheme(S[scheme], n, c)
+    total = 0
+    for cd in (c.k, c.v):
+        total += d * cd.bits // 8 + 4
+        if cd.qjl:
+            total += m // 8 + 2
+    return total
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def build_caches(inp, device, T):
+    """One QuantizedKVCache per scheme, pre-filled with T-1 tokens (untimed)."""
+    import torch
+    from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
+    caches = []
+    K = torch.from_numpy(inp.K.view(np.int16)).view(torch.bfloat16)
+    V = torch.from_numpy(inp.V.view(np.int16)).view(torch.bfloat16)
+    chunk = 4096
+    for scheme, n in SCHEMES:
+        kv = QuantizedKVCache(inp.d, inp.Hq, inp.Hkv, inp.B, T, scheme=scheme, n=n, seed=inp.seed, device=device)
+        for s in range(0, T - 1, chunk):
+            e = min(T - 1, s + chunk)
+            kv.append(K[:, :, s:e].to(device), V[:, :, s:e].to(device), [s] * inp.B)
+        caches.append(kv)
+    torch.cuda.synchronize(device)
+    return caches
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    inp = make_inputs("cfg2")
+    B, Hq, Hkv, d, T = inp.B, inp.Hq, inp.Hkv, inp.d, inp.T
+    caches = build_caches(inp, device, T)
+    # the token appended every step (position T-1) and the step's queries
+    k_new = torch.from_numpy(inp.K[:, :, T - 1:T].view(np.int16)).view(torch.bfloat16).to(device)
+    v_new = torch.from_numpy(inp.V[:, :, T - 1:T].view(np.int16)).view(torch.bfloat16).to(device)
+    q = torch.from_numpy(inp.q).to(device)
+    outs = [torch.empty_like(q) for _ in caches]
+    seq = [T] * B
+    start = [T - 1] * B
+    for kv in caches:
+        kv.workspace(T)
+    stream = torch.cuda.current_stream(device)
+    n_dec = len(caches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_dec)]
+
+    def step(timed_events=None):
+        for i, kv in enumerate(caches):
+            kv.append(k_new, v_new, start)
+            if timed_events is not None:
+                timed_events[i][0].record(stream)
+            kv.decode(q, seq, out=outs[i])
+            if timed_events is not None:
+                timed_events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    dec_ms = [0.0] * n_dec
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    per_step_events = []
+    for _ in range(args.steps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_dec)]
+        step(evs)
+        per_step_events.append(evs)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    for evs in per_step_events:
+        for i in range(n_dec):
+            dec_ms[i] += evs[i][0].elapsed_time(evs[i][1])
+    dec_ms = [x / args.steps for x in dec_ms]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = n_dec * B * Hkv * T
+    value = world * tokens_per_step / (ms_per_step * 1e-3)
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, caches, inp, device, seq, start)
+
+    # ---- append throughput on the prefill chunk of the long-context configuration
+    append = run_prefill_append(args, device) if not args.skip_append else None
+
+    peak, peak_kind = measured_peak()
+    rec = [record_bytes(s, n) for s, n in SCHEMES]
+    dec_bytes = [B * Hkv * T * r for r in rec]
+    achieved = sum(dec_bytes) / (sum(dec_ms) * 1e-3) / 1e9
+    schemes = {f"{s}{n}": {"decode_us": round(dec_ms[i] * 1e3, 2),
+                           "record_bytes": rec[i],
+                           "GB_per_s": round(dec_bytes[i] / (dec_ms[i] * 1e-3) / 1e9, 1),
+                           "cache_tokens_per_s": round(B * Hkv * T / (dec_ms[i] * 1e-3), 1)}
+               for i, (s, n) in enumerate(SCHEMES)}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded numpy PCG64; no public dataset)",
+        "config": {"workload": WORKLOAD, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": d,
+                   "context": T, "schemes": [f"{s}-n{n}" for s, n in SCHEMES],
+                   "l2": "inputs larger than L2: four caches of 285-294 MB visited per step",
+                   "arith": "append fp32; decode scores/readout fp16 MMA operands, fp32 accumulation",
+                   "parallelism": f"independent replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "kernel": "decode (query prep + fused split-K decode), all four schemes",
+                     "peak_kind": peak_kind},
+        "schemes": schemes,
+        "e2e": e2e,
+        "append": append,
+        "gpu_launches": args.steps * n_dec * 3,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, caches, budget_s=args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, caches, inp, device, seq, start):
+    """Same step through the public API, with the step's inputs copied from pinned host memory and
+    the outputs read back to the host inside the timed region."""
+    import torch
+    B, T = inp.B, inp.T
+    k_host = torch.from_numpy(inp.K[:, :, T - 1:T].copy().view(np.int16)).view(torch.bfloat16).pin_memory()
+    v_host = torch.from_numpy(inp.V[:, :, T - 1:T].copy().view(np.int16)).view(torch.bfloat16).pin_memory()
+    q_host = torch.from_numpy(inp.q.copy()).pin_memory()
+    out_host = [torch.empty(q_host.shape, dtype=torch.float32).pin_memory() for _ in caches]
+    k_dev = torch.empty(k_host.shape, dtype=k_host.dtype, device=device)
+    v_dev = torch.empty_like(k_dev)
+    q_dev = torch.empty(q_host.shape, dtype=torch.float32, device=device)
+    outs = [torch.empty_like(q_dev) for _ in caches]
+
+    def step():
+        k_dev.copy_(k_host, non_blocking=True)
+        v_dev.copy_(v_host, non_blocking=True)
+        q_dev.copy_(q_host, non_blocking=True)
+        for i, kv in enumerate(caches):
+            kv.append(k_dev, v_dev, start)
+            kv.decode(q_dev, seq, out=outs[i])
+            out_host[i].copy_(outs[i], non_blocking=True)
+        torch.cuda.current_stream(device).synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t
+    h2d = (k_host.numel() * 2 + v_host.numel() * 2 + q_host.numel() * 4)
+    d2h = sum(o.numel() * 4 for o in out_host)
+    value = len(caches) * B * inp.Hkv * T * args.steps / el
+    return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def run_prefill_append(args, device):
+    """Quantize-append of a 4096-token prefill chunk (long-context configuration, KQV n=4)."""
+    import torch
+    from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
+    B, Hkv, d, T, n_new = 1, 8, 128, 131072, 4096
+    rng = np.random.default_rng(3)
+    std = np.exp(rng.uniform(np.log(0.1), np.log(10.0), size=(2, Hkv, 1, d))).astype(np.float32)
+    k = torch.from_numpy((std[0] * rng.standard_normal((B, Hkv, n_new, d))).astype(np.float32)).to(device).bfloat16()
+    v = torch.from_numpy((std[1] * rng.standard_normal((B, Hkv, n_new, d))).astype(np.float32)).to(device).bfloat16()
+    kv = QuantizedKVCache(d, 64, Hkv, B, T, scheme="kqv", n=4, seed=3, device=device)
+    start = [T - n_new] * B
+    for _ in range(3):
+        kv.append(k, v, start)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record()
+    for _ in range(reps):
+        kv.append(k, v, start)
+    e1.record()
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / reps
+    vec = 2 * B * Hkv * n_new
+    moved = vec * d * 2 + B * Hkv * n_new * record_bytes("kqv", 4)
+    return {"workload": "B=1 Hkv=8 d=128, 4096-token prefill chunk into a 131072-token KQV n=4 cache",
+            "tok_per_s": round(B * n_new / (ms * 1e-3), 1), "vectors_per_s": round(vec / (ms * 1e-3), 1),
+            "us": round(ms * 1e3, 2), "GB_per_s": round(moved / (ms * 1e-3) / 1e9, 1)}
+
+
+def oracle_step(inp, bufs, ctxs, slabs, T):
+    """The oracle decodes the given slabs of every scheme over T tokens."""
+    done = 0
+    for orc, buf in zip(ctxs, bufs):
+        for (b, h) in slabs:
+            orc.decode(buf, inp.q, [T] * inp.B, slabs=[(b, h)])
+            done += T
+    return done
+
+
+def cpu_baseline(inp, caches, budget_s=20.0):
+    """The float64 oracle on the host cores: decode of whole slabs of each scheme's cache (the
+    cache bytes the GPU wrote), as many slabs as fit in about ``budget_s`` seconds."""
+    from oracle.pipeline import OracleContext
+    from oracle import codec as ocodec
+    T = inp.T
+    ctxs, bufs = [], []
+    for (scheme, n), kv in zip(SCHEMES, caches):
+        kc, vc = ocodec.scheme_codecs(scheme, n)
+        ctxs.append(OracleContext(inp.d, inp.Hq, inp.Hkv, inp.B, T, kc, vc, inp.seed))
+        bufs.append(kv.cache.cpu().numpy())
+    slabs = [(b, h) for b in range(inp.B) for h in range(inp.Hkv)]
+    done, t = 0, time.perf_counter()
+    used = 0
+    for s in slabs:
+        done += oracle_step(inp, bufs, ctxs, [s], T)
+        used += 1
+        if time.perf_counter() - t > budget_s:
+            break
+    el = time.perf_counter() - t
+    return {"value": round(done / el, 1), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{used} of {len(slabs)} (batch, KV head) slabs x 4 schemes, each decoded over "
+                      f"{T} tokens for its {inp.Hq // inp.Hkv} query heads ({el:.1f} s)"}
+
+
+def run_reference(args):
+    """The oracle alone, on the host cores, timed per step on a bounded sample of the workload."""
+    from oracle import codec as ocodec
+    from oracle.pipeline import OracleContext
+    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    # one slab per scheme per step: inputs for batch 1, one KV head, full context
+    inp = make_inputs("cfg2", B=1, Hkv=1, Hq=4)
+    T = inp.T
+    ctxs, bufs = [], []
+    for scheme, n in SCHEMES:
+        kc, vc = ocodec.scheme_codecs(scheme, n)
+        orc = OracleContext(inp.d, inp.Hq, inp.Hkv, 1, T, kc, vc, inp.seed)
+        buf = orc.new_cache()
+        orc.append(buf, inp.k_f32()[:, :, :T].astype(np.float64), inp.v_f32()[:, :, :T].astype(np.float64), [0])
+        ctxs.append(orc)
+        bufs.append(buf)
+    for _ in range(args.warmup):
+        oracle_step(inp, bufs, ctxs, [(0, 0)], T)
+    t = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += oracle_step(inp, bufs, ctxs, [(0, 0)], T)
+    el = time.perf_counter() - t
+    value = done / el
+    sample = f"per step: one (batch, KV head) slab of each of the 4 schemes decoded over {T} tokens, 4 query heads"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy PCG64; no public dataset)",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-append", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per decode launch, when a capture of the current kernel exists")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

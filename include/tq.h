@@ -1,0 +1,197 @@
+/*
+ * tq.h -- C ABI of the rotated-codebook quantized KV cache for NVIDIA GB300 (sm_103a).
+ *
+ * The method (three technical summaries of papers, cited by page title and section):
+ *   [TQ-KV] "Resumen Técnico: Inferencia Estadística y Medidas de Calidad de Cuantizaciones
+ *           de Cache KV Inspiradas en TurboQuant" (gist.science/es/paper/2605.08114)
+ *   [ABL]   "Resumo Técnico: Ablação, Inferência Estatística e Validação para Compressão de
+ *           KV-Cache" (gist.science/pt/paper/2607.09683)
+ *   [HEADQ] "Resumo Técnico: HeadQ: Distorção Visível ao Modelo e Correção no Espaço de
+ *           Pontuação para Quantização de KV-Cache" (gist.science/pt/paper/2605.03562)
+ *
+ * Write path (tq_quantize_append): per K/V vector, split off the norm, rotate the unit vector
+ * with a seeded randomized Walsh-Hadamard transform y = H D u / sqrt(d), quantize each
+ * coordinate with a Lloyd-Max codebook for the Beta((d-1)/2,(d-1)/2) sphere marginal, pack the
+ * codes; optionally store a 1-bit QJL sketch sign(S r) of the residual r plus ||r||, and for
+ * HeadQ keys a 4-bit side code of the residual projected on a calibrated basis.
+ * Read path (tq_decode_attention): one fused split-K kernel reads the packed cache, forms
+ * scores (with the QJL or HeadQ logit corrections), runs an online softmax and accumulates the
+ * value readout (with the QJL value correction); a last-arriving block per (batch, KV head)
+ * merges the splits and applies the inverse rotation.
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns all device memory and all streams.  The library allocates no device
+ *     memory and never synchronizes, except tq_get_device_error, which waits on its stream.
+ *   - Calls are asynchronous and ordered on the given stream (a cudaStream_t; 0 = default).
+ *   - Arguments, capacity and workspace sizes are checked on the host before any launch; a
+ *     failed check launches nothing and returns the error.  Launch failures return
+ *     TQ_ERR_CUDA.  tq_last_error() gives a message for the calling thread's last error.
+ *   - A context is host memory.  It is read-only after tq_tables_upload (and
+ *     tq_headq_set_basis), and may then be shared by threads.
+ *   - Device pointers must be 16-byte aligned; the cache and table buffers 256-byte aligned.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st* tq_stream;
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, bad enum        */
+  TQ_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, G, bit width combination      */
+  TQ_ERR_CAPACITY = 3,     /* start + n_new or a sequence length beyond the cache capacity */
+  TQ_ERR_WORKSPACE = 4,    /* workspace smaller than tq_decode_workspace_bytes             */
+  TQ_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed                  */
+  TQ_ERR_DEVICE = 6,       /* a kernel recorded an error word (see tq_get_device_error)    */
+  TQ_ERR_STATE = 7         /* tables not uploaded / HeadQ basis not set                    */
+} tq_status;
+
+/* Schemes at n bits per coordinate ([TQ-KV] "Esquemas de Cuantización"; [ABL]
+ * "Contribuições Principais" 1):
+ *   TQ_PLAIN_KV  K, V: n-bit scalar code, no rotation, no sketch.
+ *   TQ_TQ_KV     K, V: rotation + n-bit code.
+ *   TQ_KQV       K: rotation + n-bit code; V: rotation + (n-1)-bit code + 1-bit QJL.
+ *   TQ_QKQV      K, V: rotation + (n-1)-bit code + 1-bit QJL (also named TQ-QKV). */
+typedef enum { TQ_PLAIN_KV = 0, TQ_TQ_KV = 1, TQ_KQV = 2, TQ_QKQV = 3 } tq_scheme;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+/* One side's codec: scalar code bits (1..4), rotation on/off, QJL residual sketch on/off. */
+typedef struct {
+  int32_t bits;
+  int32_t rotate;
+  int32_t qjl;
+} tq_codec;
+
+typedef struct {
+  int32_t head_dim;      /* d: 128, 256, 512 or 1024 on the GPU path                       */
+  int32_t num_q_heads;   /* H_q; query head h reads KV head h / (H_q / H_kv)               */
+  int32_t num_kv_heads;  /* H_kv; G = H_q / H_kv must be 1, 2, 4 or 8                      */
+  int32_t batch;         /* B <= TQ_MAX_BATCH                                              */
+  int32_t capacity;      /* tokens per (batch, KV head) slab; a multiple of 64             */
+  tq_codec k, v;
+  int32_t qjl_m;         /* QJL sketch rows m; 0 means m = d (the only value built)        */
+  int32_t headq_rank;    /* HeadQ rank r on the K side; 0 = off; 16 is the value built      */
+  int32_t headq_bits;    /* HeadQ side-code bits; 4 is the value built                     */
+  uint64_t seed;         /* drives the rotation signs D_K, D_V and sketches S_K, S_V        */
+} tq_config;
+
+#define TQ_MAX_BATCH 512
+#define TQ_LAYOUT_VERSION 1u
+
+/* One region of the cache buffer: [B][H_kv][capacity][record_bytes], record of token t of
+ * (b, h) at offset + ((b * H_kv + h) * capacity + t) * record_bytes.  record_bytes = 0 when
+ * the region is absent. */
+typedef struct {
+  uint64_t offset;
+  uint64_t record_bytes;
+} tq_region;
+
+/* The packed cache layout (version TQ_LAYOUT_VERSION).  Regions start on 256-byte boundaries,
+ * in the order of the fields below.  Codes are stored in sign-magnitude form
+ * (s = [c >= 2^(b-1)], k = magnitude rank) as streams of power-of-two widths, coordinate i of
+ * a w-bit stream in bits [w*i, w*i + w), least significant bit first:
+ *   b = 4: (s << 3) | k;  b = 3: 2-bit stream of k then 1-bit stream of s;
+ *   b = 2: (s << 1) | k;  b = 1: s.
+ * QJL signs: bit i = 1 iff (S r)_i >= 0.  HeadQ side code: 4-bit two's complement, zeta_0 in
+ * the low nibble.  Norms are fp32; rho and side scales fp16. */
+typedef struct {
+  uint32_t layout_version;
+  uint32_t reserved;
+  uint64_t total_bytes;
+  tq_region k_codes, k_norm, k_signs, k_rho, k_side, k_side_scale;
+  tq_region v_codes, v_norm, v_signs, v_rho;
+} tq_cache_layout;
+
+typedef struct tq_context tq_context;
+
+/* Fill cfg->k and cfg->v for a scheme at n bits per coordinate (n in 1..4; KQV and QKQV need
+ * n >= 2).  Other fields are left as they are.  [TQ-KV] "Esquemas de Cuantización". */
+tq_status tq_config_from_scheme(tq_scheme scheme, int32_t n, tq_config* inout);
+
+/* Validate cfg and build the host tables: the Beta Lloyd-Max codebooks of both sides
+ * ([ABL] "Configuração Experimental": data-oblivious Beta Lloyd-Max codebook; [TQ-KV]
+ * "Marco Teórico": the Beta sphere marginal), the rotation signs and the sketch matrices
+ * (SplitMix64 counter streams D_K=1, D_V=2, S_K=3, S_V=4 of cfg->seed).  Host only; no CUDA
+ * call.  *out receives a new context on TQ_OK. */
+tq_status tq_context_create(const tq_config* cfg, tq_context** out);
+void tq_context_destroy(tq_context* ctx);
+
+/* Bytes of the device table buffer the caller must provide to tq_tables_upload. */
+size_t tq_tables_bytes(const tq_context* ctx);
+
+/* Copy the host-built table blob (the same bytes tq_tables_upload sends) into host memory.
+ * Host only.  Blob layout: fp32 k_centroids[16], k_thresholds[16], v_centroids[16],
+ * v_thresholds[16]; fp32 k_signs[d], v_signs[d] (+1/-1); fp32 S_K[m][d] (if K has QJL);
+ * fp32 S_V[m][d] (if V has QJL); then the HeadQ basis area [H_kv][d][r] (zeros until
+ * tq_headq_set_basis).  Each array starts on a 256-byte boundary. */
+tq_status tq_tables_host(const tq_context* ctx, void* host_dst, size_t bytes);
+
+/* Copy the tables into dev_tables (tq_tables_bytes bytes, caller-owned, 256-byte aligned) on
+ * stream and bind that buffer to the context.  The buffer must outlive every later call. */
+tq_status tq_tables_upload(tq_context* ctx, void* dev_tables, tq_stream stream);
+
+/* HeadQ ([HEADQ] "Visão Geral do Algoritmo" 1): store the calibrated key-side basis.
+ * dev_U is fp32 [H_kv][d][r] on the device (column k of head h is U_h e_k).  The library keeps
+ * R_K U_h in the bound table buffer (a kernel on stream), so later calls see the basis in the
+ * rotated domain.  Needs headq_rank > 0 and tables uploaded. */
+tq_status tq_headq_set_basis(tq_context* ctx, const float* dev_U, tq_stream stream);
+
+tq_status tq_get_cache_layout(const tq_context* ctx, tq_cache_layout* out);
+
+/* Write path ([TQ-KV] "Esquemas de Cuantización"; [HEADQ] "Escrita no Cache").
+ * k, v: device [B][H_kv][n_new][d] of dtype.  Token j of (b, h) is stored at position
+ * host_start[b] + j.  host_start: host array of B entries with host_start[b] + n_new <=
+ * capacity.  n_new = 0 is a no-op.  dev_cache: total_bytes of tq_get_cache_layout. */
+tq_status tq_quantize_append(const tq_context* ctx, void* dev_cache, const void* k, const void* v,
+                             tq_dtype dtype, int32_t n_new, const int32_t* host_start,
+                             tq_stream stream);
+
+/* Workspace bytes for tq_decode_attention with sequences up to max_seq tokens. */
+size_t tq_decode_workspace_bytes(const tq_context* ctx, int32_t max_seq);
+
+/* Read path: o[b][h] = sum_j softmax_j(q^T k_hat_j / sqrt(d)) v_hat_j over the first
+ * host_seq_len[b] tokens of slab (b, h / G) ([HEADQ] "Espaço de Pontuação da Chave",
+ * "Geometria de Leitura de Valores"; [TQ-KV] "Marco Teórico", K-V asymmetry).
+ * q, out: device fp32 [B][H_q][d].  host_seq_len: host array of B entries in [0, capacity];
+ * a length of 0 gives an output of zeros.  ws: device workspace of at least
+ * tq_decode_workspace_bytes(ctx, max(host_seq_len)) bytes; its contents need no
+ * initialization and are owned by the call until it completes on stream. */
+tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, const float* q,
+                              const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
+                              tq_stream stream);
+
+/* HeadQ read path, unfused ([HEADQ] "Leitura do Cache"): corrected logits
+ * s_hat_j = q^T k_base_j / sqrt(d) + q^T U z_hat_j / sqrt(d) for every stored token, written to
+ * logits[b][h][j] (fp32, row stride logits_stride >= max(host_seq_len)); entries at j >=
+ * host_seq_len[b] are not written.  For a K side without HeadQ the scores of the K codec
+ * (with the QJL correction on a QJL side) are written. */
+tq_status tq_headq_correct(const tq_context* ctx, const void* dev_cache, const float* q,
+                           const int32_t* host_seq_len, float* logits, int32_t logits_stride,
+                           tq_stream stream);
+
+/* Reconstruct k_hat, v_hat (fp32 [t1 - t0][d], device) of tokens [t0, t1) of slab (b, kvh),
+ * including QJL and HeadQ terms.  For tests and debugging. */
+tq_status tq_dequantize(const tq_context* ctx, const void* dev_cache, int32_t b, int32_t kvh,
+                        int32_t t0, int32_t t1, float* k_out, float* v_out, tq_stream stream);
+
+/* Wait for stream, then read the device error word of a decode workspace: 0 = none. */
+tq_status tq_get_device_error(const void* ws, int32_t* code, tq_stream stream);
+
+const char* tq_status_string(tq_status status);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* tq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

@@ -1,0 +1,177 @@
+"""C-ABI checks that need no GPU: exported symbols, validation, host tables and layout vs the oracle.
+
+The host tables are built by the library's own C++ code (Lloyd-Max by a continued-fraction
+incomplete beta; SplitMix64 + Box-Muller) and compared with the oracle's independent float64
+construction; no kernel runs here.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import codebook, layout, tables
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+b = pytest.importorskip("turboquant_quantized_kv_tq_gb300.binding")
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _header_functions()
+    assert len(names) >= 15
+    declared = {n for n, _, _ in b.DECLARATIONS}
+    for n in names:
+        assert hasattr(b.lib, n), n
+        assert n in declared, n
+
+
+def _cfg(d=128, hq=4, hkv=2, batch=2, cap=128, scheme="tq", n=4, seed=7, headq=0):
+    c = b.tq_config()
+    c.head_dim, c.num_q_heads, c.num_kv_heads, c.batch, c.capacity = d, hq, hkv, batch, cap
+    c.qjl_m, c.headq_rank, c.headq_bits, c.seed = 0, headq, 4, seed
+    b.check(b.tq_config_from_scheme(b.SCHEMES[scheme], n, c))
+    return c
+
+
+def _ctx(c):
+    ctx = ctypes.c_void_p()
+    b.check(b.tq_context_create(c, ctx))
+    return ctx
+
+
+def test_config_from_scheme():
+    c = _cfg(scheme="kqv", n=4)
+    assert (c.k.bits, c.k.rotate, c.k.qjl, c.v.bits, c.v.rotate, c.v.qjl) == (4, 1, 0, 3, 1, 1)
+    c = _cfg(scheme="qkqv", n=3)
+    assert (c.k.bits, c.k.qjl, c.v.bits, c.v.qjl) == (2, 1, 2, 1)
+    c = _cfg(scheme="plain", n=2)
+    assert (c.k.rotate, c.v.rotate) == (0, 0)
+    assert b.tq_config_from_scheme(b.TQ_KQV, 1, c) == b.TQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 100, b.TQ_ERR_INVALID_ARG),
+    ("head_dim", 64, b.TQ_ERR_UNSUPPORTED),
+    ("num_q_heads", 6, b.TQ_ERR_UNSUPPORTED),   # G = 3
+    ("num_q_heads", 5, b.TQ_ERR_INVALID_ARG),   # not a multiple
+    ("capacity", 100, b.TQ_ERR_INVALID_ARG),
+    ("batch", 0, b.TQ_ERR_INVALID_ARG),
+    ("batch", 513, b.TQ_ERR_INVALID_ARG),
+])
+def test_context_validation(field, value, status):
+    c = _cfg()
+    setattr(c, field, value)
+    ctx = ctypes.c_void_p()
+    assert b.tq_context_create(c, ctx) == status
+    assert not ctx.value
+    assert b.tq_last_error()
+
+
+def test_calls_before_upload_are_refused():
+    ctx = _ctx(_cfg())
+    seq = b.int_array([4, 4])
+    assert b.tq_decode_attention(ctx, None, None, seq, None, None, 0, None) == b.TQ_ERR_STATE
+    b.tq_context_destroy(ctx)
+
+
+def _blob(ctx):
+    n = b.tq_tables_bytes(ctx)
+    buf = np.zeros(n, dtype=np.uint8)
+    b.check(b.tq_tables_host(ctx, buf.ctypes.data, n))
+    return buf
+
+
+def _offsets(d, m, kq, vq, hkv, rank):
+    # mirror of the blob layout stated in tq.h (each array on a 256-byte boundary)
+    off, out = 0, {}
+    def take(name, nbytes):
+        nonlocal off
+        off = (off + 255) // 256 * 256
+        out[name] = off
+        off += nbytes
+    for nm in ("k_c", "k_t", "v_c", "v_t"):
+        take(nm, 64)
+    take("k_sign", 4 * d)
+    take("v_sign", 4 * d)
+    if kq:
+        take("S_K", 4 * m * d); take("S_K_T", 4 * m * d)
+    if vq:
+        take("S_V", 4 * m * d); take("S_V_T", 4 * m * d)
+    if rank:
+        take("U", 4 * hkv * d * rank)
+    return out
+
+
+@pytest.mark.parametrize("d", [128, 1024])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_host_codebook_matches_oracle(d, bits):
+    c = _cfg(d=d, scheme="tq", n=bits)
+    ctx = _ctx(c)
+    blob = _blob(ctx)
+    off = _offsets(d, d, 0, 0, 2, 0)
+    L = 1 << bits
+    cpp_c = blob[off["k_c"]:off["k_c"] + 64].view(np.float32)[:L]
+    cpp_t = blob[off["k_t"]:off["k_t"] + 64].view(np.float32)[:L - 1]
+    c64, t64 = codebook.lloyd_max(d, bits)
+    assert np.max(np.abs(cpp_c.astype(np.float64) - c64)) <= 0.5 * np.spacing(np.abs(c64).astype(np.float32)).max()
+    assert np.array_equal(cpp_c, c64.astype(np.float32))
+    assert np.array_equal(cpp_t, t64.astype(np.float32))
+    assert np.all(blob[off["k_t"]:off["k_t"] + 64].view(np.float32)[L - 1:] > 1e38)
+    b.tq_context_destroy(ctx)
+
+
+@pytest.mark.parametrize("seed", [0, 3, 12345])
+def test_host_rotation_and_sketch_bit_exact(seed):
+    d = 128
+    c = _cfg(d=d, scheme="qkqv", n=4, seed=seed)
+    ctx = _ctx(c)
+    blob = _blob(ctx)
+    off = _offsets(d, d, 1, 1, 2, 0)
+    f = lambda name, n: blob[off[name]:off[name] + 4 * n].view(np.float32)
+    assert np.array_equal(f("k_sign", d), tables.rotation_signs(seed, tables.STREAM_D_K, d).astype(np.float32))
+    assert np.array_equal(f("v_sign", d), tables.rotation_signs(seed, tables.STREAM_D_V, d).astype(np.float32))
+    SK = tables.sketch_matrix(seed, tables.STREAM_S_K, d, d)
+    SV = tables.sketch_matrix(seed, tables.STREAM_S_V, d, d)
+    assert np.array_equal(f("S_K", d * d).reshape(d, d), SK)
+    assert np.array_equal(f("S_K_T", d * d).reshape(d, d), SK.T)
+    assert np.array_equal(f("S_V", d * d).reshape(d, d), SV)
+    assert np.array_equal(f("S_V_T", d * d).reshape(d, d), SV.T)
+    assert b.tq_tables_bytes(ctx) >= off["S_V_T"] + 4 * d * d
+    b.tq_context_destroy(ctx)
+
+
+def test_plain_has_unit_signs():
+    c = _cfg(scheme="plain", n=3)
+    ctx = _ctx(c)
+    blob = _blob(ctx)
+    off = _offsets(128, 128, 0, 0, 2, 0)
+    assert np.all(blob[off["k_sign"]:off["k_sign"] + 512].view(np.float32) == 1.0)
+    b.tq_context_destroy(ctx)
+
+
+@pytest.mark.parametrize("scheme,n,headq", [("tq", 4, 0), ("kqv", 3, 0), ("qkqv", 2, 0), ("tq", 2, 16), ("plain", 1, 0)])
+def test_layout_matches_oracle(scheme, n, headq):
+    c = _cfg(d=128, hq=8, hkv=2, batch=3, cap=192, scheme=scheme, n=n, headq=headq)
+    ctx = _ctx(c)
+    lay = b.tq_cache_layout()
+    b.check(b.tq_get_cache_layout(ctx, lay))
+    assert lay.layout_version == 1
+    shape = layout.CacheShape(3, 2, 192, 128, c.k.bits, bool(c.k.qjl), c.v.bits, bool(c.v.qjl), 128, headq, 4)
+    regs, total = layout.regions(shape)
+    assert lay.total_bytes == total
+    for name in b.REGION_NAMES:
+        r = getattr(lay, name)
+        if name in regs:
+            assert (r.offset, r.record_bytes) == regs[name], name
+        else:
+            assert r.record_bytes == 0, name
+    b.tq_context_destroy(ctx)

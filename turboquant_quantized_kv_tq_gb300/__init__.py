@@ -1,0 +1,138 @@
+"""Rotated-codebook quantized KV cache and fused decode attention for GB300 (sm_103a).
+
+The C library (``include/tq.h``, built in-tree as ``_lib/libtq.so``) holds the codec tables,
+the cache layout and the CUDA kernels.  ``binding`` exposes its entry points by name;
+``QuantizedKVCache`` owns the device buffers (through torch) for one configuration and marshals
+tensors to those entry points.  There is no CPU fallback: without the built library the import
+fails.
+"""
+
+import numpy as np
+
+from . import binding as _b
+from .binding import TQError, check  # noqa: F401
+
+__all__ = ["QuantizedKVCache", "TQError", "binding"]
+
+_DTYPES = None
+
+
+def _dtype_code(t):
+    global _DTYPES
+    import torch
+    if _DTYPES is None:
+        _DTYPES = {torch.float32: _b.TQ_F32, torch.bfloat16: _b.TQ_BF16, torch.float16: _b.TQ_F16}
+    return _DTYPES[t.dtype]
+
+
+def _stream_handle(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class QuantizedKVCache:
+    """One packed KV cache of shape [batch][num_kv_heads][capacity] tokens on a CUDA device.
+
+    ``scheme``/``n`` pick the codecs as ``tq_config_from_scheme`` does; ``k_codec``/``v_codec``
+    (tuples bits, rotate, qjl) override them.  ``headq_rank`` = 16 turns the HeadQ side code on.
+    """
+
+    def __init__(self, head_dim, num_q_heads, num_kv_heads, batch, capacity, scheme="tq", n=4,
+                 seed=0, k_codec=None, v_codec=None, headq_rank=0, headq_bits=4, device="cuda"):
+        import torch
+        cfg = _b.tq_config()
+        cfg.head_dim, cfg.num_q_heads, cfg.num_kv_heads = head_dim, num_q_heads, num_kv_heads
+        cfg.batch, cfg.capacity = batch, capacity
+        cfg.qjl_m, cfg.headq_rank, cfg.headq_bits, cfg.seed = 0, headq_rank, headq_bits, seed
+        if scheme is not None:
+            check(_b.tq_config_from_scheme(_b.SCHEMES[scheme.lower()], n, cfg))
+        if k_codec is not None:
+            cfg.k = _b.tq_codec(*k_codec)
+        if v_codec is not None:
+            cfg.v = _b.tq_codec(*v_codec)
+        self.cfg = cfg
+        ctx = _b.c_void_p()
+        check(_b.tq_context_create(cfg, ctx))
+        self._ctx = ctx
+        self.device = torch.device(device)
+        self.head_dim, self.num_q_heads, self.num_kv_heads = head_dim, num_q_heads, num_kv_heads
+        self.batch, self.capacity = batch, capacity
+        self.tables = torch.empty(int(_b.tq_tables_bytes(ctx)), dtype=torch.uint8, device=self.device)
+        check(_b.tq_tables_upload(ctx, self.tables.data_ptr(), _stream_handle()))
+        lay = _b.tq_cache_layout()
+        check(_b.tq_get_cache_layout(ctx, lay))
+        self.layout = lay
+        self.regions = {n: (getattr(lay, n).offset, getattr(lay, n).record_bytes) for n in _b.REGION_NAMES}
+        self.cache = torch.zeros(int(lay.total_bytes), dtype=torch.uint8, device=self.device)
+        self._ws = None
+
+    def __del__(self):
+        ctx = getattr(self, "_ctx", None)
+        if ctx is not None and ctx.value:
+            _b.tq_context_destroy(ctx)
+            self._ctx = None
+
+    # ---- host tables (no GPU work)
+    def host_tables(self):
+        n = int(_b.tq_tables_bytes(self._ctx))
+        buf = np.zeros(n, dtype=np.uint8)
+        check(_b.tq_tables_host(self._ctx, buf.ctypes.data, n))
+        return buf
+
+    # ---- device calls
+    def set_headq_basis(self, U, stream=None):
+        """U: float32 CUDA tensor [num_kv_heads][head_dim][rank]."""
+        U = U.contiguous()
+        check(_b.tq_headq_set_basis(self._ctx, U.data_ptr(), _stream_handle(stream)))
+        self._U = U  # keep alive until the kernel has run
+
+    def append(self, k, v, start, stream=None):
+        """k, v: CUDA tensors [batch][num_kv_heads][n_new][head_dim] (fp32/bf16/fp16)."""
+        k, v = k.contiguous(), v.contiguous()
+        if k.shape != v.shape or k.dtype != v.dtype:
+            raise ValueError("k and v must have the same shape and dtype")
+        check(_b.tq_quantize_append(self._ctx, self.cache.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                    _dtype_code(k), int(k.shape[2]), _b.int_array(start),
+                                    _stream_handle(stream)))
+
+    def workspace(self, max_seq):
+        import torch
+        need = int(_b.tq_decode_workspace_bytes(self._ctx, int(max_seq)))
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def decode(self, q, seq_len, out=None, stream=None):
+        """q: float32 CUDA tensor [batch][num_q_heads][head_dim] -> attention output (same shape)."""
+        import torch
+        q = q.contiguous()
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(max(int(x) for x in seq_len))
+        check(_b.tq_decode_attention(self._ctx, self.cache.data_ptr(), q.data_ptr(), _b.int_array(seq_len),
+                                     out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream)))
+        return out
+
+    def logits(self, q, seq_len, stride=None, stream=None):
+        """Corrected scores [batch][num_q_heads][stride] (entries past seq_len[b] are untouched: 0)."""
+        import torch
+        q = q.contiguous()
+        stride = stride or max(1, max(int(x) for x in seq_len))
+        out = torch.zeros(q.shape[0], q.shape[1], stride, dtype=torch.float32, device=self.device)
+        check(_b.tq_headq_correct(self._ctx, self.cache.data_ptr(), q.data_ptr(), _b.int_array(seq_len),
+                                  out.data_ptr(), stride, _stream_handle(stream)))
+        return out
+
+    def dequantize(self, b, kvh, t0, t1, stream=None):
+        import torch
+        k = torch.empty(t1 - t0, self.head_dim, dtype=torch.float32, device=self.device)
+        v = torch.empty_like(k)
+        check(_b.tq_dequantize(self._ctx, self.cache.data_ptr(), b, kvh, t0, t1, k.data_ptr(), v.data_ptr(),
+                               _stream_handle(stream)))
+        return k, v
+
+    def device_error(self, stream=None):
+        code = _b.c_int32(0)
+        st = _b.tq_get_device_error(self.workspace(0).data_ptr(), code, _stream_handle(stream))
+        return st, code.value

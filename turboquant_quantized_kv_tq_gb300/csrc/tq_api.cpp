@@ -1,0 +1,282 @@
+// C ABI entry points: validation, context and table management, layout, dispatch.
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "tq_internal.h"
+
+namespace tqi {
+namespace {
+thread_local std::string g_last_error;
+}
+void set_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace tqi
+
+using namespace tqi;
+
+namespace {
+
+tq_status fail(tq_status s, const std::string& msg) {
+  set_error(msg);
+  return s;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+tq_status validate_codec(const tq_codec& c, const char* side) {
+  if (c.bits < 1 || c.bits > 4) return fail(TQ_ERR_INVALID_ARG, std::string(side) + ": bits must be 1..4");
+  if ((c.rotate != 0 && c.rotate != 1) || (c.qjl != 0 && c.qjl != 1))
+    return fail(TQ_ERR_INVALID_ARG, std::string(side) + ": rotate and qjl must be 0 or 1");
+  return TQ_OK;
+}
+
+tq_status validate_config(const tq_config& c) {
+  if (!pow2(c.head_dim) || c.head_dim < 8 || c.head_dim > 1024)
+    return fail(TQ_ERR_INVALID_ARG, "head_dim must be a power of two in [8, 1024]");
+  if (c.head_dim != 128 && c.head_dim != 256 && c.head_dim != 512 && c.head_dim != 1024)
+    return fail(TQ_ERR_UNSUPPORTED, "head_dim: the GPU path is built for 128, 256, 512, 1024");
+  if (c.num_kv_heads <= 0 || c.num_q_heads <= 0 || c.num_q_heads % c.num_kv_heads)
+    return fail(TQ_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  const int G = c.num_q_heads / c.num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(TQ_ERR_UNSUPPORTED, "G = num_q_heads / num_kv_heads must be 1, 2, 4 or 8");
+  if (c.batch <= 0 || c.batch > TQ_MAX_BATCH) return fail(TQ_ERR_INVALID_ARG, "batch must be in [1, TQ_MAX_BATCH]");
+  if (c.capacity <= 0 || c.capacity % 64) return fail(TQ_ERR_INVALID_ARG, "capacity must be a positive multiple of 64");
+  if ((uint64_t)c.batch * c.num_kv_heads * c.capacity > (1ull << 40))
+    return fail(TQ_ERR_INVALID_ARG, "cache too large");
+  tq_status s = validate_codec(c.k, "k");
+  if (s != TQ_OK) return s;
+  s = validate_codec(c.v, "v");
+  if (s != TQ_OK) return s;
+  if (c.qjl_m != 0 && c.qjl_m != c.head_dim) return fail(TQ_ERR_UNSUPPORTED, "qjl_m must be 0 or head_dim");
+  if (c.headq_rank < 0) return fail(TQ_ERR_INVALID_ARG, "headq_rank must be >= 0");
+  if (c.headq_rank) {
+    if (c.headq_rank != 16 || c.headq_bits != 4)
+      return fail(TQ_ERR_UNSUPPORTED, "HeadQ is built for rank 16 with 4-bit side codes");
+    if (c.k.qjl) return fail(TQ_ERR_UNSUPPORTED, "HeadQ with a QJL key side is not built");
+  }
+  if (c.head_dim > 128 && (c.k.qjl || c.headq_rank))
+    return fail(TQ_ERR_UNSUPPORTED, "key-side QJL and HeadQ are built for head_dim 128");
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tq_status_string(tq_status s) {
+  switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_INVALID_ARG: return "invalid argument";
+    case TQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TQ_ERR_CAPACITY: return "cache capacity exceeded";
+    case TQ_ERR_WORKSPACE: return "workspace too small";
+    case TQ_ERR_CUDA: return "CUDA error";
+    case TQ_ERR_DEVICE: return "device-side error";
+    case TQ_ERR_STATE: return "context not ready";
+  }
+  return "unknown status";
+}
+
+const char* tq_last_error(void) { return g_last_error.c_str(); }
+
+tq_status tq_config_from_scheme(tq_scheme scheme, int32_t n, tq_config* c) {
+  if (!c) return fail(TQ_ERR_INVALID_ARG, "null config");
+  if (n < 1 || n > 4) return fail(TQ_ERR_INVALID_ARG, "n must be 1..4");
+  switch (scheme) {
+    case TQ_PLAIN_KV: c->k = {n, 0, 0}; c->v = {n, 0, 0}; break;
+    case TQ_TQ_KV: c->k = {n, 1, 0}; c->v = {n, 1, 0}; break;
+    case TQ_KQV:
+      if (n < 2) return fail(TQ_ERR_INVALID_ARG, "KQV needs n >= 2");
+      c->k = {n, 1, 0}; c->v = {n - 1, 1, 1}; break;
+    case TQ_QKQV:
+      if (n < 2) return fail(TQ_ERR_INVALID_ARG, "QKQV needs n >= 2");
+      c->k = {n - 1, 1, 1}; c->v = {n - 1, 1, 1}; break;
+    default: return fail(TQ_ERR_INVALID_ARG, "unknown scheme");
+  }
+  return TQ_OK;
+}
+
+tq_status tq_context_create(const tq_config* cfg, tq_context** out) {
+  if (!cfg || !out) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  tq_status s = validate_config(*cfg);
+  if (s != TQ_OK) return s;
+  tq_context* ctx = new (std::nothrow) tq_context();
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "out of host memory");
+  ctx->cfg = *cfg;
+  const int d = cfg->head_dim;
+  ctx->m = cfg->qjl_m ? cfg->qjl_m : d;
+  ctx->tab = make_table_offsets(*cfg, ctx->m);
+  ctx->layout = make_layout(*cfg, ctx->m);
+  ctx->host_tables.assign(ctx->tab.total, 0);
+  unsigned char* base = ctx->host_tables.data();
+  double c[kMaxLevels], t[kMaxLevels];
+  auto put_codebook = [&](int bits, size_t off_c, size_t off_t) {
+    lloyd_max_beta(d, bits, c, t);
+    float* fc = (float*)(base + off_c);
+    float* ft = (float*)(base + off_t);
+    const int L = 1 << bits;
+    for (int i = 0; i < kMaxLevels; ++i) fc[i] = i < L ? (float)c[i] : 0.0f;
+    for (int i = 0; i < kMaxLevels; ++i) ft[i] = i < L - 1 ? (float)t[i] : 3.0e38f;
+  };
+  put_codebook(cfg->k.bits, ctx->tab.k_centroids, ctx->tab.k_thresholds);
+  put_codebook(cfg->v.bits, ctx->tab.v_centroids, ctx->tab.v_thresholds);
+  float* ks = (float*)(base + ctx->tab.k_signs);
+  float* vs = (float*)(base + ctx->tab.v_signs);
+  if (cfg->k.rotate) rotation_signs(cfg->seed, 1, d, ks); else for (int i = 0; i < d; ++i) ks[i] = 1.0f;
+  if (cfg->v.rotate) rotation_signs(cfg->seed, 2, d, vs); else for (int i = 0; i < d; ++i) vs[i] = 1.0f;
+  auto put_sketch = [&](uint64_t stream, size_t off, size_t off_t) {
+    float* S = (float*)(base + off);
+    float* St = (float*)(base + off_t);
+    sketch_matrix(cfg->seed, stream, ctx->m, d, S);
+    for (int i = 0; i < ctx->m; ++i)
+      for (int j = 0; j < d; ++j) St[(size_t)j * ctx->m + i] = S[(size_t)i * d + j];
+  };
+  if (cfg->k.qjl) put_sketch(3, ctx->tab.s_k, ctx->tab.s_k_t);
+  if (cfg->v.qjl) put_sketch(4, ctx->tab.s_v, ctx->tab.s_v_t);
+  *out = ctx;
+  return TQ_OK;
+}
+
+void tq_context_destroy(tq_context* ctx) { delete ctx; }
+
+size_t tq_tables_bytes(const tq_context* ctx) { return ctx ? ctx->tab.total : 0; }
+
+tq_status tq_tables_host(const tq_context* ctx, void* dst, size_t bytes) {
+  if (!ctx || !dst) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (bytes < ctx->tab.total) return fail(TQ_ERR_INVALID_ARG, "destination smaller than tq_tables_bytes");
+  std::memcpy(dst, ctx->host_tables.data(), ctx->tab.total);
+  return TQ_OK;
+}
+
+tq_status tq_tables_upload(tq_context* ctx, void* dev_tables, tq_stream stream) {
+  if (!ctx || !dev_tables) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (!aligned(dev_tables, 256)) return fail(TQ_ERR_INVALID_ARG, "dev_tables must be 256-byte aligned");
+  cudaError_t e = cudaMemcpyAsync(dev_tables, ctx->host_tables.data(), ctx->tab.total,
+                                  cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(TQ_ERR_CUDA, std::string("table upload: ") + cudaGetErrorString(e));
+  ctx->dev_tables = dev_tables;
+  ctx->basis_set = false;
+  return TQ_OK;
+}
+
+tq_status tq_headq_set_basis(tq_context* ctx, const float* dev_U, tq_stream stream) {
+  if (!ctx || !dev_U) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (!ctx->cfg.headq_rank) return fail(TQ_ERR_STATE, "HeadQ is off in this context");
+  if (!ctx->dev_tables) return fail(TQ_ERR_STATE, "tables not uploaded");
+  if (!aligned(dev_U, 16)) return fail(TQ_ERR_INVALID_ARG, "dev_U must be 16-byte aligned");
+  tq_status s = launch_rotate_basis(ctx, dev_U, stream);
+  if (s == TQ_OK) ctx->basis_set = true;
+  return s;
+}
+
+tq_status tq_get_cache_layout(const tq_context* ctx, tq_cache_layout* out) {
+  if (!ctx || !out) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  std::memset(out, 0, sizeof(*out));
+  out->layout_version = TQ_LAYOUT_VERSION;
+  out->total_bytes = ctx->layout.total;
+  tq_region* r[R_COUNT] = {&out->k_codes, &out->k_norm, &out->k_signs, &out->k_rho, &out->k_side,
+                           &out->k_side_scale, &out->v_codes, &out->v_norm, &out->v_signs, &out->v_rho};
+  for (int i = 0; i < R_COUNT; ++i) {
+    r[i]->offset = ctx->layout.off[i];
+    r[i]->record_bytes = ctx->layout.rec[i];
+  }
+  return TQ_OK;
+}
+
+static tq_status ready(const tq_context* ctx) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
+  if (!ctx->dev_tables) return fail(TQ_ERR_STATE, "tables not uploaded");
+  if (ctx->cfg.headq_rank && !ctx->basis_set) return fail(TQ_ERR_STATE, "HeadQ basis not set");
+  return TQ_OK;
+}
+
+tq_status tq_quantize_append(const tq_context* ctx, void* dev_cache, const void* k, const void* v,
+                             tq_dtype dtype, int32_t n_new, const int32_t* host_start,
+                             tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (n_new < 0) return fail(TQ_ERR_INVALID_ARG, "n_new must be >= 0");
+  if (n_new == 0) return TQ_OK;
+  if (!dev_cache || !k || !v || !host_start) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad dtype");
+  if (!aligned(dev_cache, 256)) return fail(TQ_ERR_INVALID_ARG, "cache must be 256-byte aligned");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(TQ_ERR_INVALID_ARG, "k, v must be 16-byte aligned");
+  for (int b = 0; b < ctx->cfg.batch; ++b) {
+    if (host_start[b] < 0) return fail(TQ_ERR_INVALID_ARG, "start must be >= 0");
+    if ((int64_t)host_start[b] + n_new > ctx->cfg.capacity) return fail(TQ_ERR_CAPACITY, "start + n_new > capacity");
+  }
+  return launch_append(ctx, dev_cache, k, v, dtype, n_new, host_start, stream);
+}
+
+size_t tq_decode_workspace_bytes(const tq_context* ctx, int32_t max_seq) {
+  if (!ctx || max_seq < 0) return 0;
+  return decode_workspace_bytes(ctx, max_seq);
+}
+
+static tq_status check_lengths(const tq_context* ctx, const int32_t* seq_len, int* max_seq) {
+  *max_seq = 0;
+  for (int b = 0; b < ctx->cfg.batch; ++b) {
+    if (seq_len[b] < 0) return fail(TQ_ERR_INVALID_ARG, "seq_len must be >= 0");
+    if (seq_len[b] > ctx->cfg.capacity) return fail(TQ_ERR_CAPACITY, "seq_len > capacity");
+    if (seq_len[b] > *max_seq) *max_seq = seq_len[b];
+  }
+  return TQ_OK;
+}
+
+tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, const float* q,
+                              const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
+                              tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (!dev_cache || !q || !host_seq_len || !out || !ws) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (!aligned(dev_cache, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 256))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer (cache/ws 256 B, q/out 16 B)");
+  int max_seq;
+  s = check_lengths(ctx, host_seq_len, &max_seq);
+  if (s != TQ_OK) return s;
+  if (ws_bytes < decode_workspace_bytes(ctx, max_seq)) return fail(TQ_ERR_WORKSPACE, "workspace too small");
+  return launch_decode(ctx, dev_cache, q, host_seq_len, out, ws, ws_bytes, stream);
+}
+
+tq_status tq_headq_correct(const tq_context* ctx, const void* dev_cache, const float* q,
+                           const int32_t* host_seq_len, float* logits, int32_t logits_stride,
+                           tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (!dev_cache || !q || !host_seq_len || !logits) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (!aligned(dev_cache, 256) || !aligned(q, 16) || !aligned(logits, 4))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer");
+  int max_seq;
+  s = check_lengths(ctx, host_seq_len, &max_seq);
+  if (s != TQ_OK) return s;
+  if (logits_stride < max_seq) return fail(TQ_ERR_INVALID_ARG, "logits_stride < max(seq_len)");
+  return launch_logits(ctx, dev_cache, q, host_seq_len, logits, logits_stride, stream);
+}
+
+tq_status tq_dequantize(const tq_context* ctx, const void* dev_cache, int32_t b, int32_t kvh,
+                        int32_t t0, int32_t t1, float* k_out, float* v_out, tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (!dev_cache || !k_out || !v_out) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (b < 0 || b >= ctx->cfg.batch || kvh < 0 || kvh >= ctx->cfg.num_kv_heads)
+    return fail(TQ_ERR_INVALID_ARG, "slab index out of range");
+  if (t0 < 0 || t1 < t0 || t1 > ctx->cfg.capacity) return fail(TQ_ERR_INVALID_ARG, "token range out of range");
+  if (t1 == t0) return TQ_OK;
+  if (!aligned(dev_cache, 256) || !aligned(k_out, 16) || !aligned(v_out, 16))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer");
+  return launch_dequantize(ctx, dev_cache, b, kvh, t0, t1, k_out, v_out, stream);
+}
+
+tq_status tq_get_device_error(const void* ws, int32_t* code, tq_stream stream) {
+  if (!ws || !code) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  return read_device_error(ws, code, stream);
+}
+
+}  // extern "C"

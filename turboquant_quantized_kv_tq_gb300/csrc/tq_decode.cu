@@ -1,0 +1,259 @@
+// Read path launchers: query preparation, fused split-K decode, corrected logits.
+#include <string>
+
+#include "tq_decode_kernel.cuh"
+
+namespace tqd {
+namespace {
+
+// Blocks the decode grid aims for: the kernel holds more than 128 registers per thread, so one
+// 256-thread block fits per SM; two blocks per SM of a 152-SM GB300 keep the last wave short.
+constexpr int kTargetBlocks = 2 * 152;
+constexpr int kMinTokensPerBlock = 256;
+constexpr int kLogitsTokensPerBlock = 2048;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct WsLayout {
+  size_t err, tickets, q_rot, q_sk, q_u, part, total;
+  int splits, chunk, ps;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+WsLayout ws_layout(const tq_context* ctx, int max_seq) {
+  WsLayout w;
+  const int B = ctx->cfg.batch, Hkv = ctx->cfg.num_kv_heads, Hq = ctx->cfg.num_q_heads;
+  const int D = ctx->cfg.head_dim;
+  const int pairs = B * Hkv;
+  int splits = (kTargetBlocks + pairs - 1) / pairs;
+  const int by_len = (max_seq + kMinTokensPerBlock - 1) / kMinTokensPerBlock;
+  if (splits > by_len) splits = by_len;
+  if (splits < 1) splits = 1;
+  int chunk = (max_seq + splits - 1) / splits;
+  chunk = (chunk + kTile - 1) / kTile * kTile;
+  w.splits = splits;
+  w.chunk = chunk;
+  w.ps = 4 + D + (ctx->cfg.v.qjl ? ctx->m : 0);
+  size_t off = 0;
+  w.err = off; off = align256(off + 64 * sizeof(int));
+  w.tickets = off; off = align256(off + (size_t)pairs * sizeof(int));
+  w.q_rot = off; off = align256(off + (size_t)B * Hq * D * 2);
+  w.q_sk = off; off = align256(off + (ctx->cfg.k.qjl ? (size_t)B * Hq * ctx->m * 2 : 0));
+  w.q_u = off; off = align256(off + (ctx->cfg.headq_rank ? (size_t)B * Hq * 16 * 2 : 0));
+  w.part = off; off = align256(off + (size_t)pairs * splits * kHeadsPad * w.ps * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+struct PrepParams {
+  Tables tab;
+  const float* q;
+  uint32_t* q_rot;
+  uint32_t* q_sk;
+  uint32_t* q_u;
+  int* tickets;
+  int* err;
+  int n_tickets, n_heads, Hq, G, k_rotate, kq, kh;
+};
+
+// Per query head (one warp): q_rot = R_K q; S_K q_rot for a QJL key side; U_rot^T q_rot = U^T q
+// for HeadQ; stored as fp16 pairs.  Block 0 also clears the split tickets and the error word.
+__global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
+  constexpr int D = kDecD;
+  const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < p.n_tickets; i += blockDim.x) p.tickets[i] = 0;
+    if (threadIdx.x == 0) p.err[0] = 0;
+  }
+  const int head = blockIdx.x * 8 + (threadIdx.x >> 5);  // flat [B][Hq] index
+  if (head >= p.n_heads) return;
+  const float4 q4 = *reinterpret_cast<const float4*>(p.q + (long long)head * D + 4 * lane);
+  float x[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] *= __ldg(p.tab.k_sign + 4 * lane + i);
+  if (p.k_rotate) {
+    wht_warp<4>(x);
+    const float rs = 1.f / sqrtf((float)D);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] *= rs;
+  }
+  *reinterpret_cast<uint2*>(p.q_rot + (long long)head * (D / 2) + 2 * lane) =
+      make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
+  if (p.kq) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int jl = 0; jl < 32; ++jl) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float xj = __shfl_sync(kFull, x[e], jl);
+        const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.S_K_T + (4 * jl + e) * D + 4 * lane));
+        a[0] = fmaf(s4.x, xj, a[0]); a[1] = fmaf(s4.y, xj, a[1]);
+        a[2] = fmaf(s4.z, xj, a[2]); a[3] = fmaf(s4.w, xj, a[3]);
+      }
+    }
+    *reinterpret_cast<uint2*>(p.q_sk + (long long)head * (D / 2) + 2 * lane) =
+        make_uint2(pack_half2(a[0], a[1]), pack_half2(a[2], a[3]));
+  }
+  if (p.kh) {
+    const int kvh = (head % p.Hq) / p.G;
+    const float* Ur = p.tab.U_rot + (long long)kvh * D * 16;
+    float z[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) z[k] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+#pragma unroll
+      for (int k = 0; k < 16; k += 4) {
+        const float4 u4 = __ldg(reinterpret_cast<const float4*>(Ur + (4 * lane + e) * 16 + k));
+        z[k] = fmaf(u4.x, x[e], z[k]); z[k + 1] = fmaf(u4.y, x[e], z[k + 1]);
+        z[k + 2] = fmaf(u4.z, x[e], z[k + 2]); z[k + 3] = fmaf(u4.w, x[e], z[k + 3]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) z[k] = warp_sum(z[k]);
+    if (lane == 0) {
+      uint32_t* dst = p.q_u + (long long)head * 8;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dst[k] = pack_half2(z[2 * k], z[2 * k + 1]);
+    }
+  }
+}
+
+tq_status cuda_fail(const char* what, cudaError_t e) {
+  tqi::set_error(std::string(what) + ": " + cudaGetErrorString(e));
+  return TQ_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tqd
+
+namespace tqi {
+
+size_t decode_workspace_bytes(const tq_context* ctx, int max_seq) {
+  return tqd::ws_layout(ctx, max_seq).total;
+}
+
+tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
+                        const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
+                        Stream stream) {
+  using namespace tqd;
+  (void)ws_bytes;
+  if (ctx->cfg.head_dim != kDecD) {
+    set_error("decode attention is built for head_dim 128");
+    return TQ_ERR_UNSUPPORTED;
+  }
+  int max_seq = 0;
+  for (int b = 0; b < ctx->cfg.batch; ++b) max_seq = seq_len[b] > max_seq ? seq_len[b] : max_seq;
+  const WsLayout w = ws_layout(ctx, max_seq);
+  unsigned char* base = (unsigned char*)ws;
+  const cudaStream_t s = (cudaStream_t)stream;
+  const Tables tab = make_tables(ctx);
+  const int B = ctx->cfg.batch, Hkv = ctx->cfg.num_kv_heads, Hq = ctx->cfg.num_q_heads;
+
+  PrepParams pp;
+  pp.tab = tab;
+  pp.q = q;
+  pp.q_rot = (uint32_t*)(base + w.q_rot);
+  pp.q_sk = (uint32_t*)(base + w.q_sk);
+  pp.q_u = (uint32_t*)(base + w.q_u);
+  pp.tickets = (int*)(base + w.tickets);
+  pp.err = (int*)(base + w.err);
+  pp.n_tickets = B * Hkv;
+  pp.n_heads = B * Hq;
+  pp.Hq = Hq;
+  pp.G = Hq / Hkv;
+  pp.k_rotate = ctx->cfg.k.rotate;
+  pp.kq = ctx->cfg.k.qjl;
+  pp.kh = ctx->cfg.headq_rank ? 1 : 0;
+  prep_kernel<<<(B * Hq + 7) / 8, 256, 0, s>>>(pp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail("decode prep", e);
+
+  DecodeParams p;
+  p.tab = tab;
+  p.cache = make_cache(ctx, cache);
+  p.q_rot = pp.q_rot;
+  p.q_sk = pp.q_sk;
+  p.q_u = pp.q_u;
+  p.part = (float*)(base + w.part);
+  p.tickets = pp.tickets;
+  p.out = out;
+  p.B = B;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.splits = w.splits;
+  p.chunk = w.chunk;
+  p.v_rotate = ctx->cfg.v.rotate;
+  p.score_scale = kLog2e / sqrtf((float)kDecD);
+  p.qjl_scale = (float)(1.2533141373155003 / ctx->m);
+  for (int b = 0; b < TQ_MAX_BATCH; ++b) p.seq_len[b] = b < B ? seq_len[b] : 0;
+  const dim3 grid(w.splits, Hkv, B);
+  const int kb = ctx->cfg.k.bits, kq = ctx->cfg.k.qjl, kh = ctx->cfg.headq_rank ? 1 : 0;
+  const int vb = ctx->cfg.v.bits, vq = ctx->cfg.v.qjl;
+  bool built = false;
+  e = cudaSuccess;
+  switch (kb) {
+    case 1: built = dispatch_decode_k1(kq, kh, vb, vq, p, grid, s, &e); break;
+    case 2: built = dispatch_decode_k2(kq, kh, vb, vq, p, grid, s, &e); break;
+    case 3: built = dispatch_decode_k3(kq, kh, vb, vq, p, grid, s, &e); break;
+    case 4: built = dispatch_decode_k4(kq, kh, vb, vq, p, grid, s, &e); break;
+  }
+  if (!built) {
+    set_error("decode attention is not built for this combination of key and value codecs");
+    return TQ_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail("decode", e);
+  return TQ_OK;
+}
+
+tq_status launch_logits(const tq_context* ctx, const void* cache, const float* q,
+                        const int32_t* seq_len, float* logits, int stride, Stream stream) {
+  using namespace tqd;
+  if (ctx->cfg.head_dim != kDecD) {
+    set_error("corrected logits are built for head_dim 128");
+    return TQ_ERR_UNSUPPORTED;
+  }
+  const int B = ctx->cfg.batch, Hkv = ctx->cfg.num_kv_heads, Hq = ctx->cfg.num_q_heads;
+  int max_seq = 0;
+  for (int b = 0; b < B; ++b) max_seq = seq_len[b] > max_seq ? seq_len[b] : max_seq;
+  if (max_seq == 0) return TQ_OK;
+  LogitsParams p;
+  p.tab = make_tables(ctx);
+  p.cache = make_cache(ctx, cache);
+  p.q = q;
+  p.logits = logits;
+  p.B = B;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.stride = stride;
+  p.tokens_per_block = kLogitsTokensPerBlock;
+  p.k_rotate = ctx->cfg.k.rotate;
+  p.qjl_scale = (float)(1.2533141373155003 / ctx->m);
+  p.inv_sqrt_d = 1.f / sqrtf((float)kDecD);
+  for (int b = 0; b < TQ_MAX_BATCH; ++b) p.seq_len[b] = b < B ? seq_len[b] : 0;
+  const dim3 grid((max_seq + kLogitsTokensPerBlock - 1) / kLogitsTokensPerBlock, Hkv, B);
+  const int kq = ctx->cfg.k.qjl, kh = ctx->cfg.headq_rank ? 1 : 0;
+  cudaError_t e = cudaSuccess;
+  bool built = false;
+  switch (ctx->cfg.k.bits) {
+    case 1: built = dispatch_logits_k1(kq, kh, p, grid, (cudaStream_t)stream, &e); break;
+    case 2: built = dispatch_logits_k2(kq, kh, p, grid, (cudaStream_t)stream, &e); break;
+    case 3: built = dispatch_logits_k3(kq, kh, p, grid, (cudaStream_t)stream, &e); break;
+    case 4: built = dispatch_logits_k4(kq, kh, p, grid, (cudaStream_t)stream, &e); break;
+  }
+  if (!built) {
+    set_error("corrected logits are not built for this key codec");
+    return TQ_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail("logits", e);
+  return TQ_OK;
+}
+
+tq_status read_device_error(const void* ws, int32_t* code, Stream stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return tqd::cuda_fail("stream synchronize", e);
+  e = cudaMemcpy(code, ws, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return tqd::cuda_fail("read error word", e);
+  return *code ? TQ_ERR_DEVICE : TQ_OK;
+}
+
+}  // namespace tqi

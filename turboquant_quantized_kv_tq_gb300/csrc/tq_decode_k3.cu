@@ -1,0 +1,25 @@
+// Instantiations of the decode and logits kernels for 3-bit key codes.  The codec
+// combinations built are those of the schemes at n bits (Plain-KV, TQ-KV, KQV, QKQV) and the
+// HeadQ key side; other combinations report "not built".
+#include "tq_decode_kernel.cuh"
+
+namespace tqd {
+
+bool dispatch_decode_k3(int kq, int kh, int vb, int vq, const DecodeParams& p, dim3 g, cudaStream_t s,
+                        cudaError_t* e) {
+  TQ_DECODE_CASE(3, 0, 0, 3, 0)
+  TQ_DECODE_CASE(3, 0, 0, 2, 1)
+  TQ_DECODE_CASE(3, 1, 0, 3, 1)
+  TQ_DECODE_CASE(3, 0, 1, 3, 0)
+  TQ_DECODE_CASE(3, 0, 1, 2, 1)
+  return false;
+}
+
+bool dispatch_logits_k3(int kq, int kh, const LogitsParams& p, dim3 g, cudaStream_t s, cudaError_t* e) {
+  TQ_LOGITS_CASE(3, 0, 0)
+  TQ_LOGITS_CASE(3, 1, 0)
+  TQ_LOGITS_CASE(3, 0, 1)
+  return false;
+}
+
+}  // namespace tqd

@@ -1,0 +1,210 @@
+// Device-side views and helpers shared by the write-path and read-path kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tq_internal.h"
+
+namespace tqd {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Device pointers into the table blob.
+struct Tables {
+  const float* k_c;   // centroids, ascending, 16 slots
+  const float* k_t;   // thresholds, 16 slots (unused = 3e38)
+  const float* v_c;
+  const float* v_t;
+  const float* k_sign;  // D_K as +-1 (all +1 when K is not rotated)
+  const float* v_sign;
+  const float* S_K;   // [m][d]
+  const float* S_K_T; // [d][m]
+  const float* S_V;
+  const float* S_V_T;
+  const float* U_rot; // [H_kv][d][r], R_K U
+};
+
+// The packed cache: region r of slab (b, h), token t at base + off[r] + ((b*H+h)*cap + t)*rec[r].
+struct Cache {
+  unsigned char* base;
+  unsigned long long off[tqi::R_COUNT];
+  unsigned int rec[tqi::R_COUNT];
+  int num_kv_heads;
+  int capacity;
+
+  __device__ __forceinline__ unsigned char* ptr(int r, int b, int h, int t) const {
+    return base + off[r] +
+           ((unsigned long long)(b * num_kv_heads + h) * (unsigned long long)capacity + t) * rec[r];
+  }
+  __device__ __forceinline__ unsigned char* slab(int r, int b, int h) const {
+    return base + off[r] +
+           (unsigned long long)(b * num_kv_heads + h) * (unsigned long long)capacity * rec[r];
+  }
+};
+
+inline Tables make_tables(const tq_context* ctx) {
+  const unsigned char* b = (const unsigned char*)ctx->dev_tables;
+  Tables t;
+  t.k_c = (const float*)(b + ctx->tab.k_centroids);
+  t.k_t = (const float*)(b + ctx->tab.k_thresholds);
+  t.v_c = (const float*)(b + ctx->tab.v_centroids);
+  t.v_t = (const float*)(b + ctx->tab.v_thresholds);
+  t.k_sign = (const float*)(b + ctx->tab.k_signs);
+  t.v_sign = (const float*)(b + ctx->tab.v_signs);
+  t.S_K = ctx->cfg.k.qjl ? (const float*)(b + ctx->tab.s_k) : nullptr;
+  t.S_K_T = ctx->cfg.k.qjl ? (const float*)(b + ctx->tab.s_k_t) : nullptr;
+  t.S_V = ctx->cfg.v.qjl ? (const float*)(b + ctx->tab.s_v) : nullptr;
+  t.S_V_T = ctx->cfg.v.qjl ? (const float*)(b + ctx->tab.s_v_t) : nullptr;
+  t.U_rot = ctx->cfg.headq_rank ? (const float*)(b + ctx->tab.headq_u) : nullptr;
+  return t;
+}
+
+inline Cache make_cache(const tq_context* ctx, const void* cache) {
+  Cache c;
+  c.base = (unsigned char*)cache;
+  for (int r = 0; r < tqi::R_COUNT; ++r) {
+    c.off[r] = ctx->layout.off[r];
+    c.rec[r] = (unsigned)ctx->layout.rec[r];
+  }
+  c.num_kv_heads = ctx->cfg.num_kv_heads;
+  c.capacity = ctx->cfg.capacity;
+  return c;
+}
+
+// Walsh-Hadamard butterflies over a warp holding E consecutive elements per lane
+// (element index lane * E + i): computes H x with H_ij = (-1)^popcount(i & j), natural order.
+template <int E>
+__device__ __forceinline__ void wht_warp(float (&x)[E]) {
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+    }
+  }
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float other = __shfl_xor_sync(kFull, x[i], m);
+      x[i] = (lane & m) ? (other - x[i]) : (x[i] + other);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
+  return v;
+}
+
+// Load E consecutive input elements as fp32.
+template <int E, typename T>
+__device__ __forceinline__ void load_row(const T* p, float (&x)[E]);
+
+template <int E>
+__device__ __forceinline__ void load_row(const float* p, float (&x)[E]) {
+#pragma unroll
+  for (int i = 0; i < E; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p + i);
+    x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* p, float (&x)[E]) {
+#pragma unroll
+  for (int i = 0; i < E; i += 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p + i);
+    x[i] = __uint_as_float(v.x << 16);
+    x[i + 1] = __uint_as_float(v.x & 0xffff0000u);
+    x[i + 2] = __uint_as_float(v.y << 16);
+    x[i + 3] = __uint_as_float(v.y & 0xffff0000u);
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void load_row(const __half* p, float (&x)[E]) {
+#pragma unroll
+  for (int i = 0; i < E; i += 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p + i);
+    const __half2 a = *reinterpret_cast<const __half2*>(&v.x);
+    const __half2 b = *reinterpret_cast<const __half2*>(&v.y);
+    const float2 fa = __half22float2(a), fb = __half22float2(b);
+    x[i] = fa.x; x[i + 1] = fa.y; x[i + 2] = fb.x; x[i + 3] = fb.y;
+  }
+}
+
+// ---- tensor-core fragments (mma.sync m16n8k16, fp16 inputs, fp32 accumulators) ----
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held as one register per lane in the mma
+// accumulator layout (lane (g, t) holds row g, columns 2t, 2t+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Streaming 128/64/32/16-bit loads that do not allocate in L1.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream2(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// Bits of a 32-bit word rearranged: even bits to the low half, odd bits to the high half.
+__device__ __forceinline__ uint32_t unshuffle_bits(uint32_t x) {
+  uint32_t t;
+  t = (x ^ (x >> 1)) & 0x22222222u; x ^= t ^ (t << 1);
+  t = (x ^ (x >> 2)) & 0x0C0C0C0Cu; x ^= t ^ (t << 2);
+  t = (x ^ (x >> 4)) & 0x00F000F0u; x ^= t ^ (t << 4);
+  t = (x ^ (x >> 8)) & 0x0000FF00u; x ^= t ^ (t << 8);
+  return x;
+}
+
+}  // namespace tqd

@@ -1,0 +1,72 @@
+// Internal declarations shared by the host API and the CUDA launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "tq.h"
+
+namespace tqi {
+
+constexpr int kMaxLevels = 16;     // 4-bit codebooks
+constexpr int kTableAlign = 256;
+constexpr int kRegionAlign = 256;
+
+enum RegionId {
+  R_K_CODES = 0, R_K_NORM, R_K_SIGNS, R_K_RHO, R_K_SIDE, R_K_SIDE_SCALE,
+  R_V_CODES, R_V_NORM, R_V_SIGNS, R_V_RHO, R_COUNT
+};
+
+// Byte offsets of the arrays inside the table blob (see tq_tables_host in tq.h).
+struct TableOffsets {
+  size_t k_centroids, k_thresholds, v_centroids, v_thresholds;
+  size_t k_signs, v_signs, s_k, s_k_t, s_v, s_v_t, headq_u, total;
+};
+
+struct Layout {
+  uint64_t off[R_COUNT];
+  uint64_t rec[R_COUNT];
+  uint64_t total;
+};
+
+// Host tables: Beta Lloyd-Max codebook (float64) and SplitMix64-driven D and S.
+void lloyd_max_beta(int d, int bits, double* centroids, double* thresholds);
+uint64_t splitmix_mix64(uint64_t z);
+void rotation_signs(uint64_t seed, uint64_t stream, int d, float* out);
+void sketch_matrix(uint64_t seed, uint64_t stream, int m, int d, float* out);
+
+Layout make_layout(const tq_config& cfg, int m);
+TableOffsets make_table_offsets(const tq_config& cfg, int m);
+
+void set_error(const std::string& msg);
+
+}  // namespace tqi
+
+struct tq_context {
+  tq_config cfg;
+  int m;
+  tqi::TableOffsets tab;
+  tqi::Layout layout;
+  std::vector<unsigned char> host_tables;
+  void* dev_tables = nullptr;
+  bool basis_set = false;
+};
+
+// Launchers (tq_append.cu, tq_decode.cu).  They assume validated arguments.
+namespace tqi {
+typedef struct CUstream_st* Stream;
+tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
+                        tq_dtype dtype, int n_new, const int32_t* start, Stream stream);
+tq_status launch_rotate_basis(const tq_context* ctx, const float* U, Stream stream);
+tq_status launch_dequantize(const tq_context* ctx, const void* cache, int b, int kvh, int t0,
+                            int t1, float* k_out, float* v_out, Stream stream);
+size_t decode_workspace_bytes(const tq_context* ctx, int max_seq);
+tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
+                        const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
+                        Stream stream);
+tq_status launch_logits(const tq_context* ctx, const void* cache, const float* q,
+                        const int32_t* seq_len, float* logits, int stride, Stream stream);
+tq_status read_device_error(const void* ws, int32_t* code, Stream stream);
+}  // namespace tqi
