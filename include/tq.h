@@ -169,6 +169,24 @@ tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, cons
                               const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
                               tq_stream stream);
 
+/* Size of the library's built-in decode scratch (see tq_decode_attention_static). */
+#define TQ_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* tq_decode_attention without a workspace argument: the pages have no counterpart for this
+ * entry point; it exists for callers that cannot allocate device memory at the call site --
+ * code running inside another framework's stream with no access to its allocator, real-time
+ * decode loops whose memory is planned up front and where a cudaMalloc (which may synchronize
+ * the device) is not allowed, or plugins that are handed only input and output pointers.
+ * The scratch is a file-scope device array of TQ_STATIC_SCRATCH_BYTES (8 MiB) that every GPU
+ * which loads the library holds until the process exits.  The first call on a device looks up
+ * that array's device address (with the device current) and caches it; make that first call
+ * before any stream capture.  Every call shares the one array, so calls that overlap on the GPU
+ * (other streams, other threads) race: serialize them.  A configuration whose workspace
+ * (tq_decode_workspace_bytes) exceeds TQ_STATIC_SCRATCH_BYTES returns TQ_ERR_WORKSPACE without
+ * launching.  No device memory is allocated.  Arguments otherwise as tq_decode_attention. */
+tq_status tq_decode_attention_static(const tq_context* ctx, const void* dev_cache, const float* q,
+                                     const int32_t* host_seq_len, float* out, tq_stream stream);
+
 /* HeadQ read path, unfused ([HEADQ] "Leitura do Cache"): corrected logits
  * s_hat_j = q^T k_base_j / sqrt(d) + q^T U z_hat_j / sqrt(d) for every stored token, written to
  * logits[b][h][j] (fp32, row stride logits_stride >= max(host_seq_len)); entries at j >=

@@ -87,6 +87,8 @@ DECLARATIONS = [
     ("tq_decode_workspace_bytes", c_size_t, [c_void_p, c_int32]),
     ("tq_decode_attention", c_int32, [c_void_p, c_void_p, c_void_p, ctypes.POINTER(c_int32), c_void_p,
                                       c_void_p, c_size_t, c_void_p]),
+    ("tq_decode_attention_static", c_int32, [c_void_p, c_void_p, c_void_p, ctypes.POINTER(c_int32),
+                                             c_void_p, c_void_p]),
     ("tq_headq_correct", c_int32, [c_void_p, c_void_p, c_void_p, ctypes.POINTER(c_int32), c_void_p,
                                    c_int32, c_void_p]),
     ("tq_dequantize", c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,

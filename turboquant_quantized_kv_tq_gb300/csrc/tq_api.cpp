@@ -245,6 +245,28 @@ tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, cons
   return launch_decode(ctx, dev_cache, q, host_seq_len, out, ws, ws_bytes, stream);
 }
 
+tq_status tq_decode_attention_static(const tq_context* ctx, const void* dev_cache, const float* q,
+                                     const int32_t* host_seq_len, float* out, tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (!dev_cache || !q || !host_seq_len || !out) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (!aligned(dev_cache, 256) || !aligned(q, 16) || !aligned(out, 16))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer (cache 256 B, q/out 16 B)");
+  int max_seq;
+  s = check_lengths(ctx, host_seq_len, &max_seq);
+  if (s != TQ_OK) return s;
+  const size_t need = decode_workspace_bytes(ctx, max_seq);
+  if (need > TQ_STATIC_SCRATCH_BYTES)
+    return fail(TQ_ERR_WORKSPACE, "this configuration needs " + std::to_string(need) +
+                                      " bytes of decode scratch; the built-in scratch holds " +
+                                      std::to_string((size_t)TQ_STATIC_SCRATCH_BYTES) +
+                                      " (use tq_decode_attention with a caller workspace)");
+  void* ws = nullptr;
+  s = static_scratch(&ws);
+  if (s != TQ_OK) return s;
+  return launch_decode(ctx, dev_cache, q, host_seq_len, out, ws, TQ_STATIC_SCRATCH_BYTES, stream);
+}
+
 tq_status tq_headq_correct(const tq_context* ctx, const void* dev_cache, const float* q,
                            const int32_t* host_seq_len, float* logits, int32_t logits_stride,
                            tq_stream stream) {

@@ -1,4 +1,5 @@
 // Read path launchers: query preparation, fused split-K decode, corrected logits.
+#include <mutex>
 #include <string>
 
 #include "tq_decode_kernel.cuh"
@@ -245,6 +246,35 @@ tq_status launch_logits(const tq_context* ctx, const void* cache, const float* q
     return TQ_ERR_UNSUPPORTED;
   }
   if (e != cudaSuccess) return cuda_fail("logits", e);
+  return TQ_OK;
+}
+
+// Built-in scratch of tq_decode_attention_static.  In host code the array's name is only a
+// stand-in, so its device address is looked up once per device and cached.
+static __device__ __align__(256) unsigned char g_tq_static_scratch[TQ_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+
+tq_status static_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return tqd::cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal out of range for the static scratch");
+    return TQ_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_tq_static_scratch);
+    if (e != cudaSuccess) return tqd::cuda_fail("cudaGetSymbolAddress(static scratch)", e);
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
   return TQ_OK;
 }
 

@@ -69,4 +69,6 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
 tq_status launch_logits(const tq_context* ctx, const void* cache, const float* q,
                         const int32_t* seq_len, float* logits, int stride, Stream stream);
 tq_status read_device_error(const void* ws, int32_t* code, Stream stream);
+// Device address of the built-in decode scratch on the current device (looked up once per device).
+tq_status static_scratch(void** ptr);
 }  // namespace tqi
