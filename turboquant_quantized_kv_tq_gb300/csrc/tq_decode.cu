@@ -7,33 +7,23 @@
 namespace tqd {
 namespace {
 
-// Blocks the decode grid aims for: the kernel holds more than 128 registers per thread, so one
-// 256-thread block fits per SM; two blocks per SM of a 152-SM GB300 keep the last wave short.
-constexpr int kTargetBlocks = 2 * 152;
-constexpr int kMinTokensPerBlock = 256;
 constexpr int kLogitsTokensPerBlock = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct WsLayout {
   size_t err, tickets, q_rot, q_sk, q_u, part, total;
-  int splits, chunk, ps;
+  int ps;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-WsLayout ws_layout(const tq_context* ctx, int max_seq) {
+// The workspace does not depend on the sequence lengths: partial slots are reserved for every
+// slab plus one per possible block.
+WsLayout ws_layout(const tq_context* ctx) {
   WsLayout w;
   const int B = ctx->cfg.batch, Hkv = ctx->cfg.num_kv_heads, Hq = ctx->cfg.num_q_heads;
   const int D = ctx->cfg.head_dim;
   const int pairs = B * Hkv;
-  int splits = (kTargetBlocks + pairs - 1) / pairs;
-  const int by_len = (max_seq + kMinTokensPerBlock - 1) / kMinTokensPerBlock;
-  if (splits > by_len) splits = by_len;
-  if (splits < 1) splits = 1;
-  int chunk = (max_seq + splits - 1) / splits;
-  chunk = (chunk + kTile - 1) / kTile * kTile;
-  w.splits = splits;
-  w.chunk = chunk;
   w.ps = 4 + D + (ctx->cfg.v.qjl ? ctx->m : 0);
   size_t off = 0;
   w.err = off; off = align256(off + 64 * sizeof(int));
@@ -41,9 +31,17 @@ WsLayout ws_layout(const tq_context* ctx, int max_seq) {
   w.q_rot = off; off = align256(off + (size_t)B * Hq * D * 2);
   w.q_sk = off; off = align256(off + (ctx->cfg.k.qjl ? (size_t)B * Hq * ctx->m * 2 : 0));
   w.q_u = off; off = align256(off + (ctx->cfg.headq_rank ? (size_t)B * Hq * 16 * 2 : 0));
-  w.part = off; off = align256(off + (size_t)pairs * splits * kHeadsPad * w.ps * sizeof(float));
+  w.part = off; off = align256(off + (size_t)(pairs + kMaxBlocks) * kHeadsPad * w.ps * sizeof(float));
   w.total = off;
   return w;
+}
+
+// Number of SMs of the current device (the decode runs one block per SM).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kMaxBlocks;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kMaxBlocks;
+  return n < kMaxBlocks ? n : kMaxBlocks;
 }
 
 struct PrepParams {
@@ -54,7 +52,9 @@ struct PrepParams {
   uint32_t* q_u;
   int* tickets;
   int* err;
+  float* out;
   int n_tickets, n_heads, Hq, G, k_rotate, kq, kh;
+  int seq_len[TQ_MAX_BATCH];
 };
 
 // Per query head (one warp): q_rot = R_K q; S_K q_rot for a QJL key side; U_rot^T q_rot = U^T q
@@ -68,6 +68,9 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   }
   const int head = blockIdx.x * 8 + (threadIdx.x >> 5);  // flat [B][Hq] index
   if (head >= p.n_heads) return;
+  if (p.seq_len[head / p.Hq] == 0) {  // no keys: the output is 0 and no block will write it
+    *reinterpret_cast<float4*>(p.out + (long long)head * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const float4 q4 = *reinterpret_cast<const float4*>(p.q + (long long)head * D + 4 * lane);
   float x[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
@@ -130,7 +133,22 @@ tq_status cuda_fail(const char* what, cudaError_t e) {
 namespace tqi {
 
 size_t decode_workspace_bytes(const tq_context* ctx, int max_seq) {
-  return tqd::ws_layout(ctx, max_seq).total;
+  (void)max_seq;
+  return tqd::ws_layout(ctx).total;
+}
+
+static bool dispatch_decode(const tq_context* ctx, const tqd::DecodeParams& p, dim3 grid,
+                            cudaStream_t s, cudaError_t* e) {
+  using namespace tqd;
+  const int kb = ctx->cfg.k.bits, kq = ctx->cfg.k.qjl, kh = ctx->cfg.headq_rank ? 1 : 0;
+  const int vb = ctx->cfg.v.bits, vq = ctx->cfg.v.qjl;
+  switch (kb) {
+    case 1: return dispatch_decode_k1(kq, kh, vb, vq, p, grid, s, e);
+    case 2: return dispatch_decode_k2(kq, kh, vb, vq, p, grid, s, e);
+    case 3: return dispatch_decode_k3(kq, kh, vb, vq, p, grid, s, e);
+    case 4: return dispatch_decode_k4(kq, kh, vb, vq, p, grid, s, e);
+  }
+  return false;
 }
 
 tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
@@ -142,13 +160,17 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
     set_error("decode attention is built for head_dim 128");
     return TQ_ERR_UNSUPPORTED;
   }
-  int max_seq = 0;
-  for (int b = 0; b < ctx->cfg.batch; ++b) max_seq = seq_len[b] > max_seq ? seq_len[b] : max_seq;
-  const WsLayout w = ws_layout(ctx, max_seq);
+  const WsLayout w = ws_layout(ctx);
   unsigned char* base = (unsigned char*)ws;
   const cudaStream_t s = (cudaStream_t)stream;
   const Tables tab = make_tables(ctx);
   const int B = ctx->cfg.batch, Hkv = ctx->cfg.num_kv_heads, Hq = ctx->cfg.num_q_heads;
+
+  DecodeParams p;
+  if (!dispatch_decode(ctx, p, dim3(1), s, nullptr)) {  // probe only: nothing launches
+    set_error("decode attention is not built for this combination of key and value codecs");
+    return TQ_ERR_UNSUPPORTED;
+  }
 
   PrepParams pp;
   pp.tab = tab;
@@ -165,11 +187,12 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   pp.k_rotate = ctx->cfg.k.rotate;
   pp.kq = ctx->cfg.k.qjl;
   pp.kh = ctx->cfg.headq_rank ? 1 : 0;
+  pp.out = out;
+  for (int b = 0; b < TQ_MAX_BATCH; ++b) pp.seq_len[b] = b < B ? seq_len[b] : 0;
   prep_kernel<<<(B * Hq + 7) / 8, 256, 0, s>>>(pp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail("decode prep", e);
 
-  DecodeParams p;
   p.tab = tab;
   p.cache = make_cache(ctx, cache);
   p.q_rot = pp.q_rot;
@@ -181,27 +204,22 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   p.B = B;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
-  p.splits = w.splits;
-  p.chunk = w.chunk;
   p.v_rotate = ctx->cfg.v.rotate;
   p.score_scale = kLog2e / sqrtf((float)kDecD);
   p.qjl_scale = (float)(1.2533141373155003 / ctx->m);
-  for (int b = 0; b < TQ_MAX_BATCH; ++b) p.seq_len[b] = b < B ? seq_len[b] : 0;
-  const dim3 grid(w.splits, Hkv, B);
-  const int kb = ctx->cfg.k.bits, kq = ctx->cfg.k.qjl, kh = ctx->cfg.headq_rank ? 1 : 0;
-  const int vb = ctx->cfg.v.bits, vq = ctx->cfg.v.qjl;
-  bool built = false;
+  long long W = 0;
+  for (int b = 0; b < TQ_MAX_BATCH; ++b) {
+    p.seq_len[b] = b < B ? seq_len[b] : 0;
+    p.batch_start[b] = W;
+    W += (long long)Hkv * p.seq_len[b];
+  }
+  p.batch_start[TQ_MAX_BATCH] = W;
+  p.W = W;
+  if (W == 0) return TQ_OK;  // every sequence is empty: prep wrote the zero outputs
+  const int nsm = sm_count();
+  p.nblocks = W < nsm ? (int)W : nsm;  // every block gets a non-empty range
   e = cudaSuccess;
-  switch (kb) {
-    case 1: built = dispatch_decode_k1(kq, kh, vb, vq, p, grid, s, &e); break;
-    case 2: built = dispatch_decode_k2(kq, kh, vb, vq, p, grid, s, &e); break;
-    case 3: built = dispatch_decode_k3(kq, kh, vb, vq, p, grid, s, &e); break;
-    case 4: built = dispatch_decode_k4(kq, kh, vb, vq, p, grid, s, &e); break;
-  }
-  if (!built) {
-    set_error("decode attention is not built for this combination of key and value codecs");
-    return TQ_ERR_UNSUPPORTED;
-  }
+  dispatch_decode(ctx, p, dim3(p.nblocks), s, &e);
   if (e != cudaSuccess) return cuda_fail("decode", e);
   return TQ_OK;
 }

@@ -11,17 +11,22 @@
 // side, acc_sk = sum p nu_V rho_V (2 sigma - 1); the merge applies
 // o = R_V^T (acc + sqrt(pi/2)/m S_V^T acc_sk) / l once per head.
 //
-// Work split: grid (splits, H_kv, B); each block covers one contiguous token range of one
-// (batch, KV head) slab for all G <= 8 query heads of the group; each warp streams its own
-// sub-range in tiles of 16 tokens.  Per tile:
+// Work split (balanced, "stream-K"): the (batch, KV head, token) positions of all sequences are
+// laid end to end and cut into one equal contiguous range per block, one block per SM.  A block
+// walks the slab segments of its range; for each, its warps stream contiguous sub-ranges in
+// tiles of 16 tokens and the block merges them into one partial per (slab, block).  The last
+// block to finish a slab (atomic ticket) merges that slab's partials in block order and writes
+// the output.  Per tile:
 //   scores  S[16 tok x 8 heads] = K_hat[16 x 128] Q[128 x 8]   (8 mma.m16n8k16)
 //   readout O^T[128 dims x 8 heads] += V_hat^T[128 x 16] P[16 x 8]  (8 mma), P moved from the
 //           score accumulator layout to the B operand layout with movmatrix.trans.
-// Packed codes go straight from global memory (16-byte coalesced loads) to registers and are
-// expanded to fp16 pairs through lane-replicated lookup tables in shared memory (entry e for
-// lane l at word 32 e + l: conflict-free) or, for sign bits, by moving the bit into the fp16
-// sign position.  Token order inside a tile is permuted so that each thread's value operands
-// come from four consecutive tokens: score row r <-> token pi(r) = 4((r&7)>>1) + 2(r>>3) + (r&1).
+// Loads: every thread copies exactly the bytes it will use into its own shared-memory slots
+// with cp.async, kStages tiles ahead (nothing in flight occupies registers; reading back one's
+// own slots is conflict-free).  Codes become fp16 pairs through lane-replicated tables (entry e,
+// lane l at byte 256 e + 4 l, the address built by one byte permute) or, for sign bits, by
+// moving the bit to the fp16 sign position.  Token order inside a tile is permuted so each
+// thread's value operands come from four consecutive tokens:
+// score row r <-> token pi(r) = 4((r&7)>>1) + 2(r>>3) + (r&1).
 #pragma once
 
 #include <cfloat>
@@ -34,6 +39,9 @@ constexpr int kDecD = 128;
 constexpr int kDecWarps = 8;
 constexpr int kTile = 16;
 constexpr int kHeadsPad = 8;
+constexpr int kStages = 4;
+constexpr int kMaxBlocks = 256;  // partial slots reserved for blocks (>= SM count)
+constexpr int kLutStride = 256;  // bytes between table entries
 
 struct DecodeParams {
   Tables tab;
@@ -41,13 +49,15 @@ struct DecodeParams {
   const uint32_t* q_rot;  // fp16 pairs [B][Hq][D/2]
   const uint32_t* q_sk;   // fp16 pairs [B][Hq][m/2]
   const uint32_t* q_u;    // fp16 pairs [B][Hq][8]
-  float* part;            // [B][Hkv][splits][8][PS]
-  int* tickets;           // [B][Hkv]
+  float* part;            // [B*Hkv + kMaxBlocks][8][PS]; slab p's partial from block c at p + c
+  int* tickets;           // [B*Hkv]
   float* out;             // [B][Hq][D]
-  int B, Hkv, G, splits, chunk, v_rotate;
-  float score_scale;  // log2(e) / sqrt(d)
-  float qjl_scale;    // sqrt(pi/2) / m
+  int B, Hkv, G, v_rotate, nblocks;
+  long long W;            // number of (batch, KV head, token) positions
+  float score_scale;      // log2(e) / sqrt(d)
+  float qjl_scale;        // sqrt(pi/2) / m
   int seq_len[TQ_MAX_BATCH];
+  long long batch_start[TQ_MAX_BATCH + 1];  // Hkv * sum of seq_len over earlier batches
 };
 
 template <int B>
@@ -55,10 +65,10 @@ struct LutEntries { static constexpr int value = B == 4 ? 256 : (B == 1 ? 0 : 16
 
 // Lane-replicated pair table for a b-bit codebook (sign-magnitude symbols).
 template <int B>
-__device__ __forceinline__ void build_lut(uint32_t* lut, const float* cent) {
+__device__ __forceinline__ void build_lut(unsigned char* lut, const float* cent) {
   constexpr int N = LutEntries<B>::value;
   for (int i = threadIdx.x; i < N * 32; i += blockDim.x) {
-    const int e = i >> 5;
+    const int e = i >> 5, l = i & 31;
     float lo, hi;
     if constexpr (B == 4) {
       const int a = e & 15, c = e >> 4;
@@ -72,12 +82,14 @@ __device__ __forceinline__ void build_lut(uint32_t* lut, const float* cent) {
       lo = (a & 2 ? 1.f : -1.f) * __ldg(cent + 2 + (a & 1));
       hi = (c & 2 ? 1.f : -1.f) * __ldg(cent + 2 + (c & 1));
     }
-    lut[i] = pack_half2(lo, hi);
+    *reinterpret_cast<uint32_t*>(lut + e * kLutStride + 4 * l) = pack_half2(lo, hi);
   }
 }
 
-__device__ __forceinline__ uint32_t lut_get(const uint32_t* lut_lane, uint32_t idx) {
-  return lut_lane[idx << 5];
+// Table word for index = byte j of w: byte offset w.byte_j * 256 + lane * 4 (lane4 = lane * 4).
+__device__ __forceinline__ uint32_t lut_get(const unsigned char* lut, uint32_t w, uint32_t lane4, int j) {
+  const uint32_t off = __byte_perm(w, lane4, 0x5504u | ((uint32_t)j << 4));
+  return *reinterpret_cast<const uint32_t*>(lut + off);
 }
 
 // half2 with the sign bits taken from bits 15 and 31 of ~xsh (bit set in xsh = positive).
@@ -85,20 +97,23 @@ __device__ __forceinline__ uint32_t signed_pair(uint32_t mag, uint32_t xsh) {
   return mag | (~xsh & 0x80008000u);
 }
 
+// Nibbles 0,2,4,6 / 1,3,5,7 of w, one per byte.
+__device__ __forceinline__ uint32_t nib_even(uint32_t w) { return w & 0x0F0F0F0Fu; }
+__device__ __forceinline__ uint32_t nib_odd(uint32_t w) { return (w >> 4) & 0x0F0F0F0Fu; }
+
 // ---------------------------------------------------------------------------------------------
 // Key side: per thread, the 32-coordinate chunk [32 lt, 32 lt + 32) of the two tokens of its
-// score rows.
+// score rows.  pair(p) is the fp16 pair of coordinates (2p, 2p+1) of the chunk.
 template <int KB>
 struct KChunk;
 
 template <>
 struct KChunk<4> {
   uint4 c;
-  __device__ __forceinline__ void load(const unsigned char* rec, int lt) { c = ldg_stream16(rec + 16 * lt); }
   __device__ __forceinline__ void prepare() {}
-  __device__ __forceinline__ uint32_t pair(const uint32_t* lut, uint32_t, int p) const {
+  __device__ __forceinline__ uint32_t pair(const unsigned char* lut, uint32_t lane4, uint32_t, int p) const {
     const uint32_t w = p < 4 ? c.x : p < 8 ? c.y : p < 12 ? c.z : c.w;
-    return lut_get(lut, (w >> (8 * (p & 3))) & 0xffu);
+    return lut_get(lut, w, lane4, p & 3);
   }
 };
 
@@ -106,35 +121,35 @@ template <>
 struct KChunk<3> {
   uint2 k;
   uint32_t s;
-  __device__ __forceinline__ void load(const unsigned char* rec, int lt) {
-    k = ldg_stream8(rec + 8 * lt);
-    s = ldg_stream4(rec + kDecD / 4 + 4 * lt);
+  uint32_t xe, xo, ye, yo;
+  __device__ __forceinline__ void prepare() {
+    xe = nib_even(k.x); xo = nib_odd(k.x); ye = nib_even(k.y); yo = nib_odd(k.y);
+    s = unshuffle_bits(s);
   }
-  __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
-  __device__ __forceinline__ uint32_t pair(const uint32_t* lut, uint32_t, int p) const {
-    const uint32_t w = p < 8 ? k.x : k.y;
-    const uint32_t mag = lut_get(lut, (w >> (4 * (p & 7))) & 0xfu);
-    return signed_pair(mag, s << (15 - p));
+  __device__ __forceinline__ uint32_t pair(const unsigned char* lut, uint32_t lane4, uint32_t, int p) const {
+    const uint32_t w = p < 8 ? (p & 1 ? xo : xe) : (p & 1 ? yo : ye);
+    return signed_pair(lut_get(lut, w, lane4, (p & 7) >> 1), s << (15 - p));
   }
 };
 
 template <>
 struct KChunk<2> {
   uint2 k;
-  __device__ __forceinline__ void load(const unsigned char* rec, int lt) { k = ldg_stream8(rec + 8 * lt); }
-  __device__ __forceinline__ void prepare() {}
-  __device__ __forceinline__ uint32_t pair(const uint32_t* lut, uint32_t, int p) const {
-    const uint32_t w = p < 8 ? k.x : k.y;
-    return lut_get(lut, (w >> (4 * (p & 7))) & 0xfu);
+  uint32_t xe, xo, ye, yo;
+  __device__ __forceinline__ void prepare() {
+    xe = nib_even(k.x); xo = nib_odd(k.x); ye = nib_even(k.y); yo = nib_odd(k.y);
+  }
+  __device__ __forceinline__ uint32_t pair(const unsigned char* lut, uint32_t lane4, uint32_t, int p) const {
+    const uint32_t w = p < 8 ? (p & 1 ? xo : xe) : (p & 1 ? yo : ye);
+    return lut_get(lut, w, lane4, (p & 7) >> 1);
   }
 };
 
 template <>
 struct KChunk<1> {
   uint32_t s;
-  __device__ __forceinline__ void load(const unsigned char* rec, int lt) { s = ldg_stream4(rec + 4 * lt); }
   __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
-  __device__ __forceinline__ uint32_t pair(const uint32_t*, uint32_t m0, int p) const {
+  __device__ __forceinline__ uint32_t pair(const unsigned char*, uint32_t, uint32_t m0, int p) const {
     return signed_pair(m0, s << (15 - p));
   }
 };
@@ -142,13 +157,13 @@ struct KChunk<1> {
 // Sign chunk of a QJL key: 32 bits per token, as +-1 pairs.
 struct KSign {
   uint32_t s;
-  __device__ __forceinline__ void load(const unsigned char* rec, int lt) { s = ldg_stream4(rec + 4 * lt); }
   __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
   __device__ __forceinline__ uint32_t pair(int p) const { return signed_pair(0x3C003C00u, s << (15 - p)); }
 };
 
 // ---------------------------------------------------------------------------------------------
 // Value side: per thread, dims [16 lg, 16 lg + 16) of the four tokens 4 lt .. 4 lt + 3.
+// frag(mt) gives the A operand of M-tile mt: rows = dims 16 lg + 2 mt (+1), columns = tokens.
 template <int VB>
 struct VChunk;
 
@@ -156,10 +171,6 @@ template <>
 struct VChunk<4> {
   uint2 w[4];
   uint32_t e01[2], o01[2], e23[2], o23[2];
-  __device__ __forceinline__ void load(const unsigned char* const (&rec)[4], int lg) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = ldg_stream8(rec[j] + 8 * lg);
-  }
   __device__ __forceinline__ void prepare() {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -171,93 +182,97 @@ struct VChunk<4> {
       o23[h] = ((c >> 4) & 0x0F0F0F0Fu) | (d & 0xF0F0F0F0u);
     }
   }
-  __device__ __forceinline__ void frag(const uint32_t* lut, uint32_t, int mt, uint32_t (&a)[4]) const {
-    const int h = mt >> 2, sh = 8 * (mt & 3);
-    a[0] = lut_get(lut, (e01[h] >> sh) & 0xffu);
-    a[1] = lut_get(lut, (o01[h] >> sh) & 0xffu);
-    a[2] = lut_get(lut, (e23[h] >> sh) & 0xffu);
-    a[3] = lut_get(lut, (o23[h] >> sh) & 0xffu);
+  __device__ __forceinline__ void frag(const unsigned char* lut, uint32_t lane4, uint32_t, int mt,
+                                       uint32_t (&a)[4]) const {
+    const int h = mt >> 2, j = mt & 3;
+    a[0] = lut_get(lut, e01[h], lane4, j);
+    a[1] = lut_get(lut, o01[h], lane4, j);
+    a[2] = lut_get(lut, e23[h], lane4, j);
+    a[3] = lut_get(lut, o23[h], lane4, j);
+  }
+};
+
+// 2-bit fields of two tokens interleaved into nibbles (first token low), split into even / odd
+// nibble bytes: index nibble for dim 2 mt (e) and 2 mt + 1 (o).
+struct Pair2 {
+  uint32_t e01[2], o01[2], e23[2], o23[2];
+  __device__ __forceinline__ void build(const uint32_t (&k)[4]) {
+    const uint32_t e0 = (k[0] & 0x33333333u) | ((k[1] & 0x33333333u) << 2);
+    const uint32_t o0 = ((k[0] >> 2) & 0x33333333u) | (k[1] & 0xCCCCCCCCu);
+    const uint32_t e1 = (k[2] & 0x33333333u) | ((k[3] & 0x33333333u) << 2);
+    const uint32_t o1 = ((k[2] >> 2) & 0x33333333u) | (k[3] & 0xCCCCCCCCu);
+    e01[0] = nib_even(e0); e01[1] = nib_odd(e0);
+    o01[0] = nib_even(o0); o01[1] = nib_odd(o0);
+    e23[0] = nib_even(e1); e23[1] = nib_odd(e1);
+    o23[0] = nib_even(o1); o23[1] = nib_odd(o1);
+  }
+  __device__ __forceinline__ void mags(const unsigned char* lut, uint32_t lane4, int mt, uint32_t (&a)[4]) const {
+    const int h = mt & 1, j = mt >> 1;
+    a[0] = lut_get(lut, e01[h], lane4, j);
+    a[1] = lut_get(lut, o01[h], lane4, j);
+    a[2] = lut_get(lut, e23[h], lane4, j);
+    a[3] = lut_get(lut, o23[h], lane4, j);
+  }
+};
+
+// 1-bit stream, 16 dims per token: bit i of token j for dims 16 lg + i.
+struct Bits16 {
+  uint32_t x01, x23;
+  __device__ __forceinline__ void build(const uint32_t (&s)[4]) {
+    x01 = (s[0] & 0xffffu) | (s[1] << 16);
+    x23 = (s[2] & 0xffffu) | (s[3] << 16);
+  }
+  __device__ __forceinline__ void apply(int mt, uint32_t (&a)[4]) const {
+    a[0] = signed_pair(a[0], x01 << (15 - 2 * mt));
+    a[1] = signed_pair(a[1], x01 << (14 - 2 * mt));
+    a[2] = signed_pair(a[2], x23 << (15 - 2 * mt));
+    a[3] = signed_pair(a[3], x23 << (14 - 2 * mt));
   }
 };
 
 template <>
 struct VChunk<3> {
   uint32_t k[4], s[4];
-  uint32_t e01, o01, e23, o23, x01, x23;
-  __device__ __forceinline__ void load(const unsigned char* const (&rec)[4], int lg) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      k[j] = ldg_stream4(rec[j] + 4 * lg);
-      s[j] = ldg_stream2(rec[j] + kDecD / 4 + 2 * lg);
-    }
-  }
-  __device__ __forceinline__ void prepare() {
-    e01 = (k[0] & 0x33333333u) | ((k[1] & 0x33333333u) << 2);
-    o01 = ((k[0] >> 2) & 0x33333333u) | (k[1] & 0xCCCCCCCCu);
-    e23 = (k[2] & 0x33333333u) | ((k[3] & 0x33333333u) << 2);
-    o23 = ((k[2] >> 2) & 0x33333333u) | (k[3] & 0xCCCCCCCCu);
-    x01 = (s[0] & 0xffffu) | (s[1] << 16);
-    x23 = (s[2] & 0xffffu) | (s[3] << 16);
-  }
-  __device__ __forceinline__ void frag(const uint32_t* lut, uint32_t, int mt, uint32_t (&a)[4]) const {
-    const int sh = 4 * mt;
-    a[0] = signed_pair(lut_get(lut, (e01 >> sh) & 0xfu), x01 << (15 - 2 * mt));
-    a[1] = signed_pair(lut_get(lut, (o01 >> sh) & 0xfu), x01 << (14 - 2 * mt));
-    a[2] = signed_pair(lut_get(lut, (e23 >> sh) & 0xfu), x23 << (15 - 2 * mt));
-    a[3] = signed_pair(lut_get(lut, (o23 >> sh) & 0xfu), x23 << (14 - 2 * mt));
+  Pair2 m;
+  Bits16 sg;
+  __device__ __forceinline__ void prepare() { m.build(k); sg.build(s); }
+  __device__ __forceinline__ void frag(const unsigned char* lut, uint32_t lane4, uint32_t, int mt,
+                                       uint32_t (&a)[4]) const {
+    m.mags(lut, lane4, mt, a);
+    sg.apply(mt, a);
   }
 };
 
 template <>
 struct VChunk<2> {
   uint32_t k[4];
-  uint32_t e01, o01, e23, o23;
-  __device__ __forceinline__ void load(const unsigned char* const (&rec)[4], int lg) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) k[j] = ldg_stream4(rec[j] + 4 * lg);
-  }
-  __device__ __forceinline__ void prepare() {
-    e01 = (k[0] & 0x33333333u) | ((k[1] & 0x33333333u) << 2);
-    o01 = ((k[0] >> 2) & 0x33333333u) | (k[1] & 0xCCCCCCCCu);
-    e23 = (k[2] & 0x33333333u) | ((k[3] & 0x33333333u) << 2);
-    o23 = ((k[2] >> 2) & 0x33333333u) | (k[3] & 0xCCCCCCCCu);
-  }
-  __device__ __forceinline__ void frag(const uint32_t* lut, uint32_t, int mt, uint32_t (&a)[4]) const {
-    const int sh = 4 * mt;
-    a[0] = lut_get(lut, (e01 >> sh) & 0xfu);
-    a[1] = lut_get(lut, (o01 >> sh) & 0xfu);
-    a[2] = lut_get(lut, (e23 >> sh) & 0xfu);
-    a[3] = lut_get(lut, (o23 >> sh) & 0xfu);
-  }
-};
-
-// 1-bit stream of 16 dims per token: values (+-M0) or QJL signs (+-1) depending on `base`.
-struct VBits {
-  uint32_t s[4];
-  uint32_t x01, x23;
-  __device__ __forceinline__ void load(const unsigned char* const (&rec)[4], int lg) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) s[j] = ldg_stream2(rec[j] + 2 * lg);
-  }
-  __device__ __forceinline__ void prepare() {
-    x01 = (s[0] & 0xffffu) | (s[1] << 16);
-    x23 = (s[2] & 0xffffu) | (s[3] << 16);
-  }
-  __device__ __forceinline__ void frag(uint32_t base, int mt, uint32_t (&a)[4]) const {
-    a[0] = signed_pair(base, x01 << (15 - 2 * mt));
-    a[1] = signed_pair(base, x01 << (14 - 2 * mt));
-    a[2] = signed_pair(base, x23 << (15 - 2 * mt));
-    a[3] = signed_pair(base, x23 << (14 - 2 * mt));
+  Pair2 m;
+  __device__ __forceinline__ void prepare() { m.build(k); }
+  __device__ __forceinline__ void frag(const unsigned char* lut, uint32_t lane4, uint32_t, int mt,
+                                       uint32_t (&a)[4]) const {
+    m.mags(lut, lane4, mt, a);
   }
 };
 
 template <>
 struct VChunk<1> {
-  VBits bits;
-  __device__ __forceinline__ void load(const unsigned char* const (&rec)[4], int lg) { bits.load(rec, lg); }
-  __device__ __forceinline__ void prepare() { bits.prepare(); }
-  __device__ __forceinline__ void frag(const uint32_t*, uint32_t m0, int mt, uint32_t (&a)[4]) const {
-    bits.frag(m0, mt, a);
+  uint32_t s[4];
+  Bits16 sg;
+  __device__ __forceinline__ void prepare() { sg.build(s); }
+  __device__ __forceinline__ void frag(const unsigned char*, uint32_t, uint32_t m0, int mt, uint32_t (&a)[4]) const {
+    a[0] = a[1] = a[2] = a[3] = m0;
+    sg.apply(mt, a);
+  }
+};
+
+// QJL value signs: +-1 pairs.
+struct VSign {
+  uint32_t s[4];
+  Bits16 sg;
+  __device__ __forceinline__ void prepare() { sg.build(s); }
+  __device__ __forceinline__ void frag(int mt, uint32_t (&a)[4]) const {
+    a[0] = a[1] = a[2] = a[3] = 0x3C003C00u;
+    sg.apply(mt, a);
   }
 };
 
@@ -266,20 +281,16 @@ struct VChunk<1> {
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 struct TileData {
   KChunk<KB> kA, kB;
-  KSign sA, sB;             // KQ
-  uint2 zA, zB;             // KH: side code bytes lt, lt + 4 (as two words)
+  KSign sA, sB;  // KQ
+  uint2 zA, zB;  // KH: side code bytes lt, lt + 4
   float nuKA, nuKB, rhoKA, rhoKB, zsA, zsB;
   VChunk<VB> v;
-  VBits vs;                 // VQ
+  VSign vs;  // VQ
   float nuVA, nuVB, rhoVA, rhoVB;
 };
 
-__device__ __forceinline__ float ld_f32(const unsigned char* p) {
-  return __uint_as_float(ldg_stream4(p));
-}
-__device__ __forceinline__ float ld_f16(const unsigned char* p) {
-  const unsigned short h = (unsigned short)ldg_stream2(p);
-  return __half2float(__ushort_as_half(h));
+__device__ __forceinline__ float half_of(uint32_t word, int hi) {
+  return __half2float(__ushort_as_half((unsigned short)(hi ? word >> 16 : word & 0xffffu)));
 }
 
 // Signed 4-bit pairs (two's complement) -> exact fp16 integers, low nibble first.
@@ -294,28 +305,232 @@ __device__ __forceinline__ int tile_row_token(int r) {
   return 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
 }
 
+// Slab base pointers of one (batch, KV head).
+struct SlabPtrs {
+  const unsigned char* kc;
+  const unsigned char* kn;
+  const unsigned char* ks;
+  const unsigned char* kr;
+  const unsigned char* kz;
+  const unsigned char* kzs;
+  const unsigned char* vc;
+  const unsigned char* vn;
+  const unsigned char* vs;
+  const unsigned char* vr;
+  __device__ __forceinline__ void init(const Cache& C, int b, int h) {
+    kc = C.slab(tqi::R_K_CODES, b, h);
+    kn = C.slab(tqi::R_K_NORM, b, h);
+    ks = C.slab(tqi::R_K_SIGNS, b, h);
+    kr = C.slab(tqi::R_K_RHO, b, h);
+    kz = C.slab(tqi::R_K_SIDE, b, h);
+    kzs = C.slab(tqi::R_K_SIDE_SCALE, b, h);
+    vc = C.slab(tqi::R_V_CODES, b, h);
+    vn = C.slab(tqi::R_V_NORM, b, h);
+    vs = C.slab(tqi::R_V_SIGNS, b, h);
+    vr = C.slab(tqi::R_V_RHO, b, h);
+  }
+};
+
+template <int KB> struct KRec { static constexpr int value = kDecD * KB / 8; };
+
+// Per-thread slot layout of one tile: 16-, 8- and 4-byte items, each item an array over the
+// 32 lanes (item i of size z for lane l at offset off_z + (32 i + l) z).
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, const Cache& C, int b,
-                                           int kvh, int t0, int last, int lg, int lt) {
+struct Slots {
+  static constexpr int n16 = KB == 4 ? 2 : 0;
+  static constexpr int K8 = 0;
+  static constexpr int Z8 = K8 + ((KB == 3 || KB == 2) ? 2 : 0);
+  static constexpr int V8 = Z8 + (KH ? 2 : 0);
+  static constexpr int n8 = V8 + (VB == 4 ? 4 : 0);
+  static constexpr int KS4 = 0;
+  static constexpr int NK4 = KS4 + ((KB == 3 || KB == 1) ? 2 : 0);
+  static constexpr int Q4 = NK4 + 2;
+  static constexpr int H4 = Q4 + (KQ ? 4 : 0);
+  static constexpr int V4 = H4 + (KH ? 2 : 0);
+  static constexpr int NV4 = V4 + (VB == 3 ? 8 : (VB == 2 || VB == 1) ? 4 : 0);
+  static constexpr int VQ4 = NV4 + 2;
+  static constexpr int n4 = VQ4 + (VQ ? 6 : 0);
+  static constexpr int off8 = n16 * 16 * 32;
+  static constexpr int off4 = off8 + n8 * 8 * 32;
+  static constexpr int bytes = off4 + n4 * 4 * 32;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+// Start the copies of tile [t0, t0 + 16) (tokens clamped to `last`) into the slots at `st`
+// (shared-space address).
+template <int KB, bool KQ, bool KH, int VB, bool VQ>
+__device__ __forceinline__ void issue_tile(uint32_t st, const SlabPtrs& s, int t0, int last, int lg,
+                                           int lt, int lane) {
+  using S = Slots<KB, KQ, KH, VB, VQ>;
+  constexpr int KR = KRec<KB>::value;
+  constexpr int VR = KRec<VB>::value;
   const int tA = min(t0 + tile_row_token(lg), last);
   const int tB = min(t0 + tile_row_token(lg + 8), last);
-  d.kA.load(C.ptr(tqi::R_K_CODES, b, kvh, tA), lt);
-  d.kB.load(C.ptr(tqi::R_K_CODES, b, kvh, tB), lt);
-  d.nuKA = ld_f32(C.ptr(tqi::R_K_NORM, b, kvh, tA));
-  d.nuKB = ld_f32(C.ptr(tqi::R_K_NORM, b, kvh, tB));
+  int tv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) tv[j] = min(t0 + 4 * lt + j, last);
+  auto a16 = [&](int i) { return st + (uint32_t)((32 * i + lane) * 16); };
+  auto a8 = [&](int i) { return st + (uint32_t)(S::off8 + (32 * i + lane) * 8); };
+  auto a4 = [&](int i) { return st + (uint32_t)(S::off4 + (32 * i + lane) * 4); };
+  if constexpr (KB == 4) {
+    cp_async16(a16(0), s.kc + tA * KR + 16 * lt);
+    cp_async16(a16(1), s.kc + tB * KR + 16 * lt);
+  } else if constexpr (KB == 3 || KB == 2) {
+    cp_async8(a8(S::K8), s.kc + tA * KR + 8 * lt);
+    cp_async8(a8(S::K8 + 1), s.kc + tB * KR + 8 * lt);
+    if constexpr (KB == 3) {
+      cp_async4(a4(S::KS4), s.kc + tA * KR + kDecD / 4 + 4 * lt);
+      cp_async4(a4(S::KS4 + 1), s.kc + tB * KR + kDecD / 4 + 4 * lt);
+    }
+  } else {
+    cp_async4(a4(S::KS4), s.kc + tA * KR + 4 * lt);
+    cp_async4(a4(S::KS4 + 1), s.kc + tB * KR + 4 * lt);
+  }
+  cp_async4(a4(S::NK4), s.kn + tA * 4);
+  cp_async4(a4(S::NK4 + 1), s.kn + tB * 4);
   if constexpr (KQ) {
-    d.sA.load(C.ptr(tqi::R_K_SIGNS, b, kvh, tA), lt);
-    d.sB.load(C.ptr(tqi::R_K_SIGNS, b, kvh, tB), lt);
-    d.rhoKA = ld_f16(C.ptr(tqi::R_K_RHO, b, kvh, tA));
-    d.rhoKB = ld_f16(C.ptr(tqi::R_K_RHO, b, kvh, tB));
+    cp_async4(a4(S::Q4), s.ks + tA * (kDecD / 8) + 4 * lt);
+    cp_async4(a4(S::Q4 + 1), s.ks + tB * (kDecD / 8) + 4 * lt);
+    cp_async4(a4(S::Q4 + 2), s.kr + (tA & ~1) * 2);
+    cp_async4(a4(S::Q4 + 3), s.kr + (tB & ~1) * 2);
   }
   if constexpr (KH) {
-    const uint2 sa = ldg_stream8(C.ptr(tqi::R_K_SIDE, b, kvh, tA));
-    const uint2 sb = ldg_stream8(C.ptr(tqi::R_K_SIDE, b, kvh, tB));
-    d.zA = make_uint2((sa.x >> (8 * lt)) & 0xffu, (sa.y >> (8 * lt)) & 0xffu);
-    d.zB = make_uint2((sb.x >> (8 * lt)) & 0xffu, (sb.y >> (8 * lt)) & 0xffu);
-    d.zsA = ld_f16(C.ptr(tqi::R_K_SIDE_SCALE, b, kvh, tA));
-    d.zsB = ld_f16(C.ptr(tqi::R_K_SIDE_SCALE, b, kvh, tB));
+    cp_async8(a8(S::Z8), s.kz + tA * 8);
+    cp_async8(a8(S::Z8 + 1), s.kz + tB * 8);
+    cp_async4(a4(S::H4), s.kzs + (tA & ~1) * 2);
+    cp_async4(a4(S::H4 + 1), s.kzs + (tB & ~1) * 2);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if constexpr (VB == 4) {
+      cp_async8(a8(S::V8 + j), s.vc + tv[j] * VR + 8 * lg);
+    } else if constexpr (VB == 3) {
+      cp_async4(a4(S::V4 + j), s.vc + tv[j] * VR + 4 * lg);
+      cp_async4(a4(S::V4 + 4 + j), s.vc + tv[j] * VR + kDecD / 4 + 4 * (lg >> 1));
+    } else if constexpr (VB == 2) {
+      cp_async4(a4(S::V4 + j), s.vc + tv[j] * VR + 4 * lg);
+    } else {
+      cp_async4(a4(S::V4 + j), s.vc + tv[j] * VR + 4 * (lg >> 1));
+    }
+    if constexpr (VQ) cp_async4(a4(S::VQ4 + j), s.vs + tv[j] * (kDecD / 8) + 4 * (lg >> 1));
+  }
+  cp_async4(a4(S::NV4), s.vn + tA * 4);
+  cp_async4(a4(S::NV4 + 1), s.vn + tB * 4);
+  if constexpr (VQ) {
+    cp_async4(a4(S::VQ4 + 4), s.vr + (tA & ~1) * 2);
+    cp_async4(a4(S::VQ4 + 5), s.vr + (tB & ~1) * 2);
+  }
+}
+
+// Read this thread's slots of one tile back into registers.
+template <int KB, bool KQ, bool KH, int VB, bool VQ>
+__device__ __forceinline__ void read_tile(TileData<KB, KQ, KH, VB, VQ>& d, const unsigned char* st, int t0,
+                                          int last, int lg, int lt, int lane) {
+  using S = Slots<KB, KQ, KH, VB, VQ>;
+  auto r16 = [&](int i) { return *reinterpret_cast<const uint4*>(st + (32 * i + lane) * 16); };
+  auto r8 = [&](int i) { return *reinterpret_cast<const uint2*>(st + S::off8 + (32 * i + lane) * 8); };
+  auto r4 = [&](int i) { return *reinterpret_cast<const uint32_t*>(st + S::off4 + (32 * i + lane) * 4); };
+  const int tA = min(t0 + tile_row_token(lg), last);
+  const int tB = min(t0 + tile_row_token(lg + 8), last);
+  if constexpr (KB == 4) {
+    d.kA.c = r16(0);
+    d.kB.c = r16(1);
+  } else if constexpr (KB == 3 || KB == 2) {
+    d.kA.k = r8(S::K8);
+    d.kB.k = r8(S::K8 + 1);
+    if constexpr (KB == 3) {
+      d.kA.s = r4(S::KS4);
+      d.kB.s = r4(S::KS4 + 1);
+    }
+  } else {
+    d.kA.s = r4(S::KS4);
+    d.kB.s = r4(S::KS4 + 1);
+  }
+  d.nuKA = __uint_as_float(r4(S::NK4));
+  d.nuKB = __uint_as_float(r4(S::NK4 + 1));
+  if constexpr (KQ) {
+    d.sA.s = r4(S::Q4);
+    d.sB.s = r4(S::Q4 + 1);
+    d.rhoKA = half_of(r4(S::Q4 + 2), tA & 1);
+    d.rhoKB = half_of(r4(S::Q4 + 3), tB & 1);
+  }
+  if constexpr (KH) {
+    const uint2 za = r8(S::Z8), zb = r8(S::Z8 + 1);
+    d.zA = make_uint2((za.x >> (8 * lt)) & 0xffu, (za.y >> (8 * lt)) & 0xffu);
+    d.zB = make_uint2((zb.x >> (8 * lt)) & 0xffu, (zb.y >> (8 * lt)) & 0xffu);
+    d.zsA = half_of(r4(S::H4), tA & 1);
+    d.zsB = half_of(r4(S::H4 + 1), tB & 1);
+  }
+  const int hs = lg & 1;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if constexpr (VB == 4) {
+      d.v.w[j] = r8(S::V8 + j);
+    } else if constexpr (VB == 3) {
+      d.v.k[j] = r4(S::V4 + j);
+      d.v.s[j] = hs ? r4(S::V4 + 4 + j) >> 16 : r4(S::V4 + 4 + j) & 0xffffu;
+    } else if constexpr (VB == 2) {
+      d.v.k[j] = r4(S::V4 + j);
+    } else {
+      d.v.s[j] = hs ? r4(S::V4 + j) >> 16 : r4(S::V4 + j) & 0xffffu;
+    }
+    if constexpr (VQ) d.vs.s[j] = hs ? r4(S::VQ4 + j) >> 16 : r4(S::VQ4 + j) & 0xffffu;
+  }
+  d.nuVA = __uint_as_float(r4(S::NV4));
+  d.nuVB = __uint_as_float(r4(S::NV4 + 1));
+  if constexpr (VQ) {
+    d.rhoVA = half_of(r4(S::VQ4 + 4), tA & 1);
+    d.rhoVB = half_of(r4(S::VQ4 + 5), tB & 1);
+  }
+}
+
+// Direct (uncached) loads of a tile's key data, used by the logits kernel.
+template <int KB, bool KQ, bool KH, int VB, bool VQ>
+__device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, const SlabPtrs& s, int t0,
+                                           int last, int lg, int lt) {
+  constexpr int KR = KRec<KB>::value;
+  const int tA = min(t0 + tile_row_token(lg), last);
+  const int tB = min(t0 + tile_row_token(lg + 8), last);
+  if constexpr (KB == 4) {
+    d.kA.c = ldg_stream16(s.kc + tA * KR + 16 * lt);
+    d.kB.c = ldg_stream16(s.kc + tB * KR + 16 * lt);
+  } else if constexpr (KB == 3 || KB == 2) {
+    d.kA.k = ldg_stream8(s.kc + tA * KR + 8 * lt);
+    d.kB.k = ldg_stream8(s.kc + tB * KR + 8 * lt);
+    if constexpr (KB == 3) {
+      d.kA.s = ldg_stream4(s.kc + tA * KR + kDecD / 4 + 4 * lt);
+      d.kB.s = ldg_stream4(s.kc + tB * KR + kDecD / 4 + 4 * lt);
+    }
+  } else {
+    d.kA.s = ldg_stream4(s.kc + tA * KR + 4 * lt);
+    d.kB.s = ldg_stream4(s.kc + tB * KR + 4 * lt);
+  }
+  d.nuKA = __uint_as_float(ldg_stream4(s.kn + tA * 4));
+  d.nuKB = __uint_as_float(ldg_stream4(s.kn + tB * 4));
+  if constexpr (KQ) {
+    d.sA.s = ldg_stream4(s.ks + tA * (kDecD / 8) + 4 * lt);
+    d.sB.s = ldg_stream4(s.ks + tB * (kDecD / 8) + 4 * lt);
+    d.rhoKA = half_of(ldg_stream4(s.kr + (tA & ~1) * 2), tA & 1);
+    d.rhoKB = half_of(ldg_stream4(s.kr + (tB & ~1) * 2), tB & 1);
+  }
+  if constexpr (KH) {
+    const uint2 za = ldg_stream8(s.kz + tA * 8), zb = ldg_stream8(s.kz + tB * 8);
+    d.zA = make_uint2((za.x >> (8 * lt)) & 0xffu, (za.y >> (8 * lt)) & 0xffu);
+    d.zB = make_uint2((zb.x >> (8 * lt)) & 0xffu, (zb.y >> (8 * lt)) & 0xffu);
+    d.zsA = half_of(ldg_stream4(s.kzs + (tA & ~1) * 2), tA & 1);
+    d.zsB = half_of(ldg_stream4(s.kzs + (tB & ~1) * 2), tB & 1);
   }
 }
 
@@ -325,15 +540,15 @@ __device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, cons
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, float (&s)[4],
                                            const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                           const uint32_t (&qu)[2], const uint32_t* lutK,
-                                           uint32_t k_m0, float qjl_scale) {
+                                           const uint32_t (&qu)[2], const unsigned char* lutK,
+                                           uint32_t lane4, uint32_t k_m0, float qjl_scale) {
   d.kA.prepare();
   d.kB.prepare();
   float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    mma16816(sc, d.kA.pair(lutK, k_m0, 2 * ks), d.kB.pair(lutK, k_m0, 2 * ks),
-             d.kA.pair(lutK, k_m0, 2 * ks + 1), d.kB.pair(lutK, k_m0, 2 * ks + 1), qf[2 * ks],
+    mma16816(sc, d.kA.pair(lutK, lane4, k_m0, 2 * ks), d.kB.pair(lutK, lane4, k_m0, 2 * ks),
+             d.kA.pair(lutK, lane4, k_m0, 2 * ks + 1), d.kB.pair(lutK, lane4, k_m0, 2 * ks + 1), qf[2 * ks],
              qf[2 * ks + 1]);
   }
   s[0] = sc[0] * d.nuKA;
@@ -365,29 +580,6 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
   }
 }
 
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void load_tile(TileData<KB, KQ, KH, VB, VQ>& d, const DecodeParams& p,
-                                          int b, int kvh, int t0, int last, int lg, int lt) {
-  const Cache& C = p.cache;
-  load_ktile(d, C, b, kvh, t0, last, lg, lt);
-  const int tA = min(t0 + tile_row_token(lg), last);
-  const int tB = min(t0 + tile_row_token(lg + 8), last);
-  const unsigned char* vrec[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) vrec[j] = C.ptr(tqi::R_V_CODES, b, kvh, min(t0 + 4 * lt + j, last));
-  d.v.load(vrec, lg);
-  d.nuVA = ld_f32(C.ptr(tqi::R_V_NORM, b, kvh, tA));
-  d.nuVB = ld_f32(C.ptr(tqi::R_V_NORM, b, kvh, tB));
-  if constexpr (VQ) {
-    const unsigned char* srec[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) srec[j] = C.ptr(tqi::R_V_SIGNS, b, kvh, min(t0 + 4 * lt + j, last));
-    d.vs.load(srec, lg);
-    d.rhoVA = ld_f16(C.ptr(tqi::R_V_RHO, b, kvh, tA));
-    d.rhoVB = ld_f16(C.ptr(tqi::R_V_RHO, b, kvh, tB));
-  }
-}
-
 // Per-warp running state.
 template <bool VQ>
 struct WarpState {
@@ -395,17 +587,27 @@ struct WarpState {
   float l0, l1;  // this thread's partial softmax denominators
   float acc[8][4];
   float accs[VQ ? 8 : 1][4];
+  __device__ __forceinline__ void reset() {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[mt][j] = 0.f;
+        if constexpr (VQ) accs[mt][j] = 0.f;
+      }
+  }
 };
 
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void compute_tile(TileData<KB, KQ, KH, VB, VQ>& d, WarpState<VQ>& st,
                                              const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                             const uint32_t (&qu)[2], const uint32_t* lutK,
-                                             const uint32_t* lutV, uint32_t k_m0, uint32_t v_m0,
-                                             const DecodeParams& p, int t0, int end, int lg) {
-  // ---- scores
+                                             const uint32_t (&qu)[2], const unsigned char* lutK,
+                                             const unsigned char* lutV, uint32_t lane4, uint32_t k_m0,
+                                             uint32_t v_m0, const DecodeParams& p, int t0, int end, int lg) {
   float s[4];
-  key_scores(d, s, qf, qs, qu, lutK, k_m0, p.qjl_scale);
+  key_scores(d, s, qf, qs, qu, lutK, lane4, k_m0, p.qjl_scale);
   const bool va = t0 + tile_row_token(lg) < end;
   const bool vb = t0 + tile_row_token(lg + 8) < end;
   s[0] = va ? s[0] * p.score_scale : -INFINITY;
@@ -447,7 +649,7 @@ __device__ __forceinline__ void compute_tile(TileData<KB, KQ, KH, VB, VQ>& d, Wa
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     uint32_t a[4];
-    d.v.frag(lutV, v_m0, mt, a);
+    d.v.frag(lutV, lane4, v_m0, mt, a);
     mma16816(st.acc[mt], a[0], a[1], a[2], a[3], bv0, bv1);
   }
   if constexpr (VQ) {
@@ -458,223 +660,258 @@ __device__ __forceinline__ void compute_tile(TileData<KB, KQ, KH, VB, VQ>& d, Wa
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t a[4];
-      d.vs.frag(0x3C003C00u, mt, a);
+      d.vs.frag(mt, a);
       mma16816(st.accs[mt], a[0], a[1], a[2], a[3], bs0, bs1);
     }
   }
 }
 
-template <int KB, int VB, bool VQ>
+template <int KB, bool KQ, bool KH, int VB, bool VQ>
 struct DecodeSmem {
-  static constexpr int lutK = LutEntries<KB>::value * 32;
-  static constexpr int lutV = LutEntries<VB>::value * 32;
-  // partial record per head: m, l, 2 pad words, acc[D], (acc_sk[m])
-  static constexpr int PS = 4 + kDecD + (VQ ? kDecD : 0);
-  static constexpr int merge = kDecWarps * kHeadsPad * PS;
-  static constexpr int words = (lutK + lutV) > merge ? (lutK + lutV) : merge;
-  static constexpr int bytes = words * 4 + 64;
+  static constexpr int lutK = LutEntries<KB>::value * kLutStride;
+  static constexpr int lutV = KB == VB ? 0 : LutEntries<VB>::value * kLutStride;  // same codebook
+  static constexpr int PS = 4 + kDecD + (VQ ? kDecD : 0);  // per head: m, l, pad, pad, acc, (acc_sk)
+  static constexpr int merge = kDecWarps * kHeadsPad * PS * 4;
+  static constexpr int stages = kDecWarps * kStages * Slots<KB, KQ, KH, VB, VQ>::bytes;
+  static constexpr int work = stages > merge ? stages : merge;
+  static constexpr int bytes = lutK + lutV + work;
 };
+
+// Owner block of flattened position x: the largest c with floor(c W / N) <= x.
+__device__ __forceinline__ int owner_block(long long x, long long W, int N) {
+  return (int)(((x + 1) * N - 1) / W);
+}
 
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeParams p) {
-  using SM = DecodeSmem<KB, VB, VQ>;
+  using SM = DecodeSmem<KB, KQ, KH, VB, VQ>;
+  using SL = Slots<KB, KQ, KH, VB, VQ>;
   constexpr int PS = SM::PS;
-  extern __shared__ __align__(16) uint32_t smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane >> 2, lt = lane & 3;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const uint32_t lane4 = 4u * lane;
 
-  uint32_t* lutK = smem;
-  uint32_t* lutV = smem + SM::lutK;
+  unsigned char* lutK = smem;
+  unsigned char* lutV = KB == VB ? smem : smem + SM::lutK;
+  unsigned char* work = smem + SM::lutK + SM::lutV;
   if constexpr (KB != 1) build_lut<KB>(lutK, p.tab.k_c);
-  if constexpr (VB != 1) build_lut<VB>(lutV, p.tab.v_c);
+  if constexpr (VB != 1 && VB != KB) build_lut<VB>(lutV, p.tab.v_c);
   const uint32_t k_m0 = pack_half2(__ldg(p.tab.k_c + 1), __ldg(p.tab.k_c + 1));
   const uint32_t v_m0 = pack_half2(__ldg(p.tab.v_c + 1), __ldg(p.tab.v_c + 1));
   __syncthreads();
 
-  // query fragments: head kvh * G + lg, dims [32 lt, 32 lt + 32)
+  unsigned char* my_stages = work + warp * kStages * SL::bytes;
+  const uint32_t my_stages_s = (uint32_t)__cvta_generic_to_shared(my_stages);
   const int G = p.G;
   const int Hq = p.Hkv * G;
-  const bool hv = lg < G;
-  const long long qrow = (long long)b * Hq + kvh * G + (hv ? lg : 0);
-  uint32_t qf[16], qs[16], qu[2];
-#pragma unroll
-  for (int i = 0; i < 16; i += 4) {
-    const uint4 v = hv ? *reinterpret_cast<const uint4*>(p.q_rot + qrow * (kDecD / 2) + 16 * lt + i)
-                       : make_uint4(0, 0, 0, 0);
-    qf[i] = v.x; qf[i + 1] = v.y; qf[i + 2] = v.z; qf[i + 3] = v.w;
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) qs[i] = 0;
-  if constexpr (KQ) {
+  const int N = p.nblocks;
+  long long x = (long long)blockIdx.x * p.W / N;
+  const long long x_end = (long long)(blockIdx.x + 1) * p.W / N;
+
+  while (x < x_end) {
+    // ---- locate the slab segment that starts at x
+    int lo = 0, hi = p.B - 1;  // largest b with batch_start[b] <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.batch_start[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int L = p.seq_len[b];
+    const long long off = x - p.batch_start[b];
+    const int kvh = (int)(off / L);
+    const int ts = (int)(off % L);
+    const long long slab_start = p.batch_start[b] + (long long)kvh * L;
+    const long long seg_end = min(x_end, slab_start + L);
+    const int te = ts + (int)(seg_end - x);
+    const int pair = b * p.Hkv + kvh;
+
+    // ---- query fragments: head kvh * G + lg, dims [32 lt, 32 lt + 32)
+    const bool hv = lg < G;
+    const long long qrow = (long long)b * Hq + kvh * G + (hv ? lg : 0);
+    uint32_t qf[16], qs[16], qu[2];
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
-      const uint4 v = hv ? *reinterpret_cast<const uint4*>(p.q_sk + qrow * (kDecD / 2) + 16 * lt + i)
+      const uint4 v = hv ? *reinterpret_cast<const uint4*>(p.q_rot + qrow * (kDecD / 2) + 16 * lt + i)
                          : make_uint4(0, 0, 0, 0);
-      qs[i] = v.x; qs[i + 1] = v.y; qs[i + 2] = v.z; qs[i + 3] = v.w;
+      qf[i] = v.x; qf[i + 1] = v.y; qf[i + 2] = v.z; qf[i + 3] = v.w;
     }
-  }
-  qu[0] = qu[1] = 0;
-  if constexpr (KH) {
-    if (hv) {
-      qu[0] = p.q_u[qrow * 8 + lt];
-      qu[1] = p.q_u[qrow * 8 + lt + 4];
-    }
-  }
-
-  // this warp's token range
-  const int T = p.seq_len[b];
-  const int c0 = split * p.chunk;
-  const int c1 = min(T, c0 + p.chunk);
-  const int n = max(0, c1 - c0);
-  const int per = ((n + kDecWarps - 1) / kDecWarps + kTile - 1) / kTile * kTile;
-  const int w0 = c0 + warp * per;
-  const int w1 = min(c1, w0 + per);
-
-  WarpState<VQ> st;
-  st.m0 = st.m1 = -INFINITY;
-  st.l0 = st.l1 = 0.f;
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
+    for (int i = 0; i < 16; ++i) qs[i] = 0;
+    if constexpr (KQ) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      st.acc[mt][j] = 0.f;
-      if constexpr (VQ) st.accs[mt][j] = 0.f;
-    }
-
-  if (w0 < w1) {
-    const int last = w1 - 1;
-    TileData<KB, KQ, KH, VB, VQ> cur, nxt;
-    load_tile(cur, p, b, kvh, w0, last, lg, lt);
-    for (int t0 = w0; t0 < w1; t0 += kTile) {
-      const bool more = t0 + kTile < w1;
-      if (more) load_tile(nxt, p, b, kvh, t0 + kTile, last, lg, lt);
-      compute_tile(cur, st, qf, qs, qu, lutK + lane, lutV + lane, k_m0, v_m0, p, t0, w1, lg);
-      if (more) cur = nxt;
-    }
-  }
-
-  // ---- merge the warps of this block
-  float l0 = st.l0, l1 = st.l1;
-#pragma unroll
-  for (int m = 4; m <= 16; m <<= 1) {
-    l0 += __shfl_xor_sync(kFull, l0, m);
-    l1 += __shfl_xor_sync(kFull, l1, m);
-  }
-  __syncthreads();  // tables no longer needed: reuse shared memory for the merge
-  float* mb = reinterpret_cast<float*>(smem) + warp * kHeadsPad * PS;
-  if (lg == 0) {
-    mb[(2 * lt) * PS + 0] = st.m0;
-    mb[(2 * lt) * PS + 1] = l0;
-    mb[(2 * lt + 1) * PS + 0] = st.m1;
-    mb[(2 * lt + 1) * PS + 1] = l1;
-  }
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = 16 * lg + 2 * mt;
-    mb[(2 * lt) * PS + 4 + d0] = st.acc[mt][0];
-    mb[(2 * lt + 1) * PS + 4 + d0] = st.acc[mt][1];
-    mb[(2 * lt) * PS + 4 + d0 + 1] = st.acc[mt][2];
-    mb[(2 * lt + 1) * PS + 4 + d0 + 1] = st.acc[mt][3];
-    if constexpr (VQ) {
-      mb[(2 * lt) * PS + 4 + kDecD + d0] = st.accs[mt][0];
-      mb[(2 * lt + 1) * PS + 4 + kDecD + d0] = st.accs[mt][1];
-      mb[(2 * lt) * PS + 4 + kDecD + d0 + 1] = st.accs[mt][2];
-      mb[(2 * lt + 1) * PS + 4 + kDecD + d0 + 1] = st.accs[mt][3];
-    }
-  }
-  __syncthreads();
-  const float* all = reinterpret_cast<const float*>(smem);
-  float* part_out = p.part + ((((long long)b * p.Hkv + kvh) * p.splits + split) * kHeadsPad) * PS;
-  for (int idx = threadIdx.x; idx < G * PS; idx += blockDim.x) {
-    const int h = idx / PS, e = idx % PS;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, all[(w * kHeadsPad + h) * PS]);
-    float v;
-    if (e == 0) {
-      v = M;
-    } else if (e == 2 || e == 3) {
-      v = 0.f;
-    } else {
-      v = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) {
-          const float mw = all[(w * kHeadsPad + h) * PS];
-          v = fmaf(exp2f(mw - M), all[(w * kHeadsPad + h) * PS + e], v);
-        }
+      for (int i = 0; i < 16; i += 4) {
+        const uint4 v = hv ? *reinterpret_cast<const uint4*>(p.q_sk + qrow * (kDecD / 2) + 16 * lt + i)
+                           : make_uint4(0, 0, 0, 0);
+        qs[i] = v.x; qs[i + 1] = v.y; qs[i + 2] = v.z; qs[i + 3] = v.w;
       }
     }
-    part_out[h * PS + e] = v;
-  }
+    qu[0] = qu[1] = 0;
+    if constexpr (KH) {
+      if (hv) {
+        qu[0] = p.q_u[qrow * 8 + lt];
+        qu[1] = p.q_u[qrow * 8 + lt + 4];
+      }
+    }
 
-  // ---- the last block of this (batch, KV head) merges all splits
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(p.tickets + b * p.Hkv + kvh, 1);
-    s_last = prev == p.splits - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (warp < G) {
-    const int h = warp;
-    const float* base = p.part + (((long long)b * p.Hkv + kvh) * p.splits * kHeadsPad + h) * PS;
-    const long long sstride = (long long)kHeadsPad * PS;
-    float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(base + s * sstride));
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accs = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-      for (int s = 0; s < p.splits; ++s) {
-        const float* ps = base + s * sstride;
-        const float w = exp2f(__ldcg(ps) - M);
-        L = fmaf(w, __ldcg(ps + 1), L);
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(ps + 4 + 4 * lane));
-        acc.x = fmaf(w, a.x, acc.x); acc.y = fmaf(w, a.y, acc.y);
-        acc.z = fmaf(w, a.z, acc.z); acc.w = fmaf(w, a.w, acc.w);
+    // ---- this warp's sub-range, streamed through the cp.async ring
+    const int n = te - ts;
+    const int per = ((n + kDecWarps - 1) / kDecWarps + kTile - 1) / kTile * kTile;
+    const int w0 = min(te, ts + warp * per);
+    const int w1 = min(te, w0 + per);
+    const int nt = (w1 - w0 + kTile - 1) / kTile;
+    SlabPtrs sp;
+    sp.init(p.cache, b, kvh);
+    WarpState<VQ> st;
+    st.reset();
+    const int last = max(w1 - 1, 0);
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) {
+      if (i < nt) issue_tile<KB, KQ, KH, VB, VQ>(my_stages_s + i * SL::bytes, sp, w0 + i * kTile, last, lg, lt, lane);
+      cp_commit();
+    }
+    for (int i = 0; i < nt; ++i) {
+      const int nx = i + kStages - 1;
+      if (nx < nt)
+        issue_tile<KB, KQ, KH, VB, VQ>(my_stages_s + (nx % kStages) * SL::bytes, sp, w0 + nx * kTile, last, lg,
+                                       lt, lane);
+      cp_commit();
+      cp_wait<kStages - 1>();
+      TileData<KB, KQ, KH, VB, VQ> d;
+      const int t0 = w0 + i * kTile;
+      read_tile(d, my_stages + (i % kStages) * SL::bytes, t0, last, lg, lt, lane);
+      compute_tile(d, st, qf, qs, qu, lutK, lutV, lane4, k_m0, v_m0, p, t0, w1, lg);
+    }
+    cp_wait<0>();
+
+    // ---- merge the warps of this block for this segment
+    float l0 = st.l0, l1 = st.l1;
+#pragma unroll
+    for (int m = 4; m <= 16; m <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, m);
+      l1 += __shfl_xor_sync(kFull, l1, m);
+    }
+    __syncthreads();  // every warp is done with its slots: reuse them for the merge
+    float* mb = reinterpret_cast<float*>(work) + warp * kHeadsPad * PS;
+    if (lg == 0) {
+      mb[(2 * lt) * PS + 0] = st.m0;
+      mb[(2 * lt) * PS + 1] = l0;
+      mb[(2 * lt + 1) * PS + 0] = st.m1;
+      mb[(2 * lt + 1) * PS + 1] = l1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = 16 * lg + 2 * mt;
+      mb[(2 * lt) * PS + 4 + d0] = st.acc[mt][0];
+      mb[(2 * lt + 1) * PS + 4 + d0] = st.acc[mt][1];
+      mb[(2 * lt) * PS + 4 + d0 + 1] = st.acc[mt][2];
+      mb[(2 * lt + 1) * PS + 4 + d0 + 1] = st.acc[mt][3];
+      if constexpr (VQ) {
+        mb[(2 * lt) * PS + 4 + kDecD + d0] = st.accs[mt][0];
+        mb[(2 * lt + 1) * PS + 4 + kDecD + d0] = st.accs[mt][1];
+        mb[(2 * lt) * PS + 4 + kDecD + d0 + 1] = st.accs[mt][2];
+        mb[(2 * lt + 1) * PS + 4 + kDecD + d0 + 1] = st.accs[mt][3];
+      }
+    }
+    __syncthreads();
+    const float* all = reinterpret_cast<const float*>(work);
+    float* part_out = p.part + ((long long)(pair + blockIdx.x) * kHeadsPad) * PS;
+    for (int idx = threadIdx.x; idx < G * PS; idx += blockDim.x) {
+      const int h = idx / PS, e = idx % PS;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, all[(w * kHeadsPad + h) * PS]);
+      float v;
+      if (e == 0) {
+        v = M;
+      } else if (e == 2 || e == 3) {
+        v = 0.f;
+      } else {
+        v = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kDecWarps; ++w) {
+            const float mw = all[(w * kHeadsPad + h) * PS];
+            v = fmaf(exp2f(mw - M), all[(w * kHeadsPad + h) * PS + e], v);
+          }
+        }
+      }
+      part_out[h * PS + e] = v;
+    }
+
+    // ---- the last block of this slab merges all its partials
+    const int c_first = owner_block(slab_start, p.W, N);
+    const int c_last = owner_block(slab_start + L - 1, p.W, N);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int prev = atomicAdd(p.tickets + pair, 1);
+      s_last = prev == c_last - c_first;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      if (warp < G) {
+        const int h = warp;
+        const long long sstride = (long long)kHeadsPad * PS;
+        const float* base = p.part + (long long)(pair + c_first) * sstride + h * PS;
+        const int ns = c_last - c_first + 1;
+        float M = -INFINITY;
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride));
+        float L2 = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accs = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+          for (int s = 0; s < ns; ++s) {
+            const float* ps = base + s * sstride;
+            const float w = exp2f(__ldcg(ps) - M);
+            L2 = fmaf(w, __ldcg(ps + 1), L2);
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(ps + 4 + 4 * lane));
+            acc.x = fmaf(w, a.x, acc.x); acc.y = fmaf(w, a.y, acc.y);
+            acc.z = fmaf(w, a.z, acc.z); acc.w = fmaf(w, a.w, acc.w);
+            if constexpr (VQ) {
+              const float4 c = __ldcg(reinterpret_cast<const float4*>(ps + 4 + kDecD + 4 * lane));
+              accs.x = fmaf(w, c.x, accs.x); accs.y = fmaf(w, c.y, accs.y);
+              accs.z = fmaf(w, c.z, accs.z); accs.w = fmaf(w, c.w, accs.w);
+            }
+          }
+        }
+        float o[4] = {acc.x, acc.y, acc.z, acc.w};
         if constexpr (VQ) {
-          const float4 c = __ldcg(reinterpret_cast<const float4*>(ps + 4 + kDecD + 4 * lane));
-          accs.x = fmaf(w, c.x, accs.x); accs.y = fmaf(w, c.y, accs.y);
-          accs.z = fmaf(w, c.z, accs.z); accs.w = fmaf(w, c.w, accs.w);
+          // o_rot += sqrt(pi/2)/m * S_V^T acc_sk
+          const float sv[4] = {accs.x, accs.y, accs.z, accs.w};
+          float corr[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int r4 = 0; r4 < 32; ++r4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float ar = __shfl_sync(kFull, sv[i], r4);
+              const float4 srow =
+                  __ldg(reinterpret_cast<const float4*>(p.tab.S_V + (4 * r4 + i) * kDecD + 4 * lane));
+              corr[0] = fmaf(srow.x, ar, corr[0]); corr[1] = fmaf(srow.y, ar, corr[1]);
+              corr[2] = fmaf(srow.z, ar, corr[2]); corr[3] = fmaf(srow.w, ar, corr[3]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = fmaf(p.qjl_scale, corr[i], o[i]);
         }
-      }
-    }
-    float o[4] = {acc.x, acc.y, acc.z, acc.w};
-    if constexpr (VQ) {
-      // o_rot += sqrt(pi/2)/m * S_V^T acc_sk
-      const float sv[4] = {accs.x, accs.y, accs.z, accs.w};
-      float corr[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int r4 = 0; r4 < 32; ++r4) {
+        const float invL = L2 > 0.f ? 1.f / L2 : 0.f;
+        if (p.v_rotate) {
+          wht_warp<4>(o);
+          const float rs = 1.f / sqrtf((float)kDecD);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float ar = __shfl_sync(kFull, sv[i], r4);
-          const float4 srow =
-              __ldg(reinterpret_cast<const float4*>(p.tab.S_V + (4 * r4 + i) * kDecD + 4 * lane));
-          corr[0] = fmaf(srow.x, ar, corr[0]); corr[1] = fmaf(srow.y, ar, corr[1]);
-          corr[2] = fmaf(srow.z, ar, corr[2]); corr[3] = fmaf(srow.w, ar, corr[3]);
+          for (int i = 0; i < 4; ++i) o[i] = o[i] * rs * __ldg(p.tab.v_sign + 4 * lane + i) * invL;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] *= invL;
         }
+        float* dst = p.out + ((long long)b * Hq + kvh * G + h) * kDecD + 4 * lane;
+        *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = fmaf(p.qjl_scale, corr[i], o[i]);
+      if (threadIdx.x == 0) p.tickets[pair] = 0;
     }
-    const float invL = L > 0.f ? 1.f / L : 0.f;
-    if (p.v_rotate) {
-      wht_warp<4>(o);
-      const float rs = 1.f / sqrtf((float)kDecD);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = o[i] * rs * __ldg(p.tab.v_sign + 4 * lane + i) * invL;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] *= invL;
-    }
-    float* dst = p.out + ((long long)b * Hq + kvh * G + h) * kDecD + 4 * lane;
-    *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+    __syncthreads();  // the merge area becomes the next segment's slots
+    x = seg_end;
   }
-  if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -691,23 +928,23 @@ struct LogitsParams {
 
 template <int KB>
 struct LogitsSmem {
-  static constexpr int lut = LutEntries<KB>::value * 32;
-  static constexpr int words = lut + kHeadsPad * (kDecD / 2) * 2 + kHeadsPad * 8;
-  static constexpr int bytes = words * 4;
+  static constexpr int lut = LutEntries<KB>::value * kLutStride;
+  static constexpr int bytes = lut + (kHeadsPad * (kDecD / 2) * 2 + kHeadsPad * 8) * 4;
 };
 
 template <int KB, bool KQ, bool KH>
 __global__ void __launch_bounds__(kDecWarps * 32) logits_kernel(const LogitsParams p) {
-  extern __shared__ __align__(16) uint32_t smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane >> 2, lt = lane & 3;
+  const uint32_t lane4 = 4u * lane;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int T = p.seq_len[b];
   const int c0 = blockIdx.x * p.tokens_per_block;
   if (c0 >= T) return;  // the whole block leaves together
   const int G = p.G, Hq = p.Hkv * G;
-  uint32_t* lutK = smem;
-  uint32_t* qrot = smem + LogitsSmem<KB>::lut;
+  unsigned char* lutK = smem;
+  uint32_t* qrot = reinterpret_cast<uint32_t*>(smem + LogitsSmem<KB>::lut);
   uint32_t* qsk = qrot + kHeadsPad * (kDecD / 2);
   uint32_t* qus = qsk + kHeadsPad * (kDecD / 2);
   if constexpr (KB != 1) build_lut<KB>(lutK, p.tab.k_c);
@@ -751,13 +988,9 @@ __global__ void __launch_bounds__(kDecWarps * 32) logits_kernel(const LogitsPara
       }
 #pragma unroll
       for (int k = 0; k < 16; ++k) z[k] = warp_sum(z[k]);
-      if (lane < 8) {
-        float lo = 0.f, hi = 0.f;
+      if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k == lane) { lo = z[2 * k]; hi = z[2 * k + 1]; }
-        }
-        qus[warp * 8 + lane] = pack_half2(lo, hi);
+        for (int k = 0; k < 8; ++k) qus[warp * 8 + k] = pack_half2(z[2 * k], z[2 * k + 1]);
       }
     }
   }
@@ -776,11 +1009,13 @@ __global__ void __launch_bounds__(kDecWarps * 32) logits_kernel(const LogitsPara
   const int per = ((c1 - c0 + kDecWarps - 1) / kDecWarps + kTile - 1) / kTile * kTile;
   const int w0 = c0 + warp * per;
   const int w1 = min(c1, w0 + per);
+  SlabPtrs sp;
+  sp.init(p.cache, b, kvh);
   for (int t0 = w0; t0 < w1; t0 += kTile) {
     TileData<KB, KQ, KH, 1, false> d;
-    load_ktile(d, p.cache, b, kvh, t0, w1 - 1, lg, lt);
+    load_ktile(d, sp, t0, w1 - 1, lg, lt);
     float s[4];
-    key_scores(d, s, qf, qs, qu, lutK + lane, k_m0, p.qjl_scale);
+    key_scores(d, s, qf, qs, qu, lutK, lane4, k_m0, p.qjl_scale);
     const int tA = t0 + tile_row_token(lg), tB = t0 + tile_row_token(lg + 8);
     const long long r0 = ((long long)b * Hq + kvh * G + 2 * lt) * p.stride;
     const long long r1 = r0 + p.stride;
@@ -798,7 +1033,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) logits_kernel(const LogitsPara
 // Launch helpers used by the per-bit-width instantiation units.
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
-  using SM = DecodeSmem<KB, VB, VQ>;
+  using SM = DecodeSmem<KB, KQ, KH, VB, VQ>;
+  static_assert(SM::bytes <= 227 * 1024, "decode shared memory exceeds the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<KB, KQ, KH, VB, VQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM::bytes);
   if (e != cudaSuccess) return e;
@@ -829,12 +1065,12 @@ bool dispatch_logits_k4(int kq, int kh, const LogitsParams& p, dim3 g, cudaStrea
 
 #define TQ_DECODE_CASE(KB_, KQ_, KH_, VB_, VQ_)                                           \
   if (kq == KQ_ && kh == KH_ && vb == VB_ && vq == VQ_) {                                 \
-    *e = launch_decode_t<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0>(p, g, s);                \
+    if (e) *e = launch_decode_t<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0>(p, g, s);         \
     return true;                                                                          \
   }
 #define TQ_LOGITS_CASE(KB_, KQ_, KH_)                                                     \
   if (kq == KQ_ && kh == KH_) {                                                           \
-    *e = launch_logits_t<KB_, KQ_ != 0, KH_ != 0>(p, g, s);                               \
+    if (e) *e = launch_logits_t<KB_, KQ_ != 0, KH_ != 0>(p, g, s);                        \
     return true;                                                                          \
   }
 
