@@ -85,28 +85,35 @@ typedef struct {
 } tq_config;
 
 #define TQ_MAX_BATCH 512
-#define TQ_LAYOUT_VERSION 1u
+#define TQ_LAYOUT_VERSION 2u
+#define TQ_TILE_TOKENS 16
 
-/* One region of the cache buffer: [B][H_kv][capacity][record_bytes], record of token t of
- * (b, h) at offset + ((b * H_kv + h) * capacity + t) * record_bytes.  record_bytes = 0 when
- * the region is absent. */
+/* One field of a side's 16-token block: `offset` within the block, `record_bytes` per token
+ * (0 when the field is absent).  Token j of the block has its record at offset +
+ * j * record_bytes. */
 typedef struct {
   uint64_t offset;
   uint64_t record_bytes;
 } tq_region;
 
-/* The packed cache layout (version TQ_LAYOUT_VERSION).  Regions start on 256-byte boundaries,
- * in the order of the fields below.  Codes are stored in sign-magnitude form
- * (s = [c >= 2^(b-1)], k = magnitude rank) as streams of power-of-two widths, coordinate i of
- * a w-bit stream in bits [w*i, w*i + w), least significant bit first:
+/* The packed cache layout (version TQ_LAYOUT_VERSION).  The buffer holds two arrays of
+ * 16-token blocks, K at k_offset and V at v_offset (256-byte aligned), each
+ * [B][H_kv][capacity / 16] blocks of k_block_bytes / v_block_bytes.  Token t of (b, h) lives in
+ * block (b * H_kv + h) * capacity / 16 + t / 16 at position t % 16.  A K block holds, one after
+ * another, 16 records of each present field: codes, norm, [signs, rho], [side, side_scale]; a V
+ * block: codes, norm, [signs, rho].  So one contiguous copy brings all of a tile's data of a side.
+ * Codes are stored in sign-magnitude form (s = [c >= 2^(b-1)], k = magnitude rank) as streams of
+ * power-of-two widths, coordinate i of a w-bit stream in bits [w*i, w*i + w), least significant
+ * bit first:
  *   b = 4: (s << 3) | k;  b = 3: 2-bit stream of k then 1-bit stream of s;
  *   b = 2: (s << 1) | k;  b = 1: s.
  * QJL signs: bit i = 1 iff (S r)_i >= 0.  HeadQ side code: 4-bit two's complement, zeta_0 in
  * the low nibble.  Norms are fp32; rho and side scales fp16. */
 typedef struct {
   uint32_t layout_version;
-  uint32_t reserved;
+  uint32_t tile_tokens;
   uint64_t total_bytes;
+  uint64_t k_offset, k_block_bytes, v_offset, v_block_bytes;
   tq_region k_codes, k_norm, k_signs, k_rho, k_side, k_side_scale;
   tq_region v_codes, v_norm, v_signs, v_rho;
 } tq_cache_layout;

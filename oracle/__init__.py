@@ -26,7 +26,7 @@ Modules:
 * ``rotation``  explicit Sylvester Hadamard matrix and R = H D / sqrt(d).
 * ``codec``     per-vector encoder (norm split, rotation, scalar code, QJL
   residual sketch, HeadQ side code) and the matching reconstruction.
-* ``layout``    the packed cache layout (byte streams, regions) and its parser.
+* ``layout``    the packed cache layout (byte streams, 16-token blocks) and its parser.
 * ``attention`` textbook softmax decode attention with grouped query heads.
 * ``headq``     calibration basis by PCA and the corrected logits.
 

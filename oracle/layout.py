@@ -1,4 +1,4 @@
-"""Packed cache layout: byte streams, record sizes, regions (the storage contract).
+"""Packed cache layout: byte streams, record sizes, 16-token blocks (the storage contract).
 
 [HEADQ] "Visão Geral do Algoritmo" 2 says only what the cache stores (the base
 key and the side code); no page fixes a bit layout.  The layout below is the
@@ -17,19 +17,23 @@ produce and parse cache buffers byte for byte:
   b = 1: one 1-bit stream of s.
 * QJL signs: a 1-bit stream over the m sketch rows, bit = 1 iff (S r)_i >= 0.
 * HeadQ side code: r 4-bit two's-complement nibbles, zeta_0 in the low nibble.
-* The cache is one buffer of regions, each starting on a 256-byte boundary,
-  in this order (bracketed ones only when present):
-  k_codes, k_norm (fp32), [k_signs, k_rho (fp16)], [k_side, k_side_scale (fp16)],
-  v_codes, v_norm (fp32), [v_signs, v_rho (fp16)].
-  Region ``name`` is an array [B][H_kv][capacity][record bytes]; the record of
-  token t of (batch b, KV head h) is at index (b * H_kv + h) * capacity + t.
+* The cache holds two arrays of 16-token blocks, K then V (the V array starts
+  on a 256-byte boundary).  Each array is [B][H_kv][capacity / 16] blocks; a
+  block stores, for its 16 tokens, one field after another (bracketed ones only
+  when present), each field 16 records long:
+  K block: codes, norm (fp32), [signs, rho (fp16)], [side, side_scale (fp16)];
+  V block: codes, norm (fp32), [signs, rho (fp16)].
+  Field f of token t of (batch b, KV head h) is at
+  side_offset + ((b * H_kv + h) * capacity / 16 + t // 16) * block_bytes
+  + field_offset + (t % 16) * record_bytes.
 """
 
 from dataclasses import dataclass
 
 import numpy as np
 
-REGION_ALIGN = 256
+TILE = 16          # tokens per block
+SIDE_ALIGN = 256
 
 
 @dataclass(frozen=True)
@@ -47,29 +51,48 @@ class CacheShape:
     headq_bits: int = 4
 
 
-def region_records(shape):
-    """[(name, bytes per token)] in storage order."""
+def side_fields(shape, side):
+    """[(field name, bytes per token)] of one side's block, in block order."""
     d, m = shape.head_dim, shape.m
-    regs = [("k_codes", d * shape.k_bits // 8), ("k_norm", 4)]
-    if shape.k_qjl:
-        regs += [("k_signs", m // 8), ("k_rho", 2)]
-    if shape.headq_rank:
-        regs += [("k_side", shape.headq_rank * shape.headq_bits // 8), ("k_side_scale", 2)]
-    regs += [("v_codes", d * shape.v_bits // 8), ("v_norm", 4)]
+    if side == "k":
+        f = [("k_codes", d * shape.k_bits // 8), ("k_norm", 4)]
+        if shape.k_qjl:
+            f += [("k_signs", m // 8), ("k_rho", 2)]
+        if shape.headq_rank:
+            f += [("k_side", shape.headq_rank * shape.headq_bits // 8), ("k_side_scale", 2)]
+        return f
+    f = [("v_codes", d * shape.v_bits // 8), ("v_norm", 4)]
     if shape.v_qjl:
-        regs += [("v_signs", m // 8), ("v_rho", 2)]
-    return regs
+        f += [("v_signs", m // 8), ("v_rho", 2)]
+    return f
 
 
-def regions(shape):
-    """{name: (offset, bytes per token)} and the total buffer size."""
-    slots = shape.batch * shape.num_kv_heads * shape.capacity
+def layout(shape):
+    """{side: {"offset", "block", "fields": {name: (offset in block, bytes per token)}}, "total"}."""
+    assert shape.capacity % TILE == 0
+    blocks = shape.batch * shape.num_kv_heads * (shape.capacity // TILE)
     out, off = {}, 0
-    for name, rec in region_records(shape):
-        off = (off + REGION_ALIGN - 1) // REGION_ALIGN * REGION_ALIGN
-        out[name] = (off, rec)
-        off += slots * rec
-    return out, off
+    for side in ("k", "v"):
+        off = (off + SIDE_ALIGN - 1) // SIDE_ALIGN * SIDE_ALIGN
+        fields, foff = {}, 0
+        for name, rec in side_fields(shape, side):
+            fields[name] = (foff, rec)
+            foff += TILE * rec
+        out[side] = {"offset": off, "block": foff, "fields": fields}
+        off += blocks * foff
+    out["total"] = off
+    return out
+
+
+def field_offsets(shape, name, b, h, t):
+    """Byte offset of field ``name`` of tokens t (array) of slab (b, h)."""
+    lay = layout(shape)
+    side = lay[name[0]]
+    foff, rec = side["fields"][name]
+    t = np.asarray(t, dtype=np.int64)
+    slab = b * shape.num_kv_heads + h
+    blk = slab * (shape.capacity // TILE) + t // TILE
+    return side["offset"] + blk * side["block"] + foff + (t % TILE) * rec, rec
 
 
 def to_sign_magnitude(c, bits):
@@ -146,31 +169,24 @@ def unpack_side(data, r):
     return np.where(v >= 8, v - 16, v)
 
 
-def region_view(buf, shape, name):
-    """The region as a (B, H_kv, capacity, record bytes) uint8 view of the cache buffer."""
-    regs, _ = regions(shape)
-    off, rec = regs[name]
-    n = shape.batch * shape.num_kv_heads * shape.capacity * rec
-    return np.asarray(buf, dtype=np.uint8)[off:off + n].reshape(
-        shape.batch, shape.num_kv_heads, shape.capacity, rec)
-
-
 def write_fields(buf, shape, b, h, t0, fields):
     """Store encoded fields of tokens t0.. of slab (b, h) into the cache buffer (in place).
 
-    ``fields`` maps region names to per-token records already packed as bytes
+    ``fields`` maps field names to per-token records already packed as bytes
     (N x record bytes) or to scalar arrays (norms fp32, rho / scales fp16).
     """
+    buf = np.asarray(buf, dtype=np.uint8)
     for name, val in fields.items():
-        view = region_view(buf, shape, name)
         arr = np.asarray(val)
         if arr.dtype != np.uint8:
             arr = arr.view(np.uint8).reshape(arr.shape[0], -1)
-        view[b, h, t0:t0 + arr.shape[0], :] = arr
+        off, rec = field_offsets(shape, name, b, h, np.arange(t0, t0 + arr.shape[0]))
+        buf[off[:, None] + np.arange(rec)[None, :]] = arr
 
 
 def read_field(buf, shape, name, b, h, t0, t1, dtype=None):
-    raw = region_view(buf, shape, name)[b, h, t0:t1, :].copy()
+    off, rec = field_offsets(shape, name, b, h, np.arange(t0, t1))
+    raw = np.asarray(buf, dtype=np.uint8)[off[:, None] + np.arange(rec)[None, :]].copy()
     if dtype is None:
         return raw
     return raw.view(dtype).reshape(t1 - t0)

@@ -31,7 +31,7 @@ class OracleContext:
         self.U = None if headq_basis is None else np.asarray(headq_basis, dtype=np.float32)
         self.shape = layout.CacheShape(batch, num_kv_heads, capacity, d, k_codec.bits, k_codec.qjl,
                                        v_codec.bits, v_codec.qjl, self.m, headq_rank, headq_bits)
-        _, self.cache_bytes = layout.regions(self.shape)
+        self.cache_bytes = layout.layout(self.shape)["total"]
 
     def new_cache(self):
         return np.zeros(self.cache_bytes, dtype=np.uint8)

@@ -164,14 +164,17 @@ def test_layout_matches_oracle(scheme, n, headq):
     ctx = _ctx(c)
     lay = b.tq_cache_layout()
     b.check(b.tq_get_cache_layout(ctx, lay))
-    assert lay.layout_version == 1
+    assert lay.layout_version == 2 and lay.tile_tokens == 16
     shape = layout.CacheShape(3, 2, 192, 128, c.k.bits, bool(c.k.qjl), c.v.bits, bool(c.v.qjl), 128, headq, 4)
-    regs, total = layout.regions(shape)
-    assert lay.total_bytes == total
+    want = layout.layout(shape)
+    assert lay.total_bytes == want["total"]
+    assert (lay.k_offset, lay.k_block_bytes) == (want["k"]["offset"], want["k"]["block"])
+    assert (lay.v_offset, lay.v_block_bytes) == (want["v"]["offset"], want["v"]["block"])
     for name in b.REGION_NAMES:
         r = getattr(lay, name)
-        if name in regs:
-            assert (r.offset, r.record_bytes) == regs[name], name
+        fields = want[name[0]]["fields"]
+        if name in fields:
+            assert (r.offset, r.record_bytes) == fields[name], name
         else:
             assert r.record_bytes == 0, name
     b.tq_context_destroy(ctx)

@@ -63,15 +63,25 @@ def test_pack_roundtrip():
     assert np.array_equal(layout.unpack_side(layout.pack_side(z), 16), z)
 
 
-def test_regions_aligned_and_disjoint():
+def test_blocks_aligned_and_disjoint():
     shape = layout.CacheShape(3, 2, 64, 128, 3, True, 2, True, 128, 16, 4)
-    regs, total = layout.regions(shape)
-    spans = sorted((off, off + 3 * 2 * 64 * rec) for off, rec in regs.values())
-    for (a0, a1), (b0, _) in zip(spans, spans[1:]):
-        assert a1 <= b0
-    assert all(off % 256 == 0 for off, _ in regs.values())
-    assert total == spans[-1][1]
-    assert regs["k_codes"][1] == 48 and regs["k_signs"][1] == 16 and regs["k_side"][1] == 8
+    lay = layout.layout(shape)
+    k, v = lay["k"], lay["v"]
+    # K block: codes 48 B, norm 4, signs 16, rho 2, side 8, scale 2 per token, 16 tokens each
+    assert k["fields"] == {"k_codes": (0, 48), "k_norm": (768, 4), "k_signs": (832, 16), "k_rho": (1088, 2),
+                           "k_side": (1120, 8), "k_side_scale": (1248, 2)}
+    assert k["block"] == 1280 and v["block"] == 16 * (32 + 4 + 16 + 2)
+    assert k["offset"] == 0 and v["offset"] % 256 == 0 and v["offset"] >= 3 * 2 * 4 * k["block"]
+    assert lay["total"] == v["offset"] + 3 * 2 * 4 * v["block"]
+    owner = np.full(lay["total"], -1, dtype=np.int64)
+    for name, _ in layout.side_fields(shape, "k") + layout.side_fields(shape, "v"):
+        for b in range(3):
+            for h in range(2):
+                off, rec = layout.field_offsets(shape, name, b, h, np.arange(64))
+                idx = (off[:, None] + np.arange(rec)[None, :]).ravel()
+                assert np.all(owner[idx] == -1), name
+                owner[idx] = 1
+    assert np.all(owner[:3 * 2 * 4 * k["block"]] == 1)
 
 
 def test_zero_vector():

@@ -63,7 +63,8 @@ class QuantizedKVCache:
         lay = _b.tq_cache_layout()
         check(_b.tq_get_cache_layout(ctx, lay))
         self.layout = lay
-        self.regions = {n: (getattr(lay, n).offset, getattr(lay, n).record_bytes) for n in _b.REGION_NAMES}
+        # field offsets inside a side's 16-token block, and bytes per token
+        self.fields = {n: (getattr(lay, n).offset, getattr(lay, n).record_bytes) for n in _b.REGION_NAMES}
         self.cache = torch.zeros(int(lay.total_bytes), dtype=torch.uint8, device=self.device)
         self._ws = None
 

@@ -51,8 +51,9 @@ REGION_NAMES = ["k_codes", "k_norm", "k_signs", "k_rho", "k_side", "k_side_scale
 
 
 class tq_cache_layout(ctypes.Structure):
-    _fields_ = [("layout_version", c_uint32), ("reserved", c_uint32), ("total_bytes", c_uint64)] + \
-               [(n, tq_region) for n in REGION_NAMES]
+    _fields_ = [("layout_version", c_uint32), ("tile_tokens", c_uint32), ("total_bytes", c_uint64),
+                ("k_offset", c_uint64), ("k_block_bytes", c_uint64), ("v_offset", c_uint64),
+                ("v_block_bytes", c_uint64)] + [(n, tq_region) for n in REGION_NAMES]
 
 
 class TQError(RuntimeError):

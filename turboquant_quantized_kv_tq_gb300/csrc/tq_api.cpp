@@ -180,7 +180,12 @@ tq_status tq_get_cache_layout(const tq_context* ctx, tq_cache_layout* out) {
   if (!ctx || !out) return fail(TQ_ERR_INVALID_ARG, "null argument");
   std::memset(out, 0, sizeof(*out));
   out->layout_version = TQ_LAYOUT_VERSION;
+  out->tile_tokens = TQ_TILE_TOKENS;
   out->total_bytes = ctx->layout.total;
+  out->k_offset = ctx->layout.side_off[0];
+  out->k_block_bytes = ctx->layout.block[0];
+  out->v_offset = ctx->layout.side_off[1];
+  out->v_block_bytes = ctx->layout.block[1];
   tq_region* r[R_COUNT] = {&out->k_codes, &out->k_norm, &out->k_signs, &out->k_rho, &out->k_side,
                            &out->k_side_scale, &out->v_codes, &out->v_norm, &out->v_signs, &out->v_rho};
   for (int i = 0; i < R_COUNT; ++i) {

@@ -207,11 +207,12 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   p.v_rotate = ctx->cfg.v.rotate;
   p.score_scale = kLog2e / sqrtf((float)kDecD);
   p.qjl_scale = (float)(1.2533141373155003 / ctx->m);
-  long long W = 0;
+  p.err = pp.err;
+  long long W = 0;  // 16-token tiles over all slabs
   for (int b = 0; b < TQ_MAX_BATCH; ++b) {
     p.seq_len[b] = b < B ? seq_len[b] : 0;
     p.batch_start[b] = W;
-    W += (long long)Hkv * p.seq_len[b];
+    W += (long long)Hkv * ((p.seq_len[b] + kTile - 1) / kTile);
   }
   p.batch_start[TQ_MAX_BATCH] = W;
   p.W = W;

@@ -20,12 +20,12 @@
 //   scores  S[16 tok x 8 heads] = K_hat[16 x 128] Q[128 x 8]   (8 mma.m16n8k16)
 //   readout O^T[128 dims x 8 heads] += V_hat^T[128 x 16] P[16 x 8]  (8 mma), P moved from the
 //           score accumulator layout to the B operand layout with movmatrix.trans.
-// Loads: every thread copies exactly the bytes it will use into its own shared-memory slots
-// with cp.async, kStages tiles ahead (nothing in flight occupies registers; reading back one's
-// own slots is conflict-free).  Codes become fp16 pairs through lane-replicated tables (entry e,
-// lane l at byte 256 e + 4 l, the address built by one byte permute) or, for sign bits, by
-// moving the bit to the fp16 sign position.  Token order inside a tile is permuted so each
-// thread's value operands come from four consecutive tokens:
+// Loads: each warp streams its tiles through a ring of kStages shared-memory stages; a stage is
+// one 16-token K block followed by one V block of the cache (two bulk copies, completing on the
+// stage's mbarrier), refilled as soon as its operands are in registers.  Codes become fp16 pairs
+// through lane-replicated tables (entry e, lane l at byte 256 e + 4 l, the address built by one
+// byte permute) or, for sign bits, by moving the bit to the fp16 sign position.  Token order
+// inside a tile is permuted so each thread's value operands come from four consecutive tokens:
 // score row r <-> token pi(r) = 4((r&7)>>1) + 2(r>>3) + (r&1).
 #pragma once
 
@@ -36,7 +36,11 @@
 namespace tqd {
 
 constexpr int kDecD = 128;
-constexpr int kDecWarps = 8;
+constexpr int kLogitsWarps = 8;
+// Warps per decode block: 16 (4 per scheduler) when the per-thread state fits in 128 registers;
+// the QJL variants carry 16-32 more accumulator / fragment registers and use 12.
+template <bool KQ, bool VQ>
+struct DecWarps { static constexpr int value = (KQ || VQ) ? 12 : 16; };
 constexpr int kTile = 16;
 constexpr int kHeadsPad = 8;
 constexpr int kStages = 4;
@@ -51,13 +55,14 @@ struct DecodeParams {
   const uint32_t* q_u;    // fp16 pairs [B][Hq][8]
   float* part;            // [B*Hkv + kMaxBlocks][8][PS]; slab p's partial from block c at p + c
   int* tickets;           // [B*Hkv]
+  int* err;               // device error word
   float* out;             // [B][Hq][D]
   int B, Hkv, G, v_rotate, nblocks;
-  long long W;            // number of (batch, KV head, token) positions
+  long long W;            // number of 16-token tiles over all (batch, KV head) slabs
   float score_scale;      // log2(e) / sqrt(d)
   float qjl_scale;        // sqrt(pi/2) / m
   int seq_len[TQ_MAX_BATCH];
-  long long batch_start[TQ_MAX_BATCH + 1];  // Hkv * sum of seq_len over earlier batches
+  long long batch_start[TQ_MAX_BATCH + 1];  // first tile of batch b: Hkv * sum of ceil(len/16)
 };
 
 template <int B>
@@ -86,10 +91,13 @@ __device__ __forceinline__ void build_lut(unsigned char* lut, const float* cent)
   }
 }
 
-// Table word for index = byte j of w: byte offset w.byte_j * 256 + lane * 4 (lane4 = lane * 4).
-__device__ __forceinline__ uint32_t lut_get(const unsigned char* lut, uint32_t w, uint32_t lane4, int j) {
+// Table word for index = byte j of w, for a table at shared address `lut`: byte offset
+// w.byte_j * 256 + lane * 4 (lane4 = lane * 4), read with a 32-bit shared-space load.
+__device__ __forceinline__ uint32_t lut_get(uint32_t lut, uint32_t w, uint32_t lane4, int j) {
   const uint32_t off = __byte_perm(w, lane4, 0x5504u | ((uint32_t)j << 4));
-  return *reinterpret_cast<const uint32_t*>(lut + off);
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(lut + off));
+  return v;
 }
 
 // half2 with the sign bits taken from bits 15 and 31 of ~xsh (bit set in xsh = positive).
@@ -111,7 +119,7 @@ template <>
 struct KChunk<4> {
   uint4 c;
   __device__ __forceinline__ void prepare() {}
-  __device__ __forceinline__ uint32_t pair(const unsigned char* lut, uint32_t lane4, uint32_t, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t lut, uint32_t lane4, uint32_t, int p) const {
     const uint32_t w = p < 4 ? c.x : p < 8 ? c.y : p < 12 ? c.z : c.w;
     return lut_get(lut, w, lane4, p & 3);
   }
@@ -126,7 +134,7 @@ struct KChunk<3> {
     xe = nib_even(k.x); xo = nib_odd(k.x); ye = nib_even(k.y); yo = nib_odd(k.y);
     s = unshuffle_bits(s);
   }
-  __device__ __forceinline__ uint32_t pair(const unsigned char* lut, uint32_t lane4, uint32_t, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t lut, uint32_t lane4, uint32_t, int p) const {
     const uint32_t w = p < 8 ? (p & 1 ? xo : xe) : (p & 1 ? yo : ye);
     return signed_pair(lut_get(lut, w, lane4, (p & 7) >> 1), s << (15 - p));
   }
@@ -139,7 +147,7 @@ struct KChunk<2> {
   __device__ __forceinline__ void prepare() {
     xe = nib_even(k.x); xo = nib_odd(k.x); ye = nib_even(k.y); yo = nib_odd(k.y);
   }
-  __device__ __forceinline__ uint32_t pair(const unsigned char* lut, uint32_t lane4, uint32_t, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t lut, uint32_t lane4, uint32_t, int p) const {
     const uint32_t w = p < 8 ? (p & 1 ? xo : xe) : (p & 1 ? yo : ye);
     return lut_get(lut, w, lane4, (p & 7) >> 1);
   }
@@ -149,7 +157,7 @@ template <>
 struct KChunk<1> {
   uint32_t s;
   __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
-  __device__ __forceinline__ uint32_t pair(const unsigned char*, uint32_t, uint32_t m0, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t, uint32_t, uint32_t m0, int p) const {
     return signed_pair(m0, s << (15 - p));
   }
 };
@@ -182,7 +190,7 @@ struct VChunk<4> {
       o23[h] = ((c >> 4) & 0x0F0F0F0Fu) | (d & 0xF0F0F0F0u);
     }
   }
-  __device__ __forceinline__ void frag(const unsigned char* lut, uint32_t lane4, uint32_t, int mt,
+  __device__ __forceinline__ void frag(uint32_t lut, uint32_t lane4, uint32_t, int mt,
                                        uint32_t (&a)[4]) const {
     const int h = mt >> 2, j = mt & 3;
     a[0] = lut_get(lut, e01[h], lane4, j);
@@ -206,7 +214,7 @@ struct Pair2 {
     e23[0] = nib_even(e1); e23[1] = nib_odd(e1);
     o23[0] = nib_even(o1); o23[1] = nib_odd(o1);
   }
-  __device__ __forceinline__ void mags(const unsigned char* lut, uint32_t lane4, int mt, uint32_t (&a)[4]) const {
+  __device__ __forceinline__ void mags(uint32_t lut, uint32_t lane4, int mt, uint32_t (&a)[4]) const {
     const int h = mt & 1, j = mt >> 1;
     a[0] = lut_get(lut, e01[h], lane4, j);
     a[1] = lut_get(lut, o01[h], lane4, j);
@@ -236,7 +244,7 @@ struct VChunk<3> {
   Pair2 m;
   Bits16 sg;
   __device__ __forceinline__ void prepare() { m.build(k); sg.build(s); }
-  __device__ __forceinline__ void frag(const unsigned char* lut, uint32_t lane4, uint32_t, int mt,
+  __device__ __forceinline__ void frag(uint32_t lut, uint32_t lane4, uint32_t, int mt,
                                        uint32_t (&a)[4]) const {
     m.mags(lut, lane4, mt, a);
     sg.apply(mt, a);
@@ -248,7 +256,7 @@ struct VChunk<2> {
   uint32_t k[4];
   Pair2 m;
   __device__ __forceinline__ void prepare() { m.build(k); }
-  __device__ __forceinline__ void frag(const unsigned char* lut, uint32_t lane4, uint32_t, int mt,
+  __device__ __forceinline__ void frag(uint32_t lut, uint32_t lane4, uint32_t, int mt,
                                        uint32_t (&a)[4]) const {
     m.mags(lut, lane4, mt, a);
   }
@@ -259,7 +267,7 @@ struct VChunk<1> {
   uint32_t s[4];
   Bits16 sg;
   __device__ __forceinline__ void prepare() { sg.build(s); }
-  __device__ __forceinline__ void frag(const unsigned char*, uint32_t, uint32_t m0, int mt, uint32_t (&a)[4]) const {
+  __device__ __forceinline__ void frag(uint32_t, uint32_t, uint32_t m0, int mt, uint32_t (&a)[4]) const {
     a[0] = a[1] = a[2] = a[3] = m0;
     sg.apply(mt, a);
   }
@@ -305,232 +313,160 @@ __device__ __forceinline__ int tile_row_token(int r) {
   return 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
 }
 
-// Slab base pointers of one (batch, KV head).
+// Block bases of one (batch, KV head) slab: block `tile` of a side at base + tile * bytes.
 struct SlabPtrs {
-  const unsigned char* kc;
-  const unsigned char* kn;
-  const unsigned char* ks;
-  const unsigned char* kr;
-  const unsigned char* kz;
-  const unsigned char* kzs;
-  const unsigned char* vc;
-  const unsigned char* vn;
-  const unsigned char* vs;
-  const unsigned char* vr;
+  const unsigned char* kb;
+  const unsigned char* vb;
+  unsigned int kbytes, vbytes;
   __device__ __forceinline__ void init(const Cache& C, int b, int h) {
-    kc = C.slab(tqi::R_K_CODES, b, h);
-    kn = C.slab(tqi::R_K_NORM, b, h);
-    ks = C.slab(tqi::R_K_SIGNS, b, h);
-    kr = C.slab(tqi::R_K_RHO, b, h);
-    kz = C.slab(tqi::R_K_SIDE, b, h);
-    kzs = C.slab(tqi::R_K_SIDE_SCALE, b, h);
-    vc = C.slab(tqi::R_V_CODES, b, h);
-    vn = C.slab(tqi::R_V_NORM, b, h);
-    vs = C.slab(tqi::R_V_SIGNS, b, h);
-    vr = C.slab(tqi::R_V_RHO, b, h);
+    kb = C.blockp(0, b, h, 0);
+    vb = C.blockp(1, b, h, 0);
+    kbytes = C.block[0];
+    vbytes = C.block[1];
   }
 };
 
 template <int KB> struct KRec { static constexpr int value = kDecD * KB / 8; };
 
-// Per-thread slot layout of one tile: 16-, 8- and 4-byte items, each item an array over the
-// 32 lanes (item i of size z for lane l at offset off_z + (32 i + l) z).
+// Shared-memory stage of one 16-token tile of one warp: the tile's K block then its V block, in
+// the cache's block layout (field offsets are multiples of 16 bytes).
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
-struct Slots {
-  static constexpr int n16 = KB == 4 ? 2 : 0;
-  static constexpr int K8 = 0;
-  static constexpr int Z8 = K8 + ((KB == 3 || KB == 2) ? 2 : 0);
-  static constexpr int V8 = Z8 + (KH ? 2 : 0);
-  static constexpr int n8 = V8 + (VB == 4 ? 4 : 0);
-  static constexpr int KS4 = 0;
-  static constexpr int NK4 = KS4 + ((KB == 3 || KB == 1) ? 2 : 0);
-  static constexpr int Q4 = NK4 + 2;
-  static constexpr int H4 = Q4 + (KQ ? 4 : 0);
-  static constexpr int V4 = H4 + (KH ? 2 : 0);
-  static constexpr int NV4 = V4 + (VB == 3 ? 8 : (VB == 2 || VB == 1) ? 4 : 0);
-  static constexpr int VQ4 = NV4 + 2;
-  static constexpr int n4 = VQ4 + (VQ ? 6 : 0);
-  static constexpr int off8 = n16 * 16 * 32;
-  static constexpr int off4 = off8 + n8 * 8 * 32;
-  static constexpr int bytes = off4 + n4 * 4 * 32;
+struct Stage {
+  static constexpr int KC = 0;
+  static constexpr int KN = KC + kTile * KRec<KB>::value;
+  static constexpr int KS = KN + kTile * 4;
+  static constexpr int KRH = KS + (KQ ? kTile * (kDecD / 8) : 0);
+  static constexpr int KZ = KRH + (KQ ? kTile * 2 : 0);
+  static constexpr int KZS = KZ + (KH ? kTile * 8 : 0);
+  static constexpr int VC = KZS + (KH ? kTile * 2 : 0);
+  static constexpr int VN = VC + kTile * KRec<VB>::value;
+  static constexpr int VS = VN + kTile * 4;
+  static constexpr int VRH = VS + (VQ ? kTile * (kDecD / 8) : 0);
+  static constexpr int bytes = VRH + (VQ ? kTile * 2 : 0);
+  static constexpr int copies = 4 + (KQ ? 2 : 0) + (KH ? 2 : 0) + (VQ ? 2 : 0);
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
-// Start the copies of tile [t0, t0 + 16) (tokens clamped to `last`) into the slots at `st`
-// (shared-space address).
+// Start the bulk copies of tile `tile` (tokens [16 tile, 16 tile + 16) of the slab) into the
+// stage at shared address `st`: lane 0 registers the byte count on `bar`, then lane 0 copies
+// the K block and lane 1 the V block (a stage is exactly a K block followed by a V block).
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void issue_tile(uint32_t st, const SlabPtrs& s, int t0, int last, int lg,
-                                           int lt, int lane) {
-  using S = Slots<KB, KQ, KH, VB, VQ>;
-  constexpr int KR = KRec<KB>::value;
-  constexpr int VR = KRec<VB>::value;
-  const int tA = min(t0 + tile_row_token(lg), last);
-  const int tB = min(t0 + tile_row_token(lg + 8), last);
-  int tv[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) tv[j] = min(t0 + 4 * lt + j, last);
-  auto a16 = [&](int i) { return st + (uint32_t)((32 * i + lane) * 16); };
-  auto a8 = [&](int i) { return st + (uint32_t)(S::off8 + (32 * i + lane) * 8); };
-  auto a4 = [&](int i) { return st + (uint32_t)(S::off4 + (32 * i + lane) * 4); };
-  if constexpr (KB == 4) {
-    cp_async16(a16(0), s.kc + tA * KR + 16 * lt);
-    cp_async16(a16(1), s.kc + tB * KR + 16 * lt);
-  } else if constexpr (KB == 3 || KB == 2) {
-    cp_async8(a8(S::K8), s.kc + tA * KR + 8 * lt);
-    cp_async8(a8(S::K8 + 1), s.kc + tB * KR + 8 * lt);
-    if constexpr (KB == 3) {
-      cp_async4(a4(S::KS4), s.kc + tA * KR + kDecD / 4 + 4 * lt);
-      cp_async4(a4(S::KS4 + 1), s.kc + tB * KR + kDecD / 4 + 4 * lt);
-    }
-  } else {
-    cp_async4(a4(S::KS4), s.kc + tA * KR + 4 * lt);
-    cp_async4(a4(S::KS4 + 1), s.kc + tB * KR + 4 * lt);
-  }
-  cp_async4(a4(S::NK4), s.kn + tA * 4);
-  cp_async4(a4(S::NK4 + 1), s.kn + tB * 4);
-  if constexpr (KQ) {
-    cp_async4(a4(S::Q4), s.ks + tA * (kDecD / 8) + 4 * lt);
-    cp_async4(a4(S::Q4 + 1), s.ks + tB * (kDecD / 8) + 4 * lt);
-    cp_async4(a4(S::Q4 + 2), s.kr + (tA & ~1) * 2);
-    cp_async4(a4(S::Q4 + 3), s.kr + (tB & ~1) * 2);
-  }
-  if constexpr (KH) {
-    cp_async8(a8(S::Z8), s.kz + tA * 8);
-    cp_async8(a8(S::Z8 + 1), s.kz + tB * 8);
-    cp_async4(a4(S::H4), s.kzs + (tA & ~1) * 2);
-    cp_async4(a4(S::H4 + 1), s.kzs + (tB & ~1) * 2);
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if constexpr (VB == 4) {
-      cp_async8(a8(S::V8 + j), s.vc + tv[j] * VR + 8 * lg);
-    } else if constexpr (VB == 3) {
-      cp_async4(a4(S::V4 + j), s.vc + tv[j] * VR + 4 * lg);
-      cp_async4(a4(S::V4 + 4 + j), s.vc + tv[j] * VR + kDecD / 4 + 4 * (lg >> 1));
-    } else if constexpr (VB == 2) {
-      cp_async4(a4(S::V4 + j), s.vc + tv[j] * VR + 4 * lg);
-    } else {
-      cp_async4(a4(S::V4 + j), s.vc + tv[j] * VR + 4 * (lg >> 1));
-    }
-    if constexpr (VQ) cp_async4(a4(S::VQ4 + j), s.vs + tv[j] * (kDecD / 8) + 4 * (lg >> 1));
-  }
-  cp_async4(a4(S::NV4), s.vn + tA * 4);
-  cp_async4(a4(S::NV4 + 1), s.vn + tB * 4);
-  if constexpr (VQ) {
-    cp_async4(a4(S::VQ4 + 4), s.vr + (tA & ~1) * 2);
-    cp_async4(a4(S::VQ4 + 5), s.vr + (tB & ~1) * 2);
-  }
+__device__ __forceinline__ void issue_stage(uint32_t st, uint32_t bar, const SlabPtrs& s, int tile, int lane) {
+  using S = Stage<KB, KQ, KH, VB, VQ>;
+  if (lane == 0) mbar_arrive_expect_tx(bar, S::bytes);
+  __syncwarp();
+  if (lane == 0) bulk_g2s(st, s.kb + (unsigned long long)tile * s.kbytes, S::VC, bar);
+  if (lane == 1) bulk_g2s(st + S::VC, s.vb + (unsigned long long)tile * s.vbytes, S::bytes - S::VC, bar);
 }
 
-// Read this thread's slots of one tile back into registers.
+__device__ __forceinline__ float lds_f32(const unsigned char* p) { return *reinterpret_cast<const float*>(p); }
+__device__ __forceinline__ float lds_f16(const unsigned char* p) {
+  return __half2float(*reinterpret_cast<const __half*>(p));
+}
+__device__ __forceinline__ uint32_t lds_u16(const unsigned char* p) {
+  return *reinterpret_cast<const unsigned short*>(p);
+}
+
+// Read this thread's operands of one tile from its warp's stage.
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void read_tile(TileData<KB, KQ, KH, VB, VQ>& d, const unsigned char* st, int t0,
-                                          int last, int lg, int lt, int lane) {
-  using S = Slots<KB, KQ, KH, VB, VQ>;
-  auto r16 = [&](int i) { return *reinterpret_cast<const uint4*>(st + (32 * i + lane) * 16); };
-  auto r8 = [&](int i) { return *reinterpret_cast<const uint2*>(st + S::off8 + (32 * i + lane) * 8); };
-  auto r4 = [&](int i) { return *reinterpret_cast<const uint32_t*>(st + S::off4 + (32 * i + lane) * 4); };
-  const int tA = min(t0 + tile_row_token(lg), last);
-  const int tB = min(t0 + tile_row_token(lg + 8), last);
+__device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, const unsigned char* st, int lg,
+                                           int lt) {
+  using S = Stage<KB, KQ, KH, VB, VQ>;
+  constexpr int KR = KRec<KB>::value, VR = KRec<VB>::value;
+  const int rA = tile_row_token(lg), rB = tile_row_token(lg + 8);
+  const unsigned char* ka = st + S::KC + rA * KR;
+  const unsigned char* kb = st + S::KC + rB * KR;
   if constexpr (KB == 4) {
-    d.kA.c = r16(0);
-    d.kB.c = r16(1);
+    d.kA.c = *reinterpret_cast<const uint4*>(ka + 16 * lt);
+    d.kB.c = *reinterpret_cast<const uint4*>(kb + 16 * lt);
   } else if constexpr (KB == 3 || KB == 2) {
-    d.kA.k = r8(S::K8);
-    d.kB.k = r8(S::K8 + 1);
+    d.kA.k = *reinterpret_cast<const uint2*>(ka + 8 * lt);
+    d.kB.k = *reinterpret_cast<const uint2*>(kb + 8 * lt);
     if constexpr (KB == 3) {
-      d.kA.s = r4(S::KS4);
-      d.kB.s = r4(S::KS4 + 1);
+      d.kA.s = *reinterpret_cast<const uint32_t*>(ka + kDecD / 4 + 4 * lt);
+      d.kB.s = *reinterpret_cast<const uint32_t*>(kb + kDecD / 4 + 4 * lt);
     }
   } else {
-    d.kA.s = r4(S::KS4);
-    d.kB.s = r4(S::KS4 + 1);
+    d.kA.s = *reinterpret_cast<const uint32_t*>(ka + 4 * lt);
+    d.kB.s = *reinterpret_cast<const uint32_t*>(kb + 4 * lt);
   }
-  d.nuKA = __uint_as_float(r4(S::NK4));
-  d.nuKB = __uint_as_float(r4(S::NK4 + 1));
+  d.nuKA = lds_f32(st + S::KN + 4 * rA);
+  d.nuKB = lds_f32(st + S::KN + 4 * rB);
   if constexpr (KQ) {
-    d.sA.s = r4(S::Q4);
-    d.sB.s = r4(S::Q4 + 1);
-    d.rhoKA = half_of(r4(S::Q4 + 2), tA & 1);
-    d.rhoKB = half_of(r4(S::Q4 + 3), tB & 1);
+    d.sA.s = *reinterpret_cast<const uint32_t*>(st + S::KS + rA * (kDecD / 8) + 4 * lt);
+    d.sB.s = *reinterpret_cast<const uint32_t*>(st + S::KS + rB * (kDecD / 8) + 4 * lt);
+    d.rhoKA = lds_f16(st + S::KRH + 2 * rA);
+    d.rhoKB = lds_f16(st + S::KRH + 2 * rB);
   }
   if constexpr (KH) {
-    const uint2 za = r8(S::Z8), zb = r8(S::Z8 + 1);
+    const uint2 za = *reinterpret_cast<const uint2*>(st + S::KZ + 8 * rA);
+    const uint2 zb = *reinterpret_cast<const uint2*>(st + S::KZ + 8 * rB);
     d.zA = make_uint2((za.x >> (8 * lt)) & 0xffu, (za.y >> (8 * lt)) & 0xffu);
     d.zB = make_uint2((zb.x >> (8 * lt)) & 0xffu, (zb.y >> (8 * lt)) & 0xffu);
-    d.zsA = half_of(r4(S::H4), tA & 1);
-    d.zsB = half_of(r4(S::H4 + 1), tB & 1);
+    d.zsA = lds_f16(st + S::KZS + 2 * rA);
+    d.zsB = lds_f16(st + S::KZS + 2 * rB);
   }
-  const int hs = lg & 1;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    const unsigned char* v = st + S::VC + (4 * lt + j) * VR;
     if constexpr (VB == 4) {
-      d.v.w[j] = r8(S::V8 + j);
+      d.v.w[j] = *reinterpret_cast<const uint2*>(v + 8 * lg);
     } else if constexpr (VB == 3) {
-      d.v.k[j] = r4(S::V4 + j);
-      d.v.s[j] = hs ? r4(S::V4 + 4 + j) >> 16 : r4(S::V4 + 4 + j) & 0xffffu;
+      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 4 * lg);
+      d.v.s[j] = lds_u16(v + kDecD / 4 + 2 * lg);
     } else if constexpr (VB == 2) {
-      d.v.k[j] = r4(S::V4 + j);
+      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 4 * lg);
     } else {
-      d.v.s[j] = hs ? r4(S::V4 + j) >> 16 : r4(S::V4 + j) & 0xffffu;
+      d.v.s[j] = lds_u16(v + 2 * lg);
     }
-    if constexpr (VQ) d.vs.s[j] = hs ? r4(S::VQ4 + j) >> 16 : r4(S::VQ4 + j) & 0xffffu;
+    if constexpr (VQ) d.vs.s[j] = lds_u16(st + S::VS + (4 * lt + j) * (kDecD / 8) + 2 * lg);
   }
-  d.nuVA = __uint_as_float(r4(S::NV4));
-  d.nuVB = __uint_as_float(r4(S::NV4 + 1));
+  d.nuVA = lds_f32(st + S::VN + 4 * rA);
+  d.nuVB = lds_f32(st + S::VN + 4 * rB);
   if constexpr (VQ) {
-    d.rhoVA = half_of(r4(S::VQ4 + 4), tA & 1);
-    d.rhoVB = half_of(r4(S::VQ4 + 5), tB & 1);
+    d.rhoVA = lds_f16(st + S::VRH + 2 * rA);
+    d.rhoVB = lds_f16(st + S::VRH + 2 * rB);
   }
 }
 
-// Direct (uncached) loads of a tile's key data, used by the logits kernel.
+// Direct (uncached) loads of a tile's key data from the K blocks, used by the logits kernel.
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, const SlabPtrs& s, int t0,
                                            int last, int lg, int lt) {
+  using S = Stage<KB, KQ, KH, VB, VQ>;
   constexpr int KR = KRec<KB>::value;
   const int tA = min(t0 + tile_row_token(lg), last);
   const int tB = min(t0 + tile_row_token(lg + 8), last);
+  const unsigned char* bA = s.kb + (unsigned long long)(tA / kTile) * s.kbytes;
+  const unsigned char* bB = s.kb + (unsigned long long)(tB / kTile) * s.kbytes;
+  const int jA = tA % kTile, jB = tB % kTile;
   if constexpr (KB == 4) {
-    d.kA.c = ldg_stream16(s.kc + tA * KR + 16 * lt);
-    d.kB.c = ldg_stream16(s.kc + tB * KR + 16 * lt);
+    d.kA.c = ldg_stream16(bA + S::KC + jA * KR + 16 * lt);
+    d.kB.c = ldg_stream16(bB + S::KC + jB * KR + 16 * lt);
   } else if constexpr (KB == 3 || KB == 2) {
-    d.kA.k = ldg_stream8(s.kc + tA * KR + 8 * lt);
-    d.kB.k = ldg_stream8(s.kc + tB * KR + 8 * lt);
+    d.kA.k = ldg_stream8(bA + S::KC + jA * KR + 8 * lt);
+    d.kB.k = ldg_stream8(bB + S::KC + jB * KR + 8 * lt);
     if constexpr (KB == 3) {
-      d.kA.s = ldg_stream4(s.kc + tA * KR + kDecD / 4 + 4 * lt);
-      d.kB.s = ldg_stream4(s.kc + tB * KR + kDecD / 4 + 4 * lt);
+      d.kA.s = ldg_stream4(bA + S::KC + jA * KR + kDecD / 4 + 4 * lt);
+      d.kB.s = ldg_stream4(bB + S::KC + jB * KR + kDecD / 4 + 4 * lt);
     }
   } else {
-    d.kA.s = ldg_stream4(s.kc + tA * KR + 4 * lt);
-    d.kB.s = ldg_stream4(s.kc + tB * KR + 4 * lt);
+    d.kA.s = ldg_stream4(bA + S::KC + jA * KR + 4 * lt);
+    d.kB.s = ldg_stream4(bB + S::KC + jB * KR + 4 * lt);
   }
-  d.nuKA = __uint_as_float(ldg_stream4(s.kn + tA * 4));
-  d.nuKB = __uint_as_float(ldg_stream4(s.kn + tB * 4));
+  d.nuKA = __uint_as_float(ldg_stream4(bA + S::KN + 4 * jA));
+  d.nuKB = __uint_as_float(ldg_stream4(bB + S::KN + 4 * jB));
   if constexpr (KQ) {
-    d.sA.s = ldg_stream4(s.ks + tA * (kDecD / 8) + 4 * lt);
-    d.sB.s = ldg_stream4(s.ks + tB * (kDecD / 8) + 4 * lt);
-    d.rhoKA = half_of(ldg_stream4(s.kr + (tA & ~1) * 2), tA & 1);
-    d.rhoKB = half_of(ldg_stream4(s.kr + (tB & ~1) * 2), tB & 1);
+    d.sA.s = ldg_stream4(bA + S::KS + jA * (kDecD / 8) + 4 * lt);
+    d.sB.s = ldg_stream4(bB + S::KS + jB * (kDecD / 8) + 4 * lt);
+    d.rhoKA = half_of(ldg_stream4(bA + S::KRH + (jA & ~1) * 2), jA & 1);
+    d.rhoKB = half_of(ldg_stream4(bB + S::KRH + (jB & ~1) * 2), jB & 1);
   }
   if constexpr (KH) {
-    const uint2 za = ldg_stream8(s.kz + tA * 8), zb = ldg_stream8(s.kz + tB * 8);
+    const uint2 za = ldg_stream8(bA + S::KZ + 8 * jA), zb = ldg_stream8(bB + S::KZ + 8 * jB);
     d.zA = make_uint2((za.x >> (8 * lt)) & 0xffu, (za.y >> (8 * lt)) & 0xffu);
     d.zB = make_uint2((zb.x >> (8 * lt)) & 0xffu, (zb.y >> (8 * lt)) & 0xffu);
-    d.zsA = half_of(ldg_stream4(s.kzs + (tA & ~1) * 2), tA & 1);
-    d.zsB = half_of(ldg_stream4(s.kzs + (tB & ~1) * 2), tB & 1);
+    d.zsA = half_of(ldg_stream4(bA + S::KZS + (jA & ~1) * 2), jA & 1);
+    d.zsB = half_of(ldg_stream4(bB + S::KZS + (jB & ~1) * 2), jB & 1);
   }
 }
 
@@ -540,21 +476,22 @@ __device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, cons
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, float (&s)[4],
                                            const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                           const uint32_t (&qu)[2], const unsigned char* lutK,
+                                           const uint32_t (&qu)[2], uint32_t lutK,
                                            uint32_t lane4, uint32_t k_m0, float qjl_scale) {
   d.kA.prepare();
   d.kB.prepare();
-  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  // two independent accumulator chains (even / odd k-steps) halve the MMA dependency chain
+  float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    mma16816(sc, d.kA.pair(lutK, lane4, k_m0, 2 * ks), d.kB.pair(lutK, lane4, k_m0, 2 * ks),
+    mma16816(sc[ks & 1], d.kA.pair(lutK, lane4, k_m0, 2 * ks), d.kB.pair(lutK, lane4, k_m0, 2 * ks),
              d.kA.pair(lutK, lane4, k_m0, 2 * ks + 1), d.kB.pair(lutK, lane4, k_m0, 2 * ks + 1), qf[2 * ks],
              qf[2 * ks + 1]);
   }
-  s[0] = sc[0] * d.nuKA;
-  s[1] = sc[1] * d.nuKA;
-  s[2] = sc[2] * d.nuKB;
-  s[3] = sc[3] * d.nuKB;
+  s[0] = (sc[0][0] + sc[1][0]) * d.nuKA;
+  s[1] = (sc[0][1] + sc[1][1]) * d.nuKA;
+  s[2] = (sc[0][2] + sc[1][2]) * d.nuKB;
+  s[3] = (sc[0][3] + sc[1][3]) * d.nuKB;
   if constexpr (KQ) {
     d.sA.prepare();
     d.sB.prepare();
@@ -600,23 +537,40 @@ struct WarpState {
   }
 };
 
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void compute_tile(TileData<KB, KQ, KH, VB, VQ>& d, WarpState<VQ>& st,
-                                             const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                             const uint32_t (&qu)[2], const unsigned char* lutK,
-                                             const unsigned char* lutV, uint32_t lane4, uint32_t k_m0,
-                                             uint32_t v_m0, const DecodeParams& p, int t0, int end, int lg) {
-  float s[4];
-  key_scores(d, s, qf, qs, qu, lutK, lane4, k_m0, p.qjl_scale);
-  const bool va = t0 + tile_row_token(lg) < end;
-  const bool vb = t0 + tile_row_token(lg + 8) < end;
-  s[0] = va ? s[0] * p.score_scale : -INFINITY;
-  s[1] = va ? s[1] * p.score_scale : -INFINITY;
-  s[2] = vb ? s[2] * p.score_scale : -INFINITY;
-  s[3] = vb ? s[3] * p.score_scale : -INFINITY;
+// 2^x on the special-function unit (inputs here are <= 0; -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// NT consecutive tiles (starting at token t0) through one online-softmax step.
+template <int NT, int KB, bool KQ, bool KH, int VB, bool VQ>
+__device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ>& st,
+                                              const uint32_t (&qf)[16], const uint32_t (&qs)[16],
+                                              const uint32_t (&qu)[2], uint32_t lutK,
+                                              uint32_t lutV, uint32_t lane4, uint32_t k_m0,
+                                              uint32_t v_m0, const DecodeParams& p, int t0, int end, int lg) {
+  float s[NT][4];
+  bool va[NT], vb[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    key_scores(d[j], s[j], qf, qs, qu, lutK, lane4, k_m0, p.qjl_scale);
+    va[j] = t0 + kTile * j + tile_row_token(lg) < end;
+    vb[j] = t0 + kTile * j + tile_row_token(lg + 8) < end;
+    s[j][0] = va[j] ? s[j][0] * p.score_scale : -INFINITY;
+    s[j][1] = va[j] ? s[j][1] * p.score_scale : -INFINITY;
+    s[j][2] = vb[j] ? s[j][2] * p.score_scale : -INFINITY;
+    s[j][3] = vb[j] ? s[j][3] * p.score_scale : -INFINITY;
+  }
 
   // ---- online softmax (log2 domain)
-  float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+  float mx0 = fmaxf(s[0][0], s[0][2]), mx1 = fmaxf(s[0][1], s[0][3]);
+#pragma unroll
+  for (int j = 1; j < NT; ++j) {
+    mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][2]));
+    mx1 = fmaxf(mx1, fmaxf(s[j][1], s[j][3]));
+  }
 #pragma unroll
   for (int m = 4; m <= 16; m <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, m));
@@ -624,7 +578,7 @@ __device__ __forceinline__ void compute_tile(TileData<KB, KQ, KH, VB, VQ>& d, Wa
   }
   const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
   if (__any_sync(kFull, n0 > st.m0 || n1 > st.m1)) {
-    const float a0 = exp2f(st.m0 - n0), a1 = exp2f(st.m1 - n1);
+    const float a0 = ex2(st.m0 - n0), a1 = ex2(st.m1 - n1);
     st.l0 *= a0;
     st.l1 *= a1;
 #pragma unroll
@@ -637,31 +591,36 @@ __device__ __forceinline__ void compute_tile(TileData<KB, KQ, KH, VB, VQ>& d, Wa
     st.m0 = n0;
     st.m1 = n1;
   }
-  const float p0 = exp2f(s[0] - n0), p1 = exp2f(s[1] - n1);
-  const float p2 = exp2f(s[2] - n0), p3 = exp2f(s[3] - n1);
-  st.l0 += p0 + p2;
-  st.l1 += p1 + p3;
 
   // ---- value readout
-  const uint32_t bv0 = movmatrix_trans(pack_half2(p0 * d.nuVA, p1 * d.nuVA));
-  const uint32_t bv1 = movmatrix_trans(pack_half2(p2 * d.nuVB, p3 * d.nuVB));
-  d.v.prepare();
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    uint32_t a[4];
-    d.v.frag(lutV, lane4, v_m0, mt, a);
-    mma16816(st.acc[mt], a[0], a[1], a[2], a[3], bv0, bv1);
-  }
-  if constexpr (VQ) {
-    const float fa = d.nuVA * d.rhoVA, fb = d.nuVB * d.rhoVB;
-    const uint32_t bs0 = movmatrix_trans(pack_half2(p0 * fa, p1 * fa));
-    const uint32_t bs1 = movmatrix_trans(pack_half2(p2 * fb, p3 * fb));
-    d.vs.prepare();
+  for (int j = 0; j < NT; ++j) {
+    const float p0 = ex2(s[j][0] - n0), p1 = ex2(s[j][1] - n1);
+    const float p2 = ex2(s[j][2] - n0), p3 = ex2(s[j][3] - n1);
+    st.l0 += p0 + p2;
+    st.l1 += p1 + p3;
+    // rows past the sequence end read whatever the cache holds there: select, don't multiply
+    const float nA = va[j] ? d[j].nuVA : 0.f, nB = vb[j] ? d[j].nuVB : 0.f;
+    const uint32_t bv0 = movmatrix_trans(pack_half2(p0 * nA, p1 * nA));
+    const uint32_t bv1 = movmatrix_trans(pack_half2(p2 * nB, p3 * nB));
+    d[j].v.prepare();
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t a[4];
-      d.vs.frag(mt, a);
-      mma16816(st.accs[mt], a[0], a[1], a[2], a[3], bs0, bs1);
+      d[j].v.frag(lutV, lane4, v_m0, mt, a);
+      mma16816(st.acc[mt], a[0], a[1], a[2], a[3], bv0, bv1);
+    }
+    if constexpr (VQ) {
+      const float fa = va[j] ? d[j].nuVA * d[j].rhoVA : 0.f, fb = vb[j] ? d[j].nuVB * d[j].rhoVB : 0.f;
+      const uint32_t bs0 = movmatrix_trans(pack_half2(p0 * fa, p1 * fa));
+      const uint32_t bs1 = movmatrix_trans(pack_half2(p2 * fb, p3 * fb));
+      d[j].vs.prepare();
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4];
+        d[j].vs.frag(mt, a);
+        mma16816(st.accs[mt], a[0], a[1], a[2], a[3], bs0, bs1);
+      }
     }
   }
 }
@@ -671,21 +630,26 @@ struct DecodeSmem {
   static constexpr int lutK = LutEntries<KB>::value * kLutStride;
   static constexpr int lutV = KB == VB ? 0 : LutEntries<VB>::value * kLutStride;  // same codebook
   static constexpr int PS = 4 + kDecD + (VQ ? kDecD : 0);  // per head: m, l, pad, pad, acc, (acc_sk)
-  static constexpr int merge = kDecWarps * kHeadsPad * PS * 4;
-  static constexpr int stages = kDecWarps * kStages * Slots<KB, KQ, KH, VB, VQ>::bytes;
+  static constexpr int NW = DecWarps<KQ, VQ>::value;
+  static constexpr int merge = NW * kHeadsPad * PS * 4;
+  static constexpr int stages = NW * kStages * Stage<KB, KQ, KH, VB, VQ>::bytes;
   static constexpr int work = stages > merge ? stages : merge;
-  static constexpr int bytes = lutK + lutV + work;
+  static constexpr int bars = NW * kStages * 8;
+  static constexpr int bytes = lutK + lutV + work + bars;
 };
 
-// Owner block of flattened position x: the largest c with floor(c W / N) <= x.
+// Owner block of flattened tile x: the largest c with floor(c W / N) <= x.
 __device__ __forceinline__ int owner_block(long long x, long long W, int N) {
   return (int)(((x + 1) * N - 1) / W);
 }
 
+constexpr uint32_t kWaitLimit = 1u << 20;  // polls of an mbarrier before giving up
+constexpr int kErrWaitTimeout = 1;
+
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel(const DecodeParams p) {
   using SM = DecodeSmem<KB, KQ, KH, VB, VQ>;
-  using SL = Slots<KB, KQ, KH, VB, VQ>;
+  using SG = Stage<KB, KQ, KH, VB, VQ>;
   constexpr int PS = SM::PS;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_last;
@@ -696,22 +660,30 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
   unsigned char* lutK = smem;
   unsigned char* lutV = KB == VB ? smem : smem + SM::lutK;
   unsigned char* work = smem + SM::lutK + SM::lutV;
+  unsigned char* bars = work + SM::work;
   if constexpr (KB != 1) build_lut<KB>(lutK, p.tab.k_c);
   if constexpr (VB != 1 && VB != KB) build_lut<VB>(lutV, p.tab.v_c);
   const uint32_t k_m0 = pack_half2(__ldg(p.tab.k_c + 1), __ldg(p.tab.k_c + 1));
   const uint32_t v_m0 = pack_half2(__ldg(p.tab.v_c + 1), __ldg(p.tab.v_c + 1));
+  const uint32_t my_bars = (uint32_t)__cvta_generic_to_shared(bars) + warp * kStages * 8;
+  const uint32_t lutK_s = (uint32_t)__cvta_generic_to_shared(lutK);
+  const uint32_t lutV_s = (uint32_t)__cvta_generic_to_shared(lutV);
+  if (lane < kStages) mbar_init(my_bars + 8 * lane, 1);
+  fence_mbar_init();
   __syncthreads();
 
-  unsigned char* my_stages = work + warp * kStages * SL::bytes;
+  unsigned char* my_stages = work + warp * kStages * SG::bytes;
   const uint32_t my_stages_s = (uint32_t)__cvta_generic_to_shared(my_stages);
   const int G = p.G;
   const int Hq = p.Hkv * G;
   const int N = p.nblocks;
   long long x = (long long)blockIdx.x * p.W / N;
   const long long x_end = (long long)(blockIdx.x + 1) * p.W / N;
+  unsigned seq = 0;  // tiles this warp has streamed so far: stage seq % S, phase (seq / S) & 1
+  bool timed_out = false;
 
   while (x < x_end) {
-    // ---- locate the slab segment that starts at x
+    // ---- locate the slab segment that starts at tile x
     int lo = 0, hi = p.B - 1;  // largest b with batch_start[b] <= x
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -719,11 +691,12 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
     }
     const int b = lo;
     const int L = p.seq_len[b];
+    const int ntb = (L + kTile - 1) / kTile;  // tiles per slab of batch b
     const long long off = x - p.batch_start[b];
-    const int kvh = (int)(off / L);
-    const int ts = (int)(off % L);
-    const long long slab_start = p.batch_start[b] + (long long)kvh * L;
-    const long long seg_end = min(x_end, slab_start + L);
+    const int kvh = (int)(off / ntb);
+    const int ts = (int)(off % ntb);  // first tile of the segment
+    const long long slab_start = p.batch_start[b] + (long long)kvh * ntb;
+    const long long seg_end = min(x_end, slab_start + ntb);
     const int te = ts + (int)(seg_end - x);
     const int pair = b * p.Hkv + kvh;
 
@@ -755,35 +728,52 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
       }
     }
 
-    // ---- this warp's sub-range, streamed through the cp.async ring
+    // ---- this warp's tiles of the segment, streamed through its bulk-copy ring
     const int n = te - ts;
-    const int per = ((n + kDecWarps - 1) / kDecWarps + kTile - 1) / kTile * kTile;
-    const int w0 = min(te, ts + warp * per);
-    const int w1 = min(te, w0 + per);
-    const int nt = (w1 - w0 + kTile - 1) / kTile;
+    const int per = (n + SM::NW - 1) / SM::NW;
+    const int m0t = min(te, ts + warp * per);
+    const int m1t = min(te, m0t + per);
+    const int nt = m1t - m0t;
     SlabPtrs sp;
     sp.init(p.cache, b, kvh);
     WarpState<VQ> st;
     st.reset();
-    const int last = max(w1 - 1, 0);
+    // all kStages stages in flight; tiles are consumed two at a time, and a pair's stages are
+    // refilled as soon as its operands are in registers, before the pair is computed
 #pragma unroll
-    for (int i = 0; i < kStages - 1; ++i) {
-      if (i < nt) issue_tile<KB, KQ, KH, VB, VQ>(my_stages_s + i * SL::bytes, sp, w0 + i * kTile, last, lg, lt, lane);
-      cp_commit();
+    for (int i = 0; i < kStages; ++i) {
+      if (i < nt) {
+        const unsigned sl = (seq + i) % kStages;
+        issue_stage<KB, KQ, KH, VB, VQ>(my_stages_s + sl * SG::bytes, my_bars + 8 * sl, sp, m0t + i, lane);
+      }
     }
-    for (int i = 0; i < nt; ++i) {
-      const int nx = i + kStages - 1;
-      if (nx < nt)
-        issue_tile<KB, KQ, KH, VB, VQ>(my_stages_s + (nx % kStages) * SL::bytes, sp, w0 + nx * kTile, last, lg,
-                                       lt, lane);
-      cp_commit();
-      cp_wait<kStages - 1>();
-      TileData<KB, KQ, KH, VB, VQ> d;
-      const int t0 = w0 + i * kTile;
-      read_tile(d, my_stages + (i % kStages) * SL::bytes, t0, last, lg, lt, lane);
-      compute_tile(d, st, qf, qs, qu, lutK, lutV, lane4, k_m0, v_m0, p, t0, w1, lg);
+    for (int i = 0; i < nt; i += 2) {
+      const bool two = i + 1 < nt;
+      TileData<KB, KQ, KH, VB, VQ> d[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (j == 0 || two) {
+          const unsigned cur = seq + i + j;
+          if (!mbar_wait(my_bars + 8 * (cur % kStages), (cur / kStages) & 1u, kWaitLimit)) timed_out = true;
+          read_stage(d[j], my_stages + (cur % kStages) * SG::bytes, lg, lt);
+        }
+      }
+      __syncwarp();  // every lane has read the pair's stages
+      fence_proxy_async_shared();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int nx = i + j + kStages;
+        if (nx < nt) {
+          const unsigned sl = (seq + nx) % kStages;
+          issue_stage<KB, KQ, KH, VB, VQ>(my_stages_s + sl * SG::bytes, my_bars + 8 * sl, sp, m0t + nx, lane);
+        }
+      }
+      if (two)
+        compute_tiles<2>(d, st, qf, qs, qu, lutK_s, lutV_s, lane4, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
+      else
+        compute_tiles<1>(d, st, qf, qs, qu, lutK_s, lutV_s, lane4, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
     }
-    cp_wait<0>();
+    seq += nt;
 
     // ---- merge the warps of this block for this segment
     float l0 = st.l0, l1 = st.l1;
@@ -792,7 +782,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
       l0 += __shfl_xor_sync(kFull, l0, m);
       l1 += __shfl_xor_sync(kFull, l1, m);
     }
-    __syncthreads();  // every warp is done with its slots: reuse them for the merge
+    __syncthreads();  // every warp is done with its stages: reuse them for the merge
     float* mb = reinterpret_cast<float*>(work) + warp * kHeadsPad * PS;
     if (lg == 0) {
       mb[(2 * lt) * PS + 0] = st.m0;
@@ -821,7 +811,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
       const int h = idx / PS, e = idx % PS;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, all[(w * kHeadsPad + h) * PS]);
+      for (int w = 0; w < SM::NW; ++w) M = fmaxf(M, all[(w * kHeadsPad + h) * PS]);
       float v;
       if (e == 0) {
         v = M;
@@ -831,7 +821,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
         v = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-          for (int w = 0; w < kDecWarps; ++w) {
+          for (int w = 0; w < SM::NW; ++w) {
             const float mw = all[(w * kHeadsPad + h) * PS];
             v = fmaf(exp2f(mw - M), all[(w * kHeadsPad + h) * PS + e], v);
           }
@@ -842,7 +832,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
 
     // ---- the last block of this slab merges all its partials
     const int c_first = owner_block(slab_start, p.W, N);
-    const int c_last = owner_block(slab_start + L - 1, p.W, N);
+    const int c_last = owner_block(slab_start + ntb - 1, p.W, N);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -909,9 +899,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeP
       }
       if (threadIdx.x == 0) p.tickets[pair] = 0;
     }
-    __syncthreads();  // the merge area becomes the next segment's slots
+    __syncthreads();  // the merge area becomes the next segment's stages
     x = seg_end;
   }
+  if (timed_out) atomicExch(p.err, kErrWaitTimeout);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -933,7 +924,7 @@ struct LogitsSmem {
 };
 
 template <int KB, bool KQ, bool KH>
-__global__ void __launch_bounds__(kDecWarps * 32) logits_kernel(const LogitsParams p) {
+__global__ void __launch_bounds__(kLogitsWarps * 32) logits_kernel(const LogitsParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane >> 2, lt = lane & 3;
@@ -1006,7 +997,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) logits_kernel(const LogitsPara
   qu[1] = (KH && hv) ? qus[lg * 8 + lt + 4] : 0u;
 
   const int c1 = min(T, c0 + p.tokens_per_block);
-  const int per = ((c1 - c0 + kDecWarps - 1) / kDecWarps + kTile - 1) / kTile * kTile;
+  const int per = ((c1 - c0 + kLogitsWarps - 1) / kLogitsWarps + kTile - 1) / kTile * kTile;
   const int w0 = c0 + warp * per;
   const int w1 = min(c1, w0 + per);
   SlabPtrs sp;
@@ -1015,7 +1006,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) logits_kernel(const LogitsPara
     TileData<KB, KQ, KH, 1, false> d;
     load_ktile(d, sp, t0, w1 - 1, lg, lt);
     float s[4];
-    key_scores(d, s, qf, qs, qu, lutK, lane4, k_m0, p.qjl_scale);
+    key_scores(d, s, qf, qs, qu, (uint32_t)__cvta_generic_to_shared(lutK), lane4, k_m0, p.qjl_scale);
     const int tA = t0 + tile_row_token(lg), tB = t0 + tile_row_token(lg + 8);
     const long long r0 = ((long long)b * Hq + kvh * G + 2 * lt) * p.stride;
     const long long r1 = r0 + p.stride;
@@ -1038,7 +1029,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<KB, KQ, KH, VB, VQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM::bytes);
   if (e != cudaSuccess) return e;
-  decode_kernel<KB, KQ, KH, VB, VQ><<<grid, kDecWarps * 32, SM::bytes, s>>>(p);
+  decode_kernel<KB, KQ, KH, VB, VQ><<<grid, SM::NW * 32, SM::bytes, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -1048,7 +1039,7 @@ cudaError_t launch_logits_t(const LogitsParams& p, dim3 grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(logits_kernel<KB, KQ, KH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM::bytes);
   if (e != cudaSuccess) return e;
-  logits_kernel<KB, KQ, KH><<<grid, kDecWarps * 32, SM::bytes, s>>>(p);
+  logits_kernel<KB, KQ, KH><<<grid, kLogitsWarps * 32, SM::bytes, s>>>(p);
   return cudaGetLastError();
 }
 

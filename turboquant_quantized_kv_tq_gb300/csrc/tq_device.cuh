@@ -28,21 +28,25 @@ struct Tables {
   const float* U_rot; // [H_kv][d][r], R_K U
 };
 
-// The packed cache: region r of slab (b, h), token t at base + off[r] + ((b*H+h)*cap + t)*rec[r].
+// The packed cache in 16-token blocks: field r of token t of slab s = b * H + h at
+// base + side_off[side] + (s * tiles_per_slab + t / 16) * block[side] + off[r] + (t % 16) * rec[r].
 struct Cache {
   unsigned char* base;
-  unsigned long long off[tqi::R_COUNT];
+  unsigned long long side_off[2];
+  unsigned int block[2];
+  unsigned int off[tqi::R_COUNT];
   unsigned int rec[tqi::R_COUNT];
   int num_kv_heads;
-  int capacity;
+  int tiles_per_slab;
 
-  __device__ __forceinline__ unsigned char* ptr(int r, int b, int h, int t) const {
-    return base + off[r] +
-           ((unsigned long long)(b * num_kv_heads + h) * (unsigned long long)capacity + t) * rec[r];
+  // block `tile` of slab (b, h) on side 0 (K) or 1 (V)
+  __device__ __forceinline__ unsigned char* blockp(int side, int b, int h, int tile) const {
+    return base + side_off[side] +
+           ((unsigned long long)(b * num_kv_heads + h) * tiles_per_slab + tile) * block[side];
   }
-  __device__ __forceinline__ unsigned char* slab(int r, int b, int h) const {
-    return base + off[r] +
-           (unsigned long long)(b * num_kv_heads + h) * (unsigned long long)capacity * rec[r];
+  __device__ __forceinline__ unsigned char* ptr(int r, int b, int h, int t) const {
+    const int side = r >= tqi::R_V_CODES ? 1 : 0;
+    return blockp(side, b, h, t / tqi::kTileTokens) + off[r] + (t % tqi::kTileTokens) * rec[r];
   }
 };
 
@@ -67,11 +71,15 @@ inline Cache make_cache(const tq_context* ctx, const void* cache) {
   Cache c;
   c.base = (unsigned char*)cache;
   for (int r = 0; r < tqi::R_COUNT; ++r) {
-    c.off[r] = ctx->layout.off[r];
+    c.off[r] = (unsigned)ctx->layout.off[r];
     c.rec[r] = (unsigned)ctx->layout.rec[r];
   }
+  for (int s = 0; s < 2; ++s) {
+    c.side_off[s] = ctx->layout.side_off[s];
+    c.block[s] = (unsigned)ctx->layout.block[s];
+  }
   c.num_kv_heads = ctx->cfg.num_kv_heads;
-  c.capacity = ctx->cfg.capacity;
+  c.tiles_per_slab = (int)ctx->layout.tiles_per_slab;
   return c;
 }
 
@@ -195,6 +203,44 @@ __device__ __forceinline__ uint32_t ldg_stream2(const void* p) {
   unsigned short v;
   asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
+}
+
+// ---- mbarrier + bulk (TMA) copies global -> shared ----
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// Wait for the phase with the given parity to complete; gives up after `limit` polls and
+// returns false (the caller records an error instead of spinning forever).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // Bits of a 32-bit word rearranged: even bits to the low half, odd bits to the high half.

@@ -153,7 +153,8 @@ static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 Layout make_layout(const tq_config& cfg, int m) {
   Layout L;
-  const uint64_t slots = (uint64_t)cfg.batch * cfg.num_kv_heads * cfg.capacity;
+  L.tiles_per_slab = (uint64_t)cfg.capacity / kTileTokens;
+  const uint64_t blocks = (uint64_t)cfg.batch * cfg.num_kv_heads * L.tiles_per_slab;
   const uint64_t d = cfg.head_dim;
   uint64_t rec[R_COUNT] = {0};
   rec[R_K_CODES] = d * cfg.k.bits / 8;
@@ -163,13 +164,19 @@ Layout make_layout(const tq_config& cfg, int m) {
   rec[R_V_CODES] = d * cfg.v.bits / 8;
   rec[R_V_NORM] = 4;
   if (cfg.v.qjl) { rec[R_V_SIGNS] = m / 8; rec[R_V_RHO] = 2; }
-  uint64_t off = 0;
+  uint64_t in_block[2] = {0, 0};
   for (int r = 0; r < R_COUNT; ++r) {
     L.rec[r] = rec[r];
-    if (rec[r] == 0) { L.off[r] = 0; continue; }
+    const int side = region_side(r);
+    L.off[r] = rec[r] ? in_block[side] : 0;
+    in_block[side] += kTileTokens * rec[r];
+  }
+  uint64_t off = 0;
+  for (int side = 0; side < 2; ++side) {
     off = align_up(off, kRegionAlign);
-    L.off[r] = off;
-    off += slots * rec[r];
+    L.side_off[side] = off;
+    L.block[side] = in_block[side];
+    off += blocks * in_block[side];
   }
   L.total = off;
   return L;

@@ -25,11 +25,18 @@ struct TableOffsets {
   size_t k_signs, v_signs, s_k, s_k_t, s_v, s_v_t, headq_u, total;
 };
 
+// 16-token block layout: field r of token t of slab s at
+// side_off[side(r)] + (s * tiles_per_slab + t / 16) * block[side(r)] + off[r] + (t % 16) * rec[r].
 struct Layout {
-  uint64_t off[R_COUNT];
-  uint64_t rec[R_COUNT];
+  uint64_t off[R_COUNT];  // offset of the field inside its side's block
+  uint64_t rec[R_COUNT];  // bytes per token (0 = absent)
+  uint64_t side_off[2];   // K array, V array
+  uint64_t block[2];      // bytes per block
+  uint64_t tiles_per_slab;
   uint64_t total;
 };
+constexpr int kTileTokens = TQ_TILE_TOKENS;
+inline int region_side(int r) { return r >= R_V_CODES ? 1 : 0; }
 
 // Host tables: Beta Lloyd-Max codebook (float64) and SplitMix64-driven D and S.
 void lloyd_max_beta(int d, int bits, double* centroids, double* thresholds);
