@@ -209,6 +209,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const Appen
     float acc[E];
 #pragma unroll
     for (int q = 0; q < E; ++q) acc[q] = 0.f;
+    // several rows in flight per lane: the table is read from L2 and the loop is latency-bound
+    constexpr int kUnroll = E <= 8 ? 4 : 1;
+#pragma unroll kUnroll
     for (int jl = 0; jl < 32; ++jl) {
 #pragma unroll
       for (int e = 0; e < E; ++e) {

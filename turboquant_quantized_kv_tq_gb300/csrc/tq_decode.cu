@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
       make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
   if (p.kq) {
     float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4  // 16 rows of the L2-resident table in flight per lane
     for (int jl = 0; jl < 32; ++jl) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {

@@ -91,12 +91,17 @@ __device__ __forceinline__ void build_lut(unsigned char* lut, const float* cent)
   }
 }
 
-// Table word for index = byte j of w, for a table at shared address `lut`: byte offset
-// w.byte_j * 256 + lane * 4 (lane4 = lane * 4), read with a 32-bit shared-space load.
-__device__ __forceinline__ uint32_t lut_get(uint32_t lut, uint32_t w, uint32_t lane4, int j) {
-  const uint32_t off = __byte_perm(w, lane4, 0x5504u | ((uint32_t)j << 4));
+// Tables sit at fixed shared-window addresses that are multiples of 64 KiB, so the full address
+// of entry e for lane l, A + 256 e + 4 l, is one byte permute of the code word with
+// lx = A | 4 l (bytes: 4 l, e, A >> 16, 0), and a lookup is two instructions.
+constexpr uint32_t kLutAddrK = 0x10000u;  // key table (and the value table when shared)
+constexpr uint32_t kLutAddrV = 0x20000u;  // value table when its codebook differs
+constexpr uint32_t kDynBaseMax = 0x1000u; // highest dynamic shared-memory start the plan allows
+
+__device__ __forceinline__ uint32_t lut_get(uint32_t lx, uint32_t w, int j) {
+  const uint32_t addr = __byte_perm(w, lx, 0x7604u | ((uint32_t)j << 4));
   uint32_t v;
-  asm("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(lut + off));
+  asm("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
   return v;
 }
 
@@ -119,9 +124,9 @@ template <>
 struct KChunk<4> {
   uint4 c;
   __device__ __forceinline__ void prepare() {}
-  __device__ __forceinline__ uint32_t pair(uint32_t lut, uint32_t lane4, uint32_t, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t lx, uint32_t, int p) const {
     const uint32_t w = p < 4 ? c.x : p < 8 ? c.y : p < 12 ? c.z : c.w;
-    return lut_get(lut, w, lane4, p & 3);
+    return lut_get(lx, w, p & 3);
   }
 };
 
@@ -134,9 +139,9 @@ struct KChunk<3> {
     xe = nib_even(k.x); xo = nib_odd(k.x); ye = nib_even(k.y); yo = nib_odd(k.y);
     s = unshuffle_bits(s);
   }
-  __device__ __forceinline__ uint32_t pair(uint32_t lut, uint32_t lane4, uint32_t, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t lx, uint32_t, int p) const {
     const uint32_t w = p < 8 ? (p & 1 ? xo : xe) : (p & 1 ? yo : ye);
-    return signed_pair(lut_get(lut, w, lane4, (p & 7) >> 1), s << (15 - p));
+    return signed_pair(lut_get(lx, w, (p & 7) >> 1), s << (15 - p));
   }
 };
 
@@ -147,9 +152,9 @@ struct KChunk<2> {
   __device__ __forceinline__ void prepare() {
     xe = nib_even(k.x); xo = nib_odd(k.x); ye = nib_even(k.y); yo = nib_odd(k.y);
   }
-  __device__ __forceinline__ uint32_t pair(uint32_t lut, uint32_t lane4, uint32_t, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t lx, uint32_t, int p) const {
     const uint32_t w = p < 8 ? (p & 1 ? xo : xe) : (p & 1 ? yo : ye);
-    return lut_get(lut, w, lane4, (p & 7) >> 1);
+    return lut_get(lx, w, (p & 7) >> 1);
   }
 };
 
@@ -157,7 +162,7 @@ template <>
 struct KChunk<1> {
   uint32_t s;
   __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
-  __device__ __forceinline__ uint32_t pair(uint32_t, uint32_t, uint32_t m0, int p) const {
+  __device__ __forceinline__ uint32_t pair(uint32_t, uint32_t m0, int p) const {
     return signed_pair(m0, s << (15 - p));
   }
 };
@@ -190,13 +195,13 @@ struct VChunk<4> {
       o23[h] = ((c >> 4) & 0x0F0F0F0Fu) | (d & 0xF0F0F0F0u);
     }
   }
-  __device__ __forceinline__ void frag(uint32_t lut, uint32_t lane4, uint32_t, int mt,
+  __device__ __forceinline__ void frag(uint32_t lx, uint32_t, int mt,
                                        uint32_t (&a)[4]) const {
     const int h = mt >> 2, j = mt & 3;
-    a[0] = lut_get(lut, e01[h], lane4, j);
-    a[1] = lut_get(lut, o01[h], lane4, j);
-    a[2] = lut_get(lut, e23[h], lane4, j);
-    a[3] = lut_get(lut, o23[h], lane4, j);
+    a[0] = lut_get(lx, e01[h], j);
+    a[1] = lut_get(lx, o01[h], j);
+    a[2] = lut_get(lx, e23[h], j);
+    a[3] = lut_get(lx, o23[h], j);
   }
 };
 
@@ -214,12 +219,12 @@ struct Pair2 {
     e23[0] = nib_even(e1); e23[1] = nib_odd(e1);
     o23[0] = nib_even(o1); o23[1] = nib_odd(o1);
   }
-  __device__ __forceinline__ void mags(uint32_t lut, uint32_t lane4, int mt, uint32_t (&a)[4]) const {
+  __device__ __forceinline__ void mags(uint32_t lx, int mt, uint32_t (&a)[4]) const {
     const int h = mt & 1, j = mt >> 1;
-    a[0] = lut_get(lut, e01[h], lane4, j);
-    a[1] = lut_get(lut, o01[h], lane4, j);
-    a[2] = lut_get(lut, e23[h], lane4, j);
-    a[3] = lut_get(lut, o23[h], lane4, j);
+    a[0] = lut_get(lx, e01[h], j);
+    a[1] = lut_get(lx, o01[h], j);
+    a[2] = lut_get(lx, e23[h], j);
+    a[3] = lut_get(lx, o23[h], j);
   }
 };
 
@@ -244,9 +249,9 @@ struct VChunk<3> {
   Pair2 m;
   Bits16 sg;
   __device__ __forceinline__ void prepare() { m.build(k); sg.build(s); }
-  __device__ __forceinline__ void frag(uint32_t lut, uint32_t lane4, uint32_t, int mt,
+  __device__ __forceinline__ void frag(uint32_t lx, uint32_t, int mt,
                                        uint32_t (&a)[4]) const {
-    m.mags(lut, lane4, mt, a);
+    m.mags(lx, mt, a);
     sg.apply(mt, a);
   }
 };
@@ -256,9 +261,9 @@ struct VChunk<2> {
   uint32_t k[4];
   Pair2 m;
   __device__ __forceinline__ void prepare() { m.build(k); }
-  __device__ __forceinline__ void frag(uint32_t lut, uint32_t lane4, uint32_t, int mt,
+  __device__ __forceinline__ void frag(uint32_t lx, uint32_t, int mt,
                                        uint32_t (&a)[4]) const {
-    m.mags(lut, lane4, mt, a);
+    m.mags(lx, mt, a);
   }
 };
 
@@ -267,7 +272,7 @@ struct VChunk<1> {
   uint32_t s[4];
   Bits16 sg;
   __device__ __forceinline__ void prepare() { sg.build(s); }
-  __device__ __forceinline__ void frag(uint32_t, uint32_t, uint32_t m0, int mt, uint32_t (&a)[4]) const {
+  __device__ __forceinline__ void frag(uint32_t, uint32_t m0, int mt, uint32_t (&a)[4]) const {
     a[0] = a[1] = a[2] = a[3] = m0;
     sg.apply(mt, a);
   }
@@ -476,16 +481,16 @@ __device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, cons
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, float (&s)[4],
                                            const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                           const uint32_t (&qu)[2], uint32_t lutK,
-                                           uint32_t lane4, uint32_t k_m0, float qjl_scale) {
+                                           const uint32_t (&qu)[2], uint32_t lxK, uint32_t k_m0,
+                                           float qjl_scale) {
   d.kA.prepare();
   d.kB.prepare();
   // two independent accumulator chains (even / odd k-steps) halve the MMA dependency chain
   float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    mma16816(sc[ks & 1], d.kA.pair(lutK, lane4, k_m0, 2 * ks), d.kB.pair(lutK, lane4, k_m0, 2 * ks),
-             d.kA.pair(lutK, lane4, k_m0, 2 * ks + 1), d.kB.pair(lutK, lane4, k_m0, 2 * ks + 1), qf[2 * ks],
+    mma16816(sc[ks & 1], d.kA.pair(lxK, k_m0, 2 * ks), d.kB.pair(lxK, k_m0, 2 * ks),
+             d.kA.pair(lxK, k_m0, 2 * ks + 1), d.kB.pair(lxK, k_m0, 2 * ks + 1), qf[2 * ks],
              qf[2 * ks + 1]);
   }
   s[0] = (sc[0][0] + sc[1][0]) * d.nuKA;
@@ -548,14 +553,14 @@ __device__ __forceinline__ float ex2(float x) {
 template <int NT, int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ>& st,
                                               const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                              const uint32_t (&qu)[2], uint32_t lutK,
-                                              uint32_t lutV, uint32_t lane4, uint32_t k_m0,
+                                              const uint32_t (&qu)[2], uint32_t lxK,
+                                              uint32_t lxV, uint32_t k_m0,
                                               uint32_t v_m0, const DecodeParams& p, int t0, int end, int lg) {
   float s[NT][4];
   bool va[NT], vb[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    key_scores(d[j], s[j], qf, qs, qu, lutK, lane4, k_m0, p.qjl_scale);
+    key_scores(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale);
     va[j] = t0 + kTile * j + tile_row_token(lg) < end;
     vb[j] = t0 + kTile * j + tile_row_token(lg + 8) < end;
     s[j][0] = va[j] ? s[j][0] * p.score_scale : -INFINITY;
@@ -607,7 +612,7 @@ __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t a[4];
-      d[j].v.frag(lutV, lane4, v_m0, mt, a);
+      d[j].v.frag(lxV, v_m0, mt, a);
       mma16816(st.acc[mt], a[0], a[1], a[2], a[3], bv0, bv1);
     }
     if constexpr (VQ) {
@@ -625,17 +630,36 @@ __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[
   }
 }
 
+// Shared-memory plan of a decode block, in shared-window addresses.  The code tables sit at
+// kLutAddrK / kLutAddrV; per-warp regions (the warp's bulk-copy ring, later its merge slot) fill
+// [kDynBaseMax, kLutAddrK), then the gap between the key table and the value table (when there
+// is one), then the space after the last table; the mbarriers follow the last region.  The
+// dynamic allocation covers the window from 0 to `bytes`, whatever the start of dynamic shared
+// memory (at most kDynBaseMax, checked at run time).
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 struct DecodeSmem {
-  static constexpr int lutK = LutEntries<KB>::value * kLutStride;
-  static constexpr int lutV = KB == VB ? 0 : LutEntries<VB>::value * kLutStride;  // same codebook
+  static constexpr uint32_t lutK = LutEntries<KB>::value * kLutStride;
+  static constexpr uint32_t lutV = KB == VB ? 0 : LutEntries<VB>::value * kLutStride;  // same codebook
+  static constexpr bool sepV = lutV > 0;
   static constexpr int PS = 4 + kDecD + (VQ ? kDecD : 0);  // per head: m, l, pad, pad, acc, (acc_sk)
   static constexpr int NW = DecWarps<KQ, VQ>::value;
-  static constexpr int merge = NW * kHeadsPad * PS * 4;
-  static constexpr int stages = NW * kStages * Stage<KB, KQ, KH, VB, VQ>::bytes;
-  static constexpr int work = stages > merge ? stages : merge;
-  static constexpr int bars = NW * kStages * 8;
-  static constexpr int bytes = lutK + lutV + work + bars;
+  static constexpr uint32_t ring = kStages * Stage<KB, KQ, KH, VB, VQ>::bytes;
+  static constexpr uint32_t mslot = kHeadsPad * PS * 4;
+  static constexpr uint32_t RS = ring > mslot ? ring : mslot;
+  static constexpr uint32_t a0 = kDynBaseMax;
+  static constexpr int nA = (kLutAddrK - a0) / RS < (uint32_t)NW ? (int)((kLutAddrK - a0) / RS) : NW;
+  static constexpr uint32_t b0 = kLutAddrK + lutK;
+  static constexpr int nBmax = sepV ? (int)((kLutAddrV - b0) / RS) : NW;
+  static constexpr int nB = nBmax < NW - nA ? nBmax : NW - nA;
+  static constexpr uint32_t c0 = kLutAddrV + lutV;
+  static constexpr int nC = NW - nA - nB;
+  static constexpr uint32_t bars = sepV ? c0 + nC * RS : b0 + nB * RS;
+  static constexpr uint32_t bytes = bars + NW * kStages * 8;
+  static_assert(RS % 16 == 0, "regions must keep 16-byte alignment");
+  static_assert(lutK <= kLutAddrV - kLutAddrK, "key table overlaps the value table");
+  __host__ __device__ static constexpr uint32_t region(int w) {
+    return w < nA ? a0 + w * RS : (w < nA + nB ? b0 + (w - nA) * RS : c0 + (w - nA - nB) * RS);
+  }
 };
 
 // Owner block of flattened tile x: the largest c with floor(c W / N) <= x.
@@ -645,6 +669,7 @@ __device__ __forceinline__ int owner_block(long long x, long long W, int N) {
 
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls of an mbarrier before giving up
 constexpr int kErrWaitTimeout = 1;
+constexpr int kErrSmemPlan = 2;
 
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel(const DecodeParams p) {
@@ -655,25 +680,27 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane >> 2, lt = lane & 3;
-  const uint32_t lane4 = 4u * lane;
 
-  unsigned char* lutK = smem;
-  unsigned char* lutV = KB == VB ? smem : smem + SM::lutK;
-  unsigned char* work = smem + SM::lutK + SM::lutV;
-  unsigned char* bars = work + SM::work;
-  if constexpr (KB != 1) build_lut<KB>(lutK, p.tab.k_c);
-  if constexpr (VB != 1 && VB != KB) build_lut<VB>(lutV, p.tab.v_c);
+  // generic pointer of shared-window address a
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  if (sbase > kDynBaseMax) {  // the plan does not fit this launch: report, do nothing
+    if (threadIdx.x == 0) atomicExch(p.err, kErrSmemPlan);
+    return;
+  }
+  unsigned char* const win = smem - sbase;
+  if constexpr (KB != 1) build_lut<KB>(win + kLutAddrK, p.tab.k_c);
+  if constexpr (SM::sepV && VB != 1) build_lut<VB>(win + kLutAddrV, p.tab.v_c);
   const uint32_t k_m0 = pack_half2(__ldg(p.tab.k_c + 1), __ldg(p.tab.k_c + 1));
   const uint32_t v_m0 = pack_half2(__ldg(p.tab.v_c + 1), __ldg(p.tab.v_c + 1));
-  const uint32_t my_bars = (uint32_t)__cvta_generic_to_shared(bars) + warp * kStages * 8;
-  const uint32_t lutK_s = (uint32_t)__cvta_generic_to_shared(lutK);
-  const uint32_t lutV_s = (uint32_t)__cvta_generic_to_shared(lutV);
+  const uint32_t lxK = kLutAddrK | (4u * lane);
+  const uint32_t lxV = (SM::sepV ? kLutAddrV : kLutAddrK) | (4u * lane);
+  const uint32_t my_bars = SM::bars + warp * kStages * 8;
   if (lane < kStages) mbar_init(my_bars + 8 * lane, 1);
   fence_mbar_init();
   __syncthreads();
 
-  unsigned char* my_stages = work + warp * kStages * SG::bytes;
-  const uint32_t my_stages_s = (uint32_t)__cvta_generic_to_shared(my_stages);
+  const uint32_t my_stages_s = SM::region(warp);
+  unsigned char* my_stages = win + my_stages_s;
   const int G = p.G;
   const int Hq = p.Hkv * G;
   const int N = p.nblocks;
@@ -769,9 +796,9 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
         }
       }
       if (two)
-        compute_tiles<2>(d, st, qf, qs, qu, lutK_s, lutV_s, lane4, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
+        compute_tiles<2>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
       else
-        compute_tiles<1>(d, st, qf, qs, qu, lutK_s, lutV_s, lane4, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
+        compute_tiles<1>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
     }
     seq += nt;
 
@@ -783,7 +810,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
       l1 += __shfl_xor_sync(kFull, l1, m);
     }
     __syncthreads();  // every warp is done with its stages: reuse them for the merge
-    float* mb = reinterpret_cast<float*>(work) + warp * kHeadsPad * PS;
+    float* mb = reinterpret_cast<float*>(my_stages);
     if (lg == 0) {
       mb[(2 * lt) * PS + 0] = st.m0;
       mb[(2 * lt) * PS + 1] = l0;
@@ -805,13 +832,12 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
       }
     }
     __syncthreads();
-    const float* all = reinterpret_cast<const float*>(work);
     float* part_out = p.part + ((long long)(pair + blockIdx.x) * kHeadsPad) * PS;
     for (int idx = threadIdx.x; idx < G * PS; idx += blockDim.x) {
       const int h = idx / PS, e = idx % PS;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < SM::NW; ++w) M = fmaxf(M, all[(w * kHeadsPad + h) * PS]);
+      for (int w = 0; w < SM::NW; ++w) M = fmaxf(M, reinterpret_cast<const float*>(win + SM::region(w))[h * PS]);
       float v;
       if (e == 0) {
         v = M;
@@ -822,8 +848,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
         if (M != -INFINITY) {
 #pragma unroll
           for (int w = 0; w < SM::NW; ++w) {
-            const float mw = all[(w * kHeadsPad + h) * PS];
-            v = fmaf(exp2f(mw - M), all[(w * kHeadsPad + h) * PS + e], v);
+            const float* mbw = reinterpret_cast<const float*>(win + SM::region(w)) + h * PS;
+            v = fmaf(exp2f(mbw[0] - M), mbw[e], v);
           }
         }
       }
@@ -917,10 +943,13 @@ struct LogitsParams {
   int seq_len[TQ_MAX_BATCH];
 };
 
+// Query buffers at the start of dynamic shared memory; the key table at kLutAddrK.
 template <int KB>
 struct LogitsSmem {
-  static constexpr int lut = LutEntries<KB>::value * kLutStride;
-  static constexpr int bytes = lut + (kHeadsPad * (kDecD / 2) * 2 + kHeadsPad * 8) * 4;
+  static constexpr uint32_t lut = LutEntries<KB>::value * kLutStride;
+  static constexpr uint32_t qbytes = (kHeadsPad * (kDecD / 2) * 2 + kHeadsPad * 8) * 4;
+  static constexpr uint32_t bytes = KB == 1 ? qbytes : kLutAddrK + lut;
+  static_assert(kDynBaseMax + qbytes <= kLutAddrK, "query buffers overlap the key table");
 };
 
 template <int KB, bool KQ, bool KH>
@@ -928,17 +957,19 @@ __global__ void __launch_bounds__(kLogitsWarps * 32) logits_kernel(const LogitsP
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane >> 2, lt = lane & 3;
-  const uint32_t lane4 = 4u * lane;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int T = p.seq_len[b];
   const int c0 = blockIdx.x * p.tokens_per_block;
   if (c0 >= T) return;  // the whole block leaves together
   const int G = p.G, Hq = p.Hkv * G;
-  unsigned char* lutK = smem;
-  uint32_t* qrot = reinterpret_cast<uint32_t*>(smem + LogitsSmem<KB>::lut);
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  if (sbase > kDynBaseMax) {  // cannot happen with the documented limits; nothing is written
+    return;
+  }
+  uint32_t* qrot = reinterpret_cast<uint32_t*>(smem);
   uint32_t* qsk = qrot + kHeadsPad * (kDecD / 2);
   uint32_t* qus = qsk + kHeadsPad * (kDecD / 2);
-  if constexpr (KB != 1) build_lut<KB>(lutK, p.tab.k_c);
+  if constexpr (KB != 1) build_lut<KB>(smem - sbase + kLutAddrK, p.tab.k_c);
   const uint32_t k_m0 = pack_half2(__ldg(p.tab.k_c + 1), __ldg(p.tab.k_c + 1));
   if (warp < G) {
     const float4 q4 = *reinterpret_cast<const float4*>(p.q + ((long long)b * Hq + kvh * G + warp) * kDecD + 4 * lane);
@@ -1006,7 +1037,7 @@ __global__ void __launch_bounds__(kLogitsWarps * 32) logits_kernel(const LogitsP
     TileData<KB, KQ, KH, 1, false> d;
     load_ktile(d, sp, t0, w1 - 1, lg, lt);
     float s[4];
-    key_scores(d, s, qf, qs, qu, (uint32_t)__cvta_generic_to_shared(lutK), lane4, k_m0, p.qjl_scale);
+    key_scores(d, s, qf, qs, qu, kLutAddrK | (4u * lane), k_m0, p.qjl_scale);
     const int tA = t0 + tile_row_token(lg), tB = t0 + tile_row_token(lg + 8);
     const long long r0 = ((long long)b * Hq + kvh * G + 2 * lt) * p.stride;
     const long long r1 = r0 + p.stride;
@@ -1021,13 +1052,29 @@ __global__ void __launch_bounds__(kLogitsWarps * 32) logits_kernel(const LogitsP
   }
 }
 
+// Host check of the shared-memory plans: dynamic shared memory starts after the reserved and
+// static shared memory, which must stay below kDynBaseMax.
+template <typename K>
+cudaError_t check_dyn_base(K kernel) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  int dev = 0, reserved = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
+    return e;
+  return (size_t)reserved + fa.sharedSizeBytes <= kDynBaseMax ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 // Launch helpers used by the per-bit-width instantiation units.
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
   using SM = DecodeSmem<KB, KQ, KH, VB, VQ>;
   static_assert(SM::bytes <= 227 * 1024, "decode shared memory exceeds the per-block limit");
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<KB, KQ, KH, VB, VQ>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SM::bytes);
+  cudaError_t e = check_dyn_base(decode_kernel<KB, KQ, KH, VB, VQ>);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_kernel<KB, KQ, KH, VB, VQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)SM::bytes);
   if (e != cudaSuccess) return e;
   decode_kernel<KB, KQ, KH, VB, VQ><<<grid, SM::NW * 32, SM::bytes, s>>>(p);
   return cudaGetLastError();
@@ -1036,8 +1083,10 @@ cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
 template <int KB, bool KQ, bool KH>
 cudaError_t launch_logits_t(const LogitsParams& p, dim3 grid, cudaStream_t s) {
   using SM = LogitsSmem<KB>;
-  cudaError_t e = cudaFuncSetAttribute(logits_kernel<KB, KQ, KH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SM::bytes);
+  cudaError_t e = check_dyn_base(logits_kernel<KB, KQ, KH>);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(logits_kernel<KB, KQ, KH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)SM::bytes);
   if (e != cudaSuccess) return e;
   logits_kernel<KB, KQ, KH><<<grid, kLogitsWarps * 32, SM::bytes, s>>>(p);
   return cudaGetLastError();
