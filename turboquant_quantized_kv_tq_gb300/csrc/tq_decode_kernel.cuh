@@ -20,9 +20,10 @@
 //   scores  S[16 tok x 8 heads] = K_hat[16 x 128] Q[128 x 8]   (8 mma.m16n8k16)
 //   readout O^T[128 dims x 8 heads] += V_hat^T[128 x 16] P[16 x 8]  (8 mma), P moved from the
 //           score accumulator layout to the B operand layout with movmatrix.trans.
-// Loads: each warp streams its tiles through a ring of kStages shared-memory stages; a stage is
-// one 16-token K block followed by one V block of the cache (two bulk copies, completing on the
-// stage's mbarrier), refilled as soon as its operands are in registers.  Codes become fp16 pairs
+// Loads: each warp streams its tiles, two at a time, through a ring of two shared-memory stages;
+// a stage holds two adjacent 16-token K blocks and the two matching V blocks of the cache (one
+// bulk copy per side, completing on the stage's mbarrier) and is refilled as soon as its
+// operands are in registers.  Codes become fp16 pairs
 // through lane-replicated tables (entry e, lane l at byte 256 e + 4 l, the address built by one
 // byte permute) or, for sign bits, by moving the bit to the fp16 sign position.  Token order
 // inside a tile is permuted so each thread's value operands come from four consecutive tokens:
@@ -43,7 +44,7 @@ template <bool KQ, bool VQ>
 struct DecWarps { static constexpr int value = (KQ || VQ) ? 12 : 16; };
 constexpr int kTile = 16;
 constexpr int kHeadsPad = 8;
-constexpr int kStages = 4;
+constexpr int kPairStages = 2;  // per-warp ring of 32-token (two-tile) stages
 constexpr int kMaxBlocks = 256;  // partial slots reserved for blocks (>= SM count)
 constexpr int kLutStride = 256;  // bytes between table entries
 
@@ -351,16 +352,20 @@ struct Stage {
   static constexpr int copies = 4 + (KQ ? 2 : 0) + (KH ? 2 : 0) + (VQ ? 2 : 0);
 };
 
-// Start the bulk copies of tile `tile` (tokens [16 tile, 16 tile + 16) of the slab) into the
-// stage at shared address `st`: lane 0 registers the byte count on `bar`, then lane 0 copies
-// the K block and lane 1 the V block (a stage is exactly a K block followed by a V block).
+// Start the bulk copies of tiles [tile, tile + nt) (nt = 1 or 2: adjacent 16-token blocks of the
+// slab, so each side is one contiguous copy) into the pair stage at shared address `st`: K blocks
+// at st, V blocks at st + 2 * (K block bytes).  Lane 0 registers the byte count on `bar` and
+// issues both copies.
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void issue_stage(uint32_t st, uint32_t bar, const SlabPtrs& s, int tile, int lane) {
+__device__ __forceinline__ void issue_pair(uint32_t st, uint32_t bar, const SlabPtrs& s, int tile, int nt,
+                                           int lane) {
   using S = Stage<KB, KQ, KH, VB, VQ>;
-  if (lane == 0) mbar_arrive_expect_tx(bar, S::bytes);
-  __syncwarp();
-  if (lane == 0) bulk_g2s(st, s.kb + (unsigned long long)tile * s.kbytes, S::VC, bar);
-  if (lane == 1) bulk_g2s(st + S::VC, s.vb + (unsigned long long)tile * s.vbytes, S::bytes - S::VC, bar);
+  constexpr uint32_t KBL = S::VC, VBL = S::bytes - S::VC;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)nt * (KBL + VBL));
+    bulk_g2s(st, s.kb + (unsigned long long)tile * KBL, (uint32_t)nt * KBL, bar);
+    bulk_g2s(st + 2 * KBL, s.vb + (unsigned long long)tile * VBL, (uint32_t)nt * VBL, bar);
+  }
 }
 
 __device__ __forceinline__ float lds_f32(const unsigned char* p) { return *reinterpret_cast<const float*>(p); }
@@ -371,10 +376,11 @@ __device__ __forceinline__ uint32_t lds_u16(const unsigned char* p) {
   return *reinterpret_cast<const unsigned short*>(p);
 }
 
-// Read this thread's operands of one tile from its warp's stage.
+// Read this thread's operands of one tile from its warp's stage: the tile's K block at `st`, its
+// V block at `vst` + S::VC (V field offsets of a 16-token stage are relative to `vst`).
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, const unsigned char* st, int lg,
-                                           int lt) {
+__device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, const unsigned char* st,
+                                           const unsigned char* vst, int lg, int lt) {
   using S = Stage<KB, KQ, KH, VB, VQ>;
   constexpr int KR = KRec<KB>::value, VR = KRec<VB>::value;
   const int rA = tile_row_token(lg), rB = tile_row_token(lg + 8);
@@ -412,7 +418,7 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const unsigned char* v = st + S::VC + (4 * lt + j) * VR;
+    const unsigned char* v = vst + S::VC + (4 * lt + j) * VR;
     if constexpr (VB == 4) {
       d.v.w[j] = *reinterpret_cast<const uint2*>(v + 8 * lg);
     } else if constexpr (VB == 3) {
@@ -423,13 +429,13 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
     } else {
       d.v.s[j] = lds_u16(v + 2 * lg);
     }
-    if constexpr (VQ) d.vs.s[j] = lds_u16(st + S::VS + (4 * lt + j) * (kDecD / 8) + 2 * lg);
+    if constexpr (VQ) d.vs.s[j] = lds_u16(vst + S::VS + (4 * lt + j) * (kDecD / 8) + 2 * lg);
   }
-  d.nuVA = lds_f32(st + S::VN + 4 * rA);
-  d.nuVB = lds_f32(st + S::VN + 4 * rB);
+  d.nuVA = lds_f32(vst + S::VN + 4 * rA);
+  d.nuVB = lds_f32(vst + S::VN + 4 * rB);
   if constexpr (VQ) {
-    d.rhoVA = lds_f16(st + S::VRH + 2 * rA);
-    d.rhoVB = lds_f16(st + S::VRH + 2 * rB);
+    d.rhoVA = lds_f16(vst + S::VRH + 2 * rA);
+    d.rhoVB = lds_f16(vst + S::VRH + 2 * rB);
   }
 }
 
@@ -475,14 +481,14 @@ __device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, cons
   }
 }
 
-// Unscaled key scores of the thread's four accumulator slots (tokens pi(lg), pi(lg+8) x heads
-// 2 lt, 2 lt + 1): nu <q_rot, C[c]> (+ nu rho sqrt(pi/2)/m <S q_rot, 2 sigma - 1>)
-// (+ scale <U^T q, zeta>).  Multiply by 1/sqrt(d) for the logit.
+// Key scores of the thread's four accumulator slots (tokens pi(lg), pi(lg+8) x heads 2 lt,
+// 2 lt + 1), times `sscale`: nu <q_rot, C[c]> (+ nu rho sqrt(pi/2)/m <S q_rot, 2 sigma - 1>)
+// (+ scale <U^T q, zeta>).  sscale = 1/sqrt(d) gives the logit.
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, float (&s)[4],
                                            const uint32_t (&qf)[16], const uint32_t (&qs)[16],
                                            const uint32_t (&qu)[2], uint32_t lxK, uint32_t k_m0,
-                                           float qjl_scale) {
+                                           float qjl_scale, float sscale) {
   d.kA.prepare();
   d.kB.prepare();
   // two independent accumulator chains (even / odd k-steps) halve the MMA dependency chain
@@ -493,10 +499,11 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
              d.kA.pair(lxK, k_m0, 2 * ks + 1), d.kB.pair(lxK, k_m0, 2 * ks + 1), qf[2 * ks],
              qf[2 * ks + 1]);
   }
-  s[0] = (sc[0][0] + sc[1][0]) * d.nuKA;
-  s[1] = (sc[0][1] + sc[1][1]) * d.nuKA;
-  s[2] = (sc[0][2] + sc[1][2]) * d.nuKB;
-  s[3] = (sc[0][3] + sc[1][3]) * d.nuKB;
+  const float nA = d.nuKA * sscale, nB = d.nuKB * sscale;
+  s[0] = (sc[0][0] + sc[1][0]) * nA;
+  s[1] = (sc[0][1] + sc[1][1]) * nA;
+  s[2] = (sc[0][2] + sc[1][2]) * nB;
+  s[3] = (sc[0][3] + sc[1][3]) * nB;
   if constexpr (KQ) {
     d.sA.prepare();
     d.sB.prepare();
@@ -506,7 +513,7 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
       mma16816(sq, d.sA.pair(2 * ks), d.sB.pair(2 * ks), d.sA.pair(2 * ks + 1), d.sB.pair(2 * ks + 1),
                qs[2 * ks], qs[2 * ks + 1]);
     }
-    const float fa = d.nuKA * d.rhoKA * qjl_scale, fb = d.nuKB * d.rhoKB * qjl_scale;
+    const float fa = nA * d.rhoKA * qjl_scale, fb = nB * d.rhoKB * qjl_scale;
     s[0] = fmaf(sq[0], fa, s[0]);
     s[1] = fmaf(sq[1], fa, s[1]);
     s[2] = fmaf(sq[2], fb, s[2]);
@@ -515,10 +522,11 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
   if constexpr (KH) {
     float sz[4] = {0.f, 0.f, 0.f, 0.f};
     mma16816(sz, side_pair(d.zA.x), side_pair(d.zB.x), side_pair(d.zA.y), side_pair(d.zB.y), qu[0], qu[1]);
-    s[0] = fmaf(sz[0], d.zsA, s[0]);
-    s[1] = fmaf(sz[1], d.zsA, s[1]);
-    s[2] = fmaf(sz[2], d.zsB, s[2]);
-    s[3] = fmaf(sz[3], d.zsB, s[3]);
+    const float zA = d.zsA * sscale, zB = d.zsB * sscale;
+    s[0] = fmaf(sz[0], zA, s[0]);
+    s[1] = fmaf(sz[1], zA, s[1]);
+    s[2] = fmaf(sz[2], zB, s[2]);
+    s[3] = fmaf(sz[3], zB, s[3]);
   }
 }
 
@@ -549,8 +557,9 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// NT consecutive tiles (starting at token t0) through one online-softmax step.
-template <int NT, int KB, bool KQ, bool KH, int VB, bool VQ>
+// NT consecutive tiles (starting at token t0) through one online-softmax step.  MASK = false
+// when every token of the NT tiles is below `end`.
+template <int NT, bool MASK, int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ>& st,
                                               const uint32_t (&qf)[16], const uint32_t (&qs)[16],
                                               const uint32_t (&qu)[2], uint32_t lxK,
@@ -560,13 +569,15 @@ __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[
   bool va[NT], vb[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    key_scores(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale);
-    va[j] = t0 + kTile * j + tile_row_token(lg) < end;
-    vb[j] = t0 + kTile * j + tile_row_token(lg + 8) < end;
-    s[j][0] = va[j] ? s[j][0] * p.score_scale : -INFINITY;
-    s[j][1] = va[j] ? s[j][1] * p.score_scale : -INFINITY;
-    s[j][2] = vb[j] ? s[j][2] * p.score_scale : -INFINITY;
-    s[j][3] = vb[j] ? s[j][3] * p.score_scale : -INFINITY;
+    key_scores(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale);
+    va[j] = !MASK || t0 + kTile * j + tile_row_token(lg) < end;
+    vb[j] = !MASK || t0 + kTile * j + tile_row_token(lg + 8) < end;
+    if constexpr (MASK) {
+      s[j][0] = va[j] ? s[j][0] : -INFINITY;
+      s[j][1] = va[j] ? s[j][1] : -INFINITY;
+      s[j][2] = vb[j] ? s[j][2] : -INFINITY;
+      s[j][3] = vb[j] ? s[j][3] : -INFINITY;
+    }
   }
 
   // ---- online softmax (log2 domain)
@@ -643,7 +654,7 @@ struct DecodeSmem {
   static constexpr bool sepV = lutV > 0;
   static constexpr int PS = 4 + kDecD + (VQ ? kDecD : 0);  // per head: m, l, pad, pad, acc, (acc_sk)
   static constexpr int NW = DecWarps<KQ, VQ>::value;
-  static constexpr uint32_t ring = kStages * Stage<KB, KQ, KH, VB, VQ>::bytes;
+  static constexpr uint32_t ring = kPairStages * 2 * Stage<KB, KQ, KH, VB, VQ>::bytes;
   static constexpr uint32_t mslot = kHeadsPad * PS * 4;
   static constexpr uint32_t RS = ring > mslot ? ring : mslot;
   static constexpr uint32_t a0 = kDynBaseMax;
@@ -654,7 +665,7 @@ struct DecodeSmem {
   static constexpr uint32_t c0 = kLutAddrV + lutV;
   static constexpr int nC = NW - nA - nB;
   static constexpr uint32_t bars = sepV ? c0 + nC * RS : b0 + nB * RS;
-  static constexpr uint32_t bytes = bars + NW * kStages * 8;
+  static constexpr uint32_t bytes = bars + NW * kPairStages * 8;
   static_assert(RS % 16 == 0, "regions must keep 16-byte alignment");
   static_assert(lutK <= kLutAddrV - kLutAddrK, "key table overlaps the value table");
   __host__ __device__ static constexpr uint32_t region(int w) {
@@ -694,8 +705,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
   const uint32_t v_m0 = pack_half2(__ldg(p.tab.v_c + 1), __ldg(p.tab.v_c + 1));
   const uint32_t lxK = kLutAddrK | (4u * lane);
   const uint32_t lxV = (SM::sepV ? kLutAddrV : kLutAddrK) | (4u * lane);
-  const uint32_t my_bars = SM::bars + warp * kStages * 8;
-  if (lane < kStages) mbar_init(my_bars + 8 * lane, 1);
+  const uint32_t my_bars = SM::bars + warp * kPairStages * 8;
+  if (lane < kPairStages) mbar_init(my_bars + 8 * lane, 1);
   fence_mbar_init();
   __syncthreads();
 
@@ -706,7 +717,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
   const int N = p.nblocks;
   long long x = (long long)blockIdx.x * p.W / N;
   const long long x_end = (long long)(blockIdx.x + 1) * p.W / N;
-  unsigned seq = 0;  // tiles this warp has streamed so far: stage seq % S, phase (seq / S) & 1
+  unsigned seq = 0;  // tile pairs this warp has streamed so far: stage seq % S, phase (seq / S) & 1
   bool timed_out = false;
 
   while (x < x_end) {
@@ -765,42 +776,42 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
     sp.init(p.cache, b, kvh);
     WarpState<VQ> st;
     st.reset();
-    // all kStages stages in flight; tiles are consumed two at a time, and a pair's stages are
-    // refilled as soon as its operands are in registers, before the pair is computed
+    // both pair stages in flight; a pair stage is refilled as soon as its operands are in
+    // registers, before the pair is computed
+    constexpr uint32_t KBL = SG::VC, VBL = SG::bytes - SG::VC, PB = 2 * SG::bytes;
+    const int npairs = (nt + 1) >> 1;
 #pragma unroll
-    for (int i = 0; i < kStages; ++i) {
-      if (i < nt) {
-        const unsigned sl = (seq + i) % kStages;
-        issue_stage<KB, KQ, KH, VB, VQ>(my_stages_s + sl * SG::bytes, my_bars + 8 * sl, sp, m0t + i, lane);
+    for (int k = 0; k < kPairStages; ++k) {
+      if (k < npairs) {
+        const unsigned sl = (seq + k) % kPairStages;
+        issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
+                                       min(2, nt - 2 * k), lane);
       }
     }
-    for (int i = 0; i < nt; i += 2) {
-      const bool two = i + 1 < nt;
+    for (int k = 0; k < npairs; ++k) {
+      const unsigned cur = seq + k, sl = cur % kPairStages;
+      const bool two = 2 * k + 1 < nt;
+      if (!mbar_wait(my_bars + 8 * sl, (cur / kPairStages) & 1u, kWaitLimit)) timed_out = true;
+      const unsigned char* stg = my_stages + sl * PB;
       TileData<KB, KQ, KH, VB, VQ> d[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        if (j == 0 || two) {
-          const unsigned cur = seq + i + j;
-          if (!mbar_wait(my_bars + 8 * (cur % kStages), (cur / kStages) & 1u, kWaitLimit)) timed_out = true;
-          read_stage(d[j], my_stages + (cur % kStages) * SG::bytes, lg, lt);
-        }
-      }
-      __syncwarp();  // every lane has read the pair's stages
+      read_stage(d[0], stg, stg + 2 * KBL - SG::VC, lg, lt);
+      if (two) read_stage(d[1], stg + KBL, stg + 2 * KBL + VBL - SG::VC, lg, lt);
+      __syncwarp();  // every lane has read the stage
       fence_proxy_async_shared();
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int nx = i + j + kStages;
-        if (nx < nt) {
-          const unsigned sl = (seq + nx) % kStages;
-          issue_stage<KB, KQ, KH, VB, VQ>(my_stages_s + sl * SG::bytes, my_bars + 8 * sl, sp, m0t + nx, lane);
-        }
+      if (k + kPairStages < npairs)
+        issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * (k + kPairStages),
+                                       min(2, nt - 2 * (k + kPairStages)), lane);
+      const int t0 = (m0t + 2 * k) * kTile;
+      if (two) {
+        if (t0 + 2 * kTile <= L)
+          compute_tiles<2, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+        else
+          compute_tiles<2, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+      } else {
+        compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
       }
-      if (two)
-        compute_tiles<2>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
-      else
-        compute_tiles<1>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, (m0t + i) * kTile, L, lg);
     }
-    seq += nt;
+    seq += npairs;
 
     // ---- merge the warps of this block for this segment
     float l0 = st.l0, l1 = st.l1;
@@ -1037,17 +1048,17 @@ __global__ void __launch_bounds__(kLogitsWarps * 32) logits_kernel(const LogitsP
     TileData<KB, KQ, KH, 1, false> d;
     load_ktile(d, sp, t0, w1 - 1, lg, lt);
     float s[4];
-    key_scores(d, s, qf, qs, qu, kLutAddrK | (4u * lane), k_m0, p.qjl_scale);
+    key_scores(d, s, qf, qs, qu, kLutAddrK | (4u * lane), k_m0, p.qjl_scale, p.inv_sqrt_d);
     const int tA = t0 + tile_row_token(lg), tB = t0 + tile_row_token(lg + 8);
     const long long r0 = ((long long)b * Hq + kvh * G + 2 * lt) * p.stride;
     const long long r1 = r0 + p.stride;
     if (tA < w1) {
-      if (2 * lt < G) p.logits[r0 + tA] = s[0] * p.inv_sqrt_d;
-      if (2 * lt + 1 < G) p.logits[r1 + tA] = s[1] * p.inv_sqrt_d;
+      if (2 * lt < G) p.logits[r0 + tA] = s[0];
+      if (2 * lt + 1 < G) p.logits[r1 + tA] = s[1];
     }
     if (tB < w1) {
-      if (2 * lt < G) p.logits[r0 + tB] = s[2] * p.inv_sqrt_d;
-      if (2 * lt + 1 < G) p.logits[r1 + tB] = s[3] * p.inv_sqrt_d;
+      if (2 * lt < G) p.logits[r0 + tB] = s[2];
+      if (2 * lt + 1 < G) p.logits[r1 + tB] = s[3];
     }
   }
 }
