@@ -74,6 +74,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, device=None):
+    """The largest of every rank's ``value`` (the job's time is its slowest rank's); the value
+    itself when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank_step, world, ms_per_step):
+    """Units all ranks processed per second: every rank does the same work per step (weak
+    scaling), and a step lasts as long as the slowest rank's."""
+    return world * units_per_rank_step / (ms_per_step * 1e-3)
+
+
 def record_bytes(scheme, n, d=128, m=128):
     """Packed bytes of one cache record (K and V of one token of one slab)."""
     from turboquant_quantized_kv_tq_gb300.binding import SCHEMES as S, tq_config, tq_config_from_scheme
@@ -222,13 +240,10 @@ def run_gpu(args):
         for i in range(n_dec):
             dec_ms[i] += evs[i][0].elapsed_time(evs[i][1])
     dec_ms = [x / args.steps for x in dec_ms]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, device)
     ms_per_step = total_ms / args.steps
     tokens_per_step = n_dec * B * Hkv * T
-    value = world * tokens_per_step / (ms_per_step * 1e-3)
+    value = whole_job_value(tokens_per_step, world, ms_per_step)
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, caches, inp, device, seq, start)

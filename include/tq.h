@@ -137,9 +137,12 @@ size_t tq_tables_bytes(const tq_context* ctx);
 
 /* Copy the host-built table blob (the same bytes tq_tables_upload sends) into host memory.
  * Host only.  Blob layout: fp32 k_centroids[16], k_thresholds[16], v_centroids[16],
- * v_thresholds[16]; fp32 k_signs[d], v_signs[d] (+1/-1); fp32 S_K[m][d] (if K has QJL);
- * fp32 S_V[m][d] (if V has QJL); then the HeadQ basis area [H_kv][d][r] (zeros until
- * tq_headq_set_basis).  Each array starts on a 256-byte boundary. */
+ * v_thresholds[16]; fp32 k_signs[d], v_signs[d] (+1/-1); fp32 S_K[m][d] and its transpose
+ * [d][m] (if K has QJL); fp32 S_V[m][d] and its transpose (if V has QJL); the HeadQ basis area
+ * [H_kv][d][r] (zeros until tq_headq_set_basis); and, when d > 128 and V has QJL, fp32
+ * S_V R_V [m][d] (R_V = H D_V / sqrt(d), each row rounded once from a float64 transform), which
+ * maps the value sketch accumulator straight to the output domain.  Each array starts on a
+ * 256-byte boundary. */
 tq_status tq_tables_host(const tq_context* ctx, void* host_dst, size_t bytes);
 
 /* Copy the tables into dev_tables (tq_tables_bytes bytes, caller-owned, 256-byte aligned) on

@@ -134,9 +134,9 @@ def rel_err(out, ref):
     return float(np.max(r))
 
 
-def small_inputs(name, B=2, T=300, Hkv=2, Hq=None, seed=None):
+def small_inputs(name, B=2, T=300, Hkv=2, Hq=None, seed=None, d=None):
     from turboquant_quantized_kv_tq_gb300.workloads import CONFIGS
     c = CONFIGS[name]
     G = c["Hq"] // c["Hkv"]
     Hq = Hq if Hq is not None else G * Hkv
-    return make_inputs(name, B=B, T=T, Hkv=Hkv, Hq=Hq, seed=seed)
+    return make_inputs(name, B=B, T=T, Hkv=Hkv, Hq=Hq, seed=seed, d=d)

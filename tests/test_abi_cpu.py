@@ -178,3 +178,22 @@ def test_layout_matches_oracle(scheme, n, headq):
         else:
             assert r.record_bytes == 0, name
     b.tq_context_destroy(ctx)
+
+
+@pytest.mark.parametrize("d", [256, 1024])
+def test_value_sketch_output_domain_table(d):
+    # head dims above 128 with a QJL value side carry S_V R_V after the other arrays
+    from oracle import rotation
+    c = _cfg(d=d, scheme="kqv", n=4, seed=5)
+    ctx = _ctx(c)
+    blob = _blob(ctx)
+    off = _offsets(d, d, 0, 1, 2, 0)
+    start = (off["S_V_T"] + 4 * d * d + 255) // 256 * 256
+    assert b.tq_tables_bytes(ctx) >= start + 4 * d * d
+    T = blob[start:start + 4 * d * d].view(np.float32).reshape(d, d).astype(np.float64)
+    SV = tables.sketch_matrix(5, tables.STREAM_S_V, d, d).astype(np.float64)
+    R = rotation.rotation_matrix(tables.rotation_signs(5, tables.STREAM_D_V, d))
+    want = SV @ R  # R_V^T S_V^T x = (S_V R_V)^T x
+    ulp = np.spacing(np.abs(want).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(T - want) <= ulp)
+    b.tq_context_destroy(ctx)

@@ -15,8 +15,13 @@ SCHEMES_128 = [("plain", n) for n in (1, 2, 3, 4)] + [("tq", n) for n in (1, 2, 
 
 # the configurations' own (name, scheme, n)
 CONFIG_CASES = [("cfg1", "tq", 4), ("cfg2", "plain", 4), ("cfg2", "tq", 4), ("cfg2", "kqv", 4),
-                ("cfg2", "qkqv", 4), ("cfg4", "kqv", 2), ("cfg4", "kqv", 3), ("cfg4", "kqv", 4),
+                ("cfg2", "qkqv", 4), ("cfg3", "tq", 2), ("cfg3", "tq", 4), ("cfg3", "kqv", 2),
+                ("cfg3", "kqv", 4), ("cfg4", "kqv", 2), ("cfg4", "kqv", 3), ("cfg4", "kqv", 4),
                 ("cfg5", "headq", 2)]
+
+# head dims above 128: every codec combination built for them (no key-side QJL, no HeadQ)
+WIDE_CODECS = [("plain", 1), ("tq", 2), ("tq", 3), ("tq", 4), ("kqv", 2), ("kqv", 3), ("kqv", 4)]
+WIDE_CASES = [(d, s, n) for d in (256, 512, 1024) for s, n in WIDE_CODECS]
 
 
 def _inputs_for(name):
@@ -72,13 +77,32 @@ def test_all_schemes_d128(scheme, n):
     assert rel_err(out, ref) <= ATTN_TOL, rel_err(out, ref)
 
 
-@pytest.mark.parametrize("scheme,n", [("tq", 2), ("tq", 4), ("kqv", 2), ("kqv", 4)])
-def test_append_d1024_low_rank(scheme, n):
-    # the low-rank d = 1024 regime: write path only (decode is built for d = 128)
-    inp = small_inputs("cfg3", B=1, T=70, Hkv=2)
+@pytest.mark.parametrize("d,scheme,n", WIDE_CASES)
+def test_wide_head_dims(d, scheme, n):
+    # G = 4 query heads per KV head; ragged lengths; 64-token append chunks
+    inp = small_inputs("cfg2", B=2, T=150, Hkv=2, seed=13, d=d)
     pair = Pair(inp, scheme, n)
-    pair.append_gpu(chunk=70)
-    _check_all_slabs(pair, inp.T)
+    pair.append_gpu(chunk=64)
+    buf = _check_all_slabs(pair, inp.T)
+    seq = [150, 37]
+    out = pair.decode_gpu(seq)
+    ref = pair.orc.decode(buf, inp.q, seq)
+    assert rel_err(out, ref) <= ATTN_TOL, rel_err(out, ref)
+
+
+@pytest.mark.parametrize("lens", [[0, 17], [16, 0], [1, 33]])
+def test_wide_sequence_length_edge_cases(lens):
+    # the value-sketch pass runs over every head, including those of empty sequences
+    inp = small_inputs("cfg3", B=2, T=40, Hkv=2, seed=14)
+    pair = Pair(inp, "kqv", 2)
+    pair.append_gpu()
+    buf = pair.gpu_bytes()
+    out = pair.decode_gpu(lens)
+    ref = pair.orc.decode(buf, inp.q, lens)
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.all(out[b] == 0)
+    assert rel_err(out, ref) <= ATTN_TOL
 
 
 @pytest.mark.parametrize("lens", [[0, 5], [1, 16], [15, 17], [300, 0], [299, 300]])

@@ -1,4 +1,5 @@
 // C ABI entry points: validation, context and table management, layout, dispatch.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -140,6 +141,27 @@ tq_status tq_context_create(const tq_config* cfg, tq_context** out) {
   };
   if (cfg->k.qjl) put_sketch(3, ctx->tab.s_k, ctx->tab.s_k_t);
   if (cfg->v.qjl) put_sketch(4, ctx->tab.s_v, ctx->tab.s_v_t);
+  if (ctx->tab.s_v_r) {
+    // rows of S_V R_V = S_V H D_V / sqrt(d): a float64 Walsh-Hadamard transform of each row of
+    // S_V, then the D_V signs and the 1/sqrt(d) scale, rounded once to fp32 (R_V = I when the
+    // value side is not rotated)
+    const float* S = (const float*)(base + ctx->tab.s_v);
+    float* T = (float*)(base + ctx->tab.s_v_r);
+    std::vector<double> row(d);
+    const bool rot = cfg->v.rotate != 0;
+    const double rs = rot ? 1.0 / std::sqrt((double)d) : 1.0;
+    for (int i = 0; i < ctx->m; ++i) {
+      for (int j = 0; j < d; ++j) row[j] = S[(size_t)i * d + j];
+      for (int h = 1; rot && h < d; h <<= 1)
+        for (int j = 0; j < d; j += 2 * h)
+          for (int k = j; k < j + h; ++k) {
+            const double a = row[k], b = row[k + h];
+            row[k] = a + b;
+            row[k + h] = a - b;
+          }
+      for (int j = 0; j < d; ++j) T[(size_t)i * d + j] = (float)(row[j] * vs[j] * rs);
+    }
+  }
   *out = ctx;
   return TQ_OK;
 }

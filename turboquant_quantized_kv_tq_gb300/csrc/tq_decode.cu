@@ -3,6 +3,7 @@
 #include <string>
 
 #include "tq_decode_kernel.cuh"
+#include "tq_decode_wide.cuh"
 
 namespace tqd {
 namespace {
@@ -11,7 +12,7 @@ constexpr int kLogitsTokensPerBlock = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct WsLayout {
-  size_t err, tickets, q_rot, q_sk, q_u, part, total;
+  size_t err, tickets, q_rot, q_sk, q_u, part, sk_final, sk_part, total;
   int ps;
 };
 
@@ -31,7 +32,10 @@ WsLayout ws_layout(const tq_context* ctx) {
   w.q_rot = off; off = align256(off + (size_t)B * Hq * D * 2);
   w.q_sk = off; off = align256(off + (ctx->cfg.k.qjl ? (size_t)B * Hq * ctx->m * 2 : 0));
   w.q_u = off; off = align256(off + (ctx->cfg.headq_rank ? (size_t)B * Hq * 16 * 2 : 0));
-  w.part = off; off = align256(off + (size_t)(pairs + kMaxBlocks) * kHeadsPad * w.ps * sizeof(float));
+  w.part = off; off = align256(off + (size_t)(pairs + kMaxBlocks) * (Hq / Hkv) * w.ps * sizeof(float));
+  const bool wide_vq = D > kDecD && ctx->cfg.v.qjl;  // acc_sk / l per head for the sketch pass
+  w.sk_final = off; off = align256(off + (wide_vq ? (size_t)B * Hq * ctx->m * sizeof(float) : 0));
+  w.sk_part = off; off = align256(off + (wide_vq ? (size_t)(ctx->m / kSkRows) * B * Hq * D * sizeof(float) : 0));
   w.total = off;
   return w;
 }
@@ -53,14 +57,18 @@ struct PrepParams {
   int* tickets;
   int* err;
   float* out;
-  int n_tickets, n_heads, Hq, G, k_rotate, kq, kh;
+  float* sk_final;  // zeroed for empty sequences (head dim > 128 with a QJL value side)
+  int n_tickets, n_heads, Hq, G, k_rotate, kq, kh, m;
   int seq_len[TQ_MAX_BATCH];
 };
 
-// Per query head (one warp): q_rot = R_K q; S_K q_rot for a QJL key side; U_rot^T q_rot = U^T q
-// for HeadQ; stored as fp16 pairs.  Block 0 also clears the split tickets and the error word.
+// Per query head (one warp, E = D / 32 coordinates per lane): q_rot = R_K q; for head dim 128
+// also S_K q_rot for a QJL key side and U_rot^T q_rot = U^T q for HeadQ; stored as fp16 pairs.
+// Block 0 also clears the split tickets and the error word; heads of empty sequences get a zero
+// output (no decode block writes them).
+template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
-  constexpr int D = kDecD;
+  constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < p.n_tickets; i += blockDim.x) p.tickets[i] = 0;
@@ -68,57 +76,70 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   }
   const int head = blockIdx.x * 8 + (threadIdx.x >> 5);  // flat [B][Hq] index
   if (head >= p.n_heads) return;
-  if (p.seq_len[head / p.Hq] == 0) {  // no keys: the output is 0 and no block will write it
-    *reinterpret_cast<float4*>(p.out + (long long)head * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  const float4 q4 = *reinterpret_cast<const float4*>(p.q + (long long)head * D + 4 * lane);
-  float x[4] = {q4.x, q4.y, q4.z, q4.w};
+  if (p.seq_len[head / p.Hq] == 0) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) x[i] *= __ldg(p.tab.k_sign + 4 * lane + i);
+    for (int e = 0; e < E; e += 4)
+      *reinterpret_cast<float4*>(p.out + (long long)head * D + lane * E + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.sk_final)
+      for (int i = lane; i < p.m; i += 32) p.sk_final[(long long)head * p.m + i] = 0.f;
+  }
+  float x[E];
+  load_row<E>(p.q + (long long)head * D + lane * E, x);
+#pragma unroll
+  for (int i = 0; i < E; ++i) x[i] *= __ldg(p.tab.k_sign + lane * E + i);
   if (p.k_rotate) {
-    wht_warp<4>(x);
+    wht_warp<E>(x);
     const float rs = 1.f / sqrtf((float)D);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] *= rs;
+    for (int i = 0; i < E; ++i) x[i] *= rs;
   }
-  *reinterpret_cast<uint2*>(p.q_rot + (long long)head * (D / 2) + 2 * lane) =
-      make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
-  if (p.kq) {
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t* qr = p.q_rot + (long long)head * (D / 2) + lane * (E / 2);
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2*>(qr) = make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; i += 8)
+      *reinterpret_cast<uint4*>(qr + i / 2) = make_uint4(pack_half2(x[i], x[i + 1]), pack_half2(x[i + 2], x[i + 3]),
+                                                         pack_half2(x[i + 4], x[i + 5]), pack_half2(x[i + 6], x[i + 7]));
+  }
+  if constexpr (D == kDecD) {
+    if (p.kq) {
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4  // 16 rows of the L2-resident table in flight per lane
-    for (int jl = 0; jl < 32; ++jl) {
+      for (int jl = 0; jl < 32; ++jl) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float xj = __shfl_sync(kFull, x[e], jl);
+          const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.S_K_T + (4 * jl + e) * D + 4 * lane));
+          a[0] = fmaf(s4.x, xj, a[0]); a[1] = fmaf(s4.y, xj, a[1]);
+          a[2] = fmaf(s4.z, xj, a[2]); a[3] = fmaf(s4.w, xj, a[3]);
+        }
+      }
+      *reinterpret_cast<uint2*>(p.q_sk + (long long)head * (D / 2) + 2 * lane) =
+          make_uint2(pack_half2(a[0], a[1]), pack_half2(a[2], a[3]));
+    }
+    if (p.kh) {
+      const int kvh = (head % p.Hq) / p.G;
+      const float* Ur = p.tab.U_rot + (long long)kvh * D * 16;
+      float z[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) z[k] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float xj = __shfl_sync(kFull, x[e], jl);
-        const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.S_K_T + (4 * jl + e) * D + 4 * lane));
-        a[0] = fmaf(s4.x, xj, a[0]); a[1] = fmaf(s4.y, xj, a[1]);
-        a[2] = fmaf(s4.z, xj, a[2]); a[3] = fmaf(s4.w, xj, a[3]);
+#pragma unroll
+        for (int k = 0; k < 16; k += 4) {
+          const float4 u4 = __ldg(reinterpret_cast<const float4*>(Ur + (4 * lane + e) * 16 + k));
+          z[k] = fmaf(u4.x, x[e], z[k]); z[k + 1] = fmaf(u4.y, x[e], z[k + 1]);
+          z[k + 2] = fmaf(u4.z, x[e], z[k + 2]); z[k + 3] = fmaf(u4.w, x[e], z[k + 3]);
+        }
       }
-    }
-    *reinterpret_cast<uint2*>(p.q_sk + (long long)head * (D / 2) + 2 * lane) =
-        make_uint2(pack_half2(a[0], a[1]), pack_half2(a[2], a[3]));
-  }
-  if (p.kh) {
-    const int kvh = (head % p.Hq) / p.G;
-    const float* Ur = p.tab.U_rot + (long long)kvh * D * 16;
-    float z[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) z[k] = 0.f;
+      for (int k = 0; k < 16; ++k) z[k] = warp_sum(z[k]);
+      if (lane == 0) {
+        uint32_t* dst = p.q_u + (long long)head * 8;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-#pragma unroll
-      for (int k = 0; k < 16; k += 4) {
-        const float4 u4 = __ldg(reinterpret_cast<const float4*>(Ur + (4 * lane + e) * 16 + k));
-        z[k] = fmaf(u4.x, x[e], z[k]); z[k + 1] = fmaf(u4.y, x[e], z[k + 1]);
-        z[k + 2] = fmaf(u4.z, x[e], z[k + 2]); z[k + 3] = fmaf(u4.w, x[e], z[k + 3]);
+        for (int k = 0; k < 8; ++k) dst[k] = pack_half2(z[2 * k], z[2 * k + 1]);
       }
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) z[k] = warp_sum(z[k]);
-    if (lane == 0) {
-      uint32_t* dst = p.q_u + (long long)head * 8;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) dst[k] = pack_half2(z[2 * k], z[2 * k + 1]);
     }
   }
 }
@@ -143,6 +164,15 @@ static bool dispatch_decode(const tq_context* ctx, const tqd::DecodeParams& p, d
   using namespace tqd;
   const int kb = ctx->cfg.k.bits, kq = ctx->cfg.k.qjl, kh = ctx->cfg.headq_rank ? 1 : 0;
   const int vb = ctx->cfg.v.bits, vq = ctx->cfg.v.qjl;
+  if (ctx->cfg.head_dim != kDecD) {
+    if (kq || kh) return false;
+    switch (ctx->cfg.head_dim) {
+      case 256: return dispatch_decode_wide_d256(kb, vb, vq, p, grid, s, e);
+      case 512: return dispatch_decode_wide_d512(kb, vb, vq, p, grid, s, e);
+      case 1024: return dispatch_decode_wide_d1024(kb, vb, vq, p, grid, s, e);
+    }
+    return false;
+  }
   switch (kb) {
     case 1: return dispatch_decode_k1(kq, kh, vb, vq, p, grid, s, e);
     case 2: return dispatch_decode_k2(kq, kh, vb, vq, p, grid, s, e);
@@ -157,10 +187,7 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
                         Stream stream) {
   using namespace tqd;
   (void)ws_bytes;
-  if (ctx->cfg.head_dim != kDecD) {
-    set_error("decode attention is built for head_dim 128");
-    return TQ_ERR_UNSUPPORTED;
-  }
+  const int D = ctx->cfg.head_dim;
   const WsLayout w = ws_layout(ctx);
   unsigned char* base = (unsigned char*)ws;
   const cudaStream_t s = (cudaStream_t)stream;
@@ -189,8 +216,17 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   pp.kq = ctx->cfg.k.qjl;
   pp.kh = ctx->cfg.headq_rank ? 1 : 0;
   pp.out = out;
+  const bool wide_vq = D > kDecD && ctx->cfg.v.qjl;
+  pp.sk_final = wide_vq ? (float*)(base + w.sk_final) : nullptr;
+  pp.m = ctx->m;
   for (int b = 0; b < TQ_MAX_BATCH; ++b) pp.seq_len[b] = b < B ? seq_len[b] : 0;
-  prep_kernel<<<(B * Hq + 7) / 8, 256, 0, s>>>(pp);
+  const dim3 pgrid((B * Hq + 7) / 8);
+  switch (D) {
+    case 128: prep_kernel<128><<<pgrid, 256, 0, s>>>(pp); break;
+    case 256: prep_kernel<256><<<pgrid, 256, 0, s>>>(pp); break;
+    case 512: prep_kernel<512><<<pgrid, 256, 0, s>>>(pp); break;
+    default: prep_kernel<1024><<<pgrid, 256, 0, s>>>(pp); break;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail("decode prep", e);
 
@@ -206,7 +242,8 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
   p.v_rotate = ctx->cfg.v.rotate;
-  p.score_scale = kLog2e / sqrtf((float)kDecD);
+  p.sk_final = pp.sk_final;
+  p.score_scale = kLog2e / sqrtf((float)D);
   p.qjl_scale = (float)(1.2533141373155003 / ctx->m);
   p.err = pp.err;
   long long W = 0;  // 16-token tiles over all slabs
@@ -223,6 +260,11 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   e = cudaSuccess;
   dispatch_decode(ctx, p, dim3(p.nblocks), s, &e);
   if (e != cudaSuccess) return cuda_fail("decode", e);
+  if (wide_vq) {  // out += sqrt(pi/2)/m (S_V R_V)^T acc_sk / l, all heads in one pass
+    e = launch_finalize_sketch(D, tab.S_V_R, pp.sk_final, (float*)(base + w.sk_part), out, B * Hq, ctx->m,
+                               p.qjl_scale, s);
+    if (e != cudaSuccess) return cuda_fail("decode sketch finalize", e);
+  }
   return TQ_OK;
 }
 

@@ -54,10 +54,11 @@ struct DecodeParams {
   const uint32_t* q_rot;  // fp16 pairs [B][Hq][D/2]
   const uint32_t* q_sk;   // fp16 pairs [B][Hq][m/2]
   const uint32_t* q_u;    // fp16 pairs [B][Hq][8]
-  float* part;            // [B*Hkv + kMaxBlocks][8][PS]; slab p's partial from block c at p + c
+  float* part;            // [B*Hkv + kMaxBlocks][G][PS]; slab p's partial from block c at p + c
   int* tickets;           // [B*Hkv]
   int* err;               // device error word
   float* out;             // [B][Hq][D]
+  float* sk_final;        // [B][Hq][m]: acc_sk / l (head dim > 128 with a QJL value side)
   int B, Hkv, G, v_rotate, nblocks;
   long long W;            // number of 16-token tiles over all (batch, KV head) slabs
   float score_scale;      // log2(e) / sqrt(d)
@@ -332,24 +333,23 @@ struct SlabPtrs {
   }
 };
 
-template <int KB> struct KRec { static constexpr int value = kDecD * KB / 8; };
+template <int KB, int D = kDecD> struct KRec { static constexpr int value = D * KB / 8; };
 
-// Shared-memory stage of one 16-token tile of one warp: the tile's K block then its V block, in
-// the cache's block layout (field offsets are multiples of 16 bytes).
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
+// Shared-memory stage of one 16-token tile: the tile's K block then its V block, in the cache's
+// block layout for head dim D (QJL rows m = D; field offsets are multiples of 16 bytes).
+template <int KB, bool KQ, bool KH, int VB, bool VQ, int D = kDecD>
 struct Stage {
   static constexpr int KC = 0;
-  static constexpr int KN = KC + kTile * KRec<KB>::value;
+  static constexpr int KN = KC + kTile * KRec<KB, D>::value;
   static constexpr int KS = KN + kTile * 4;
-  static constexpr int KRH = KS + (KQ ? kTile * (kDecD / 8) : 0);
+  static constexpr int KRH = KS + (KQ ? kTile * (D / 8) : 0);
   static constexpr int KZ = KRH + (KQ ? kTile * 2 : 0);
   static constexpr int KZS = KZ + (KH ? kTile * 8 : 0);
   static constexpr int VC = KZS + (KH ? kTile * 2 : 0);
-  static constexpr int VN = VC + kTile * KRec<VB>::value;
+  static constexpr int VN = VC + kTile * KRec<VB, D>::value;
   static constexpr int VS = VN + kTile * 4;
-  static constexpr int VRH = VS + (VQ ? kTile * (kDecD / 8) : 0);
+  static constexpr int VRH = VS + (VQ ? kTile * (D / 8) : 0);
   static constexpr int bytes = VRH + (VQ ? kTile * 2 : 0);
-  static constexpr int copies = 4 + (KQ ? 2 : 0) + (KH ? 2 : 0) + (VQ ? 2 : 0);
 };
 
 // Start the bulk copies of tiles [tile, tile + nt) (nt = 1 or 2: adjacent 16-token blocks of the
@@ -376,25 +376,29 @@ __device__ __forceinline__ uint32_t lds_u16(const unsigned char* p) {
   return *reinterpret_cast<const unsigned short*>(p);
 }
 
-// Read this thread's operands of one tile from its warp's stage: the tile's K block at `st`, its
-// V block at `vst` + S::VC (V field offsets of a 16-token stage are relative to `vst`).
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
+// Read this thread's operands of one tile from a stage: the tile's K block at `st`, its V block
+// at `vst` + S::VC (V field offsets of a 16-token stage are relative to `vst`).  For head dim D,
+// the warp reads the 128-coordinate slice `sl` of every code and sign stream (sl = 0 for 128).
+template <int KB, bool KQ, bool KH, int VB, bool VQ, int D = kDecD>
 __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, const unsigned char* st,
-                                           const unsigned char* vst, int lg, int lt) {
-  using S = Stage<KB, KQ, KH, VB, VQ>;
-  constexpr int KR = KRec<KB>::value, VR = KRec<VB>::value;
+                                           const unsigned char* vst, int lg, int lt, int sl = 0) {
+  using S = Stage<KB, KQ, KH, VB, VQ, D>;
+  constexpr int KR = KRec<KB, D>::value, VR = KRec<VB, D>::value;
   const int rA = tile_row_token(lg), rB = tile_row_token(lg + 8);
-  const unsigned char* ka = st + S::KC + rA * KR;
-  const unsigned char* kb = st + S::KC + rB * KR;
+  // a 128-coordinate slice is 16 bytes per bit of a stream's width
+  const unsigned char* ra = st + S::KC + rA * KR;  // token rows
+  const unsigned char* rb = st + S::KC + rB * KR;
+  const unsigned char* ka = ra + sl * (KB == 3 ? 32 : 16 * KB);
+  const unsigned char* kb = rb + sl * (KB == 3 ? 32 : 16 * KB);
   if constexpr (KB == 4) {
     d.kA.c = *reinterpret_cast<const uint4*>(ka + 16 * lt);
     d.kB.c = *reinterpret_cast<const uint4*>(kb + 16 * lt);
   } else if constexpr (KB == 3 || KB == 2) {
     d.kA.k = *reinterpret_cast<const uint2*>(ka + 8 * lt);
     d.kB.k = *reinterpret_cast<const uint2*>(kb + 8 * lt);
-    if constexpr (KB == 3) {
-      d.kA.s = *reinterpret_cast<const uint32_t*>(ka + kDecD / 4 + 4 * lt);
-      d.kB.s = *reinterpret_cast<const uint32_t*>(kb + kDecD / 4 + 4 * lt);
+    if constexpr (KB == 3) {  // the 1-bit stream follows the 2-bit stream (D / 4 bytes)
+      d.kA.s = *reinterpret_cast<const uint32_t*>(ra + D / 4 + 16 * sl + 4 * lt);
+      d.kB.s = *reinterpret_cast<const uint32_t*>(rb + D / 4 + 16 * sl + 4 * lt);
     }
   } else {
     d.kA.s = *reinterpret_cast<const uint32_t*>(ka + 4 * lt);
@@ -403,8 +407,8 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
   d.nuKA = lds_f32(st + S::KN + 4 * rA);
   d.nuKB = lds_f32(st + S::KN + 4 * rB);
   if constexpr (KQ) {
-    d.sA.s = *reinterpret_cast<const uint32_t*>(st + S::KS + rA * (kDecD / 8) + 4 * lt);
-    d.sB.s = *reinterpret_cast<const uint32_t*>(st + S::KS + rB * (kDecD / 8) + 4 * lt);
+    d.sA.s = *reinterpret_cast<const uint32_t*>(st + S::KS + rA * (D / 8) + 16 * sl + 4 * lt);
+    d.sB.s = *reinterpret_cast<const uint32_t*>(st + S::KS + rB * (D / 8) + 16 * sl + 4 * lt);
     d.rhoKA = lds_f16(st + S::KRH + 2 * rA);
     d.rhoKB = lds_f16(st + S::KRH + 2 * rB);
   }
@@ -420,16 +424,16 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
   for (int j = 0; j < 4; ++j) {
     const unsigned char* v = vst + S::VC + (4 * lt + j) * VR;
     if constexpr (VB == 4) {
-      d.v.w[j] = *reinterpret_cast<const uint2*>(v + 8 * lg);
+      d.v.w[j] = *reinterpret_cast<const uint2*>(v + 64 * sl + 8 * lg);
     } else if constexpr (VB == 3) {
-      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 4 * lg);
-      d.v.s[j] = lds_u16(v + kDecD / 4 + 2 * lg);
+      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 32 * sl + 4 * lg);
+      d.v.s[j] = lds_u16(v + D / 4 + 16 * sl + 2 * lg);
     } else if constexpr (VB == 2) {
-      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 4 * lg);
+      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 32 * sl + 4 * lg);
     } else {
-      d.v.s[j] = lds_u16(v + 2 * lg);
+      d.v.s[j] = lds_u16(v + 16 * sl + 2 * lg);
     }
-    if constexpr (VQ) d.vs.s[j] = lds_u16(vst + S::VS + (4 * lt + j) * (kDecD / 8) + 2 * lg);
+    if constexpr (VQ) d.vs.s[j] = lds_u16(vst + S::VS + (4 * lt + j) * (D / 8) + 16 * sl + 2 * lg);
   }
   d.nuVA = lds_f32(vst + S::VN + 4 * rA);
   d.nuVB = lds_f32(vst + S::VN + 4 * rB);
@@ -557,19 +561,16 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// NT consecutive tiles (starting at token t0) through one online-softmax step.  MASK = false
-// when every token of the NT tiles is below `end`.
+// Online-softmax step over NT consecutive tiles (starting at token t0) whose scores are in s:
+// mask rows at or past `end` (MASK = false when every token of the NT tiles is below it),
+// rescale the running state, and accumulate the value readout.
 template <int NT, bool MASK, int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ>& st,
-                                              const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                              const uint32_t (&qu)[2], uint32_t lxK,
-                                              uint32_t lxV, uint32_t k_m0,
-                                              uint32_t v_m0, const DecodeParams& p, int t0, int end, int lg) {
-  float s[NT][4];
+__device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d)[2], float (&s)[NT][4],
+                                                WarpState<VQ>& st, uint32_t lxV, uint32_t v_m0, int t0,
+                                                int end, int lg) {
   bool va[NT], vb[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    key_scores(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale);
     va[j] = !MASK || t0 + kTile * j + tile_row_token(lg) < end;
     vb[j] = !MASK || t0 + kTile * j + tile_row_token(lg + 8) < end;
     if constexpr (MASK) {
@@ -641,12 +642,46 @@ __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[
   }
 }
 
-// Shared-memory plan of a decode block, in shared-window addresses.  The code tables sit at
-// kLutAddrK / kLutAddrV; per-warp regions (the warp's bulk-copy ring, later its merge slot) fill
-// [kDynBaseMax, kLutAddrK), then the gap between the key table and the value table (when there
-// is one), then the space after the last table; the mbarriers follow the last region.  The
-// dynamic allocation covers the window from 0 to `bytes`, whatever the start of dynamic shared
-// memory (at most kDynBaseMax, checked at run time).
+// Scores and online-softmax step of NT consecutive tiles held by one warp (head dim 128).
+template <int NT, bool MASK, int KB, bool KQ, bool KH, int VB, bool VQ>
+__device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ>& st,
+                                              const uint32_t (&qf)[16], const uint32_t (&qs)[16],
+                                              const uint32_t (&qu)[2], uint32_t lxK,
+                                              uint32_t lxV, uint32_t k_m0,
+                                              uint32_t v_m0, const DecodeParams& p, int t0, int end, int lg) {
+  float s[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) key_scores(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale);
+  softmax_readout<NT, MASK>(d, s, st, lxV, v_m0, t0, end, lg);
+}
+
+// Placement of N equal regions of RS bytes around the code tables, in shared-window addresses:
+// the key table (lutK bytes) sits at kLutAddrK, a separate value table (lutV bytes, 0 when the
+// sides share one) at kLutAddrV.  Regions fill [kDynBaseMax, kLutAddrK), then the gap between
+// the key table and the value table (when there is one), then the space after the last table;
+// `bars` (8-byte aligned) follows the last region.  A dynamic allocation of `end(extra)` bytes
+// covers the window from 0 to the end of `extra` bytes after `bars`, whatever the start of
+// dynamic shared memory (at most kDynBaseMax, checked at run time).
+template <uint32_t lutK, uint32_t lutV, uint32_t RS, int N>
+struct RegionPlan {
+  static constexpr bool sepV = lutV > 0;
+  static constexpr uint32_t a0 = kDynBaseMax;
+  static constexpr int nA = (kLutAddrK - a0) / RS < (uint32_t)N ? (int)((kLutAddrK - a0) / RS) : N;
+  static constexpr uint32_t b0 = kLutAddrK + lutK;
+  static constexpr int nBmax = sepV ? (int)((kLutAddrV - b0) / RS) : N;
+  static constexpr int nB = nBmax < N - nA ? nBmax : N - nA;
+  static constexpr uint32_t c0 = kLutAddrV + lutV;
+  static constexpr int nC = N - nA - nB;
+  static constexpr uint32_t bars = sepV ? c0 + nC * RS : b0 + nB * RS;
+  static_assert(RS % 16 == 0, "regions must keep 16-byte alignment");
+  static_assert(lutK <= kLutAddrV - kLutAddrK, "key table overlaps the value table");
+  __host__ __device__ static constexpr uint32_t region(int w) {
+    return w < nA ? a0 + w * RS : (w < nA + nB ? b0 + (w - nA) * RS : c0 + (w - nA - nB) * RS);
+  }
+};
+
+// Shared-memory plan of a decode block: per-warp regions (the warp's bulk-copy ring, later its
+// merge slot) placed by RegionPlan, then one mbarrier per pair stage and warp.
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
 struct DecodeSmem {
   static constexpr uint32_t lutK = LutEntries<KB>::value * kLutStride;
@@ -657,20 +692,10 @@ struct DecodeSmem {
   static constexpr uint32_t ring = kPairStages * 2 * Stage<KB, KQ, KH, VB, VQ>::bytes;
   static constexpr uint32_t mslot = kHeadsPad * PS * 4;
   static constexpr uint32_t RS = ring > mslot ? ring : mslot;
-  static constexpr uint32_t a0 = kDynBaseMax;
-  static constexpr int nA = (kLutAddrK - a0) / RS < (uint32_t)NW ? (int)((kLutAddrK - a0) / RS) : NW;
-  static constexpr uint32_t b0 = kLutAddrK + lutK;
-  static constexpr int nBmax = sepV ? (int)((kLutAddrV - b0) / RS) : NW;
-  static constexpr int nB = nBmax < NW - nA ? nBmax : NW - nA;
-  static constexpr uint32_t c0 = kLutAddrV + lutV;
-  static constexpr int nC = NW - nA - nB;
-  static constexpr uint32_t bars = sepV ? c0 + nC * RS : b0 + nB * RS;
+  using Plan = RegionPlan<lutK, lutV, RS, NW>;
+  static constexpr uint32_t bars = Plan::bars;
   static constexpr uint32_t bytes = bars + NW * kPairStages * 8;
-  static_assert(RS % 16 == 0, "regions must keep 16-byte alignment");
-  static_assert(lutK <= kLutAddrV - kLutAddrK, "key table overlaps the value table");
-  __host__ __device__ static constexpr uint32_t region(int w) {
-    return w < nA ? a0 + w * RS : (w < nA + nB ? b0 + (w - nA) * RS : c0 + (w - nA - nB) * RS);
-  }
+  __host__ __device__ static constexpr uint32_t region(int w) { return Plan::region(w); }
 };
 
 // Owner block of flattened tile x: the largest c with floor(c W / N) <= x.
@@ -843,7 +868,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
       }
     }
     __syncthreads();
-    float* part_out = p.part + ((long long)(pair + blockIdx.x) * kHeadsPad) * PS;
+    float* part_out = p.part + ((long long)(pair + blockIdx.x) * G) * PS;
     for (int idx = threadIdx.x; idx < G * PS; idx += blockDim.x) {
       const int h = idx / PS, e = idx % PS;
       float M = -INFINITY;
@@ -881,7 +906,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
       __threadfence();
       if (warp < G) {
         const int h = warp;
-        const long long sstride = (long long)kHeadsPad * PS;
+        const long long sstride = (long long)G * PS;
         const float* base = p.part + (long long)(pair + c_first) * sstride + h * PS;
         const int ns = c_last - c_first + 1;
         float M = -INFINITY;

@@ -26,6 +26,7 @@ struct Tables {
   const float* S_V;
   const float* S_V_T;
   const float* U_rot; // [H_kv][d][r], R_K U
+  const float* S_V_R; // [m][d], S_V R_V (head dim > 128 with a QJL value side)
 };
 
 // The packed cache in 16-token blocks: field r of token t of slab s = b * H + h at
@@ -64,6 +65,7 @@ inline Tables make_tables(const tq_context* ctx) {
   t.S_V = ctx->cfg.v.qjl ? (const float*)(b + ctx->tab.s_v) : nullptr;
   t.S_V_T = ctx->cfg.v.qjl ? (const float*)(b + ctx->tab.s_v_t) : nullptr;
   t.U_rot = ctx->cfg.headq_rank ? (const float*)(b + ctx->tab.headq_u) : nullptr;
+  t.S_V_R = ctx->tab.s_v_r ? (const float*)(b + ctx->tab.s_v_r) : nullptr;
   return t;
 }
 

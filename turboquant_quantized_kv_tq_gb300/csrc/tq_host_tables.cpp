@@ -198,6 +198,7 @@ TableOffsets make_table_offsets(const tq_config& cfg, int m) {
   T.s_v = cfg.v.qjl ? take((uint64_t)m * d * 4) : 0;
   T.s_v_t = cfg.v.qjl ? take((uint64_t)m * d * 4) : 0;
   T.headq_u = cfg.headq_rank ? take((uint64_t)cfg.num_kv_heads * d * cfg.headq_rank * 4) : 0;
+  T.s_v_r = (cfg.v.qjl && d > 128) ? take((uint64_t)m * d * 4) : 0;
   T.total = align_up(off, kTableAlign);
   return T;
 }

@@ -22,7 +22,7 @@ enum RegionId {
 // Byte offsets of the arrays inside the table blob (see tq_tables_host in tq.h).
 struct TableOffsets {
   size_t k_centroids, k_thresholds, v_centroids, v_thresholds;
-  size_t k_signs, v_signs, s_k, s_k_t, s_v, s_v_t, headq_u, total;
+  size_t k_signs, v_signs, s_k, s_k_t, s_v, s_v_t, headq_u, s_v_r, total;
 };
 
 // 16-token block layout: field r of token t of slab s at
