@@ -819,21 +819,43 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
       if (!mbar_wait(my_bars + 8 * sl, (cur / kPairStages) & 1u, kWaitLimit)) timed_out = true;
       const unsigned char* stg = my_stages + sl * PB;
       TileData<KB, KQ, KH, VB, VQ> d[2];
-      read_stage(d[0], stg, stg + 2 * KBL - SG::VC, lg, lt);
-      if (two) read_stage(d[1], stg + KBL, stg + 2 * KBL + VBL - SG::VC, lg, lt);
-      __syncwarp();  // every lane has read the stage
-      fence_proxy_async_shared();
-      if (k + kPairStages < npairs)
-        issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * (k + kPairStages),
-                                       min(2, nt - 2 * (k + kPairStages)), lane);
       const int t0 = (m0t + 2 * k) * kTile;
-      if (two) {
-        if (t0 + 2 * kTile <= L)
-          compute_tiles<2, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
-        else
-          compute_tiles<2, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+      if constexpr (!(KQ || VQ || KH)) {
+        read_stage(d[0], stg, stg + 2 * KBL - SG::VC, lg, lt);
+        if (two) read_stage(d[1], stg + KBL, stg + 2 * KBL + VBL - SG::VC, lg, lt);
+        __syncwarp();  // every lane has read the stage
+        fence_proxy_async_shared();
+        if (k + kPairStages < npairs)
+          issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * (k + kPairStages),
+                                         min(2, nt - 2 * (k + kPairStages)), lane);
+        if (two) {
+          if (t0 + 2 * kTile <= L)
+            compute_tiles<2, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+          else
+            compute_tiles<2, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+        } else {
+          compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+        }
       } else {
-        compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+        // QJL and HeadQ variants keep one tile in registers at a time (their extra state leaves no
+        // room for two); the stage is refilled once its last tile has been read
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+          if (j == 1 && !two) break;
+          read_stage(d[0], stg + j * KBL, stg + 2 * KBL + j * VBL - SG::VC, lg, lt);
+          if (j == 1 || !two) {
+            __syncwarp();
+            fence_proxy_async_shared();
+            if (k + kPairStages < npairs)
+              issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp,
+                                             m0t + 2 * (k + kPairStages), min(2, nt - 2 * (k + kPairStages)), lane);
+          }
+          const int tj = t0 + j * kTile;
+          if (tj + kTile <= L)
+            compute_tiles<1, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, lg);
+          else
+            compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, lg);
+        }
       }
     }
     seq += npairs;
