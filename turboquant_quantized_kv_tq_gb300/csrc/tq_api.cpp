@@ -128,6 +128,18 @@ tq_status tq_context_create(const tq_config* cfg, tq_context** out) {
   };
   put_codebook(cfg->k.bits, ctx->tab.k_centroids, ctx->tab.k_thresholds);
   put_codebook(cfg->v.bits, ctx->tab.v_centroids, ctx->tab.v_thresholds);
+  // the write path's sign-magnitude code search relies on exactly symmetric thresholds
+  for (int side = 0; side < 2; ++side) {
+    const int bits = side ? cfg->v.bits : cfg->k.bits;
+    const float* ft = (const float*)(base + (side ? ctx->tab.v_thresholds : ctx->tab.k_thresholds));
+    const int h = 1 << (bits - 1);
+    bool ok = ft[h - 1] == 0.0f;
+    for (int k = 1; k < h; ++k) ok = ok && ft[h - 1 + k] == -ft[h - 1 - k];
+    if (!ok) {
+      delete ctx;
+      return fail(TQ_ERR_INVALID_ARG, "codebook thresholds are not symmetric");
+    }
+  }
   float* ks = (float*)(base + ctx->tab.k_signs);
   float* vs = (float*)(base + ctx->tab.v_signs);
   if (cfg->k.rotate) rotation_signs(cfg->seed, 1, d, ks); else for (int i = 0; i < d; ++i) ks[i] = 1.0f;

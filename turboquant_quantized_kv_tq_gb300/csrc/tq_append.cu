@@ -18,6 +18,9 @@ namespace tqd {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+// vectors per warp of append_kernel, their chains interleaved (one for the wide head dims,
+// whose per-lane state is already large)
+template <int D> struct AppendNV { static constexpr int value = D == 128 ? 2 : 1; };
 
 struct AppendParams {
   Tables tab;
@@ -27,8 +30,18 @@ struct AppendParams {
   int B, Hkv, n_new, m;
   int bits[2], rotate[2], qjl[2];
   int headq_rank;
+  int qjl_mma;  // QJL sides go to append_qjl_mma_kernel (head dim 128, large appends)
   int start[TQ_MAX_BATCH];
 };
+
+// Flat vector index (over [B][H_kv][n_new]) -> batch, KV head, index in the chunk, position.
+__device__ __forceinline__ void split_vec(const AppendParams& p, long long vec, int& b, int& h, int& j, int& t) {
+  j = (int)(vec % p.n_new);
+  const long long r = vec / p.n_new;
+  h = (int)(r % p.Hkv);
+  b = (int)(r / p.Hkv);
+  t = p.start[b] + j;
+}
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = a + b;
@@ -113,172 +126,419 @@ __device__ __forceinline__ void load_stream(const unsigned char* src, uint32_t (
   }
 }
 
-template <int D, typename Tin>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+// NV vectors of one side through the write path ([TQ-KV] "Esquemas de Cuantización"), their
+// dependency chains (loads, shuffle reductions, butterflies) interleaved: norm, rotation,
+// scalar code, code and norm stores; on a QJL side the residual r = y - C[c] (left in res) and
+// its fp16 norm; on a key with HeadQ the side code ([HEADQ] "Escrita no Cache").  Vectors with
+// valid[v] false (the same in every lane) are neither loaded nor stored and leave res = 0.
+template <int D, typename Tin, int NV>
+__device__ __forceinline__ void encode_vectors(const AppendParams& p, int side, const int (&b)[NV],
+                                               const int (&h)[NV], const int (&j)[NV], const int (&t)[NV],
+                                               const bool (&valid)[NV], float (&res)[NV][D / 32]) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
-  const long long vec = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  const long long per_side = (long long)p.B * p.Hkv * p.n_new;
-  if (vec >= 2 * per_side) return;
-  const int side = vec >= per_side ? 1 : 0;
-  long long r = side ? vec - per_side : vec;
-  const int j = (int)(r % p.n_new);
-  r /= p.n_new;
-  const int h = (int)(r % p.Hkv);
-  const int b = (int)(r / p.Hkv);
-  const int t = p.start[b] + j;
-
-  const Tin* src = reinterpret_cast<const Tin*>(side ? p.v : p.k) +
-                   ((long long)(b * p.Hkv + h) * p.n_new + j) * D;
-  float x[E];
-  load_row<E>(src + lane * E, x);
-
-  const float nu = norm_compensated<E>(x);
   const int bits = p.bits[side];
   const bool rotate = p.rotate[side] != 0;
   const float* sgn = side ? p.tab.v_sign : p.tab.k_sign;
   const float* cent = side ? p.tab.v_c : p.tab.k_c;
   const float* thr = side ? p.tab.v_t : p.tab.k_t;
+  const Tin* base = reinterpret_cast<const Tin*>(side ? p.v : p.k);
 
-  float hrot[E];
+  float x[NV][E];
 #pragma unroll
-  for (int i = 0; i < E; ++i) hrot[i] = x[i] * __ldg(sgn + lane * E + i);
-  if (rotate) wht_warp<E>(hrot);
+  for (int v = 0; v < NV; ++v) {
+    if (valid[v]) {
+      load_row<E>(base + ((long long)(b[v] * p.Hkv + h[v]) * p.n_new + j[v]) * D + lane * E, x[v]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) x[v][i] = 0.f;
+    }
+  }
+  float nu[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) nu[v] = norm_compensated<E>(x[v]);
+
+  float dsg[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) dsg[i] = __ldg(sgn + lane * E + i);
+  float hrot[NV][E];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < E; ++i) hrot[v][i] = x[v][i] * dsg[i];
+  if (rotate) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) wht_warp<E>(hrot[v]);
+  }
   const float rs = rotate ? 1.f / sqrtf((float)D) : 1.f;
   const float scale = rotate ? sqrtf((float)D) : 1.f;
-  const float inv = nu > 0.f ? 1.f / (nu * scale) : 0.f;
 
-  float y[E];
-#pragma unroll
-  for (int i = 0; i < E; ++i) y[i] = hrot[i] * inv;
-
-  float tr[15];
-#pragma unroll
-  for (int k = 0; k < 15; ++k) tr[k] = __ldg(thr + k);
-  uint32_t code[E];
-#pragma unroll
-  for (int i = 0; i < E; ++i) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int k = 0; k < 15; ++k) c += y[i] > tr[k] ? 1u : 0u;
-    code[i] = c;
-  }
-
-  // sign-magnitude symbols
+  // The code c = #{k : y > t_k} (ties to the lower cell) in sign-magnitude form.  The
+  // thresholds are symmetric (t_{h-1} = 0 and t_{h-1+k} = -t_{h-1-k} exactly, h = 2^(b-1);
+  // checked when the context is created), so s = [y > 0] and the magnitude counts only the
+  // upper thresholds: #{k >= h : y > t_k} for y > 0, #{k >= h : -y >= t_k} otherwise; -y >= t
+  // is tested as nextup(-y) > t.
   const uint32_t halfL = 1u << (bits - 1);
-  uint32_t sgnbit[E], mag[E];
+  float tu[7];  // t_h .. t_{h+6}; slots past the last threshold hold 3e38
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    const bool s = code[i] >= halfL;
-    sgnbit[i] = s ? 1u : 0u;
-    mag[i] = s ? code[i] - halfL : halfL - 1u - code[i];
+  for (int k = 0; k < 7; ++k) tu[k] = __ldg(thr + halfL + k);
+  float y[NV][E];
+  uint32_t code[NV][E], sgnbit[NV][E], mag[NV][E];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const float inv = nu[v] > 0.f ? 1.f / (nu[v] * scale) : 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      y[v][i] = hrot[v][i] * inv;
+      const bool pos = y[v][i] > 0.f;
+      const float a = pos ? y[v][i] : __int_as_float(__float_as_int(-y[v][i]) + 1);
+      uint32_t m = 0;
+#pragma unroll
+      for (int k = 0; k < 7; ++k) m += a > tu[k] ? 1u : 0u;
+      sgnbit[v][i] = pos ? 1u : 0u;
+      mag[v][i] = m;
+      code[v][i] = pos ? halfL + m : halfL - 1u - m;
+    }
   }
 
   const Cache& C = p.cache;
   const int rc = side ? tqi::R_V_CODES : tqi::R_K_CODES;
-  unsigned char* codes = C.ptr(rc, b, h, t);
-  if (bits == 4) {
-    uint32_t v[E];
 #pragma unroll
-    for (int i = 0; i < E; ++i) v[i] = (sgnbit[i] << 3) | mag[i];
-    store_stream<E, 4>(codes, v);
-  } else if (bits == 3) {
-    store_stream<E, 2>(codes, mag);
-    store_stream<E, 1>(codes + D / 4, sgnbit);
-  } else if (bits == 2) {
-    uint32_t v[E];
+  for (int v = 0; v < NV; ++v) {
+    if (!valid[v]) continue;
+    unsigned char* codes = C.ptr(rc, b[v], h[v], t[v]);
+    if (bits == 4) {
+      uint32_t w[E];
 #pragma unroll
-    for (int i = 0; i < E; ++i) v[i] = (sgnbit[i] << 1) | mag[i];
-    store_stream<E, 2>(codes, v);
-  } else {
-    store_stream<E, 1>(codes, sgnbit);
+      for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 3) | mag[v][i];
+      store_stream<E, 4>(codes, w);
+    } else if (bits == 3) {
+      store_stream<E, 2>(codes, mag[v]);
+      store_stream<E, 1>(codes + D / 4, sgnbit[v]);
+    } else if (bits == 2) {
+      uint32_t w[E];
+#pragma unroll
+      for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 1) | mag[v][i];
+      store_stream<E, 2>(codes, w);
+    } else {
+      store_stream<E, 1>(codes, sgnbit[v]);
+    }
+    if (lane == 0) *reinterpret_cast<float*>(C.ptr(side ? tqi::R_V_NORM : tqi::R_K_NORM, b[v], h[v], t[v])) = nu[v];
   }
-  if (lane == 0) *reinterpret_cast<float*>(C.ptr(side ? tqi::R_V_NORM : tqi::R_K_NORM, b, h, t)) = nu;
 
   if (p.qjl[side]) {
-    // residual of the rotated unit vector, its norm, and the signs of S r
-    float res[E];
-    float ss = 0.f;
+    float ss[NV];
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
-      res[i] = y[i] - __ldg(cent + code[i]);
-      ss = fmaf(res[i], res[i], ss);
-    }
-    ss = warp_sum(ss);
-    const float* ST = side ? p.tab.S_V_T : p.tab.S_K_T;  // [d][m], m == d
-    float acc[E];
+    for (int v = 0; v < NV; ++v) {
+      ss[v] = 0.f;
 #pragma unroll
-    for (int q = 0; q < E; ++q) acc[q] = 0.f;
-    // several rows in flight per lane: the table is read from L2 and the loop is latency-bound
-    constexpr int kUnroll = E <= 8 ? 4 : 1;
-#pragma unroll kUnroll
-    for (int jl = 0; jl < 32; ++jl) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float rj = __shfl_sync(kFull, res[e], jl);
-        const float* row = ST + (long long)(jl * E + e) * D + lane * E;
-#pragma unroll
-        for (int q = 0; q < E; q += 4) {
-          const float4 s4 = __ldg(reinterpret_cast<const float4*>(row + q));
-          acc[q] = fmaf(s4.x, rj, acc[q]);
-          acc[q + 1] = fmaf(s4.y, rj, acc[q + 1]);
-          acc[q + 2] = fmaf(s4.z, rj, acc[q + 2]);
-          acc[q + 3] = fmaf(s4.w, rj, acc[q + 3]);
-        }
+      for (int i = 0; i < E; ++i) {
+        res[v][i] = valid[v] ? y[v][i] - __ldg(cent + code[v][i]) : 0.f;
+        ss[v] = fmaf(res[v][i], res[v][i], ss[v]);
       }
     }
-    uint32_t sbit[E];
 #pragma unroll
-    for (int q = 0; q < E; ++q) sbit[q] = acc[q] >= 0.f ? 1u : 0u;
-    store_stream<E, 1>(C.ptr(side ? tqi::R_V_SIGNS : tqi::R_K_SIGNS, b, h, t), sbit);
-    if (lane == 0)
-      *reinterpret_cast<__half*>(C.ptr(side ? tqi::R_V_RHO : tqi::R_K_RHO, b, h, t)) =
-          __float2half_rn(sqrtf(ss));
+    for (int v = 0; v < NV; ++v) ss[v] = warp_sum(ss[v]);
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+      if (valid[v] && lane == 0)
+        *reinterpret_cast<__half*>(C.ptr(side ? tqi::R_V_RHO : tqi::R_K_RHO, b[v], h[v], t[v])) =
+            __float2half_rn(sqrtf(ss[v]));
   }
 
   if (side == 0 && p.headq_rank) {
     // e_rot = R k - nu C[c]; z = (R U)^T e_rot = U^T e   ([HEADQ] "Escrita no Cache")
     constexpr int RK = 16;
-    const float* Ur = p.tab.U_rot + (long long)h * D * RK;
-    float z[RK];
 #pragma unroll
-    for (int k = 0; k < RK; ++k) z[k] = 0.f;
+    for (int v = 0; v < NV; ++v) {
+      if (!valid[v]) continue;
+      const float* Ur = p.tab.U_rot + (long long)h[v] * D * RK;
+      float z[RK];
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const float e = hrot[i] * rs - nu * __ldg(cent + code[i]);
-      const float* urow = Ur + (lane * E + i) * RK;
+      for (int k = 0; k < RK; ++k) z[k] = 0.f;
 #pragma unroll
-      for (int k = 0; k < RK; k += 4) {
-        const float4 u4 = __ldg(reinterpret_cast<const float4*>(urow + k));
-        z[k] = fmaf(u4.x, e, z[k]);
-        z[k + 1] = fmaf(u4.y, e, z[k + 1]);
-        z[k + 2] = fmaf(u4.z, e, z[k + 2]);
-        z[k + 3] = fmaf(u4.w, e, z[k + 3]);
+      for (int i = 0; i < E; ++i) {
+        const float e = hrot[v][i] * rs - nu[v] * __ldg(cent + code[v][i]);
+        const float* urow = Ur + (lane * E + i) * RK;
+#pragma unroll
+        for (int k = 0; k < RK; k += 4) {
+          const float4 u4 = __ldg(reinterpret_cast<const float4*>(urow + k));
+          z[k] = fmaf(u4.x, e, z[k]);
+          z[k + 1] = fmaf(u4.y, e, z[k + 1]);
+          z[k + 2] = fmaf(u4.z, e, z[k + 2]);
+          z[k + 3] = fmaf(u4.w, e, z[k + 3]);
+        }
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int k = 0; k < RK; ++k) {
+        z[k] = warp_sum(z[k]);
+        amax = fmaxf(amax, fabsf(z[k]));
+      }
+      const __half sh = __float2half_rn(amax / 7.0f);
+      const float s32 = __half2float(sh);
+      uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+      for (int k = 0; k < RK; ++k) {
+        int qz = 0;
+        if (s32 > 0.f) {
+          const float q = rintf(__fdiv_rn(z[k], s32));
+          qz = (int)fminf(fmaxf(q, -7.f), 7.f);
+        }
+        const uint32_t nib = (uint32_t)qz & 0xFu;
+        if (k < 8) w0 |= nib << (4 * k); else w1 |= nib << (4 * (k - 8));
+      }
+      if (lane == 0) {
+        *reinterpret_cast<uint2*>(C.ptr(tqi::R_K_SIDE, b[v], h[v], t[v])) = make_uint2(w0, w1);
+        *reinterpret_cast<__half*>(C.ptr(tqi::R_K_SIDE_SCALE, b[v], h[v], t[v])) = sh;
       }
     }
-    float amax = 0.f;
+  }
+}
+
+// One vector (see encode_vectors).
+template <int D, typename Tin>
+__device__ __forceinline__ void encode_vector(const AppendParams& p, int side, int b, int h, int j, int t,
+                                              float (&res)[D / 32]) {
+  const int bb[1] = {b}, hh[1] = {h}, jj[1] = {j}, tt[1] = {t};
+  const bool ok[1] = {true};
+  float r[1][D / 32];
+  encode_vectors<D, Tin, 1>(p, side, bb, hh, jj, tt, ok, r);
 #pragma unroll
-    for (int k = 0; k < RK; ++k) {
-      z[k] = warp_sum(z[k]);
-      amax = fmaxf(amax, fabsf(z[k]));
-    }
-    const __half sh = __float2half_rn(amax / 7.0f);
-    const float s32 = __half2float(sh);
-    uint32_t w0 = 0, w1 = 0;
+  for (int i = 0; i < D / 32; ++i) res[i] = r[0][i];
+}
+
+// Signs of S r for one vector by an FFMA product with S^T read from L2.
+template <int D>
+__device__ __forceinline__ void sketch_signs_ffma(const AppendParams& p, int side, int b, int h, int t,
+                                                  const float (&res)[D / 32]) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const Cache& C = p.cache;
+  const float* ST = side ? p.tab.S_V_T : p.tab.S_K_T;  // [d][m], m == d
+  float acc[E];
 #pragma unroll
-    for (int k = 0; k < RK; ++k) {
-      int qz = 0;
-      if (s32 > 0.f) {
-        const float v = rintf(__fdiv_rn(z[k], s32));
-        qz = (int)fminf(fmaxf(v, -7.f), 7.f);
+  for (int q = 0; q < E; ++q) acc[q] = 0.f;
+  // several rows in flight per lane: the table is read from L2 and the loop is latency-bound
+  constexpr int kUnroll = E <= 8 ? 4 : 1;
+#pragma unroll kUnroll
+  for (int jl = 0; jl < 32; ++jl) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float rj = __shfl_sync(kFull, res[e], jl);
+      const float* row = ST + (long long)(jl * E + e) * D + lane * E;
+#pragma unroll
+      for (int q = 0; q < E; q += 4) {
+        const float4 s4 = __ldg(reinterpret_cast<const float4*>(row + q));
+        acc[q] = fmaf(s4.x, rj, acc[q]);
+        acc[q + 1] = fmaf(s4.y, rj, acc[q + 1]);
+        acc[q + 2] = fmaf(s4.z, rj, acc[q + 2]);
+        acc[q + 3] = fmaf(s4.w, rj, acc[q + 3]);
       }
-      const uint32_t nib = (uint32_t)qz & 0xFu;
-      if (k < 8) w0 |= nib << (4 * k); else w1 |= nib << (4 * (k - 8));
     }
-    if (lane == 0) {
-      *reinterpret_cast<uint2*>(C.ptr(tqi::R_K_SIDE, b, h, t)) = make_uint2(w0, w1);
-      *reinterpret_cast<__half*>(C.ptr(tqi::R_K_SIDE_SCALE, b, h, t)) = sh;
+  }
+  uint32_t sbit[E];
+#pragma unroll
+  for (int q = 0; q < E; ++q) sbit[q] = acc[q] >= 0.f ? 1u : 0u;
+  store_stream<E, 1>(C.ptr(side ? tqi::R_V_SIGNS : tqi::R_K_SIGNS, b, h, t), sbit);
+}
+
+// AppendNV consecutive vectors of one side per warp (warps [0, W) take the keys, [W, 2W) the
+// values, W = ceil(vectors per side / NV)).
+template <int D, typename Tin>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+  constexpr int E = D / 32;
+  constexpr int NV = AppendNV<D>::value;
+  const long long w = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const long long per_side = (long long)p.B * p.Hkv * p.n_new;
+  const long long W = (per_side + NV - 1) / NV;
+  if (w >= 2 * W) return;
+  const int side = w >= W ? 1 : 0;
+  if (p.qjl[side] && p.qjl_mma) return;  // left to append_qjl_mma_kernel
+  const long long v0 = (side ? w - W : w) * NV;
+  int b[NV], h[NV], j[NV], t[NV];
+  bool ok[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    ok[v] = v0 + v < per_side;
+    split_vec(p, ok[v] ? v0 + v : v0, b[v], h[v], j[v], t[v]);
+  }
+  float res[NV][E];
+  encode_vectors<D, Tin, NV>(p, side, b, h, j, t, ok, res);
+  if (p.qjl[side]) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+      if (ok[v]) sketch_signs_ffma<D>(p, side, b[v], h[v], t[v], res[v]);
+  }
+}
+
+// QJL sides of large appends at head dim 128: a block of kQjlWarps warps takes 64 vectors of one
+// side.  (1) Each warp runs 8 of them through encode_vector and keeps r, scaled by 256, in shared
+// memory as two fp16 terms (hi, lo = fp16(256 r - hi)).  (2) S r for the 64 vectors is a
+// [64 x 128] x [128 x 128] product on the tensor cores: mma.sync m16n8k16 with ldmatrix
+// fragments, S split the same way and staged once per block, hi*hi in one fp32 chain and
+// hi*lo + lo*hi in another; warp ballots turn the signs into bytes of the 1-bit stream.
+// (3) The sign records are stored.  (4) A vector with any |S r| below kSignRecheck gets all its
+// signs again from the FFMA path, so decisions near zero have that path's accuracy.
+constexpr int kQjlWarps = 8;
+constexpr int kQjlBlockVec = 64;        // vectors per block: 4 MMA row tiles of 16
+constexpr int kSRow = 136;              // fp16 row pitch: 272 B keeps ldmatrix rows on distinct banks
+constexpr float kQjlUp = 256.f;         // residual scale before the fp16 split
+constexpr float kSignRecheck = 2e-5f;   // in units of S r
+constexpr long long kQjlMmaMin = 256;   // vectors per side from which the tensor-core path is used
+
+struct QjlSmem {
+  static constexpr int table = 128 * kSRow * 2;             // one fp16 table (hi or lo)
+  static constexpr int resid = kQjlBlockVec * kSRow * 2;    // one fp16 residual array (hi or lo)
+  static constexpr int signs = kQjlBlockVec * 16;           // sign records of the block
+  static constexpr int flags = kQjlBlockVec * 4;
+  static constexpr int bytes = 2 * table + 2 * resid + signs + flags;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// bits 0..3 of n to bits 0, 2, 4, 6
+__device__ __forceinline__ uint32_t spread4(uint32_t n) {
+  n = (n | (n << 2)) & 0x33u;
+  return (n | (n << 1)) & 0x55u;
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const AppendParams p) {
+  constexpr int D = 128, E = 4;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int side = (p.qjl[0] && p.qjl[1]) ? (int)blockIdx.y : (p.qjl[0] ? 0 : 1);
+  __half* Shi = reinterpret_cast<__half*>(smem);
+  __half* Slo = reinterpret_cast<__half*>(smem + QjlSmem::table);
+  __half* Rhi = reinterpret_cast<__half*>(smem + 2 * QjlSmem::table);
+  __half* Rlo = reinterpret_cast<__half*>(smem + 2 * QjlSmem::table + QjlSmem::resid);
+  unsigned char* sg = smem + 2 * QjlSmem::table + 2 * QjlSmem::resid;  // [64][16] sign bytes
+  uint32_t* unc = reinterpret_cast<uint32_t*>(sg + QjlSmem::signs);    // [64] near-zero flags
+  const long long per_side = (long long)p.B * p.Hkv * p.n_new;
+  const long long v0 = (long long)blockIdx.x * kQjlBlockVec;
+
+  // ---- (0) S as fp16 hi / lo, and cleared flags
+  const float* S = side ? p.tab.S_V : p.tab.S_K;  // [m][d], S[i][j]
+  for (int idx = threadIdx.x * 4; idx < D * D; idx += blockDim.x * 4) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(S + idx));
+    const int i = idx / D, jj = idx % D;
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    __half hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      hi[e] = __float2half_rn(xs[e]);
+      lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
     }
+    *reinterpret_cast<uint2*>(Shi + i * kSRow + jj) = *reinterpret_cast<const uint2*>(hi);
+    *reinterpret_cast<uint2*>(Slo + i * kSRow + jj) = *reinterpret_cast<const uint2*>(lo);
+  }
+  for (int i = threadIdx.x; i < kQjlBlockVec; i += blockDim.x) unc[i] = 0u;
+
+  // ---- (1) the block's vectors through the codec, two at a time; residuals to shared memory
+  constexpr int NV = 2;
+  for (int vb = warp * (kQjlBlockVec / kQjlWarps); vb < (warp + 1) * (kQjlBlockVec / kQjlWarps); vb += NV) {
+    int b[NV], h[NV], j[NV], t[NV];
+    bool ok[NV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      ok[u] = v0 + vb + u < per_side;
+      split_vec(p, ok[u] ? v0 + vb + u : v0, b[u], h[u], j[u], t[u]);
+    }
+    float res[NV][E];
+    encode_vectors<D, Tin, NV>(p, side, b, h, j, t, ok, res);
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      __half hi[E], lo[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float x = res[u][e] * kQjlUp;
+        hi[e] = __float2half_rn(x);
+        lo[e] = __float2half_rn(x - __half2float(hi[e]));
+      }
+      *reinterpret_cast<uint2*>(Rhi + (vb + u) * kSRow + lane * E) = *reinterpret_cast<const uint2*>(hi);
+      *reinterpret_cast<uint2*>(Rlo + (vb + u) * kSRow + lane * E) = *reinterpret_cast<const uint2*>(lo);
+    }
+  }
+  __syncthreads();
+
+  // ---- (2) S r: warp w takes row tile w / 2 (vectors 16 (w / 2) ..) and sketch rows
+  // 64 (w % 2) .. + 63 (n-tiles of 8)
+  const int rt = warp >> 1, nt0 = 8 * (warp & 1);
+  const uint32_t rhi_s = (uint32_t)__cvta_generic_to_shared(Rhi), rlo_s = (uint32_t)__cvta_generic_to_shared(Rlo);
+  const uint32_t shi_s = (uint32_t)__cvta_generic_to_shared(Shi), slo_s = (uint32_t)__cvta_generic_to_shared(Slo);
+  const int mi = lane >> 3, mr = lane & 7;
+  uint32_t ah[8][4], al[8][4];
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = (uint32_t)(((16 * rt + mr + 8 * (mi & 1)) * kSRow + 16 * ks + 8 * (mi >> 1)) * 2);
+    ldsm_x4(rhi_s + off, ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3]);
+    ldsm_x4(rlo_s + off, al[ks][0], al[ks][1], al[ks][2], al[ks][3]);
+  }
+  const float thr = kSignRecheck * kQjlUp;
+  uint32_t U0 = 0u, U1 = 0u;
+#pragma unroll 1
+  for (int nt = nt0; nt < nt0 + 8; ++nt) {
+    float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kp = 0; kp < 4; ++kp) {
+      const uint32_t off = (uint32_t)(((8 * nt + mr) * kSRow + 16 * (2 * kp + (mi >> 1)) + 8 * (mi & 1)) * 2);
+      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+      ldsm_x4(shi_s + off, h0, h1, h2, h3);
+      ldsm_x4(slo_s + off, l0, l1, l2, l3);
+      const int k0 = 2 * kp, k1 = 2 * kp + 1;
+      mma16816(c, ah[k0][0], ah[k0][1], ah[k0][2], ah[k0][3], h0, h1);
+      mma16816(e, ah[k0][0], ah[k0][1], ah[k0][2], ah[k0][3], l0, l1);
+      mma16816(e, al[k0][0], al[k0][1], al[k0][2], al[k0][3], h0, h1);
+      mma16816(c, ah[k1][0], ah[k1][1], ah[k1][2], ah[k1][3], h2, h3);
+      mma16816(e, ah[k1][0], ah[k1][1], ah[k1][2], ah[k1][3], l2, l3);
+      mma16816(e, al[k1][0], al[k1][1], al[k1][2], al[k1][3], h2, h3);
+    }
+    // accumulator (row g, columns 2t, 2t + 1) = vector g, sketch rows 8 nt + 2t (+1); rows g + 8
+    const float s0 = c[0] + e[0], s1 = c[1] + e[1], s2 = c[2] + e[2], s3 = c[3] + e[3];
+    const uint32_t b0 = __ballot_sync(kFull, s0 >= 0.f), b1 = __ballot_sync(kFull, s1 >= 0.f);
+    const uint32_t b2 = __ballot_sync(kFull, s2 >= 0.f), b3 = __ballot_sync(kFull, s3 >= 0.f);
+    U0 |= __ballot_sync(kFull, fabsf(s0) < thr || fabsf(s1) < thr);
+    U1 |= __ballot_sync(kFull, fabsf(s2) < thr || fabsf(s3) < thr);
+    if (lane < 16) {  // byte nt of vector 16 rt + lane: bit 2t from b0 / b2, bit 2t + 1 from b1 / b3
+      const int sh = 4 * (lane & 7);
+      const uint32_t lo = ((lane < 8 ? b0 : b2) >> sh) & 0xFu, hi = ((lane < 8 ? b1 : b3) >> sh) & 0xFu;
+      sg[(16 * rt + lane) * 16 + nt] = (unsigned char)(spread4(lo) | (spread4(hi) << 1));
+    }
+  }
+  if (lane < 16) {
+    const uint32_t u = lane < 8 ? U0 : U1;
+    if ((u >> (4 * (lane & 7))) & 0xFu) atomicOr(unc + 16 * rt + lane, 1u);
+  }
+  __syncthreads();
+
+  // ---- (3) sign records of the valid vectors, one 32-bit word per thread
+  const Cache& C = p.cache;
+  for (int w = threadIdx.x; w < kQjlBlockVec * 4; w += blockDim.x) {
+    const int v = w >> 2;
+    const long long vec = v0 + v;
+    if (vec < per_side) {
+      int b, h, j, t;
+      split_vec(p, vec, b, h, j, t);
+      reinterpret_cast<uint32_t*>(C.ptr(side ? tqi::R_V_SIGNS : tqi::R_K_SIGNS, b, h, t))[w & 3] =
+          reinterpret_cast<const uint32_t*>(sg)[w];
+    }
+  }
+  __syncthreads();
+
+  // ---- (4) vectors with a value too close to zero: every sign again from the FFMA path (rare)
+  for (int v = warp * (kQjlBlockVec / kQjlWarps); v < (warp + 1) * (kQjlBlockVec / kQjlWarps); ++v) {
+    const long long vec = v0 + v;
+    if (vec >= per_side || !unc[v]) continue;
+    int b, h, j, t;
+    split_vec(p, vec, b, h, j, t);
+    float res[E];
+    encode_vector<D, Tin>(p, side, b, h, j, t, res);
+    sketch_signs_ffma<D>(p, side, b, h, t, res);
   }
 }
 
@@ -436,18 +696,42 @@ tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const
   p.bits[1] = ctx->cfg.v.bits; p.rotate[1] = ctx->cfg.v.rotate; p.qjl[1] = ctx->cfg.v.qjl;
   p.headq_rank = ctx->cfg.headq_rank;
   for (int b = 0; b < TQ_MAX_BATCH; ++b) p.start[b] = b < ctx->cfg.batch ? start[b] : 0;
-  const long long vectors = 2LL * p.B * p.Hkv * n_new;
-  const long long blocks = (vectors + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const int nv = ctx->cfg.head_dim == 128 ? AppendNV<128>::value : 1;
+  const long long warps = 2LL * (((long long)p.B * p.Hkv * n_new + nv - 1) / nv);
+  const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks > 0x7fffffffLL) { set_error("append too large"); return TQ_ERR_INVALID_ARG; }
+  const int nq = (p.qjl[0] ? 1 : 0) + (p.qjl[1] ? 1 : 0);
+  const long long per_side = (long long)p.B * p.Hkv * n_new;
+  p.qjl_mma = (ctx->cfg.head_dim == 128 && nq > 0 && per_side >= kQjlMmaMin) ? 1 : 0;
+  const cudaStream_t cs = (cudaStream_t)stream;
   tq_status s = dispatch_d(ctx->cfg.head_dim, [&](auto dc) {
     constexpr int D = decltype(dc)::value;
     const dim3 grid((unsigned)blocks), block(kWarpsPerBlock * 32);
-    if (dtype == TQ_F32) append_kernel<D, float><<<grid, block, 0, (cudaStream_t)stream>>>(p);
-    else if (dtype == TQ_BF16) append_kernel<D, __nv_bfloat16><<<grid, block, 0, (cudaStream_t)stream>>>(p);
-    else append_kernel<D, __half><<<grid, block, 0, (cudaStream_t)stream>>>(p);
+    if (dtype == TQ_F32) append_kernel<D, float><<<grid, block, 0, cs>>>(p);
+    else if (dtype == TQ_BF16) append_kernel<D, __nv_bfloat16><<<grid, block, 0, cs>>>(p);
+    else append_kernel<D, __half><<<grid, block, 0, cs>>>(p);
   });
   if (s != TQ_OK) return s;
-  return launch_status("append");
+  s = launch_status("append");
+  if (s != TQ_OK || !p.qjl_mma) return s;
+  const dim3 qgrid((unsigned)((per_side + kQjlBlockVec - 1) / kQjlBlockVec), (unsigned)nq), qblock(kQjlWarps * 32);
+  cudaError_t e;
+  if (dtype == TQ_F32) {
+    e = cudaFuncSetAttribute(append_qjl_mma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, QjlSmem::bytes);
+    if (e == cudaSuccess) append_qjl_mma_kernel<float><<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
+  } else if (dtype == TQ_BF16) {
+    e = cudaFuncSetAttribute(append_qjl_mma_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             QjlSmem::bytes);
+    if (e == cudaSuccess) append_qjl_mma_kernel<__nv_bfloat16><<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(append_qjl_mma_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, QjlSmem::bytes);
+    if (e == cudaSuccess) append_qjl_mma_kernel<__half><<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
+  }
+  if (e != cudaSuccess) {
+    set_error(std::string("append sketch: ") + cudaGetErrorString(e));
+    return TQ_ERR_CUDA;
+  }
+  return launch_status("append sketch");
 }
 
 tq_status launch_rotate_basis(const tq_context* ctx, const float* U, Stream stream) {
