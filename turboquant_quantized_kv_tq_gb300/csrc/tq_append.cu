@@ -30,7 +30,8 @@ struct AppendParams {
   int B, Hkv, n_new, m;
   int bits[2], rotate[2], qjl[2];
   int headq_rank;
-  int qjl_mma;  // QJL sides go to append_qjl_mma_kernel (head dim 128, large appends)
+  int qjl_mma;   // QJL sides go to append_qjl_mma_kernel (head dim 128, large appends)
+  int stage_st;  // append_kernel blocks of a QJL side stage S^T in shared memory
   int start[TQ_MAX_BATCH];
 };
 
@@ -308,18 +309,18 @@ __device__ __forceinline__ void encode_vector(const AppendParams& p, int side, i
   for (int i = 0; i < D / 32; ++i) res[i] = r[0][i];
 }
 
-// Signs of S r for one vector by an FFMA product with S^T read from L2.
+// Signs of S r for one vector by an FFMA product with ST = S^T ([d][m], m == d), read from
+// shared memory when the block staged it, else from L2.
 template <int D>
 __device__ __forceinline__ void sketch_signs_ffma(const AppendParams& p, int side, int b, int h, int t,
-                                                  const float (&res)[D / 32]) {
+                                                  const float (&res)[D / 32], const float* ST) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const Cache& C = p.cache;
-  const float* ST = side ? p.tab.S_V_T : p.tab.S_K_T;  // [d][m], m == d
   float acc[E];
 #pragma unroll
   for (int q = 0; q < E; ++q) acc[q] = 0.f;
-  // several rows in flight per lane: the table is read from L2 and the loop is latency-bound
+  // several rows in flight per lane: the loop is bound by the table's load latency
   constexpr int kUnroll = E <= 8 ? 4 : 1;
 #pragma unroll kUnroll
   for (int jl = 0; jl < 32; ++jl) {
@@ -329,7 +330,7 @@ __device__ __forceinline__ void sketch_signs_ffma(const AppendParams& p, int sid
       const float* row = ST + (long long)(jl * E + e) * D + lane * E;
 #pragma unroll
       for (int q = 0; q < E; q += 4) {
-        const float4 s4 = __ldg(reinterpret_cast<const float4*>(row + q));
+        const float4 s4 = *reinterpret_cast<const float4*>(row + q);
         acc[q] = fmaf(s4.x, rj, acc[q]);
         acc[q + 1] = fmaf(s4.y, rj, acc[q + 1]);
         acc[q + 2] = fmaf(s4.z, rj, acc[q + 2]);
@@ -343,19 +344,28 @@ __device__ __forceinline__ void sketch_signs_ffma(const AppendParams& p, int sid
   store_stream<E, 1>(C.ptr(side ? tqi::R_V_SIGNS : tqi::R_K_SIGNS, b, h, t), sbit);
 }
 
-// AppendNV consecutive vectors of one side per warp (warps [0, W) take the keys, [W, 2W) the
-// values, W = ceil(vectors per side / NV)).
+// AppendNV consecutive vectors of side blockIdx.y per warp.  With stage_st set (small appends
+// at head dim 128 with a QJL side), a block of a QJL side first copies S^T (64 KiB) into shared
+// memory, so the sketch's 128 dependent table rows come from there instead of L2.
 template <int D, typename Tin>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
   constexpr int E = D / 32;
   constexpr int NV = AppendNV<D>::value;
+  extern __shared__ __align__(16) float st_smem[];
+  const int side = (int)blockIdx.y;
+  if (p.qjl[side] && p.qjl_mma) return;  // left to append_qjl_mma_kernel (whole block)
+  const float* ST = side ? p.tab.S_V_T : p.tab.S_K_T;
+  if (D == 128 && p.stage_st && p.qjl[side]) {
+    for (int i = threadIdx.x * 4; i < D * D; i += blockDim.x * 4)
+      *reinterpret_cast<float4*>(st_smem + i) = __ldg(reinterpret_cast<const float4*>(ST + i));
+    __syncthreads();
+    ST = st_smem;
+  }
   const long long w = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const long long per_side = (long long)p.B * p.Hkv * p.n_new;
   const long long W = (per_side + NV - 1) / NV;
-  if (w >= 2 * W) return;
-  const int side = w >= W ? 1 : 0;
-  if (p.qjl[side] && p.qjl_mma) return;  // left to append_qjl_mma_kernel
-  const long long v0 = (side ? w - W : w) * NV;
+  if (w >= W) return;
+  const long long v0 = w * NV;
   int b[NV], h[NV], j[NV], t[NV];
   bool ok[NV];
 #pragma unroll
@@ -368,7 +378,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const Appen
   if (p.qjl[side]) {
 #pragma unroll
     for (int v = 0; v < NV; ++v)
-      if (ok[v]) sketch_signs_ffma<D>(p, side, b[v], h[v], t[v], res[v]);
+      if (ok[v]) sketch_signs_ffma<D>(p, side, b[v], h[v], t[v], res[v], ST);
   }
 }
 
@@ -538,7 +548,7 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     split_vec(p, vec, b, h, j, t);
     float res[E];
     encode_vector<D, Tin>(p, side, b, h, j, t, res);
-    sketch_signs_ffma<D>(p, side, b, h, t, res);
+    sketch_signs_ffma<D>(p, side, b, h, t, res, side ? p.tab.S_V_T : p.tab.S_K_T);
   }
 }
 
@@ -697,20 +707,30 @@ tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const
   p.headq_rank = ctx->cfg.headq_rank;
   for (int b = 0; b < TQ_MAX_BATCH; ++b) p.start[b] = b < ctx->cfg.batch ? start[b] : 0;
   const int nv = ctx->cfg.head_dim == 128 ? AppendNV<128>::value : 1;
-  const long long warps = 2LL * (((long long)p.B * p.Hkv * n_new + nv - 1) / nv);
-  const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const long long per_side = (long long)p.B * p.Hkv * n_new;
+  const long long blocks = ((per_side + nv - 1) / nv + kWarpsPerBlock - 1) / kWarpsPerBlock;  // per side
   if (blocks > 0x7fffffffLL) { set_error("append too large"); return TQ_ERR_INVALID_ARG; }
   const int nq = (p.qjl[0] ? 1 : 0) + (p.qjl[1] ? 1 : 0);
-  const long long per_side = (long long)p.B * p.Hkv * n_new;
   p.qjl_mma = (ctx->cfg.head_dim == 128 && nq > 0 && per_side >= kQjlMmaMin) ? 1 : 0;
+  p.stage_st = (ctx->cfg.head_dim == 128 && nq > 0 && !p.qjl_mma) ? 1 : 0;
+  const int smem = p.stage_st ? 128 * 128 * 4 : 0;
   const cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t ae = cudaSuccess;
   tq_status s = dispatch_d(ctx->cfg.head_dim, [&](auto dc) {
     constexpr int D = decltype(dc)::value;
-    const dim3 grid((unsigned)blocks), block(kWarpsPerBlock * 32);
-    if (dtype == TQ_F32) append_kernel<D, float><<<grid, block, 0, cs>>>(p);
-    else if (dtype == TQ_BF16) append_kernel<D, __nv_bfloat16><<<grid, block, 0, cs>>>(p);
-    else append_kernel<D, __half><<<grid, block, 0, cs>>>(p);
+    const dim3 grid((unsigned)blocks, 2), block(kWarpsPerBlock * 32);
+    auto go = [&](auto kern) {
+      if (smem) ae = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (ae == cudaSuccess) kern<<<grid, block, smem, cs>>>(p);
+    };
+    if (dtype == TQ_F32) go(append_kernel<D, float>);
+    else if (dtype == TQ_BF16) go(append_kernel<D, __nv_bfloat16>);
+    else go(append_kernel<D, __half>);
   });
+  if (ae != cudaSuccess) {
+    set_error(std::string("append: ") + cudaGetErrorString(ae));
+    return TQ_ERR_CUDA;
+  }
   if (s != TQ_OK) return s;
   s = launch_status("append");
   if (s != TQ_OK || !p.qjl_mma) return s;

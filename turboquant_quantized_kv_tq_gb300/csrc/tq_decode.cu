@@ -70,6 +70,14 @@ template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
+  extern __shared__ __align__(16) float skt_smem[];
+  const float* SKT = p.tab.S_K_T;
+  if (D == kDecD && p.kq) {  // S_K^T (64 KiB) into shared memory: 128 dependent rows per head
+    for (int i = threadIdx.x * 4; i < D * D; i += blockDim.x * 4)
+      *reinterpret_cast<float4*>(skt_smem + i) = __ldg(reinterpret_cast<const float4*>(SKT + i));
+    __syncthreads();
+    SKT = skt_smem;
+  }
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < p.n_tickets; i += blockDim.x) p.tickets[i] = 0;
     if (threadIdx.x == 0) p.err[0] = 0;
@@ -105,12 +113,12 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   if constexpr (D == kDecD) {
     if (p.kq) {
       float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4  // 16 rows of the L2-resident table in flight per lane
+#pragma unroll 4
       for (int jl = 0; jl < 32; ++jl) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float xj = __shfl_sync(kFull, x[e], jl);
-          const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.S_K_T + (4 * jl + e) * D + 4 * lane));
+          const float4 s4 = *reinterpret_cast<const float4*>(SKT + (4 * jl + e) * D + 4 * lane);
           a[0] = fmaf(s4.x, xj, a[0]); a[1] = fmaf(s4.y, xj, a[1]);
           a[2] = fmaf(s4.z, xj, a[2]); a[3] = fmaf(s4.w, xj, a[3]);
         }
@@ -221,8 +229,13 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   pp.m = ctx->m;
   for (int b = 0; b < TQ_MAX_BATCH; ++b) pp.seq_len[b] = b < B ? seq_len[b] : 0;
   const dim3 pgrid((B * Hq + 7) / 8);
+  const int psmem = (D == kDecD && pp.kq) ? kDecD * kDecD * 4 : 0;
+  if (psmem) {
+    cudaError_t ae = cudaFuncSetAttribute(prep_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
+    if (ae != cudaSuccess) return cuda_fail("decode prep", ae);
+  }
   switch (D) {
-    case 128: prep_kernel<128><<<pgrid, 256, 0, s>>>(pp); break;
+    case 128: prep_kernel<128><<<pgrid, 256, psmem, s>>>(pp); break;
     case 256: prep_kernel<256><<<pgrid, 256, 0, s>>>(pp); break;
     case 512: prep_kernel<512><<<pgrid, 256, 0, s>>>(pp); break;
     default: prep_kernel<1024><<<pgrid, 256, 0, s>>>(pp); break;
