@@ -251,6 +251,9 @@ def run_gpu(args):
     # ---- append throughput on the prefill chunk of the long-context configuration
     append = run_prefill_append(args, device) if not args.skip_append else None
 
+    # ---- several queries per sequence (G * nq = 8 query columns per KV head) on the first cache
+    multi = run_multi_query(caches[0], SCHEMES[0], inp, device, T)
+
     peak, peak_kind = measured_peak()
     rec = [record_bytes(s, n) for s, n in SCHEMES]
     dec_bytes = [B * Hkv * T * r for r in rec]
@@ -278,6 +281,7 @@ def run_gpu(args):
         "schemes": schemes,
         "e2e": e2e,
         "append": append,
+        "multi_query": multi,
         "gpu_launches": args.steps * n_dec * 3,
         "clocks": clocks,
     }
@@ -323,6 +327,30 @@ def run_e2e(args, caches, inp, device, seq, start):
     d2h = sum(o.numel() * 4 for o in out_host)
     value = len(caches) * B * inp.Hkv * T * args.steps / el
     return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def run_multi_query(kv, scheme, inp, device, T):
+    """Decode of nq = 8 / G queries per sequence in one pass (the chunk's last positions)."""
+    import torch
+    G = inp.Hq // inp.Hkv
+    nq = max(1, 8 // G)
+    rng = np.random.default_rng(7)
+    q = torch.from_numpy(rng.standard_normal((inp.B, nq, inp.Hq, inp.d)).astype(np.float32)).to(device)
+    out = torch.empty_like(q)
+    seq = [T] * inp.B
+    for _ in range(3):
+        kv.decode_multi(q, seq, out=out)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record()
+    for _ in range(reps):
+        kv.decode_multi(q, seq, out=out)
+    e1.record()
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) / reps * 1e3
+    return {"scheme": f"{scheme[0]}{scheme[1]}", "nq": nq, "decode_us": round(us, 2),
+            "query_cache_tokens_per_s": round(nq * inp.B * inp.Hkv * T / (us * 1e-6), 1)}
 
 
 def run_prefill_append(args, device):

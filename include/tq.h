@@ -179,6 +179,19 @@ tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, cons
                               const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
                               tq_stream stream);
 
+/* Several queries per sequence in one pass over the cache (speculative-decode drafts, prefill
+ * chunks; [ABL] "Recomendações Práticas" names prefill workloads): the nq queries of sequence b
+ * are the chunk's last nq positions, and query i attends causally to the first
+ * host_seq_len[b] - nq + 1 + i tokens (none when that is <= 0: output zeros).  Each query's
+ * result is what tq_decode_attention gives for that query alone over that prefix; the packed
+ * tiles are read and unpacked once for all nq queries (they become extra MMA columns).
+ * q, out: device fp32 [B][nq][H_q][d].  Built for head dim 128 with G * nq <= 8 (G =
+ * H_q / H_kv); otherwise TQ_ERR_UNSUPPORTED.  ws as for tq_decode_attention (the same size
+ * serves every nq).  nq = 1 is tq_decode_attention. */
+tq_status tq_decode_attention_multi(const tq_context* ctx, const void* dev_cache, const float* q,
+                                    int32_t nq, const int32_t* host_seq_len, float* out, void* ws,
+                                    size_t ws_bytes, tq_stream stream);
+
 /* Size of the library's built-in decode scratch (see tq_decode_attention_static). */
 #define TQ_STATIC_SCRATCH_BYTES (8u << 20)
 

@@ -194,3 +194,49 @@ def test_device_error_word_clear():
     pair.decode_gpu([32])
     st, code = pair.gpu.device_error()
     assert st == 0 and code == 0
+
+
+def _multi_queries(inp, nq, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((inp.B, nq, inp.Hq, inp.d)).astype(np.float32)
+
+
+@pytest.mark.parametrize("scheme,n,hq,hkv,nq,lens", [
+    ("tq", 4, 8, 2, 2, [200, 131]),
+    ("kqv", 4, 8, 2, 2, [200, 17]),
+    ("qkqv", 4, 8, 2, 2, [199, 64]),
+    ("tq", 3, 2, 2, 8, [100, 5]),      # G = 1: eight queries; queries 0..2 of batch 1 see nothing
+    ("plain", 2, 4, 2, 4, [33, 200]),
+    ("headq", 2, 8, 2, 2, [150, 97]),
+])
+def test_multi_query_decode(scheme, n, hq, hkv, nq, lens):
+    import torch
+    name = "cfg5" if scheme == "headq" else "cfg2"
+    inp = small_inputs(name, B=2, T=200, Hkv=hkv, Hq=hq, seed=21)
+    pair = Pair(inp, scheme, n)
+    pair.append_gpu(chunk=100)
+    buf = pair.gpu_bytes()
+    qm = _multi_queries(inp, nq, 22)
+    out = pair.gpu.decode_multi(torch.from_numpy(qm).cuda(), lens).cpu().numpy().astype(np.float64)
+    for i in range(nq):
+        seq_i = [max(0, L - nq + 1 + i) for L in lens]
+        ref = pair.orc.decode(buf, qm[:, i], seq_i)
+        for b, L in enumerate(seq_i):
+            if L == 0:
+                assert np.all(out[b, i] == 0)
+        assert rel_err(out[:, i], ref) <= ATTN_TOL, (i, rel_err(out[:, i], ref))
+
+
+def test_multi_query_single_equals_decode_and_limits():
+    import torch
+    from turboquant_quantized_kv_tq_gb300 import TQError
+    inp = small_inputs("cfg2", B=2, T=120, Hkv=2, Hq=8, seed=23)
+    pair = Pair(inp, "kqv", 4)
+    pair.append_gpu()
+    q = torch.from_numpy(inp.q).cuda()
+    a = pair.gpu.decode(q, [120, 77]).cpu().numpy()
+    b = pair.gpu.decode_multi(q[:, None].contiguous(), [120, 77])[:, 0].cpu().numpy()
+    assert np.array_equal(a, b)
+    with pytest.raises(TQError) as e:  # G = 4: at most two queries per sequence
+        pair.gpu.decode_multi(torch.zeros(2, 3, 8, 128, device="cuda"), [120, 77])
+    assert e.value.status == 2

@@ -115,6 +115,19 @@ class QuantizedKVCache:
                                      out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream)))
         return out
 
+    def decode_multi(self, q, seq_len, out=None, stream=None):
+        """q: float32 CUDA tensor [batch][nq][num_q_heads][head_dim]: the last nq positions of each
+        sequence, query i attending to the first seq_len[b] - nq + 1 + i tokens."""
+        import torch
+        q = q.contiguous()
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(max(int(x) for x in seq_len))
+        check(_b.tq_decode_attention_multi(self._ctx, self.cache.data_ptr(), q.data_ptr(), int(q.shape[1]),
+                                           _b.int_array(seq_len), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                           _stream_handle(stream)))
+        return out
+
     def logits(self, q, seq_len, stride=None, stream=None):
         """Corrected scores [batch][num_q_heads][stride] (entries past seq_len[b] are untouched: 0)."""
         import torch

@@ -90,6 +90,8 @@ DECLARATIONS = [
                                       c_void_p, c_size_t, c_void_p]),
     ("tq_decode_attention_static", c_int32, [c_void_p, c_void_p, c_void_p, ctypes.POINTER(c_int32),
                                              c_void_p, c_void_p]),
+    ("tq_decode_attention_multi", c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(c_int32),
+                                            c_void_p, c_void_p, c_size_t, c_void_p]),
     ("tq_headq_correct", c_int32, [c_void_p, c_void_p, c_void_p, ctypes.POINTER(c_int32), c_void_p,
                                    c_int32, c_void_p]),
     ("tq_dequantize", c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,

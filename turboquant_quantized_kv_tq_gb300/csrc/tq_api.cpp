@@ -284,6 +284,25 @@ tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, cons
   return launch_decode(ctx, dev_cache, q, host_seq_len, out, ws, ws_bytes, stream);
 }
 
+tq_status tq_decode_attention_multi(const tq_context* ctx, const void* dev_cache, const float* q,
+                                    int32_t nq, const int32_t* host_seq_len, float* out, void* ws,
+                                    size_t ws_bytes, tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (!dev_cache || !q || !host_seq_len || !out || !ws) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (nq < 1) return fail(TQ_ERR_INVALID_ARG, "nq must be >= 1");
+  const int G = ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads;
+  if (nq > 1 && (ctx->cfg.head_dim != 128 || (int64_t)G * nq > 8))
+    return fail(TQ_ERR_UNSUPPORTED, "several queries per sequence are built for head_dim 128 with G * nq <= 8");
+  if (!aligned(dev_cache, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 256))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer (cache/ws 256 B, q/out 16 B)");
+  int max_seq;
+  s = check_lengths(ctx, host_seq_len, &max_seq);
+  if (s != TQ_OK) return s;
+  if (ws_bytes < decode_workspace_bytes(ctx, max_seq)) return fail(TQ_ERR_WORKSPACE, "workspace too small");
+  return launch_decode_multi(ctx, dev_cache, q, nq, host_seq_len, out, ws, ws_bytes, stream);
+}
+
 tq_status tq_decode_attention_static(const tq_context* ctx, const void* dev_cache, const float* q,
                                      const int32_t* host_seq_len, float* out, tq_stream stream) {
   tq_status s = ready(ctx);

@@ -29,10 +29,12 @@ WsLayout ws_layout(const tq_context* ctx) {
   size_t off = 0;
   w.err = off; off = align256(off + 64 * sizeof(int));
   w.tickets = off; off = align256(off + (size_t)pairs * sizeof(int));
-  w.q_rot = off; off = align256(off + (size_t)B * Hq * D * 2);
-  w.q_sk = off; off = align256(off + (ctx->cfg.k.qjl ? (size_t)B * Hq * ctx->m * 2 : 0));
-  w.q_u = off; off = align256(off + (ctx->cfg.headq_rank ? (size_t)B * Hq * 16 * 2 : 0));
-  w.part = off; off = align256(off + (size_t)(pairs + kMaxBlocks) * (Hq / Hkv) * w.ps * sizeof(float));
+  // query columns per KV head: up to 8 at head dim 128 (several queries per sequence), G otherwise
+  const size_t cols = (size_t)Hkv * (D == kDecD ? kHeadsPad : Hq / Hkv);
+  w.q_rot = off; off = align256(off + (size_t)B * cols * D * 2);
+  w.q_sk = off; off = align256(off + (ctx->cfg.k.qjl ? (size_t)B * cols * ctx->m * 2 : 0));
+  w.q_u = off; off = align256(off + (ctx->cfg.headq_rank ? (size_t)B * cols * 16 * 2 : 0));
+  w.part = off; off = align256(off + (size_t)(pairs + kMaxBlocks) * (cols / Hkv) * w.ps * sizeof(float));
   const bool wide_vq = D > kDecD && ctx->cfg.v.qjl;  // acc_sk / l per head for the sketch pass
   w.sk_final = off; off = align256(off + (wide_vq ? (size_t)B * Hq * ctx->m * sizeof(float) : 0));
   w.sk_part = off; off = align256(off + (wide_vq ? (size_t)(ctx->m / kSkRows) * B * Hq * D * sizeof(float) : 0));
@@ -58,14 +60,15 @@ struct PrepParams {
   int* err;
   float* out;
   float* sk_final;  // zeroed for empty sequences (head dim > 128 with a QJL value side)
-  int n_tickets, n_heads, Hq, G, k_rotate, kq, kh, m;
+  int n_tickets, n_heads, Hq, Hkv, G, Gc, nq, k_rotate, kq, kh, m;
   int seq_len[TQ_MAX_BATCH];
 };
 
-// Per query head (one warp, E = D / 32 coordinates per lane): q_rot = R_K q; for head dim 128
-// also S_K q_rot for a QJL key side and U_rot^T q_rot = U^T q for HeadQ; stored as fp16 pairs.
-// Block 0 also clears the split tickets and the error word; heads of empty sequences get a zero
-// output (no decode block writes them).
+// Per query column (one warp, E = D / 32 coordinates per lane; columns [B][Hkv][Gc], column c
+// = query c / G of the sequence, head c % G of the KV head's group): q_rot = R_K q; for head
+// dim 128 also S_K q_rot for a QJL key side and U_rot^T q_rot = U^T q for HeadQ; stored as fp16
+// pairs.  Block 0 also clears the split tickets and the error word; queries of empty sequences
+// get a zero output (no decode block writes them).
 template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   constexpr int E = D / 32;
@@ -82,17 +85,20 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
     for (int i = threadIdx.x; i < p.n_tickets; i += blockDim.x) p.tickets[i] = 0;
     if (threadIdx.x == 0) p.err[0] = 0;
   }
-  const int head = blockIdx.x * 8 + (threadIdx.x >> 5);  // flat [B][Hq] index
+  const int head = blockIdx.x * 8 + (threadIdx.x >> 5);  // flat column index
   if (head >= p.n_heads) return;
-  if (p.seq_len[head / p.Hq] == 0) {
+  const int b = head / (p.Hkv * p.Gc), r = head % (p.Hkv * p.Gc);
+  const int kvh = r / p.Gc, c = r % p.Gc;
+  const long long qrow = ((long long)b * p.nq + c / p.G) * p.Hq + kvh * p.G + c % p.G;  // [B][nq][Hq]
+  if (p.seq_len[b] == 0) {
 #pragma unroll
     for (int e = 0; e < E; e += 4)
-      *reinterpret_cast<float4*>(p.out + (long long)head * D + lane * E + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(p.out + qrow * D + lane * E + e) = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.sk_final)
-      for (int i = lane; i < p.m; i += 32) p.sk_final[(long long)head * p.m + i] = 0.f;
+      for (int i = lane; i < p.m; i += 32) p.sk_final[qrow * p.m + i] = 0.f;
   }
   float x[E];
-  load_row<E>(p.q + (long long)head * D + lane * E, x);
+  load_row<E>(p.q + qrow * D + lane * E, x);
 #pragma unroll
   for (int i = 0; i < E; ++i) x[i] *= __ldg(p.tab.k_sign + lane * E + i);
   if (p.k_rotate) {
@@ -127,7 +133,6 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
           make_uint2(pack_half2(a[0], a[1]), pack_half2(a[2], a[3]));
     }
     if (p.kh) {
-      const int kvh = (head % p.Hq) / p.G;
       const float* Ur = p.tab.U_rot + (long long)kvh * D * 16;
       float z[16];
 #pragma unroll
@@ -193,6 +198,12 @@ static bool dispatch_decode(const tq_context* ctx, const tqd::DecodeParams& p, d
 tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
                         const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
                         Stream stream) {
+  return launch_decode_multi(ctx, cache, q, 1, seq_len, out, ws, ws_bytes, stream);
+}
+
+tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const float* q, int nq,
+                              const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
+                              Stream stream) {
   using namespace tqd;
   (void)ws_bytes;
   const int D = ctx->cfg.head_dim;
@@ -217,9 +228,12 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   pp.tickets = (int*)(base + w.tickets);
   pp.err = (int*)(base + w.err);
   pp.n_tickets = B * Hkv;
-  pp.n_heads = B * Hq;
+  pp.n_heads = B * Hq * nq;
   pp.Hq = Hq;
+  pp.Hkv = Hkv;
   pp.G = Hq / Hkv;
+  pp.nq = nq;
+  pp.Gc = pp.G * nq;
   pp.k_rotate = ctx->cfg.k.rotate;
   pp.kq = ctx->cfg.k.qjl;
   pp.kh = ctx->cfg.headq_rank ? 1 : 0;
@@ -228,7 +242,7 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   pp.sk_final = wide_vq ? (float*)(base + w.sk_final) : nullptr;
   pp.m = ctx->m;
   for (int b = 0; b < TQ_MAX_BATCH; ++b) pp.seq_len[b] = b < B ? seq_len[b] : 0;
-  const dim3 pgrid((B * Hq + 7) / 8);
+  const dim3 pgrid((B * Hq * nq + 7) / 8);
   const int psmem = (D == kDecD && pp.kq) ? kDecD * kDecD * 4 : 0;
   if (psmem) {
     cudaError_t ae = cudaFuncSetAttribute(prep_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
@@ -254,6 +268,8 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   p.B = B;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
+  p.nq = nq;
+  p.Gc = p.G * nq;
   p.v_rotate = ctx->cfg.v.rotate;
   p.sk_final = pp.sk_final;
   p.score_scale = kLog2e / sqrtf((float)D);

@@ -51,15 +51,18 @@ constexpr int kLutStride = 256;  // bytes between table entries
 struct DecodeParams {
   Tables tab;
   Cache cache;
-  const uint32_t* q_rot;  // fp16 pairs [B][Hq][D/2]
-  const uint32_t* q_sk;   // fp16 pairs [B][Hq][m/2]
-  const uint32_t* q_u;    // fp16 pairs [B][Hq][8]
+  // Query columns: column c of KV head h is query i = c / G of the chunk, head h G + c % G
+  // (nq queries per sequence, Gc = G nq <= 8 columns; nq = 1 is plain decode).
+  const uint32_t* q_rot;  // fp16 pairs [B][Hkv][Gc][D/2]
+  const uint32_t* q_sk;   // fp16 pairs [B][Hkv][Gc][m/2]
+  const uint32_t* q_u;    // fp16 pairs [B][Hkv][Gc][8]
   float* part;            // [B*Hkv + kMaxBlocks][G][PS]; slab p's partial from block c at p + c
   int* tickets;           // [B*Hkv]
   int* err;               // device error word
-  float* out;             // [B][Hq][D]
+  float* out;             // [B][nq][Hq][D]
   float* sk_final;        // [B][Hq][m]: acc_sk / l (head dim > 128 with a QJL value side)
   int B, Hkv, G, v_rotate, nblocks;
+  int nq, Gc;             // queries per sequence (query i sees tokens [0, seq_len - nq + 1 + i))
   long long W;            // number of 16-token tiles over all (batch, KV head) slabs
   float score_scale;      // log2(e) / sqrt(d)
   float qjl_scale;        // sqrt(pi/2) / m
@@ -534,15 +537,20 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
   }
 }
 
+constexpr float kMaxFloor = -1e30f;
+
 // Per-warp running state.
 template <bool VQ>
 struct WarpState {
-  float m0, m1;  // running max (log2 domain) of heads 2 lt, 2 lt + 1
+  // running max (log2 domain) of columns 2 lt, 2 lt + 1; it starts at kMaxFloor, not -inf, so
+  // a column whose query has seen no token yet (all scores -inf) gets weights exp2(-inf) = 0
+  // instead of exp2(-inf + inf)
+  float m0, m1;
   float l0, l1;  // this thread's partial softmax denominators
   float acc[8][4];
   float accs[VQ ? 8 : 1][4];
   __device__ __forceinline__ void reset() {
-    m0 = m1 = -INFINITY;
+    m0 = m1 = kMaxFloor;
     l0 = l1 = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -564,20 +572,26 @@ __device__ __forceinline__ float ex2(float x) {
 // Online-softmax step over NT consecutive tiles (starting at token t0) whose scores are in s:
 // mask rows at or past `end` (MASK = false when every token of the NT tiles is below it),
 // rescale the running state, and accumulate the value readout.
+// Rows (tokens) at or past `end` carry no data; a score of column c counts only for tokens
+// below lmin + c / G, the causal end of that column's query (c = 2 lt, 2 lt + 1; lmin = end
+// for plain decode).
 template <int NT, bool MASK, int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d)[2], float (&s)[NT][4],
                                                 WarpState<VQ>& st, uint32_t lxV, uint32_t v_m0, int t0,
-                                                int end, int lg) {
+                                                int end, int lmin, int G, int lg) {
+  const int lt2 = 2 * ((int)threadIdx.x & 3);
+  const int e0 = lmin + lt2 / G, e1 = lmin + (lt2 + 1) / G;  // used on masked tiles only
   bool va[NT], vb[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    va[j] = !MASK || t0 + kTile * j + tile_row_token(lg) < end;
-    vb[j] = !MASK || t0 + kTile * j + tile_row_token(lg + 8) < end;
+    const int tA = t0 + kTile * j + tile_row_token(lg), tB = t0 + kTile * j + tile_row_token(lg + 8);
+    va[j] = !MASK || tA < end;
+    vb[j] = !MASK || tB < end;
     if constexpr (MASK) {
-      s[j][0] = va[j] ? s[j][0] : -INFINITY;
-      s[j][1] = va[j] ? s[j][1] : -INFINITY;
-      s[j][2] = vb[j] ? s[j][2] : -INFINITY;
-      s[j][3] = vb[j] ? s[j][3] : -INFINITY;
+      s[j][0] = tA < e0 ? s[j][0] : -INFINITY;
+      s[j][1] = tA < e1 ? s[j][1] : -INFINITY;
+      s[j][2] = tB < e0 ? s[j][2] : -INFINITY;
+      s[j][3] = tB < e1 ? s[j][3] : -INFINITY;
     }
   }
 
@@ -648,11 +662,12 @@ __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[
                                               const uint32_t (&qf)[16], const uint32_t (&qs)[16],
                                               const uint32_t (&qu)[2], uint32_t lxK,
                                               uint32_t lxV, uint32_t k_m0,
-                                              uint32_t v_m0, const DecodeParams& p, int t0, int end, int lg) {
+                                              uint32_t v_m0, const DecodeParams& p, int t0, int end, int lmin,
+                                              int lg) {
   float s[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) key_scores(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale);
-  softmax_readout<NT, MASK>(d, s, st, lxV, v_m0, t0, end, lg);
+  softmax_readout<NT, MASK>(d, s, st, lxV, v_m0, t0, end, lmin, p.G, lg);
 }
 
 // Placement of N equal regions of RS bytes around the code tables, in shared-window addresses:
@@ -737,7 +752,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
 
   const uint32_t my_stages_s = SM::region(warp);
   unsigned char* my_stages = win + my_stages_s;
-  const int G = p.G;
+  const int G = p.G;          // query heads per KV head
+  const int Gc = p.Gc;        // query columns per KV head (G nq)
   const int Hq = p.Hkv * G;
   const int N = p.nblocks;
   long long x = (long long)blockIdx.x * p.W / N;
@@ -763,9 +779,10 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
     const int te = ts + (int)(seg_end - x);
     const int pair = b * p.Hkv + kvh;
 
-    // ---- query fragments: head kvh * G + lg, dims [32 lt, 32 lt + 32)
-    const bool hv = lg < G;
-    const long long qrow = (long long)b * Hq + kvh * G + (hv ? lg : 0);
+    // ---- query fragments: column lg of KV head kvh, dims [32 lt, 32 lt + 32)
+    const bool hv = lg < Gc;
+    const long long qrow = (long long)(b * p.Hkv + kvh) * Gc + (hv ? lg : 0);
+    const int Lmin = L - p.nq + 1;  // causal end of the chunk's first query
     uint32_t qf[16], qs[16], qu[2];
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
@@ -829,12 +846,12 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
           issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * (k + kPairStages),
                                          min(2, nt - 2 * (k + kPairStages)), lane);
         if (two) {
-          if (t0 + 2 * kTile <= L)
-            compute_tiles<2, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+          if (t0 + 2 * kTile <= Lmin)
+            compute_tiles<2, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
           else
-            compute_tiles<2, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+            compute_tiles<2, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
         } else {
-          compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, lg);
+          compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
         }
       } else {
         // QJL and HeadQ variants keep one tile in registers at a time (their extra state leaves no
@@ -851,10 +868,10 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
                                              m0t + 2 * (k + kPairStages), min(2, nt - 2 * (k + kPairStages)), lane);
           }
           const int tj = t0 + j * kTile;
-          if (tj + kTile <= L)
-            compute_tiles<1, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, lg);
+          if (tj + kTile <= Lmin)
+            compute_tiles<1, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, Lmin, lg);
           else
-            compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, lg);
+            compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, Lmin, lg);
         }
       }
     }
@@ -890,8 +907,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
       }
     }
     __syncthreads();
-    float* part_out = p.part + ((long long)(pair + blockIdx.x) * G) * PS;
-    for (int idx = threadIdx.x; idx < G * PS; idx += blockDim.x) {
+    float* part_out = p.part + ((long long)(pair + blockIdx.x) * Gc) * PS;
+    for (int idx = threadIdx.x; idx < Gc * PS; idx += blockDim.x) {
       const int h = idx / PS, e = idx % PS;
       float M = -INFINITY;
 #pragma unroll
@@ -926,9 +943,9 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
     __syncthreads();
     if (s_last) {
       __threadfence();
-      if (warp < G) {
-        const int h = warp;
-        const long long sstride = (long long)G * PS;
+      if (warp < Gc) {
+        const int h = warp;  // query column
+        const long long sstride = (long long)Gc * PS;
         const float* base = p.part + (long long)(pair + c_first) * sstride + h * PS;
         const int ns = c_last - c_first + 1;
         float M = -INFINITY;
@@ -978,7 +995,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
 #pragma unroll
           for (int i = 0; i < 4; ++i) o[i] *= invL;
         }
-        float* dst = p.out + ((long long)b * Hq + kvh * G + h) * kDecD + 4 * lane;
+        float* dst = p.out + (((long long)b * p.nq + h / G) * Hq + kvh * G + h % G) * kDecD + 4 * lane;
         *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
       }
       if (threadIdx.x == 0) p.tickets[pair] = 0;

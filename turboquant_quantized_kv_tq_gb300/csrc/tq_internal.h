@@ -70,6 +70,9 @@ tq_status launch_rotate_basis(const tq_context* ctx, const float* U, Stream stre
 tq_status launch_dequantize(const tq_context* ctx, const void* cache, int b, int kvh, int t0,
                             int t1, float* k_out, float* v_out, Stream stream);
 size_t decode_workspace_bytes(const tq_context* ctx, int max_seq);
+tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const float* q, int nq,
+                              const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
+                              Stream stream);
 tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
                         const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
                         Stream stream);
