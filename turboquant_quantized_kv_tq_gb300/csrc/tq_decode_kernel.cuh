@@ -423,11 +423,20 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
     d.zsA = lds_f16(st + S::KZS + 2 * rA);
     d.zsB = lds_f16(st + S::KZS + 2 * rB);
   }
+  if constexpr (VB == 4) {
+    // 8-byte loads of rows 64 bytes apart: lanes with odd lt take the four tokens in the order
+    // 1, 0, 3, 2, so each load mixes token parities and has 2-way instead of 4-way bank conflicts
+    uint2 t[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      t[k] = *reinterpret_cast<const uint2*>(vst + S::VC + (4 * lt + (k ^ (lt & 1))) * VR + 64 * sl + 8 * lg);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d.v.w[j] = (lt & 1) ? t[j ^ 1] : t[j];
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const unsigned char* v = vst + S::VC + (4 * lt + j) * VR;
     if constexpr (VB == 4) {
-      d.v.w[j] = *reinterpret_cast<const uint2*>(v + 64 * sl + 8 * lg);
     } else if constexpr (VB == 3) {
       d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 32 * sl + 4 * lg);
       d.v.s[j] = lds_u16(v + D / 4 + 16 * sl + 2 * lg);
