@@ -117,7 +117,10 @@ def compare_slab(pair, buf, b, h, T, tokens=None):
             sc_o, sc_g = o["side_scale"], g["side_scale"]
             same_scale = sc_o == sc_g
             ulp_s = np.spacing(np.abs(sc_o)).astype(np.float64)
-            assert np.all(np.abs(sc_g.astype(np.float64) - sc_o.astype(np.float64)) <= ulp_s + 1e-12), "side scale"
+            # a key whose base code differs (exempt, at a cell boundary) has a different residual
+            # and so a different side code and scale: exempt like its signs and rho
+            ok_s = np.abs(sc_g.astype(np.float64) - sc_o.astype(np.float64)) <= ulp_s + 1e-12
+            assert np.all(ok_s | ~vec_ok), ("side scale", np.argwhere(~ok_s & vec_ok)[:5])
             zmis = g["side"] != o["side"]
             zex = (o["side_margin"] < BOUNDARY) | ~same_scale[:, None] | ~vec_ok[:, None]
             assert not (zmis & ~zex).any(), ("side code", np.argwhere(zmis & ~zex)[:5])

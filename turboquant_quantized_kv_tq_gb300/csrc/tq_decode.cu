@@ -12,7 +12,7 @@ constexpr int kLogitsTokensPerBlock = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct WsLayout {
-  size_t err, tickets, q_rot, q_sk, q_u, part, sk_final, sk_part, total;
+  size_t err, tickets, q_rot, q_sk, q_u, q_rot_lo, q_sk_lo, part, sk_final, sk_part, total;
   int ps;
 };
 
@@ -29,12 +29,16 @@ WsLayout ws_layout(const tq_context* ctx) {
   size_t off = 0;
   w.err = off; off = align256(off + 64 * sizeof(int));
   w.tickets = off; off = align256(off + (size_t)pairs * sizeof(int));
-  // query columns per KV head: up to 8 at head dim 128 (several queries per sequence), G otherwise
-  const size_t cols = (size_t)Hkv * (D == kDecD ? kHeadsPad : Hq / Hkv);
+  // eight query columns per KV head (queries of the chunk x heads of the group, then the lo
+  // terms of the queries when they fit); partial slots for up to 8 columns at head dim 128
+  const size_t cols = (size_t)Hkv * kQCols;
   w.q_rot = off; off = align256(off + (size_t)B * cols * D * 2);
   w.q_sk = off; off = align256(off + (ctx->cfg.k.qjl ? (size_t)B * cols * ctx->m * 2 : 0));
   w.q_u = off; off = align256(off + (ctx->cfg.headq_rank ? (size_t)B * cols * 16 * 2 : 0));
-  w.part = off; off = align256(off + (size_t)(pairs + kMaxBlocks) * (cols / Hkv) * w.ps * sizeof(float));
+  w.q_rot_lo = off; off = align256(off + (D == kDecD ? (size_t)B * cols * D * 2 : 0));
+  w.q_sk_lo = off; off = align256(off + (D == kDecD && ctx->cfg.k.qjl ? (size_t)B * cols * ctx->m * 2 : 0));
+  const size_t pcols = D == kDecD ? kHeadsPad : Hq / Hkv;
+  w.part = off; off = align256(off + (size_t)(pairs + kMaxBlocks) * pcols * w.ps * sizeof(float));
   const bool wide_vq = D > kDecD && ctx->cfg.v.qjl;  // acc_sk / l per head for the sketch pass
   w.sk_final = off; off = align256(off + (wide_vq ? (size_t)B * Hq * ctx->m * sizeof(float) : 0));
   w.sk_part = off; off = align256(off + (wide_vq ? (size_t)(ctx->m / kSkRows) * B * Hq * D * sizeof(float) : 0));
@@ -56,6 +60,8 @@ struct PrepParams {
   uint32_t* q_rot;
   uint32_t* q_sk;
   uint32_t* q_u;
+  uint32_t* q_rot_lo;  // lo terms when they do not fit the spare columns (else nullptr)
+  uint32_t* q_sk_lo;
   int* tickets;
   int* err;
   float* out;
@@ -63,6 +69,24 @@ struct PrepParams {
   int n_tickets, n_heads, Hq, Hkv, G, Gc, nq, k_rotate, kq, kh, m;
   int seq_len[TQ_MAX_BATCH];
 };
+
+// E values as fp16 pairs at hi and their fp16 remainders (x - hi) at lo.
+template <int E>
+__device__ __forceinline__ void store_hi_lo(uint32_t* hi, uint32_t* lo, const float (&x)[E]) {
+  uint32_t h[E / 2], l[E / 2];
+#pragma unroll
+  for (int i = 0; i < E; i += 2) {
+    const __half2 hh = __floats2half2_rn(x[i], x[i + 1]);
+    const float2 hf = __half22float2(hh);
+    h[i / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+    l[i / 2] = pack_half2(x[i] - hf.x, x[i + 1] - hf.y);
+  }
+#pragma unroll
+  for (int i = 0; i < E / 2; i += 2) {
+    *reinterpret_cast<uint2*>(hi + i) = make_uint2(h[i], h[i + 1]);
+    *reinterpret_cast<uint2*>(lo + i) = make_uint2(l[i], l[i + 1]);
+  }
+}
 
 // Per query column (one warp, E = D / 32 coordinates per lane; columns [B][Hkv][Gc], column c
 // = query c / G of the sequence, head c % G of the KV head's group): q_rot = R_K q; for head
@@ -107,15 +131,11 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
 #pragma unroll
     for (int i = 0; i < E; ++i) x[i] *= rs;
   }
-  uint32_t* qr = p.q_rot + (long long)head * (D / 2) + lane * (E / 2);
-  if constexpr (E == 4) {
-    *reinterpret_cast<uint2*>(qr) = make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
-  } else {
-#pragma unroll
-    for (int i = 0; i < E; i += 8)
-      *reinterpret_cast<uint4*>(qr + i / 2) = make_uint4(pack_half2(x[i], x[i + 1]), pack_half2(x[i + 2], x[i + 3]),
-                                                         pack_half2(x[i + 4], x[i + 5]), pack_half2(x[i + 6], x[i + 7]));
-  }
+  // hi term to column c, lo term (x - hi) to column Gc + c or to the separate lo array
+  const long long col = ((long long)b * p.Hkv + kvh) * kQCols + c;
+  const long long col_lo = p.q_rot_lo ? col : col + p.Gc;
+  uint32_t* lo_base = p.q_rot_lo ? p.q_rot_lo : p.q_rot;
+  store_hi_lo<E>(p.q_rot + col * (D / 2) + lane * (E / 2), lo_base + col_lo * (D / 2) + lane * (E / 2), x);
   if constexpr (D == kDecD) {
     if (p.kq) {
       float a[4] = {0.f, 0.f, 0.f, 0.f};
@@ -129,8 +149,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
           a[2] = fmaf(s4.z, xj, a[2]); a[3] = fmaf(s4.w, xj, a[3]);
         }
       }
-      *reinterpret_cast<uint2*>(p.q_sk + (long long)head * (D / 2) + 2 * lane) =
-          make_uint2(pack_half2(a[0], a[1]), pack_half2(a[2], a[3]));
+      uint32_t* sk_lo = p.q_sk_lo ? p.q_sk_lo : p.q_sk;
+      store_hi_lo<4>(p.q_sk + col * (D / 2) + 2 * lane, sk_lo + col_lo * (D / 2) + 2 * lane, a);
     }
     if (p.kh) {
       const float* Ur = p.tab.U_rot + (long long)kvh * D * 16;
@@ -149,7 +169,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
 #pragma unroll
       for (int k = 0; k < 16; ++k) z[k] = warp_sum(z[k]);
       if (lane == 0) {
-        uint32_t* dst = p.q_u + (long long)head * 8;
+        uint32_t* dst = p.q_u + col * 8;
 #pragma unroll
         for (int k = 0; k < 8; ++k) dst[k] = pack_half2(z[2 * k], z[2 * k + 1]);
       }
@@ -225,6 +245,14 @@ tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const fl
   pp.q_rot = (uint32_t*)(base + w.q_rot);
   pp.q_sk = (uint32_t*)(base + w.q_sk);
   pp.q_u = (uint32_t*)(base + w.q_u);
+  const int Gc = (Hq / Hkv) * nq;
+  const bool lo_sep = 2 * Gc > kQCols;  // the lo terms do not fit the spare columns
+  if (lo_sep && D != kDecD) {
+    set_error("head dims above 128 are built for H_q / H_kv <= 4");
+    return TQ_ERR_UNSUPPORTED;
+  }
+  pp.q_rot_lo = lo_sep ? (uint32_t*)(base + w.q_rot_lo) : nullptr;
+  pp.q_sk_lo = lo_sep ? (uint32_t*)(base + w.q_sk_lo) : nullptr;
   pp.tickets = (int*)(base + w.tickets);
   pp.err = (int*)(base + w.err);
   pp.n_tickets = B * Hkv;
@@ -262,6 +290,9 @@ tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const fl
   p.q_rot = pp.q_rot;
   p.q_sk = pp.q_sk;
   p.q_u = pp.q_u;
+  p.q_rot_lo = pp.q_rot_lo;
+  p.q_sk_lo = pp.q_sk_lo;
+  p.lo_xor = lo_sep ? 0 : (Gc == 1 ? -1 : Gc / 2);
   p.part = (float*)(base + w.part);
   p.tickets = pp.tickets;
   p.out = out;

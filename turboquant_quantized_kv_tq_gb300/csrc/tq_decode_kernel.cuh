@@ -42,6 +42,7 @@ constexpr int kLogitsWarps = 8;
 // the QJL variants carry 16-32 more accumulator / fragment registers and use 12.
 template <bool KQ, bool VQ>
 struct DecWarps { static constexpr int value = (KQ || VQ) ? 12 : 16; };
+constexpr int kQCols = 8;  // query columns per KV head in the prepared query arrays
 constexpr int kTile = 16;
 constexpr int kHeadsPad = 8;
 constexpr int kPairStages = 2;  // per-warp ring of 32-token (two-tile) stages
@@ -53,9 +54,15 @@ struct DecodeParams {
   Cache cache;
   // Query columns: column c of KV head h is query i = c / G of the chunk, head h G + c % G
   // (nq queries per sequence, Gc = G nq <= 8 columns; nq = 1 is plain decode).
-  const uint32_t* q_rot;  // fp16 pairs [B][Hkv][Gc][D/2]
-  const uint32_t* q_sk;   // fp16 pairs [B][Hkv][Gc][m/2]
-  const uint32_t* q_u;    // fp16 pairs [B][Hkv][Gc][8]
+  // Queries are split into two fp16 terms, hi + lo (one rounding of q alone is a systematic
+  // score error that long contexts turn into an output error of ~3e-3).  With 2 Gc <= 8 the lo
+  // terms ride in columns Gc .. 2 Gc - 1 of the same MMA and are added back by a shuffle
+  // (lo_xor); otherwise they sit in q_rot_lo / q_sk_lo and get their own MMA.
+  const uint32_t* q_rot;  // fp16 pairs [B][Hkv][8 columns][D/2]
+  const uint32_t* q_sk;   // fp16 pairs [B][Hkv][8][m/2]
+  const uint32_t* q_u;    // fp16 pairs [B][Hkv][8][8] (hi term only: a small correction)
+  const uint32_t* q_rot_lo;  // [B][Hkv][8][D/2], separate lo terms
+  const uint32_t* q_sk_lo;
   float* part;            // [B*Hkv + kMaxBlocks][G][PS]; slab p's partial from block c at p + c
   int* tickets;           // [B*Hkv]
   int* err;               // device error word
@@ -63,6 +70,7 @@ struct DecodeParams {
   float* sk_final;        // [B][Hq][m]: acc_sk / l (head dim > 128 with a QJL value side)
   int B, Hkv, G, v_rotate, nblocks;
   int nq, Gc;             // queries per sequence (query i sees tokens [0, seq_len - nq + 1 + i))
+  int lo_xor;             // lo columns: lane xor to add them back (Gc / 2), -1 when Gc = 1
   long long W;            // number of 16-token tiles over all (batch, KV head) slabs
   float score_scale;      // log2(e) / sqrt(d)
   float qjl_scale;        // sqrt(pi/2) / m
@@ -500,20 +508,25 @@ __device__ __forceinline__ void load_ktile(TileData<KB, KQ, KH, VB, VQ>& d, cons
 // Key scores of the thread's four accumulator slots (tokens pi(lg), pi(lg+8) x heads 2 lt,
 // 2 lt + 1), times `sscale`: nu <q_rot, C[c]> (+ nu rho sqrt(pi/2)/m <S q_rot, 2 sigma - 1>)
 // (+ scale <U^T q, zeta>).  sscale = 1/sqrt(d) gives the logit.
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
+//
+// The query's fp16 lo terms: with QLO in qfl / qsl (own MMAs on the same key fragments);
+// otherwise, when lo_xor != 0, in other columns whose scores are added back at the end.
+template <bool QLO = false, int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, float (&s)[4],
                                            const uint32_t (&qf)[16], const uint32_t (&qs)[16],
                                            const uint32_t (&qu)[2], uint32_t lxK, uint32_t k_m0,
-                                           float qjl_scale, float sscale) {
+                                           float qjl_scale, float sscale, const uint32_t (&qfl)[16],
+                                           const uint32_t (&qsl)[16], int lo_xor) {
   d.kA.prepare();
   d.kB.prepare();
   // two independent accumulator chains (even / odd k-steps) halve the MMA dependency chain
   float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    mma16816(sc[ks & 1], d.kA.pair(lxK, k_m0, 2 * ks), d.kB.pair(lxK, k_m0, 2 * ks),
-             d.kA.pair(lxK, k_m0, 2 * ks + 1), d.kB.pair(lxK, k_m0, 2 * ks + 1), qf[2 * ks],
-             qf[2 * ks + 1]);
+    const uint32_t a0 = d.kA.pair(lxK, k_m0, 2 * ks), a1 = d.kB.pair(lxK, k_m0, 2 * ks);
+    const uint32_t a2 = d.kA.pair(lxK, k_m0, 2 * ks + 1), a3 = d.kB.pair(lxK, k_m0, 2 * ks + 1);
+    mma16816(sc[ks & 1], a0, a1, a2, a3, qf[2 * ks], qf[2 * ks + 1]);
+    if constexpr (QLO) mma16816(sc[ks & 1], a0, a1, a2, a3, qfl[2 * ks], qfl[2 * ks + 1]);
   }
   const float nA = d.nuKA * sscale, nB = d.nuKB * sscale;
   s[0] = (sc[0][0] + sc[1][0]) * nA;
@@ -526,8 +539,10 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
     float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      mma16816(sq, d.sA.pair(2 * ks), d.sB.pair(2 * ks), d.sA.pair(2 * ks + 1), d.sB.pair(2 * ks + 1),
-               qs[2 * ks], qs[2 * ks + 1]);
+      const uint32_t a0 = d.sA.pair(2 * ks), a1 = d.sB.pair(2 * ks);
+      const uint32_t a2 = d.sA.pair(2 * ks + 1), a3 = d.sB.pair(2 * ks + 1);
+      mma16816(sq, a0, a1, a2, a3, qs[2 * ks], qs[2 * ks + 1]);
+      if constexpr (QLO) mma16816(sq, a0, a1, a2, a3, qsl[2 * ks], qsl[2 * ks + 1]);
     }
     const float fa = nA * d.rhoKA * qjl_scale, fb = nB * d.rhoKB * qjl_scale;
     s[0] = fmaf(sq[0], fa, s[0]);
@@ -543,6 +558,13 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
     s[1] = fmaf(sz[1], zA, s[1]);
     s[2] = fmaf(sz[2], zB, s[2]);
     s[3] = fmaf(sz[3], zB, s[3]);
+  }
+  if (lo_xor > 0) {  // lo columns (2 lt ^ 2 lo_xor, ...) belong to this thread's hi columns
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] += __shfl_xor_sync(kFull, s[k], lo_xor);
+  } else if (lo_xor < 0) {  // one query column: its lo term is column 1 of the same thread
+    s[0] += s[1];
+    s[2] += s[3];
   }
 }
 
@@ -666,16 +688,18 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
 }
 
 // Scores and online-softmax step of NT consecutive tiles held by one warp (head dim 128).
-template <int NT, bool MASK, int KB, bool KQ, bool KH, int VB, bool VQ>
+template <int NT, bool MASK, bool QLO, int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ>& st,
                                               const uint32_t (&qf)[16], const uint32_t (&qs)[16],
-                                              const uint32_t (&qu)[2], uint32_t lxK,
+                                              const uint32_t (&qu)[2], const uint32_t (&qfl)[16],
+                                              const uint32_t (&qsl)[16], uint32_t lxK,
                                               uint32_t lxV, uint32_t k_m0,
                                               uint32_t v_m0, const DecodeParams& p, int t0, int end, int lmin,
                                               int lg) {
   float s[NT][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) key_scores(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale);
+  for (int j = 0; j < NT; ++j)
+    key_scores<QLO>(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale, qfl, qsl, p.lo_xor);
   softmax_readout<NT, MASK>(d, s, st, lxV, v_m0, t0, end, lmin, p.G, lg);
 }
 
@@ -706,13 +730,13 @@ struct RegionPlan {
 
 // Shared-memory plan of a decode block: per-warp regions (the warp's bulk-copy ring, later its
 // merge slot) placed by RegionPlan, then one mbarrier per pair stage and warp.
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
+template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO = false>
 struct DecodeSmem {
   static constexpr uint32_t lutK = LutEntries<KB>::value * kLutStride;
   static constexpr uint32_t lutV = KB == VB ? 0 : LutEntries<VB>::value * kLutStride;  // same codebook
   static constexpr bool sepV = lutV > 0;
   static constexpr int PS = 4 + kDecD + (VQ ? kDecD : 0);  // per head: m, l, pad, pad, acc, (acc_sk)
-  static constexpr int NW = DecWarps<KQ, VQ>::value;
+  static constexpr int NW = DecWarps<KQ, VQ || QLO>::value;
   static constexpr uint32_t ring = kPairStages * 2 * Stage<KB, KQ, KH, VB, VQ>::bytes;
   static constexpr uint32_t mslot = kHeadsPad * PS * 4;
   static constexpr uint32_t RS = ring > mslot ? ring : mslot;
@@ -731,9 +755,9 @@ constexpr uint32_t kWaitLimit = 1u << 20;  // polls of an mbarrier before giving
 constexpr int kErrWaitTimeout = 1;
 constexpr int kErrSmemPlan = 2;
 
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
-__global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel(const DecodeParams p) {
-  using SM = DecodeSmem<KB, KQ, KH, VB, VQ>;
+template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO>
+__global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode_kernel(const DecodeParams p) {
+  using SM = DecodeSmem<KB, KQ, KH, VB, VQ, QLO>;
   using SG = Stage<KB, KQ, KH, VB, VQ>;
   constexpr int PS = SM::PS;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -788,9 +812,10 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
     const int te = ts + (int)(seg_end - x);
     const int pair = b * p.Hkv + kvh;
 
-    // ---- query fragments: column lg of KV head kvh, dims [32 lt, 32 lt + 32)
-    const bool hv = lg < Gc;
-    const long long qrow = (long long)(b * p.Hkv + kvh) * Gc + (hv ? lg : 0);
+    // ---- query fragments: column lg of KV head kvh, dims [32 lt, 32 lt + 32); columns Gc ..
+    // 2 Gc - 1 hold the lo terms when they ride in the same MMA
+    const bool hv = lg < (QLO ? Gc : 2 * Gc);
+    const long long qrow = (long long)(b * p.Hkv + kvh) * kQCols + (hv ? lg : 0);
     const int Lmin = L - p.nq + 1;  // causal end of the chunk's first query
     uint32_t qf[16], qs[16], qu[2];
 #pragma unroll
@@ -809,9 +834,26 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
         qs[i] = v.x; qs[i + 1] = v.y; qs[i + 2] = v.z; qs[i + 3] = v.w;
       }
     }
+    uint32_t qfl[16], qsl[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qfl[i] = qsl[i] = 0;
+    if constexpr (QLO) {
+      const bool hl = lg < Gc;
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const uint4 v = hl ? *reinterpret_cast<const uint4*>(p.q_rot_lo + qrow * (kDecD / 2) + 16 * lt + i)
+                           : make_uint4(0, 0, 0, 0);
+        qfl[i] = v.x; qfl[i + 1] = v.y; qfl[i + 2] = v.z; qfl[i + 3] = v.w;
+        if constexpr (KQ) {
+          const uint4 w = hl ? *reinterpret_cast<const uint4*>(p.q_sk_lo + qrow * (kDecD / 2) + 16 * lt + i)
+                             : make_uint4(0, 0, 0, 0);
+          qsl[i] = w.x; qsl[i + 1] = w.y; qsl[i + 2] = w.z; qsl[i + 3] = w.w;
+        }
+      }
+    }
     qu[0] = qu[1] = 0;
     if constexpr (KH) {
-      if (hv) {
+      if (lg < Gc) {  // hi columns only: a lo column must carry lo terms alone
         qu[0] = p.q_u[qrow * 8 + lt];
         qu[1] = p.q_u[qrow * 8 + lt + 4];
       }
@@ -856,11 +898,11 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
                                          min(2, nt - 2 * (k + kPairStages)), lane);
         if (two) {
           if (t0 + 2 * kTile <= Lmin)
-            compute_tiles<2, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
+            compute_tiles<2, false, QLO>(d, st, qf, qs, qu, qfl, qsl, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
           else
-            compute_tiles<2, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
+            compute_tiles<2, true, QLO>(d, st, qf, qs, qu, qfl, qsl, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
         } else {
-          compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
+          compute_tiles<1, true, QLO>(d, st, qf, qs, qu, qfl, qsl, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
         }
       } else {
         // QJL and HeadQ variants keep one tile in registers at a time (their extra state leaves no
@@ -878,9 +920,9 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ>::value * 32, 1) decode_kernel
           }
           const int tj = t0 + j * kTile;
           if (tj + kTile <= Lmin)
-            compute_tiles<1, false>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, Lmin, lg);
+            compute_tiles<1, false, QLO>(d, st, qf, qs, qu, qfl, qsl, lxK, lxV, k_m0, v_m0, p, tj, L, Lmin, lg);
           else
-            compute_tiles<1, true>(d, st, qf, qs, qu, lxK, lxV, k_m0, v_m0, p, tj, L, Lmin, lg);
+            compute_tiles<1, true, QLO>(d, st, qf, qs, qu, qfl, qsl, lxK, lxV, k_m0, v_m0, p, tj, L, Lmin, lg);
         }
       }
     }
@@ -1121,7 +1163,7 @@ __global__ void __launch_bounds__(kLogitsWarps * 32) logits_kernel(const LogitsP
     TileData<KB, KQ, KH, 1, false> d;
     load_ktile(d, sp, t0, w1 - 1, lg, lt);
     float s[4];
-    key_scores(d, s, qf, qs, qu, kLutAddrK | (4u * lane), k_m0, p.qjl_scale, p.inv_sqrt_d);
+    key_scores(d, s, qf, qs, qu, kLutAddrK | (4u * lane), k_m0, p.qjl_scale, p.inv_sqrt_d, qs, qs, 0);
     const int tA = t0 + tile_row_token(lg), tB = t0 + tile_row_token(lg + 8);
     const long long r0 = ((long long)b * Hq + kvh * G + 2 * lt) * p.stride;
     const long long r1 = r0 + p.stride;
@@ -1151,16 +1193,16 @@ cudaError_t check_dyn_base(K kernel) {
 }
 
 // Launch helpers used by the per-bit-width instantiation units.
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
+template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
-  using SM = DecodeSmem<KB, KQ, KH, VB, VQ>;
+  using SM = DecodeSmem<KB, KQ, KH, VB, VQ, QLO>;
   static_assert(SM::bytes <= 227 * 1024, "decode shared memory exceeds the per-block limit");
-  cudaError_t e = check_dyn_base(decode_kernel<KB, KQ, KH, VB, VQ>);
+  cudaError_t e = check_dyn_base(decode_kernel<KB, KQ, KH, VB, VQ, QLO>);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<KB, KQ, KH, VB, VQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_kernel<KB, KQ, KH, VB, VQ, QLO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SM::bytes);
   if (e != cudaSuccess) return e;
-  decode_kernel<KB, KQ, KH, VB, VQ><<<grid, SM::NW * 32, SM::bytes, s>>>(p);
+  decode_kernel<KB, KQ, KH, VB, VQ, QLO><<<grid, SM::NW * 32, SM::bytes, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -1189,7 +1231,8 @@ bool dispatch_logits_k4(int kq, int kh, const LogitsParams& p, dim3 g, cudaStrea
 
 #define TQ_DECODE_CASE(KB_, KQ_, KH_, VB_, VQ_)                                           \
   if (kq == KQ_ && kh == KH_ && vb == VB_ && vq == VQ_) {                                 \
-    if (e) *e = launch_decode_t<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0>(p, g, s);         \
+    if (e) *e = p.lo_xor == 0 ? launch_decode_t<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0, true>(p, g, s)      \
+                              : launch_decode_t<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0, false>(p, g, s);    \
     return true;                                                                          \
   }
 #define TQ_LOGITS_CASE(KB_, KQ_, KH_)                                                     \

@@ -122,9 +122,10 @@ __global__ void __launch_bounds__(WideCfg<D, KB, VB, VQ>::NW * 32, 1) decode_wid
     const int te = ts + (int)(seg_end - x);
     const int pair = b * p.Hkv + kvh;
 
-    // ---- query fragments of this warp's slice: head kvh * G + lg, dims 128 sl + [32 lt, 32 lt + 32)
-    const bool hv = lg < G;
-    const long long qrow = (long long)b * Hq + kvh * G + (hv ? lg : 0);
+    // ---- query fragments of this warp's slice: column lg of KV head kvh (columns G .. 2 G - 1
+    // hold the lo terms), dims 128 sl + [32 lt, 32 lt + 32)
+    const bool hv = lg < 2 * G;
+    const long long qrow = (long long)(b * p.Hkv + kvh) * kQCols + (hv ? lg : 0);
     uint32_t qf[16];
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(WideCfg<D, KB, VB, VQ>::NW * 32, 1) decode_wid
       read_stage<KB, false, false, VB, VQ, D>(d[0], stg, stg, lg, lt, sl);
       fence_proxy_async_shared();
       float s[1][4];
-      key_scores(d[0], s[0], qf, zero16, zero2, lxK, k_m0, p.qjl_scale, p.score_scale);
+      key_scores(d[0], s[0], qf, zero16, zero2, lxK, k_m0, p.qjl_scale, p.score_scale, zero16, zero16, p.lo_xor);
       float4* xb = xch + (i & 1) * DS * 32;
       xb[sl * 32 + lane] = make_float4(s[0][0], s[0][1], s[0][2], s[0][3]);
       named_barrier(1 + grp, DS * 32);  // every warp of the group has read the stage and written
