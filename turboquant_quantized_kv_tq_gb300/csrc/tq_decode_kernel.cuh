@@ -626,20 +626,25 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
     }
   }
 
-  // ---- online softmax (log2 domain)
+  // ---- online softmax (log2 domain).  A column's maximum over the tiles exceeds its running
+  // maximum exactly when some lane's own maximum does, so the max-reduction across the lanes of
+  // a column (and the rescale) runs only on tiles that raise a maximum; elsewhere the running
+  // maximum is already the new one.
   float mx0 = fmaxf(s[0][0], s[0][2]), mx1 = fmaxf(s[0][1], s[0][3]);
 #pragma unroll
   for (int j = 1; j < NT; ++j) {
     mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][2]));
     mx1 = fmaxf(mx1, fmaxf(s[j][1], s[j][3]));
   }
+  float n0 = st.m0, n1 = st.m1;
+  if (__any_sync(kFull, mx0 > st.m0 || mx1 > st.m1)) {
 #pragma unroll
-  for (int m = 4; m <= 16; m <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, m));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, m));
-  }
-  const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
-  if (__any_sync(kFull, n0 > st.m0 || n1 > st.m1)) {
+    for (int m = 4; m <= 16; m <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, m));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, m));
+    }
+    n0 = fmaxf(st.m0, mx0);
+    n1 = fmaxf(st.m1, mx1);
     const float a0 = ex2(st.m0 - n0), a1 = ex2(st.m1 - n1);
     st.l0 *= a0;
     st.l1 *= a1;
