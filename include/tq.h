@@ -85,7 +85,7 @@ typedef struct {
 } tq_config;
 
 #define TQ_MAX_BATCH 512
-#define TQ_LAYOUT_VERSION 2u
+#define TQ_LAYOUT_VERSION 3u
 #define TQ_TILE_TOKENS 16
 
 /* One field of a side's 16-token block: `offset` within the block, `record_bytes` per token
@@ -102,6 +102,12 @@ typedef struct {
  * block (b * H_kv + h) * capacity / 16 + t / 16 at position t % 16.  A K block holds, one after
  * another, 16 records of each present field: codes, norm, [signs, rho], [side, side_scale]; a V
  * block: codes, norm, [signs, rho].  So one contiguous copy brings all of a tile's data of a side.
+ * Record p of a field sits at offset + p * record_bytes, except the V block's streams (its codes,
+ * each stream of a 3-bit code on its own, and its QJL signs): a w-bit stream there is stored by
+ * groups of 16 coordinates, [coordinates / 16][16 tokens][2w bytes], so byte j of token p's record
+ * is at (j / 2w) * 32w + p * 2w + j % 2w from the stream's start (the 1-bit stream of a 3-bit code
+ * starts 16 * d / 4 bytes after the 2-bit one).  One coordinate group of several tokens is then
+ * one contiguous read.
  * Codes are stored in sign-magnitude form (s = [c >= 2^(b-1)], k = magnitude rank) as streams of
  * power-of-two widths, coordinate i of a w-bit stream in bits [w*i, w*i + w), least significant
  * bit first:
@@ -224,7 +230,53 @@ tq_status tq_headq_correct(const tq_context* ctx, const void* dev_cache, const f
 tq_status tq_dequantize(const tq_context* ctx, const void* dev_cache, int32_t b, int32_t kvh,
                         int32_t t0, int32_t t1, float* k_out, float* v_out, tq_stream stream);
 
-/* Wait for stream, then read the device error word of a decode workspace: 0 = none. */
+/* ---- Paged cache (serving layout) ---------------------------------------------------------
+ * The pages speak of KV-cache traffic in serving terms ([ABL] "Declaração do Problema") but give
+ * no cache organisation; this one is the library's own.  A pool of pages replaces the
+ * [B][H_kv][capacity] slabs: a page holds one 16-token block per KV head on each side, so page p's
+ * K block of head h is K block p * H_kv + h (and likewise for V), each block laid out exactly as
+ * in tq_cache_layout.  A block table maps logical block j of sequence b (tokens 16 j .. 16 j + 15)
+ * to a page.  Sequence lengths and append positions come from device memory, so a serving step
+ * (append + decode) can be captured once in a CUDA graph and replayed while they change.
+ * Entries are not checked on the host.  On the device, a position at or past
+ * 16 * max_blocks_per_seq, or a page outside [0, num_pages), is redirected to an extra page at
+ * the end of the pool that belongs to no sequence, and an error code is recorded.  Memory
+ * outside the pool is never touched.  Built for head dim 128. */
+typedef struct {
+  const int32_t* block_table;   /* device [B][max_blocks_per_seq] page indices */
+  int32_t max_blocks_per_seq;
+  int32_t num_pages;            /* pages the caller owns in the pool */
+} tq_page_table;
+
+/* Device error codes (tq_get_device_error, or the append's dev_error word). */
+#define TQ_DEVERR_WAIT_TIMEOUT 1  /* a bulk-copy wait gave up (the output is not valid)        */
+#define TQ_DEVERR_SMEM_PLAN 2     /* the shared-memory plan did not fit the launch             */
+#define TQ_DEVERR_BAD_PAGE 3      /* a block-table entry or position outside the pool/table    */
+#define TQ_DEVERR_BAD_LENGTH 4    /* a device sequence length outside [0, 16 * max_blocks]     */
+
+/* Layout of a pool of num_pages pages (plus the one redirect page): total_bytes and the block
+ * offsets/sizes of the K and V arrays, each [(num_pages + 1) * H_kv] blocks. */
+tq_status tq_get_paged_cache_layout(const tq_context* ctx, int32_t num_pages, tq_cache_layout* out);
+
+/* tq_quantize_append into a paged pool: token j of (b, h) goes to position dev_start[b] + j
+ * (dev_start: device int32 [B]).  k, v as for tq_quantize_append.  dev_error: device int32 or
+ * NULL; on a bad position or page the kernel stores a TQ_DEVERR_* code there (the caller zeroes
+ * it beforehand). */
+tq_status tq_quantize_append_paged(const tq_context* ctx, void* dev_pool, const tq_page_table* pages,
+                                   const void* k, const void* v, tq_dtype dtype, int32_t n_new,
+                                   const int32_t* dev_start, int32_t* dev_error, tq_stream stream);
+
+/* tq_decode_attention_multi over a paged pool with device sequence lengths (dev_seq_len: device
+ * int32 [B], each in [0, 16 * max_blocks_per_seq]; a length outside is clamped and recorded as
+ * TQ_DEVERR_BAD_LENGTH).  ws: tq_decode_workspace_bytes(ctx, 16 * max_blocks_per_seq) bytes.
+ * nq = 1 is plain decode.  The work split over the GPU is computed on the device from the
+ * lengths. */
+tq_status tq_decode_attention_paged(const tq_context* ctx, const void* dev_pool, const tq_page_table* pages,
+                                    const float* q, int32_t nq, const int32_t* dev_seq_len, float* out,
+                                    void* ws, size_t ws_bytes, tq_stream stream);
+
+/* Wait for stream, then read the device error word of a decode workspace: 0 = none, else a
+ * TQ_DEVERR_* code. */
 tq_status tq_get_device_error(const void* ws, int32_t* code, tq_stream stream);
 
 const char* tq_status_string(tq_status status);

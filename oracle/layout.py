@@ -23,9 +23,16 @@ produce and parse cache buffers byte for byte:
   when present), each field 16 records long:
   K block: codes, norm (fp32), [signs, rho (fp16)], [side, side_scale (fp16)];
   V block: codes, norm (fp32), [signs, rho (fp16)].
-  Field f of token t of (batch b, KV head h) is at
-  side_offset + ((b * H_kv + h) * capacity / 16 + t // 16) * block_bytes
-  + field_offset + (t % 16) * record_bytes.
+  Token t of (batch b, KV head h) is in block
+  side_offset + ((b * H_kv + h) * capacity / 16 + t // 16) * block_bytes, at
+  position p = t % 16.  A field of fixed-size records stores record p at
+  field_offset + p * record_bytes, except the value side's streams: the codes
+  (each stream of a b = 3 code on its own, one after the other) and the QJL
+  signs of a V block are stored by groups of 16 coordinates.  In a w-bit
+  stream each group holds the 2w bytes of coordinates [16 g, 16 g + 16) of the
+  16 tokens, [groups][16 tokens][2w bytes], so byte j of token p's record is at
+  stream_offset + (j // 2w) * 32 w + p * 2w + j % 2w.  (A decoder that reads
+  one coordinate group for several tokens then makes one contiguous load.)
 """
 
 from dataclasses import dataclass
@@ -84,8 +91,48 @@ def layout(shape):
     return out
 
 
+def grouped_streams(shape, name):
+    """[(width w, coordinates n)] of a value-side field stored by coordinate groups, else None."""
+    if name == "v_codes":
+        d, b = shape.head_dim, shape.v_bits
+        return {4: [(4, d)], 3: [(2, d), (1, d)], 2: [(2, d)], 1: [(1, d)]}[b]
+    if name == "v_signs":
+        return [(1, shape.m)]
+    return None
+
+
+def record_byte_positions(shape, name, p):
+    """In-field byte offset of each byte of the records of block positions p (array): shape
+    (len(p), record bytes)."""
+    p = np.asarray(p, dtype=np.int64)
+    rec = dict(side_fields(shape, name[0]))[name]
+    streams = grouped_streams(shape, name)
+    if streams is None:
+        return p[:, None] * rec + np.arange(rec)[None, :]
+    cols, base = [], 0
+    for w, n in streams:
+        j = np.arange(n * w // 8)
+        cols.append(base + (j // (2 * w))[None, :] * 32 * w + p[:, None] * 2 * w + (j % (2 * w))[None, :])
+        base += TILE * n * w // 8
+    return np.concatenate(cols, axis=1)
+
+
+def field_positions(shape, name, b, h, t):
+    """Absolute byte positions (len(t) x record bytes) of field ``name`` of tokens t of slab (b, h)."""
+    lay = layout(shape)
+    side = lay[name[0]]
+    foff, rec = side["fields"][name]
+    t = np.asarray(t, dtype=np.int64)
+    slab = b * shape.num_kv_heads + h
+    blk = slab * (shape.capacity // TILE) + t // TILE
+    start = side["offset"] + blk * side["block"] + foff
+    return start[:, None] + record_byte_positions(shape, name, t % TILE)
+
+
 def field_offsets(shape, name, b, h, t):
-    """Byte offset of field ``name`` of tokens t (array) of slab (b, h)."""
+    """Byte offset of field ``name`` of tokens t (array) of slab (b, h), for the fields stored
+    as whole records (every field but the value side's streams)."""
+    assert grouped_streams(shape, name) is None
     lay = layout(shape)
     side = lay[name[0]]
     foff, rec = side["fields"][name]
@@ -180,13 +227,11 @@ def write_fields(buf, shape, b, h, t0, fields):
         arr = np.asarray(val)
         if arr.dtype != np.uint8:
             arr = arr.view(np.uint8).reshape(arr.shape[0], -1)
-        off, rec = field_offsets(shape, name, b, h, np.arange(t0, t0 + arr.shape[0]))
-        buf[off[:, None] + np.arange(rec)[None, :]] = arr
+        buf[field_positions(shape, name, b, h, np.arange(t0, t0 + arr.shape[0]))] = arr
 
 
 def read_field(buf, shape, name, b, h, t0, t1, dtype=None):
-    off, rec = field_offsets(shape, name, b, h, np.arange(t0, t1))
-    raw = np.asarray(buf, dtype=np.uint8)[off[:, None] + np.arange(rec)[None, :]].copy()
+    raw = np.asarray(buf, dtype=np.uint8)[field_positions(shape, name, b, h, np.arange(t0, t1))].copy()
     if dtype is None:
         return raw
     return raw.view(dtype).reshape(t1 - t0)

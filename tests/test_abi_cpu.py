@@ -164,7 +164,7 @@ def test_layout_matches_oracle(scheme, n, headq):
     ctx = _ctx(c)
     lay = b.tq_cache_layout()
     b.check(b.tq_get_cache_layout(ctx, lay))
-    assert lay.layout_version == 2 and lay.tile_tokens == 16
+    assert lay.layout_version == 3 and lay.tile_tokens == 16
     shape = layout.CacheShape(3, 2, 192, 128, c.k.bits, bool(c.k.qjl), c.v.bits, bool(c.v.qjl), 128, headq, 4)
     want = layout.layout(shape)
     assert lay.total_bytes == want["total"]

@@ -77,11 +77,27 @@ def test_blocks_aligned_and_disjoint():
     for name, _ in layout.side_fields(shape, "k") + layout.side_fields(shape, "v"):
         for b in range(3):
             for h in range(2):
-                off, rec = layout.field_offsets(shape, name, b, h, np.arange(64))
-                idx = (off[:, None] + np.arange(rec)[None, :]).ravel()
+                idx = layout.field_positions(shape, name, b, h, np.arange(64)).ravel()
                 assert np.all(owner[idx] == -1), name
                 owner[idx] = 1
     assert np.all(owner[:3 * 2 * 4 * k["block"]] == 1)
+    assert np.all(owner[v["offset"]:] == 1)
+
+
+def test_value_streams_grouped_by_16_coordinates():
+    # d = 32, 3-bit values with QJL (m = 32): the 2-bit stream (8 B per token) in groups of
+    # 16 coordinates = 4 B, then the 1-bit stream (4 B per token) in groups of 2 B; the QJL
+    # signs likewise; key fields stay whole records
+    shape = layout.CacheShape(1, 1, 16, 32, 4, False, 3, True, 32)
+    p = np.array([0, 5])
+    got = layout.record_byte_positions(shape, "v_codes", p)
+    two = [(j // 4) * 64 + p * 4 + j % 4 for j in range(8)]
+    one = [128 + (j // 2) * 32 + p * 2 + j % 2 for j in range(4)]
+    assert np.array_equal(got, np.stack(two + one, axis=1))
+    sg = layout.record_byte_positions(shape, "v_signs", p)
+    assert np.array_equal(sg, np.stack([(j // 2) * 32 + p * 2 + j % 2 for j in range(4)], axis=1))
+    kc = layout.record_byte_positions(shape, "k_codes", p)
+    assert np.array_equal(kc, p[:, None] * 16 + np.arange(16)[None, :])
 
 
 def test_zero_vector():

@@ -12,7 +12,7 @@ import numpy as np
 from . import binding as _b
 from .binding import TQError, check  # noqa: F401
 
-__all__ = ["QuantizedKVCache", "TQError", "binding"]
+__all__ = ["QuantizedKVCache", "PagedKVCache", "TQError", "binding"]
 
 _DTYPES = None
 
@@ -31,15 +31,11 @@ def _stream_handle(stream=None):
     return s.cuda_stream
 
 
-class QuantizedKVCache:
-    """One packed KV cache of shape [batch][num_kv_heads][capacity] tokens on a CUDA device.
+class _Codec:
+    """A library context for one configuration with its tables uploaded to ``device``."""
 
-    ``scheme``/``n`` pick the codecs as ``tq_config_from_scheme`` does; ``k_codec``/``v_codec``
-    (tuples bits, rotate, qjl) override them.  ``headq_rank`` = 16 turns the HeadQ side code on.
-    """
-
-    def __init__(self, head_dim, num_q_heads, num_kv_heads, batch, capacity, scheme="tq", n=4,
-                 seed=0, k_codec=None, v_codec=None, headq_rank=0, headq_bits=4, device="cuda"):
+    def _setup(self, head_dim, num_q_heads, num_kv_heads, batch, capacity, scheme, n, seed, k_codec,
+               v_codec, headq_rank, headq_bits, device):
         import torch
         cfg = _b.tq_config()
         cfg.head_dim, cfg.num_q_heads, cfg.num_kv_heads = head_dim, num_q_heads, num_kv_heads
@@ -60,12 +56,6 @@ class QuantizedKVCache:
         self.batch, self.capacity = batch, capacity
         self.tables = torch.empty(int(_b.tq_tables_bytes(ctx)), dtype=torch.uint8, device=self.device)
         check(_b.tq_tables_upload(ctx, self.tables.data_ptr(), _stream_handle()))
-        lay = _b.tq_cache_layout()
-        check(_b.tq_get_cache_layout(ctx, lay))
-        self.layout = lay
-        # field offsets inside a side's 16-token block, and bytes per token
-        self.fields = {n: (getattr(lay, n).offset, getattr(lay, n).record_bytes) for n in _b.REGION_NAMES}
-        self.cache = torch.zeros(int(lay.total_bytes), dtype=torch.uint8, device=self.device)
         self._ws = None
 
     def __del__(self):
@@ -73,6 +63,40 @@ class QuantizedKVCache:
         if ctx is not None and ctx.value:
             _b.tq_context_destroy(ctx)
             self._ctx = None
+
+    def workspace(self, max_seq):
+        import torch
+        need = int(_b.tq_decode_workspace_bytes(self._ctx, int(max_seq)))
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def device_error(self, stream=None):
+        """(status, code) of the decode workspace's error word (waits for the stream)."""
+        code = _b.c_int32(0)
+        st = _b.tq_get_device_error(self.workspace(0).data_ptr(), code, _stream_handle(stream))
+        return st, code.value
+
+
+class QuantizedKVCache(_Codec):
+    """One packed KV cache of shape [batch][num_kv_heads][capacity] tokens on a CUDA device.
+
+    ``scheme``/``n`` pick the codecs as ``tq_config_from_scheme`` does; ``k_codec``/``v_codec``
+    (tuples bits, rotate, qjl) override them.  ``headq_rank`` = 16 turns the HeadQ side code on.
+    """
+
+    def __init__(self, head_dim, num_q_heads, num_kv_heads, batch, capacity, scheme="tq", n=4,
+                 seed=0, k_codec=None, v_codec=None, headq_rank=0, headq_bits=4, device="cuda"):
+        import torch
+        self._setup(head_dim, num_q_heads, num_kv_heads, batch, capacity, scheme, n, seed, k_codec,
+                    v_codec, headq_rank, headq_bits, device)
+        ctx = self._ctx
+        lay = _b.tq_cache_layout()
+        check(_b.tq_get_cache_layout(ctx, lay))
+        self.layout = lay
+        # field offsets inside a side's 16-token block, and bytes per token
+        self.fields = {n: (getattr(lay, n).offset, getattr(lay, n).record_bytes) for n in _b.REGION_NAMES}
+        self.cache = torch.zeros(int(lay.total_bytes), dtype=torch.uint8, device=self.device)
 
     # ---- host tables (no GPU work)
     def host_tables(self):
@@ -96,13 +120,6 @@ class QuantizedKVCache:
         check(_b.tq_quantize_append(self._ctx, self.cache.data_ptr(), k.data_ptr(), v.data_ptr(),
                                     _dtype_code(k), int(k.shape[2]), _b.int_array(start),
                                     _stream_handle(stream)))
-
-    def workspace(self, max_seq):
-        import torch
-        need = int(_b.tq_decode_workspace_bytes(self._ctx, int(max_seq)))
-        if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
-        return self._ws
 
     def decode(self, q, seq_len, out=None, stream=None):
         """q: float32 CUDA tensor [batch][num_q_heads][head_dim] -> attention output (same shape)."""
@@ -146,7 +163,64 @@ class QuantizedKVCache:
                                _stream_handle(stream)))
         return k, v
 
-    def device_error(self, stream=None):
-        code = _b.c_int32(0)
-        st = _b.tq_get_device_error(self.workspace(0).data_ptr(), code, _stream_handle(stream))
-        return st, code.value
+
+class PagedKVCache(_Codec):
+    """A pool of ``num_pages`` pages on a CUDA device, each holding one 16-token block per KV head
+    of both sides (``tq_get_paged_cache_layout``).  ``block_table`` is an int32 CUDA tensor
+    [batch][max_blocks_per_seq] of page indices owned by the caller; start positions and sequence
+    lengths are int32 CUDA tensors [batch].  All three are read on the device, so they may change
+    between replays of a captured CUDA graph.  Head dim 128.
+    """
+
+    def __init__(self, head_dim, num_q_heads, num_kv_heads, batch, num_pages, max_blocks_per_seq,
+                 scheme="tq", n=4, seed=0, k_codec=None, v_codec=None, device="cuda"):
+        import torch
+        # the context's contiguous capacity is not used by the pool: the smallest valid one
+        self._setup(head_dim, num_q_heads, num_kv_heads, batch, 64, scheme, n, seed, k_codec, v_codec,
+                    0, 4, device)
+        self.num_pages, self.max_blocks_per_seq = int(num_pages), int(max_blocks_per_seq)
+        lay = _b.tq_cache_layout()
+        check(_b.tq_get_paged_cache_layout(self._ctx, self.num_pages, lay))
+        self.layout = lay
+        self.fields = {n: (getattr(lay, n).offset, getattr(lay, n).record_bytes) for n in _b.REGION_NAMES}
+        self.pool = torch.zeros(int(lay.total_bytes), dtype=torch.uint8, device=self.device)
+
+    def _pages(self, block_table):
+        if block_table.dtype != _torch().int32 or not block_table.is_contiguous():
+            raise ValueError("block_table must be a contiguous int32 tensor")
+        if tuple(block_table.shape) != (self.batch, self.max_blocks_per_seq):
+            raise ValueError("block_table must be [batch][max_blocks_per_seq]")
+        return _b.tq_page_table(block_table.data_ptr(), self.max_blocks_per_seq, self.num_pages)
+
+    def append(self, k, v, start, block_table, error=None, stream=None):
+        """k, v: CUDA tensors [batch][num_kv_heads][n_new][head_dim]; start: int32 CUDA [batch];
+        error: optional int32 CUDA tensor of one element that receives a TQ_DEVERR_* code."""
+        k, v = k.contiguous(), v.contiguous()
+        if k.shape != v.shape or k.dtype != v.dtype:
+            raise ValueError("k and v must have the same shape and dtype")
+        pt = self._pages(block_table)
+        check(_b.tq_quantize_append_paged(self._ctx, self.pool.data_ptr(), pt, k.data_ptr(), v.data_ptr(),
+                                          _dtype_code(k), int(k.shape[2]), start.data_ptr(),
+                                          error.data_ptr() if error is not None else None,
+                                          _stream_handle(stream)))
+
+    def decode(self, q, seq_len, block_table, out=None, stream=None):
+        """q: float32 CUDA tensor [batch][nq][num_q_heads][head_dim] (or [batch][num_q_heads][head_dim]
+        for one query); seq_len: int32 CUDA [batch].  Query i of nq attends to the first
+        seq_len[b] - nq + 1 + i tokens."""
+        import torch
+        q = q.contiguous()
+        nq = int(q.shape[1]) if q.dim() == 4 else 1
+        if out is None:
+            out = torch.empty_like(q)
+        pt = self._pages(block_table)
+        ws = self.workspace(16 * self.max_blocks_per_seq)
+        check(_b.tq_decode_attention_paged(self._ctx, self.pool.data_ptr(), pt, q.data_ptr(), nq,
+                                           seq_len.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                           _stream_handle(stream)))
+        return out
+
+
+def _torch():
+    import torch
+    return torch

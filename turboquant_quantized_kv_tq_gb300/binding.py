@@ -56,6 +56,16 @@ class tq_cache_layout(ctypes.Structure):
                 ("v_block_bytes", c_uint64)] + [(n, tq_region) for n in REGION_NAMES]
 
 
+class tq_page_table(ctypes.Structure):
+    _fields_ = [("block_table", c_void_p), ("max_blocks_per_seq", c_int32), ("num_pages", c_int32)]
+
+
+TQ_DEVERR_WAIT_TIMEOUT = 1
+TQ_DEVERR_SMEM_PLAN = 2
+TQ_DEVERR_BAD_PAGE = 3
+TQ_DEVERR_BAD_LENGTH = 4
+
+
 class TQError(RuntimeError):
     def __init__(self, status, message):
         super().__init__(f"{message} (status {status})")
@@ -96,6 +106,11 @@ DECLARATIONS = [
                                    c_int32, c_void_p]),
     ("tq_dequantize", c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
                                 c_void_p, c_void_p]),
+    ("tq_get_paged_cache_layout", c_int32, [c_void_p, c_int32, ctypes.POINTER(tq_cache_layout)]),
+    ("tq_quantize_append_paged", c_int32, [c_void_p, c_void_p, ctypes.POINTER(tq_page_table), c_void_p,
+                                           c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
+    ("tq_decode_attention_paged", c_int32, [c_void_p, c_void_p, ctypes.POINTER(tq_page_table), c_void_p,
+                                            c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     ("tq_get_device_error", c_int32, [c_void_p, ctypes.POINTER(c_int32), c_void_p]),
     ("tq_status_string", ctypes.c_char_p, [c_int32]),
     ("tq_last_error", ctypes.c_char_p, []),

@@ -229,6 +229,27 @@ tq_status tq_get_cache_layout(const tq_context* ctx, tq_cache_layout* out) {
   return TQ_OK;
 }
 
+static tq_status check_pages(const tq_context* ctx, const tq_page_table* pt) {
+  if (!pt || !pt->block_table) return fail(TQ_ERR_INVALID_ARG, "null page table");
+  if (pt->max_blocks_per_seq < 1 || pt->num_pages < 1) return fail(TQ_ERR_INVALID_ARG, "empty page table");
+  if ((int64_t)pt->max_blocks_per_seq * TQ_TILE_TOKENS > INT32_MAX / 2)
+    return fail(TQ_ERR_INVALID_ARG, "max_blocks_per_seq too large");
+  if (!aligned(pt->block_table, 4)) return fail(TQ_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
+  if (ctx->cfg.head_dim != 128) return fail(TQ_ERR_UNSUPPORTED, "the paged pool is built for head_dim 128");
+  return TQ_OK;
+}
+
+tq_status tq_get_paged_cache_layout(const tq_context* ctx, int32_t num_pages, tq_cache_layout* out) {
+  tq_status s = tq_get_cache_layout(ctx, out);
+  if (s != TQ_OK) return s;
+  if (num_pages < 1) return fail(TQ_ERR_INVALID_ARG, "num_pages must be >= 1");
+  const Layout L = make_layout(ctx->cfg, ctx->m, num_pages);
+  out->total_bytes = L.total;
+  out->k_offset = L.side_off[0];
+  out->v_offset = L.side_off[1];
+  return TQ_OK;
+}
+
 static tq_status ready(const tq_context* ctx) {
   if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
   if (!ctx->dev_tables) return fail(TQ_ERR_STATE, "tables not uploaded");
@@ -252,6 +273,42 @@ tq_status tq_quantize_append(const tq_context* ctx, void* dev_cache, const void*
     if ((int64_t)host_start[b] + n_new > ctx->cfg.capacity) return fail(TQ_ERR_CAPACITY, "start + n_new > capacity");
   }
   return launch_append(ctx, dev_cache, k, v, dtype, n_new, host_start, stream);
+}
+
+tq_status tq_quantize_append_paged(const tq_context* ctx, void* dev_pool, const tq_page_table* pages,
+                                   const void* k, const void* v, tq_dtype dtype, int32_t n_new,
+                                   const int32_t* dev_start, int32_t* dev_error, tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (n_new < 0) return fail(TQ_ERR_INVALID_ARG, "n_new must be >= 0");
+  if (n_new == 0) return TQ_OK;
+  if (!dev_pool || !k || !v || !dev_start) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  s = check_pages(ctx, pages);
+  if (s != TQ_OK) return s;
+  if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad dtype");
+  if (!aligned(dev_pool, 256)) return fail(TQ_ERR_INVALID_ARG, "pool must be 256-byte aligned");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(TQ_ERR_INVALID_ARG, "k, v must be 16-byte aligned");
+  if (!aligned(dev_start, 4) || !aligned(dev_error, 4)) return fail(TQ_ERR_INVALID_ARG, "misaligned pointer");
+  return launch_append_paged(ctx, dev_pool, pages, k, v, dtype, n_new, dev_start, dev_error, stream);
+}
+
+tq_status tq_decode_attention_paged(const tq_context* ctx, const void* dev_pool, const tq_page_table* pages,
+                                    const float* q, int32_t nq, const int32_t* dev_seq_len, float* out,
+                                    void* ws, size_t ws_bytes, tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (!dev_pool || !q || !dev_seq_len || !out || !ws) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  s = check_pages(ctx, pages);
+  if (s != TQ_OK) return s;
+  if (nq < 1) return fail(TQ_ERR_INVALID_ARG, "nq must be >= 1");
+  const int G = ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads;
+  if ((int64_t)G * nq > 8) return fail(TQ_ERR_UNSUPPORTED, "several queries per sequence are built for G * nq <= 8");
+  if (!aligned(dev_pool, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 256) ||
+      !aligned(dev_seq_len, 4))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer (pool/ws 256 B, q/out 16 B, lengths 4 B)");
+  if (ws_bytes < decode_workspace_bytes(ctx, TQ_TILE_TOKENS * pages->max_blocks_per_seq))
+    return fail(TQ_ERR_WORKSPACE, "workspace too small");
+  return launch_decode_paged(ctx, dev_pool, pages, q, nq, dev_seq_len, out, ws, ws_bytes, stream);
 }
 
 size_t tq_decode_workspace_bytes(const tq_context* ctx, int32_t max_seq) {

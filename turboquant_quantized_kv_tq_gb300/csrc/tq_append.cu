@@ -33,6 +33,7 @@ struct AppendParams {
   int qjl_mma;   // QJL sides go to append_qjl_mma_kernel (head dim 128, large appends)
   int stage_st;  // append_kernel blocks of a QJL side stage S^T in shared memory
   int start[TQ_MAX_BATCH];
+  const int* dev_start;  // set: start positions from device memory (paged pool)
 };
 
 // Flat vector index (over [B][H_kv][n_new]) -> batch, KV head, index in the chunk, position.
@@ -41,7 +42,7 @@ __device__ __forceinline__ void split_vec(const AppendParams& p, long long vec, 
   const long long r = vec / p.n_new;
   h = (int)(r % p.Hkv);
   b = (int)(r / p.Hkv);
-  t = p.start[b] + j;
+  t = (p.dev_start ? __ldg(p.dev_start + b) : p.start[b]) + j;
 }
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -116,14 +117,49 @@ __device__ __forceinline__ void store_stream(unsigned char* dst, const uint32_t 
   }
 }
 
-// Read back element values of a w-bit stream for this lane's E coordinates.
+// Store a W-bit value-side stream of one vector at block position pos: lane l's E values are
+// coordinates [l*E, (l+1)*E); the group of coordinates [16 g, 16 g + 16) of this token is the
+// 2W bytes at stream + g * 32W + pos * 2W (see grouped_byte).
 template <int E, int W>
-__device__ __forceinline__ void load_stream(const unsigned char* src, uint32_t (&v)[E]) {
+__device__ __forceinline__ void store_stream_grouped(unsigned char* stream, int pos, const uint32_t (&v)[E]) {
+  static_assert(16 % E == 0 || E % 16 == 0, "a lane holds part of one group or whole groups");
+  const int lane = threadIdx.x & 31;
+  auto put = [&](int g, unsigned long long bits) {
+    unsigned char* dst = stream + g * 32 * W + pos * 2 * W;
+    if constexpr (W == 4) *reinterpret_cast<unsigned long long*>(dst) = bits;
+    else if constexpr (W == 2) *reinterpret_cast<uint32_t*>(dst) = (uint32_t)bits;
+    else *reinterpret_cast<unsigned short*>(dst) = (unsigned short)bits;
+  };
+  if constexpr (E >= 16) {
+#pragma unroll
+    for (int g = 0; g < E / 16; ++g) {
+      unsigned long long bits = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) bits |= (unsigned long long)v[16 * g + i] << (i * W);
+      put(lane * (E / 16) + g, bits);
+    }
+  } else {
+    constexpr int LPG = 16 / E;  // lanes per group
+    unsigned long long bits = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) bits |= (unsigned long long)v[i] << (((lane % LPG) * E + i) * W);
+#pragma unroll
+    for (int m = 1; m < LPG; m <<= 1) bits |= __shfl_xor_sync(kFull, bits, m);
+    if (lane % LPG == 0) put(lane / LPG, bits);
+  }
+}
+
+// Read back element values of a w-bit stream for this lane's E coordinates: a whole record at
+// src (pos < 0), or a value-side stream at src stored by coordinate groups (block position pos).
+template <int E, int W>
+__device__ __forceinline__ void load_stream(const unsigned char* src, uint32_t (&v)[E], int pos = -1) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
     const int bit = (lane * E + i) * W;
-    v[i] = (src[bit >> 3] >> (bit & 7)) & ((1u << W) - 1u);
+    const unsigned j = (unsigned)bit >> 3;
+    const unsigned char byte = pos < 0 ? src[j] : src[grouped_byte(j, (unsigned)pos, W)];
+    v[i] = (byte >> (bit & 7)) & ((1u << W) - 1u);
   }
 }
 
@@ -207,22 +243,43 @@ __device__ __forceinline__ void encode_vectors(const AppendParams& p, int side, 
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     if (!valid[v]) continue;
-    unsigned char* codes = C.ptr(rc, b[v], h[v], t[v]);
-    if (bits == 4) {
-      uint32_t w[E];
+    if (side == 0) {  // key records: whole records, token-major
+      unsigned char* codes = C.ptr(rc, b[v], h[v], t[v]);
+      if (bits == 4) {
+        uint32_t w[E];
 #pragma unroll
-      for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 3) | mag[v][i];
-      store_stream<E, 4>(codes, w);
-    } else if (bits == 3) {
-      store_stream<E, 2>(codes, mag[v]);
-      store_stream<E, 1>(codes + D / 4, sgnbit[v]);
-    } else if (bits == 2) {
-      uint32_t w[E];
+        for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 3) | mag[v][i];
+        store_stream<E, 4>(codes, w);
+      } else if (bits == 3) {
+        store_stream<E, 2>(codes, mag[v]);
+        store_stream<E, 1>(codes + D / 4, sgnbit[v]);
+      } else if (bits == 2) {
+        uint32_t w[E];
 #pragma unroll
-      for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 1) | mag[v][i];
-      store_stream<E, 2>(codes, w);
-    } else {
-      store_stream<E, 1>(codes, sgnbit[v]);
+        for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 1) | mag[v][i];
+        store_stream<E, 2>(codes, w);
+      } else {
+        store_stream<E, 1>(codes, sgnbit[v]);
+      }
+    } else {  // value streams: by groups of 16 coordinates
+      unsigned char* f = C.fieldp(rc, b[v], h[v], t[v]);
+      const int pos = t[v] & (tqi::kTileTokens - 1);
+      if (bits == 4) {
+        uint32_t w[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 3) | mag[v][i];
+        store_stream_grouped<E, 4>(f, pos, w);
+      } else if (bits == 3) {
+        store_stream_grouped<E, 2>(f, pos, mag[v]);
+        store_stream_grouped<E, 1>(f + tqi::kTileTokens * (D / 4), pos, sgnbit[v]);
+      } else if (bits == 2) {
+        uint32_t w[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) w[i] = (sgnbit[v][i] << 1) | mag[v][i];
+        store_stream_grouped<E, 2>(f, pos, w);
+      } else {
+        store_stream_grouped<E, 1>(f, pos, sgnbit[v]);
+      }
     }
     if (lane == 0) *reinterpret_cast<float*>(C.ptr(side ? tqi::R_V_NORM : tqi::R_K_NORM, b[v], h[v], t[v])) = nu[v];
   }
@@ -341,7 +398,10 @@ __device__ __forceinline__ void sketch_signs_ffma(const AppendParams& p, int sid
   uint32_t sbit[E];
 #pragma unroll
   for (int q = 0; q < E; ++q) sbit[q] = acc[q] >= 0.f ? 1u : 0u;
-  store_stream<E, 1>(C.ptr(side ? tqi::R_V_SIGNS : tqi::R_K_SIGNS, b, h, t), sbit);
+  if (side == 0)
+    store_stream<E, 1>(C.ptr(tqi::R_K_SIGNS, b, h, t), sbit);
+  else
+    store_stream_grouped<E, 1>(C.fieldp(tqi::R_V_SIGNS, b, h, t), t & (tqi::kTileTokens - 1), sbit);
 }
 
 // AppendNV consecutive vectors of side blockIdx.y per warp.  With stage_st set (small appends
@@ -534,8 +594,15 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     if (vec < per_side) {
       int b, h, j, t;
       split_vec(p, vec, b, h, j, t);
-      reinterpret_cast<uint32_t*>(C.ptr(side ? tqi::R_V_SIGNS : tqi::R_K_SIGNS, b, h, t))[w & 3] =
-          reinterpret_cast<const uint32_t*>(sg)[w];
+      const uint32_t word = reinterpret_cast<const uint32_t*>(sg)[w];  // signs of rows 32 (w & 3) ..
+      if (side == 0) {
+        reinterpret_cast<uint32_t*>(C.ptr(tqi::R_K_SIGNS, b, h, t))[w & 3] = word;
+      } else {  // two 16-row groups of the value side's sign stream
+        unsigned char* f = C.fieldp(tqi::R_V_SIGNS, b, h, t);
+        const int pos = t & (tqi::kTileTokens - 1);
+        *reinterpret_cast<unsigned short*>(f + grouped_byte(4 * (w & 3), pos, 1)) = (unsigned short)word;
+        *reinterpret_cast<unsigned short*>(f + grouped_byte(4 * (w & 3) + 2, pos, 1)) = (unsigned short)(word >> 16);
+      }
     }
   }
   __syncthreads();
@@ -594,23 +661,26 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const DequantParams p) 
   const int t = p.t0 + (side ? w - p.n : w);
   const Cache& C = p.cache;
   const int bits = p.bits[side];
-  const unsigned char* codes = C.ptr(side ? tqi::R_V_CODES : tqi::R_K_CODES, p.b, p.kvh, t);
+  // key records are whole; value streams are stored by coordinate groups at block position pos
+  const int pos = side ? (t & (tqi::kTileTokens - 1)) : -1;
+  const unsigned char* codes = side ? C.fieldp(tqi::R_V_CODES, p.b, p.kvh, t) : C.ptr(tqi::R_K_CODES, p.b, p.kvh, t);
+  const int second = side ? tqi::kTileTokens * (D / 4) : D / 4;  // start of a 3-bit code's 1-bit stream
   const float* cent = side ? p.tab.v_c : p.tab.k_c;
   const uint32_t halfL = 1u << (bits - 1);
   uint32_t sym[E], sgn[E];
   if (bits == 4) {
-    load_stream<E, 4>(codes, sym);
+    load_stream<E, 4>(codes, sym, pos);
 #pragma unroll
     for (int i = 0; i < E; ++i) { sgn[i] = sym[i] >> 3; sym[i] &= 7u; }
   } else if (bits == 3) {
-    load_stream<E, 2>(codes, sym);
-    load_stream<E, 1>(codes + D / 4, sgn);
+    load_stream<E, 2>(codes, sym, pos);
+    load_stream<E, 1>(codes + second, sgn, pos);
   } else if (bits == 2) {
-    load_stream<E, 2>(codes, sym);
+    load_stream<E, 2>(codes, sym, pos);
 #pragma unroll
     for (int i = 0; i < E; ++i) { sgn[i] = sym[i] >> 1; sym[i] &= 1u; }
   } else {
-    load_stream<E, 1>(codes, sgn);
+    load_stream<E, 1>(codes, sgn, pos);
 #pragma unroll
     for (int i = 0; i < E; ++i) sym[i] = 0;
   }
@@ -622,14 +692,15 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const DequantParams p) 
   }
   const float nu = *reinterpret_cast<const float*>(C.ptr(side ? tqi::R_V_NORM : tqi::R_K_NORM, p.b, p.kvh, t));
   if (p.qjl[side]) {
-    const unsigned char* sg = C.ptr(side ? tqi::R_V_SIGNS : tqi::R_K_SIGNS, p.b, p.kvh, t);
+    const unsigned char* sg = side ? C.fieldp(tqi::R_V_SIGNS, p.b, p.kvh, t) : C.ptr(tqi::R_K_SIGNS, p.b, p.kvh, t);
     const float rho = __half2float(*reinterpret_cast<const __half*>(C.ptr(side ? tqi::R_V_RHO : tqi::R_K_RHO, p.b, p.kvh, t)));
     const float* S = side ? p.tab.S_V : p.tab.S_K;  // [m][d]
     float acc[E];
 #pragma unroll
     for (int i = 0; i < E; ++i) acc[i] = 0.f;
     for (int i = 0; i < p.m; ++i) {
-      const float pm = ((sg[i >> 3] >> (i & 7)) & 1u) ? 1.f : -1.f;
+      const unsigned char byte = side ? sg[grouped_byte((unsigned)i >> 3, (unsigned)pos, 1)] : sg[i >> 3];
+      const float pm = ((byte >> (i & 7)) & 1u) ? 1.f : -1.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] = fmaf(__ldg(S + (long long)i * D + lane * E + e), pm, acc[e]);
     }
@@ -690,12 +761,21 @@ tq_status launch_status(const char* what) {
 
 namespace tqi {
 
-tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
-                        tq_dtype dtype, int n_new, const int32_t* start, Stream stream) {
+// Paged pool (tq_quantize_append_paged): block table, device start positions, error word.
+struct PagedAppend {
+  const tq_page_table* pt;
+  const int32_t* dev_start;
+  int32_t* dev_error;
+};
+
+static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, const void* v,
+                             tq_dtype dtype, int n_new, const int32_t* start, const PagedAppend* pg,
+                             Stream stream) {
   using namespace tqd;
   AppendParams p;
   p.tab = make_tables(ctx);
-  p.cache = make_cache(ctx, cache);
+  p.cache = pg ? make_paged_cache(ctx, cache, *pg->pt, pg->dev_error) : make_cache(ctx, cache);
+  p.dev_start = pg ? pg->dev_start : nullptr;
   p.k = k;
   p.v = v;
   p.B = ctx->cfg.batch;
@@ -705,7 +785,7 @@ tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const
   p.bits[0] = ctx->cfg.k.bits; p.rotate[0] = ctx->cfg.k.rotate; p.qjl[0] = ctx->cfg.k.qjl;
   p.bits[1] = ctx->cfg.v.bits; p.rotate[1] = ctx->cfg.v.rotate; p.qjl[1] = ctx->cfg.v.qjl;
   p.headq_rank = ctx->cfg.headq_rank;
-  for (int b = 0; b < TQ_MAX_BATCH; ++b) p.start[b] = b < ctx->cfg.batch ? start[b] : 0;
+  for (int b = 0; b < TQ_MAX_BATCH; ++b) p.start[b] = (!pg && b < ctx->cfg.batch) ? start[b] : 0;
   const int nv = ctx->cfg.head_dim == 128 ? AppendNV<128>::value : 1;
   const long long per_side = (long long)p.B * p.Hkv * n_new;
   const long long blocks = ((per_side + nv - 1) / nv + kWarpsPerBlock - 1) / kWarpsPerBlock;  // per side
@@ -752,6 +832,18 @@ tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const
     return TQ_ERR_CUDA;
   }
   return launch_status("append sketch");
+}
+
+tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
+                        tq_dtype dtype, int n_new, const int32_t* start, Stream stream) {
+  return append_impl(ctx, cache, k, v, dtype, n_new, start, nullptr, stream);
+}
+
+tq_status launch_append_paged(const tq_context* ctx, void* pool, const tq_page_table* pt, const void* k,
+                              const void* v, tq_dtype dtype, int n_new, const int32_t* dev_start,
+                              int32_t* dev_error, Stream stream) {
+  const PagedAppend pg{pt, dev_start, dev_error};
+  return append_impl(ctx, pool, k, v, dtype, n_new, nullptr, &pg, stream);
 }
 
 tq_status launch_rotate_basis(const tq_context* ctx, const float* U, Stream stream) {

@@ -12,7 +12,7 @@ constexpr int kLogitsTokensPerBlock = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct WsLayout {
-  size_t err, tickets, q_rot, q_sk, q_u, q_rot_lo, q_sk_lo, part, sk_final, sk_part, total;
+  size_t err, tickets, q_rot, q_sk, q_u, q_rot_lo, q_sk_lo, part, sk_final, sk_part, plan, total;
   int ps;
 };
 
@@ -42,6 +42,7 @@ WsLayout ws_layout(const tq_context* ctx) {
   const bool wide_vq = D > kDecD && ctx->cfg.v.qjl;  // acc_sk / l per head for the sketch pass
   w.sk_final = off; off = align256(off + (wide_vq ? (size_t)B * Hq * ctx->m * sizeof(float) : 0));
   w.sk_part = off; off = align256(off + (wide_vq ? (size_t)(ctx->m / kSkRows) * B * Hq * D * sizeof(float) : 0));
+  w.plan = off; off = align256(off + (D == kDecD ? sizeof(DevPlan) : 0));  // device lengths (paged)
   w.total = off;
   return w;
 }
@@ -66,9 +67,59 @@ struct PrepParams {
   int* err;
   float* out;
   float* sk_final;  // zeroed for empty sequences (head dim > 128 with a QJL value side)
-  int n_tickets, n_heads, Hq, Hkv, G, Gc, nq, k_rotate, kq, kh, m;
+  int n_tickets, n_heads, Hq, Hkv, G, Gc, nq, k_rotate, kq, kh, m, B;
   int seq_len[TQ_MAX_BATCH];
+  const int* dev_seq_len;  // set: lengths from device memory, clamped to [0, lmax]; the work
+  int lmax;                // split is then computed into *plan
+  DevPlan* plan;
+  __device__ __forceinline__ int len(int b) const {
+    if (!dev_seq_len) return seq_len[b];
+    const int L = __ldg(dev_seq_len + b);
+    return L < 0 ? 0 : (L > lmax ? lmax : L);
+  }
 };
+
+// Work split of the decode from device lengths, by block 0 of prep_kernel (256 threads, two
+// batch entries each): plan->seq_len = the clamped lengths, plan->batch_start = the exclusive
+// prefix sum of H_kv * ceil(len / 16), plan->W = the total.  A length outside [0, lmax] is
+// recorded as TQ_DEVERR_BAD_LENGTH (after the error word's reset).
+__device__ void build_plan(const PrepParams& p) {
+  static_assert(TQ_MAX_BATCH == 512, "two batch entries per thread of a 256-thread block");
+  __shared__ long long wtot[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long v[2];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int b = 2 * threadIdx.x + i;
+    int L = 0;
+    if (b < p.B) {
+      const int raw = __ldg(p.dev_seq_len + b);
+      bad |= raw < 0 || raw > p.lmax;
+      L = p.len(b);
+    }
+    p.plan->seq_len[b] = L;
+    v[i] = (long long)p.Hkv * ((L + kTile - 1) / kTile);
+  }
+  long long t = v[0] + v[1];  // inclusive scan over the block
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(kFull, t, o);
+    if (lane >= o) t += n;
+  }
+  if (lane == 31) wtot[warp] = t;
+  __syncthreads();
+  long long before = 0;
+  for (int w = 0; w < warp; ++w) before += wtot[w];
+  const long long ex = before + t - v[0] - v[1];
+  p.plan->batch_start[2 * threadIdx.x] = ex;
+  p.plan->batch_start[2 * threadIdx.x + 1] = ex + v[0];
+  if (threadIdx.x == blockDim.x - 1) {
+    p.plan->batch_start[TQ_MAX_BATCH] = before + t;
+    p.plan->W = before + t;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicExch(p.err, TQ_DEVERR_BAD_LENGTH);
+}
 
 // E values as fp16 pairs at hi and their fp16 remainders (x - hi) at lo.
 template <int E>
@@ -108,13 +159,17 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < p.n_tickets; i += blockDim.x) p.tickets[i] = 0;
     if (threadIdx.x == 0) p.err[0] = 0;
+    if (p.plan) {
+      __syncthreads();  // the reset above comes before any error the plan records
+      build_plan(p);
+    }
   }
   const int head = blockIdx.x * 8 + (threadIdx.x >> 5);  // flat column index
   if (head >= p.n_heads) return;
   const int b = head / (p.Hkv * p.Gc), r = head % (p.Hkv * p.Gc);
   const int kvh = r / p.Gc, c = r % p.Gc;
   const long long qrow = ((long long)b * p.nq + c / p.G) * p.Hq + kvh * p.G + c % p.G;  // [B][nq][Hq]
-  if (p.seq_len[b] == 0) {
+  if (p.len(b) == 0) {
 #pragma unroll
     for (int e = 0; e < E; e += 4)
       *reinterpret_cast<float4*>(p.out + qrow * D + lane * E + e) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -221,11 +276,16 @@ tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q
   return launch_decode_multi(ctx, cache, q, 1, seq_len, out, ws, ws_bytes, stream);
 }
 
-tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const float* q, int nq,
-                              const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
-                              Stream stream) {
+// Paged pool and device lengths (tq_decode_attention_paged), or none (host lengths).
+struct PagedDecode {
+  const tq_page_table* pt;
+  const int32_t* dev_seq_len;
+};
+
+static tq_status decode_impl(const tq_context* ctx, const void* cache, const float* q, int nq,
+                             const int32_t* seq_len, const PagedDecode* pg, float* out, void* ws,
+                             Stream stream) {
   using namespace tqd;
-  (void)ws_bytes;
   const int D = ctx->cfg.head_dim;
   const WsLayout w = ws_layout(ctx);
   unsigned char* base = (unsigned char*)ws;
@@ -269,7 +329,15 @@ tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const fl
   const bool wide_vq = D > kDecD && ctx->cfg.v.qjl;
   pp.sk_final = wide_vq ? (float*)(base + w.sk_final) : nullptr;
   pp.m = ctx->m;
-  for (int b = 0; b < TQ_MAX_BATCH; ++b) pp.seq_len[b] = b < B ? seq_len[b] : 0;
+  pp.B = B;
+  for (int b = 0; b < TQ_MAX_BATCH; ++b) pp.seq_len[b] = (!pg && b < B) ? seq_len[b] : 0;
+  pp.dev_seq_len = pg ? pg->dev_seq_len : nullptr;
+  pp.lmax = pg ? kTile * pg->pt->max_blocks_per_seq : 0;
+  pp.plan = pg ? (DevPlan*)(base + w.plan) : nullptr;
+  if (pg && D != kDecD) {
+    set_error("the paged decode is built for head dim 128");
+    return TQ_ERR_UNSUPPORTED;
+  }
   const dim3 pgrid((B * Hq * nq + 7) / 8);
   const int psmem = (D == kDecD && pp.kq) ? kDecD * kDecD * 4 : 0;
   if (psmem) {
@@ -286,7 +354,8 @@ tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const fl
   if (e != cudaSuccess) return cuda_fail("decode prep", e);
 
   p.tab = tab;
-  p.cache = make_cache(ctx, cache);
+  p.cache = pg ? make_paged_cache(ctx, cache, *pg->pt, pp.err) : make_cache(ctx, cache);
+  p.plan = pp.plan;
   p.q_rot = pp.q_rot;
   p.q_sk = pp.q_sk;
   p.q_u = pp.q_u;
@@ -308,15 +377,19 @@ tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const fl
   p.err = pp.err;
   long long W = 0;  // 16-token tiles over all slabs
   for (int b = 0; b < TQ_MAX_BATCH; ++b) {
-    p.seq_len[b] = b < B ? seq_len[b] : 0;
+    p.seq_len[b] = pp.seq_len[b];
     p.batch_start[b] = W;
     W += (long long)Hkv * ((p.seq_len[b] + kTile - 1) / kTile);
   }
   p.batch_start[TQ_MAX_BATCH] = W;
   p.W = W;
-  if (W == 0) return TQ_OK;  // every sequence is empty: prep wrote the zero outputs
   const int nsm = sm_count();
-  p.nblocks = W < nsm ? (int)W : nsm;  // every block gets a non-empty range
+  if (pg) {
+    p.nblocks = nsm;  // the split is computed on the device; blocks with an empty range exit
+  } else {
+    if (W == 0) return TQ_OK;  // every sequence is empty: prep wrote the zero outputs
+    p.nblocks = W < nsm ? (int)W : nsm;  // every block gets a non-empty range
+  }
   e = cudaSuccess;
   dispatch_decode(ctx, p, dim3(p.nblocks), s, &e);
   if (e != cudaSuccess) return cuda_fail("decode", e);
@@ -326,6 +399,21 @@ tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const fl
     if (e != cudaSuccess) return cuda_fail("decode sketch finalize", e);
   }
   return TQ_OK;
+}
+
+tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const float* q, int nq,
+                              const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
+                              Stream stream) {
+  (void)ws_bytes;
+  return decode_impl(ctx, cache, q, nq, seq_len, nullptr, out, ws, stream);
+}
+
+tq_status launch_decode_paged(const tq_context* ctx, const void* pool, const tq_page_table* pt,
+                              const float* q, int nq, const int32_t* dev_seq_len, float* out, void* ws,
+                              size_t ws_bytes, Stream stream) {
+  (void)ws_bytes;
+  const PagedDecode pg{pt, dev_seq_len};
+  return decode_impl(ctx, pool, q, nq, nullptr, &pg, out, ws, stream);
 }
 
 tq_status launch_logits(const tq_context* ctx, const void* cache, const float* q,

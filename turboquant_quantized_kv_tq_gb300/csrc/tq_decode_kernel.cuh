@@ -49,6 +49,14 @@ constexpr int kPairStages = 2;  // per-warp ring of 32-token (two-tile) stages
 constexpr int kMaxBlocks = 256;  // partial slots reserved for blocks (>= SM count)
 constexpr int kLutStride = 256;  // bytes between table entries
 
+// The work split when sequence lengths live in device memory: written by prep_kernel from the
+// lengths (clamped to the block table) and read by the decode in place of the DecodeParams copies.
+struct DevPlan {
+  long long W;
+  long long batch_start[TQ_MAX_BATCH + 1];
+  int seq_len[TQ_MAX_BATCH];
+};
+
 struct DecodeParams {
   Tables tab;
   Cache cache;
@@ -76,6 +84,14 @@ struct DecodeParams {
   float qjl_scale;        // sqrt(pi/2) / m
   int seq_len[TQ_MAX_BATCH];
   long long batch_start[TQ_MAX_BATCH + 1];  // first tile of batch b: Hkv * sum of ceil(len/16)
+  const DevPlan* plan;    // paged pool: W, seq_len and batch_start come from here (device lengths)
+  template <bool DEV> __device__ __forceinline__ long long tiles() const { return DEV ? __ldcg(&plan->W) : W; }
+  template <bool DEV> __device__ __forceinline__ long long bstart(int b) const {
+    return DEV ? __ldcg(plan->batch_start + b) : batch_start[b];
+  }
+  template <bool DEV> __device__ __forceinline__ int len(int b) const {
+    return DEV ? __ldcg(plan->seq_len + b) : seq_len[b];
+  }
 };
 
 template <int B>
@@ -241,12 +257,13 @@ struct Pair2 {
   }
 };
 
-// 1-bit stream, 16 dims per token: bit i of token j for dims 16 lg + i.
+// 1-bit stream, 16 dims per token: bit i of token j for dims 16 lg + i; x01 holds tokens 0 (low
+// half) and 1, x23 tokens 2 and 3 (the stream's group layout stores them that way).
 struct Bits16 {
   uint32_t x01, x23;
-  __device__ __forceinline__ void build(const uint32_t (&s)[4]) {
-    x01 = (s[0] & 0xffffu) | (s[1] << 16);
-    x23 = (s[2] & 0xffffu) | (s[3] << 16);
+  __device__ __forceinline__ void build(const uint32_t (&s)[2]) {
+    x01 = s[0];
+    x23 = s[1];
   }
   __device__ __forceinline__ void apply(int mt, uint32_t (&a)[4]) const {
     a[0] = signed_pair(a[0], x01 << (15 - 2 * mt));
@@ -258,7 +275,7 @@ struct Bits16 {
 
 template <>
 struct VChunk<3> {
-  uint32_t k[4], s[4];
+  uint32_t k[4], s[2];
   Pair2 m;
   Bits16 sg;
   __device__ __forceinline__ void prepare() { m.build(k); sg.build(s); }
@@ -282,7 +299,7 @@ struct VChunk<2> {
 
 template <>
 struct VChunk<1> {
-  uint32_t s[4];
+  uint32_t s[2];
   Bits16 sg;
   __device__ __forceinline__ void prepare() { sg.build(s); }
   __device__ __forceinline__ void frag(uint32_t, uint32_t m0, int mt, uint32_t (&a)[4]) const {
@@ -293,7 +310,7 @@ struct VChunk<1> {
 
 // QJL value signs: +-1 pairs.
 struct VSign {
-  uint32_t s[4];
+  uint32_t s[2];
   Bits16 sg;
   __device__ __forceinline__ void prepare() { sg.build(s); }
   __device__ __forceinline__ void frag(int mt, uint32_t (&a)[4]) const {
@@ -364,18 +381,26 @@ struct Stage {
 };
 
 // Start the bulk copies of tiles [tile, tile + nt) (nt = 1 or 2: adjacent 16-token blocks of the
-// slab, so each side is one contiguous copy) into the pair stage at shared address `st`: K blocks
-// at st, V blocks at st + 2 * (K block bytes).  Lane 0 registers the byte count on `bar` and
-// issues both copies.
-template <int KB, bool KQ, bool KH, int VB, bool VQ>
+// slab (b, h), so each side is one contiguous copy) into the pair stage at shared address `st`:
+// K blocks at st, V blocks at st + 2 * (K block bytes).  Lane 0 registers the byte count on `bar`
+// and issues the copies; a paged pool (PAGED) takes one copy per block (its pages are not
+// adjacent), its blocks looked up through the block table.
+template <int KB, bool KQ, bool KH, int VB, bool VQ, bool PAGED>
 __device__ __forceinline__ void issue_pair(uint32_t st, uint32_t bar, const SlabPtrs& s, int tile, int nt,
-                                           int lane) {
+                                           int lane, const Cache& C, int b, int h) {
   using S = Stage<KB, KQ, KH, VB, VQ>;
   constexpr uint32_t KBL = S::VC, VBL = S::bytes - S::VC;
   if (lane == 0) {
     mbar_arrive_expect_tx(bar, (uint32_t)nt * (KBL + VBL));
-    bulk_g2s(st, s.kb + (unsigned long long)tile * KBL, (uint32_t)nt * KBL, bar);
-    bulk_g2s(st + 2 * KBL, s.vb + (unsigned long long)tile * VBL, (uint32_t)nt * VBL, bar);
+    if constexpr (!PAGED) {
+      bulk_g2s(st, s.kb + (unsigned long long)tile * KBL, (uint32_t)nt * KBL, bar);
+      bulk_g2s(st + 2 * KBL, s.vb + (unsigned long long)tile * VBL, (uint32_t)nt * VBL, bar);
+    } else {
+      for (int i = 0; i < nt; ++i) {
+        bulk_g2s(st + i * KBL, C.blockp(0, b, h, tile + i), KBL, bar);
+        bulk_g2s(st + 2 * KBL + i * VBL, C.blockp(1, b, h, tile + i), VBL, bar);
+      }
+    }
   }
 }
 
@@ -431,29 +456,36 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
     d.zsA = lds_f16(st + S::KZS + 2 * rA);
     d.zsB = lds_f16(st + S::KZS + 2 * rB);
   }
+  // value streams, stored by groups of 16 coordinates ([groups][16 tokens][2W bytes]): the four
+  // tokens 4 lt .. 4 lt + 3 of this thread's group g are contiguous in every stream
+  const int g = 8 * sl + lg;
+  const unsigned char* vc = vst + S::VC;
   if constexpr (VB == 4) {
-    // 8-byte loads of rows 64 bytes apart: lanes with odd lt take the four tokens in the order
-    // 1, 0, 3, 2, so each load mixes token parities and has 2-way instead of 4-way bank conflicts
-    uint2 t[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      t[k] = *reinterpret_cast<const uint2*>(vst + S::VC + (4 * lt + (k ^ (lt & 1))) * VR + 64 * sl + 8 * lg);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) d.v.w[j] = (lt & 1) ? t[j ^ 1] : t[j];
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const unsigned char* v = vst + S::VC + (4 * lt + j) * VR;
-    if constexpr (VB == 4) {
-    } else if constexpr (VB == 3) {
-      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 32 * sl + 4 * lg);
-      d.v.s[j] = lds_u16(v + D / 4 + 16 * sl + 2 * lg);
-    } else if constexpr (VB == 2) {
-      d.v.k[j] = *reinterpret_cast<const uint32_t*>(v + 32 * sl + 4 * lg);
-    } else {
-      d.v.s[j] = lds_u16(v + 16 * sl + 2 * lg);
+    // 32 bytes; threads of odd groups load the two halves in the other order, so the eight
+    // 16-byte loads of a quarter warp fall on distinct banks
+    const unsigned char* a = vc + g * 128 + 32 * lt;
+    const int o = 16 * (lg & 1);
+    const uint4 h0 = *reinterpret_cast<const uint4*>(a + o);
+    const uint4 h1 = *reinterpret_cast<const uint4*>(a + (16 ^ o));
+    const uint4 lo = (lg & 1) ? h1 : h0, hi = (lg & 1) ? h0 : h1;
+    d.v.w[0] = make_uint2(lo.x, lo.y);
+    d.v.w[1] = make_uint2(lo.z, lo.w);
+    d.v.w[2] = make_uint2(hi.x, hi.y);
+    d.v.w[3] = make_uint2(hi.z, hi.w);
+  } else if constexpr (VB == 3 || VB == 2) {
+    const uint4 k4 = *reinterpret_cast<const uint4*>(vc + g * 64 + 16 * lt);
+    d.v.k[0] = k4.x; d.v.k[1] = k4.y; d.v.k[2] = k4.z; d.v.k[3] = k4.w;
+    if constexpr (VB == 3) {  // the 1-bit stream follows the 2-bit stream's 16 records
+      const uint2 s2 = *reinterpret_cast<const uint2*>(vc + kTile * (D / 4) + g * 32 + 8 * lt);
+      d.v.s[0] = s2.x; d.v.s[1] = s2.y;
     }
-    if constexpr (VQ) d.vs.s[j] = lds_u16(vst + S::VS + (4 * lt + j) * (D / 8) + 16 * sl + 2 * lg);
+  } else {
+    const uint2 s2 = *reinterpret_cast<const uint2*>(vc + g * 32 + 8 * lt);
+    d.v.s[0] = s2.x; d.v.s[1] = s2.y;
+  }
+  if constexpr (VQ) {
+    const uint2 s2 = *reinterpret_cast<const uint2*>(vst + S::VS + g * 32 + 8 * lt);
+    d.vs.s[0] = s2.x; d.vs.s[1] = s2.y;
   }
   d.nuVA = lds_f32(vst + S::VN + 4 * rA);
   d.nuVB = lds_f32(vst + S::VN + 4 * rB);
@@ -757,10 +789,10 @@ __device__ __forceinline__ int owner_block(long long x, long long W, int N) {
 }
 
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls of an mbarrier before giving up
-constexpr int kErrWaitTimeout = 1;
-constexpr int kErrSmemPlan = 2;
+constexpr int kErrWaitTimeout = TQ_DEVERR_WAIT_TIMEOUT;
+constexpr int kErrSmemPlan = TQ_DEVERR_SMEM_PLAN;
 
-template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO>
+template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO, bool PAGED>
 __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode_kernel(const DecodeParams p) {
   using SM = DecodeSmem<KB, KQ, KH, VB, VQ, QLO>;
   using SG = Stage<KB, KQ, KH, VB, VQ>;
@@ -793,9 +825,13 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
   const int G = p.G;          // query heads per KV head
   const int Gc = p.Gc;        // query columns per KV head (G nq)
   const int Hq = p.Hkv * G;
-  const int N = p.nblocks;
-  long long x = (long long)blockIdx.x * p.W / N;
-  const long long x_end = (long long)(blockIdx.x + 1) * p.W / N;
+  const long long W = p.tiles<PAGED>();
+  // with host lengths nblocks = min(W, #SMs); with device lengths (paged) the grid is #SMs and the
+  // same min is taken here, so every working block has a non-empty range (the merge counts on it)
+  const int N = PAGED ? (int)(W < p.nblocks ? W : p.nblocks) : p.nblocks;
+  if ((int)blockIdx.x >= N) return;
+  long long x = (long long)blockIdx.x * W / N;
+  const long long x_end = (long long)(blockIdx.x + 1) * W / N;
   unsigned seq = 0;  // tile pairs this warp has streamed so far: stage seq % S, phase (seq / S) & 1
   bool timed_out = false;
 
@@ -804,15 +840,16 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
     int lo = 0, hi = p.B - 1;  // largest b with batch_start[b] <= x
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.batch_start[mid] <= x) lo = mid; else hi = mid - 1;
+      if (p.bstart<PAGED>(mid) <= x) lo = mid; else hi = mid - 1;
     }
     const int b = lo;
-    const int L = p.seq_len[b];
+    const int L = p.len<PAGED>(b);
     const int ntb = (L + kTile - 1) / kTile;  // tiles per slab of batch b
-    const long long off = x - p.batch_start[b];
+    const long long bs = p.bstart<PAGED>(b);
+    const long long off = x - bs;
     const int kvh = (int)(off / ntb);
     const int ts = (int)(off % ntb);  // first tile of the segment
-    const long long slab_start = p.batch_start[b] + (long long)kvh * ntb;
+    const long long slab_start = bs + (long long)kvh * ntb;
     const long long seg_end = min(x_end, slab_start + ntb);
     const int te = ts + (int)(seg_end - x);
     const int pair = b * p.Hkv + kvh;
@@ -871,7 +908,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
     const int m1t = min(te, m0t + per);
     const int nt = m1t - m0t;
     SlabPtrs sp;
-    sp.init(p.cache, b, kvh);
+    if constexpr (!PAGED) sp.init(p.cache, b, kvh);
     WarpState<VQ> st;
     st.reset();
     // both pair stages in flight; a pair stage is refilled as soon as its operands are in
@@ -882,8 +919,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
     for (int k = 0; k < kPairStages; ++k) {
       if (k < npairs) {
         const unsigned sl = (seq + k) % kPairStages;
-        issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
-                                       min(2, nt - 2 * k), lane);
+        issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
+                                       min(2, nt - 2 * k), lane, p.cache, b, kvh);
       }
     }
     for (int k = 0; k < npairs; ++k) {
@@ -899,8 +936,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
         __syncwarp();  // every lane has read the stage
         fence_proxy_async_shared();
         if (k + kPairStages < npairs)
-          issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * (k + kPairStages),
-                                         min(2, nt - 2 * (k + kPairStages)), lane);
+          issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * (k + kPairStages),
+                                         min(2, nt - 2 * (k + kPairStages)), lane, p.cache, b, kvh);
         if (two) {
           if (t0 + 2 * kTile <= Lmin)
             compute_tiles<2, false, QLO>(d, st, qf, qs, qu, qfl, qsl, lxK, lxV, k_m0, v_m0, p, t0, L, Lmin, lg);
@@ -920,8 +957,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
             __syncwarp();
             fence_proxy_async_shared();
             if (k + kPairStages < npairs)
-              issue_pair<KB, KQ, KH, VB, VQ>(my_stages_s + sl * PB, my_bars + 8 * sl, sp,
-                                             m0t + 2 * (k + kPairStages), min(2, nt - 2 * (k + kPairStages)), lane);
+              issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp,
+                                             m0t + 2 * (k + kPairStages), min(2, nt - 2 * (k + kPairStages)), lane, p.cache, b, kvh);
           }
           const int tj = t0 + j * kTile;
           if (tj + kTile <= Lmin)
@@ -988,8 +1025,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
     }
 
     // ---- the last block of this slab merges all its partials
-    const int c_first = owner_block(slab_start, p.W, N);
-    const int c_last = owner_block(slab_start + ntb - 1, p.W, N);
+    const int c_first = owner_block(slab_start, W, N);
+    const int c_last = owner_block(slab_start + ntb - 1, W, N);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1198,17 +1235,26 @@ cudaError_t check_dyn_base(K kernel) {
 }
 
 // Launch helpers used by the per-bit-width instantiation units.
-template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO>
+template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO, bool PAGED>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
   using SM = DecodeSmem<KB, KQ, KH, VB, VQ, QLO>;
   static_assert(SM::bytes <= 227 * 1024, "decode shared memory exceeds the per-block limit");
-  cudaError_t e = check_dyn_base(decode_kernel<KB, KQ, KH, VB, VQ, QLO>);
+  auto kern = decode_kernel<KB, KQ, KH, VB, VQ, QLO, PAGED>;
+  cudaError_t e = check_dyn_base(kern);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<KB, KQ, KH, VB, VQ, QLO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)SM::bytes);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::bytes);
   if (e != cudaSuccess) return e;
-  decode_kernel<KB, KQ, KH, VB, VQ, QLO><<<grid, SM::NW * 32, SM::bytes, s>>>(p);
+  kern<<<grid, SM::NW * 32, SM::bytes, s>>>(p);
   return cudaGetLastError();
+}
+
+template <int KB, bool KQ, bool KH, int VB, bool VQ>
+cudaError_t launch_decode_any(const DecodeParams& p, dim3 grid, cudaStream_t s) {
+  const bool qlo = p.lo_xor == 0, paged = p.cache.block_table != nullptr;
+  if (paged) return qlo ? launch_decode_t<KB, KQ, KH, VB, VQ, true, true>(p, grid, s)
+                        : launch_decode_t<KB, KQ, KH, VB, VQ, false, true>(p, grid, s);
+  return qlo ? launch_decode_t<KB, KQ, KH, VB, VQ, true, false>(p, grid, s)
+             : launch_decode_t<KB, KQ, KH, VB, VQ, false, false>(p, grid, s);
 }
 
 template <int KB, bool KQ, bool KH>
@@ -1236,8 +1282,7 @@ bool dispatch_logits_k4(int kq, int kh, const LogitsParams& p, dim3 g, cudaStrea
 
 #define TQ_DECODE_CASE(KB_, KQ_, KH_, VB_, VQ_)                                           \
   if (kq == KQ_ && kh == KH_ && vb == VB_ && vq == VQ_) {                                 \
-    if (e) *e = p.lo_xor == 0 ? launch_decode_t<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0, true>(p, g, s)      \
-                              : launch_decode_t<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0, false>(p, g, s);    \
+    if (e) *e = launch_decode_any<KB_, KQ_ != 0, KH_ != 0, VB_, VQ_ != 0>(p, g, s);                \
     return true;                                                                          \
   }
 #define TQ_LOGITS_CASE(KB_, KQ_, KH_)                                                     \

@@ -31,6 +31,10 @@ struct Tables {
 
 // The packed cache in 16-token blocks: field r of token t of slab s = b * H + h at
 // base + side_off[side] + (s * tiles_per_slab + t / 16) * block[side] + off[r] + (t % 16) * rec[r].
+// Paged (block_table set): block t / 16 of (b, h) is block page * H + h of its side's array, page
+// = block_table[b * max_blocks + t / 16]; a block index past max_blocks or a page outside
+// [0, num_pages) goes to page num_pages (the pool's redirect page) and records
+// TQ_DEVERR_BAD_PAGE in *err (when err is set).
 struct Cache {
   unsigned char* base;
   unsigned long long side_off[2];
@@ -39,17 +43,46 @@ struct Cache {
   unsigned int rec[tqi::R_COUNT];
   int num_kv_heads;
   int tiles_per_slab;
+  const int* block_table;
+  int max_blocks;
+  int num_pages;
+  int* err;
 
+  __device__ __forceinline__ int page_of(int b, int tile) const {
+    int page = -1;
+    if ((unsigned)tile < (unsigned)max_blocks) page = __ldg(block_table + (long long)b * max_blocks + tile);
+    if ((unsigned)page >= (unsigned)num_pages) {
+      if (err) atomicExch(err, TQ_DEVERR_BAD_PAGE);
+      page = num_pages;
+    }
+    return page;
+  }
   // block `tile` of slab (b, h) on side 0 (K) or 1 (V)
   __device__ __forceinline__ unsigned char* blockp(int side, int b, int h, int tile) const {
-    return base + side_off[side] +
-           ((unsigned long long)(b * num_kv_heads + h) * tiles_per_slab + tile) * block[side];
+    const unsigned long long blk =
+        block_table ? (unsigned long long)page_of(b, tile) * num_kv_heads + h
+                    : (unsigned long long)(b * num_kv_heads + h) * tiles_per_slab + tile;
+    return base + side_off[side] + blk * block[side];
   }
+  // (t >> 4, t & 15: a negative position of a paged append lands in the redirect page)
   __device__ __forceinline__ unsigned char* ptr(int r, int b, int h, int t) const {
     const int side = r >= tqi::R_V_CODES ? 1 : 0;
-    return blockp(side, b, h, t / tqi::kTileTokens) + off[r] + (t % tqi::kTileTokens) * rec[r];
+    return blockp(side, b, h, t >> 4) + off[r] + (t & (tqi::kTileTokens - 1)) * rec[r];
+  }
+  // start of field r in the block of token t (for the value streams, stored by coordinate group)
+  __device__ __forceinline__ unsigned char* fieldp(int r, int b, int h, int t) const {
+    const int side = r >= tqi::R_V_CODES ? 1 : 0;
+    return blockp(side, b, h, t >> 4) + off[r];
   }
 };
+
+// Value-side streams (V codes, each stream of a 3-bit code on its own, V QJL signs) are stored
+// by groups of 16 coordinates: [groups][16 tokens][2W bytes] for a W-bit stream, so byte j of
+// the record of block position pos is at grouped_byte(j, pos, W) from the stream's start.
+__device__ __forceinline__ unsigned grouped_byte(unsigned j, unsigned pos, unsigned W) {
+  return (j / (2 * W)) * 32 * W + pos * 2 * W + j % (2 * W);
+}
+static_assert(tqi::kTileTokens == 16, "ptr() splits positions with shifts by 4");
 
 inline Tables make_tables(const tq_context* ctx) {
   const unsigned char* b = (const unsigned char*)ctx->dev_tables;
@@ -82,6 +115,24 @@ inline Cache make_cache(const tq_context* ctx, const void* cache) {
   }
   c.num_kv_heads = ctx->cfg.num_kv_heads;
   c.tiles_per_slab = (int)ctx->layout.tiles_per_slab;
+  c.block_table = nullptr;
+  c.max_blocks = 0;
+  c.num_pages = 0;
+  c.err = nullptr;
+  return c;
+}
+
+// The paged pool's view: the same block format, arrays of (num_pages + 1) * H_kv blocks.
+inline Cache make_paged_cache(const tq_context* ctx, const void* pool, const tq_page_table& pt, int* err) {
+  Cache c = make_cache(ctx, pool);
+  const tqi::Layout L = tqi::make_layout(ctx->cfg, ctx->m, pt.num_pages);
+  c.side_off[0] = L.side_off[0];
+  c.side_off[1] = L.side_off[1];
+  c.tiles_per_slab = 0;
+  c.block_table = pt.block_table;
+  c.max_blocks = pt.max_blocks_per_seq;
+  c.num_pages = pt.num_pages;
+  c.err = err;
   return c;
 }
 

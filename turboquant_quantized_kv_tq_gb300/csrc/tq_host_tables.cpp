@@ -151,10 +151,11 @@ void sketch_matrix(uint64_t seed, uint64_t stream, int m, int d, float* out) {
 
 static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
-Layout make_layout(const tq_config& cfg, int m) {
+Layout make_layout(const tq_config& cfg, int m, long long pages) {
   Layout L;
-  L.tiles_per_slab = (uint64_t)cfg.capacity / kTileTokens;
-  const uint64_t blocks = (uint64_t)cfg.batch * cfg.num_kv_heads * L.tiles_per_slab;
+  L.tiles_per_slab = pages < 0 ? (uint64_t)cfg.capacity / kTileTokens : 0;
+  const uint64_t blocks = pages < 0 ? (uint64_t)cfg.batch * cfg.num_kv_heads * L.tiles_per_slab
+                                    : (uint64_t)(pages + 1) * cfg.num_kv_heads;
   const uint64_t d = cfg.head_dim;
   uint64_t rec[R_COUNT] = {0};
   rec[R_K_CODES] = d * cfg.k.bits / 8;

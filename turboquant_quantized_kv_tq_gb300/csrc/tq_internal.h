@@ -44,7 +44,8 @@ uint64_t splitmix_mix64(uint64_t z);
 void rotation_signs(uint64_t seed, uint64_t stream, int d, float* out);
 void sketch_matrix(uint64_t seed, uint64_t stream, int m, int d, float* out);
 
-Layout make_layout(const tq_config& cfg, int m);
+// pages >= 0: a paged pool of pages + 1 pages (the last one takes redirected accesses)
+Layout make_layout(const tq_config& cfg, int m, long long pages = -1);
 TableOffsets make_table_offsets(const tq_config& cfg, int m);
 
 void set_error(const std::string& msg);
@@ -66,6 +67,9 @@ namespace tqi {
 typedef struct CUstream_st* Stream;
 tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
                         tq_dtype dtype, int n_new, const int32_t* start, Stream stream);
+tq_status launch_append_paged(const tq_context* ctx, void* pool, const tq_page_table* pt, const void* k,
+                              const void* v, tq_dtype dtype, int n_new, const int32_t* dev_start,
+                              int32_t* dev_error, Stream stream);
 tq_status launch_rotate_basis(const tq_context* ctx, const float* U, Stream stream);
 tq_status launch_dequantize(const tq_context* ctx, const void* cache, int b, int kvh, int t0,
                             int t1, float* k_out, float* v_out, Stream stream);
@@ -73,6 +77,9 @@ size_t decode_workspace_bytes(const tq_context* ctx, int max_seq);
 tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const float* q, int nq,
                               const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
                               Stream stream);
+tq_status launch_decode_paged(const tq_context* ctx, const void* pool, const tq_page_table* pt,
+                              const float* q, int nq, const int32_t* dev_seq_len, float* out, void* ws,
+                              size_t ws_bytes, Stream stream);
 tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
                         const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
                         Stream stream);
