@@ -148,6 +148,9 @@ template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
+  // the decode launched after this kernel may start its own setup now (it waits for this
+  // kernel's results before reading them)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   extern __shared__ __align__(16) float skt_smem[];
   const float* SKT = p.tab.S_K_T;
   if (D == kDecD && p.kq) {  // S_K^T (64 KiB) into shared memory: 128 dependent rows per head

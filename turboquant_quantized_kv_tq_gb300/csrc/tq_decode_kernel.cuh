@@ -788,6 +788,10 @@ __device__ __forceinline__ int owner_block(long long x, long long W, int N) {
   return (int)(((x + 1) * N - 1) / W);
 }
 
+// Programmatic dependent launch: wait until the preceding kernel of the stream has completed and
+// its memory is visible (returns at once when the launch had no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls of an mbarrier before giving up
 constexpr int kErrWaitTimeout = TQ_DEVERR_WAIT_TIMEOUT;
 constexpr int kErrSmemPlan = TQ_DEVERR_SMEM_PLAN;
@@ -805,6 +809,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
   // generic pointer of shared-window address a
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
   if (sbase > kDynBaseMax) {  // the plan does not fit this launch: report, do nothing
+    grid_dependency_wait();    // (after the prep kernel's reset of the error word)
     if (threadIdx.x == 0) atomicExch(p.err, kErrSmemPlan);
     return;
   }
@@ -825,6 +830,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
   const int G = p.G;          // query heads per KV head
   const int Gc = p.Gc;        // query columns per KV head (G nq)
   const int Hq = p.Hkv * G;
+  if constexpr (PAGED) grid_dependency_wait();  // the work split itself comes from the prep kernel
   const long long W = p.tiles<PAGED>();
   // with host lengths nblocks = min(W, #SMs); with device lengths (paged) the grid is #SMs and the
   // same min is taken here, so every working block has a non-empty range (the merge counts on it)
@@ -853,6 +859,33 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
     const long long seg_end = min(x_end, slab_start + ntb);
     const int te = ts + (int)(seg_end - x);
     const int pair = b * p.Hkv + kvh;
+
+    // ---- this warp's tiles of the segment, streamed through its bulk-copy ring
+    const int n = te - ts;
+    const int per = (n + SM::NW - 1) / SM::NW;
+    const int m0t = min(te, ts + warp * per);
+    const int m1t = min(te, m0t + per);
+    const int nt = m1t - m0t;
+    SlabPtrs sp;
+    if constexpr (!PAGED) sp.init(p.cache, b, kvh);
+    WarpState<VQ> st;
+    st.reset();
+    // both pair stages in flight; a pair stage is refilled as soon as its operands are in
+    // registers, before the pair is computed
+    constexpr uint32_t KBL = SG::VC, VBL = SG::bytes - SG::VC, PB = 2 * SG::bytes;
+    const int npairs = (nt + 1) >> 1;
+#pragma unroll
+    for (int k = 0; k < kPairStages; ++k) {
+      if (k < npairs) {
+        const unsigned sl = (seq + k) % kPairStages;
+        issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
+                                       min(2, nt - 2 * k), lane, p.cache, b, kvh);
+      }
+    }
+    // the query prep kernel runs just before this one: its outputs (query fragments, tickets,
+    // error word) are read only from here on, so the table build and the first bulk copies above
+    // overlap it (programmatic dependent launch; a no-op without one)
+    grid_dependency_wait();
 
     // ---- query fragments: column lg of KV head kvh, dims [32 lt, 32 lt + 32); columns Gc ..
     // 2 Gc - 1 hold the lo terms when they ride in the same MMA
@@ -901,28 +934,6 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
       }
     }
 
-    // ---- this warp's tiles of the segment, streamed through its bulk-copy ring
-    const int n = te - ts;
-    const int per = (n + SM::NW - 1) / SM::NW;
-    const int m0t = min(te, ts + warp * per);
-    const int m1t = min(te, m0t + per);
-    const int nt = m1t - m0t;
-    SlabPtrs sp;
-    if constexpr (!PAGED) sp.init(p.cache, b, kvh);
-    WarpState<VQ> st;
-    st.reset();
-    // both pair stages in flight; a pair stage is refilled as soon as its operands are in
-    // registers, before the pair is computed
-    constexpr uint32_t KBL = SG::VC, VBL = SG::bytes - SG::VC, PB = 2 * SG::bytes;
-    const int npairs = (nt + 1) >> 1;
-#pragma unroll
-    for (int k = 0; k < kPairStages; ++k) {
-      if (k < npairs) {
-        const unsigned sl = (seq + k) % kPairStages;
-        issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
-                                       min(2, nt - 2 * k), lane, p.cache, b, kvh);
-      }
-    }
     for (int k = 0; k < npairs; ++k) {
       const unsigned cur = seq + k, sl = cur % kPairStages;
       const bool two = 2 * k + 1 < nt;
@@ -1244,8 +1255,19 @@ cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, SM::NW * 32, SM::bytes, s>>>(p);
-  return cudaGetLastError();
+  // may start while the query prep kernel still runs (it waits in grid_dependency_wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(SM::NW * 32);
+  cfg.dynamicSmemBytes = SM::bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int KB, bool KQ, bool KH, int VB, bool VQ>
