@@ -32,6 +32,8 @@ struct AppendParams {
   int headq_rank;
   int qjl_mma;   // QJL sides go to append_qjl_mma_kernel (head dim 128, large appends)
   int stage_st;  // append_kernel blocks of a QJL side stage S^T in shared memory
+  int side_base;     // append_kernel: side of blockIdx.y = 0 (the other, if any, is side_base + 1)
+  int wait_primary;  // append_kernel runs as the dependent launch of append_qjl_mma_kernel
   int start[TQ_MAX_BATCH];
   const int* dev_start;  // set: start positions from device memory (paged pool)
 };
@@ -404,15 +406,12 @@ __device__ __forceinline__ void sketch_signs_ffma(const AppendParams& p, int sid
     store_stream_grouped<E, 1>(C.fieldp(tqi::R_V_SIGNS, b, h, t), t & (tqi::kTileTokens - 1), sbit);
 }
 
-// AppendNV consecutive vectors of side blockIdx.y per warp.  With stage_st set (small appends
-// at head dim 128 with a QJL side), a block of a QJL side first copies S^T (64 KiB) into shared
-// memory, so the sketch's 128 dependent table rows come from there instead of L2.
+// One block of append_kernel (below).
 template <int D, typename Tin>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+__device__ __forceinline__ void append_body(const AppendParams& p, float* st_smem) {
   constexpr int E = D / 32;
   constexpr int NV = AppendNV<D>::value;
-  extern __shared__ __align__(16) float st_smem[];
-  const int side = (int)blockIdx.y;
+  const int side = p.side_base + (int)blockIdx.y;
   if (p.qjl[side] && p.qjl_mma) return;  // left to append_qjl_mma_kernel (whole block)
   const float* ST = side ? p.tab.S_V_T : p.tab.S_K_T;
   if (D == 128 && p.stage_st && p.qjl[side]) {
@@ -440,6 +439,19 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const Appen
     for (int v = 0; v < NV; ++v)
       if (ok[v]) sketch_signs_ffma<D>(p, side, b[v], h[v], t[v], res[v], ST);
   }
+}
+
+// AppendNV consecutive vectors of side side_base + blockIdx.y per warp.  With stage_st set
+// (small appends at head dim 128 with a QJL side), a block of a QJL side first copies S^T
+// (64 KiB) into shared memory, so the sketch's 128 dependent table rows come from there instead
+// of L2.  Launched right after append_qjl_mma_kernel as its programmatic dependent (the other,
+// non-QJL side of a large append), its blocks fill that kernel's last wave; each waits for it
+// before exiting, so this grid's completion still implies the whole append's.
+template <int D, typename Tin>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+  extern __shared__ __align__(16) float st_smem[];
+  append_body<D, Tin>(p, st_smem);
+  if (p.wait_primary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // QJL sides of large appends at head dim 128: a block of kQjlWarps warps takes 64 vectors of one
@@ -489,6 +501,9 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
   __half* Rlo = reinterpret_cast<__half*>(smem + 2 * QjlSmem::table + QjlSmem::resid);
   unsigned char* sg = smem + 2 * QjlSmem::table + 2 * QjlSmem::resid;  // [64][16] sign bytes
   uint32_t* unc = reinterpret_cast<uint32_t*>(sg + QjlSmem::signs);    // [64] near-zero flags
+  // the other side's append_kernel, launched next as a programmatic dependent, may start as soon
+  // as every block of this grid is running (it fills the last wave)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const long long per_side = (long long)p.B * p.Hkv * p.n_new;
   const long long v0 = (long long)blockIdx.x * kQjlBlockVec;
 
@@ -795,13 +810,49 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
   p.stage_st = (ctx->cfg.head_dim == 128 && nq > 0 && !p.qjl_mma) ? 1 : 0;
   const int smem = p.stage_st ? 128 * 128 * 4 : 0;
   const cudaStream_t cs = (cudaStream_t)stream;
+  // A large append with a QJL side: the tensor-core sketch kernel takes the QJL side(s) first,
+  // and append_kernel the other side (if any) as its programmatic dependent launch.
+  if (p.qjl_mma) {
+    const dim3 qgrid((unsigned)((per_side + kQjlBlockVec - 1) / kQjlBlockVec), (unsigned)nq),
+        qblock(kQjlWarps * 32);
+    auto goq = [&](auto kern) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QjlSmem::bytes);
+      if (e == cudaSuccess) kern<<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
+      return e;
+    };
+    const cudaError_t e = dtype == TQ_F32 ? goq(append_qjl_mma_kernel<float>)
+                          : dtype == TQ_BF16 ? goq(append_qjl_mma_kernel<__nv_bfloat16>)
+                                             : goq(append_qjl_mma_kernel<__half>);
+    if (e != cudaSuccess) {
+      set_error(std::string("append sketch: ") + cudaGetErrorString(e));
+      return TQ_ERR_CUDA;
+    }
+    tq_status s = launch_status("append sketch");
+    if (s != TQ_OK || nq == 2) return s;  // both sides done by the sketch kernel
+    p.side_base = p.qjl[0] ? 1 : 0;
+    p.wait_primary = 1;
+  } else {
+    p.side_base = 0;
+    p.wait_primary = 0;
+  }
+  const unsigned nsides = p.qjl_mma ? 1u : 2u;
   cudaError_t ae = cudaSuccess;
   tq_status s = dispatch_d(ctx->cfg.head_dim, [&](auto dc) {
     constexpr int D = decltype(dc)::value;
-    const dim3 grid((unsigned)blocks, 2), block(kWarpsPerBlock * 32);
     auto go = [&](auto kern) {
       if (smem) ae = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (ae == cudaSuccess) kern<<<grid, block, smem, cs>>>(p);
+      if (ae != cudaSuccess) return;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)blocks, nsides);
+      cfg.blockDim = dim3(kWarpsPerBlock * 32);
+      cfg.dynamicSmemBytes = (size_t)smem;
+      cfg.stream = cs;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = p.wait_primary ? 1 : 0;
+      ae = cudaLaunchKernelEx(&cfg, kern, p);
     };
     if (dtype == TQ_F32) go(append_kernel<D, float>);
     else if (dtype == TQ_BF16) go(append_kernel<D, __nv_bfloat16>);
@@ -812,26 +863,7 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
     return TQ_ERR_CUDA;
   }
   if (s != TQ_OK) return s;
-  s = launch_status("append");
-  if (s != TQ_OK || !p.qjl_mma) return s;
-  const dim3 qgrid((unsigned)((per_side + kQjlBlockVec - 1) / kQjlBlockVec), (unsigned)nq), qblock(kQjlWarps * 32);
-  cudaError_t e;
-  if (dtype == TQ_F32) {
-    e = cudaFuncSetAttribute(append_qjl_mma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, QjlSmem::bytes);
-    if (e == cudaSuccess) append_qjl_mma_kernel<float><<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
-  } else if (dtype == TQ_BF16) {
-    e = cudaFuncSetAttribute(append_qjl_mma_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             QjlSmem::bytes);
-    if (e == cudaSuccess) append_qjl_mma_kernel<__nv_bfloat16><<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(append_qjl_mma_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, QjlSmem::bytes);
-    if (e == cudaSuccess) append_qjl_mma_kernel<__half><<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
-  }
-  if (e != cudaSuccess) {
-    set_error(std::string("append sketch: ") + cudaGetErrorString(e));
-    return TQ_ERR_CUDA;
-  }
-  return launch_status("append sketch");
+  return launch_status("append");
 }
 
 tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
