@@ -180,6 +180,27 @@ def test_layout_matches_oracle(scheme, n, headq):
     b.tq_context_destroy(ctx)
 
 
+@pytest.mark.parametrize("scheme,n,pages", [("tq", 4, 1), ("kqv", 4, 37), ("qkqv", 3, 5)])
+def test_paged_layout(scheme, n, pages):
+    # the pool's arrays are [(num_pages + 1) * H_kv] blocks of the contiguous layout's block
+    # format (one extra page takes redirected accesses); the V array starts on a 256-byte boundary
+    c = _cfg(d=128, hq=8, hkv=2, batch=3, cap=192, scheme=scheme, n=n)
+    ctx = _ctx(c)
+    flat, lay = b.tq_cache_layout(), b.tq_cache_layout()
+    b.check(b.tq_get_cache_layout(ctx, flat))
+    b.check(b.tq_get_paged_cache_layout(ctx, pages, lay))
+    blocks = (pages + 1) * 2
+    assert (lay.k_block_bytes, lay.v_block_bytes) == (flat.k_block_bytes, flat.v_block_bytes)
+    assert lay.k_offset == 0
+    assert lay.v_offset == (blocks * lay.k_block_bytes + 255) // 256 * 256
+    assert lay.total_bytes == lay.v_offset + blocks * lay.v_block_bytes
+    for name in b.REGION_NAMES:
+        assert (getattr(lay, name).offset, getattr(lay, name).record_bytes) == \
+            (getattr(flat, name).offset, getattr(flat, name).record_bytes), name
+    assert b.tq_get_paged_cache_layout(ctx, 0, lay) == b.TQ_ERR_INVALID_ARG
+    b.tq_context_destroy(ctx)
+
+
 @pytest.mark.parametrize("d", [256, 1024])
 def test_value_sketch_output_domain_table(d):
     # head dims above 128 with a QJL value side carry S_V R_V after the other arrays
