@@ -501,6 +501,66 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_workload(args):
+    """Decode throughput of one of the other configurations at its full shape, per scheme: the
+    cache filled by the library's append (4096-token chunks), then `reps` decode calls timed
+    with CUDA events (query prep + decode).  One JSON line; not the headline contract line."""
+    import torch
+    from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
+    from turboquant_quantized_kv_tq_gb300.workloads import CONFIGS, make_inputs
+    name = args.workload
+    device = torch.device("cuda", 0)
+    inp = make_inputs(name)
+    c = CONFIGS[name]
+    B, Hq, Hkv, d, T = inp.B, inp.Hq, inp.Hkv, inp.d, inp.T
+    to_t = (lambda a: torch.from_numpy(a)) if inp.dtype == "f32" else \
+        (lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16))
+    q = torch.from_numpy(inp.q).to(device)
+    out = torch.empty_like(q)
+    seq = [T] * B
+    peak, peak_kind = measured_peak()
+    res = {}
+    for scheme, n in c["schemes"]:
+        if scheme == "headq":
+            kv = QuantizedKVCache(d, Hq, Hkv, B, T, scheme=None, seed=inp.seed, k_codec=(n, 1, 0),
+                                  v_codec=(4, 1, 0), headq_rank=c["headq_rank"], device=device)
+            U = []
+            for h in range(Hkv):  # calibration basis: top eigenvectors of the centred query covariance
+                x = inp.extra["calib"][h].astype(np.float64)
+                x = x - x.mean(axis=0, keepdims=True)
+                w, vecs = np.linalg.eigh(x.T @ x)
+                U.append(vecs[:, np.argsort(-w)[:c["headq_rank"]]])
+            kv.set_headq_basis(torch.from_numpy(np.stack(U).astype(np.float32)).to(device))
+        else:
+            kv = QuantizedKVCache(d, Hq, Hkv, B, T, scheme=scheme, n=n, seed=inp.seed, device=device)
+        for s0 in range(0, T, 4096):
+            e = min(T, s0 + 4096)
+            kv.append(to_t(inp.K[:, :, s0:e]).to(device), to_t(inp.V[:, :, s0:e]).to(device), [s0] * B)
+        kv.workspace(T)
+        for _ in range(args.warmup):
+            kv.decode(q, seq, out=out)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 50
+        e0.record()
+        for _ in range(reps):
+            kv.decode(q, seq, out=out)
+        e1.record()
+        torch.cuda.synchronize(device)
+        us = e0.elapsed_time(e1) / reps * 1e3
+        rec = (kv.layout.k_block_bytes + kv.layout.v_block_bytes) / 16.0
+        nbytes = B * Hkv * T * rec
+        res[f"{scheme}{n}"] = {"decode_us": round(us, 2), "record_bytes": rec,
+                               "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                               "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
+                               "cache_tokens_per_s": round(B * Hkv * T / (us * 1e-6), 1)}
+        del kv
+        torch.cuda.empty_cache()
+    print(json.dumps({"workload": f"{name}: B={B} Hq={Hq} Hkv={Hkv} d={d} T={T}", "unit": UNIT,
+                      "peak_GBps": peak, "peak_kind": peak_kind, "timing": "CUDA events, 50 decode calls",
+                      "schemes": res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -513,7 +573,12 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")
     ap.add_argument("--schemes", default=None,
                     help="comma-separated subset of plain4,tq4,kqv4,qkqv4 (default: all four)")
+    ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5"],
+                    help="decode throughput of another configuration at full size (one JSON line)")
     args = ap.parse_args()
+    if args.workload:
+        run_workload(args)
+        return
     if args.schemes:
         global SCHEMES
         known = {f"{s}{n}": (s, n) for s, n in SCHEMES}
