@@ -481,15 +481,22 @@ def run_reference(args):
         orc.append(buf, inp.k_f32()[:, :, :T].astype(np.float64), inp.v_f32()[:, :, :T].astype(np.float64), [0])
         ctxs.append(orc)
         bufs.append(buf)
+    # each step decodes the first L tokens of the slab, L sized from the warm-up so that the K
+    # timed steps take about args.ref_seconds in all (the oracle's cost is linear in L)
+    t = time.perf_counter()
     for _ in range(args.warmup):
         oracle_step(inp, bufs, ctxs, [(0, 0)], T)
+    per_full = (time.perf_counter() - t) / max(1, args.warmup)
+    L = int(T * args.ref_seconds / (args.steps * per_full)) // 16 * 16
+    L = max(16, min(T, L))
     t = time.perf_counter()
     done = 0
     for _ in range(args.steps):
-        done += oracle_step(inp, bufs, ctxs, [(0, 0)], T)
+        done += oracle_step(inp, bufs, ctxs, [(0, 0)], L)
     el = time.perf_counter() - t
     value = done / el
-    sample = f"per step: one (batch, KV head) slab of each of the 4 schemes decoded over {T} tokens, 4 query heads"
+    sample = (f"per step: one (batch, KV head) slab of each of the 4 schemes decoded over its first {L} "
+              f"of {T} tokens (sized so {args.steps} steps take about {args.ref_seconds:.0f} s), 4 query heads")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -568,6 +575,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: approximate time of the timed steps")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-append", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")
