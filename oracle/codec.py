@@ -47,6 +47,7 @@ class SideCodec:
     bits: int
     rotate: bool
     qjl: bool
+    spectral: bool = False  # SQU-KV (oracle/spectral.py): calibrated basis, 32 x 4 + 96 x 1 bits
 
 
 def scheme_codecs(scheme, n):
@@ -64,6 +65,10 @@ def scheme_codecs(scheme, n):
         if n < 2:
             raise ValueError("QKQV needs n >= 2")
         return SideCodec(n - 1, True, True), SideCodec(n - 1, True, True)
+    if s in ("squ", "squ-kv"):
+        if n != 2:
+            raise ValueError("SQU-KV is built at n = 2 (its record is TQ-KV n=2's size)")
+        return SideCodec(2, False, False, True), SideCodec(2, False, False, True)
     raise ValueError("unknown scheme " + scheme)
 
 

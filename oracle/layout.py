@@ -56,19 +56,21 @@ class CacheShape:
     m: int
     headq_rank: int = 0
     headq_bits: int = 4
+    k_sq: bool = False  # SQU-KV sides (oracle/spectral.py): d/4-byte code records
+    v_sq: bool = False
 
 
 def side_fields(shape, side):
     """[(field name, bytes per token)] of one side's block, in block order."""
     d, m = shape.head_dim, shape.m
     if side == "k":
-        f = [("k_codes", d * shape.k_bits // 8), ("k_norm", 4)]
+        f = [("k_codes", d // 4 if shape.k_sq else d * shape.k_bits // 8), ("k_norm", 4)]
         if shape.k_qjl:
             f += [("k_signs", m // 8), ("k_rho", 2)]
         if shape.headq_rank:
             f += [("k_side", shape.headq_rank * shape.headq_bits // 8), ("k_side_scale", 2)]
         return f
-    f = [("v_codes", d * shape.v_bits // 8), ("v_norm", 4)]
+    f = [("v_codes", d // 4 if shape.v_sq else d * shape.v_bits // 8), ("v_norm", 4)]
     if shape.v_qjl:
         f += [("v_signs", m // 8), ("v_rho", 2)]
     return f
@@ -93,6 +95,8 @@ def layout(shape):
 
 def grouped_streams(shape, name):
     """[(width w, coordinates n)] of a value-side field stored by coordinate groups, else None."""
+    if name == "v_codes" and shape.v_sq:  # magnitudes then signs, 2 bytes per group each
+        return [(1, shape.head_dim), (1, shape.head_dim)]
     if name == "v_codes":
         d, b = shape.head_dim, shape.v_bits
         return {4: [(4, d)], 3: [(2, d), (1, d)], 2: [(2, d)], 1: [(1, d)]}[b]

@@ -7,12 +7,15 @@ module only routes arrays (see ``codec``, ``layout``, ``attention``, ``headq``).
 
 import numpy as np
 
-from . import attention, codebook, codec, layout, rotation, tables
+from . import attention, codebook, codec, layout, rotation, spectral, tables
 
 
 class OracleContext:
     def __init__(self, head_dim, num_q_heads, num_kv_heads, batch, capacity,
-                 k_codec, v_codec, seed, m=None, headq_rank=0, headq_bits=4, headq_basis=None):
+                 k_codec, v_codec, seed, m=None, headq_rank=0, headq_bits=4, headq_basis=None,
+                 spectral_k=None, spectral_v=None):
+        """spectral_k / spectral_v: per KV head (E32, s32) storage-order tables of an SQU-KV side
+        (oracle/spectral.py)."""
         d = head_dim
         self.d, self.Hq, self.Hkv, self.B, self.capacity = d, num_q_heads, num_kv_heads, batch, capacity
         self.G = num_q_heads // num_kv_heads
@@ -29,8 +32,13 @@ class OracleContext:
         self.S_K = tables.sketch_matrix(seed, tables.STREAM_S_K, self.m, d) if k_codec.qjl else None
         self.S_V = tables.sketch_matrix(seed, tables.STREAM_S_V, self.m, d) if v_codec.qjl else None
         self.U = None if headq_basis is None else np.asarray(headq_basis, dtype=np.float32)
+        self.sq = {"k": spectral_k, "v": spectral_v}
+        if k_codec.spectral or v_codec.spectral:
+            self.C4, self.T4 = codebook.fp32_tables(d, spectral.TOP_BITS)
+            self.C1, self.T1 = codebook.fp32_tables(d, spectral.FLOOR_BITS)
         self.shape = layout.CacheShape(batch, num_kv_heads, capacity, d, k_codec.bits, k_codec.qjl,
-                                       v_codec.bits, v_codec.qjl, self.m, headq_rank, headq_bits)
+                                       v_codec.bits, v_codec.qjl, self.m, headq_rank, headq_bits,
+                                       k_codec.spectral, v_codec.spectral)
         self.cache_bytes = layout.layout(self.shape)["total"]
 
     def new_cache(self):
@@ -38,6 +46,10 @@ class OracleContext:
 
     def encode_side(self, X, side, kvh=0):
         """Encode vectors X (N x d) of one KV head; returns the codec fields (+ side code for HeadQ K)."""
+        cdc = self.k_codec if side == "k" else self.v_codec
+        if cdc.spectral:
+            E32, s32 = self.sq[side][kvh]
+            return spectral.encode(X, side, E32, s32, self.C4, self.T4, self.C1, self.T1)
         if side == "k":
             f = codec.encode(X, self.k_codec, self.C_K, self.T_K, self.R_K, self.S_K)
             if self.headq_rank:
@@ -47,7 +59,10 @@ class OracleContext:
         return codec.encode(X, self.v_codec, self.C_V, self.T_V, self.R_V, self.S_V)
 
     def packed_fields(self, f, side):
-        bits = self.k_codec.bits if side == "k" else self.v_codec.bits
+        cdc = self.k_codec if side == "k" else self.v_codec
+        if cdc.spectral:
+            return {side + "_codes": spectral.pack(f["codes"], side), side + "_norm": f["norm"]}
+        bits = cdc.bits
         out = {side + "_codes": layout.pack_codes(f["codes"], bits), side + "_norm": f["norm"]}
         if "signs" in f:
             out[side + "_signs"] = layout.pack_stream(f["signs"].astype(np.int64), 1)
@@ -80,7 +95,11 @@ class OracleContext:
         """Parse the stored fields of tokens [0, T) of slab (b, h) back from the cache bytes."""
         bits = self.k_codec.bits if side == "k" else self.v_codec.bits
         cdc = self.k_codec if side == "k" else self.v_codec
-        f = {"codes": layout.unpack_codes(layout.read_field(buf, self.shape, side + "_codes", b, h, 0, T), bits, self.d),
+        raw = layout.read_field(buf, self.shape, side + "_codes", b, h, 0, T)
+        if cdc.spectral:
+            return {"codes": spectral.unpack(raw, side, self.d),
+                    "norm": layout.read_field(buf, self.shape, side + "_norm", b, h, 0, T, np.float32)}
+        f = {"codes": layout.unpack_codes(raw, bits, self.d),
              "norm": layout.read_field(buf, self.shape, side + "_norm", b, h, 0, T, np.float32)}
         if cdc.qjl:
             f["signs"] = layout.unpack_stream(layout.read_field(buf, self.shape, side + "_signs", b, h, 0, T), 1, self.m) == 1
@@ -94,6 +113,10 @@ class OracleContext:
         """(K_hat, V_hat) of tokens [0, T) of slab (b, h), float64, from the stored bytes."""
         fk = self.stored_fields(buf, "k", b, h, T)
         fv = self.stored_fields(buf, "v", b, h, T)
+        if self.k_codec.spectral and self.v_codec.spectral:
+            Kh = spectral.reconstruct(fk["codes"], fk["norm"], "k", *self.sq["k"][h], self.C4, self.C1)
+            Vh = spectral.reconstruct(fv["codes"], fv["norm"], "v", *self.sq["v"][h], self.C4, self.C1)
+            return Kh, Vh
         Kh = codec.reconstruct(self.k_codec, fk["codes"], fk["norm"], self.C_K, self.R_K,
                                fk.get("rho"), fk.get("signs"), self.S_K,
                                fk.get("side"), fk.get("side_scale"),
