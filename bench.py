@@ -540,6 +540,11 @@ def run_workload(args):
             kv.set_headq_basis(torch.from_numpy(np.stack(U).astype(np.float32)).to(device))
         else:
             kv = QuantizedKVCache(d, Hq, Hkv, B, T, scheme=scheme, n=n, seed=inp.seed, device=device)
+            if scheme == "squ":  # the regime's separate calibration sets for K and V
+                from turboquant_quantized_kv_tq_gb300.calibration import spectral_tables
+                for side, key in enumerate(("calib_k", "calib_v")):
+                    E, sc, _ = spectral_tables(inp.extra[key])
+                    kv.set_spectral_basis(side, torch.from_numpy(E).to(device), torch.from_numpy(sc).to(device))
         for s0 in range(0, T, 4096):
             e = min(T, s0 + 4096)
             kv.append(to_t(inp.K[:, :, s0:e]).to(device), to_t(inp.V[:, :, s0:e]).to(device), [s0] * B)
@@ -582,7 +587,7 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")
     ap.add_argument("--schemes", default=None,
                     help="comma-separated subset of plain4,tq4,kqv4,qkqv4 (default: all four)")
-    ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5"],
+    ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5", "sq"],
                     help="decode throughput of another configuration at full size (one JSON line)")
     args = ap.parse_args()
     if args.workload:

@@ -60,11 +60,24 @@ typedef enum {
  *   TQ_TQ_KV     K, V: rotation + n-bit code.
  *   TQ_KQV       K: rotation + n-bit code; V: rotation + (n-1)-bit code + 1-bit QJL.
  *   TQ_QKQV      K, V: rotation + (n-1)-bit code + 1-bit QJL (also named TQ-QKV). */
-typedef enum { TQ_PLAIN_KV = 0, TQ_TQ_KV = 1, TQ_KQV = 2, TQ_QKQV = 3 } tq_scheme;
+typedef enum { TQ_PLAIN_KV = 0, TQ_TQ_KV = 1, TQ_KQV = 2, TQ_QKQV = 3, TQ_SQU_KV = 4 } tq_scheme;
 
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
 
-/* One side's codec: scalar code bits (1..4), rotation on/off, QJL residual sketch on/off. */
+/* One side's codec: scalar code bits (1..4), rotation (0 none, 1 seeded Walsh-Hadamard, 2 the
+ * calibrated per-head eigenbasis of SQU-KV), QJL residual sketch on/off.
+ *
+ * rotate = 2 (SQU-KV, SpectralQuant with uniform allocation; [ABL] "Configuração Experimental",
+ * "Armazenamento vs. Qualidade", "Recomendações Práticas" 2-3): bits must be 2 (the budget: 256
+ * bits per vector), qjl 0, head_dim 128.  Per head, the 32 highest-variance directions of the
+ * calibrated basis are coded at 4 bits (the 4-bit Beta Lloyd-Max codebook) and the other 96 at
+ * 1 bit.  Coordinate c of the stored vector is (E^T u)_c / s_c, with E and s set by
+ * tq_spectral_set_basis.  Storage order: with eigen-rank i, key coordinate 32 (i % 4) + i / 4
+ * and value coordinate 16 (i % 8) + i / 8 hold the 32 modeled ranks; the other coordinates
+ * hold ranks 32.. in increasing order.  A code record (32 bytes) is the 4-bit stream of the
+ * modeled coordinates' magnitudes (sign-magnitude form, in increasing coordinate order), then
+ * the 1-bit stream of all 128 signs (1 = positive); on the value side each of the two streams
+ * is stored by 16-coordinate groups (2 bytes per group and token, see tq_cache_layout). */
 typedef struct {
   int32_t bits;
   int32_t rotate;
@@ -108,6 +121,7 @@ typedef struct {
  * is at (j / 2w) * 32w + p * 2w + j % 2w from the stream's start (the 1-bit stream of a 3-bit code
  * starts 16 * d / 4 bytes after the 2-bit one).  One coordinate group of several tokens is then
  * one contiguous read.
+ * (A spectral side's 32-byte code record is described with tq_codec.)
  * Codes are stored in sign-magnitude form (s = [c >= 2^(b-1)], k = magnitude rank) as streams of
  * power-of-two widths, coordinate i of a w-bit stream in bits [w*i, w*i + w), least significant
  * bit first:
@@ -145,15 +159,29 @@ size_t tq_tables_bytes(const tq_context* ctx);
  * Host only.  Blob layout: fp32 k_centroids[16], k_thresholds[16], v_centroids[16],
  * v_thresholds[16]; fp32 k_signs[d], v_signs[d] (+1/-1); fp32 S_K[m][d] and its transpose
  * [d][m] (if K has QJL); fp32 S_V[m][d] and its transpose (if V has QJL); the HeadQ basis area
- * [H_kv][d][r] (zeros until tq_headq_set_basis); and, when d > 128 and V has QJL, fp32
+ * [H_kv][d][r] (zeros until tq_headq_set_basis); when d > 128 and V has QJL, fp32
  * S_V R_V [m][d] (R_V = H D_V / sqrt(d), each row rounded once from a float64 transform), which
- * maps the value sketch accumulator straight to the output domain.  Each array starts on a
- * 256-byte boundary. */
+ * maps the value sketch accumulator straight to the output domain; fp32 c1[2], the 1-bit
+ * codebook's upper centroid (a spectral side's floor); and for each spectral side (K, then V)
+ * its basis E and E^T [H_kv][d][d] and scales s [H_kv][d] in storage order (zeros until
+ * tq_spectral_set_basis).  A spectral side's centroid / threshold slots hold the 4-bit codebook.
+ * Each array starts on a 256-byte boundary. */
 tq_status tq_tables_host(const tq_context* ctx, void* host_dst, size_t bytes);
 
 /* Copy the tables into dev_tables (tq_tables_bytes bytes, caller-owned, 256-byte aligned) on
  * stream and bind that buffer to the context.  The buffer must outlive every later call. */
 tq_status tq_tables_upload(tq_context* ctx, void* dev_tables, tq_stream stream);
+
+/* SQU-KV: store a spectral side's calibrated basis (side 0 = K, 1 = V).  dev_E is fp32
+ * [H_kv][d][d] on the device with column j of head h = eigenvector j (component i at
+ * dev_E[(h d + i) d + j]), ordered by descending eigenvalue.  dev_s is fp32 [H_kv][d], the
+ * coordinate scales in the same eigen-rank order: s_j = sqrt(d lambda_j) for an eigenvalue
+ * lambda_j of the mean of u u^T over the side's calibration unit vectors u (a caller may floor
+ * it; every s_j must be > 0).  The library permutes both into the storage order (see tq_codec)
+ * in the bound table buffer, with a kernel on stream; no value is rounded again.  Needs a
+ * spectral side and uploaded tables; every spectral side must be set before append or decode. */
+tq_status tq_spectral_set_basis(tq_context* ctx, int32_t side, const float* dev_E, const float* dev_s,
+                                tq_stream stream);
 
 /* HeadQ ([HEADQ] "Visão Geral do Algoritmo" 1): store the calibrated key-side basis.
  * dev_U is fp32 [H_kv][d][r] on the device (column k of head h is U_h e_k).  The library keeps

@@ -86,14 +86,20 @@ def top_mask(side, d=128):
     return rank_of_coord(side, d) < TOP
 
 
-def storage_tables(E, lam, side):
-    """(E32, s32): the basis and scales in storage order, rounded to fp32 once (the tables
-    both sides use)."""
+def rank_tables(E, lam):
+    """(E32, s32) in eigen-rank order, rounded to fp32 once: s_j = sqrt(d lambda_j), floored."""
     d = E.shape[0]
     lam = np.asarray(lam, dtype=np.float64)
     s = np.maximum(np.sqrt(d * lam), np.sqrt(d * EIG_FLOOR * lam[0]))
-    r = rank_of_coord(side, d)
-    return np.asarray(E[:, r], dtype=np.float32), np.asarray(s[r], dtype=np.float32)
+    return np.asarray(E, dtype=np.float32), np.asarray(s, dtype=np.float32)
+
+
+def storage_tables(E, lam, side):
+    """(E32, s32): the basis and scales in storage order (a permutation of rank_tables; the
+    tables both sides use)."""
+    E32, s32 = rank_tables(E, lam)
+    r = rank_of_coord(side, E32.shape[0])
+    return E32[:, r], s32[r]
 
 
 def encode(X, side, E32, s32, C4, T4, C1, T1):

@@ -35,7 +35,9 @@ REGIMES = [
     # (config, label, sizes, schemes)
     ("cfg2", "heavy-tailed (Student-t 3), d=128", dict(B=2, Hkv=2, T=2048),
      [("plain", 4), ("tq", 2), ("tq", 3), ("tq", 4), ("kqv", 2), ("kqv", 3), ("kqv", 4),
-      ("qkqv", 2), ("qkqv", 3), ("qkqv", 4)]),
+      ("qkqv", 2), ("qkqv", 3), ("qkqv", 4), ("squ", 2)]),
+    ("sq", "low-rank K and V (rank 16), d=128", dict(B=2, Hkv=2, T=2048),
+     [("tq", 2), ("squ", 2), ("kqv", 2), ("tq", 4)]),
     ("cfg4", "outlier channels (log-uniform std), d=128", dict(B=1, Hkv=2, T=4096),
      [("tq", 4), ("kqv", 2), ("kqv", 3), ("kqv", 4), ("qkqv", 4)]),
     ("cfg3", "low-rank keys (rank 16), d=1024", dict(B=2, Hkv=2, T=1024),
@@ -115,9 +117,20 @@ def _row(regime, label, scheme, n, K, V, Kh, Vh, q, o_ref, o_hat, d, G):
             "out_relmse": orr, "out_dir": od, "kl": kl, "top5": r5}
 
 
+def _calibration_sets(name, inp, sizes):
+    """Per-side calibration vectors [H_kv][n][d] for SQU-KV: the regime's own calibration sets
+    when it has them, else a separate draw of the same recipe (another seed)."""
+    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    if "calib_k" in inp.extra:
+        return inp.extra["calib_k"], inp.extra["calib_v"]
+    cal = make_inputs(name, B=1, T=4096, Hkv=sizes["Hkv"], Hq=inp.Hq, seed=inp.seed + 100)
+    return cal.k_f32()[0].astype(np.float64), cal.v_f32()[0].astype(np.float64)
+
+
 def run_regime(name, label, sizes, schemes, device):
     import torch
     from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
+    from turboquant_quantized_kv_tq_gb300.calibration import spectral_tables
     from turboquant_quantized_kv_tq_gb300.workloads import CONFIGS, make_inputs
     c = CONFIGS[name]
     G = c["Hq"] // c["Hkv"]
@@ -132,6 +145,10 @@ def run_regime(name, label, sizes, schemes, device):
     for scheme, n in schemes:
         kv = QuantizedKVCache(d, Hq, Hkv, B, (T + 63) // 64 * 64, scheme=scheme, n=n, seed=inp.seed,
                               device=device)
+        if scheme == "squ":
+            for side, X in enumerate(_calibration_sets(name, inp, sizes)):
+                E, sc, _ = spectral_tables(X)
+                kv.set_spectral_basis(side, torch.from_numpy(E).to(device), torch.from_numpy(sc).to(device))
         kv.append(Kt, Vt, [0] * B)
         o_hat = kv.decode(torch.from_numpy(inp.q).to(device), [T] * B).cpu().numpy().astype(np.float64)
         Kh, Vh = _dequantize_all(kv, B, Hkv, T, d)

@@ -218,3 +218,36 @@ def test_value_sketch_output_domain_table(d):
     ulp = np.spacing(np.abs(want).astype(np.float32)).astype(np.float64)
     assert np.all(np.abs(T - want) <= ulp)
     b.tq_context_destroy(ctx)
+
+
+def test_spectral_scheme_config_and_validation():
+    c = _cfg(scheme="squ", n=2)
+    assert (c.k.bits, c.k.rotate, c.k.qjl, c.v.bits, c.v.rotate, c.v.qjl) == (2, 2, 0, 2, 2, 0)
+    assert b.tq_config_from_scheme(b.TQ_SQU_KV, 3, c) == b.TQ_ERR_UNSUPPORTED
+    bad = []
+    c1 = _cfg(scheme="squ", n=2); c1.v.rotate = 1; bad.append(c1)        # one side only
+    c2 = _cfg(scheme="squ", n=2); c2.k.bits = 3; bad.append(c2)          # not the 2-bit budget
+    c3 = _cfg(scheme="squ", n=2, d=256); bad.append(c3)                  # head dim 128 only
+    c4 = _cfg(scheme="squ", n=2); c4.headq_rank = 16; bad.append(c4)     # no HeadQ with it
+    for c in bad:
+        ctx = ctypes.c_void_p()
+        assert b.tq_context_create(c, ctx) == b.TQ_ERR_UNSUPPORTED
+        assert not ctx.value
+
+
+def test_spectral_codebook_slots_and_layout():
+    # the centroid / threshold slots of a spectral side hold the 4-bit codebook; the record is
+    # the 2-bit budget (32 bytes at d = 128)
+    c = _cfg(scheme="squ", n=2)
+    ctx = _ctx(c)
+    blob = _blob(ctx)
+    c4, t4 = codebook.fp32_tables(128, 4)
+    off = _offsets(128, 128, 0, 0, 4, 0)
+    assert np.array_equal(blob[off["k_c"]:off["k_c"] + 64].view(np.float32), c4)
+    assert np.array_equal(blob[off["k_t"]:off["k_t"] + 60].view(np.float32), t4)
+    lay = b.tq_cache_layout()
+    b.check(b.tq_get_cache_layout(ctx, lay))
+    assert lay.k_codes.record_bytes == 32 and lay.v_codes.record_bytes == 32
+    shape = layout.CacheShape(2, 2, 128, 128, 2, False, 2, False, 128, 0, 4, True, True)
+    assert lay.total_bytes == layout.layout(shape)["total"]
+    b.tq_context_destroy(ctx)

@@ -189,3 +189,18 @@ def test_pipeline_store_and_read_back():
             want_k = spectral.reconstruct(fields[(b, h)][0]["codes"], fields[(b, h)][0]["norm"], "k",
                                           *tabs["k"][h], C4, C1)
             assert np.allclose(Kh, want_k, atol=1e-12)
+
+
+def test_package_calibration_agrees_with_the_oracle():
+    # the package's host calibration (its own numpy code) gives the oracle's eigenvalues, scales
+    # and subspace; eigenvectors agree up to sign
+    from turboquant_quantized_kv_tq_gb300.calibration import spectral_basis
+    rng = np.random.default_rng(9)
+    X, _ = _low_rank(3000, 128, 12, 0.02, rng)
+    E, lam, d_eff = spectral.calibrate(X)
+    E32o, s32o = spectral.rank_tables(E, lam)
+    Ep, sp, dp = spectral_basis(X)
+    assert dp == d_eff == 12
+    assert np.allclose(sp, s32o, rtol=1e-5)
+    G = np.abs(Ep[:, :12].astype(np.float64).T @ E32o[:, :12].astype(np.float64))
+    assert np.allclose(G, np.eye(12), atol=1e-4)

@@ -71,6 +71,14 @@ class _Codec:
             self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
         return self._ws
 
+    def set_spectral_basis(self, side, E, s, stream=None):
+        """SQU-KV: side 0 (K) or 1 (V); E float32 CUDA [num_kv_heads][d][d], column j = eigenvector j
+        by descending eigenvalue; s float32 CUDA [num_kv_heads][d], s_j = sqrt(d lambda_j)."""
+        E, s = E.contiguous(), s.contiguous()
+        check(_b.tq_spectral_set_basis(self._ctx, int(side), E.data_ptr(), s.data_ptr(), _stream_handle(stream)))
+        self._sq = getattr(self, "_sq", {})
+        self._sq[side] = (E, s)  # keep alive until the kernel has run
+
     def device_error(self, stream=None):
         """(status, code) of the decode workspace's error word (waits for the stream)."""
         code = _b.c_int32(0)

@@ -23,12 +23,13 @@ TQ_ERR_CUDA = 5
 TQ_ERR_DEVICE = 6
 TQ_ERR_STATE = 7
 
-TQ_PLAIN_KV, TQ_TQ_KV, TQ_KQV, TQ_QKQV = 0, 1, 2, 3
+TQ_PLAIN_KV, TQ_TQ_KV, TQ_KQV, TQ_QKQV, TQ_SQU_KV = 0, 1, 2, 3, 4
 TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 TQ_MAX_BATCH = 512
 
 SCHEMES = {"plain": TQ_PLAIN_KV, "plain-kv": TQ_PLAIN_KV, "kv": TQ_PLAIN_KV,
-           "tq": TQ_TQ_KV, "tq-kv": TQ_TQ_KV, "kqv": TQ_KQV, "qkqv": TQ_QKQV, "tq-qkv": TQ_QKQV}
+           "tq": TQ_TQ_KV, "tq-kv": TQ_TQ_KV, "kqv": TQ_KQV, "qkqv": TQ_QKQV, "tq-qkv": TQ_QKQV,
+           "squ": TQ_SQU_KV, "squ-kv": TQ_SQU_KV}
 
 
 class tq_codec(ctypes.Structure):
@@ -92,6 +93,7 @@ DECLARATIONS = [
     ("tq_tables_host", c_int32, [c_void_p, c_void_p, c_size_t]),
     ("tq_tables_upload", c_int32, [c_void_p, c_void_p, c_void_p]),
     ("tq_headq_set_basis", c_int32, [c_void_p, c_void_p, c_void_p]),
+    ("tq_spectral_set_basis", c_int32, [c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
     ("tq_get_cache_layout", c_int32, [c_void_p, ctypes.POINTER(tq_cache_layout)]),
     ("tq_quantize_append", c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                      ctypes.POINTER(c_int32), c_void_p]),

@@ -31,8 +31,10 @@ bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 tq_status validate_codec(const tq_codec& c, const char* side) {
   if (c.bits < 1 || c.bits > 4) return fail(TQ_ERR_INVALID_ARG, std::string(side) + ": bits must be 1..4");
-  if ((c.rotate != 0 && c.rotate != 1) || (c.qjl != 0 && c.qjl != 1))
-    return fail(TQ_ERR_INVALID_ARG, std::string(side) + ": rotate and qjl must be 0 or 1");
+  if ((c.rotate < 0 || c.rotate > 2) || (c.qjl != 0 && c.qjl != 1))
+    return fail(TQ_ERR_INVALID_ARG, std::string(side) + ": rotate must be 0, 1 or 2 and qjl 0 or 1");
+  if (c.rotate == 2 && (c.bits != 2 || c.qjl))
+    return fail(TQ_ERR_UNSUPPORTED, std::string(side) + ": the spectral codec is built at 2 bits without QJL");
   return TQ_OK;
 }
 
@@ -63,6 +65,10 @@ tq_status validate_config(const tq_config& c) {
   }
   if (c.head_dim > 128 && (c.k.qjl || c.headq_rank))
     return fail(TQ_ERR_UNSUPPORTED, "key-side QJL and HeadQ are built for head_dim 128");
+  if ((c.k.rotate == 2) != (c.v.rotate == 2))
+    return fail(TQ_ERR_UNSUPPORTED, "the spectral codec is built for both sides together (SQU-KV)");
+  if (c.k.rotate == 2 && (c.head_dim != 128 || c.headq_rank))
+    return fail(TQ_ERR_UNSUPPORTED, "the spectral codec is built for head_dim 128 without HeadQ");
   return TQ_OK;
 }
 
@@ -98,6 +104,9 @@ tq_status tq_config_from_scheme(tq_scheme scheme, int32_t n, tq_config* c) {
     case TQ_QKQV:
       if (n < 2) return fail(TQ_ERR_INVALID_ARG, "QKQV needs n >= 2");
       c->k = {n - 1, 1, 1}; c->v = {n - 1, 1, 1}; break;
+    case TQ_SQU_KV:
+      if (n != 2) return fail(TQ_ERR_UNSUPPORTED, "SQU-KV is built at n = 2");
+      c->k = {2, 2, 0}; c->v = {2, 2, 0}; break;
     default: return fail(TQ_ERR_INVALID_ARG, "unknown scheme");
   }
   return TQ_OK;
@@ -126,11 +135,18 @@ tq_status tq_context_create(const tq_config* cfg, tq_context** out) {
     for (int i = 0; i < kMaxLevels; ++i) fc[i] = i < L ? (float)c[i] : 0.0f;
     for (int i = 0; i < kMaxLevels; ++i) ft[i] = i < L - 1 ? (float)t[i] : 3.0e38f;
   };
-  put_codebook(cfg->k.bits, ctx->tab.k_centroids, ctx->tab.k_thresholds);
-  put_codebook(cfg->v.bits, ctx->tab.v_centroids, ctx->tab.v_thresholds);
+  // a spectral side's modeled coordinates use the 4-bit codebook, its floor the 1-bit centroid
+  const int kcb = cfg->k.rotate == 2 ? 4 : cfg->k.bits, vcb = cfg->v.rotate == 2 ? 4 : cfg->v.bits;
+  put_codebook(kcb, ctx->tab.k_centroids, ctx->tab.k_thresholds);
+  put_codebook(vcb, ctx->tab.v_centroids, ctx->tab.v_thresholds);
+  {
+    lloyd_max_beta(d, 1, c, t);
+    float* c1 = (float*)(base + ctx->tab.sq_c1);
+    c1[0] = c1[1] = (float)c[1];
+  }
   // the write path's sign-magnitude code search relies on exactly symmetric thresholds
   for (int side = 0; side < 2; ++side) {
-    const int bits = side ? cfg->v.bits : cfg->k.bits;
+    const int bits = side ? vcb : kcb;
     const float* ft = (const float*)(base + (side ? ctx->tab.v_thresholds : ctx->tab.k_thresholds));
     const int h = 1 << (bits - 1);
     bool ok = ft[h - 1] == 0.0f;
@@ -197,6 +213,7 @@ tq_status tq_tables_upload(tq_context* ctx, void* dev_tables, tq_stream stream) 
   if (e != cudaSuccess) return fail(TQ_ERR_CUDA, std::string("table upload: ") + cudaGetErrorString(e));
   ctx->dev_tables = dev_tables;
   ctx->basis_set = false;
+  ctx->sq_set[0] = ctx->sq_set[1] = false;
   return TQ_OK;
 }
 
@@ -207,6 +224,18 @@ tq_status tq_headq_set_basis(tq_context* ctx, const float* dev_U, tq_stream stre
   if (!aligned(dev_U, 16)) return fail(TQ_ERR_INVALID_ARG, "dev_U must be 16-byte aligned");
   tq_status s = launch_rotate_basis(ctx, dev_U, stream);
   if (s == TQ_OK) ctx->basis_set = true;
+  return s;
+}
+
+tq_status tq_spectral_set_basis(tq_context* ctx, int32_t side, const float* dev_E, const float* dev_s,
+                                tq_stream stream) {
+  if (!ctx || !dev_E || !dev_s) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (side != 0 && side != 1) return fail(TQ_ERR_INVALID_ARG, "side must be 0 (K) or 1 (V)");
+  if ((side ? ctx->cfg.v.rotate : ctx->cfg.k.rotate) != 2) return fail(TQ_ERR_STATE, "not a spectral side");
+  if (!ctx->dev_tables) return fail(TQ_ERR_STATE, "tables not uploaded");
+  if (!aligned(dev_E, 16) || !aligned(dev_s, 4)) return fail(TQ_ERR_INVALID_ARG, "misaligned pointer");
+  tq_status s = launch_spectral_basis(ctx, side, dev_E, dev_s, stream);
+  if (s == TQ_OK) ctx->sq_set[side] = true;
   return s;
 }
 
@@ -254,6 +283,9 @@ static tq_status ready(const tq_context* ctx) {
   if (!ctx) return fail(TQ_ERR_INVALID_ARG, "null context");
   if (!ctx->dev_tables) return fail(TQ_ERR_STATE, "tables not uploaded");
   if (ctx->cfg.headq_rank && !ctx->basis_set) return fail(TQ_ERR_STATE, "HeadQ basis not set");
+  for (int side = 0; side < 2; ++side)
+    if ((side ? ctx->cfg.v.rotate : ctx->cfg.k.rotate) == 2 && !ctx->sq_set[side])
+      return fail(TQ_ERR_STATE, "spectral basis not set");
   return TQ_OK;
 }
 
@@ -386,6 +418,8 @@ tq_status tq_headq_correct(const tq_context* ctx, const void* dev_cache, const f
                            const int32_t* host_seq_len, float* logits, int32_t logits_stride,
                            tq_stream stream) {
   tq_status s = ready(ctx);
+  if (s == TQ_OK && ctx->cfg.k.rotate == 2)
+    return fail(TQ_ERR_UNSUPPORTED, "corrected logits are not built for the spectral codec");
   if (s != TQ_OK) return s;
   if (!dev_cache || !q || !host_seq_len || !logits) return fail(TQ_ERR_INVALID_ARG, "null argument");
   if (!aligned(dev_cache, 256) || !aligned(q, 16) || !aligned(logits, 4))

@@ -356,6 +356,96 @@ __device__ __forceinline__ void encode_vectors(const AppendParams& p, int side, 
   }
 }
 
+// SQU-KV write path (head dim 128, rotate = 2): NV vectors of a spectral side.  The norm split
+// as for the other codecs; the calibrated basis in place of the rotation, y = E^T x (E column c
+// = stored coordinate c of head h), z = y / (nu s); a modeled coordinate takes the 4-bit code of
+// z (sign-magnitude, the symmetric search of encode_vectors), a floor coordinate its sign.
+// Stores the record: the modeled coordinates' 4-bit magnitudes, then all 128 signs (value side:
+// both streams by 16-coordinate groups).  [ABL] "Configuração Experimental" (SpectralQuant),
+// "Recomendações Práticas" 2 (uniform allocation).
+template <typename Tin, int NV>
+__device__ __forceinline__ void encode_vectors_sq(const AppendParams& p, int side, const int (&b)[NV],
+                                                  const int (&h)[NV], const int (&j)[NV], const int (&t)[NV],
+                                                  const bool (&valid)[NV]) {
+  constexpr int D = 128, E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const Tin* base = reinterpret_cast<const Tin*>(side ? p.v : p.k);
+  float x[NV][E];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    if (valid[v]) {
+      load_row<E>(base + ((long long)(b[v] * p.Hkv + h[v]) * p.n_new + j[v]) * D + lane * E, x[v]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) x[v][i] = 0.f;
+    }
+  }
+  float nu[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) nu[v] = norm_compensated<E>(x[v]);
+  // y_c = sum_i E[i][c] x_i for this lane's coordinates c = 4 lane + jj
+  float y[NV][E];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int jj = 0; jj < E; ++jj) y[v][jj] = 0.f;
+  const float* Eh[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) Eh[v] = p.tab.sq_E[side] + (long long)h[v] * D * D + lane * E;
+#pragma unroll 4
+  for (int sl = 0; sl < 32; ++sl) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float xi = __shfl_sync(kFull, x[v][e], sl);
+        const float4 er = __ldg(reinterpret_cast<const float4*>(Eh[v] + (E * sl + e) * D));
+        y[v][0] = fmaf(er.x, xi, y[v][0]);
+        y[v][1] = fmaf(er.y, xi, y[v][1]);
+        y[v][2] = fmaf(er.z, xi, y[v][2]);
+        y[v][3] = fmaf(er.w, xi, y[v][3]);
+      }
+    }
+  }
+  const float* thr = side ? p.tab.v_t : p.tab.k_t;  // the 4-bit thresholds on a spectral side
+  float tu[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) tu[k] = __ldg(thr + 8 + k);
+  const bool modeled = sq_modeled(side, E * lane);  // the same for the lane's 4 coordinates
+  const Cache& C = p.cache;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.sq_s[side] + (long long)h[v] * D + lane * E));
+    const float sc[E] = {s4.x, s4.y, s4.z, s4.w};
+    uint32_t sgnbit[E], nib = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float z = nu[v] > 0.f ? __fdiv_rn(y[v][i], nu[v] * sc[i]) : 0.f;
+      const bool pos = z > 0.f;
+      const float a = pos ? z : __int_as_float(__float_as_int(-z) + 1);
+      uint32_t m = 0;
+#pragma unroll
+      for (int k = 0; k < 7; ++k) m += a > tu[k] ? 1u : 0u;
+      sgnbit[i] = pos ? 1u : 0u;
+      nib |= m << (4 * i);
+    }
+    if (!valid[v]) continue;
+    const int pos = t[v] & (tqi::kTileTokens - 1);
+    if (side == 0) {
+      unsigned char* rec = C.ptr(tqi::R_K_CODES, b[v], h[v], t[v]);
+      if (modeled)  // lanes 8 lt, 8 lt + 1 hold chunk lt's 8 modeled coordinates
+        *reinterpret_cast<unsigned short*>(rec + 4 * (lane / 8) + 2 * (lane % 8)) = (unsigned short)nib;
+      store_stream<E, 1>(rec + 16, sgnbit);
+    } else {
+      unsigned char* f = C.fieldp(tqi::R_V_CODES, b[v], h[v], t[v]);
+      if (modeled)  // lane 4 g holds group g's 4 modeled coordinates
+        *reinterpret_cast<unsigned short*>(f + grouped_byte(2 * (lane / 4), pos, 1)) = (unsigned short)nib;
+      store_stream_grouped<E, 1>(f + tqi::kTileTokens * 16, pos, sgnbit);
+    }
+    if (lane == 0) *reinterpret_cast<float*>(C.ptr(side ? tqi::R_V_NORM : tqi::R_K_NORM, b[v], h[v], t[v])) = nu[v];
+  }
+}
+
 // One vector (see encode_vectors).
 template <int D, typename Tin>
 __device__ __forceinline__ void encode_vector(const AppendParams& p, int side, int b, int h, int j, int t,
@@ -431,6 +521,12 @@ __device__ __forceinline__ void append_body(const AppendParams& p, float* st_sme
   for (int v = 0; v < NV; ++v) {
     ok[v] = v0 + v < per_side;
     split_vec(p, ok[v] ? v0 + v : v0, b[v], h[v], j[v], t[v]);
+  }
+  if constexpr (D == 128) {
+    if (p.rotate[side] == 2) {
+      encode_vectors_sq<Tin, NV>(p, side, b, h, j, t, ok);
+      return;
+    }
   }
   float res[NV][E];
   encode_vectors<D, Tin, NV>(p, side, b, h, j, t, ok, res);
@@ -634,6 +730,20 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
   }
 }
 
+// SQU-KV tables in storage order: E_st[h][i][c] = E[h][i][rank(c)], its transpose, and
+// s_st[h][c] = s[h][rank(c)] (a permutation: no value changes).
+__global__ void __launch_bounds__(256) spectral_basis_kernel(const float* E, const float* sv, float* E_st,
+                                                             float* ET_st, float* s_st, int side, int H, int D) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)H * D * D) return;
+  const int c = (int)(idx % D), i = (int)((idx / D) % D), h = (int)(idx / ((long long)D * D));
+  const int r = sq_rank_of_coord(side, c);
+  const float e = E[((long long)h * D + i) * D + r];
+  E_st[((long long)h * D + i) * D + c] = e;
+  ET_st[((long long)h * D + c) * D + i] = e;
+  if (i == 0) s_st[(long long)h * D + c] = sv[(long long)h * D + r];
+}
+
 // R_K U for every column of every KV head's basis: U [H][d][r] -> U_rot [H][d][r].
 template <int D>
 __global__ void __launch_bounds__(256) rotate_basis_kernel(const float* U, float* U_rot,
@@ -681,6 +791,45 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const DequantParams p) 
   const unsigned char* codes = side ? C.fieldp(tqi::R_V_CODES, p.b, p.kvh, t) : C.ptr(tqi::R_K_CODES, p.b, p.kvh, t);
   const int second = side ? tqi::kTileTokens * (D / 4) : D / 4;  // start of a 3-bit code's 1-bit stream
   const float* cent = side ? p.tab.v_c : p.tab.k_c;
+  if (p.rotate[side] == 2) {
+    if constexpr (D == 128) {
+      // SQU-KV: z_hat_c = +-M[m] (modeled) or +-c1 (floor), x_hat = nu E (s z_hat)
+      const bool modeled = sq_modeled(side, E * lane);
+      uint32_t sg[E];
+      load_stream<E, 1>(codes + (side ? tqi::kTileTokens * 16 : 16), sg, pos);
+      uint32_t mag = 0;
+      if (modeled) {
+        const int byte = side ? 2 * (lane / 4) : 4 * (lane / 8) + 2 * (lane % 8);
+        const unsigned char* mp = side ? codes + grouped_byte((unsigned)byte, (unsigned)pos, 1) : codes + byte;
+        mag = mp[0] | ((uint32_t)mp[side ? 1 : 1] << 8);
+      }
+      const float c1 = __ldg(p.tab.sq_c1 + side);
+      const float nu = *reinterpret_cast<const float*>(C.ptr(side ? tqi::R_V_NORM : tqi::R_K_NORM, p.b, p.kvh, t));
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.sq_s[side] + (long long)p.kvh * D + lane * E));
+      const float sc[E] = {s4.x, s4.y, s4.z, s4.w};
+      float a[E];
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const float mg = modeled ? __ldg(cent + 8 + ((mag >> (4 * i)) & 7u)) : c1;
+        a[i] = nu * sc[i] * (sg[i] ? mg : -mg);
+      }
+      float o[E] = {0.f, 0.f, 0.f, 0.f};
+      const float* ET = p.tab.sq_ET[side] + (long long)p.kvh * D * D + lane * E;
+      for (int sl = 0; sl < 32; ++sl) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float ac = __shfl_sync(kFull, a[e], sl);
+          const float4 er = __ldg(reinterpret_cast<const float4*>(ET + (E * sl + e) * D));
+          o[0] = fmaf(er.x, ac, o[0]); o[1] = fmaf(er.y, ac, o[1]);
+          o[2] = fmaf(er.z, ac, o[2]); o[3] = fmaf(er.w, ac, o[3]);
+        }
+      }
+      float* out = p.out[side] + (long long)(t - p.t0) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) out[e] = o[e];
+    }
+    return;
+  }
   const uint32_t halfL = 1u << (bits - 1);
   uint32_t sym[E], sgn[E];
   if (bits == 4) {
@@ -876,6 +1025,17 @@ tq_status launch_append_paged(const tq_context* ctx, void* pool, const tq_page_t
                               int32_t* dev_error, Stream stream) {
   const PagedAppend pg{pt, dev_start, dev_error};
   return append_impl(ctx, pool, k, v, dtype, n_new, nullptr, &pg, stream);
+}
+
+tq_status launch_spectral_basis(const tq_context* ctx, int side, const float* E, const float* sv, Stream stream) {
+  using namespace tqd;
+  const Tables t = make_tables(ctx);
+  const int H = ctx->cfg.num_kv_heads, D = ctx->cfg.head_dim;
+  const long long n = (long long)H * D * D;
+  spectral_basis_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+      E, sv, const_cast<float*>(t.sq_E[side]), const_cast<float*>(t.sq_ET[side]), const_cast<float*>(t.sq_s[side]),
+      side, H, D);
+  return launch_status("spectral_basis");
 }
 
 tq_status launch_rotate_basis(const tq_context* ctx, const float* U, Stream stream) {

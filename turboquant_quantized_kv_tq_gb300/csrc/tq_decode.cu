@@ -181,13 +181,32 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   }
   float x[E];
   load_row<E>(p.q + qrow * D + lane * E, x);
+  if (p.k_rotate == 2) {
+    // SQU-KV keys: q_c = s_c sum_i E[i][c] q_i (the basis and scales of KV head kvh), so that
+    // <q_c, z_hat_c> summed over stored coordinates is q^T E (s z_hat)
+    float y[E];
 #pragma unroll
-  for (int i = 0; i < E; ++i) x[i] *= __ldg(p.tab.k_sign + lane * E + i);
-  if (p.k_rotate) {
-    wht_warp<E>(x);
-    const float rs = 1.f / sqrtf((float)D);
+    for (int i = 0; i < E; ++i) y[i] = 0.f;
+    const float* Eh = p.tab.sq_E[0] + (long long)kvh * D * D + lane * E;
+    for (int sl = 0; sl < 32; ++sl) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) x[i] *= rs;
+      for (int e = 0; e < E; ++e) {
+        const float qi = __shfl_sync(kFull, x[e], sl);
+#pragma unroll
+        for (int i = 0; i < E; ++i) y[i] = fmaf(__ldg(Eh + (E * sl + e) * D + i), qi, y[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = y[i] * __ldg(p.tab.sq_s[0] + (long long)kvh * D + lane * E + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] *= __ldg(p.tab.k_sign + lane * E + i);
+    if (p.k_rotate) {
+      wht_warp<E>(x);
+      const float rs = 1.f / sqrtf((float)D);
+#pragma unroll
+      for (int i = 0; i < E; ++i) x[i] *= rs;
+    }
   }
   // hi term to column c, lo term (x - hi) to column Gc + c or to the separate lo array
   const long long col = ((long long)b * p.Hkv + kvh) * kQCols + c;
@@ -253,8 +272,10 @@ size_t decode_workspace_bytes(const tq_context* ctx, int max_seq) {
 static bool dispatch_decode(const tq_context* ctx, const tqd::DecodeParams& p, dim3 grid,
                             cudaStream_t s, cudaError_t* e) {
   using namespace tqd;
-  const int kb = ctx->cfg.k.bits, kq = ctx->cfg.k.qjl, kh = ctx->cfg.headq_rank ? 1 : 0;
-  const int vb = ctx->cfg.v.bits, vq = ctx->cfg.v.qjl;
+  // code-width tag of the decode templates: kSQ for a spectral (SQU-KV) side
+  const int kb = ctx->cfg.k.rotate == 2 ? kSQ : ctx->cfg.k.bits, kq = ctx->cfg.k.qjl;
+  const int kh = ctx->cfg.headq_rank ? 1 : 0;
+  const int vb = ctx->cfg.v.rotate == 2 ? kSQ : ctx->cfg.v.bits, vq = ctx->cfg.v.qjl;
   if (ctx->cfg.head_dim != kDecD) {
     if (kq || kh) return false;
     switch (ctx->cfg.head_dim) {
@@ -269,6 +290,7 @@ static bool dispatch_decode(const tq_context* ctx, const tqd::DecodeParams& p, d
     case 2: return dispatch_decode_k2(kq, kh, vb, vq, p, grid, s, e);
     case 3: return dispatch_decode_k3(kq, kh, vb, vq, p, grid, s, e);
     case 4: return dispatch_decode_k4(kq, kh, vb, vq, p, grid, s, e);
+    case kSQ: return dispatch_decode_ksq(kq, kh, vb, vq, p, grid, s, e);
   }
   return false;
 }

@@ -37,6 +37,7 @@
 namespace tqd {
 
 constexpr int kDecD = 128;
+constexpr int kSQ = 5;  // code-width tag of a spectral (SQU-KV) side in the decode templates
 constexpr int kLogitsWarps = 8;
 // Warps per decode block: 16 (4 per scheduler) when the per-thread state fits in 128 registers;
 // the QJL variants carry 16-32 more accumulator / fragment registers and use 12.
@@ -95,7 +96,7 @@ struct DecodeParams {
 };
 
 template <int B>
-struct LutEntries { static constexpr int value = B == 4 ? 256 : (B == 1 ? 0 : 16); };
+struct LutEntries { static constexpr int value = (B == 4 || B == kSQ) ? 256 : (B == 1 ? 0 : 16); };
 
 // Lane-replicated pair table for a b-bit codebook (sign-magnitude symbols).
 template <int B>
@@ -108,6 +109,9 @@ __device__ __forceinline__ void build_lut(unsigned char* lut, const float* cent)
       const int a = e & 15, c = e >> 4;
       lo = (a & 8 ? 1.f : -1.f) * __ldg(cent + 8 + (a & 7));
       hi = (c & 8 ? 1.f : -1.f) * __ldg(cent + 8 + (c & 7));
+    } else if constexpr (B == kSQ) {  // magnitudes of the 4-bit codebook, two 3-bit fields
+      lo = __ldg(cent + 8 + (e & 7));
+      hi = __ldg(cent + 8 + ((e >> 4) & 7));
     } else if constexpr (B == 3) {  // magnitudes only
       lo = __ldg(cent + 4 + (e & 3));
       hi = __ldg(cent + 4 + (e >> 2));
@@ -193,6 +197,19 @@ struct KChunk<1> {
   __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
   __device__ __forceinline__ uint32_t pair(uint32_t, uint32_t m0, int p) const {
     return signed_pair(m0, s << (15 - p));
+  }
+};
+
+// SQU-KV key chunk: the chunk's first 8 coordinates are modeled (4-bit magnitudes in mg, byte p
+// = coordinates 2p, 2p + 1), the other 24 the 1-bit floor (magnitude m0 = the 1-bit centroid);
+// s holds the 32 signs.
+template <>
+struct KChunk<kSQ> {
+  uint32_t mg;
+  uint32_t s;
+  __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
+  __device__ __forceinline__ uint32_t pair(uint32_t lx, uint32_t m0, int p) const {
+    return signed_pair(p < 4 ? lut_get(lx, mg, p) : m0, s << (15 - p));
   }
 };
 
@@ -308,6 +325,36 @@ struct VChunk<1> {
   }
 };
 
+// SQU-KV value chunk: dims 16 lg .. 16 lg + 3 of the group are modeled.  m[0] holds the 4-bit
+// magnitudes of those dims for tokens 0 (low half) and 1, m[1] for tokens 2 and 3; s the signs.
+// e01 / e23: byte d = magnitude of dim d of the first token | that of the second << 4.
+__device__ __forceinline__ uint32_t nibbles_to_bytes(uint32_t x16) {
+  x16 = (x16 | (x16 << 8)) & 0x00FF00FFu;
+  return (x16 | (x16 << 4)) & 0x0F0F0F0Fu;
+}
+template <>
+struct VChunk<kSQ> {
+  uint32_t m[2], s[2];
+  uint32_t e01, e23;
+  Bits16 sg;
+  __device__ __forceinline__ void prepare() {
+    e01 = nibbles_to_bytes(m[0] & 0xffffu) | (nibbles_to_bytes(m[0] >> 16) << 4);
+    e23 = nibbles_to_bytes(m[1] & 0xffffu) | (nibbles_to_bytes(m[1] >> 16) << 4);
+    sg.build(s);
+  }
+  __device__ __forceinline__ void frag(uint32_t lx, uint32_t m0, int mt, uint32_t (&a)[4]) const {
+    if (mt < 2) {
+      a[0] = lut_get(lx, e01, 2 * mt);
+      a[1] = lut_get(lx, e01, 2 * mt + 1);
+      a[2] = lut_get(lx, e23, 2 * mt);
+      a[3] = lut_get(lx, e23, 2 * mt + 1);
+    } else {
+      a[0] = a[1] = a[2] = a[3] = m0;
+    }
+    sg.apply(mt, a);
+  }
+};
+
 // QJL value signs: +-1 pairs.
 struct VSign {
   uint32_t s[2];
@@ -361,7 +408,7 @@ struct SlabPtrs {
   }
 };
 
-template <int KB, int D = kDecD> struct KRec { static constexpr int value = D * KB / 8; };
+template <int KB, int D = kDecD> struct KRec { static constexpr int value = KB == kSQ ? D / 4 : D * KB / 8; };
 
 // Shared-memory stage of one 16-token tile: the tile's K block then its V block, in the cache's
 // block layout for head dim D (QJL rows m = D; field offsets are multiples of 16 bytes).
@@ -426,7 +473,12 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
   const unsigned char* rb = st + S::KC + rB * KR;
   const unsigned char* ka = ra + sl * (KB == 3 ? 32 : 16 * KB);
   const unsigned char* kb = rb + sl * (KB == 3 ? 32 : 16 * KB);
-  if constexpr (KB == 4) {
+  if constexpr (KB == kSQ) {  // magnitudes (16 bytes) then signs (16 bytes), chunk lt = 4 bytes each
+    d.kA.mg = *reinterpret_cast<const uint32_t*>(ra + 4 * lt);
+    d.kB.mg = *reinterpret_cast<const uint32_t*>(rb + 4 * lt);
+    d.kA.s = *reinterpret_cast<const uint32_t*>(ra + 16 + 4 * lt);
+    d.kB.s = *reinterpret_cast<const uint32_t*>(rb + 16 + 4 * lt);
+  } else if constexpr (KB == 4) {
     d.kA.c = *reinterpret_cast<const uint4*>(ka + 16 * lt);
     d.kB.c = *reinterpret_cast<const uint4*>(kb + 16 * lt);
   } else if constexpr (KB == 3 || KB == 2) {
@@ -460,7 +512,12 @@ __device__ __forceinline__ void read_stage(TileData<KB, KQ, KH, VB, VQ>& d, cons
   // tokens 4 lt .. 4 lt + 3 of this thread's group g are contiguous in every stream
   const int g = 8 * sl + lg;
   const unsigned char* vc = vst + S::VC;
-  if constexpr (VB == 4) {
+  if constexpr (VB == kSQ) {  // magnitude stream, then sign stream (16 records each), 2 bytes per group
+    const uint2 m2 = *reinterpret_cast<const uint2*>(vc + g * 32 + 8 * lt);
+    const uint2 s2 = *reinterpret_cast<const uint2*>(vc + kTile * 16 + g * 32 + 8 * lt);
+    d.v.m[0] = m2.x; d.v.m[1] = m2.y;
+    d.v.s[0] = s2.x; d.v.s[1] = s2.y;
+  } else if constexpr (VB == 4) {
     // 32 bytes; threads of odd groups load the two halves in the other order, so the eight
     // 16-byte loads of a quarter warp fall on distinct banks
     const unsigned char* a = vc + g * 128 + 32 * lt;
@@ -816,8 +873,11 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
   unsigned char* const win = smem - sbase;
   if constexpr (KB != 1) build_lut<KB>(win + kLutAddrK, p.tab.k_c);
   if constexpr (SM::sepV && VB != 1) build_lut<VB>(win + kLutAddrV, p.tab.v_c);
-  const uint32_t k_m0 = pack_half2(__ldg(p.tab.k_c + 1), __ldg(p.tab.k_c + 1));
-  const uint32_t v_m0 = pack_half2(__ldg(p.tab.v_c + 1), __ldg(p.tab.v_c + 1));
+  // the 1-bit magnitude: a 1-bit codebook's upper centroid, or a spectral side's floor centroid
+  const float kc1 = KB == kSQ ? __ldg(p.tab.sq_c1) : __ldg(p.tab.k_c + 1);
+  const float vc1 = VB == kSQ ? __ldg(p.tab.sq_c1 + 1) : __ldg(p.tab.v_c + 1);
+  const uint32_t k_m0 = pack_half2(kc1, kc1);
+  const uint32_t v_m0 = pack_half2(vc1, vc1);
   const uint32_t lxK = kLutAddrK | (4u * lane);
   const uint32_t lxV = (SM::sepV ? kLutAddrV : kLutAddrK) | (4u * lane);
   const uint32_t my_bars = SM::bars + warp * kPairStages * 8;
@@ -1090,7 +1150,24 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
           for (int i = 0; i < 4; ++i) o[i] = fmaf(p.qjl_scale, corr[i], o[i]);
         }
         const float invL = L2 > 0.f ? 1.f / L2 : 0.f;
-        if (p.v_rotate) {
+        if (p.v_rotate == 2) {
+          // SQU-KV values: o = E (s acc) / l with the basis and scales of KV head kvh
+          const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.sq_s[1] + (long long)kvh * kDecD + 4 * lane));
+          const float a[4] = {o[0] * s4.x, o[1] * s4.y, o[2] * s4.z, o[3] * s4.w};
+          float r[4] = {0.f, 0.f, 0.f, 0.f};
+          const float* ET = p.tab.sq_ET[1] + (long long)kvh * kDecD * kDecD + 4 * lane;
+          for (int sl = 0; sl < 32; ++sl) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float ac = __shfl_sync(kFull, a[e], sl);
+              const float4 er = __ldg(reinterpret_cast<const float4*>(ET + (4 * sl + e) * kDecD));
+              r[0] = fmaf(er.x, ac, r[0]); r[1] = fmaf(er.y, ac, r[1]);
+              r[2] = fmaf(er.z, ac, r[2]); r[3] = fmaf(er.w, ac, r[3]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = r[i] * invL;
+        } else if (p.v_rotate) {
           wht_warp<4>(o);
           const float rs = 1.f / sqrtf((float)kDecD);
 #pragma unroll
@@ -1297,6 +1374,7 @@ bool dispatch_decode_k1(int kq, int kh, int vb, int vq, const DecodeParams& p, d
 bool dispatch_decode_k2(int kq, int kh, int vb, int vq, const DecodeParams& p, dim3 g, cudaStream_t s, cudaError_t* e);
 bool dispatch_decode_k3(int kq, int kh, int vb, int vq, const DecodeParams& p, dim3 g, cudaStream_t s, cudaError_t* e);
 bool dispatch_decode_k4(int kq, int kh, int vb, int vq, const DecodeParams& p, dim3 g, cudaStream_t s, cudaError_t* e);
+bool dispatch_decode_ksq(int kq, int kh, int vb, int vq, const DecodeParams& p, dim3 g, cudaStream_t s, cudaError_t* e);
 bool dispatch_logits_k1(int kq, int kh, const LogitsParams& p, dim3 g, cudaStream_t s, cudaError_t* e);
 bool dispatch_logits_k2(int kq, int kh, const LogitsParams& p, dim3 g, cudaStream_t s, cudaError_t* e);
 bool dispatch_logits_k3(int kq, int kh, const LogitsParams& p, dim3 g, cudaStream_t s, cudaError_t* e);

@@ -27,6 +27,10 @@ struct Tables {
   const float* S_V_T;
   const float* U_rot; // [H_kv][d][r], R_K U
   const float* S_V_R; // [m][d], S_V R_V (head dim > 128 with a QJL value side)
+  const float* sq_c1;     // [2]: 1-bit centroid of each side (spectral sides' floor)
+  const float* sq_E[2];   // spectral side: [H_kv][d][d] basis, column c = stored coordinate c
+  const float* sq_ET[2];  // its transpose
+  const float* sq_s[2];   // [H_kv][d] coordinate scales, storage order
 };
 
 // The packed cache in 16-token blocks: field r of token t of slab s = b * H + h at
@@ -76,6 +80,23 @@ struct Cache {
   }
 };
 
+// SQU-KV storage order (head dim 128): the eigen-rank held by stored coordinate c of a side.
+// Keys: the first 8 coordinates of each 32-coordinate chunk hold ranks 0..31 (rank 4 r + chunk);
+// values: the first 4 of each 16-coordinate group (rank 8 r + group); the others hold ranks
+// 32.. in increasing coordinate order.
+__host__ __device__ __forceinline__ int sq_rank_of_coord(int side, int c) {
+  if (side == 0) {
+    const int lt = c / 32, r = c % 32;
+    return r < 8 ? 4 * r + lt : 32 + 24 * lt + (r - 8);
+  }
+  const int g = c / 16, r = c % 16;
+  return r < 4 ? 8 * r + g : 32 + 12 * g + (r - 4);
+}
+// whether stored coordinate c of a side is modeled (4 bits) rather than floor (1 bit)
+__host__ __device__ __forceinline__ bool sq_modeled(int side, int c) {
+  return side == 0 ? (c % 32) < 8 : (c % 16) < 4;
+}
+
 // Value-side streams (V codes, each stream of a 3-bit code on its own, V QJL signs) are stored
 // by groups of 16 coordinates: [groups][16 tokens][2W bytes] for a W-bit stream, so byte j of
 // the record of block position pos is at grouped_byte(j, pos, W) from the stream's start.
@@ -99,6 +120,13 @@ inline Tables make_tables(const tq_context* ctx) {
   t.S_V_T = ctx->cfg.v.qjl ? (const float*)(b + ctx->tab.s_v_t) : nullptr;
   t.U_rot = ctx->cfg.headq_rank ? (const float*)(b + ctx->tab.headq_u) : nullptr;
   t.S_V_R = ctx->tab.s_v_r ? (const float*)(b + ctx->tab.s_v_r) : nullptr;
+  t.sq_c1 = (const float*)(b + ctx->tab.sq_c1);
+  for (int side = 0; side < 2; ++side) {
+    const bool sq = ctx->tab.sq_e[side] != 0;
+    t.sq_E[side] = sq ? (const float*)(b + ctx->tab.sq_e[side]) : nullptr;
+    t.sq_ET[side] = sq ? (const float*)(b + ctx->tab.sq_et[side]) : nullptr;
+    t.sq_s[side] = sq ? (const float*)(b + ctx->tab.sq_s[side]) : nullptr;
+  }
   return t;
 }
 

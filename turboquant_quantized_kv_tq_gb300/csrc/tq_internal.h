@@ -22,9 +22,11 @@ enum RegionId {
 // Byte offsets of the arrays inside the table blob (see tq_tables_host in tq.h).
 struct TableOffsets {
   size_t k_centroids, k_thresholds, v_centroids, v_thresholds;
-  size_t k_signs, v_signs, s_k, s_k_t, s_v, s_v_t, headq_u, s_v_r, total;
+  size_t k_signs, v_signs, s_k, s_k_t, s_v, s_v_t, headq_u, s_v_r;
+  size_t sq_c1;                          // fp32 [2]: 1-bit centroid of each spectral side
+  size_t sq_e[2], sq_et[2], sq_s[2];     // spectral side: E, E^T [H_kv][d][d], s [H_kv][d] (storage order)
+  size_t total;
 };
-
 // 16-token block layout: field r of token t of slab s at
 // side_off[side(r)] + (s * tiles_per_slab + t / 16) * block[side(r)] + off[r] + (t % 16) * rec[r].
 struct Layout {
@@ -60,6 +62,7 @@ struct tq_context {
   std::vector<unsigned char> host_tables;
   void* dev_tables = nullptr;
   bool basis_set = false;
+  bool sq_set[2] = {false, false};  // spectral sides: basis stored
 };
 
 // Launchers (tq_append.cu, tq_decode.cu).  They assume validated arguments.
@@ -71,6 +74,7 @@ tq_status launch_append_paged(const tq_context* ctx, void* pool, const tq_page_t
                               const void* v, tq_dtype dtype, int n_new, const int32_t* dev_start,
                               int32_t* dev_error, Stream stream);
 tq_status launch_rotate_basis(const tq_context* ctx, const float* U, Stream stream);
+tq_status launch_spectral_basis(const tq_context* ctx, int side, const float* E, const float* s, Stream stream);
 tq_status launch_dequantize(const tq_context* ctx, const void* cache, int b, int kvh, int t0,
                             int t1, float* k_out, float* v_out, Stream stream);
 size_t decode_workspace_bytes(const tq_context* ctx, int max_seq);

@@ -34,6 +34,10 @@ CONFIGS = {
                  schemes=[("kqv", 2), ("kqv", 3), ("kqv", 4)], append_chunk=4096),
     "cfg5": dict(B=16, Hq=32, Hkv=8, d=128, T=16384, dtype="bf16", seed=4,
                  schemes=[("headq", 2)], headq_rank=16, calib=4096),
+    # SQU-KV regime: structured (rank-16) keys and values per KV head, with separate calibration
+    # sets for K and V ([ABL] "Recomendações Práticas" 2); the headline shape at T = 8192
+    "sq": dict(B=8, Hq=32, Hkv=8, d=128, T=8192, dtype="bf16", seed=5,
+               schemes=[("squ", 2), ("tq", 2)], calib=4096),
 }
 
 
@@ -130,6 +134,28 @@ def make_inputs(name, B=None, T=None, Hkv=None, Hq=None, d=None, seed=None):
                 V[b, h] = conv(sv[h] * rng.standard_normal((T, d)))
         q = rng.standard_normal((B, Hq, d)).astype(np.float32)
         extra.update(k_std=sk, v_std=sv)
+    elif name == "sq":
+        # per KV head: K = z U_K^T + eps, V = w U_V^T + eps (rank 16, eps variance 0.01),
+        # queries in the key subspace; 4096 calibration vectors per head and side, fresh draws
+        UK = np.stack([_orthonormal(rng, d, 16) for _ in range(Hkv)])
+        UV = np.stack([_orthonormal(rng, d, 16) for _ in range(Hkv)])
+        for b in range(B):
+            for h in range(Hkv):
+                K[b, h] = conv(rng.standard_normal((T, 16)) @ UK[h].T + 0.1 * rng.standard_normal((T, d)))
+        for b in range(B):
+            for h in range(Hkv):
+                V[b, h] = conv(rng.standard_normal((T, 16)) @ UV[h].T + 0.1 * rng.standard_normal((T, d)))
+        G = Hq // Hkv
+        q = np.empty((B, Hq, d), dtype=np.float32)
+        for b in range(B):
+            for h in range(Hq):
+                q[b, h] = UK[h // G] @ rng.standard_normal(16) + 0.1 * rng.standard_normal(d)
+        n_cal = c["calib"]
+        calib_k = np.stack([rng.standard_normal((n_cal, 16)) @ UK[h].T + 0.1 * rng.standard_normal((n_cal, d))
+                            for h in range(Hkv)])
+        calib_v = np.stack([rng.standard_normal((n_cal, 16)) @ UV[h].T + 0.1 * rng.standard_normal((n_cal, d))
+                            for h in range(Hkv)])
+        extra.update(UK=UK, UV=UV, calib_k=calib_k, calib_v=calib_v)
     elif name == "cfg5":
         for b in range(B):
             for h in range(Hkv):
