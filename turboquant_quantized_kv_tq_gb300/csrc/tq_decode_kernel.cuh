@@ -1150,7 +1150,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
           for (int i = 0; i < 4; ++i) o[i] = fmaf(p.qjl_scale, corr[i], o[i]);
         }
         const float invL = L2 > 0.f ? 1.f / L2 : 0.f;
-        if (p.v_rotate == 2) {
+        if constexpr (VB == kSQ) {
           // SQU-KV values: o = E (s acc) / l with the basis and scales of KV head kvh
           const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.tab.sq_s[1] + (long long)kvh * kDecD + 4 * lane));
           const float a[4] = {o[0] * s4.x, o[1] * s4.y, o[2] * s4.z, o[3] * s4.w};

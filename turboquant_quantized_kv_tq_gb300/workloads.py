@@ -35,8 +35,8 @@ CONFIGS = {
     "cfg5": dict(B=16, Hq=32, Hkv=8, d=128, T=16384, dtype="bf16", seed=4,
                  schemes=[("headq", 2)], headq_rank=16, calib=4096),
     # SQU-KV regime: structured (rank-16) keys and values per KV head, with separate calibration
-    # sets for K and V ([ABL] "Recomendações Práticas" 2); the headline shape at T = 8192
-    "sq": dict(B=8, Hq=32, Hkv=8, d=128, T=8192, dtype="bf16", seed=5,
+    # sets for K and V ([ABL] "Recomendações Práticas" 2), at the headline shape
+    "sq": dict(B=8, Hq=32, Hkv=8, d=128, T=32768, dtype="bf16", seed=5,
                schemes=[("squ", 2), ("tq", 2)], calib=4096),
 }
 
