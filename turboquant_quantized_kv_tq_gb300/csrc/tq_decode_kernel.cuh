@@ -96,7 +96,7 @@ struct DecodeParams {
 };
 
 template <int B>
-struct LutEntries { static constexpr int value = (B == 4 || B == kSQ) ? 256 : (B == 1 ? 0 : 16); };
+struct LutEntries { static constexpr int value = (B == 4 || B == kSQ) ? 256 : B == 3 ? 64 : (B == 1 ? 0 : 16); };
 
 // Lane-replicated pair table for a b-bit codebook (sign-magnitude symbols).
 template <int B>
@@ -112,9 +112,9 @@ __device__ __forceinline__ void build_lut(unsigned char* lut, const float* cent)
     } else if constexpr (B == kSQ) {  // magnitudes of the 4-bit codebook, two 3-bit fields
       lo = __ldg(cent + 8 + (e & 7));
       hi = __ldg(cent + 8 + ((e >> 4) & 7));
-    } else if constexpr (B == 3) {  // magnitudes only
-      lo = __ldg(cent + 4 + (e & 3));
-      hi = __ldg(cent + 4 + (e >> 2));
+    } else if constexpr (B == 3) {  // magnitudes in bits 0-1 / 2-3, their signs in bits 4 / 5
+      lo = (e & 16 ? 1.f : -1.f) * __ldg(cent + 4 + (e & 3));
+      hi = (e & 32 ? 1.f : -1.f) * __ldg(cent + 4 + ((e >> 2) & 3));
     } else {  // B == 2: field (s << 1) | k
       const int a = e & 3, c = e >> 2;
       lo = (a & 2 ? 1.f : -1.f) * __ldg(cent + 2 + (a & 1));
@@ -143,6 +143,34 @@ __device__ __forceinline__ uint32_t signed_pair(uint32_t mag, uint32_t xsh) {
   return mag | (~xsh & 0x80008000u);
 }
 
+// Byte j of the result = nibble j of x (low half) | nibble 4 + j of x << 4.
+__device__ __forceinline__ uint32_t nibble_pairs(uint32_t x) {
+  x = __byte_perm(x, 0, 0x3120);  // nibbles 0 1 4 5 2 3 6 7
+  const uint32_t t = (x ^ (x >> 4)) & 0x00F000F0u;
+  return x ^ t ^ (t << 4);
+}
+
+// Outer perfect shuffle: bit i of the low half -> bit 2 i, bit i of the high half -> 2 i + 1.
+__device__ __forceinline__ uint32_t shuffle_halves(uint32_t x) {
+  uint32_t t;
+  x = __byte_perm(x, 0, 0x3120);
+  t = (x ^ (x >> 4)) & 0x00F000F0u; x ^= t ^ (t << 4);
+  t = (x ^ (x >> 2)) & 0x0C0C0C0Cu; x ^= t ^ (t << 2);
+  t = (x ^ (x >> 1)) & 0x22222222u; x ^= t ^ (t << 1);
+  return x;
+}
+
+// Sign bits of 16 coordinate pairs (bit 2 p, 2 p + 1 of s for pair p) as two words in which pair
+// p's bits sit at 2 (p & 7) and 2 (p & 7) + 16: lo for p < 8, hi for p >= 8.
+struct PairSigns {
+  uint32_t lo, hi;
+  __device__ __forceinline__ void build(uint32_t s) {
+    lo = __byte_perm(s, s << 15, 0x7610);
+    hi = __byte_perm(s, s >> 1, 0x7632);
+  }
+  __device__ __forceinline__ uint32_t at(int p) const { return (p < 8 ? lo : hi) << (15 - 2 * (p & 7)); }
+};
+
 // Nibbles 0,2,4,6 / 1,3,5,7 of w, one per byte.
 __device__ __forceinline__ uint32_t nib_even(uint32_t w) { return w & 0x0F0F0F0Fu; }
 __device__ __forceinline__ uint32_t nib_odd(uint32_t w) { return (w >> 4) & 0x0F0F0F0Fu; }
@@ -163,18 +191,25 @@ struct KChunk<4> {
   }
 };
 
+// 3-bit keys: the magnitude nibble of a pair (two 2-bit fields) and its two sign bits form one
+// 6-bit table index, so a signed pair is one lookup.  With t = nibble_pairs(s), byte j of t holds
+// the signs of coordinates 4j .. 4j + 3 (bits 0-3) and 16 + 4j .. 16 + 4j + 3 (bits 4-7), so one
+// shift per index word brings a pair's two signs to bits 4 and 5 of its byte.
 template <>
 struct KChunk<3> {
   uint2 k;
   uint32_t s;
   uint32_t xe, xo, ye, yo;
   __device__ __forceinline__ void prepare() {
-    xe = nib_even(k.x); xo = nib_odd(k.x); ye = nib_even(k.y); yo = nib_odd(k.y);
-    s = unshuffle_bits(s);
+    const uint32_t t = nibble_pairs(s);
+    xe = nib_even(k.x) | ((t << 4) & 0x30303030u);
+    xo = nib_odd(k.x) | ((t << 2) & 0x30303030u);
+    ye = nib_even(k.y) | (t & 0x30303030u);
+    yo = nib_odd(k.y) | ((t >> 2) & 0x30303030u);
   }
   __device__ __forceinline__ uint32_t pair(uint32_t lx, uint32_t, int p) const {
     const uint32_t w = p < 8 ? (p & 1 ? xo : xe) : (p & 1 ? yo : ye);
-    return signed_pair(lut_get(lx, w, (p & 7) >> 1), s << (15 - p));
+    return lut_get(lx, w, (p & 7) >> 1);
   }
 };
 
@@ -194,9 +229,10 @@ struct KChunk<2> {
 template <>
 struct KChunk<1> {
   uint32_t s;
-  __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
+  PairSigns ps;
+  __device__ __forceinline__ void prepare() { ps.build(s); }
   __device__ __forceinline__ uint32_t pair(uint32_t, uint32_t m0, int p) const {
-    return signed_pair(m0, s << (15 - p));
+    return signed_pair(m0, ps.at(p));
   }
 };
 
@@ -207,17 +243,19 @@ template <>
 struct KChunk<kSQ> {
   uint32_t mg;
   uint32_t s;
-  __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
+  PairSigns ps;
+  __device__ __forceinline__ void prepare() { ps.build(s); }
   __device__ __forceinline__ uint32_t pair(uint32_t lx, uint32_t m0, int p) const {
-    return signed_pair(p < 4 ? lut_get(lx, mg, p) : m0, s << (15 - p));
+    return signed_pair(p < 4 ? lut_get(lx, mg, p) : m0, ps.at(p));
   }
 };
 
 // Sign chunk of a QJL key: 32 bits per token, as +-1 pairs.
 struct KSign {
   uint32_t s;
-  __device__ __forceinline__ void prepare() { s = unshuffle_bits(s); }
-  __device__ __forceinline__ uint32_t pair(int p) const { return signed_pair(0x3C003C00u, s << (15 - p)); }
+  PairSigns ps;
+  __device__ __forceinline__ void prepare() { ps.build(s); }
+  __device__ __forceinline__ uint32_t pair(int p) const { return signed_pair(0x3C003C00u, ps.at(p)); }
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -290,16 +328,28 @@ struct Bits16 {
   }
 };
 
+// 3-bit values: as on the key side the two sign bits join the magnitude nibble in the table
+// index.  After shuffle_halves, byte j of a sign word holds dims 4 j .. 4 j + 3 of the two tokens
+// interleaved (token 0 at even bits), so one shift per index word places them at bits 4 and 5.
 template <>
 struct VChunk<3> {
   uint32_t k[4], s[2];
   Pair2 m;
-  Bits16 sg;
-  __device__ __forceinline__ void prepare() { m.build(k); sg.build(s); }
+  __device__ __forceinline__ static void fold(uint32_t x, uint32_t (&e)[2], uint32_t (&o)[2]) {
+    x = shuffle_halves(x);
+    e[0] |= (x << 4) & 0x30303030u;
+    o[0] |= (x << 2) & 0x30303030u;
+    e[1] |= x & 0x30303030u;
+    o[1] |= (x >> 2) & 0x30303030u;
+  }
+  __device__ __forceinline__ void prepare() {
+    m.build(k);
+    fold(s[0], m.e01, m.o01);
+    fold(s[1], m.e23, m.o23);
+  }
   __device__ __forceinline__ void frag(uint32_t lx, uint32_t, int mt,
                                        uint32_t (&a)[4]) const {
     m.mags(lx, mt, a);
-    sg.apply(mt, a);
   }
 };
 

@@ -324,14 +324,4 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// Bits of a 32-bit word rearranged: even bits to the low half, odd bits to the high half.
-__device__ __forceinline__ uint32_t unshuffle_bits(uint32_t x) {
-  uint32_t t;
-  t = (x ^ (x >> 1)) & 0x22222222u; x ^= t ^ (t << 1);
-  t = (x ^ (x >> 2)) & 0x0C0C0C0Cu; x ^= t ^ (t << 2);
-  t = (x ^ (x >> 4)) & 0x00F000F0u; x ^= t ^ (t << 4);
-  t = (x ^ (x >> 8)) & 0x0000FF00u; x ^= t ^ (t << 8);
-  return x;
-}
-
 }  // namespace tqd
