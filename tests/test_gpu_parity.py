@@ -206,6 +206,7 @@ def _multi_queries(inp, nq, seed):
     ("kqv", 4, 8, 2, 2, [200, 17]),
     ("qkqv", 4, 8, 2, 2, [199, 64]),
     ("tq", 3, 2, 2, 8, [100, 5]),      # G = 1: eight queries; queries 0..2 of batch 1 see nothing
+    ("kqv", 4, 2, 2, 3, [100, 2]),     # G = 1, three queries: odd Gc takes the separate lo terms
     ("plain", 2, 4, 2, 4, [33, 200]),
     ("headq", 2, 8, 2, 2, [150, 97]),
 ])
@@ -225,6 +226,25 @@ def test_multi_query_decode(scheme, n, hq, hkv, nq, lens):
             if L == 0:
                 assert np.all(out[b, i] == 0)
         assert rel_err(out[:, i], ref) <= ATTN_TOL, (i, rel_err(out[:, i], ref))
+
+
+@pytest.mark.parametrize("scheme", ["kqv", "qkqv"])
+@pytest.mark.parametrize("hq,nq", [(2, 1), (4, 1), (2, 2), (4, 2), (2, 4)])
+def test_qjl_value_readout_query_columns(scheme, hq, nq):
+    # Gc = G nq query columns of 1, 2 and 4: the value sketch's readout rides in columns
+    # Gc .. 2 Gc - 1 of the value MMA, as copies of the query columns' scores, and takes their
+    # causal ends
+    import torch
+    inp = small_inputs("cfg2", B=2, T=180, Hkv=2, Hq=hq, seed=24)
+    pair = Pair(inp, scheme, 4)
+    pair.append_gpu(chunk=90)
+    buf = pair.gpu_bytes()
+    qm = _multi_queries(inp, nq, 25)
+    lens = [180, 19]
+    out = pair.gpu.decode_multi(torch.from_numpy(qm).cuda(), lens).cpu().numpy().astype(np.float64)
+    for i in range(nq):
+        seq_i = [L - nq + 1 + i for L in lens]
+        assert rel_err(out[:, i], pair.orc.decode(buf, qm[:, i], seq_i)) <= ATTN_TOL, i
 
 
 def test_multi_query_single_equals_decode_and_limits():

@@ -331,7 +331,9 @@ static tq_status decode_impl(const tq_context* ctx, const void* cache, const flo
   pp.q_sk = (uint32_t*)(base + w.q_sk);
   pp.q_u = (uint32_t*)(base + w.q_u);
   const int Gc = (Hq / Hkv) * nq;
-  const bool lo_sep = 2 * Gc > kQCols;  // the lo terms do not fit the spare columns
+  // the lo terms go to a separate array when they do not fit the spare columns, or when Gc is odd
+  // and above 1: the shuffle that adds them back pairs lanes, which takes an even Gc
+  const bool lo_sep = 2 * Gc > kQCols || (Gc > 1 && Gc % 2);
   if (lo_sep && D != kDecD) {
     set_error("head dims above 128 are built for H_q / H_kv <= 4");
     return TQ_ERR_UNSUPPORTED;

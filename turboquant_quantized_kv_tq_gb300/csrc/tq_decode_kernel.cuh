@@ -39,10 +39,12 @@ namespace tqd {
 constexpr int kDecD = 128;
 constexpr int kSQ = 5;  // code-width tag of a spectral (SQU-KV) side in the decode templates
 constexpr int kLogitsWarps = 8;
-// Warps per decode block: 16 (4 per scheduler) when the per-thread state fits in 128 registers;
-// the QJL variants carry 16-32 more accumulator / fragment registers and use 12.
-template <bool KQ, bool VQ>
-struct DecWarps { static constexpr int value = (KQ || VQ) ? 12 : 16; };
+// Warps per decode block: 16 (4 per scheduler, 128 registers a thread), or 12 (170 registers)
+// when the query's lo terms take their own MMAs (QLO): their fragments, and with a QJL value
+// side a second accumulator (32 registers), do not fit 128.  Without QLO a QJL value side's
+// readout shares the value MMA and its accumulator.
+template <bool KQ, bool VQ, bool QLO>
+struct DecWarps { static constexpr int value = (QLO || KQ || VQ) ? 12 : 16; };
 constexpr int kQCols = 8;  // query columns per KV head in the prepared query arrays
 constexpr int kTile = 16;
 constexpr int kHeadsPad = 8;
@@ -704,6 +706,10 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
   } else if (lo_xor < 0) {  // one query column: its lo term is column 1 of the same thread
     s[0] += s[1];
     s[2] += s[3];
+    if constexpr (VQ && !QLO) {  // column 1 becomes the value sketch's copy of column 0
+      s[1] = s[0];
+      s[3] = s[2];
+    }
   }
 }
 
@@ -745,12 +751,19 @@ __device__ __forceinline__ float ex2(float x) {
 // Rows (tokens) at or past `end` carry no data; a score of column c counts only for tokens
 // below lmin + c / G, the causal end of that column's query (c = 2 lt, 2 lt + 1; lmin = end
 // for plain decode).
-template <int NT, bool MASK, int KB, bool KQ, bool KH, int VB, bool VQ>
+// PK (a QJL value side, query columns Gc <= 4): columns c < Gc carry the code readout of query
+// column c and columns Gc <= c < 2 Gc, whose scores are copies of column c - Gc's, its value
+// sketch readout.  One MMA then takes the 8 tokens of a score-row half twice along k, codes
+// then signs, against a B operand holding p nu in the code columns of the first half and
+// p nu rho in the sketch columns of the second.  Both readouts share one accumulator.
+template <int NT, bool MASK, bool PK = false, int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d)[2], float (&s)[NT][4],
-                                                WarpState<VQ>& st, uint32_t lxV, uint32_t v_m0, int t0,
-                                                int end, int lmin, int G, int lg) {
+                                                WarpState<VQ && !PK>& st, uint32_t lxV, uint32_t v_m0, int t0,
+                                                int end, int lmin, int G, int Gc, int lg) {
+  static_assert(!PK || VQ, "a packed sketch readout needs a QJL value side");
   const int lt2 = 2 * ((int)threadIdx.x & 3);
-  const int e0 = lmin + lt2 / G, e1 = lmin + (lt2 + 1) / G;  // used on masked tiles only
+  // causal end of each column's query (a sketch column takes its code column's); masked tiles only
+  const int e0 = lmin + (lt2 % Gc) / G, e1 = lmin + ((lt2 + 1) % Gc) / G;
   bool va[NT], vb[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
@@ -790,7 +803,7 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       st.acc[mt][0] *= a0; st.acc[mt][1] *= a1; st.acc[mt][2] *= a0; st.acc[mt][3] *= a1;
-      if constexpr (VQ) {
+      if constexpr (VQ && !PK) {
         st.accs[mt][0] *= a0; st.accs[mt][1] *= a1; st.accs[mt][2] *= a0; st.accs[mt][3] *= a1;
       }
     }
@@ -807,6 +820,25 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
     st.l1 += p1 + p3;
     // rows past the sequence end read whatever the cache holds there: select, don't multiply
     const float nA = va[j] ? d[j].nuVA : 0.f, nB = vb[j] ? d[j].nuVB : 0.f;
+    if constexpr (PK) {
+      const bool c0 = lt2 < Gc, c1 = lt2 + 1 < Gc;  // code columns (else sketch columns)
+      const float fA = va[j] ? d[j].nuVA * d[j].rhoVA : 0.f, fB = vb[j] ? d[j].nuVB * d[j].rhoVB : 0.f;
+      const uint32_t cA = movmatrix_trans(pack_half2(c0 ? p0 * nA : 0.f, c1 ? p1 * nA : 0.f));
+      const uint32_t sA = movmatrix_trans(pack_half2(c0 ? 0.f : p0 * fA, c1 ? 0.f : p1 * fA));
+      const uint32_t cB = movmatrix_trans(pack_half2(c0 ? p2 * nB : 0.f, c1 ? p3 * nB : 0.f));
+      const uint32_t sB = movmatrix_trans(pack_half2(c0 ? 0.f : p2 * fB, c1 ? 0.f : p3 * fB));
+      d[j].v.prepare();
+      d[j].vs.prepare();
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4], g[4];
+        d[j].v.frag(lxV, v_m0, mt, a);
+        d[j].vs.frag(mt, g);
+        mma16816(st.acc[mt], a[0], a[1], g[0], g[1], cA, sA);
+        mma16816(st.acc[mt], a[2], a[3], g[2], g[3], cB, sB);
+      }
+      continue;
+    }
     const uint32_t bv0 = movmatrix_trans(pack_half2(p0 * nA, p1 * nA));
     const uint32_t bv1 = movmatrix_trans(pack_half2(p2 * nB, p3 * nB));
     d[j].v.prepare();
@@ -816,7 +848,7 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
       d[j].v.frag(lxV, v_m0, mt, a);
       mma16816(st.acc[mt], a[0], a[1], a[2], a[3], bv0, bv1);
     }
-    if constexpr (VQ) {
+    if constexpr (VQ && !PK) {
       const float fa = va[j] ? d[j].nuVA * d[j].rhoVA : 0.f, fb = vb[j] ? d[j].nuVB * d[j].rhoVB : 0.f;
       const uint32_t bs0 = movmatrix_trans(pack_half2(p0 * fa, p1 * fa));
       const uint32_t bs1 = movmatrix_trans(pack_half2(p2 * fb, p3 * fb));
@@ -833,7 +865,7 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
 
 // Scores and online-softmax step of NT consecutive tiles held by one warp (head dim 128).
 template <int NT, bool MASK, bool QLO, int KB, bool KQ, bool KH, int VB, bool VQ>
-__device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ>& st,
+__device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[2], WarpState<VQ && QLO>& st,
                                               const uint32_t (&qf)[16], const uint32_t (&qs)[16],
                                               const uint32_t (&qu)[2], const uint32_t (&qfl)[16],
                                               const uint32_t (&qsl)[16], uint32_t lxK,
@@ -844,7 +876,7 @@ __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[
 #pragma unroll
   for (int j = 0; j < NT; ++j)
     key_scores<QLO>(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale, qfl, qsl, p.lo_xor);
-  softmax_readout<NT, MASK>(d, s, st, lxV, v_m0, t0, end, lmin, p.G, lg);
+  softmax_readout<NT, MASK, VQ && !QLO>(d, s, st, lxV, v_m0, t0, end, lmin, p.G, p.Gc, lg);
 }
 
 // Placement of N equal regions of RS bytes around the code tables, in shared-window addresses:
@@ -874,17 +906,20 @@ struct RegionPlan {
 
 // Shared-memory plan of a decode block: per-warp regions (the warp's bulk-copy ring, later its
 // merge slot) placed by RegionPlan, then one mbarrier per pair stage and warp.
+// A value codebook other than the key one gets its own table in the upper half (bytes 128 .. 255)
+// of the key table's entries, so both share one 64 KiB-aligned range.
 template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO = false>
 struct DecodeSmem {
-  static constexpr uint32_t lutK = LutEntries<KB>::value * kLutStride;
-  static constexpr uint32_t lutV = KB == VB ? 0 : LutEntries<VB>::value * kLutStride;  // same codebook
-  static constexpr bool sepV = lutV > 0;
+  static constexpr int NK = LutEntries<KB>::value, NV = LutEntries<VB>::value;
+  static constexpr bool sepV = KB != VB && NV > 0;  // same width, same codebook
+  static constexpr uint32_t lutK = (NK > NV ? NK : NV) * kLutStride;
+  static constexpr uint32_t kVHalf = 128;  // byte offset of the value table inside an entry
   static constexpr int PS = 4 + kDecD + (VQ ? kDecD : 0);  // per head: m, l, pad, pad, acc, (acc_sk)
-  static constexpr int NW = DecWarps<KQ, VQ || QLO>::value;
+  static constexpr int NW = DecWarps<KQ, VQ, QLO>::value;
   static constexpr uint32_t ring = kPairStages * 2 * Stage<KB, KQ, KH, VB, VQ>::bytes;
   static constexpr uint32_t mslot = kHeadsPad * PS * 4;
   static constexpr uint32_t RS = ring > mslot ? ring : mslot;
-  using Plan = RegionPlan<lutK, lutV, RS, NW>;
+  using Plan = RegionPlan<lutK, 0, RS, NW>;
   static constexpr uint32_t bars = Plan::bars;
   static constexpr uint32_t bytes = bars + NW * kPairStages * 8;
   __host__ __device__ static constexpr uint32_t region(int w) { return Plan::region(w); }
@@ -904,7 +939,7 @@ constexpr int kErrWaitTimeout = TQ_DEVERR_WAIT_TIMEOUT;
 constexpr int kErrSmemPlan = TQ_DEVERR_SMEM_PLAN;
 
 template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO, bool PAGED>
-__global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_kernel(const DecodeParams p) {
   using SM = DecodeSmem<KB, KQ, KH, VB, VQ, QLO>;
   using SG = Stage<KB, KQ, KH, VB, VQ>;
   constexpr int PS = SM::PS;
@@ -922,14 +957,14 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
   }
   unsigned char* const win = smem - sbase;
   if constexpr (KB != 1) build_lut<KB>(win + kLutAddrK, p.tab.k_c);
-  if constexpr (SM::sepV && VB != 1) build_lut<VB>(win + kLutAddrV, p.tab.v_c);
+  if constexpr (SM::sepV) build_lut<VB>(win + kLutAddrK + SM::kVHalf, p.tab.v_c);
   // the 1-bit magnitude: a 1-bit codebook's upper centroid, or a spectral side's floor centroid
   const float kc1 = KB == kSQ ? __ldg(p.tab.sq_c1) : __ldg(p.tab.k_c + 1);
   const float vc1 = VB == kSQ ? __ldg(p.tab.sq_c1 + 1) : __ldg(p.tab.v_c + 1);
   const uint32_t k_m0 = pack_half2(kc1, kc1);
   const uint32_t v_m0 = pack_half2(vc1, vc1);
   const uint32_t lxK = kLutAddrK | (4u * lane);
-  const uint32_t lxV = (SM::sepV ? kLutAddrV : kLutAddrK) | (4u * lane);
+  const uint32_t lxV = kLutAddrK | (SM::sepV ? SM::kVHalf : 0u) | (4u * lane);
   const uint32_t my_bars = SM::bars + warp * kPairStages * 8;
   if (lane < kPairStages) mbar_init(my_bars + 8 * lane, 1);
   fence_mbar_init();
@@ -978,7 +1013,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
     const int nt = m1t - m0t;
     SlabPtrs sp;
     if constexpr (!PAGED) sp.init(p.cache, b, kvh);
-    WarpState<VQ> st;
+    WarpState<VQ && QLO> st;
     st.reset();
     // both pair stages in flight; a pair stage is refilled as soon as its operands are in
     // registers, before the pair is computed
@@ -1051,7 +1086,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
       const unsigned char* stg = my_stages + sl * PB;
       TileData<KB, KQ, KH, VB, VQ> d[2];
       const int t0 = (m0t + 2 * k) * kTile;
-      if constexpr (!(KQ || VQ || KH)) {
+      if constexpr (!(KQ || KH || (VQ && QLO))) {
         read_stage(d[0], stg, stg + 2 * KBL - SG::VC, lg, lt);
         if (two) read_stage(d[1], stg + KBL, stg + 2 * KBL + VBL - SG::VC, lg, lt);
         __syncwarp();  // every lane has read the stage
@@ -1106,14 +1141,21 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ || QLO>::value * 32, 1) decode
       mb[(2 * lt + 1) * PS + 0] = st.m1;
       mb[(2 * lt + 1) * PS + 1] = l1;
     }
+    // accumulator of column c: the code readout of slot c, or with a packed sketch readout
+    // (Gc <= c < 2 Gc) the sketch readout of slot c - Gc
+    int o0 = (2 * lt) * PS + 4, o1 = (2 * lt + 1) * PS + 4;
+    if constexpr (VQ && !QLO) {
+      if (2 * lt >= Gc && 2 * lt < 2 * Gc) o0 = (2 * lt - Gc) * PS + 4 + kDecD;
+      if (2 * lt + 1 >= Gc && 2 * lt + 1 < 2 * Gc) o1 = (2 * lt + 1 - Gc) * PS + 4 + kDecD;
+    }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const int d0 = 16 * lg + 2 * mt;
-      mb[(2 * lt) * PS + 4 + d0] = st.acc[mt][0];
-      mb[(2 * lt + 1) * PS + 4 + d0] = st.acc[mt][1];
-      mb[(2 * lt) * PS + 4 + d0 + 1] = st.acc[mt][2];
-      mb[(2 * lt + 1) * PS + 4 + d0 + 1] = st.acc[mt][3];
-      if constexpr (VQ) {
+      mb[o0 + d0] = st.acc[mt][0];
+      mb[o1 + d0] = st.acc[mt][1];
+      mb[o0 + d0 + 1] = st.acc[mt][2];
+      mb[o1 + d0 + 1] = st.acc[mt][3];
+      if constexpr (VQ && QLO) {
         mb[(2 * lt) * PS + 4 + kDecD + d0] = st.accs[mt][0];
         mb[(2 * lt + 1) * PS + 4 + kDecD + d0] = st.accs[mt][1];
         mb[(2 * lt) * PS + 4 + kDecD + d0 + 1] = st.accs[mt][2];

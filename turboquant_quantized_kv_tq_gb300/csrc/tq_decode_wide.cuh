@@ -173,9 +173,9 @@ __global__ void __launch_bounds__(WideCfg<D, KB, VB, VQ>::NW * 32, 1) decode_wid
       s[0][0] = t.x; s[0][1] = t.y; s[0][2] = t.z; s[0][3] = t.w;
       const int t0 = (m0t + i) * kTile;
       if (t0 + kTile <= L)
-        softmax_readout<1, false>(d, s, st, lxV, v_m0, t0, L, L, kHeadsPad, lg);
+        softmax_readout<1, false>(d, s, st, lxV, v_m0, t0, L, L, kHeadsPad, kHeadsPad, lg);
       else
-        softmax_readout<1, true>(d, s, st, lxV, v_m0, t0, L, L, kHeadsPad, lg);
+        softmax_readout<1, true>(d, s, st, lxV, v_m0, t0, L, L, kHeadsPad, kHeadsPad, lg);
     }
     seq += nt;
 
