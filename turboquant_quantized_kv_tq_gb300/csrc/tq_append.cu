@@ -505,8 +505,7 @@ __device__ __forceinline__ void append_body(const AppendParams& p, float* st_sme
   if (p.qjl[side] && p.qjl_mma) return;  // left to append_qjl_mma_kernel (whole block)
   const float* ST = side ? p.tab.S_V_T : p.tab.S_K_T;
   if (D == 128 && p.stage_st && p.qjl[side]) {
-    for (int i = threadIdx.x * 4; i < D * D; i += blockDim.x * 4)
-      *reinterpret_cast<float4*>(st_smem + i) = __ldg(reinterpret_cast<const float4*>(ST + i));
+    stage_table<kWarpsPerBlock * 32>(st_smem, ST, D * D);
     __syncthreads();
     ST = st_smem;
   }

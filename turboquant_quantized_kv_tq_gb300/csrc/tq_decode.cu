@@ -154,8 +154,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   extern __shared__ __align__(16) float skt_smem[];
   const float* SKT = p.tab.S_K_T;
   if (D == kDecD && p.kq) {  // S_K^T (64 KiB) into shared memory: 128 dependent rows per head
-    for (int i = threadIdx.x * 4; i < D * D; i += blockDim.x * 4)
-      *reinterpret_cast<float4*>(skt_smem + i) = __ldg(reinterpret_cast<const float4*>(SKT + i));
+    stage_table<256>(skt_smem, SKT, D * D);
     __syncthreads();
     SKT = skt_smem;
   }

@@ -1086,7 +1086,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
       const unsigned char* stg = my_stages + sl * PB;
       TileData<KB, KQ, KH, VB, VQ> d[2];
       const int t0 = (m0t + 2 * k) * kTile;
-      if constexpr (!(KQ || KH || (VQ && QLO))) {
+      if constexpr (!(KH || ((KQ || VQ) && QLO))) {
         read_stage(d[0], stg, stg + 2 * KBL - SG::VC, lg, lt);
         if (two) read_stage(d[1], stg + KBL, stg + 2 * KBL + VBL - SG::VC, lg, lt);
         __syncwarp();  // every lane has read the stage
@@ -1228,6 +1228,8 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
           // o_rot += sqrt(pi/2)/m * S_V^T acc_sk
           const float sv[4] = {accs.x, accs.y, accs.z, accs.w};
           float corr[4] = {0.f, 0.f, 0.f, 0.f};
+          // the block waits for this product: keep many rows' loads in flight
+#pragma unroll 8
           for (int r4 = 0; r4 < 32; ++r4) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -1248,6 +1250,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
           const float a[4] = {o[0] * s4.x, o[1] * s4.y, o[2] * s4.z, o[3] * s4.w};
           float r[4] = {0.f, 0.f, 0.f, 0.f};
           const float* ET = p.tab.sq_ET[1] + (long long)kvh * kDecD * kDecD + 4 * lane;
+#pragma unroll 4
           for (int sl = 0; sl < 32; ++sl) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {

@@ -324,4 +324,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Copies n floats (n a multiple of 32 NT) from global to shared memory with the NT threads of a
+// block, eight 16-byte loads in flight per thread.  Used for the 64 KiB sketch tables that a
+// block stages once: they are often evicted from L2 between calls, and one load in flight per
+// thread would pay a DRAM latency per 4 KiB of table.
+template <int NT>
+__device__ __forceinline__ void stage_table(float* dst, const float* __restrict__ src, int n) {
+  for (int base = (int)threadIdx.x * 4; base < n; base += NT * 32) {
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __ldg(reinterpret_cast<const float4*>(src + base + k * NT * 4));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) *reinterpret_cast<float4*>(dst + base + k * NT * 4) = v[k];
+  }
+}
+
 }  // namespace tqd
