@@ -7,7 +7,9 @@
 // tile, each warp computes its slice's partial key scores with the head-dim-128 building blocks,
 // the group adds the D / 128 partials through a shared-memory exchange (one named barrier per
 // tile; every warp sums them in the same order, so all warps hold identical scores and identical
-// softmax state), and each warp accumulates the value readout of its own slice.
+// softmax state), and each warp accumulates the value readout of its own slice.  With a QJL value
+// side the sketch readout rides in query columns G .. 2 G - 1 of the value MMA, as in the
+// head-dim-128 kernel, so every variant runs the same 16 warps per block.
 //
 // Loads: per group, a ring of single-tile stages (K block then V block, one bulk copy each)
 // issued by the group's first lane and refilled once the exchange barrier shows that every warp
@@ -26,7 +28,7 @@ namespace tqd {
 template <int D, int KB, int VB, bool VQ>
 struct WideCfg {
   static constexpr int DS = D / kDecD;                  // warps per group
-  static constexpr int NG = (VQ ? 256 : 512) / (DS * 32);  // groups per block
+  static constexpr int NG = 512 / (DS * 32);             // groups per block
   static constexpr int NW = DS * NG;
   static constexpr int kSlots = 3;                       // single-tile stages per group
   using S = Stage<KB, false, false, VB, VQ, D>;
@@ -36,7 +38,8 @@ struct WideCfg {
   static constexpr bool sepV = lutV > 0;
   static constexpr uint32_t ring = kSlots * S::bytes;
   static constexpr uint32_t xch = 2 * DS * 32 * 16;       // partial-score exchange, double-buffered
-  static constexpr uint32_t mslot = kHeadsPad * PS * 4;    // merge slot of the group (up to 8 heads)
+  static constexpr int kHeads = 4;                         // query heads per KV head (G <= 4 here)
+  static constexpr uint32_t mslot = kHeads * PS * 4;       // merge slot of the group
   static constexpr uint32_t RS0 = ring + xch > mslot ? ring + xch : mslot;
   static constexpr uint32_t RS = (RS0 + 15) / 16 * 16;
   using Plan = RegionPlan<lutK, lutV, RS, NG>;
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(WideCfg<D, KB, VB, VQ>::NW * 32, 1) decode_wid
     const int nt = m1t - m0t;
     SlabPtrs sp;
     sp.init(p.cache, b, kvh);
-    WarpState<VQ> st;
+    WarpState<false> st;  // a value sketch's readout shares the value MMA (columns G .. 2 G - 1)
     st.reset();
     if (leader) {
       for (int i = 0; i < C::kSlots && i < nt; ++i) {
@@ -173,9 +176,9 @@ __global__ void __launch_bounds__(WideCfg<D, KB, VB, VQ>::NW * 32, 1) decode_wid
       s[0][0] = t.x; s[0][1] = t.y; s[0][2] = t.z; s[0][3] = t.w;
       const int t0 = (m0t + i) * kTile;
       if (t0 + kTile <= L)
-        softmax_readout<1, false>(d, s, st, lxV, v_m0, t0, L, L, kHeadsPad, kHeadsPad, lg);
+        softmax_readout<1, false, VQ>(d, s, st, lxV, v_m0, t0, L, L, G, G, lg);
       else
-        softmax_readout<1, true>(d, s, st, lxV, v_m0, t0, L, L, kHeadsPad, kHeadsPad, lg);
+        softmax_readout<1, true, VQ>(d, s, st, lxV, v_m0, t0, L, L, G, G, lg);
     }
     seq += nt;
 
@@ -188,24 +191,25 @@ __global__ void __launch_bounds__(WideCfg<D, KB, VB, VQ>::NW * 32, 1) decode_wid
     }
     __syncthreads();  // every group is done with its ring and exchange: reuse them for the merge
     float* mg = reinterpret_cast<float*>(win + PL::region(grp));
+    // column c < G: head c's m, l and code readout; G <= c < 2 G (QJL value side): head c - G's
+    // sketch readout; other columns carry nothing
+    const int c0 = 2 * lt, c1 = 2 * lt + 1;
     if (sl == 0 && lg == 0) {
-      mg[(2 * lt) * PS + 0] = st.m0;
-      mg[(2 * lt) * PS + 1] = l0;
-      mg[(2 * lt + 1) * PS + 0] = st.m1;
-      mg[(2 * lt + 1) * PS + 1] = l1;
+      if (c0 < G) { mg[c0 * PS + 0] = st.m0; mg[c0 * PS + 1] = l0; }
+      if (c1 < G) { mg[c1 * PS + 0] = st.m1; mg[c1 * PS + 1] = l1; }
     }
+    const int o0 = c0 < G ? c0 * PS + 4 : (VQ && c0 < 2 * G ? (c0 - G) * PS + 4 + D : -1);
+    const int o1 = c1 < G ? c1 * PS + 4 : (VQ && c1 < 2 * G ? (c1 - G) * PS + 4 + D : -1);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const int d0 = kDecD * sl + 16 * lg + 2 * mt;
-      mg[(2 * lt) * PS + 4 + d0] = st.acc[mt][0];
-      mg[(2 * lt + 1) * PS + 4 + d0] = st.acc[mt][1];
-      mg[(2 * lt) * PS + 4 + d0 + 1] = st.acc[mt][2];
-      mg[(2 * lt + 1) * PS + 4 + d0 + 1] = st.acc[mt][3];
-      if constexpr (VQ) {
-        mg[(2 * lt) * PS + 4 + D + d0] = st.accs[mt][0];
-        mg[(2 * lt + 1) * PS + 4 + D + d0] = st.accs[mt][1];
-        mg[(2 * lt) * PS + 4 + D + d0 + 1] = st.accs[mt][2];
-        mg[(2 * lt + 1) * PS + 4 + D + d0 + 1] = st.accs[mt][3];
+      if (o0 >= 0) {
+        mg[o0 + d0] = st.acc[mt][0];
+        mg[o0 + d0 + 1] = st.acc[mt][2];
+      }
+      if (o1 >= 0) {
+        mg[o1 + d0] = st.acc[mt][1];
+        mg[o1 + d0 + 1] = st.acc[mt][3];
       }
     }
     __syncthreads();
