@@ -31,11 +31,13 @@ Modules:
 * ``headq``     calibration basis by PCA and the corrected logits.
 
 Parity status: every function is pinned by ``tests/test_oracle_*.py`` against
-closed forms, published values, invariants or brute force, except the HeadQ
-PCA basis (``headq.calibration_basis``), which is **parity unpinned**: an
-eigenvector's sign and a near-degenerate subspace are not unique.  The basis
-is calibration data handed identically to both sides, so it never enters a
-parity comparison.
+closed forms, published values, invariants or brute force.  The HeadQ PCA basis
+(``headq.calibration_basis``) is pinned through what is unique about it (an
+eigenvector's sign and a degenerate subspace are not): its projector against
+a planted subspace, orthonormality, maximal captured variance against other
+frames, invariance to a common offset and to scale, and the leading direction
+by brute force at d = 2.  It is calibration data handed identically to both
+sides, so it never enters a parity comparison.
 """
 
 from . import codebook, tables, rotation, codec, layout, attention, headq, pipeline  # noqa: F401

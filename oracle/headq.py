@@ -9,9 +9,12 @@ Readings: the basis is per KV head (the side code is stored once per key, so
 the G query heads of a group share it), and it is the top-r eigenvectors of
 the centred sample covariance of that group's calibration queries.
 
-Parity unpinned: ``calibration_basis`` (eigenvector signs and near-degenerate
-subspaces are not unique).  It is calibration input handed identically to
-both sides as an fp32 table and never compared.
+``calibration_basis`` is pinned by tests/test_oracle_headq_basis.py through
+what is unique about it (eigenvector signs and degenerate subspaces are not):
+the projector onto a planted subspace, orthonormality, maximal captured
+variance (Ky Fan) against other frames, invariance to a common offset and to
+scale, and the leading direction by brute force at d = 2.  It is calibration
+input handed identically to both sides as an fp32 table and never compared.
 """
 
 import numpy as np
