@@ -579,6 +579,71 @@ def run_workload(args):
                       "schemes": res}), flush=True)
 
 
+def run_paged(args):
+    """The paged pool at the headline shape (B=8 Hq=32 Hkv=8 d=128 T=32768), per scheme: each
+    sequence's 2048 blocks on shuffled pages, filled by the paged append (4096-token chunks, start
+    positions on the device), then `reps` paged decode calls with device lengths, timed with CUDA
+    events (query prep with the device work split + decode).  The same decode of a contiguous
+    cache is timed beside it.  One JSON line; not the headline contract line."""
+    import torch
+    from turboquant_quantized_kv_tq_gb300 import PagedKVCache, QuantizedKVCache
+    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    device = torch.device("cuda", 0)
+    inp = make_inputs("cfg2")
+    B, Hq, Hkv, d, T = inp.B, inp.Hq, inp.Hkv, inp.d, inp.T
+    to_t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    mb = T // 16
+    num_pages = B * mb + 64
+    table = np.random.default_rng(11).permutation(num_pages)[:B * mb].reshape(B, mb).astype(np.int32)
+    tdev = torch.from_numpy(table).to(device)
+    q = torch.from_numpy(inp.q).to(device)
+    out = torch.empty_like(q)
+    seq_dev = torch.full((B,), T, dtype=torch.int32, device=device)
+    peak, peak_kind = measured_peak()
+    reps = 50
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    res = {}
+    for scheme, n in SCHEMES:
+        pool = PagedKVCache(d, Hq, Hkv, B, num_pages, mb, scheme=scheme, n=n, seed=inp.seed, device=device)
+        for s0 in range(0, T, 4096):
+            start = torch.full((B,), s0, dtype=torch.int32, device=device)
+            pool.append(to_t(inp.K[:, :, s0:s0 + 4096]).to(device), to_t(inp.V[:, :, s0:s0 + 4096]).to(device),
+                        start, tdev)
+        us_paged = timed(lambda: pool.decode(q, seq_dev, tdev, out=out))
+        rec = (pool.layout.k_block_bytes + pool.layout.v_block_bytes) / 16.0
+        del pool
+        torch.cuda.empty_cache()
+        kv = QuantizedKVCache(d, Hq, Hkv, B, T, scheme=scheme, n=n, seed=inp.seed, device=device)
+        for s0 in range(0, T, 4096):
+            kv.append(to_t(inp.K[:, :, s0:s0 + 4096]).to(device), to_t(inp.V[:, :, s0:s0 + 4096]).to(device),
+                      [s0] * B)
+        kv.workspace(T)
+        us_contig = timed(lambda: kv.decode(q, [T] * B, out=out))
+        del kv
+        torch.cuda.empty_cache()
+        nbytes = B * Hkv * T * rec
+        res[f"{scheme}{n}"] = {"paged_decode_us": round(us_paged, 2), "contiguous_decode_us": round(us_contig, 2),
+                               "record_bytes": rec, "GB_per_s": round(nbytes / (us_paged * 1e-6) / 1e9, 1),
+                               "frac": round(nbytes / (us_paged * 1e-6) / 1e9 / peak, 4),
+                               "cache_tokens_per_s": round(B * Hkv * T / (us_paged * 1e-6), 1)}
+    print(json.dumps({"workload": f"paged: B={B} Hq={Hq} Hkv={Hkv} d={d} T={T}, {num_pages} pages of 16 "
+                                  f"tokens x {Hkv} KV heads, block tables a random permutation",
+                      "unit": UNIT, "peak_GBps": peak, "peak_kind": peak_kind,
+                      "timing": f"CUDA events, {reps} decode calls", "schemes": res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -593,18 +658,22 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")
     ap.add_argument("--schemes", default=None,
                     help="comma-separated subset of plain4,tq4,kqv4,qkqv4 (default: all four)")
-    ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5", "sq"],
-                    help="decode throughput of another configuration at full size (one JSON line)")
+    ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5", "sq", "paged"],
+                    help="decode throughput of another configuration at full size, or of the paged pool "
+                         "at the headline shape (one JSON line)")
     args = ap.parse_args()
-    if args.workload:
-        run_workload(args)
-        return
     if args.schemes:
         global SCHEMES
         known = {f"{s}{n}": (s, n) for s, n in SCHEMES}
         SCHEMES = [known[x.strip()] for x in args.schemes.split(",")]
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "paged":
+        run_paged(args)
+        return
+    if args.workload:
+        run_workload(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
