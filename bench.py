@@ -182,7 +182,7 @@ def build_caches(inp, device, T):
 def run_gpu(args):
     import torch
     import torch.distributed as dist
-    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    from workloads import make_inputs
 
     rank, world, local = dist_env()
     if world > 1:
@@ -472,7 +472,7 @@ def run_reference(args):
     """The oracle alone, on the host cores, timed per step on a bounded sample of the workload."""
     from oracle import codec as ocodec
     from oracle.pipeline import OracleContext
-    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    from workloads import make_inputs
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -520,7 +520,7 @@ def run_workload(args):
     with CUDA events (query prep + decode).  One JSON line; not the headline contract line."""
     import torch
     from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
-    from turboquant_quantized_kv_tq_gb300.workloads import CONFIGS, make_inputs
+    from workloads import CONFIGS, make_inputs
     name = args.workload
     device = torch.device("cuda", 0)
     inp = make_inputs(name)
@@ -587,7 +587,7 @@ def run_paged(args):
     cache is timed beside it.  One JSON line; not the headline contract line."""
     import torch
     from turboquant_quantized_kv_tq_gb300 import PagedKVCache, QuantizedKVCache
-    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    from workloads import make_inputs
     device = torch.device("cuda", 0)
     inp = make_inputs("cfg2")
     B, Hq, Hkv, d, T = inp.B, inp.Hq, inp.Hkv, inp.d, inp.T

@@ -240,9 +240,20 @@ tq_status tq_decode_attention_multi(const tq_context* ctx, const void* dev_cache
  * before any stream capture.  Every call shares the one array, so calls that overlap on the GPU
  * (other streams, other threads) race: serialize them.  A configuration whose workspace
  * (tq_decode_workspace_bytes) exceeds TQ_STATIC_SCRATCH_BYTES returns TQ_ERR_WORKSPACE without
- * launching.  No device memory is allocated.  Arguments otherwise as tq_decode_attention. */
+ * launching.  No device memory is allocated.  Arguments otherwise as tq_decode_attention.
+ * The cached address belongs to the device's current primary context: it does not survive a
+ * cudaDeviceReset (or any teardown of that context), after which this entry point must not be
+ * called again in the process.  The kernels report a device-side failure (a bounded wait that
+ * gave up, a shared-memory plan that did not fit) in the scratch's error word, and then leave
+ * `out` unwritten; read it with tq_get_static_device_error. */
 tq_status tq_decode_attention_static(const tq_context* ctx, const void* dev_cache, const float* q,
                                      const int32_t* host_seq_len, float* out, tq_stream stream);
+
+/* Wait for stream, then read the error word of the built-in scratch on the current device (the
+ * one tq_decode_attention_static used): 0 = the last static decode completed, else a
+ * TQ_DEVERR_* code (and TQ_ERR_DEVICE is returned).  Each static decode clears the word before
+ * its kernels run.  Like tq_get_device_error, it synchronizes the stream. */
+tq_status tq_get_static_device_error(int32_t* code, tq_stream stream);
 
 /* HeadQ read path, unfused ([HEADQ] "Leitura do Cache"): corrected logits
  * s_hat_j = q^T k_base_j / sqrt(d) + q^T U z_hat_j / sqrt(d) for every stored token, written to

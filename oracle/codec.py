@@ -119,14 +119,28 @@ def headq_encode(x, codes, norm32, centroids32, R, U, side_bits=4):
     kbase = norm32.astype(np.float64)[:, None] * (np.asarray(centroids32, dtype=np.float64)[codes] @ R)
     e = x - kbase
     z = e @ np.asarray(U, dtype=np.float64)
-    s16 = (np.max(np.abs(z), axis=1) / qmax).astype(np.float16)
+    a = np.max(np.abs(z), axis=1) / qmax
+    s16 = a.astype(np.float16)
     s32 = s16.astype(np.float32)
     zs = np.where(s32[:, None] > 0, z.astype(np.float32) / np.where(s32 > 0, s32, 1)[:, None], np.float32(0))
     zeta = np.clip(np.rint(zs), -qmax, qmax).astype(np.int64)
     # distance of z to the nearest rounding boundary s*(k + 1/2), in the key's units
     frac = np.abs(z / np.where(s32 > 0, s32, 1).astype(np.float64)[:, None])
     margin = np.abs(frac - (np.floor(frac) + 0.5)) * s32.astype(np.float64)[:, None]
-    return {"side": zeta, "side_scale": s16, "z": z, "side_margin": margin}
+    return {"side": zeta, "side_scale": s16, "z": z, "side_margin": margin,
+            "scale_margin": fp16_midpoint_distance(a)}
+
+
+def fp16_midpoint_distance(a):
+    """Relative distance of each float64 value ``a`` to the nearest point where rounding to fp16
+    changes (the midpoint between the two fp16 values around it); the exempt-zone measure of
+    the HeadQ side scale, whose fp16 rounding is a decision like a code's."""
+    a = np.asarray(a, dtype=np.float64)
+    h = a.astype(np.float16)
+    hf = h.astype(np.float64)
+    other = np.where(hf <= a, np.nextafter(h, np.float16(np.inf)), np.nextafter(h, np.float16(-np.inf)))
+    mid = (hf + other.astype(np.float64)) / 2.0
+    return np.abs(a - mid) / np.where(a > 0, a, 1.0)
 
 
 def reconstruct(codec, codes, norm32, centroids32, R, rho16=None, signs=None, S=None,

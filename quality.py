@@ -120,7 +120,7 @@ def _row(regime, label, scheme, n, K, V, Kh, Vh, q, o_ref, o_hat, d, G):
 def _calibration_sets(name, inp, sizes):
     """Per-side calibration vectors [H_kv][n][d] for SQU-KV: the regime's own calibration sets
     when it has them, else a separate draw of the same recipe (another seed)."""
-    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    from workloads import make_inputs
     if "calib_k" in inp.extra:
         return inp.extra["calib_k"], inp.extra["calib_v"]
     cal = make_inputs(name, B=1, T=4096, Hkv=sizes["Hkv"], Hq=inp.Hq, seed=inp.seed + 100)
@@ -131,7 +131,7 @@ def run_regime(name, label, sizes, schemes, device):
     import torch
     from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
     from turboquant_quantized_kv_tq_gb300.calibration import spectral_tables
-    from turboquant_quantized_kv_tq_gb300.workloads import CONFIGS, make_inputs
+    from workloads import CONFIGS, make_inputs
     c = CONFIGS[name]
     G = c["Hq"] // c["Hkv"]
     inp = make_inputs(name, B=sizes["B"], T=sizes["T"], Hkv=sizes["Hkv"], Hq=G * sizes["Hkv"])
@@ -162,7 +162,7 @@ def run_headq(device):
     n=2 keys without a side code for reference."""
     import torch
     from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
-    from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+    from workloads import make_inputs
     inp = make_inputs("cfg5", B=2, T=2048, Hkv=2, Hq=8)
     B, Hq, Hkv, d, T = inp.B, inp.Hq, inp.Hkv, inp.d, inp.T
     G = Hq // Hkv

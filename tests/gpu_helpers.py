@@ -12,7 +12,7 @@ from oracle import codec as ocodec
 from oracle import headq as oheadq
 from oracle.pipeline import OracleContext
 from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
-from turboquant_quantized_kv_tq_gb300.workloads import make_inputs
+from workloads import make_inputs
 
 BOUNDARY = 1e-6
 EXEMPT_FRACTION = 1e-4
@@ -116,17 +116,26 @@ def compare_slab(pair, buf, b, h, T, tokens=None):
         if side == "k" and "side" in o:
             sc_o, sc_g = o["side_scale"], g["side_scale"]
             same_scale = sc_o == sc_g
-            ulp_s = np.spacing(np.abs(sc_o)).astype(np.float64)
-            # a key whose base code differs (exempt, at a cell boundary) has a different residual
-            # and so a different side code and scale: exempt like its signs and rho
-            ok_s = np.abs(sc_g.astype(np.float64) - sc_o.astype(np.float64)) <= ulp_s + 1e-12
-            assert np.all(ok_s | ~vec_ok), ("side scale", np.argwhere(~ok_s & vec_ok)[:5])
+            # the scale's fp16 rounding is a decision: max|z|/7 may round the other way only
+            # within 1e-6 (relative) of an fp16 midpoint, or where the key's base code differs
+            # (exempt, at a cell boundary: its residual, and so z, differs)
+            sex_scale = (o["scale_margin"] < BOUNDARY) | ~vec_ok
+            assert not (~same_scale & ~sex_scale).any(), \
+                ("side scale", np.argwhere(~same_scale & ~sex_scale)[:5])
+            exempt_total += int((~same_scale).sum())
+            coords += same_scale.size
+            # a key whose scale differs has every side code decided against another scale
             zmis = g["side"] != o["side"]
             zex = (o["side_margin"] < BOUNDARY) | ~same_scale[:, None] | ~vec_ok[:, None]
             assert not (zmis & ~zex).any(), ("side code", np.argwhere(zmis & ~zex)[:5])
             exempt_total += int(zmis.sum())
             coords += zmis.size
     return exempt_total, coords
+
+
+def check_exempt(ex, n):
+    """The exempt mismatches of one test: at most 1e-4 of every coordinate it compared."""
+    assert ex <= EXEMPT_FRACTION * n, (ex, n, EXEMPT_FRACTION * n)
 
 
 def rel_err(out, ref):
@@ -138,7 +147,7 @@ def rel_err(out, ref):
 
 
 def small_inputs(name, B=2, T=300, Hkv=2, Hq=None, seed=None, d=None):
-    from turboquant_quantized_kv_tq_gb300.workloads import CONFIGS
+    from workloads import CONFIGS
     c = CONFIGS[name]
     G = c["Hq"] // c["Hkv"]
     Hq = Hq if Hq is not None else G * Hkv

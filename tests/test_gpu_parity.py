@@ -4,7 +4,7 @@ seeded inputs.  Sizes span several 16-token tiles, several split blocks and a ra
 import numpy as np
 import pytest
 
-from tests.gpu_helpers import (ATTN_TOL, EXEMPT_FRACTION, Pair, compare_slab, rel_err,
+from tests.gpu_helpers import (ATTN_TOL, Pair, check_exempt, compare_slab, rel_err,
                                small_inputs)
 
 pytestmark = pytest.mark.gpu
@@ -42,7 +42,7 @@ def _check_all_slabs(pair, T):
             e, c = compare_slab(pair, buf, b, h, T)
             ex += e
             n += c
-    assert ex <= max(2, EXEMPT_FRACTION * n), (ex, n)
+    check_exempt(ex, n)
     return buf
 
 

@@ -10,7 +10,7 @@ and of the oracle's own cache.
 import numpy as np
 import pytest
 
-from gpu_helpers import ATTN_TOL, EXEMPT_FRACTION, compare_slab, rel_err, small_inputs, to_torch
+from gpu_helpers import ATTN_TOL, check_exempt, compare_slab, rel_err, small_inputs, to_torch
 from oracle import codec as ocodec
 from oracle import spectral
 from oracle.pipeline import OracleContext
@@ -64,7 +64,7 @@ def _check_fields(pair, T):
             e, c = compare_slab(pair, buf, b, h, T)
             ex += e
             n += c
-    assert ex <= max(2, EXEMPT_FRACTION * n), (ex, n)
+    check_exempt(ex, n)
     return buf
 
 

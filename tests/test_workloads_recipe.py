@@ -1,11 +1,11 @@
-"""The seeded input generators (turboquant_quantized_kv_tq_gb300/workloads.py) against their stated
+"""The seeded input generators (workloads.py at the repository root) against their stated
 recipe, at reduced sizes: distributions, structure (rank, subspaces, per-channel scales), the bf16
 rounding, shapes and seeding.  Statistical checks use bounds many standard errors wide."""
 
 import numpy as np
 import pytest
 
-from turboquant_quantized_kv_tq_gb300.workloads import CONFIGS, bf16_bits, bf16_to_f32, make_inputs
+from workloads import CONFIGS, bf16_bits, bf16_to_f32, make_inputs
 
 
 def _svals(X):

@@ -114,6 +114,7 @@ DECLARATIONS = [
     ("tq_decode_attention_paged", c_int32, [c_void_p, c_void_p, ctypes.POINTER(tq_page_table), c_void_p,
                                             c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     ("tq_get_device_error", c_int32, [c_void_p, ctypes.POINTER(c_int32), c_void_p]),
+    ("tq_get_static_device_error", c_int32, [ctypes.POINTER(c_int32), c_void_p]),
     ("tq_status_string", ctypes.c_char_p, [c_int32]),
     ("tq_last_error", ctypes.c_char_p, []),
 ]

@@ -450,4 +450,9 @@ tq_status tq_get_device_error(const void* ws, int32_t* code, tq_stream stream) {
   return read_device_error(ws, code, stream);
 }
 
+tq_status tq_get_static_device_error(int32_t* code, tq_stream stream) {
+  if (!code) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  return read_static_device_error(code, stream);
+}
+
 }  // extern "C"

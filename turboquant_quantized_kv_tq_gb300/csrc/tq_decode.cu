@@ -514,6 +514,13 @@ tq_status static_scratch(void** ptr) {
   return TQ_OK;
 }
 
+tq_status read_static_device_error(int32_t* code, Stream stream) {
+  void* ws = nullptr;
+  tq_status s = static_scratch(&ws);
+  if (s != TQ_OK) return s;
+  return read_device_error(ws, code, stream);
+}
+
 tq_status read_device_error(const void* ws, int32_t* code, Stream stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return tqd::cuda_fail("stream synchronize", e);

@@ -92,4 +92,5 @@ tq_status launch_logits(const tq_context* ctx, const void* cache, const float* q
 tq_status read_device_error(const void* ws, int32_t* code, Stream stream);
 // Device address of the built-in decode scratch on the current device (looked up once per device).
 tq_status static_scratch(void** ptr);
+tq_status read_static_device_error(int32_t* code, Stream stream);
 }  // namespace tqi
