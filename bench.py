@@ -278,6 +278,9 @@ def run_gpu(args):
     # ---- several queries per sequence (G * nq = 8 query columns per KV head) on the first cache
     multi = run_multi_query(caches[0], SCHEMES[0], inp, device, T)
 
+    # ---- the second target configuration (128k context, G = 8), with its own roofline
+    long_ctx = run_long_context(args, device) if not args.skip_long_context else None
+
     peak, peak_kind = measured_peak()
     rec = [record_bytes(s, n) for s, n in SCHEMES]
     dec_bytes = [B * Hkv * T * r for r in rec]
@@ -307,6 +310,7 @@ def run_gpu(args):
         "e2e": e2e,
         "append": append,
         "multi_query": multi,
+        "long_context": long_ctx,
         "gpu_launches": args.steps * n_dec * 3,
         "clocks": clocks,
     }
@@ -428,9 +432,81 @@ def run_prefill_append(args, device):
     ms = e0.elapsed_time(e1) / reps
     vec = 2 * B * Hkv * n_new
     moved = vec * d * 2 + B * Hkv * n_new * record_bytes("kqv", 4)
+    peak, peak_kind = measured_peak()
+    gbs = moved / (ms * 1e-3) / 1e9
     return {"workload": "B=1 Hkv=8 d=128, 4096-token prefill chunk into a 131072-token KQV n=4 cache",
             "tok_per_s": round(B * n_new / (ms * 1e-3), 1), "vectors_per_s": round(vec / (ms * 1e-3), 1),
-            "us": round(ms * 1e3, 2), "GB_per_s": round(moved / (ms * 1e-3) / 1e9, 1)}
+            "us": round(ms * 1e3, 2), "GB_per_s": round(gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "algorithmic_bytes": int(moved),
+                         "bytes": "bf16 K and V read (2 x 256 B per token and KV head) + the packed "
+                                  "KQV n=4 record written (138 B)",
+                         "kernel": "append (encode + QJL residual sketch), CUDA events over 10 calls",
+                         "peak_kind": peak_kind}}
+
+
+def run_long_context(args, device):
+    """The 128k-context configuration (B=1, Hq=64, Hkv=8, d=128, T=131072; KQV n=2/3/4): each
+    scheme's cache filled by the library's append, then steps of three decode calls (one per
+    scheme, so each decode's cache was last touched two caches -- 189-256 MB -- earlier, more
+    than L2 holds), each call bracketed by CUDA events on the launching stream."""
+    import torch
+    from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
+    from workloads import CONFIGS, make_inputs
+    c = CONFIGS["cfg4"]
+    inp = make_inputs("cfg4")
+    B, Hq, Hkv, d, T = inp.B, inp.Hq, inp.Hkv, inp.d, inp.T
+    to_t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    q = torch.from_numpy(inp.q).to(device)
+    seq = [T] * B
+    caches = []
+    for scheme, n in c["schemes"]:
+        kv = QuantizedKVCache(d, Hq, Hkv, B, T, scheme=scheme, n=n, seed=inp.seed, device=device)
+        for s0 in range(0, T, 4096):
+            e = min(T, s0 + 4096)
+            kv.append(to_t(inp.K[:, :, s0:e]).to(device), to_t(inp.V[:, :, s0:e]).to(device), [s0] * B)
+        kv.workspace(T)
+        caches.append(kv)
+    outs = [torch.empty_like(q) for _ in caches]
+    stream = torch.cuda.current_stream(device)
+    for _ in range(max(3, args.warmup)):
+        for kv, o in zip(caches, outs):
+            kv.decode(q, seq, out=o)
+    torch.cuda.synchronize(device)
+    reps = 50
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in caches]
+           for _ in range(reps)]
+    for r in range(reps):
+        for i, (kv, o) in enumerate(zip(caches, outs)):
+            evs[r][i][0].record(stream)
+            kv.decode(q, seq, out=o)
+            evs[r][i][1].record(stream)
+    torch.cuda.synchronize(device)
+    peak, peak_kind = measured_peak()
+    res, tot_bytes, tot_s = {}, 0.0, 0.0
+    for i, ((scheme, n), kv) in enumerate(zip(c["schemes"], caches)):
+        us = sum(evs[r][i][0].elapsed_time(evs[r][i][1]) for r in range(reps)) / reps * 1e3
+        rec = record_bytes(scheme, n)
+        nbytes = B * Hkv * T * rec
+        tot_bytes += nbytes
+        tot_s += us * 1e-6
+        res[f"{scheme}{n}"] = {"decode_us": round(us, 2), "record_bytes": rec,
+                               "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                               "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
+                               "cache_tokens_per_s": round(B * Hkv * T / (us * 1e-6), 1)}
+    del caches
+    torch.cuda.empty_cache()
+    achieved = tot_bytes / tot_s / 1e9
+    return {"workload": f"cfg4 long context: B={B} Hq={Hq} Hkv={Hkv} d={d} T={T}, KQV n=2/3/4, "
+                        "Gaussian K/V with log-uniform per-channel std in [0.1, 10]",
+            "timing": f"CUDA events per decode call (query prep + decode), {reps} steps of the three",
+            "cache_tokens_per_s": round(len(res) * B * Hkv * T / tot_s, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "decode (query prep + fused split-K decode), KQV n=2/3/4",
+                         "peak_kind": peak_kind},
+            "schemes": res}
 
 
 def oracle_step(inp, bufs, ctxs, slabs, T):
@@ -655,6 +731,8 @@ def main():
                     help="--impl reference: approximate time of the timed steps")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-append", action="store_true")
+    ap.add_argument("--skip-long-context", action="store_true",
+                    help="leave out the 128k-context (cfg4) decode leg")
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")
     ap.add_argument("--schemes", default=None,
                     help="comma-separated subset of plain4,tq4,kqv4,qkqv4 (default: all four)")

@@ -42,6 +42,13 @@ REGIMES = [
      [("tq", 4), ("kqv", 2), ("kqv", 3), ("kqv", 4), ("qkqv", 4)]),
     ("cfg3", "low-rank keys (rank 16), d=1024", dict(B=2, Hkv=2, T=1024),
      [("tq", 2), ("tq", 4), ("kqv", 2), ("kqv", 4)]),
+    # peaked attention on low-rank keys ([TQ-KV] "Contribuciones Clave" 3 reports its KL
+    # blow-up at d = 1024): the same recipes with the queries scaled so the exact scores have
+    # standard deviation 3 over each regime's tokens, at d = 1024 and at d = 128
+    ("cfg3", "low-rank keys, peaked attention (score std 3), d=1024", dict(B=2, Hkv=2, T=1024, score_std=3.0),
+     [("tq", 2), ("tq", 4), ("kqv", 2), ("kqv", 4)]),
+    ("sq", "low-rank K and V, peaked attention (score std 3), d=128", dict(B=2, Hkv=2, T=1024, score_std=3.0),
+     [("tq", 2), ("tq", 4), ("kqv", 2), ("kqv", 4)]),
 ]
 
 
@@ -127,7 +134,17 @@ def _calibration_sets(name, inp, sizes):
     return cal.k_f32()[0].astype(np.float64), cal.v_f32()[0].astype(np.float64)
 
 
-def run_regime(name, label, sizes, schemes, device):
+def score_scale(q, K, d, G, target_std):
+    """Factor that gives the exact scores q . k / sqrt(d) standard deviation ``target_std`` over
+    all (batch, query head, token)."""
+    s = np.concatenate([(K[b, hq // G] @ q[b, hq] / np.sqrt(d)).ravel()
+                        for b in range(q.shape[0]) for hq in range(q.shape[1])])
+    return float(target_std / np.std(s))
+
+
+def run_regime(name, label, sizes, schemes, device, keep=None):
+    """Rows of one regime.  ``keep``: a list that receives (scheme, n, cache, inputs, q) for each
+    scheme (the tests recompute a row from the oracle's reading of the same cache)."""
     import torch
     from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
     from turboquant_quantized_kv_tq_gb300.calibration import spectral_tables
@@ -138,7 +155,10 @@ def run_regime(name, label, sizes, schemes, device):
     B, Hq, Hkv, d, T = inp.B, inp.Hq, inp.Hkv, inp.d, inp.T
     K = inp.k_f32().astype(np.float64)
     V = inp.v_f32().astype(np.float64)
-    q = inp.q.astype(np.float64)
+    q32 = inp.q
+    if "score_std" in sizes:
+        q32 = (inp.q * score_scale(inp.q.astype(np.float64), K, d, G, sizes["score_std"])).astype(np.float32)
+    q = q32.astype(np.float64)
     o_ref = _reference_output(q, K, V, d, G)
     Kt, Vt = _torch_bf16(inp.K).to(device), _torch_bf16(inp.V).to(device)
     rows = []
@@ -150,9 +170,11 @@ def run_regime(name, label, sizes, schemes, device):
                 E, sc, _ = spectral_tables(X)
                 kv.set_spectral_basis(side, torch.from_numpy(E).to(device), torch.from_numpy(sc).to(device))
         kv.append(Kt, Vt, [0] * B)
-        o_hat = kv.decode(torch.from_numpy(inp.q).to(device), [T] * B).cpu().numpy().astype(np.float64)
+        o_hat = kv.decode(torch.from_numpy(q32).to(device), [T] * B).cpu().numpy().astype(np.float64)
         Kh, Vh = _dequantize_all(kv, B, Hkv, T, d)
         rows.append(_row(name, label, scheme, n, K, V, Kh, Vh, q, o_ref, o_hat, d, G))
+        if keep is not None:
+            keep.append((scheme, n, kv, inp, q32))
     return rows
 
 

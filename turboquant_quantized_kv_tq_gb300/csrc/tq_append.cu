@@ -84,6 +84,38 @@ __device__ __forceinline__ float norm_compensated(const float (&x)[E]) {
   return r + res / (2.f * r);
 }
 
+// The norm split for any finite input.  The fast path is norm_compensated of x itself.  When
+// that norm leaves [2^-30, 2^50) (a sum of squares that overflowed, underflowed, or lost bits
+// to subnormal squares), x is first multiplied by the power of two 2^-e that brings max|x| to
+// [1, 2) (clamped to e in [-126, 126]).  The scaling is exact and leaves the unit vector as it
+// was, so the rotation, codes, residual and side code are computed from the scaled vector with
+// no change; within the fast path's range it would give the same bits.  Returns the norm to
+// store, nu_work * 2^e (which may round once more, or overflow to inf, only when it leaves the
+// fp32 range); nu_work is the norm of the vector left in x, and pw = 2^e.
+template <int E>
+__device__ __forceinline__ float norm_split(float (&x)[E], float& nu_work, float& pw) {
+  const float nu = norm_compensated<E>(x);  // the same value in every lane
+  pw = 1.f;
+  nu_work = nu;
+  if (nu >= 0x1p-30f && nu < 0x1p50f) return nu;
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) m = fmaxf(m, fabsf(x[i]));
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, s));
+  if (!(m > 0.f)) {
+    nu_work = 0.f;
+    return 0.f;
+  }
+  const int e = max(-126, min(126, ((__float_as_int(m) >> 23) & 0xFF) - 127));
+  const float down = __int_as_float((127 - e) << 23);
+  pw = __int_as_float((127 + e) << 23);
+#pragma unroll
+  for (int i = 0; i < E; ++i) x[i] *= down;
+  nu_work = norm_compensated<E>(x);
+  return nu_work * pw;
+}
+
 // Store a w-bit stream: lane l's E values occupy bits [l*E*W, (l+1)*E*W) of the stream.
 template <int E, int W>
 __device__ __forceinline__ void store_stream(unsigned char* dst, const uint32_t (&v)[E]) {
@@ -193,9 +225,9 @@ __device__ __forceinline__ void encode_vectors(const AppendParams& p, int side, 
       for (int i = 0; i < E; ++i) x[v][i] = 0.f;
     }
   }
-  float nu[NV];
+  float nu[NV], nw[NV], pw[NV];  // stored norm, norm of the (possibly rescaled) x, rescale 2^e
 #pragma unroll
-  for (int v = 0; v < NV; ++v) nu[v] = norm_compensated<E>(x[v]);
+  for (int v = 0; v < NV; ++v) nu[v] = norm_split<E>(x[v], nw[v], pw[v]);
 
   float dsg[E];
 #pragma unroll
@@ -225,7 +257,7 @@ __device__ __forceinline__ void encode_vectors(const AppendParams& p, int side, 
   uint32_t code[NV][E], sgnbit[NV][E], mag[NV][E];
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    const float inv = nu[v] > 0.f ? 1.f / (nu[v] * scale) : 0.f;
+    const float inv = nw[v] > 0.f ? 1.f / (nw[v] * scale) : 0.f;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
       y[v][i] = hrot[v][i] * inv;
@@ -318,7 +350,7 @@ __device__ __forceinline__ void encode_vectors(const AppendParams& p, int side, 
       for (int k = 0; k < RK; ++k) z[k] = 0.f;
 #pragma unroll
       for (int i = 0; i < E; ++i) {
-        const float e = hrot[v][i] * rs - nu[v] * __ldg(cent + code[v][i]);
+        const float e = hrot[v][i] * rs - nw[v] * __ldg(cent + code[v][i]);
         const float* urow = Ur + (lane * E + i) * RK;
 #pragma unroll
         for (int k = 0; k < RK; k += 4) {
@@ -332,7 +364,7 @@ __device__ __forceinline__ void encode_vectors(const AppendParams& p, int side, 
       float amax = 0.f;
 #pragma unroll
       for (int k = 0; k < RK; ++k) {
-        z[k] = warp_sum(z[k]);
+        z[k] = warp_sum(z[k]) * pw[v];  // back to the key's units (exact)
         amax = fmaxf(amax, fabsf(z[k]));
       }
       const __half sh = __float2half_rn(amax / 7.0f);
@@ -380,9 +412,9 @@ __device__ __forceinline__ void encode_vectors_sq(const AppendParams& p, int sid
       for (int i = 0; i < E; ++i) x[v][i] = 0.f;
     }
   }
-  float nu[NV];
+  float nu[NV], nw[NV], pw[NV];  // stored norm, norm of the (possibly rescaled) x, rescale 2^e
 #pragma unroll
-  for (int v = 0; v < NV; ++v) nu[v] = norm_compensated<E>(x[v]);
+  for (int v = 0; v < NV; ++v) nu[v] = norm_split<E>(x[v], nw[v], pw[v]);
   // y_c = sum_i E[i][c] x_i for this lane's coordinates c = 4 lane + jj
   float y[NV][E];
 #pragma unroll
@@ -420,7 +452,7 @@ __device__ __forceinline__ void encode_vectors_sq(const AppendParams& p, int sid
     uint32_t sgnbit[E], nib = 0;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-      const float z = nu[v] > 0.f ? __fdiv_rn(y[v][i], nu[v] * sc[i]) : 0.f;
+      const float z = nw[v] > 0.f ? __fdiv_rn(y[v][i], nw[v] * sc[i]) : 0.f;
       const bool pos = z > 0.f;
       const float a = pos ? z : __int_as_float(__float_as_int(-z) + 1);
       uint32_t m = 0;
