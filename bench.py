@@ -278,6 +278,9 @@ def run_gpu(args):
     # ---- several queries per sequence (G * nq = 8 query columns per KV head) on the first cache
     multi = run_multi_query(caches[0], SCHEMES[0], inp, device, T)
 
+    # ---- chunked prefill over the same caches (dense tensor-core products)
+    prefill = run_prefill(args, caches, inp, device, T) if not args.skip_prefill else None
+
     # ---- the second target configuration (128k context, G = 8), with its own roofline
     long_ctx = run_long_context(args, device) if not args.skip_long_context else None
 
@@ -311,6 +314,7 @@ def run_gpu(args):
         "append": append,
         "multi_query": multi,
         "long_context": long_ctx,
+        "prefill": prefill,
         "gpu_launches": args.steps * n_dec * 3,
         "clocks": clocks,
     }
@@ -444,6 +448,70 @@ def run_prefill_append(args, device):
                                   "KQV n=4 record written (138 B)",
                          "kernel": "append (encode + QJL residual sketch), CUDA events over 10 calls",
                          "peak_kind": peak_kind}}
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor-core TFLOP/s of this machine's GPUs (burst: the prefill is timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def prefill_flops(scheme, n, B, Hq, nq, L, d=128, m=128):
+    """Algorithmic FLOPs of a chunked prefill: per (query head, visible token) the score (d MACs,
+    plus m for a QJL key sketch) and the readout (d MACs, plus m for a QJL value sketch)."""
+    from turboquant_quantized_kv_tq_gb300.binding import SCHEMES as S, tq_config, tq_config_from_scheme
+    c = tq_config()
+    tq_config_from_scheme(S[scheme], n, c)
+    macs = 2 * d + (m if c.k.qjl else 0) + (m if c.v.qjl else 0)
+    visible = sum(max(0, L - nq + 1 + i) for i in range(nq))
+    return 2.0 * macs * B * Hq * visible
+
+
+def run_prefill(args, caches, inp, device, T, nq=512):
+    """Chunked prefill over the headline caches: the last nq = 512 positions of each sequence as
+    queries (G = 4 query heads per KV head: 2048 rows per KV head), each attending causally to its
+    prefix of the T = 32768 stored tokens.  CUDA events over 5 calls per scheme."""
+    import torch
+    rng = np.random.default_rng(9)
+    q = torch.from_numpy(rng.standard_normal((inp.B, nq, inp.Hq, inp.d)).astype(np.float32)).to(device)
+    out = torch.empty_like(q)
+    peak, peak_kind = measured_tensor_peak()
+    res, tot_flops, tot_s = {}, 0.0, 0.0
+    for (scheme, n), kv in zip(SCHEMES, caches):
+        ws = torch.empty(kv.prefill_workspace_bytes(nq), dtype=torch.uint8, device=device)
+        for _ in range(2):
+            kv.prefill(q, [T] * inp.B, out=out, ws=ws)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record()
+        for _ in range(reps):
+            kv.prefill(q, [T] * inp.B, out=out, ws=ws)
+        e1.record()
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / reps
+        fl = prefill_flops(scheme, n, inp.B, inp.Hq, nq, T)
+        tot_flops += fl
+        tot_s += ms * 1e-3
+        res[f"{scheme}{n}"] = {"ms": round(ms, 3), "query_tokens_per_s": round(inp.B * nq / (ms * 1e-3), 1),
+                               "TFLOP_per_s": round(fl / (ms * 1e-3) / 1e12, 1),
+                               "frac": round(fl / (ms * 1e-3) / 1e12 / peak, 4)}
+        del ws
+    achieved = tot_flops / tot_s / 1e12
+    return {"workload": f"chunked prefill: B={inp.B} Hq={inp.Hq} Hkv={inp.Hkv} d={inp.d}, the last {nq} of "
+                        f"{T} positions as queries (causal within the chunk), the headline caches",
+            "timing": "CUDA events, 5 calls per scheme (query prep + prefill kernel)",
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "flops": "per (query head, visible token): 2 x (2 d + m per QJL side) -- the "
+                                  "method's score and readout contractions, the fp16 lo terms not counted",
+                         "kernel": "prefill (query prep + fused prefill kernel), all four schemes",
+                         "peak_kind": peak_kind + " (bf16 dense, burst; fp16 MMAs run at the bf16 rate)"},
+            "schemes": res}
 
 
 def run_long_context(args, device):
@@ -731,6 +799,7 @@ def main():
                     help="--impl reference: approximate time of the timed steps")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-append", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true", help="leave out the chunked-prefill leg")
     ap.add_argument("--skip-long-context", action="store_true",
                     help="leave out the 128k-context (cfg4) decode leg")
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")

@@ -226,6 +226,25 @@ tq_status tq_decode_attention_multi(const tq_context* ctx, const void* dev_cache
                                     int32_t nq, const int32_t* host_seq_len, float* out, void* ws,
                                     size_t ws_bytes, tq_stream stream);
 
+/* Chunked-prefill attention ([ABL] "Recomendações Práticas" 2 names prefill workloads): the
+ * same result as tq_decode_attention_multi -- the nq queries of sequence b are the chunk's last
+ * nq positions, already appended, and query i attends causally to the first
+ * host_seq_len[b] - nq + 1 + i tokens (none when that is <= 0: output zeros) -- for chunks of any
+ * size.  The (query, head) rows of a KV head are taken 128 at a time; each 32-token tile of the
+ * packed cache is unpacked once per 128 rows into shared memory and both products (scores and
+ * value readout) run as dense fp16 tensor-core MMAs with fp32 accumulation, the queries split
+ * into fp16 hi + lo terms.  q, out: device fp32 [B][nq][H_q][d] (16-byte aligned).  ws: device
+ * workspace of at least tq_prefill_workspace_bytes(ctx, nq) bytes (an error word, then the
+ * rotated queries as fp16 terms), 256-byte aligned, owned by the call until it completes on
+ * stream; tq_get_device_error(ws, ...) reads the error word (a bounded copy wait that gave up).  Built for head dim
+ * 128 (m = 128), every Plain / TQ-KV / KQV / QKQV codec pair and any G = H_q / H_kv; HeadQ and
+ * spectral codecs, or more than 65535 (batch, KV head) slabs, give TQ_ERR_UNSUPPORTED.  Errors
+ * are detected on the host before any launch. */
+size_t tq_prefill_workspace_bytes(const tq_context* ctx, int32_t nq);
+tq_status tq_prefill_attention(const tq_context* ctx, const void* dev_cache, const float* q, int32_t nq,
+                               const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
+                               tq_stream stream);
+
 /* Size of the library's built-in decode scratch (see tq_decode_attention_static). */
 #define TQ_STATIC_SCRATCH_BYTES (8u << 20)
 

@@ -153,6 +153,26 @@ class QuantizedKVCache(_Codec):
                                            _stream_handle(stream)))
         return out
 
+    def prefill(self, q, seq_len, out=None, ws=None, stream=None):
+        """Chunked-prefill attention.  q: float32 CUDA tensor [batch][nq][num_q_heads][head_dim], the
+        chunk's last nq positions (already appended); query i attends to the first
+        seq_len[b] - nq + 1 + i tokens.  ``ws``: optional uint8 CUDA workspace of at least
+        prefill_workspace_bytes(nq) bytes (allocated here otherwise)."""
+        import torch
+        q = q.contiguous()
+        nq = int(q.shape[1])
+        if out is None:
+            out = torch.empty_like(q)
+        need = self.prefill_workspace_bytes(nq)
+        if ws is None:
+            ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        check(_b.tq_prefill_attention(self._ctx, self.cache.data_ptr(), q.data_ptr(), nq, _b.int_array(seq_len),
+                                      out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream)))
+        return out
+
+    def prefill_workspace_bytes(self, nq):
+        return int(_b.tq_prefill_workspace_bytes(self._ctx, int(nq)))
+
     def logits(self, q, seq_len, stride=None, stream=None):
         """Corrected scores [batch][num_q_heads][stride] (entries past seq_len[b] are untouched: 0)."""
         import torch

@@ -392,6 +392,35 @@ tq_status tq_decode_attention_multi(const tq_context* ctx, const void* dev_cache
   return launch_decode_multi(ctx, dev_cache, q, nq, host_seq_len, out, ws, ws_bytes, stream);
 }
 
+size_t tq_prefill_workspace_bytes(const tq_context* ctx, int32_t nq) {
+  if (!ctx || nq < 1) return 0;
+  return prefill_workspace_bytes(ctx, nq);
+}
+
+tq_status tq_prefill_attention(const tq_context* ctx, const void* dev_cache, const float* q, int32_t nq,
+                               const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
+                               tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (!dev_cache || !q || !host_seq_len || !out || !ws) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (nq < 1) return fail(TQ_ERR_INVALID_ARG, "nq must be >= 1");
+  if (ctx->cfg.head_dim != 128 || ctx->m != 128)
+    return fail(TQ_ERR_UNSUPPORTED, "prefill attention is built for head_dim 128 (m = 128)");
+  if (ctx->cfg.headq_rank || ctx->cfg.k.rotate == 2 || ctx->cfg.v.rotate == 2)
+    return fail(TQ_ERR_UNSUPPORTED, "prefill attention is not built for HeadQ or spectral codecs");
+  if ((int64_t)ctx->cfg.batch * ctx->cfg.num_kv_heads > 65535)
+    return fail(TQ_ERR_UNSUPPORTED, "prefill attention takes at most 65535 (batch, KV head) slabs");
+  if ((int64_t)nq * (ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads) > (int64_t)1 << 24)
+    return fail(TQ_ERR_INVALID_ARG, "nq too large");
+  if (!aligned(dev_cache, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 256))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer (cache/ws 256 B, q/out 16 B)");
+  int max_seq;
+  s = check_lengths(ctx, host_seq_len, &max_seq);
+  if (s != TQ_OK) return s;
+  if (ws_bytes < prefill_workspace_bytes(ctx, nq)) return fail(TQ_ERR_WORKSPACE, "workspace too small");
+  return launch_prefill(ctx, dev_cache, q, nq, host_seq_len, out, ws, stream);
+}
+
 tq_status tq_decode_attention_static(const tq_context* ctx, const void* dev_cache, const float* q,
                                      const int32_t* host_seq_len, float* out, tq_stream stream) {
   tq_status s = ready(ctx);

@@ -65,7 +65,7 @@ struct tq_context {
   bool sq_set[2] = {false, false};  // spectral sides: basis stored
 };
 
-// Launchers (tq_append.cu, tq_decode.cu).  They assume validated arguments.
+// Launchers (tq_append.cu, tq_decode.cu, tq_prefill.cu).  They assume validated arguments.
 namespace tqi {
 typedef struct CUstream_st* Stream;
 tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
@@ -87,6 +87,9 @@ tq_status launch_decode_paged(const tq_context* ctx, const void* pool, const tq_
 tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
                         const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
                         Stream stream);
+size_t prefill_workspace_bytes(const tq_context* ctx, int nq);
+tq_status launch_prefill(const tq_context* ctx, const void* cache, const float* q, int nq,
+                         const int32_t* seq_len, float* out, void* ws, Stream stream);
 tq_status launch_logits(const tq_context* ctx, const void* cache, const float* q,
                         const int32_t* seq_len, float* logits, int stride, Stream stream);
 tq_status read_device_error(const void* ws, int32_t* code, Stream stream);
