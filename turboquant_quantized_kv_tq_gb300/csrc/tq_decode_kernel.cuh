@@ -328,7 +328,37 @@ struct Bits16 {
     a[2] = signed_pair(a[2], x23 << (15 - 2 * mt));
     a[3] = signed_pair(a[3], x23 << (14 - 2 * mt));
   }
+  // The bits of dims 16 lg + 2 mt (+1) as masked operands.  A word holds the bit of dim offset k
+  // at k (first token) and k + 16 (second token).  Shifted left by s(k) = 0 (k >= 10), 6 (k >= 4)
+  // or 12 (k < 4) -- three shifted copies of the word serve all 16 dims -- it sits at
+  // pos(k) = k + s(k) in [10, 15], and masking it there gives an fp16 number 0 or 2^e(pos), all
+  // normal (tensor cores flush subnormal inputs): 2^-14, 2^-13, 2^-11, 2^-7, 2^1 for pos 10 .. 14.
+  // The readout's row k is then 2^e sum_j w_j sigma_j, and sum_j w_j (2 sigma_j - 1) =
+  // 2 2^-e row - sum_j w_j.  pos 15 is the fp16 sign: those dims (k = 3, 9, 15) take +-1 instead.
+  // One LOP3 per operand plus two shifts per word, where moving each bit to the sign position
+  // takes a shift and a LOP3 per operand.
+  __device__ __forceinline__ static uint32_t mask_bit(uint32_t x, int k) {
+    const int sft = k >= 10 ? 0 : (k >= 4 ? 6 : 12), pos = k + sft;
+    const uint32_t y = x << sft;
+    // (a set bit is sigma = 1: +1, so the sign field takes the complement)
+    return pos == 15 ? ((~y & 0x80008000u) | 0x3C003C00u) : (y & (0x00010001u << pos));
+  }
+  __device__ __forceinline__ void mask(int mt, uint32_t (&a)[4]) const {
+    a[0] = mask_bit(x01, 2 * mt);
+    a[1] = mask_bit(x01, 2 * mt + 1);
+    a[2] = mask_bit(x23, 2 * mt);
+    a[3] = mask_bit(x23, 2 * mt + 1);
+  }
 };
+
+// Whether dim offset k's masked operand is +-1 (its bit lands on the fp16 sign) rather than
+// sigma 2^e, and 2^-e for the others (Bits16::mask_bit).
+__device__ __forceinline__ bool mask_is_pm1(int k) { return k == 3 || k == 9 || k == 15; }
+__device__ __forceinline__ float mask_unscale(int k) {
+  const int pos = k + (k >= 10 ? 0 : (k >= 4 ? 6 : 12));
+  const int e = pos == 10 ? -14 : pos == 11 ? -13 : pos == 12 ? -11 : pos == 13 ? -7 : 1;
+  return __int_as_float((127 - e) << 23);
+}
 
 // 3-bit values: as on the key side the two sign bits join the magnitude nibble in the table
 // index.  After shuffle_halves, byte j of a sign word holds dims 4 j .. 4 j + 3 of the two tokens
@@ -375,6 +405,8 @@ struct VChunk<1> {
     a[0] = a[1] = a[2] = a[3] = m0;
     sg.apply(mt, a);
   }
+  // sign bits as masked operands (Bits16::mask); the centroid magnitude is applied at the merge
+  __device__ __forceinline__ void frag_mask(int mt, uint32_t (&a)[4]) const { sg.mask(mt, a); }
 };
 
 // SQU-KV value chunk: dims 16 lg .. 16 lg + 3 of the group are modeled.  m[0] holds the 4-bit
@@ -416,6 +448,7 @@ struct VSign {
     a[0] = a[1] = a[2] = a[3] = 0x3C003C00u;
     sg.apply(mt, a);
   }
+  __device__ __forceinline__ void frag_mask(int mt, uint32_t (&a)[4]) const { sg.mask(mt, a); }
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -714,6 +747,12 @@ __device__ __forceinline__ void key_scores(TileData<KB, KQ, KH, VB, VQ>& d, floa
 }
 
 constexpr float kMaxFloor = -1e30f;
+// The running maximum is raised only when a score exceeds it by more than this (log2 units), so
+// the weights 2^(s - m) stay below 2^3 between raises.  Most tiles then skip the column max
+// reduction and the accumulator rescale (with eight query columns a warp otherwise raised some
+// column's maximum on most tiles).  The value operands p nu stay fp16: value norms up to
+// 65504 / 8.
+constexpr float kRescaleSlack = 3.f;
 
 // Per-warp running state.
 template <bool VQ>
@@ -723,11 +762,16 @@ struct WarpState {
   // instead of exp2(-inf + inf)
   float m0, m1;
   float l0, l1;  // this thread's partial softmax denominators
+  // weight sums of the masked sign operands per column 2 lt, 2 lt + 1 (Bits16::mask): [0] the
+  // code readout of 1-bit value codes, [1] the value sketch; with the sketch readout packed into
+  // the value MMA, [0] holds a sketch column's sum
+  float w[2][2];
   float acc[8][4];
   float accs[VQ ? 8 : 1][4];
   __device__ __forceinline__ void reset() {
     m0 = m1 = kMaxFloor;
     l0 = l1 = 0.f;
+    w[0][0] = w[0][1] = w[1][0] = w[1][1] = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -737,6 +781,11 @@ struct WarpState {
       }
   }
 };
+
+// The two fp16 halves of a packed pair as floats (low, high).
+__device__ __forceinline__ float2 half2_floats(uint32_t h) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
 
 // 2^x on the special-function unit (inputs here are <= 0; -inf gives 0).
 __device__ __forceinline__ float ex2(float x) {
@@ -756,7 +805,9 @@ __device__ __forceinline__ float ex2(float x) {
 // sketch readout.  One MMA then takes the 8 tokens of a score-row half twice along k, codes
 // then signs, against a B operand holding p nu in the code columns of the first half and
 // p nu rho in the sketch columns of the second.  Both readouts share one accumulator.
-template <int NT, bool MASK, bool PK = false, int KB, bool KQ, bool KH, int VB, bool VQ>
+// MV: the value sketch's sign bits (and 1-bit value codes) enter as masked operands
+// (Bits16::mask), with their weight sums kept in st.w for the merge.
+template <int NT, bool MASK, bool PK = false, bool MV = false, int KB, bool KQ, bool KH, int VB, bool VQ>
 __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d)[2], float (&s)[NT][4],
                                                 WarpState<VQ && !PK>& st, uint32_t lxV, uint32_t v_m0, int t0,
                                                 int end, int lmin, int G, int Gc, int lg) {
@@ -779,9 +830,9 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
   }
 
   // ---- online softmax (log2 domain).  A column's maximum over the tiles exceeds its running
-  // maximum exactly when some lane's own maximum does, so the max-reduction across the lanes of
-  // a column (and the rescale) runs only on tiles that raise a maximum; elsewhere the running
-  // maximum is already the new one.
+  // maximum (plus the slack) exactly when some lane's own maximum does, so the max-reduction
+  // across the lanes of a column (and the rescale) runs only on tiles that raise a maximum by
+  // more than kRescaleSlack; elsewhere the running maximum stays the reference of the weights.
   float mx0 = fmaxf(s[0][0], s[0][2]), mx1 = fmaxf(s[0][1], s[0][3]);
 #pragma unroll
   for (int j = 1; j < NT; ++j) {
@@ -789,7 +840,7 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
     mx1 = fmaxf(mx1, fmaxf(s[j][1], s[j][3]));
   }
   float n0 = st.m0, n1 = st.m1;
-  if (__any_sync(kFull, mx0 > st.m0 || mx1 > st.m1)) {
+  if (__any_sync(kFull, mx0 > st.m0 + kRescaleSlack || mx1 > st.m1 + kRescaleSlack)) {
 #pragma unroll
     for (int m = 4; m <= 16; m <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, m));
@@ -800,6 +851,10 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
     const float a0 = ex2(st.m0 - n0), a1 = ex2(st.m1 - n1);
     st.l0 *= a0;
     st.l1 *= a1;
+    if constexpr (MV) {
+      st.w[0][0] *= a0; st.w[1][0] *= a0;
+      st.w[0][1] *= a1; st.w[1][1] *= a1;
+    }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       st.acc[mt][0] *= a0; st.acc[mt][1] *= a1; st.acc[mt][2] *= a0; st.acc[mt][3] *= a1;
@@ -823,45 +878,70 @@ __device__ __forceinline__ void softmax_readout(TileData<KB, KQ, KH, VB, VQ> (&d
     if constexpr (PK) {
       const bool c0 = lt2 < Gc, c1 = lt2 + 1 < Gc;  // code columns (else sketch columns)
       const float fA = va[j] ? d[j].nuVA * d[j].rhoVA : 0.f, fB = vb[j] ? d[j].nuVB * d[j].rhoVB : 0.f;
-      const uint32_t cA = movmatrix_trans(pack_half2(c0 ? p0 * nA : 0.f, c1 ? p1 * nA : 0.f));
-      const uint32_t sA = movmatrix_trans(pack_half2(c0 ? 0.f : p0 * fA, c1 ? 0.f : p1 * fA));
-      const uint32_t cB = movmatrix_trans(pack_half2(c0 ? p2 * nB : 0.f, c1 ? p3 * nB : 0.f));
-      const uint32_t sB = movmatrix_trans(pack_half2(c0 ? 0.f : p2 * fB, c1 ? 0.f : p3 * fB));
+      const uint32_t hcA = pack_half2(c0 ? p0 * nA : 0.f, c1 ? p1 * nA : 0.f);
+      const uint32_t hsA = pack_half2(c0 ? 0.f : p0 * fA, c1 ? 0.f : p1 * fA);
+      const uint32_t hcB = pack_half2(c0 ? p2 * nB : 0.f, c1 ? p3 * nB : 0.f);
+      const uint32_t hsB = pack_half2(c0 ? 0.f : p2 * fB, c1 ? 0.f : p3 * fB);
+      if constexpr (MV) {
+        // one sum per column (the code readout's for 1-bit codes, or the sketch's), of the fp16
+        // weights the MMA multiplies: a rounding common to all of a column's dims would
+        // otherwise survive the 2 sum - W step and the inverse rotation gathers it into one
+        // output coordinate
+        const float2 a = half2_floats(VB == 1 ? (hcA | hsA) : hsA), bb = half2_floats(VB == 1 ? (hcB | hsB) : hsB);
+        st.w[0][0] += a.x + bb.x;
+        st.w[0][1] += a.y + bb.y;
+      }
+      const uint32_t cA = movmatrix_trans(hcA), sA = movmatrix_trans(hsA);
+      const uint32_t cB = movmatrix_trans(hcB), sB = movmatrix_trans(hsB);
       d[j].v.prepare();
       d[j].vs.prepare();
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t a[4], g[4];
-        d[j].v.frag(lxV, v_m0, mt, a);
-        d[j].vs.frag(mt, g);
+        if constexpr (MV && VB == 1) d[j].v.frag_mask(mt, a); else d[j].v.frag(lxV, v_m0, mt, a);
+        if constexpr (MV) d[j].vs.frag_mask(mt, g); else d[j].vs.frag(mt, g);
         mma16816(st.acc[mt], a[0], a[1], g[0], g[1], cA, sA);
         mma16816(st.acc[mt], a[2], a[3], g[2], g[3], cB, sB);
       }
       continue;
     }
-    const uint32_t bv0 = movmatrix_trans(pack_half2(p0 * nA, p1 * nA));
-    const uint32_t bv1 = movmatrix_trans(pack_half2(p2 * nB, p3 * nB));
+    const uint32_t hv0 = pack_half2(p0 * nA, p1 * nA), hv1 = pack_half2(p2 * nB, p3 * nB);
+    if constexpr (MV && VB == 1) {  // sums of the fp16 weights the MMA multiplies
+      const float2 a = half2_floats(hv0), bb = half2_floats(hv1);
+      st.w[0][0] += a.x + bb.x;
+      st.w[0][1] += a.y + bb.y;
+    }
+    const uint32_t bv0 = movmatrix_trans(hv0), bv1 = movmatrix_trans(hv1);
     d[j].v.prepare();
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t a[4];
-      d[j].v.frag(lxV, v_m0, mt, a);
+      if constexpr (MV && VB == 1) d[j].v.frag_mask(mt, a); else d[j].v.frag(lxV, v_m0, mt, a);
       mma16816(st.acc[mt], a[0], a[1], a[2], a[3], bv0, bv1);
     }
     if constexpr (VQ && !PK) {
       const float fa = va[j] ? d[j].nuVA * d[j].rhoVA : 0.f, fb = vb[j] ? d[j].nuVB * d[j].rhoVB : 0.f;
-      const uint32_t bs0 = movmatrix_trans(pack_half2(p0 * fa, p1 * fa));
-      const uint32_t bs1 = movmatrix_trans(pack_half2(p2 * fb, p3 * fb));
+      const uint32_t hs0 = pack_half2(p0 * fa, p1 * fa), hs1 = pack_half2(p2 * fb, p3 * fb);
+      if constexpr (MV) {
+        const float2 a = half2_floats(hs0), bb = half2_floats(hs1);
+        st.w[1][0] += a.x + bb.x;
+        st.w[1][1] += a.y + bb.y;
+      }
+      const uint32_t bs0 = movmatrix_trans(hs0), bs1 = movmatrix_trans(hs1);
       d[j].vs.prepare();
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t a[4];
-        d[j].vs.frag(mt, a);
+        if constexpr (MV) d[j].vs.frag_mask(mt, a); else d[j].vs.frag(mt, a);
         mma16816(st.accs[mt], a[0], a[1], a[2], a[3], bs0, bs1);
       }
     }
   }
 }
+
+// Value sides whose sign bits the head-dim-128 decode reads as masked operands: a QJL sketch, or
+// 1-bit codes.
+template <int VB, bool VQ> struct kMaskedValues { static constexpr bool value = VQ || VB == 1; };
 
 // Scores and online-softmax step of NT consecutive tiles held by one warp (head dim 128).
 template <int NT, bool MASK, bool QLO, int KB, bool KQ, bool KH, int VB, bool VQ>
@@ -876,7 +956,8 @@ __device__ __forceinline__ void compute_tiles(TileData<KB, KQ, KH, VB, VQ> (&d)[
 #pragma unroll
   for (int j = 0; j < NT; ++j)
     key_scores<QLO>(d[j], s[j], qf, qs, qu, lxK, k_m0, p.qjl_scale, p.score_scale, qfl, qsl, p.lo_xor);
-  softmax_readout<NT, MASK, VQ && !QLO>(d, s, st, lxV, v_m0, t0, end, lmin, p.G, p.Gc, lg);
+  softmax_readout<NT, MASK, VQ && !QLO, kMaskedValues<VB, VQ>::value>(d, s, st, lxV, v_m0, t0, end, lmin, p.G,
+                                                                   p.Gc, lg);
 }
 
 // Placement of N equal regions of RS bytes around the code tables, in shared-window addresses:
@@ -904,6 +985,8 @@ struct RegionPlan {
   }
 };
 
+constexpr uint32_t kSkA = 4096;  // byte offset of a column's merged acc_sk in its warp's region
+
 // Shared-memory plan of a decode block: per-warp regions (the warp's bulk-copy ring, later its
 // merge slot) placed by RegionPlan, then one mbarrier per pair stage and warp.
 // A value codebook other than the key one gets its own table in the upper half (bytes 128 .. 255)
@@ -921,6 +1004,9 @@ struct DecodeSmem {
   static constexpr uint32_t RS = ring > mslot ? ring : mslot;
   using Plan = RegionPlan<lutK, 0, RS, NW>;
   static constexpr uint32_t bars = Plan::bars;
+  // the slab merge of a QJL value side: per-column partial sketch products at the start of each
+  // warp's region, the merged acc_sk of column h at kSkA in warp h's region
+  static_assert(!VQ || (RS >= kSkA + 4 * kDecD && kHeadsPad * kDecD * 4 <= kSkA), "merge scratch");
   static constexpr uint32_t bytes = bars + NW * kPairStages * 8;
   __host__ __device__ static constexpr uint32_t region(int w) { return Plan::region(w); }
 };
@@ -1127,11 +1213,22 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     seq += npairs;
 
     // ---- merge the warps of this block for this segment
+    constexpr bool MV = kMaskedValues<VB, VQ>::value;
     float l0 = st.l0, l1 = st.l1;
+    constexpr bool PKD = VQ && !QLO;  // the sketch readout rides in the value MMA
+    float w00 = st.w[0][0], w01 = st.w[0][1], w10 = st.w[1][0], w11 = st.w[1][1];
 #pragma unroll
     for (int m = 4; m <= 16; m <<= 1) {
       l0 += __shfl_xor_sync(kFull, l0, m);
       l1 += __shfl_xor_sync(kFull, l1, m);
+      if constexpr (MV) {
+        w00 += __shfl_xor_sync(kFull, w00, m);
+        w01 += __shfl_xor_sync(kFull, w01, m);
+        if constexpr (!PKD) {
+          w10 += __shfl_xor_sync(kFull, w10, m);
+          w11 += __shfl_xor_sync(kFull, w11, m);
+        }
+      }
     }
     __syncthreads();  // every warp is done with its stages: reuse them for the merge
     float* mb = reinterpret_cast<float*>(my_stages);
@@ -1140,6 +1237,23 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
       mb[(2 * lt) * PS + 1] = l0;
       mb[(2 * lt + 1) * PS + 0] = st.m1;
       mb[(2 * lt + 1) * PS + 1] = l1;
+      if constexpr (MV) {
+        // slot offsets 2 / 3: the code readout's and the value sketch's weight sums; with a
+        // packed sketch readout a sketch column (Gc <= c < 2 Gc) files its sum under c - Gc
+        const int cc[2] = {2 * lt, 2 * lt + 1};
+        const float wc[2] = {w00, w01}, ws[2] = {w10, w11};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c = cc[k];
+          if (PKD) {
+            if (c < Gc) mb[c * PS + 2] = wc[k];
+            else if (c < 2 * Gc) mb[(c - Gc) * PS + 3] = wc[k];
+          } else {
+            mb[c * PS + 2] = wc[k];
+            mb[c * PS + 3] = ws[k];
+          }
+        }
+      }
     }
     // accumulator of column c: the code readout of slot c, or with a packed sketch readout
     // (Gc <= c < 2 Gc) the sketch readout of slot c - Gc
@@ -1172,7 +1286,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
       float v;
       if (e == 0) {
         v = M;
-      } else if (e == 2 || e == 3) {
+      } else if (!MV && (e == 2 || e == 3)) {
         v = 0.f;
       } else {
         v = 0.f;
@@ -1199,50 +1313,123 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     __syncthreads();
     if (s_last) {
       __threadfence();
+      // (1) warp h < Gc merges query column h's partials; with a QJL value side the merged
+      // acc_sk goes to shared memory for (2)
+      const int h = warp;  // query column
+      float L2 = 0.f;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
       if (warp < Gc) {
-        const int h = warp;  // query column
         const long long sstride = (long long)Gc * PS;
         const float* base = p.part + (long long)(pair + c_first) * sstride + h * PS;
         const int ns = c_last - c_first + 1;
         float M = -INFINITY;
-        for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride));
-        float L2 = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accs = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-          for (int s = 0; s < ns; ++s) {
-            const float* ps = base + s * sstride;
-            const float w = exp2f(__ldcg(ps) - M);
-            L2 = fmaf(w, __ldcg(ps + 1), L2);
-            const float4 a = __ldcg(reinterpret_cast<const float4*>(ps + 4 + 4 * lane));
-            acc.x = fmaf(w, a.x, acc.x); acc.y = fmaf(w, a.y, acc.y);
-            acc.z = fmaf(w, a.z, acc.z); acc.w = fmaf(w, a.w, acc.w);
-            if constexpr (VQ) {
-              const float4 c = __ldcg(reinterpret_cast<const float4*>(ps + 4 + kDecD + 4 * lane));
-              accs.x = fmaf(w, c.x, accs.x); accs.y = fmaf(w, c.y, accs.y);
-              accs.z = fmaf(w, c.z, accs.z); accs.w = fmaf(w, c.w, accs.w);
+        float Wc = 0.f, Ws = 0.f;  // weight sums of the masked operands (MV)
+        if constexpr (MV) {
+          // the partials' maxima, denominators and weight sums are read lane-parallel (lane s
+          // takes partial s, 32 at a time): a slab spread over many blocks (long contexts, few
+          // slabs) would otherwise pay one dependent L2 round trip per partial
+          for (int s0 = 0; s0 < ns; s0 += 32)
+            if (s0 + lane < ns) M = fmaxf(M, __ldcg(base + (s0 + lane) * sstride));
+          M = warp_max(M);
+          if (M != -INFINITY) {
+            for (int s0 = 0; s0 < ns; s0 += 32) {
+              const int nn = min(32, ns - s0);
+              float wl = 0.f;
+              if (lane < nn) {
+                const float* ps = base + (s0 + lane) * sstride;
+                wl = exp2f(__ldcg(ps) - M);
+                L2 = fmaf(wl, __ldcg(ps + 1), L2);
+                Wc = fmaf(wl, __ldcg(ps + 2), Wc);
+                Ws = fmaf(wl, __ldcg(ps + 3), Ws);
+              }
+#pragma unroll 4
+              for (int i = 0; i < nn; ++i) {
+                const float w = __shfl_sync(kFull, wl, i);
+                const float* ps = base + (s0 + i) * sstride;
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(ps + 4 + 4 * lane));
+                acc.x = fmaf(w, a.x, acc.x); acc.y = fmaf(w, a.y, acc.y);
+                acc.z = fmaf(w, a.z, acc.z); acc.w = fmaf(w, a.w, acc.w);
+                if constexpr (VQ) {
+                  const float4 c = __ldcg(reinterpret_cast<const float4*>(ps + 4 + kDecD + 4 * lane));
+                  accs.x = fmaf(w, c.x, accs.x); accs.y = fmaf(w, c.y, accs.y);
+                  accs.z = fmaf(w, c.z, accs.z); accs.w = fmaf(w, c.w, accs.w);
+                }
+              }
+            }
+            L2 = warp_sum(L2);
+            Wc = warp_sum(Wc);
+            Ws = warp_sum(Ws);
+          }
+        } else {
+          for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(base + s * sstride));
+          if (M != -INFINITY) {
+            for (int s = 0; s < ns; ++s) {
+              const float* ps = base + s * sstride;
+              const float w = exp2f(__ldcg(ps) - M);
+              L2 = fmaf(w, __ldcg(ps + 1), L2);
+              const float4 a = __ldcg(reinterpret_cast<const float4*>(ps + 4 + 4 * lane));
+              acc.x = fmaf(w, a.x, acc.x); acc.y = fmaf(w, a.y, acc.y);
+              acc.z = fmaf(w, a.z, acc.z); acc.w = fmaf(w, a.w, acc.w);
             }
           }
         }
-        float o[4] = {acc.x, acc.y, acc.z, acc.w};
-        if constexpr (VQ) {
-          // o_rot += sqrt(pi/2)/m * S_V^T acc_sk
-          const float sv[4] = {accs.x, accs.y, accs.z, accs.w};
-          float corr[4] = {0.f, 0.f, 0.f, 0.f};
-          // the block waits for this product: keep many rows' loads in flight
-#pragma unroll 8
-          for (int r4 = 0; r4 < 32; ++r4) {
+        o[0] = acc.x; o[1] = acc.y; o[2] = acc.z; o[3] = acc.w;
+        if constexpr (MV) {
+          // masked operands: row k of a 16-dim group holds 2^e sum w sigma (the +-1 dims:
+          // sum w (2 sigma - 1)); turn it into sum w (2 sigma - 1), times the 1-bit centroid for
+          // value codes
+          float sk[4] = {accs.x, accs.y, accs.z, accs.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float ar = __shfl_sync(kFull, sv[i], r4);
-              const float4 srow =
-                  __ldg(reinterpret_cast<const float4*>(p.tab.S_V + (4 * r4 + i) * kDecD + 4 * lane));
-              corr[0] = fmaf(srow.x, ar, corr[0]); corr[1] = fmaf(srow.y, ar, corr[1]);
-              corr[2] = fmaf(srow.z, ar, corr[2]); corr[3] = fmaf(srow.w, ar, corr[3]);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int k = (4 * lane + e) & 15;
+            const float f2 = 2.f * mask_unscale(k);
+            const bool pm = mask_is_pm1(k);
+            if constexpr (VB == 1) o[e] = vc1 * (pm ? o[e] : fmaf(f2, o[e], -Wc));
+            if constexpr (VQ) sk[e] = pm ? sk[e] : fmaf(f2, sk[e], -Ws);
+          }
+          accs = make_float4(sk[0], sk[1], sk[2], sk[3]);
+        }
+        if constexpr (VQ)
+          *reinterpret_cast<float4*>(win + SM::region(h) + kSkA + 16 * lane) = accs;
+      }
+      if constexpr (VQ) {
+        // (2) o_rot += sqrt(pi/2)/m S_V^T acc_sk for every column: the warps split the m sketch
+        // rows, so each loads its rows of S_V once (all in flight) and applies them to every
+        // column; partial sums go to shared memory and (3) adds them up
+        __syncthreads();
+        constexpr int RPW = (kDecD + SM::NW - 1) / SM::NW;  // sketch rows per warp
+        const int j0 = warp * RPW;
+        float4 srow[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+          srow[r] = j0 + r < kDecD ? __ldg(reinterpret_cast<const float4*>(p.tab.S_V + (j0 + r) * kDecD + 4 * lane))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        float* part_sum = reinterpret_cast<float*>(win + SM::region(warp));
+        for (int c = 0; c < Gc; ++c) {
+          const float* a = reinterpret_cast<const float*>(win + SM::region(c) + kSkA);
+          float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int r = 0; r < RPW; ++r) {
+            const float ar = j0 + r < kDecD ? a[j0 + r] : 0.f;
+            t.x = fmaf(srow[r].x, ar, t.x); t.y = fmaf(srow[r].y, ar, t.y);
+            t.z = fmaf(srow[r].z, ar, t.z); t.w = fmaf(srow[r].w, ar, t.w);
+          }
+          *reinterpret_cast<float4*>(part_sum + c * kDecD + 4 * lane) = t;
+        }
+        __syncthreads();
+        if (warp < Gc) {  // (3)
+          float corr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int w = 0; w < SM::NW; ++w) {
+            const float4 t = *reinterpret_cast<const float4*>(win + SM::region(w) + (h * kDecD + 4 * lane) * 4);
+            corr[0] += t.x; corr[1] += t.y; corr[2] += t.z; corr[3] += t.w;
           }
 #pragma unroll
           for (int i = 0; i < 4; ++i) o[i] = fmaf(p.qjl_scale, corr[i], o[i]);
         }
+      }
+      if (warp < Gc) {
         const float invL = L2 > 0.f ? 1.f / L2 : 0.f;
         if constexpr (VB == kSQ) {
           // SQU-KV values: o = E (s acc) / l with the basis and scales of KV head kvh
