@@ -146,6 +146,14 @@ def test_host_rotation_and_sketch_bit_exact(seed):
     assert np.array_equal(f("S_V", d * d).reshape(d, d), SV)
     assert np.array_equal(f("S_V_T", d * d).reshape(d, d), SV.T)
     assert b.tq_tables_bytes(ctx) >= off["S_V_T"] + 4 * d * d
+    # the fp16 hi / lo rows of S_K then S_V (272-byte pitch) for the tensor-core sketch
+    start = (off["S_V_T"] + 4 * d * d + 255) // 256 * 256
+    for k, S in enumerate((SK, SV)):
+        o = start + k * ((2 * 128 * 136 * 2 + 255) // 256 * 256)
+        h16 = blob[o:o + 2 * 128 * 136 * 2].view(np.float16).reshape(2, 128, 136)
+        hi = S.astype(np.float16)
+        lo = (S - hi.astype(np.float32)).astype(np.float16)
+        assert np.array_equal(h16[0, :, :128], hi) and np.array_equal(h16[1, :, :128], lo)
     b.tq_context_destroy(ctx)
 
 

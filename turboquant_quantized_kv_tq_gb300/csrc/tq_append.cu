@@ -581,6 +581,243 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const Appen
   if (p.wait_primary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
+// ---- Large appends at head dim 128: four lanes per vector ----------------------------------
+// A warp encodes eight vectors at once: lane l takes vector l / 4 and its coordinates
+// [32 q, 32 q + 32), q = l % 4.  The rotation's first five butterfly stages run in registers and
+// only the last two cross lanes (within the four lanes of a vector); the norm and residual sums
+// reduce over those four lanes, and each lane's codes form whole words of the packed record.
+// The stages run in the order and with the arithmetic of encode_vectors (butterflies over
+// coordinate bits 0 .. 6), so the rotated values, and with them the codes, are the same.
+constexpr int kQE = 32;  // coordinates per lane
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(kFull, v, 1);
+  return v + __shfl_xor_sync(kFull, v, 2);
+}
+
+// norm_compensated over the four lanes of a vector (their first lane's result in all four).
+// EXACT_SQ: the squares are exact in fp32 (16-bit inputs: at most 22 significant bits), so the
+// product error term, fma(x, x, -x x), is zero and is left out.
+template <bool EXACT_SQ>
+__device__ __forceinline__ float norm_compensated_quad(const float (&x)[kQE]) {
+  float S = 0.f, C = 0.f;
+#pragma unroll
+  for (int i = 0; i < kQE; ++i) {
+    const float pr = x[i] * x[i];
+    const float pe = EXACT_SQ ? 0.f : fmaf(x[i], x[i], -pr);
+    float s, e;
+    two_sum(S, pr, s, e);
+    S = s;
+    C += e + pe;
+  }
+#pragma unroll
+  for (int m = 2; m >= 1; m >>= 1) {
+    const float So = __shfl_xor_sync(kFull, S, m);
+    const float Co = __shfl_xor_sync(kFull, C, m);
+    float s, e;
+    two_sum(S, So, s, e);
+    S = s;
+    C = (C + Co) + e;
+  }
+  const int q0 = (threadIdx.x & 31) & ~3;
+  S = __shfl_sync(kFull, S, q0);
+  C = __shfl_sync(kFull, C, q0);
+  if (S <= 0.f) return 0.f;
+  const float r = sqrtf(S);
+  const float res = fmaf(-r, r, S) + C;
+  return r + res / (2.f * r);
+}
+
+// norm_split for a vector held by four lanes (see norm_split).  The shuffles run in every lane
+// of the warp: a vector that needs the rescale makes the whole warp take that branch.
+template <bool EXACT_SQ>
+__device__ __forceinline__ float norm_split_quad(float (&x)[kQE], float& nu_work, float& pw) {
+  const float nu = norm_compensated_quad<EXACT_SQ>(x);  // the same value in the vector's four lanes
+  pw = 1.f;
+  nu_work = nu;
+  const bool fast = nu >= 0x1p-30f && nu < 0x1p50f;
+  if (__all_sync(kFull, fast)) return nu;
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < kQE; ++i) m = fmaxf(m, fabsf(x[i]));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+  const bool rescale = !fast && m > 0.f;
+  const int e = rescale ? max(-126, min(126, ((__float_as_int(m) >> 23) & 0xFF) - 127)) : 0;
+  if (rescale) {
+    const float down = __int_as_float((127 - e) << 23);
+#pragma unroll
+    for (int i = 0; i < kQE; ++i) x[i] *= down;
+  }
+  const float nu2 = norm_compensated_quad<EXACT_SQ>(x);
+  if (fast) return nu;
+  if (!rescale) {
+    nu_work = 0.f;
+    return 0.f;
+  }
+  pw = __int_as_float((127 + e) << 23);
+  nu_work = nu2;
+  return nu2 * pw;
+}
+
+// Walsh-Hadamard butterflies of a vector held as 32 consecutive coordinates per lane by four
+// lanes: stages over coordinate bits 0 .. 4 in registers, bits 5 and 6 by lane shuffles.
+__device__ __forceinline__ void wht_quad(float (&x)[kQE]) {
+#pragma unroll
+  for (int hb = 1; hb < kQE; hb <<= 1) {
+#pragma unroll
+    for (int i = 0; i < kQE; ++i) {
+      if ((i & hb) == 0) {
+        const float a = x[i], b = x[i + hb];
+        x[i] = a + b;
+        x[i + hb] = a - b;
+      }
+    }
+  }
+  const int q = threadIdx.x & 3;
+#pragma unroll
+  for (int m = 1; m < 4; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < kQE; ++i) {
+      const float other = __shfl_xor_sync(kFull, x[i], m);
+      x[i] = (q & m) ? (other - x[i]) : (x[i] + other);
+    }
+  }
+}
+
+// One vector per four lanes through the write path ([TQ-KV] "Esquemas de Cuantización"):
+// norm, rotation, scalar code, code and norm stores, and on a QJL side the residual (left in
+// res) and its fp16 norm.  Sides without a HeadQ side code and not spectral.  An invalid vector
+// (the same in its four lanes) is neither loaded nor stored and leaves res = 0.
+template <typename Tin, int BITS>
+__device__ __forceinline__ void encode_quad(const AppendParams& p, int side, int b, int h, int j, int t,
+                                            bool valid, float (&res)[kQE]) {
+  constexpr int D = 128;
+  const int q = threadIdx.x & 3;
+  constexpr int bits = BITS;
+  const bool rotate = p.rotate[side] != 0;
+  const float* sgn = side ? p.tab.v_sign : p.tab.k_sign;
+  const float* cent = side ? p.tab.v_c : p.tab.k_c;
+  const float* thr = side ? p.tab.v_t : p.tab.k_t;
+  const Tin* base = reinterpret_cast<const Tin*>(side ? p.v : p.k);
+  float x[kQE];
+  if (valid) {
+    load_row<kQE>(base + ((long long)(b * p.Hkv + h) * p.n_new + j) * D + kQE * q, x);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kQE; ++i) x[i] = 0.f;
+  }
+  float nw, pw;
+  const float nu = norm_split_quad<!std::is_same<Tin, float>::value>(x, nw, pw);
+#pragma unroll
+  for (int i = 0; i < kQE; i += 4) {
+    const float4 s4 = __ldg(reinterpret_cast<const float4*>(sgn + kQE * q + i));
+    x[i] *= s4.x; x[i + 1] *= s4.y; x[i + 2] *= s4.z; x[i + 3] *= s4.w;
+  }
+  if (rotate) wht_quad(x);
+  const float scale = rotate ? sqrtf((float)D) : 1.f;
+  const float inv = nw > 0.f ? 1.f / (nw * scale) : 0.f;
+  // the sign-magnitude code of encode_vectors: s = [y > 0], the magnitude from the upper
+  // thresholds (-y >= t tested as nextup(-y) > t)
+  const uint32_t halfL = 1u << (bits - 1);
+  float tu[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) tu[k] = __ldg(thr + halfL + k);
+  uint32_t w4[4] = {0u, 0u, 0u, 0u}, w2[2] = {0u, 0u}, w1 = 0u;  // packed streams
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kQE; ++i) {
+    const float y = x[i] * inv;
+    const bool pos = y > 0.f;
+    const float a = pos ? y : __int_as_float(__float_as_int(-y) + 1);
+    // m = #{k : a > tu[k]} over the ascending tu[0..6] (unused slots 3e38), by binary search
+    const bool c4 = a > tu[3];
+    const bool c2 = a > (c4 ? tu[5] : tu[1]);
+    const bool c1 = a > (c4 ? (c2 ? tu[6] : tu[4]) : (c2 ? tu[2] : tu[0]));
+    const uint32_t m = (c4 ? 4u : 0u) | (c2 ? 2u : 0u) | (c1 ? 1u : 0u);
+    const uint32_t sb = pos ? 1u : 0u;
+    if constexpr (BITS == 4) w4[i >> 3] |= ((sb << 3) | m) << (4 * (i & 7));
+    if constexpr (BITS == 2) w2[i >> 4] |= ((sb << 1) | m) << (2 * (i & 15));
+    if constexpr (BITS == 3) w2[i >> 4] |= m << (2 * (i & 15));  // magnitudes; signs below
+    if constexpr (BITS == 3 || BITS == 1) w1 |= sb << i;
+    if (p.qjl[side]) {
+      const uint32_t code = pos ? halfL + m : halfL - 1u - m;
+      res[i] = valid ? y - __ldg(cent + code) : 0.f;
+      ss = fmaf(res[i], res[i], ss);
+    }
+  }
+  if (p.qjl[side]) ss = quad_sum(ss);  // (every lane: the shuffles take the whole warp)
+  if (!valid) return;
+  const Cache& C = p.cache;
+  if (side == 0) {  // key records, token-major: this lane's coordinates are bytes [4 q W, ..)
+    unsigned char* codes = C.ptr(tqi::R_K_CODES, b, h, t);
+    if (bits == 4) {
+      *reinterpret_cast<uint4*>(codes + 16 * q) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    } else if (bits == 3) {
+      *reinterpret_cast<uint2*>(codes + 8 * q) = make_uint2(w2[0], w2[1]);
+      *reinterpret_cast<uint32_t*>(codes + D / 4 + 4 * q) = w1;
+    } else if (bits == 2) {
+      *reinterpret_cast<uint2*>(codes + 8 * q) = make_uint2(w2[0], w2[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(codes + 4 * q) = w1;
+    }
+  } else {  // value streams by 16-coordinate groups 2 q and 2 q + 1 at block position pos
+    unsigned char* f = C.fieldp(tqi::R_V_CODES, b, h, t);
+    const int pos = t & (tqi::kTileTokens - 1);
+    const int g0 = 2 * q, g1 = 2 * q + 1;
+    if (bits == 4) {
+      *reinterpret_cast<uint2*>(f + g0 * 128 + pos * 8) = make_uint2(w4[0], w4[1]);
+      *reinterpret_cast<uint2*>(f + g1 * 128 + pos * 8) = make_uint2(w4[2], w4[3]);
+    } else if (bits == 3 || bits == 2) {
+      *reinterpret_cast<uint32_t*>(f + g0 * 64 + pos * 4) = w2[0];
+      *reinterpret_cast<uint32_t*>(f + g1 * 64 + pos * 4) = w2[1];
+      if (bits == 3) {
+        unsigned char* s1 = f + tqi::kTileTokens * (D / 4);
+        *reinterpret_cast<unsigned short*>(s1 + g0 * 32 + pos * 2) = (unsigned short)w1;
+        *reinterpret_cast<unsigned short*>(s1 + g1 * 32 + pos * 2) = (unsigned short)(w1 >> 16);
+      }
+    } else {
+      *reinterpret_cast<unsigned short*>(f + g0 * 32 + pos * 2) = (unsigned short)w1;
+      *reinterpret_cast<unsigned short*>(f + g1 * 32 + pos * 2) = (unsigned short)(w1 >> 16);
+    }
+  }
+  if (q == 0) *reinterpret_cast<float*>(C.ptr(side ? tqi::R_V_NORM : tqi::R_K_NORM, b, h, t)) = nu;
+  if (p.qjl[side] && q == 0)
+    *reinterpret_cast<__half*>(C.ptr(side ? tqi::R_V_RHO : tqi::R_K_RHO, b, h, t)) = __float2half_rn(sqrtf(ss));
+}
+
+template <typename Tin>
+__device__ __forceinline__ void encode_quad_bits(const AppendParams& p, int side, int b, int h, int j, int t,
+                                                 bool valid, float (&res)[kQE]) {
+  switch (p.bits[side]) {
+    case 4: encode_quad<Tin, 4>(p, side, b, h, j, t, valid, res); break;
+    case 3: encode_quad<Tin, 3>(p, side, b, h, j, t, valid, res); break;
+    case 2: encode_quad<Tin, 2>(p, side, b, h, j, t, valid, res); break;
+    default: encode_quad<Tin, 1>(p, side, b, h, j, t, valid, res); break;
+  }
+}
+
+// Sides of a large append at head dim 128 that carry no QJL sketch (a QJL side goes to
+// append_qjl_mma_kernel): 64 vectors per block of 8 warps, four lanes per vector.  As the
+// programmatic dependent of append_qjl_mma_kernel (wait_primary) it waits for that kernel
+// before exiting, as append_kernel does.
+template <typename Tin>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_quad_kernel(const AppendParams p) {
+  const int side = p.side_base + (int)blockIdx.y;
+  if (!(p.qjl[side] && p.qjl_mma)) {
+    const long long per_side = (long long)p.B * p.Hkv * p.n_new;
+    const long long v = (long long)blockIdx.x * (kWarpsPerBlock * 8) + (threadIdx.x >> 2);
+    const bool ok = v < per_side;
+    int b, h, j, t;
+    split_vec(p, ok ? v : 0, b, h, j, t);
+    float res[kQE];
+    encode_quad_bits<Tin>(p, side, b, h, j, t, ok, res);
+  }
+  if (p.wait_primary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+constexpr uint32_t kStageWaitLimit = 1u << 20;  // polls of a table copy's mbarrier
+
 // QJL sides of large appends at head dim 128: a block of kQjlWarps warps takes 64 vectors of one
 // side.  (1) Each warp runs 8 of them through encode_vector and keeps r, scaled by 256, in shared
 // memory as two fp16 terms (hi, lo = fp16(256 r - hi)).  (2) S r for the 64 vectors is a
@@ -616,7 +853,9 @@ __device__ __forceinline__ uint32_t spread4(uint32_t n) {
   return (n | (n << 1)) & 0x55u;
 }
 
-template <typename Tin>
+// BITS: the code width of the QJL side(s) as a compile-time constant (one encode variant in the
+// kernel's code), or 0 when two QJL sides differ (chosen at run time).
+template <typename Tin, int BITS>
 __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const AppendParams p) {
   constexpr int D = 128, E = 4;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -634,24 +873,47 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
   const long long per_side = (long long)p.B * p.Hkv * p.n_new;
   const long long v0 = (long long)blockIdx.x * kQjlBlockVec;
 
-  // ---- (0) S as fp16 hi / lo, and cleared flags
-  const float* S = side ? p.tab.S_V : p.tab.S_K;  // [m][d], S[i][j]
-  for (int idx = threadIdx.x * 4; idx < D * D; idx += blockDim.x * 4) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(S + idx));
-    const int i = idx / D, jj = idx % D;
-    const float xs[4] = {x.x, x.y, x.z, x.w};
-    __half hi[4], lo[4];
+  // ---- (0) S as fp16 hi / lo rows: the table blob holds them in this layout, so bulk copies
+  // bring them in while the vectors are encoded; cleared flags
+  static_assert(2 * QjlSmem::table == (int)tqi::kSketchH16Bytes && kSRow == tqi::kSketchPitch, "table layout");
+  __shared__ __align__(8) unsigned long long s_bar;
+  const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(&s_bar);
+  if (threadIdx.x == 0) {
+    constexpr uint32_t kPiece = (uint32_t)tqi::kSketchH16Bytes / 4;
+    mbar_init(sbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(sbar, (uint32_t)tqi::kSketchH16Bytes);
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      hi[e] = __float2half_rn(xs[e]);
-      lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
-    }
-    *reinterpret_cast<uint2*>(Shi + i * kSRow + jj) = *reinterpret_cast<const uint2*>(hi);
-    *reinterpret_cast<uint2*>(Slo + i * kSRow + jj) = *reinterpret_cast<const uint2*>(lo);
+    for (uint32_t k = 0; k < 4; ++k) bulk_g2s(dst + k * kPiece, p.tab.S_h16[side] + k * kPiece, kPiece, sbar);
   }
   for (int i = threadIdx.x; i < kQjlBlockVec; i += blockDim.x) unc[i] = 0u;
 
-  // ---- (1) the block's vectors through the codec, two at a time; residuals to shared memory
+  // ---- (1) the block's vectors through the codec; residuals to shared memory.  Four lanes per
+  // vector (encode_quad), eight vectors per warp; a key side with a HeadQ side code takes
+  // encode_vectors, two vectors at a time per warp.
+  static_assert(kQjlBlockVec == kQjlWarps * 8, "eight vectors per warp");
+  if (!(side == 0 && p.headq_rank)) {
+    const int vl = warp * 8 + (lane >> 2), q = lane & 3;
+    const bool okq = v0 + vl < per_side;
+    int bq, hq, jq, tq;
+    split_vec(p, okq ? v0 + vl : v0, bq, hq, jq, tq);
+    float rq[kQE];
+    if constexpr (BITS == 0) encode_quad_bits<Tin>(p, side, bq, hq, jq, tq, okq, rq);
+    else encode_quad<Tin, BITS>(p, side, bq, hq, jq, tq, okq, rq);
+#pragma unroll
+    for (int i = 0; i < kQE; i += 8) {
+      __half hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = rq[i + e] * kQjlUp;
+        hi[e] = __float2half_rn(x);
+        lo[e] = __float2half_rn(x - __half2float(hi[e]));
+      }
+      *reinterpret_cast<uint4*>(Rhi + vl * kSRow + kQE * q + i) = *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(Rlo + vl * kSRow + kQE * q + i) = *reinterpret_cast<const uint4*>(lo);
+    }
+  } else {
   constexpr int NV = 2;
   for (int vb = warp * (kQjlBlockVec / kQjlWarps); vb < (warp + 1) * (kQjlBlockVec / kQjlWarps); vb += NV) {
     int b[NV], h[NV], j[NV], t[NV];
@@ -674,6 +936,25 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
       }
       *reinterpret_cast<uint2*>(Rhi + (vb + u) * kSRow + lane * E) = *reinterpret_cast<const uint2*>(hi);
       *reinterpret_cast<uint2*>(Rlo + (vb + u) * kSRow + lane * E) = *reinterpret_cast<const uint2*>(lo);
+    }
+  }
+  }
+  __syncthreads();  // residuals in place; the barrier's initialization is visible
+  if (!mbar_wait(sbar, 0, kStageWaitLimit)) {
+    // the copy did not arrive within the poll limit: convert the fp32 table here (the same values)
+    const float* S = side ? p.tab.S_V : p.tab.S_K;  // [m][d], S[i][j]
+    for (int idx = threadIdx.x * 4; idx < D * D; idx += blockDim.x * 4) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(S + idx));
+      const int i = idx / D, jj = idx % D;
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+      __half hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = __float2half_rn(xs[e]);
+        lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
+      }
+      *reinterpret_cast<uint2*>(Shi + i * kSRow + jj) = *reinterpret_cast<const uint2*>(hi);
+      *reinterpret_cast<uint2*>(Slo + i * kSRow + jj) = *reinterpret_cast<const uint2*>(lo);
     }
   }
   __syncthreads();
@@ -1000,9 +1281,21 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
       if (e == cudaSuccess) kern<<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
       return e;
     };
-    const cudaError_t e = dtype == TQ_F32 ? goq(append_qjl_mma_kernel<float>)
-                          : dtype == TQ_BF16 ? goq(append_qjl_mma_kernel<__nv_bfloat16>)
-                                             : goq(append_qjl_mma_kernel<__half>);
+    // the QJL sides' code width as a template constant (0: two QJL sides of different widths)
+    const int qb = (p.qjl[0] && p.qjl[1] && p.bits[0] != p.bits[1]) ? 0 : p.bits[p.qjl[0] ? 0 : 1];
+    auto by_bits = [&](auto tin) {
+      using T = decltype(tin);
+      switch (qb) {
+        case 4: return goq(append_qjl_mma_kernel<T, 4>);
+        case 3: return goq(append_qjl_mma_kernel<T, 3>);
+        case 2: return goq(append_qjl_mma_kernel<T, 2>);
+        case 1: return goq(append_qjl_mma_kernel<T, 1>);
+        default: return goq(append_qjl_mma_kernel<T, 0>);
+      }
+    };
+    const cudaError_t e = dtype == TQ_F32 ? by_bits(float())
+                          : dtype == TQ_BF16 ? by_bits(__nv_bfloat16())
+                                             : by_bits(__half());
     if (e != cudaSuccess) {
       set_error(std::string("append sketch: ") + cudaGetErrorString(e));
       return TQ_ERR_CUDA;
@@ -1017,6 +1310,32 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
   }
   const unsigned nsides = p.qjl_mma ? 1u : 2u;
   cudaError_t ae = cudaSuccess;
+  // large appends at head dim 128 (no HeadQ side code, no spectral side): four lanes per vector
+  const bool quad = ctx->cfg.head_dim == 128 && per_side >= kQjlMmaMin && !ctx->cfg.headq_rank &&
+                    ctx->cfg.k.rotate != 2 && ctx->cfg.v.rotate != 2;
+  if (quad) {
+    auto go = [&](auto kern) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)((per_side + kWarpsPerBlock * 8 - 1) / (kWarpsPerBlock * 8)), nsides);
+      cfg.blockDim = dim3(kWarpsPerBlock * 32);
+      cfg.dynamicSmemBytes = 0;
+      cfg.stream = cs;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = p.wait_primary ? 1 : 0;
+      ae = cudaLaunchKernelEx(&cfg, kern, p);
+    };
+    if (dtype == TQ_F32) go(append_quad_kernel<float>);
+    else if (dtype == TQ_BF16) go(append_quad_kernel<__nv_bfloat16>);
+    else go(append_quad_kernel<__half>);
+    if (ae != cudaSuccess) {
+      set_error(std::string("append: ") + cudaGetErrorString(ae));
+      return TQ_ERR_CUDA;
+    }
+    return launch_status("append");
+  }
   tq_status s = dispatch_d(ctx->cfg.head_dim, [&](auto dc) {
     constexpr int D = decltype(dc)::value;
     auto go = [&](auto kern) {

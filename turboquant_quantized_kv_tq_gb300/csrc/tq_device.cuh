@@ -27,6 +27,7 @@ struct Tables {
   const float* S_V_T;
   const float* U_rot; // [H_kv][d][r], R_K U
   const float* S_V_R; // [m][d], S_V R_V (head dim > 128 with a QJL value side)
+  const unsigned char* S_h16[2];  // fp16 hi / lo rows of S_K, S_V (head dim 128; tqi::kSketchH16Bytes)
   const float* sq_c1;     // [2]: 1-bit centroid of each side (spectral sides' floor)
   const float* sq_E[2];   // spectral side: [H_kv][d][d] basis, column c = stored coordinate c
   const float* sq_ET[2];  // its transpose
@@ -120,6 +121,7 @@ inline Tables make_tables(const tq_context* ctx) {
   t.S_V_T = ctx->cfg.v.qjl ? (const float*)(b + ctx->tab.s_v_t) : nullptr;
   t.U_rot = ctx->cfg.headq_rank ? (const float*)(b + ctx->tab.headq_u) : nullptr;
   t.S_V_R = ctx->tab.s_v_r ? (const float*)(b + ctx->tab.s_v_r) : nullptr;
+  for (int side = 0; side < 2; ++side) t.S_h16[side] = ctx->tab.s_h16[side] ? b + ctx->tab.s_h16[side] : nullptr;
   t.sq_c1 = (const float*)(b + ctx->tab.sq_c1);
   for (int side = 0; side < 2; ++side) {
     const bool sq = ctx->tab.sq_e[side] != 0;

@@ -200,6 +200,8 @@ TableOffsets make_table_offsets(const tq_config& cfg, int m) {
   T.s_v_t = cfg.v.qjl ? take((uint64_t)m * d * 4) : 0;
   T.headq_u = cfg.headq_rank ? take((uint64_t)cfg.num_kv_heads * d * cfg.headq_rank * 4) : 0;
   T.s_v_r = (cfg.v.qjl && d > 128) ? take((uint64_t)m * d * 4) : 0;
+  T.s_h16[0] = (cfg.k.qjl && d == 128 && m == 128) ? take(kSketchH16Bytes) : 0;
+  T.s_h16[1] = (cfg.v.qjl && d == 128 && m == 128) ? take(kSketchH16Bytes) : 0;
   T.sq_c1 = take(2 * 4);
   const uint64_t hdd = (uint64_t)cfg.num_kv_heads * d * d * 4;
   for (int side = 0; side < 2; ++side) {

@@ -23,6 +23,7 @@ enum RegionId {
 struct TableOffsets {
   size_t k_centroids, k_thresholds, v_centroids, v_thresholds;
   size_t k_signs, v_signs, s_k, s_k_t, s_v, s_v_t, headq_u, s_v_r;
+  size_t s_h16[2];                       // head dim 128, QJL side: S as fp16 hi then lo rows (sketch_h16_bytes)
   size_t sq_c1;                          // fp32 [2]: 1-bit centroid of each spectral side
   size_t sq_e[2], sq_et[2], sq_s[2];     // spectral side: E, E^T [H_kv][d][d], s [H_kv][d] (storage order)
   size_t total;
@@ -38,6 +39,11 @@ struct Layout {
   uint64_t total;
 };
 constexpr int kTileTokens = TQ_TILE_TOKENS;
+// fp16 copies of a 128 x 128 sketch matrix for the tensor-core residual sketch: rows of 136
+// halves (the 272-byte pitch the kernel's shared-memory tables use), the hi terms fp16(S) then
+// the lo terms fp16(S - hi)
+constexpr int kSketchPitch = 136;
+constexpr size_t kSketchH16Bytes = 2 * 128 * kSketchPitch * 2;
 inline int region_side(int r) { return r >= R_V_CODES ? 1 : 0; }
 
 // Host tables: Beta Lloyd-Max codebook (float64) and SplitMix64-driven D and S.
