@@ -105,6 +105,17 @@ def record_bytes(scheme, n, d=128, m=128):
     return total
 
 
+def step_launches(scheme, n):
+    """Kernels one decode step launches for a scheme at head dim 128: the append (the sketch
+    kernel for QJL sides, then the other side's encode if it has none), the query prep and the
+    decode."""
+    from turboquant_quantized_kv_tq_gb300.binding import SCHEMES as S, tq_config, tq_config_from_scheme
+    c = tq_config()
+    tq_config_from_scheme(S[scheme], n, c)
+    nq = int(bool(c.k.qjl)) + int(bool(c.v.qjl))
+    return (2 if nq == 1 else 1) + 2
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -315,7 +326,7 @@ def run_gpu(args):
         "multi_query": multi,
         "long_context": long_ctx,
         "prefill": prefill,
-        "gpu_launches": args.steps * n_dec * 3,
+        "gpu_launches": args.steps * sum(step_launches(s, n) for s, n in SCHEMES),
         "clocks": clocks,
     }
     if rank == 0 and not args.skip_cpu_baseline:
@@ -805,9 +816,9 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")
     ap.add_argument("--schemes", default=None,
                     help="comma-separated subset of plain4,tq4,kqv4,qkqv4 (default: all four)")
-    ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5", "sq", "paged"],
-                    help="decode throughput of another configuration at full size, or of the paged pool "
-                         "at the headline shape (one JSON line)")
+    ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5", "sq", "paged", "append"],
+                    help="decode throughput of another configuration at full size, of the paged pool "
+                         "at the headline shape, or the prefill-chunk append alone (one JSON line)")
     args = ap.parse_args()
     if args.schemes:
         global SCHEMES
@@ -817,6 +828,11 @@ def main():
         args.warmup = 3
     if args.workload == "paged":
         run_paged(args)
+        return
+    if args.workload == "append":
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps(run_prefill_append(args, torch.device("cuda", 0))), flush=True)
         return
     if args.workload:
         run_workload(args)

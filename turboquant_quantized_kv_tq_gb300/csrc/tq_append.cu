@@ -7,6 +7,7 @@
 // One warp owns one vector; lane l holds coordinates [l*E, l*E + E), E = d / 32.  The rotation
 // runs in registers (local butterflies, then warp shuffles); codes are packed so that lane l's
 // bits are contiguous in the stream and stored with one coalesced store per lane group.
+#include <algorithm>
 #include <cstdio>
 #include <string>
 #include <type_traits>
@@ -30,20 +31,37 @@ struct AppendParams {
   int B, Hkv, n_new, m;
   int bits[2], rotate[2], qjl[2];
   int headq_rank;
-  int qjl_mma;   // QJL sides go to append_qjl_mma_kernel (head dim 128, large appends)
-  int stage_st;  // append_kernel blocks of a QJL side stage S^T in shared memory
+  int qjl_mma;   // QJL sides go to append_qjl_mma_kernel (head dim 128)
   int side_base;     // append_kernel: side of blockIdx.y = 0 (the other, if any, is side_base + 1)
   int wait_primary;  // append_kernel runs as the dependent launch of append_qjl_mma_kernel
   int start[TQ_MAX_BATCH];
   const int* dev_start;  // set: start positions from device memory (paged pool)
+  // n / n_new and n / Hkv for 0 <= n < 2^31 as (umulhi(n, mul) + n) >> shift
+  uint32_t div_n_mul, div_n_shift, div_h_mul, div_h_shift;
 };
 
-// Flat vector index (over [B][H_kv][n_new]) -> batch, KV head, index in the chunk, position.
+// Multiplier and shift of the division by d (1 <= d < 2^31) for dividends below 2^31: with
+// l = ceil(log2 d) and mul = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(n, mul) + n) >> l
+// (the round-up reciprocal method; umulhi(n, mul) + n stays below 2^32).
+inline void fast_div_magic(uint32_t d, uint32_t& mul, uint32_t& shift) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  mul = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d + 1) & 0xffffffffull);
+  shift = l;
+}
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, uint32_t mul, uint32_t shift) {
+  return (__umulhi(n, mul) + n) >> shift;
+}
+
+// Flat vector index (over [B][H_kv][n_new], below 2^31) -> batch, KV head, index in the chunk,
+// position.
 __device__ __forceinline__ void split_vec(const AppendParams& p, long long vec, int& b, int& h, int& j, int& t) {
-  j = (int)(vec % p.n_new);
-  const long long r = vec / p.n_new;
-  h = (int)(r % p.Hkv);
-  b = (int)(r / p.Hkv);
+  const uint32_t v = (uint32_t)vec;
+  const uint32_t r = fast_div(v, p.div_n_mul, p.div_n_shift);
+  j = (int)(v - r * (uint32_t)p.n_new);
+  const uint32_t bq = fast_div(r, p.div_h_mul, p.div_h_shift);
+  h = (int)(r - bq * (uint32_t)p.Hkv);
+  b = (int)bq;
   t = (p.dev_start ? __ldg(p.dev_start + b) : p.start[b]) + j;
 }
 
@@ -530,17 +548,12 @@ __device__ __forceinline__ void sketch_signs_ffma(const AppendParams& p, int sid
 
 // One block of append_kernel (below).
 template <int D, typename Tin>
-__device__ __forceinline__ void append_body(const AppendParams& p, float* st_smem) {
+__device__ __forceinline__ void append_body(const AppendParams& p) {
   constexpr int E = D / 32;
   constexpr int NV = AppendNV<D>::value;
   const int side = p.side_base + (int)blockIdx.y;
   if (p.qjl[side] && p.qjl_mma) return;  // left to append_qjl_mma_kernel (whole block)
   const float* ST = side ? p.tab.S_V_T : p.tab.S_K_T;
-  if (D == 128 && p.stage_st && p.qjl[side]) {
-    stage_table<kWarpsPerBlock * 32>(st_smem, ST, D * D);
-    __syncthreads();
-    ST = st_smem;
-  }
   const long long w = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const long long per_side = (long long)p.B * p.Hkv * p.n_new;
   const long long W = (per_side + NV - 1) / NV;
@@ -568,16 +581,14 @@ __device__ __forceinline__ void append_body(const AppendParams& p, float* st_sme
   }
 }
 
-// AppendNV consecutive vectors of side side_base + blockIdx.y per warp.  With stage_st set
-// (small appends at head dim 128 with a QJL side), a block of a QJL side first copies S^T
-// (64 KiB) into shared memory, so the sketch's 128 dependent table rows come from there instead
-// of L2.  Launched right after append_qjl_mma_kernel as its programmatic dependent (the other,
-// non-QJL side of a large append), its blocks fill that kernel's last wave; each waits for it
-// before exiting, so this grid's completion still implies the whole append's.
+// AppendNV consecutive vectors of side side_base + blockIdx.y per warp (a QJL side at head dim
+// above 128 takes its sketch on the FFMA path, S^T from L2).  Launched right after
+// append_qjl_mma_kernel as its programmatic dependent (the other, non-QJL side), its blocks fill
+// that kernel's last wave; each waits for it before exiting, so this grid's completion still
+// implies the whole append's.
 template <int D, typename Tin>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
-  extern __shared__ __align__(16) float st_smem[];
-  append_body<D, Tin>(p, st_smem);
+  append_body<D, Tin>(p);
   if (p.wait_primary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
@@ -588,7 +599,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const Appen
 // reduce over those four lanes, and each lane's codes form whole words of the packed record.
 // The stages run in the order and with the arithmetic of encode_vectors (butterflies over
 // coordinate bits 0 .. 6), so the rotated values, and with them the codes, are the same.
-constexpr int kQE = 32;  // coordinates per lane
+constexpr int kQE = 32;        // coordinates per lane
+constexpr int kQuadWarps = 4;  // warps per block of append_quad_kernel
 
 __device__ __forceinline__ float quad_sum(float v) {
   v += __shfl_xor_sync(kFull, v, 1);
@@ -677,10 +689,13 @@ __device__ __forceinline__ void wht_quad(float (&x)[kQE]) {
   const int q = threadIdx.x & 3;
 #pragma unroll
   for (int m = 1; m < 4; m <<= 1) {
+    // the upper lane of the butterfly takes other - x, the lower x + other: one fma with a
+    // factor of -1 or 1 gives the same rounded sum
+    const float f = (q & m) ? -1.f : 1.f;
 #pragma unroll
     for (int i = 0; i < kQE; ++i) {
       const float other = __shfl_xor_sync(kFull, x[i], m);
-      x[i] = (q & m) ? (other - x[i]) : (x[i] + other);
+      x[i] = fmaf(f, x[i], other);
     }
   }
 }
@@ -798,15 +813,16 @@ __device__ __forceinline__ void encode_quad_bits(const AppendParams& p, int side
 }
 
 // Sides of a large append at head dim 128 that carry no QJL sketch (a QJL side goes to
-// append_qjl_mma_kernel): 64 vectors per block of 8 warps, four lanes per vector.  As the
+// append_qjl_mma_kernel): 32 vectors per block of 4 warps, four lanes per vector; seven blocks
+// per SM (at most 73 registers) put a 4096-token chunk of eight heads in one wave.  As the
 // programmatic dependent of append_qjl_mma_kernel (wait_primary) it waits for that kernel
 // before exiting, as append_kernel does.
 template <typename Tin>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_quad_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kQuadWarps * 32, 7) append_quad_kernel(const AppendParams p) {
   const int side = p.side_base + (int)blockIdx.y;
   if (!(p.qjl[side] && p.qjl_mma)) {
     const long long per_side = (long long)p.B * p.Hkv * p.n_new;
-    const long long v = (long long)blockIdx.x * (kWarpsPerBlock * 8) + (threadIdx.x >> 2);
+    const long long v = (long long)blockIdx.x * (kQuadWarps * 8) + (threadIdx.x >> 2);
     const bool ok = v < per_side;
     int b, h, j, t;
     split_vec(p, ok ? v : 0, b, h, j, t);
@@ -818,27 +834,36 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_quad_kernel(const 
 
 constexpr uint32_t kStageWaitLimit = 1u << 20;  // polls of a table copy's mbarrier
 
-// QJL sides of large appends at head dim 128: a block of kQjlWarps warps takes 64 vectors of one
-// side.  (1) Each warp runs 8 of them through encode_vector and keeps r, scaled by 256, in shared
-// memory as two fp16 terms (hi, lo = fp16(256 r - hi)).  (2) S r for the 64 vectors is a
-// [64 x 128] x [128 x 128] product on the tensor cores: mma.sync m16n8k16 with ldmatrix
-// fragments, S split the same way and staged once per block, hi*hi in one fp32 chain and
+// QJL sides at head dim 128: a block of kQjlWarps warps takes VEC vectors of one side (64 for
+// large appends, 16 for small ones).  (1) The vectors go through the codec -- four lanes per
+// vector for VEC = 64, a warp per vector (two at a time) for VEC = 16, where the latency of one
+// vector matters more than the throughput -- and r, scaled by 256, is kept in shared memory as
+// two fp16 terms (hi, lo = fp16(256 r - hi)).  (2) S r for the block is a [VEC x 128] x
+// [128 x 128] product on the tensor cores: mma.sync m16n8k16 with ldmatrix fragments, S split
+// the same way and bulk-copied from the table blob once per block, hi*hi in one fp32 chain and
 // hi*lo + lo*hi in another; warp ballots turn the signs into bytes of the 1-bit stream.
-// (3) The sign records are stored.  (4) A vector with any |S r| below kSignRecheck gets all its
-// signs again from the FFMA path, so decisions near zero have that path's accuracy.
+// (3) Every product with |S r| below kSignRecheck is listed and taken again as an fp32 FFMA dot
+// product of the row of S with hi + lo (a warp per listed product), so decisions near zero have
+// fp32 accuracy; the sign bits are patched.  (If more than kRecheckMax products of a block are
+// listed, a vector whose product did not fit gets all its signs from the FFMA path instead.)
+// (4) The sign records are stored.
 constexpr int kQjlWarps = 8;
-constexpr int kQjlBlockVec = 64;        // vectors per block: 4 MMA row tiles of 16
+constexpr int kQjlBlockVec = 64;        // vectors per block of a large append: 4 MMA row tiles of 16
+constexpr int kQjlSmallVec = 16;        // vectors per block of a small append: one row tile
 constexpr int kSRow = 136;              // fp16 row pitch: 272 B keeps ldmatrix rows on distinct banks
 constexpr float kQjlUp = 256.f;         // residual scale before the fp16 split
 constexpr float kSignRecheck = 2e-5f;   // in units of S r
-constexpr long long kQjlMmaMin = 256;   // vectors per side from which the tensor-core path is used
+constexpr long long kQjlMmaMin = 256;   // vectors per side from which 64-vector blocks are used
+constexpr int kRecheckMax = 256;        // listed near-zero products per block
 
+template <int VEC>
 struct QjlSmem {
   static constexpr int table = 128 * kSRow * 2;             // one fp16 table (hi or lo)
-  static constexpr int resid = kQjlBlockVec * kSRow * 2;    // one fp16 residual array (hi or lo)
-  static constexpr int signs = kQjlBlockVec * 16;           // sign records of the block
-  static constexpr int flags = kQjlBlockVec * 4;
-  static constexpr int bytes = 2 * table + 2 * resid + signs + flags;
+  static constexpr int resid = VEC * kSRow * 2;             // one fp16 residual array (hi or lo)
+  static constexpr int signs = VEC * 16;                    // sign records of the block
+  static constexpr int flags = VEC * 4;
+  static constexpr int list = kRecheckMax * 4 + 16;         // listed products + their count
+  static constexpr int bytes = 2 * table + 2 * resid + signs + flags + list;
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -854,10 +879,15 @@ __device__ __forceinline__ uint32_t spread4(uint32_t n) {
 }
 
 // BITS: the code width of the QJL side(s) as a compile-time constant (one encode variant in the
-// kernel's code), or 0 when two QJL sides differ (chosen at run time).
-template <typename Tin, int BITS>
+// kernel's code), or 0 when two QJL sides differ (chosen at run time).  HQ: the key side carries
+// a HeadQ side code (its vectors take encode_vectors); only that variant holds that code.
+template <typename Tin, int BITS, bool HQ, int VEC = kQjlBlockVec>
 __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const AppendParams p) {
   constexpr int D = 128, E = 4;
+  using QjlSmem = tqd::QjlSmem<VEC>;
+  // MMA row tiles of the block, warps per row tile, n-tiles (8 sketch rows) per warp
+  constexpr int RT = VEC / 16, WPR = kQjlWarps / RT, NTW = 16 / WPR;
+  static_assert(VEC == kQjlBlockVec || VEC == kQjlSmallVec, "block sizes");
   extern __shared__ __align__(16) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int side = (p.qjl[0] && p.qjl[1]) ? (int)blockIdx.y : (p.qjl[0] ? 0 : 1);
@@ -865,13 +895,15 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
   __half* Slo = reinterpret_cast<__half*>(smem + QjlSmem::table);
   __half* Rhi = reinterpret_cast<__half*>(smem + 2 * QjlSmem::table);
   __half* Rlo = reinterpret_cast<__half*>(smem + 2 * QjlSmem::table + QjlSmem::resid);
-  unsigned char* sg = smem + 2 * QjlSmem::table + 2 * QjlSmem::resid;  // [64][16] sign bytes
-  uint32_t* unc = reinterpret_cast<uint32_t*>(sg + QjlSmem::signs);    // [64] near-zero flags
+  unsigned char* sg = smem + 2 * QjlSmem::table + 2 * QjlSmem::resid;  // [VEC][16] sign bytes
+  uint32_t* unc = reinterpret_cast<uint32_t*>(sg + QjlSmem::signs);    // [VEC] whole-vector recheck flags
+  uint32_t* re_list = unc + VEC;                                       // [kRecheckMax] (v << 7) | row
+  uint32_t* re_cnt = re_list + kRecheckMax;
   // the other side's append_kernel, launched next as a programmatic dependent, may start as soon
   // as every block of this grid is running (it fills the last wave)
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const long long per_side = (long long)p.B * p.Hkv * p.n_new;
-  const long long v0 = (long long)blockIdx.x * kQjlBlockVec;
+  const long long v0 = (long long)blockIdx.x * VEC;
 
   // ---- (0) S as fp16 hi / lo rows: the table blob holds them in this layout, so bulk copies
   // bring them in while the vectors are encoded; cleared flags
@@ -887,13 +919,14 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
 #pragma unroll
     for (uint32_t k = 0; k < 4; ++k) bulk_g2s(dst + k * kPiece, p.tab.S_h16[side] + k * kPiece, kPiece, sbar);
   }
-  for (int i = threadIdx.x; i < kQjlBlockVec; i += blockDim.x) unc[i] = 0u;
+  for (int i = threadIdx.x; i < VEC; i += blockDim.x) unc[i] = 0u;
+  if (threadIdx.x == 0) *re_cnt = 0u;
 
   // ---- (1) the block's vectors through the codec; residuals to shared memory.  Four lanes per
-  // vector (encode_quad), eight vectors per warp; a key side with a HeadQ side code takes
-  // encode_vectors, two vectors at a time per warp.
+  // vector (encode_quad), eight vectors per warp; a key side with a HeadQ side code, and every
+  // side of a small append, takes encode_vectors, two vectors at a time per warp.
   static_assert(kQjlBlockVec == kQjlWarps * 8, "eight vectors per warp");
-  if (!(side == 0 && p.headq_rank)) {
+  if (VEC == kQjlBlockVec && !(HQ && side == 0)) {
     const int vl = warp * 8 + (lane >> 2), q = lane & 3;
     const bool okq = v0 + vl < per_side;
     int bq, hq, jq, tq;
@@ -915,7 +948,7 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     }
   } else {
   constexpr int NV = 2;
-  for (int vb = warp * (kQjlBlockVec / kQjlWarps); vb < (warp + 1) * (kQjlBlockVec / kQjlWarps); vb += NV) {
+  for (int vb = warp * (VEC / kQjlWarps); vb < (warp + 1) * (VEC / kQjlWarps); vb += NV) {
     int b[NV], h[NV], j[NV], t[NV];
     bool ok[NV];
 #pragma unroll
@@ -959,9 +992,9 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
   }
   __syncthreads();
 
-  // ---- (2) S r: warp w takes row tile w / 2 (vectors 16 (w / 2) ..) and sketch rows
-  // 64 (w % 2) .. + 63 (n-tiles of 8)
-  const int rt = warp >> 1, nt0 = 8 * (warp & 1);
+  // ---- (2) S r: warp w takes row tile w / WPR (vectors 16 (w / WPR) ..) and the NTW n-tiles
+  // (8 sketch rows each) from NTW (w % WPR)
+  const int rt = warp / WPR, nt0 = NTW * (warp % WPR);
   const uint32_t rhi_s = (uint32_t)__cvta_generic_to_shared(Rhi), rlo_s = (uint32_t)__cvta_generic_to_shared(Rlo);
   const uint32_t shi_s = (uint32_t)__cvta_generic_to_shared(Shi), slo_s = (uint32_t)__cvta_generic_to_shared(Slo);
   const int mi = lane >> 3, mr = lane & 7;
@@ -973,9 +1006,16 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     ldsm_x4(rlo_s + off, al[ks][0], al[ks][1], al[ks][2], al[ks][3]);
   }
   const float thr = kSignRecheck * kQjlUp;
-  uint32_t U0 = 0u, U1 = 0u;
+  // a product too close to zero goes on the block's list (or, past its end, flags the vector)
+  auto near_zero = [&](float sv, int v, int row) {
+    if (fabsf(sv) < thr && v0 + v < per_side) {
+      const uint32_t k = atomicAdd(re_cnt, 1u);
+      if (k < (uint32_t)kRecheckMax) re_list[k] = ((uint32_t)v << 7) | (uint32_t)row;
+      else atomicOr(unc + v, 1u);
+    }
+  };
 #pragma unroll 1
-  for (int nt = nt0; nt < nt0 + 8; ++nt) {
+  for (int nt = nt0; nt < nt0 + NTW; ++nt) {
     float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kp = 0; kp < 4; ++kp) {
@@ -995,23 +1035,57 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     const float s0 = c[0] + e[0], s1 = c[1] + e[1], s2 = c[2] + e[2], s3 = c[3] + e[3];
     const uint32_t b0 = __ballot_sync(kFull, s0 >= 0.f), b1 = __ballot_sync(kFull, s1 >= 0.f);
     const uint32_t b2 = __ballot_sync(kFull, s2 >= 0.f), b3 = __ballot_sync(kFull, s3 >= 0.f);
-    U0 |= __ballot_sync(kFull, fabsf(s0) < thr || fabsf(s1) < thr);
-    U1 |= __ballot_sync(kFull, fabsf(s2) < thr || fabsf(s3) < thr);
+    if (__any_sync(kFull, fminf(fminf(fabsf(s0), fabsf(s1)), fminf(fabsf(s2), fabsf(s3))) < thr)) {
+      const int vg = 16 * rt + (lane >> 2), rw = 8 * nt + 2 * (lane & 3);
+      near_zero(s0, vg, rw);
+      near_zero(s1, vg, rw + 1);
+      near_zero(s2, vg + 8, rw);
+      near_zero(s3, vg + 8, rw + 1);
+    }
     if (lane < 16) {  // byte nt of vector 16 rt + lane: bit 2t from b0 / b2, bit 2t + 1 from b1 / b3
       const int sh = 4 * (lane & 7);
       const uint32_t lo = ((lane < 8 ? b0 : b2) >> sh) & 0xFu, hi = ((lane < 8 ? b1 : b3) >> sh) & 0xFu;
       sg[(16 * rt + lane) * 16 + nt] = (unsigned char)(spread4(lo) | (spread4(hi) << 1));
     }
   }
-  if (lane < 16) {
-    const uint32_t u = lane < 8 ? U0 : U1;
-    if ((u >> (4 * (lane & 7))) & 0xFu) atomicOr(unc + 16 * rt + lane, 1u);
+  __syncthreads();
+
+  // ---- (3) listed products again in fp32: row `row` of S (fp32, L2) against hi + lo of the
+  // vector's scaled residual, a warp per product; the sign bit is patched in place
+  {
+    const uint32_t nre = min(*re_cnt, (uint32_t)kRecheckMax);
+    const float* S = side ? p.tab.S_V : p.tab.S_K;  // [m][d], S[i][j]
+    for (uint32_t k = warp; k < nre; k += kQjlWarps) {
+      const uint32_t e = re_list[k];
+      const int v = (int)(e >> 7), row = (int)(e & 127u);
+      if (unc[v]) continue;  // the whole vector is taken again below
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(S + row * D + 4 * lane));
+      const uint2 h4 = *reinterpret_cast<const uint2*>(Rhi + v * kSRow + 4 * lane);
+      const uint2 l4 = *reinterpret_cast<const uint2*>(Rlo + v * kSRow + 4 * lane);
+      const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&h4.x));
+      const float2 h23 = __half22float2(*reinterpret_cast<const __half2*>(&h4.y));
+      const float2 l01 = __half22float2(*reinterpret_cast<const __half2*>(&l4.x));
+      const float2 l23 = __half22float2(*reinterpret_cast<const __half2*>(&l4.y));
+      float acc = s4.x * (h01.x + l01.x);
+      acc = fmaf(s4.y, h01.y + l01.y, acc);
+      acc = fmaf(s4.z, h23.x + l23.x, acc);
+      acc = fmaf(s4.w, h23.y + l23.y, acc);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+      if (lane == 0) {
+        const int byte = v * 16 + (row >> 3);
+        const uint32_t bit = 1u << (8 * (byte & 3) + (row & 7));
+        uint32_t* word = reinterpret_cast<uint32_t*>(sg) + (byte >> 2);
+        if (acc >= 0.f) atomicOr(word, bit);
+        else atomicAnd(word, ~bit);
+      }
+    }
   }
   __syncthreads();
 
-  // ---- (3) sign records of the valid vectors, one 32-bit word per thread
+  // ---- (4) sign records of the valid vectors, one 32-bit word per thread
   const Cache& C = p.cache;
-  for (int w = threadIdx.x; w < kQjlBlockVec * 4; w += blockDim.x) {
+  for (int w = threadIdx.x; w < VEC * 4; w += blockDim.x) {
     const int v = w >> 2;
     const long long vec = v0 + v;
     if (vec < per_side) {
@@ -1030,8 +1104,9 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
   }
   __syncthreads();
 
-  // ---- (4) vectors with a value too close to zero: every sign again from the FFMA path (rare)
-  for (int v = warp * (kQjlBlockVec / kQjlWarps); v < (warp + 1) * (kQjlBlockVec / kQjlWarps); ++v) {
+  // ---- (5) vectors whose near-zero products overflowed the list: every sign again from the
+  // FFMA path (only when a block has more than kRecheckMax of them)
+  for (int v = warp * (VEC / kQjlWarps); v < (warp + 1) * (VEC / kQjlWarps); ++v) {
     const long long vec = v0 + v;
     if (vec >= per_side || !unc[v]) continue;
     int b, h, j, t;
@@ -1265,32 +1340,38 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
   const int nv = ctx->cfg.head_dim == 128 ? AppendNV<128>::value : 1;
   const long long per_side = (long long)p.B * p.Hkv * n_new;
   const long long blocks = ((per_side + nv - 1) / nv + kWarpsPerBlock - 1) / kWarpsPerBlock;  // per side
-  if (blocks > 0x7fffffffLL) { set_error("append too large"); return TQ_ERR_INVALID_ARG; }
+  if (per_side >= 0x7fffffffLL) { set_error("append too large"); return TQ_ERR_INVALID_ARG; }
+  fast_div_magic((uint32_t)std::max(n_new, 1), p.div_n_mul, p.div_n_shift);
+  fast_div_magic((uint32_t)p.Hkv, p.div_h_mul, p.div_h_shift);
   const int nq = (p.qjl[0] ? 1 : 0) + (p.qjl[1] ? 1 : 0);
-  p.qjl_mma = (ctx->cfg.head_dim == 128 && nq > 0 && per_side >= kQjlMmaMin) ? 1 : 0;
-  p.stage_st = (ctx->cfg.head_dim == 128 && nq > 0 && !p.qjl_mma) ? 1 : 0;
-  const int smem = p.stage_st ? 128 * 128 * 4 : 0;
+  p.qjl_mma = (ctx->cfg.head_dim == 128 && nq > 0) ? 1 : 0;
   const cudaStream_t cs = (cudaStream_t)stream;
-  // A large append with a QJL side: the tensor-core sketch kernel takes the QJL side(s) first,
-  // and append_kernel the other side (if any) as its programmatic dependent launch.
+  // An append with a QJL side at head dim 128: the tensor-core sketch kernel takes the QJL
+  // side(s) first (64-vector blocks for large appends, 16-vector blocks for small ones), and the
+  // other side (if any) follows as its programmatic dependent launch.
   if (p.qjl_mma) {
-    const dim3 qgrid((unsigned)((per_side + kQjlBlockVec - 1) / kQjlBlockVec), (unsigned)nq),
-        qblock(kQjlWarps * 32);
+    const bool small = per_side < kQjlMmaMin;
+    const int vec = small ? kQjlSmallVec : kQjlBlockVec;
+    const int qbytes = small ? QjlSmem<kQjlSmallVec>::bytes : QjlSmem<kQjlBlockVec>::bytes;
+    const dim3 qgrid((unsigned)((per_side + vec - 1) / vec), (unsigned)nq), qblock(kQjlWarps * 32);
     auto goq = [&](auto kern) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QjlSmem::bytes);
-      if (e == cudaSuccess) kern<<<qgrid, qblock, QjlSmem::bytes, cs>>>(p);
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, qbytes);
+      if (e == cudaSuccess) kern<<<qgrid, qblock, qbytes, cs>>>(p);
       return e;
     };
     // the QJL sides' code width as a template constant (0: two QJL sides of different widths)
     const int qb = (p.qjl[0] && p.qjl[1] && p.bits[0] != p.bits[1]) ? 0 : p.bits[p.qjl[0] ? 0 : 1];
+    const bool hq = p.headq_rank && p.qjl[0];
     auto by_bits = [&](auto tin) {
       using T = decltype(tin);
+      if (small) return goq(append_qjl_mma_kernel<T, 0, true, kQjlSmallVec>);
+      if (hq) return goq(append_qjl_mma_kernel<T, 0, true>);
       switch (qb) {
-        case 4: return goq(append_qjl_mma_kernel<T, 4>);
-        case 3: return goq(append_qjl_mma_kernel<T, 3>);
-        case 2: return goq(append_qjl_mma_kernel<T, 2>);
-        case 1: return goq(append_qjl_mma_kernel<T, 1>);
-        default: return goq(append_qjl_mma_kernel<T, 0>);
+        case 4: return goq(append_qjl_mma_kernel<T, 4, false>);
+        case 3: return goq(append_qjl_mma_kernel<T, 3, false>);
+        case 2: return goq(append_qjl_mma_kernel<T, 2, false>);
+        case 1: return goq(append_qjl_mma_kernel<T, 1, false>);
+        default: return goq(append_qjl_mma_kernel<T, 0, false>);
       }
     };
     const cudaError_t e = dtype == TQ_F32 ? by_bits(float())
@@ -1316,8 +1397,8 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
   if (quad) {
     auto go = [&](auto kern) {
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3((unsigned)((per_side + kWarpsPerBlock * 8 - 1) / (kWarpsPerBlock * 8)), nsides);
-      cfg.blockDim = dim3(kWarpsPerBlock * 32);
+      cfg.gridDim = dim3((unsigned)((per_side + kQuadWarps * 8 - 1) / (kQuadWarps * 8)), nsides);
+      cfg.blockDim = dim3(kQuadWarps * 32);
       cfg.dynamicSmemBytes = 0;
       cfg.stream = cs;
       cudaLaunchAttribute attr[1];
@@ -1339,12 +1420,10 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
   tq_status s = dispatch_d(ctx->cfg.head_dim, [&](auto dc) {
     constexpr int D = decltype(dc)::value;
     auto go = [&](auto kern) {
-      if (smem) ae = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (ae != cudaSuccess) return;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)blocks, nsides);
       cfg.blockDim = dim3(kWarpsPerBlock * 32);
-      cfg.dynamicSmemBytes = (size_t)smem;
+      cfg.dynamicSmemBytes = 0;
       cfg.stream = cs;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
