@@ -481,15 +481,39 @@ __device__ __forceinline__ int tile_row_token(int r) {
 }
 
 // Block bases of one (batch, KV head) slab: block `tile` of a side at base + tile * bytes.
+// A paged pool instead keeps the pages of the warp's tiles (below t_end) in windows of 32 tiles
+// -- lane l holds the page of tile t_base + l in pg0 and of tile t_base + 32 + l in pg1 -- so the
+// window after the current one is already loaded and a copy's issue does not wait on its
+// block-table entry.
 struct SlabPtrs {
   const unsigned char* kb;
   const unsigned char* vb;
   unsigned int kbytes, vbytes;
+  int t_base, t_end, pg0, pg1;
   __device__ __forceinline__ void init(const Cache& C, int b, int h) {
     kb = C.blockp(0, b, h, 0);
     vb = C.blockp(1, b, h, 0);
     kbytes = C.block[0];
     vbytes = C.block[1];
+  }
+  __device__ __forceinline__ static int load_page(const Cache& C, int b, int t, int t_end) {
+    return t < t_end ? C.page_of(b, t) : 0;
+  }
+  __device__ __forceinline__ void init_pages(const Cache& C, int b, int m0t, int m1t, int lane) {
+    t_base = m0t;
+    t_end = m1t;
+    pg0 = load_page(C, b, m0t + lane, m1t);
+    pg1 = load_page(C, b, m0t + 32 + lane, m1t);
+  }
+  // page of `tile` (warp-uniform and non-decreasing from call to call; every lane calls)
+  __device__ __forceinline__ int page(const Cache& C, int b, int tile, int lane) {
+    const int w = (tile - t_base) >> 5;
+    if (w != 0) {  // a later window: shift (the next one is in pg1) and load the one after it
+      pg0 = w == 1 ? pg1 : load_page(C, b, t_base + 32 * w + lane, t_end);
+      t_base += 32 * w;
+      pg1 = load_page(C, b, t_base + 32 + lane, t_end);
+    }
+    return __shfl_sync(kFull, pg0, (tile - t_base) & 31);
   }
 };
 
@@ -518,19 +542,25 @@ struct Stage {
 // and issues the copies; a paged pool (PAGED) takes one copy per block (its pages are not
 // adjacent), its blocks looked up through the block table.
 template <int KB, bool KQ, bool KH, int VB, bool VQ, bool PAGED>
-__device__ __forceinline__ void issue_pair(uint32_t st, uint32_t bar, const SlabPtrs& s, int tile, int nt,
+__device__ __forceinline__ void issue_pair(uint32_t st, uint32_t bar, SlabPtrs& s, int tile, int nt,
                                            int lane, const Cache& C, int b, int h) {
   using S = Stage<KB, KQ, KH, VB, VQ>;
   constexpr uint32_t KBL = S::VC, VBL = S::bytes - S::VC;
-  if (lane == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)nt * (KBL + VBL));
-    if constexpr (!PAGED) {
+  if constexpr (!PAGED) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)nt * (KBL + VBL));
       bulk_g2s(st, s.kb + (unsigned long long)tile * KBL, (uint32_t)nt * KBL, bar);
       bulk_g2s(st + 2 * KBL, s.vb + (unsigned long long)tile * VBL, (uint32_t)nt * VBL, bar);
-    } else {
+    }
+  } else {
+    int pg[2];
+    pg[0] = s.page(C, b, tile, lane);
+    pg[1] = nt > 1 ? s.page(C, b, tile + 1, lane) : pg[0];
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)nt * (KBL + VBL));
       for (int i = 0; i < nt; ++i) {
-        bulk_g2s(st + i * KBL, C.blockp(0, b, h, tile + i), KBL, bar);
-        bulk_g2s(st + 2 * KBL + i * VBL, C.blockp(1, b, h, tile + i), VBL, bar);
+        bulk_g2s(st + i * KBL, C.page_block(0, pg[i], h), KBL, bar);
+        bulk_g2s(st + 2 * KBL + i * VBL, C.page_block(1, pg[i], h), VBL, bar);
       }
     }
   }
@@ -1099,6 +1129,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     const int nt = m1t - m0t;
     SlabPtrs sp;
     if constexpr (!PAGED) sp.init(p.cache, b, kvh);
+    else sp.init_pages(p.cache, b, m0t, m1t, lane);
     WarpState<VQ && QLO> st;
     st.reset();
     // both pair stages in flight; a pair stage is refilled as soon as its operands are in

@@ -69,6 +69,10 @@ struct Cache {
                     : (unsigned long long)(b * num_kv_heads + h) * tiles_per_slab + tile;
     return base + side_off[side] + blk * block[side];
   }
+  // block of KV head h in page `page` of a paged pool, side 0 (K) or 1 (V)
+  __device__ __forceinline__ const unsigned char* page_block(int side, int page, int h) const {
+    return base + side_off[side] + ((unsigned long long)page * num_kv_heads + h) * block[side];
+  }
   // (t >> 4, t & 15: a negative position of a paged append lands in the redirect page)
   __device__ __forceinline__ unsigned char* ptr(int r, int b, int h, int t) const {
     const int side = r >= tqi::R_V_CODES ? 1 : 0;
