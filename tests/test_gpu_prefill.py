@@ -3,7 +3,8 @@
 The chunk's nq queries are its last positions, already appended; query i attends to the first
 L - nq + 1 + i tokens.  The oracle reconstructs each slab of the GPU-written cache once and runs
 textbook attention for every query over its causal prefix; every output row is compared under
-the decode tolerance.  Cases span nq = 16, 128 and 512 (several 128-row blocks, a ragged last
+the decode tolerance.  Schemes with a QJL side run the mma.sync kernel, the others the tcgen05
+one; the size, group and long-prefix cases run both.  Cases span nq = 16, 128 and 512 (several 128-row blocks, a ragged last
 block), G = 1, 4 and 8, ragged sequence lengths (one shorter than the chunk, so some queries see
 no token), every Plain / TQ-KV / KQV / QKQV codec family, and the one-query-column case against
 tq_decode_attention_multi.
@@ -64,15 +65,18 @@ def test_prefill_schemes_nq128(scheme, n):
     _run(scheme, n, nq=128, G=4, lens=[700, 311], T=700, seed=70)
 
 
+# KQV runs the mma.sync kernel (a QJL value side), TQ-KV the tcgen05 one (no sketch)
+@pytest.mark.parametrize("scheme", ["kqv", "tq"])
 @pytest.mark.parametrize("nq,G,lens", [(16, 4, [333, 16, 9]), (512, 4, [900, 600]), (512, 1, [777, 513]),
                                        (128, 8, [640, 129])])
-def test_prefill_chunk_sizes_and_groups(nq, G, lens):
-    _run("kqv", 4, nq=nq, G=G, lens=lens, T=max(lens), seed=71 + nq + G)
+def test_prefill_chunk_sizes_and_groups(scheme, nq, G, lens):
+    _run(scheme, 4, nq=nq, G=G, lens=lens, T=max(lens), seed=71 + nq + G)
 
 
-def test_prefill_outlier_channels_long_prefix():
-    # the long-context recipe (per-channel std in [0.1, 10]) with a 2048-token prefix, KQV n = 2
-    _run("kqv", 2, nq=64, G=8, lens=[2048], T=2048, seed=75, name="cfg4")
+@pytest.mark.parametrize("scheme", ["kqv", "tq"])
+def test_prefill_outlier_channels_long_prefix(scheme):
+    # the long-context recipe (per-channel std in [0.1, 10]) with a 2048-token prefix at n = 2
+    _run(scheme, 2, nq=64, G=8, lens=[2048], T=2048, seed=75, name="cfg4")
 
 
 def test_prefill_matches_multi_query_decode():

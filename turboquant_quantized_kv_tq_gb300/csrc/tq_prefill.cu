@@ -19,9 +19,11 @@
 // fp16 hi + lo terms: a single rounding of q is a score error common to every token of a row,
 // and one of a centroid an error common to every token with that code; with peaked attention
 // (outlier channels) either reaches the output undiluted.
+#include <algorithm>
 #include <string>
 
 #include "tq_device.cuh"
+#include "tq_tc05.cuh"
 
 namespace tqd {
 namespace {
@@ -155,6 +157,20 @@ __device__ __forceinline__ void unpack_codes(const unsigned char* codes, int bit
   }
 }
 
+// The packed blocks of tile `tile` of slab (b, h) -- nb 16-token blocks from block nb * tile --
+// into a stage: the K blocks at dst, the V blocks at dst + nb * kblk.  The copy stops at the
+// slab's last block, and the mbarrier expects the bytes actually copied.
+__device__ __forceinline__ void pf_issue_stage(const Cache& C, int b, int h, int tile, int nb, unsigned kblk,
+                                               unsigned vblk, uint32_t dst, uint32_t bar) {
+  const int first = tile * nb;
+  const int n = max(0, min(nb, C.tiles_per_slab - first));
+  mbar_arrive_expect_tx(bar, (uint32_t)n * (kblk + vblk));
+  if (n > 0) {
+    bulk_g2s(dst, C.blockp(0, b, h, first), (uint32_t)n * kblk, bar);
+    bulk_g2s(dst + (uint32_t)nb * kblk, C.blockp(1, b, h, first), (uint32_t)n * vblk, bar);
+  }
+}
+
 __device__ __forceinline__ void st_half4(unsigned char* dst, const float (&v)[4]) {
   const uint32_t a = pack_half2(v[0], v[1]), b = pack_half2(v[2], v[3]);
   *reinterpret_cast<uint2*>(dst) = make_uint2(a, b);
@@ -278,9 +294,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_kernel(const Prefill
     fence_mbar_init();
     for (int k = 0; k < 2 && k < ntiles; ++k) {
       const uint32_t dst = sb + SM::STG + k * SB;
-      mbar_arrive_expect_tx(bar0 + 8 * k, SB);
-      bulk_g2s(dst, C.blockp(0, b, h, 2 * k), 2 * kblk, bar0 + 8 * k);
-      bulk_g2s(dst + 2 * kblk, C.blockp(1, b, h, 2 * k), 2 * vblk, bar0 + 8 * k);
+      pf_issue_stage(C, b, h, k, 2, kblk, vblk, dst, bar0 + 8 * k);
     }
   }
   bool timed_out = false;
@@ -351,9 +365,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_kernel(const Prefill
     if (threadIdx.x == 0 && k + 2 < ntiles) {
       fence_proxy_async_shared();
       const uint32_t dst = sb + SM::STG + stage * SB;
-      mbar_arrive_expect_tx(bar0 + 8 * stage, SB);
-      bulk_g2s(dst, C.blockp(0, b, h, 2 * (k + 2)), 2 * kblk, bar0 + 8 * stage);
-      bulk_g2s(dst + 2 * kblk, C.blockp(1, b, h, 2 * (k + 2)), 2 * vblk, bar0 + 8 * stage);
+      pf_issue_stage(C, b, h, k + 2, 2, kblk, vblk, dst, bar0 + 8 * stage);
     }
     if (t0 >= ew) continue;  // every row of this warp is past its causal end (warp-uniform)
 
@@ -569,6 +581,424 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_kernel(const Prefill
   if (timed_out) atomicExch(p.err, TQ_DEVERR_WAIT_TIMEOUT);
 }
 
+// ---- The same product on the 5th-generation tensor cores (sides without a QJL sketch) ------
+// A block takes 128 rows, one per tensor-memory lane, and the slab's tokens in 64-token tiles:
+//   S[128 x 64]   = Q_hi K_hi^T + Q_lo K_hi^T + Q_hi K_lo^T      (tcgen05.mma, M = 128, N = 64)
+//   O[128 x 128] += P V,  P = 2^(s - m) nu_V as fp16               (tcgen05.mma, M = 128, N = 128)
+// Q_hi, Q_lo, S (two buffers), P and O live in tensor memory; the unpacked K and V tiles in
+// shared memory (two buffers).  Warps 0-3 own the rows (thread r <-> row r <-> lane r): they
+// load the queries into tensor memory, run the online softmax on S and write P, rescale O when
+// a row's maximum rises, and finish o = R_V^T O / l.  Warps 4-11 unpack the tiles, which bulk
+// copies bring into two packed stages.  One thread of warp 12 issues the MMAs.  The stages hand
+// over through mbarriers: a tile unpacked (U), its scores done (S), its P written (P), its
+// readout done (O, which frees the tile's buffers and P).
+constexpr int kTcTok = 64;                       // tokens per tile
+constexpr int kTcBlk = kTcTok / 16;              // 16-token cache blocks per tile
+constexpr int kTcThreads = 416;                  // warps 0-3 rows, 4-11 unpack, 12 MMA issue
+constexpr int kTcUnpack = 256;                   // unpacking threads
+constexpr uint32_t kTcCols = 512;  // the whole tensor memory: one block per SM
+constexpr uint32_t kTcQhi = 0, kTcQlo = 64, kTcS = 128, kTcO = 256, kTcP = 384;  // columns (S: two buffers)
+constexpr int kTcSmemMin = 116 * 1024;  // asking for more than half the shared memory keeps one block per SM
+
+// Shared-memory plan.  Tiles are token-major core matrices: element (token j, dim d) at
+// (j / 8) * 2048 + (d / 8) * 128 + (j % 8) * 16 + (d % 8) * 2 -- a K-major B operand for the
+// scores (LBO 128, SBO 2048) and an MN-major B operand for the readout (LBO 2048, SBO 128).
+struct TcSmem {
+  static constexpr int TILE = kTcTok * kPfD * 2;                 // 16 KiB
+  static constexpr int KHI = 0, KLO = 2 * TILE, VV = 4 * TILE;   // two buffers each
+  static constexpr int NUK = 6 * TILE;                            // float [2][kTcTok]
+  static constexpr int NUV = NUK + 2 * kTcTok * 4;                // float [2][kTcTok]
+  static constexpr int CENT = NUV + 2 * kTcTok * 4;               // [16] (K hi | K lo << 16), [16] V fp16
+  static constexpr int STG = (CENT + 16 * 4 + 16 * 2 + 127) / 128 * 128;  // two packed stages
+};
+
+// Spread the 2-bit fields of a 16-bit value into the low bits of 8 nibbles, and the 8 bits of a
+// byte into bit 0 of 8 nibbles.
+__device__ __forceinline__ uint32_t spread2(uint32_t x) {
+  x = (x | (x << 8)) & 0x00FF00FFu;
+  x = (x | (x << 4)) & 0x0F0F0F0Fu;
+  return (x | (x << 2)) & 0x33333333u;
+}
+__device__ __forceinline__ uint32_t spread1(uint32_t x) {
+  x = (x | (x << 12)) & 0x000F000Fu;
+  x = (x | (x << 6)) & 0x03030303u;
+  return (x | (x << 3)) & 0x11111111u;
+}
+
+// Codebook indices (one per nibble, dim 8 c + e in nibble e) of 8 coordinates of a b-bit
+// sign-magnitude stream whose bytes for those coordinates start at `src` (4-bit: 4 bytes;
+// 3-bit: 2 magnitude bytes at src, the sign byte at sgn; 2-bit: 2 bytes; 1-bit: 1 byte).  A sign
+// bit s and magnitude rank k give index s ? 2^(b-1) + k : 2^(b-1) - 1 - k, i.e. the stored
+// symbol with its magnitude bits inverted when s = 0.
+__device__ __forceinline__ uint32_t codes8(const unsigned char* src, const unsigned char* sgn, int bits) {
+  if (bits == 4) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+    return w ^ (((~w >> 3) & 0x11111111u) * 7u);
+  }
+  if (bits == 3) {
+    const uint32_t m = spread2(*reinterpret_cast<const unsigned short*>(src));
+    const uint32_t s = spread1(*sgn);
+    return (m | (s << 2)) ^ ((~s & 0x11111111u) * 3u);
+  }
+  if (bits == 2) {
+    const uint32_t x = spread2(*reinterpret_cast<const unsigned short*>(src));
+    return x ^ ((~x >> 1) & 0x11111111u);
+  }
+  return spread1(*src);
+}
+
+__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il);
+
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const PrefillParams p) {
+  using SM = TcSmem;
+  extern __shared__ __align__(128) unsigned char smem[];
+  // mbarriers: packed stages [2], unpacked tiles U [2], scores S [2], readouts O [2], P
+  __shared__ __align__(8) unsigned long long s_bars[9];
+  __shared__ uint32_t s_tmem;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slab = blockIdx.y;
+  const int b = slab / p.Hkv, h = slab % p.Hkv;
+  const int r0 = blockIdx.x * kPfRows;
+  const int L = p.seq_len[b];
+  const int Lmin = L - p.nq + 1;
+  const int rlast = min(r0 + kPfRows, p.rows) - 1;
+  const int eblk = max(0, min(L, Lmin + rlast / p.G));
+  const int ntiles = (eblk + kTcTok - 1) / kTcTok;
+  const uint32_t sb = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t bar = (uint32_t)__cvta_generic_to_shared(s_bars);
+  const uint32_t B_STG = bar, B_U = bar + 16, B_S = bar + 32, B_O = bar + 48, B_P = bar + 64;
+  const Cache& C = p.cache;
+  const unsigned kblk = p.kblk, vblk = p.vblk, SB = kTcBlk * (kblk + vblk);
+  bool timed_out = false;
+
+  if (warp == 12) tc_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kTcCols);
+  if (tid == 0) {
+    mbar_init(B_STG, 1);
+    mbar_init(B_STG + 8, 1);
+    mbar_init(B_U, kTcUnpack);
+    mbar_init(B_U + 8, kTcUnpack);
+    mbar_init(B_S, 1);
+    mbar_init(B_S + 8, 1);
+    mbar_init(B_O, 1);
+    mbar_init(B_O + 8, 1);
+    mbar_init(B_P, 128);
+    fence_mbar_init();
+    for (int k = 0; k < 2 && k < ntiles; ++k) {
+      const uint32_t dst = sb + SM::STG + k * SB;
+      pf_issue_stage(C, b, h, k, kTcBlk, kblk, vblk, dst, B_STG + 8 * k);
+    }
+  }
+  // codebooks: key centroids as fp16 hi | lo << 16, value centroids as fp16
+  if (tid < 16) {
+    const float c = __ldg(p.tab.k_c + tid);
+    const __half hi = __float2half_rn(c);
+    const __half lo = __float2half_rn(c - __half2float(hi));
+    reinterpret_cast<uint32_t*>(smem + SM::CENT)[tid] =
+        (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+  } else if (tid < 32) {
+    reinterpret_cast<__half*>(smem + SM::CENT + 64)[tid - 16] = __float2half_rn(__ldg(p.tab.v_c + tid - 16));
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp < 4) {
+    // ---- row owners: the row's queries (fp16 pairs) into tensor memory
+    const int r = tid;
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t* qh = reinterpret_cast<const uint32_t*>(p.qhi + ((long long)slab * p.R_pad + r0 + r) * kPfD);
+    const uint32_t* ql = reinterpret_cast<const uint32_t*>(p.qlo + ((long long)slab * p.R_pad + r0 + r) * kPfD);
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(qh + c0 + i);
+        v[i] = __uint_as_float(x.x); v[i + 1] = __uint_as_float(x.y);
+        v[i + 2] = __uint_as_float(x.z); v[i + 3] = __uint_as_float(x.w);
+      }
+      tc_st32(trow + kTcQhi + c0, v);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(ql + c0 + i);
+        v[i] = __uint_as_float(x.x); v[i + 1] = __uint_as_float(x.y);
+        v[i + 2] = __uint_as_float(x.z); v[i + 3] = __uint_as_float(x.w);
+      }
+      tc_st32(trow + kTcQlo + c0, v);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // the queries are in tensor memory before the first score MMA
+  tc_fence_after();
+
+  if (warp >= 4 && warp < 12) {
+    // ---- unpack: thread pt takes 8-coordinate chunk c of tokens 8 jg + t8 (jg = pt / 128 + 2 i,
+    // i = 0..3), so the eight threads of a quarter warp write the eight 16-byte rows of one core
+    // matrix
+    const int pt = tid - 128, c = (pt >> 3) & 15, t8 = pt & 7, jg0 = pt >> 7;
+    const uint32_t* kcent = reinterpret_cast<const uint32_t*>(smem + SM::CENT);
+    const unsigned short* vcent = reinterpret_cast<const unsigned short*>(smem + SM::CENT + 64);
+    const int g = c >> 1, hv = c & 1;  // the chunk's 16-coordinate value group and half of it
+    for (int k = 0; k < ntiles; ++k) {
+      const int bf = k & 1, t0 = k * kTcTok;
+      // the tile two back has been read out: its buffers are free
+      if (k >= 2 && !mbar_wait(B_O + 8 * bf, (uint32_t)((k - 2) >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+      if (!mbar_wait(B_STG + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+      const unsigned char* stg = smem + SM::STG + bf * SB;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int j = 8 * (jg0 + 2 * it) + t8, pos = j & (tqi::kTileTokens - 1);
+        const bool ok = t0 + j < L;
+        const unsigned char* kp = stg + (j >> 4) * kblk;             // the token's K block
+        const unsigned char* vp = stg + kTcBlk * kblk + (j >> 4) * vblk;  // and V block
+        uint4 khi = make_uint4(0, 0, 0, 0), klo = khi, vv = khi;
+        float nk = 0.f, nv = 0.f;
+        if (ok) {
+          const unsigned char* kr = kp + C.off[tqi::R_K_CODES] + pos * C.rec[tqi::R_K_CODES];
+          const int kb = p.kbits;
+          const uint32_t kc = codes8(kr + (kb == 1 ? c : kb == 4 ? 4 * c : 2 * c), kr + kPfD / 4 + c, kb);
+          // value streams by 16-coordinate groups: W bytes of the W-bit stream per chunk
+          const unsigned char* vr = vp + C.off[tqi::R_V_CODES];
+          const int vb = p.vbits;
+          const int W = vb == 3 ? 2 : vb;
+          const uint32_t vc = codes8(vr + g * 32 * W + pos * 2 * W + hv * W,
+                                     vr + tqi::kTileTokens * (kPfD / 4) + g * 32 + pos * 2 + hv, vb);
+          uint32_t kh[4], kl[4], vw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t a = kcent[(kc >> (8 * e)) & 15u], bq = kcent[(kc >> (8 * e + 4)) & 15u];
+            kh[e] = __byte_perm(a, bq, 0x5410);
+            kl[e] = __byte_perm(a, bq, 0x7632);
+            vw[e] = (uint32_t)vcent[(vc >> (8 * e)) & 15u] | ((uint32_t)vcent[(vc >> (8 * e + 4)) & 15u] << 16);
+          }
+          khi = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+          klo = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+          vv = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+          nk = *reinterpret_cast<const float*>(kp + C.off[tqi::R_K_NORM] + 4 * pos);
+          nv = *reinterpret_cast<const float*>(vp + C.off[tqi::R_V_NORM] + 4 * pos);
+        }
+        const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
+        *reinterpret_cast<uint4*>(smem + SM::KHI + bf * SM::TILE + off) = khi;
+        *reinterpret_cast<uint4*>(smem + SM::KLO + bf * SM::TILE + off) = klo;
+        *reinterpret_cast<uint4*>(smem + SM::VV + bf * SM::TILE + off) = vv;
+        if (c == 0) {
+          reinterpret_cast<float*>(smem + SM::NUK)[kTcTok * bf + j] = nk;
+          reinterpret_cast<float*>(smem + SM::NUV)[kTcTok * bf + j] = nv;
+        }
+      }
+      tc_fence_smem();  // the tile's rows are visible to the tensor cores' operand reads
+      tc_mbar_arrive(B_U + 8 * bf);
+      asm volatile("bar.sync 1, 256;\n" ::: "memory");  // every unpacking thread is done with the stage
+      if (pt == 0 && k + 2 < ntiles) {
+        fence_proxy_async_shared();
+        const uint32_t dst = sb + SM::STG + bf * SB;
+        pf_issue_stage(C, b, h, k + 2, kTcBlk, kblk, vblk, dst, B_STG + 8 * bf);
+      }
+    }
+  }
+
+  if (warp == 12 && lane == 0) {
+    // ---- MMA issue: the scores of tile k as soon as it is unpacked, then the readout of tile
+    // k - 1 as soon as its P is written
+    constexpr uint32_t idS = tc_idesc_f16(128, kTcTok), idO = tc_idesc_f16(128, kPfD, true);
+    auto readout = [&](int kk) {
+      if (!mbar_wait(B_P, (uint32_t)kk & 1u, kPfWaitLimit)) timed_out = true;
+      tc_fence_after();
+      const uint32_t vb = sb + SM::VV + (kk & 1) * SM::TILE;
+#pragma unroll
+      for (int ks = 0; ks < kTcTok / 16; ++ks)
+        tc_mma_f16_ta(tmem + kTcO, tmem + kTcP + 8 * ks, tc_sdesc(vb + 4096 * ks, 2048, 128), idO,
+                      (kk > 0 || ks > 0) ? 1u : 0u);
+      tc_commit(B_O + 8 * (kk & 1));
+    };
+    for (int k = 0; k < ntiles; ++k) {
+      const int bf = k & 1;
+      if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+      tc_fence_after();
+      const uint32_t kh = sb + SM::KHI + bf * SM::TILE, kl = sb + SM::KLO + bf * SM::TILE;
+      const uint32_t dS = tmem + kTcS + kTcTok * bf;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * ks, tc_sdesc(kh + 256 * ks, 128, 2048), idS, ks > 0 ? 1u : 0u);
+        tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * ks, tc_sdesc(kh + 256 * ks, 128, 2048), idS, 1u);
+        tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * ks, tc_sdesc(kl + 256 * ks, 128, 2048), idS, 1u);
+      }
+      tc_commit(B_S + 8 * bf);
+      if (k >= 1) readout(k - 1);
+    }
+    if (ntiles > 0) readout(ntiles - 1);
+  }
+
+  if (warp < 4) {
+    // ---- row owners: online softmax (log2 domain) over the tiles, then o = R_V^T O / l
+    const int r = tid, rr = r0 + r;
+    const int er = rr < p.rows ? Lmin + rr / p.G : 0;  // row rr sees tokens [0, er)
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    const float* nuK = reinterpret_cast<const float*>(smem + SM::NUK);
+    const float* nuV = reinterpret_cast<const float*>(smem + SM::NUV);
+    float m = kPfFloor, l = 0.f;
+    for (int k = 0; k < ntiles; ++k) {
+      const int bf = k & 1, t0 = k * kTcTok;
+      if (!mbar_wait(B_S + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+      if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;  // the norms
+      tc_fence_after();
+      float s[kTcTok];
+      {
+        float h0[32], h1[32];
+        tc_ld32(trow + kTcS + kTcTok * bf, h0);
+        tc_ld32(trow + kTcS + kTcTok * bf + 32, h1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          s[j] = h0[j];
+          s[32 + j] = h1[j];
+        }
+      }
+      float mx = kPfFloor;
+#pragma unroll
+      for (int j = 0; j < kTcTok; ++j) {
+        s[j] = t0 + j < er ? s[j] * (nuK[kTcTok * bf + j] * p.score_scale) : -INFINITY;
+        mx = fmaxf(mx, s[j]);
+      }
+      const float mn = fmaxf(m, mx);
+      const float alpha = pf_ex2(m - mn);
+      float ps = 0.f;
+      uint32_t pw[kTcTok / 2];
+#pragma unroll
+      for (int j = 0; j < kTcTok; j += 2) {
+        const float pa = pf_ex2(s[j] - mn), pb = pf_ex2(s[j + 1] - mn);
+        ps += pa + pb;
+        pw[j / 2] = pack_half2(pa * nuV[kTcTok * bf + j], pb * nuV[kTcTok * bf + j + 1]);
+      }
+      l = l * alpha + ps;
+      m = mn;
+      if (k >= 1) {  // the readout of tile k - 1 is done: O is settled and P's columns are free
+        if (!mbar_wait(B_O + 8 * ((k - 1) & 1), (uint32_t)((k - 1) >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+        tc_fence_after();
+        if (__any_sync(kFull, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float o[32];
+            tc_ld32(trow + kTcO + 32 * c4, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tc_st32(trow + kTcO + 32 * c4, o);
+          }
+        }
+      }
+      {
+        float pf[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pf[i] = __uint_as_float(pw[i]);
+        tc_st32(trow + kTcP, pf);
+      }
+      tc_fence_before();
+      tc_mbar_arrive(B_P);
+    }
+    if (ntiles > 0) {
+      if (!mbar_wait(B_O + 8 * ((ntiles - 1) & 1), (uint32_t)((ntiles - 1) >> 1) & 1u, kPfWaitLimit))
+        timed_out = true;
+      tc_fence_after();
+    }
+    tc_out_row(p, b, h, rr, ntiles > 0 ? trow + kTcO : 0u, l > 0.f ? 1.f / l : 0.f);
+  }
+
+  tc_fence_before();
+  __syncthreads();  // every MMA has completed (the row owners waited for the last readout)
+  if (warp == 12) {
+    tc_fence_after();
+    tc_dealloc(tmem, kTcCols);
+  }
+  if (timed_out) atomicExch(p.err, TQ_DEVERR_WAIT_TIMEOUT);
+}
+
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Row rr of the slab's output from its accumulator (128 columns from t_o; t_o = 0: no token,
+// the row is zero): o = O il, then, when the value side is rotated, x = D_V H o / sqrt(d) --
+// butterflies over coordinate bits 0 .. 4 within each 32-column piece (written back), then over
+// bits 5 and 6 across the four pieces, 8 columns at a time -- stored to out.  Every thread of
+// the warp calls (tensor-memory loads are warp-wide); rows past the chunk store nothing.
+__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il) {
+  const bool store = rr < p.rows;
+  const int Hq = p.Hkv * p.G;
+  float* dst = store ? p.out + (((long long)b * p.nq + rr / p.G) * Hq + h * p.G + rr % p.G) * kPfD : nullptr;
+  const bool have = __any_sync(kFull, t_o != 0u);  // uniform: every row of the block shares the tiles
+#pragma unroll 1
+  for (int c4 = 0; c4 < 4; ++c4) {
+    float v[32];
+    if (have) tc_ld32(t_o + 32 * c4, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = have ? v[i] * il : 0.f;
+    if (p.v_rotate) {
+#pragma unroll
+      for (int hb = 1; hb < 32; hb <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if ((i & hb) == 0) {
+            const float x0 = v[i], x1 = v[i + hb];
+            v[i] = x0 + x1;
+            v[i + hb] = x0 - x1;
+          }
+        }
+      }
+      if (have) tc_st32(t_o + 32 * c4, v);
+    } else if (store) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + 32 * c4 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+  }
+  if (!p.v_rotate) return;
+  const float rs = 1.f / sqrtf((float)kPfD);
+#pragma unroll 1
+  for (int i0 = 0; i0 < 32; i0 += 8) {
+    float v[4][8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (have) {
+        tc_ld8(t_o + 32 * q + i0, v[q]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[q][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int hq = 1; hq < 4; hq <<= 1) {  // coordinate bits 5 (hq = 1) and 6 (hq = 2)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if ((q & hq) == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x0 = v[q][i], x1 = v[q + hq][i];
+            v[q][i] = x0 + x1;
+            v[q + hq][i] = x0 - x1;
+          }
+        }
+      }
+    }
+    if (store) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int d0 = 32 * q + i0;
+        float w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = v[q][i] * (__ldg(p.tab.v_sign + d0 + i) * rs);
+        *reinterpret_cast<float4*>(dst + d0) = make_float4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<float4*>(dst + d0 + 4) = make_float4(w[4], w[5], w[6], w[7]);
+      }
+    }
+  }
+}
+
 size_t pf_align(size_t x) { return (x + 255) / 256 * 256; }
 
 tq_status pf_fail(const char* what, cudaError_t e) {
@@ -587,6 +1017,14 @@ cudaError_t launch_pf(const PrefillParams& p, dim3 grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<KQ, VQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   prefill_kernel<KQ, VQ><<<grid, kPfWarps * 32, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pf_tc(const PrefillParams& p, dim3 grid, cudaStream_t s) {
+  const int smem = std::max(TcSmem::STG + 4 * (int)(p.kblk + p.vblk), kTcSmemMin);
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  prefill_tc_kernel<<<grid, kTcThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -670,7 +1108,7 @@ tq_status launch_prefill(const tq_context* ctx, const void* cache, const float* 
   if (kq && vq) e = launch_pf<true, true>(p, grid, s);
   else if (kq) e = launch_pf<true, false>(p, grid, s);
   else if (vq) e = launch_pf<false, true>(p, grid, s);
-  else e = launch_pf<false, false>(p, grid, s);
+  else e = launch_pf_tc(p, grid, s);  // no sketch: the tcgen05 kernel
   if (e != cudaSuccess) return tqd::pf_fail("prefill", e);
   return TQ_OK;
 }
