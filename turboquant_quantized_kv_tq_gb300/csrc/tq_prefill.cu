@@ -586,16 +586,23 @@ __global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_kernel(const Prefill
 //   S[128 x 64]   = Q_hi K_hi^T + Q_lo K_hi^T + Q_hi K_lo^T      (tcgen05.mma, M = 128, N = 64)
 //   O[128 x 128] += P V,  P = 2^(s - m) nu_V as fp16               (tcgen05.mma, M = 128, N = 128)
 // Q_hi, Q_lo, S (two buffers), P and O live in tensor memory; the unpacked K and V tiles in
-// shared memory (two buffers).  Warps 0-3 own the rows (thread r <-> row r <-> lane r): they
-// load the queries into tensor memory, run the online softmax on S and write P, rescale O when
-// a row's maximum rises, and finish o = R_V^T O / l.  Warps 4-11 unpack the tiles, which bulk
-// copies bring into two packed stages.  One thread of warp 12 issues the MMAs.  The stages hand
+// shared memory (three buffers).  Warps 0-7 own the rows: warp w takes the rows of tensor-memory
+// lanes 32 (w % 4) .. + 31 and tokens 32 (w / 4) .. + 31 of every tile.  They load the queries
+// into tensor memory, run the online softmax on S (the two threads of a row share their maxima
+// through shared memory) and write P, rescale O when a row's maximum rises, and finish
+// o = R_V^T O / l.  Warps 8-15 unpack the tiles, which bulk copies bring into packed stages; with
+// three tile buffers the unpacking runs up to two tiles ahead.  One thread of warp 16 issues the
+// MMAs, each as soon as its inputs are ready: a tile's scores when it is unpacked, its readout
+// when its P is written.  The stages hand
 // over through mbarriers: a tile unpacked (U), its scores done (S), its P written (P), its
 // readout done (O, which frees the tile's buffers and P).
 constexpr int kTcTok = 64;                       // tokens per tile
 constexpr int kTcBlk = kTcTok / 16;              // 16-token cache blocks per tile
-constexpr int kTcThreads = 416;                  // warps 0-3 rows, 4-11 unpack, 12 MMA issue
+constexpr int kTcNB = 3;                         // tile buffers (and packed stages): unpacking runs two tiles ahead
+constexpr int kTcThreads = 544;                  // warps 0-7 rows, 8-15 unpack, 16 MMA issue
+constexpr int kTcRowThreads = 256;               // two threads per row, 32 of a tile's tokens each
 constexpr int kTcUnpack = 256;                   // unpacking threads
+constexpr int kTcIssueWarp = 16;
 constexpr uint32_t kTcCols = 512;  // the whole tensor memory: one block per SM
 constexpr uint32_t kTcQhi = 0, kTcQlo = 64, kTcS = 128, kTcO = 256, kTcP = 384;  // columns (S: two buffers)
 constexpr int kTcSmemMin = 116 * 1024;  // asking for more than half the shared memory keeps one block per SM
@@ -605,11 +612,12 @@ constexpr int kTcSmemMin = 116 * 1024;  // asking for more than half the shared 
 // scores (LBO 128, SBO 2048) and an MN-major B operand for the readout (LBO 2048, SBO 128).
 struct TcSmem {
   static constexpr int TILE = kTcTok * kPfD * 2;                 // 16 KiB
-  static constexpr int KHI = 0, KLO = 2 * TILE, VV = 4 * TILE;   // two buffers each
-  static constexpr int NUK = 6 * TILE;                            // float [2][kTcTok]
-  static constexpr int NUV = NUK + 2 * kTcTok * 4;                // float [2][kTcTok]
-  static constexpr int CENT = NUV + 2 * kTcTok * 4;               // [16] (K hi | K lo << 16), [16] V fp16
-  static constexpr int STG = (CENT + 16 * 4 + 16 * 2 + 127) / 128 * 128;  // two packed stages
+  static constexpr int KHI = 0, KLO = kTcNB * TILE, VV = 2 * kTcNB * TILE;  // kTcNB buffers each
+  static constexpr int NUK = 3 * kTcNB * TILE;                    // float [kTcNB][kTcTok]
+  static constexpr int NUV = NUK + kTcNB * kTcTok * 4;            // float [kTcNB][kTcTok]
+  static constexpr int CENT = NUV + kTcNB * kTcTok * 4;           // [16] (K hi | K lo << 16), [16] V fp16
+  static constexpr int XCH = CENT + 128;  // float [3][2 halves][128 rows]: maxima (by tile parity), then l
+  static constexpr int STG = (XCH + 3 * 2 * 128 * 4 + 127) / 128 * 128;  // kTcNB packed stages
 };
 
 // Spread the 2-bit fields of a 16-bit value into the low bits of 8 nibbles, and the 8 bits of a
@@ -647,13 +655,13 @@ __device__ __forceinline__ uint32_t codes8(const unsigned char* src, const unsig
   return spread1(*src);
 }
 
-__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il);
+__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf);
 
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const PrefillParams p) {
   using SM = TcSmem;
   extern __shared__ __align__(128) unsigned char smem[];
-  // mbarriers: packed stages [2], unpacked tiles U [2], scores S [2], readouts O [2], P
-  __shared__ __align__(8) unsigned long long s_bars[9];
+  // mbarriers: packed stages [3], unpacked tiles U [3], scores S [2], readouts O [3], P
+  __shared__ __align__(8) unsigned long long s_bars[12];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slab = blockIdx.y;
@@ -666,24 +674,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
   const int ntiles = (eblk + kTcTok - 1) / kTcTok;
   const uint32_t sb = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t bar = (uint32_t)__cvta_generic_to_shared(s_bars);
-  const uint32_t B_STG = bar, B_U = bar + 16, B_S = bar + 32, B_O = bar + 48, B_P = bar + 64;
+  const uint32_t B_STG = bar, B_U = bar + 24, B_S = bar + 48, B_O = bar + 64, B_P = bar + 88;
   const Cache& C = p.cache;
   const unsigned kblk = p.kblk, vblk = p.vblk, SB = kTcBlk * (kblk + vblk);
   bool timed_out = false;
 
-  if (warp == 12) tc_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kTcCols);
+  if (warp == kTcIssueWarp) tc_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kTcCols);
   if (tid == 0) {
-    mbar_init(B_STG, 1);
-    mbar_init(B_STG + 8, 1);
-    mbar_init(B_U, kTcUnpack);
-    mbar_init(B_U + 8, kTcUnpack);
+    for (int i = 0; i < kTcNB; ++i) {
+      mbar_init(B_STG + 8 * i, 1);
+      mbar_init(B_U + 8 * i, kTcUnpack);
+      mbar_init(B_O + 8 * i, 1);
+    }
     mbar_init(B_S, 1);
     mbar_init(B_S + 8, 1);
-    mbar_init(B_O, 1);
-    mbar_init(B_O + 8, 1);
-    mbar_init(B_P, 128);
+    mbar_init(B_P, kTcRowThreads);
     fence_mbar_init();
-    for (int k = 0; k < 2 && k < ntiles; ++k) {
+    for (int k = 0; k < kTcNB && k < ntiles; ++k) {
       const uint32_t dst = sb + SM::STG + k * SB;
       pf_issue_stage(C, b, h, k, kTcBlk, kblk, vblk, dst, B_STG + 8 * k);
     }
@@ -732,19 +739,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
   __syncthreads();  // the queries are in tensor memory before the first score MMA
   tc_fence_after();
 
-  if (warp >= 4 && warp < 12) {
+  if (warp >= 8 && warp < 16) {
     // ---- unpack: thread pt takes 8-coordinate chunk c of tokens 8 jg + t8 (jg = pt / 128 + 2 i,
     // i = 0..3), so the eight threads of a quarter warp write the eight 16-byte rows of one core
     // matrix
-    const int pt = tid - 128, c = (pt >> 3) & 15, t8 = pt & 7, jg0 = pt >> 7;
+    const int pt = tid - 256, c = (pt >> 3) & 15, t8 = pt & 7, jg0 = pt >> 7;
+    const int kbits = p.kbits, vbits = p.vbits, vW = vbits == 3 ? 2 : vbits;
+    const unsigned kc_off = C.off[tqi::R_K_CODES], kc_rec = C.rec[tqi::R_K_CODES];
+    const unsigned kn_off = C.off[tqi::R_K_NORM], vc_off = C.off[tqi::R_V_CODES], vn_off = C.off[tqi::R_V_NORM];
+    const int kbyte = kbits == 1 ? c : kbits == 4 ? 4 * c : 2 * c;  // the chunk's first code byte in a key record
+    const float kscale = p.score_scale;
     const uint32_t* kcent = reinterpret_cast<const uint32_t*>(smem + SM::CENT);
     const unsigned short* vcent = reinterpret_cast<const unsigned short*>(smem + SM::CENT + 64);
     const int g = c >> 1, hv = c & 1;  // the chunk's 16-coordinate value group and half of it
     for (int k = 0; k < ntiles; ++k) {
-      const int bf = k & 1, t0 = k * kTcTok;
-      // the tile two back has been read out: its buffers are free
-      if (k >= 2 && !mbar_wait(B_O + 8 * bf, (uint32_t)((k - 2) >> 1) & 1u, kPfWaitLimit)) timed_out = true;
-      if (!mbar_wait(B_STG + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+      const int bf = k % kTcNB, t0 = k * kTcTok;
+      // the tile kTcNB back has been read out: its buffers are free
+      if (k >= kTcNB && !mbar_wait(B_O + 8 * bf, (uint32_t)(k / kTcNB - 1) & 1u, kPfWaitLimit)) timed_out = true;
+      if (!mbar_wait(B_STG + 8 * bf, (uint32_t)(k / kTcNB) & 1u, kPfWaitLimit)) timed_out = true;
       const unsigned char* stg = smem + SM::STG + bf * SB;
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
@@ -752,18 +764,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         const bool ok = t0 + j < L;
         const unsigned char* kp = stg + (j >> 4) * kblk;             // the token's K block
         const unsigned char* vp = stg + kTcBlk * kblk + (j >> 4) * vblk;  // and V block
-        uint4 khi = make_uint4(0, 0, 0, 0), klo = khi, vv = khi;
-        float nk = 0.f, nv = 0.f;
-        if (ok) {
-          const unsigned char* kr = kp + C.off[tqi::R_K_CODES] + pos * C.rec[tqi::R_K_CODES];
-          const int kb = p.kbits;
-          const uint32_t kc = codes8(kr + (kb == 1 ? c : kb == 4 ? 4 * c : 2 * c), kr + kPfD / 4 + c, kb);
+        // (tokens past the sequence: the stage holds stale bytes there, read but replaced by zeros)
+        uint4 khi, klo, vv;
+        float nk, nv;
+        {
+          const unsigned char* kr = kp + kc_off + pos * kc_rec;
+          const uint32_t kc = codes8(kr + kbyte, kr + kPfD / 4 + c, kbits);
           // value streams by 16-coordinate groups: W bytes of the W-bit stream per chunk
-          const unsigned char* vr = vp + C.off[tqi::R_V_CODES];
-          const int vb = p.vbits;
-          const int W = vb == 3 ? 2 : vb;
-          const uint32_t vc = codes8(vr + g * 32 * W + pos * 2 * W + hv * W,
-                                     vr + tqi::kTileTokens * (kPfD / 4) + g * 32 + pos * 2 + hv, vb);
+          const unsigned char* vr = vp + vc_off;
+          const uint32_t vc = codes8(vr + g * 32 * vW + pos * 2 * vW + hv * vW,
+                                     vr + tqi::kTileTokens * (kPfD / 4) + g * 32 + pos * 2 + hv, vbits);
           uint32_t kh[4], kl[4], vw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -772,11 +782,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
             kl[e] = __byte_perm(a, bq, 0x7632);
             vw[e] = (uint32_t)vcent[(vc >> (8 * e)) & 15u] | ((uint32_t)vcent[(vc >> (8 * e + 4)) & 15u] << 16);
           }
-          khi = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-          klo = make_uint4(kl[0], kl[1], kl[2], kl[3]);
-          vv = make_uint4(vw[0], vw[1], vw[2], vw[3]);
-          nk = *reinterpret_cast<const float*>(kp + C.off[tqi::R_K_NORM] + 4 * pos);
-          nv = *reinterpret_cast<const float*>(vp + C.off[tqi::R_V_NORM] + 4 * pos);
+          const uint32_t z = ok ? 0xffffffffu : 0u;
+          khi = make_uint4(kh[0] & z, kh[1] & z, kh[2] & z, kh[3] & z);
+          klo = make_uint4(kl[0] & z, kl[1] & z, kl[2] & z, kl[3] & z);
+          vv = make_uint4(vw[0] & z, vw[1] & z, vw[2] & z, vw[3] & z);
+          nk = ok ? *reinterpret_cast<const float*>(kp + kn_off + 4 * pos) * kscale : 0.f;  // nu_K log2(e) / sqrt(d)
+          nv = ok ? *reinterpret_cast<const float*>(vp + vn_off + 4 * pos) : 0.f;
         }
         const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
         *reinterpret_cast<uint4*>(smem + SM::KHI + bf * SM::TILE + off) = khi;
@@ -790,122 +801,138 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       tc_fence_smem();  // the tile's rows are visible to the tensor cores' operand reads
       tc_mbar_arrive(B_U + 8 * bf);
       asm volatile("bar.sync 1, 256;\n" ::: "memory");  // every unpacking thread is done with the stage
-      if (pt == 0 && k + 2 < ntiles) {
+      if (pt == 0 && k + kTcNB < ntiles) {
         fence_proxy_async_shared();
         const uint32_t dst = sb + SM::STG + bf * SB;
-        pf_issue_stage(C, b, h, k + 2, kTcBlk, kblk, vblk, dst, B_STG + 8 * bf);
+        pf_issue_stage(C, b, h, k + kTcNB, kTcBlk, kblk, vblk, dst, B_STG + 8 * bf);
       }
     }
   }
 
-  if (warp == 12 && lane == 0) {
-    // ---- MMA issue: the scores of tile k as soon as it is unpacked, then the readout of tile
-    // k - 1 as soon as its P is written
+  if (warp == kTcIssueWarp && lane == 0) {
+    // ---- MMA issue, each as soon as its inputs are ready: the scores of tile ks once it is
+    // unpacked (and at most one tile ahead of the readouts: S(ks) reuses S(ks - 2)'s columns,
+    // free once P(ks - 2) has been read), the readout of tile kr once its P is written
     constexpr uint32_t idS = tc_idesc_f16(128, kTcTok), idO = tc_idesc_f16(128, kPfD, true);
-    auto readout = [&](int kk) {
-      if (!mbar_wait(B_P, (uint32_t)kk & 1u, kPfWaitLimit)) timed_out = true;
-      tc_fence_after();
-      const uint32_t vb = sb + SM::VV + (kk & 1) * SM::TILE;
+    int ks = 0, kr = 0;
+    uint32_t idle = 0;
+    while (kr < ntiles) {
+      bool moved = false;
+      if (ks < ntiles && ks <= kr + 1 && mbar_wait(B_U + 8 * (ks % kTcNB), (uint32_t)(ks / kTcNB) & 1u, 1)) {
+        tc_fence_after();
+        const int bf = ks % kTcNB;
+        const uint32_t kh = sb + SM::KHI + bf * SM::TILE, kl = sb + SM::KLO + bf * SM::TILE;
+        const uint32_t dS = tmem + kTcS + kTcTok * (ks & 1);
 #pragma unroll
-      for (int ks = 0; ks < kTcTok / 16; ++ks)
-        tc_mma_f16_ta(tmem + kTcO, tmem + kTcP + 8 * ks, tc_sdesc(vb + 4096 * ks, 2048, 128), idO,
-                      (kk > 0 || ks > 0) ? 1u : 0u);
-      tc_commit(B_O + 8 * (kk & 1));
-    };
-    for (int k = 0; k < ntiles; ++k) {
-      const int bf = k & 1;
-      if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
-      tc_fence_after();
-      const uint32_t kh = sb + SM::KHI + bf * SM::TILE, kl = sb + SM::KLO + bf * SM::TILE;
-      const uint32_t dS = tmem + kTcS + kTcTok * bf;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * ks, tc_sdesc(kh + 256 * ks, 128, 2048), idS, ks > 0 ? 1u : 0u);
-        tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * ks, tc_sdesc(kh + 256 * ks, 128, 2048), idS, 1u);
-        tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * ks, tc_sdesc(kl + 256 * ks, 128, 2048), idS, 1u);
+        for (int kk = 0; kk < 8; ++kk) {
+          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, kk > 0 ? 1u : 0u);
+          tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, 1u);
+          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kl + 256 * kk, 128, 2048), idS, 1u);
+        }
+        tc_commit(B_S + 8 * (ks & 1));
+        ++ks;
+        moved = true;
       }
-      tc_commit(B_S + 8 * bf);
-      if (k >= 1) readout(k - 1);
+      if (kr < ks && mbar_wait(B_P, (uint32_t)kr & 1u, 1)) {
+        tc_fence_after();
+        const uint32_t vb = sb + SM::VV + (kr % kTcNB) * SM::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kTcTok / 16; ++kk)
+          tc_mma_f16_ta(tmem + kTcO, tmem + kTcP + 8 * kk, tc_sdesc(vb + 4096 * kk, 2048, 128), idO,
+                        (kr > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(B_O + 8 * (kr % kTcNB));
+        ++kr;
+        moved = true;
+      }
+      if (moved) {
+        idle = 0;
+      } else if (++idle > 4u * kPfWaitLimit) {  // nothing became ready: give up (the error word says so)
+        timed_out = true;
+        break;
+      }
     }
-    if (ntiles > 0) readout(ntiles - 1);
   }
 
-  if (warp < 4) {
-    // ---- row owners: online softmax (log2 domain) over the tiles, then o = R_V^T O / l
-    const int r = tid, rr = r0 + r;
+  if (warp < 8) {
+    // ---- row owners: online softmax (log2 domain) over the tiles, then o = R_V^T O / l.  Thread
+    // (q, hf) of row r = 32 q + lane takes tokens 32 hf .. 32 hf + 31 of each tile.
+    const int q = warp & 3, hf = warp >> 2, r = 32 * q + lane, rr = r0 + r;
     const int er = rr < p.rows ? Lmin + rr / p.G : 0;  // row rr sees tokens [0, er)
-    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-    const float* nuK = reinterpret_cast<const float*>(smem + SM::NUK);
-    const float* nuV = reinterpret_cast<const float*>(smem + SM::NUV);
-    float m = kPfFloor, l = 0.f;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    float* xch = reinterpret_cast<float*>(smem + SM::XCH);  // [tile parity][half][row]
+    float m = kPfFloor, l = 0.f;  // l: this thread's share of the row sum
     for (int k = 0; k < ntiles; ++k) {
-      const int bf = k & 1, t0 = k * kTcTok;
-      if (!mbar_wait(B_S + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
-      if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;  // the norms
+      const int bf = k % kTcNB, sbf = k & 1, t0 = k * kTcTok + 32 * hf;
+      if (!mbar_wait(B_S + 8 * sbf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+      if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k / kTcNB) & 1u, kPfWaitLimit)) timed_out = true;  // the norms
       tc_fence_after();
-      float s[kTcTok];
-      {
-        float h0[32], h1[32];
-        tc_ld32(trow + kTcS + kTcTok * bf, h0);
-        tc_ld32(trow + kTcS + kTcTok * bf + 32, h1);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          s[j] = h0[j];
-          s[32 + j] = h1[j];
-        }
-      }
+      float s[32];
+      tc_ld32(trow + kTcS + kTcTok * sbf + 32 * hf, s);
+      const float4* nk4 = reinterpret_cast<const float4*>(smem + SM::NUK) + (kTcTok * bf + 32 * hf) / 4;
       float mx = kPfFloor;
 #pragma unroll
-      for (int j = 0; j < kTcTok; ++j) {
-        s[j] = t0 + j < er ? s[j] * (nuK[kTcTok * bf + j] * p.score_scale) : -INFINITY;
-        mx = fmaxf(mx, s[j]);
+      for (int j = 0; j < 32; j += 4) {
+        const float4 n = nk4[j / 4];  // nu_K log2(e) / sqrt(d)
+        s[j] *= n.x; s[j + 1] *= n.y; s[j + 2] *= n.z; s[j + 3] *= n.w;
       }
-      const float mn = fmaxf(m, mx);
-      const float alpha = pf_ex2(m - mn);
-      float ps = 0.f;
-      uint32_t pw[kTcTok / 2];
+      if (t0 + 32 > er) {  // the tile reaches this row's end
 #pragma unroll
-      for (int j = 0; j < kTcTok; j += 2) {
-        const float pa = pf_ex2(s[j] - mn), pb = pf_ex2(s[j + 1] - mn);
-        ps += pa + pb;
-        pw[j / 2] = pack_half2(pa * nuV[kTcTok * bf + j], pb * nuV[kTcTok * bf + j + 1]);
+        for (int j = 0; j < 32; ++j) s[j] = t0 + j < er ? s[j] : -INFINITY;
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, s[j]);
+      // the row's maximum over both halves
+      xch[(sbf * 2 + hf) * 128 + r] = mx;
+      asm volatile("bar.sync 2, 256;\n" ::: "memory");
+      const float mn = fmaxf(m, fmaxf(mx, xch[(sbf * 2 + (hf ^ 1)) * 128 + r]));
+      const float alpha = pf_ex2(m - mn);
+      const float4* nv4 = reinterpret_cast<const float4*>(smem + SM::NUV) + (kTcTok * bf + 32 * hf) / 4;
+      float ps = 0.f;
+      uint32_t pw[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 n = nv4[j / 4];
+        const float p0 = pf_ex2(s[j] - mn), p1 = pf_ex2(s[j + 1] - mn);
+        const float p2 = pf_ex2(s[j + 2] - mn), p3 = pf_ex2(s[j + 3] - mn);
+        ps += (p0 + p1) + (p2 + p3);
+        pw[j / 2] = pack_half2(p0 * n.x, p1 * n.y);
+        pw[j / 2 + 1] = pack_half2(p2 * n.z, p3 * n.w);
       }
       l = l * alpha + ps;
       m = mn;
       if (k >= 1) {  // the readout of tile k - 1 is done: O is settled and P's columns are free
-        if (!mbar_wait(B_O + 8 * ((k - 1) & 1), (uint32_t)((k - 1) >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+        if (!mbar_wait(B_O + 8 * ((k - 1) % kTcNB), (uint32_t)((k - 1) / kTcNB) & 1u, kPfWaitLimit)) timed_out = true;
         tc_fence_after();
-        if (__any_sync(kFull, alpha != 1.f)) {
+        if (__any_sync(kFull, alpha != 1.f)) {  // this thread's half of the row's accumulator
 #pragma unroll 1
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c4 = 0; c4 < 2; ++c4) {
             float o[32];
-            tc_ld32(trow + kTcO + 32 * c4, o);
+            tc_ld32(trow + kTcO + 64 * hf + 32 * c4, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc_st32(trow + kTcO + 32 * c4, o);
+            tc_st32(trow + kTcO + 64 * hf + 32 * c4, o);
           }
         }
       }
-      {
-        float pf[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pf[i] = __uint_as_float(pw[i]);
-        tc_st32(trow + kTcP, pf);
-      }
+      tc_st16(trow + kTcP + 16 * hf, pw);
       tc_fence_before();
       tc_mbar_arrive(B_P);
     }
     if (ntiles > 0) {
-      if (!mbar_wait(B_O + 8 * ((ntiles - 1) & 1), (uint32_t)((ntiles - 1) >> 1) & 1u, kPfWaitLimit))
+      if (!mbar_wait(B_O + 8 * ((ntiles - 1) % kTcNB), (uint32_t)((ntiles - 1) / kTcNB) & 1u, kPfWaitLimit))
         timed_out = true;
       tc_fence_after();
     }
-    tc_out_row(p, b, h, rr, ntiles > 0 ? trow + kTcO : 0u, l > 0.f ? 1.f / l : 0.f);
+    // the row sum over both halves
+    xch[(4 + hf) * 128 + r] = l;
+    asm volatile("bar.sync 2, 256;\n" ::: "memory");
+    const float lt = l + xch[(4 + (hf ^ 1)) * 128 + r];
+    tc_out_row(p, b, h, rr, ntiles > 0 ? trow + kTcO : 0u, lt > 0.f ? 1.f / lt : 0.f, hf);
   }
 
   tc_fence_before();
   __syncthreads();  // every MMA has completed (the row owners waited for the last readout)
-  if (warp == 12) {
+  if (warp == kTcIssueWarp) {
     tc_fence_after();
     tc_dealloc(tmem, kTcCols);
   }
@@ -925,15 +952,17 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
 // Row rr of the slab's output from its accumulator (128 columns from t_o; t_o = 0: no token,
 // the row is zero): o = O il, then, when the value side is rotated, x = D_V H o / sqrt(d) --
 // butterflies over coordinate bits 0 .. 4 within each 32-column piece (written back), then over
-// bits 5 and 6 across the four pieces, 8 columns at a time -- stored to out.  Every thread of
-// the warp calls (tensor-memory loads are warp-wide); rows past the chunk store nothing.
-__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il) {
+// bits 5 and 6 across the four pieces, 8 columns at a time -- stored to out.  The row's two
+// threads (hf = 0, 1) split the work: pieces 2 hf, 2 hf + 1, then columns 16 hf .. 16 hf + 15 of
+// every piece, with the row owners' barrier between.  Every thread of the 8 row-owner warps
+// calls (tensor-memory loads are warp-wide); rows past the chunk store nothing.
+__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf) {
   const bool store = rr < p.rows;
   const int Hq = p.Hkv * p.G;
   float* dst = store ? p.out + (((long long)b * p.nq + rr / p.G) * Hq + h * p.G + rr % p.G) * kPfD : nullptr;
   const bool have = __any_sync(kFull, t_o != 0u);  // uniform: every row of the block shares the tiles
 #pragma unroll 1
-  for (int c4 = 0; c4 < 4; ++c4) {
+  for (int c4 = 2 * hf; c4 < 2 * hf + 2; ++c4) {
     float v[32];
     if (have) tc_ld32(t_o + 32 * c4, v);
 #pragma unroll
@@ -958,9 +987,12 @@ __device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h,
     }
   }
   if (!p.v_rotate) return;
+  tc_fence_before();
+  asm volatile("bar.sync 2, 256;\n" ::: "memory");  // both threads' pieces are back in tensor memory
+  tc_fence_after();
   const float rs = 1.f / sqrtf((float)kPfD);
 #pragma unroll 1
-  for (int i0 = 0; i0 < 32; i0 += 8) {
+  for (int i0 = 16 * hf; i0 < 16 * hf + 16; i0 += 8) {
     float v[4][8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -1021,7 +1053,8 @@ cudaError_t launch_pf(const PrefillParams& p, dim3 grid, cudaStream_t s) {
 }
 
 cudaError_t launch_pf_tc(const PrefillParams& p, dim3 grid, cudaStream_t s) {
-  const int smem = std::max(TcSmem::STG + 4 * (int)(p.kblk + p.vblk), kTcSmemMin);
+  // the packed stages: kTcNB of kTcBlk K blocks and kTcBlk V blocks each
+  const int smem = std::max(TcSmem::STG + kTcNB * kTcBlk * (int)(p.kblk + p.vblk), kTcSmemMin);
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   prefill_tc_kernel<<<grid, kTcThreads, smem, s>>>(p);
