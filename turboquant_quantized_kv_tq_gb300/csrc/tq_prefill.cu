@@ -810,15 +810,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
   }
 
   if (warp == kTcIssueWarp && lane == 0) {
-    // ---- MMA issue, each as soon as its inputs are ready: the scores of tile ks once it is
-    // unpacked (and at most one tile ahead of the readouts: S(ks) reuses S(ks - 2)'s columns,
-    // free once P(ks - 2) has been read), the readout of tile kr once its P is written
+    // ---- MMA issue, each as soon as its inputs are ready: the readout of tile kr once its P is
+    // written (checked first: it is what the rows wait for), the scores of tile ks once it is
+    // unpacked and at most one tile ahead of the readouts (S(ks) reuses S(ks - 2)'s columns, free
+    // once P(ks - 2) has been read).  A tile's 24 score MMAs go back to back.
     constexpr uint32_t idS = tc_idesc_f16(128, kTcTok), idO = tc_idesc_f16(128, kPfD, true);
     int ks = 0, kr = 0;
     uint32_t idle = 0;
     while (kr < ntiles) {
       bool moved = false;
-      if (ks < ntiles && ks <= kr + 1 && mbar_wait(B_U + 8 * (ks % kTcNB), (uint32_t)(ks / kTcNB) & 1u, 1)) {
+      if (kr < ks && tc_mbar_test(B_P, (uint32_t)kr & 1u)) {
+        tc_fence_after();
+        const uint32_t vb = sb + SM::VV + (kr % kTcNB) * SM::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kTcTok / 16; ++kk)
+          tc_mma_f16_ta(tmem + kTcO, tmem + kTcP + 8 * kk, tc_sdesc(vb + 4096 * kk, 2048, 128), idO,
+                        (kr > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(B_O + 8 * (kr % kTcNB));
+        ++kr;
+        moved = true;
+      }
+      if (ks < ntiles && ks <= kr + 1 && tc_mbar_test(B_U + 8 * (ks % kTcNB), (uint32_t)(ks / kTcNB) & 1u)) {
         tc_fence_after();
         const int bf = ks % kTcNB;
         const uint32_t kh = sb + SM::KHI + bf * SM::TILE, kl = sb + SM::KLO + bf * SM::TILE;
@@ -833,20 +845,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         ++ks;
         moved = true;
       }
-      if (kr < ks && mbar_wait(B_P, (uint32_t)kr & 1u, 1)) {
-        tc_fence_after();
-        const uint32_t vb = sb + SM::VV + (kr % kTcNB) * SM::TILE;
-#pragma unroll
-        for (int kk = 0; kk < kTcTok / 16; ++kk)
-          tc_mma_f16_ta(tmem + kTcO, tmem + kTcP + 8 * kk, tc_sdesc(vb + 4096 * kk, 2048, 128), idO,
-                        (kr > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(B_O + 8 * (kr % kTcNB));
-        ++kr;
-        moved = true;
-      }
       if (moved) {
         idle = 0;
-      } else if (++idle > 4u * kPfWaitLimit) {  // nothing became ready: give up (the error word says so)
+      } else if (++idle > 64u * kPfWaitLimit) {  // nothing became ready: give up (the error word says so)
         timed_out = true;
         break;
       }
