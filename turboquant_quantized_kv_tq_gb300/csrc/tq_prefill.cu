@@ -638,7 +638,9 @@ __device__ __forceinline__ uint32_t spread1(uint32_t x) {
 // 3-bit: 2 magnitude bytes at src, the sign byte at sgn; 2-bit: 2 bytes; 1-bit: 1 byte).  A sign
 // bit s and magnitude rank k give index s ? 2^(b-1) + k : 2^(b-1) - 1 - k, i.e. the stored
 // symbol with its magnitude bits inverted when s = 0.
-__device__ __forceinline__ uint32_t codes8(const unsigned char* src, const unsigned char* sgn, int bits) {
+template <int BITS = 0>
+__device__ __forceinline__ uint32_t codes8(const unsigned char* src, const unsigned char* sgn, int rbits) {
+  const int bits = BITS ? BITS : rbits;
   if (bits == 4) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
     return w ^ (((~w >> 3) & 0x11111111u) * 7u);
@@ -657,6 +659,8 @@ __device__ __forceinline__ uint32_t codes8(const unsigned char* src, const unsig
 
 __device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf);
 
+// KB, VB: the key and value code widths as compile-time constants (0: read from the parameters)
+template <int KB, int VB>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const PrefillParams p) {
   using SM = TcSmem;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -744,7 +748,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     // i = 0..3), so the eight threads of a quarter warp write the eight 16-byte rows of one core
     // matrix
     const int pt = tid - 256, c = (pt >> 3) & 15, t8 = pt & 7, jg0 = pt >> 7;
-    const int kbits = p.kbits, vbits = p.vbits, vW = vbits == 3 ? 2 : vbits;
+    const int kbits = KB ? KB : p.kbits, vbits = VB ? VB : p.vbits, vW = vbits == 3 ? 2 : vbits;
     const unsigned kc_off = C.off[tqi::R_K_CODES], kc_rec = C.rec[tqi::R_K_CODES];
     const unsigned kn_off = C.off[tqi::R_K_NORM], vc_off = C.off[tqi::R_V_CODES], vn_off = C.off[tqi::R_V_NORM];
     const int kbyte = kbits == 1 ? c : kbits == 4 ? 4 * c : 2 * c;  // the chunk's first code byte in a key record
@@ -769,11 +773,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         float nk, nv;
         {
           const unsigned char* kr = kp + kc_off + pos * kc_rec;
-          const uint32_t kc = codes8(kr + kbyte, kr + kPfD / 4 + c, kbits);
+          const uint32_t kc = codes8<KB>(kr + kbyte, kr + kPfD / 4 + c, kbits);
           // value streams by 16-coordinate groups: W bytes of the W-bit stream per chunk
           const unsigned char* vr = vp + vc_off;
-          const uint32_t vc = codes8(vr + g * 32 * vW + pos * 2 * vW + hv * vW,
-                                     vr + tqi::kTileTokens * (kPfD / 4) + g * 32 + pos * 2 + hv, vbits);
+          const uint32_t vc = codes8<VB>(vr + g * 32 * vW + pos * 2 * vW + hv * vW,
+                                         vr + tqi::kTileTokens * (kPfD / 4) + g * 32 + pos * 2 + hv, vbits);
           uint32_t kh[4], kl[4], vw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -847,9 +851,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       }
       if (moved) {
         idle = 0;
-      } else if (++idle > 64u * kPfWaitLimit) {  // nothing became ready: give up (the error word says so)
+      } else if (++idle > 4u * kPfWaitLimit) {  // nothing became ready: give up (the error word says so)
         timed_out = true;
         break;
+      } else {
+        __nanosleep(32);  // a short back-off keeps the poll from taking issue slots from the other warps
       }
     }
   }
@@ -1056,10 +1062,22 @@ cudaError_t launch_pf(const PrefillParams& p, dim3 grid, cudaStream_t s) {
 cudaError_t launch_pf_tc(const PrefillParams& p, dim3 grid, cudaStream_t s) {
   // the packed stages: kTcNB of kTcBlk K blocks and kTcBlk V blocks each
   const int smem = std::max(TcSmem::STG + kTcNB * kTcBlk * (int)(p.kblk + p.vblk), kTcSmemMin);
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  prefill_tc_kernel<<<grid, kTcThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  auto go = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kTcThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  };
+  // one code width on both sides (Plain-KV, TQ-KV) has its own variant
+  if (p.kbits == p.vbits) {
+    switch (p.kbits) {
+      case 4: return go(prefill_tc_kernel<4, 4>);
+      case 3: return go(prefill_tc_kernel<3, 3>);
+      case 2: return go(prefill_tc_kernel<2, 2>);
+      case 1: return go(prefill_tc_kernel<1, 1>);
+    }
+  }
+  return go(prefill_tc_kernel<0, 0>);
 }
 
 }  // namespace
