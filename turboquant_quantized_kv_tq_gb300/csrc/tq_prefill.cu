@@ -604,18 +604,28 @@ constexpr int kTcRowThreads = 256;               // two threads per row, 32 of a
 constexpr int kTcUnpack = 256;                   // unpacking threads
 constexpr int kTcIssueWarp = 16;
 constexpr uint32_t kTcCols = 512;  // the whole tensor memory: one block per SM
-constexpr uint32_t kTcQhi = 0, kTcQlo = 64, kTcS = 128, kTcO = 256, kTcP = 384;  // columns (S: two buffers)
+constexpr uint32_t kTcQhi = 0, kTcQlo = 64, kTcS = 128, kTcO = 256;  // tensor-memory columns
+// Without a value sketch: S in two buffers (128 .. 255), P at 384 (32 columns).  With one: S in
+// one buffer (128 .. 191), P at 192, P_sk at 224, O at 256 and O_sk at 384 (the whole memory).
+template <bool VQ> struct TcCols {
+  static constexpr int NS = VQ ? 1 : 2;  // score buffers
+  static constexpr uint32_t P = VQ ? 192 : 384, PSK = 224, OSK = 384;
+};
 constexpr int kTcSmemMin = 116 * 1024;  // asking for more than half the shared memory keeps one block per SM
+constexpr int kTcSmemMax = 227 * 1024;  // a block's shared memory
 
 // Shared-memory plan.  Tiles are token-major core matrices: element (token j, dim d) at
 // (j / 8) * 2048 + (d / 8) * 128 + (j % 8) * 16 + (d % 8) * 2 -- a K-major B operand for the
 // scores (LBO 128, SBO 2048) and an MN-major B operand for the readout (LBO 2048, SBO 128).
+template <bool VQ>
 struct TcSmem {
   static constexpr int TILE = kTcTok * kPfD * 2;                 // 16 KiB
   static constexpr int KHI = 0, KLO = kTcNB * TILE, VV = 2 * kTcNB * TILE;  // kTcNB buffers each
-  static constexpr int NUK = 3 * kTcNB * TILE;                    // float [kTcNB][kTcTok]
+  static constexpr int VS = 3 * kTcNB * TILE;                     // value signs 2 sigma - 1 (VQ)
+  static constexpr int NUK = (VQ ? 4 : 3) * kTcNB * TILE;         // float [kTcNB][kTcTok]
   static constexpr int NUV = NUK + kTcNB * kTcTok * 4;            // float [kTcNB][kTcTok]
-  static constexpr int CENT = NUV + kTcNB * kTcTok * 4;           // [16] (K hi | K lo << 16), [16] V fp16
+  static constexpr int FV = NUV + kTcNB * kTcTok * 4;             // nu_V rho_V, float [kTcNB][kTcTok] (VQ)
+  static constexpr int CENT = FV + (VQ ? kTcNB * kTcTok * 4 : 0); // [16] (K hi | K lo << 16), [16] V fp16
   static constexpr int XCH = CENT + 128;  // float [3][2 halves][128 rows]: maxima (by tile parity), then l
   static constexpr int STG = (XCH + 3 * 2 * 128 * 4 + 127) / 128 * 128;  // kTcNB packed stages
 };
@@ -657,15 +667,20 @@ __device__ __forceinline__ uint32_t codes8(const unsigned char* src, const unsig
   return spread1(*src);
 }
 
-__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf);
+__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf,
+                                           uint32_t t_add);
 
-// KB, VB: the key and value code widths as compile-time constants (0: read from the parameters)
-template <int KB, int VB>
+// KB, VB: the key and value code widths as compile-time constants (0: read from the parameters).
+// VQ: a QJL value side -- its sketch readout O_sk += P_sk (2 sigma_V - 1), P_sk = p nu_V rho_V,
+// rides beside the code readout, and the epilogue adds c S_V^T O_sk / l as one more MMA.
+template <int KB, int VB, bool VQ>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const PrefillParams p) {
-  using SM = TcSmem;
+  using SM = TcSmem<VQ>;
+  using TC = TcCols<VQ>;
   extern __shared__ __align__(128) unsigned char smem[];
-  // mbarriers: packed stages [3], unpacked tiles U [3], scores S [2], readouts O [3], P
-  __shared__ __align__(8) unsigned long long s_bars[12];
+  // mbarriers: packed stages [3], unpacked tiles U [3], scores S [2], readouts O [3], P, scores
+  // consumed (one score buffer), the epilogue's sketch product
+  __shared__ __align__(8) unsigned long long s_bars[14];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slab = blockIdx.y;
@@ -679,6 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
   const uint32_t sb = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t bar = (uint32_t)__cvta_generic_to_shared(s_bars);
   const uint32_t B_STG = bar, B_U = bar + 24, B_S = bar + 48, B_O = bar + 64, B_P = bar + 88;
+  const uint32_t B_SC = bar + 96, B_E = bar + 104;
   const Cache& C = p.cache;
   const unsigned kblk = p.kblk, vblk = p.vblk, SB = kTcBlk * (kblk + vblk);
   bool timed_out = false;
@@ -693,6 +709,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     mbar_init(B_S, 1);
     mbar_init(B_S + 8, 1);
     mbar_init(B_P, kTcRowThreads);
+    mbar_init(B_SC, kTcRowThreads);
+    mbar_init(B_E, 1);
     fence_mbar_init();
     for (int k = 0; k < kTcNB && k < ntiles; ++k) {
       const uint32_t dst = sb + SM::STG + k * SB;
@@ -751,6 +769,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     const int kbits = KB ? KB : p.kbits, vbits = VB ? VB : p.vbits, vW = vbits == 3 ? 2 : vbits;
     const unsigned kc_off = C.off[tqi::R_K_CODES], kc_rec = C.rec[tqi::R_K_CODES];
     const unsigned kn_off = C.off[tqi::R_K_NORM], vc_off = C.off[tqi::R_V_CODES], vn_off = C.off[tqi::R_V_NORM];
+    const unsigned vs_off = C.off[tqi::R_V_SIGNS], vr_off = C.off[tqi::R_V_RHO];
     const int kbyte = kbits == 1 ? c : kbits == 4 ? 4 * c : 2 * c;  // the chunk's first code byte in a key record
     const float kscale = p.score_scale;
     const uint32_t* kcent = reinterpret_cast<const uint32_t*>(smem + SM::CENT);
@@ -793,6 +812,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
           nk = ok ? *reinterpret_cast<const float*>(kp + kn_off + 4 * pos) * kscale : 0.f;  // nu_K log2(e) / sqrt(d)
           nv = ok ? *reinterpret_cast<const float*>(vp + vn_off + 4 * pos) : 0.f;
         }
+        if constexpr (VQ) {  // the value sketch's signs as +-1 (stream by 16-coordinate groups) and nu_V rho_V
+          const uint32_t sgb = vp[vs_off + g * 32 + pos * 2 + hv];
+          uint32_t sw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sw[e] = (0x3C003C00u | ((~sgb >> (2 * e)) & 1u) << 15 | ((~sgb >> (2 * e + 1)) & 1u) << 31) &
+                    (ok ? 0xffffffffu : 0u);
+          const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
+          *reinterpret_cast<uint4*>(smem + SM::VS + bf * SM::TILE + off) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+          if (c == 0)
+            reinterpret_cast<float*>(smem + SM::FV)[kTcTok * bf + j] =
+                ok ? nv * __half2float(*reinterpret_cast<const __half*>(vp + vr_off + 2 * pos)) : 0.f;
+        }
         const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
         *reinterpret_cast<uint4*>(smem + SM::KHI + bf * SM::TILE + off) = khi;
         *reinterpret_cast<uint4*>(smem + SM::KLO + bf * SM::TILE + off) = klo;
@@ -828,24 +860,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         const uint32_t vb = sb + SM::VV + (kr % kTcNB) * SM::TILE;
 #pragma unroll
         for (int kk = 0; kk < kTcTok / 16; ++kk)
-          tc_mma_f16_ta(tmem + kTcO, tmem + kTcP + 8 * kk, tc_sdesc(vb + 4096 * kk, 2048, 128), idO,
+          tc_mma_f16_ta(tmem + kTcO, tmem + TC::P + 8 * kk, tc_sdesc(vb + 4096 * kk, 2048, 128), idO,
                         (kr > 0 || kk > 0) ? 1u : 0u);
+        if constexpr (VQ) {
+          const uint32_t vsb = sb + SM::VS + (kr % kTcNB) * SM::TILE;
+#pragma unroll
+          for (int kk = 0; kk < kTcTok / 16; ++kk)
+            tc_mma_f16_ta(tmem + TC::OSK, tmem + TC::PSK + 8 * kk, tc_sdesc(vsb + 4096 * kk, 2048, 128), idO,
+                          (kr > 0 || kk > 0) ? 1u : 0u);
+        }
         tc_commit(B_O + 8 * (kr % kTcNB));
         ++kr;
         moved = true;
       }
-      if (ks < ntiles && ks <= kr + 1 && tc_mbar_test(B_U + 8 * (ks % kTcNB), (uint32_t)(ks / kTcNB) & 1u)) {
+      // one score buffer: S(ks) only after the rows have read S(ks - 1)
+      if (ks < ntiles && ks <= kr + 1 && (TC::NS == 2 || ks == 0 || tc_mbar_test(B_SC, (uint32_t)(ks - 1) & 1u)) &&
+          tc_mbar_test(B_U + 8 * (ks % kTcNB), (uint32_t)(ks / kTcNB) & 1u)) {
         tc_fence_after();
         const int bf = ks % kTcNB;
         const uint32_t kh = sb + SM::KHI + bf * SM::TILE, kl = sb + SM::KLO + bf * SM::TILE;
-        const uint32_t dS = tmem + kTcS + kTcTok * (ks & 1);
+        const uint32_t dS = tmem + kTcS + kTcTok * (TC::NS == 2 ? (ks & 1) : 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, kk > 0 ? 1u : 0u);
           tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, 1u);
           tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kl + 256 * kk, 128, 2048), idS, 1u);
         }
-        tc_commit(B_S + 8 * (ks & 1));
+        tc_commit(B_S + 8 * (TC::NS == 2 ? (ks & 1) : 0));
         ++ks;
         moved = true;
       }
@@ -869,12 +910,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     float* xch = reinterpret_cast<float*>(smem + SM::XCH);  // [tile parity][half][row]
     float m = kPfFloor, l = 0.f;  // l: this thread's share of the row sum
     for (int k = 0; k < ntiles; ++k) {
-      const int bf = k % kTcNB, sbf = k & 1, t0 = k * kTcTok + 32 * hf;
-      if (!mbar_wait(B_S + 8 * sbf, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
+      const int bf = k % kTcNB, sbf = TC::NS == 2 ? (k & 1) : 0, t0 = k * kTcTok + 32 * hf;
+      if (!mbar_wait(B_S + 8 * sbf, (uint32_t)(TC::NS == 2 ? (k >> 1) : k) & 1u, kPfWaitLimit)) timed_out = true;
       if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k / kTcNB) & 1u, kPfWaitLimit)) timed_out = true;  // the norms
       tc_fence_after();
       float s[32];
       tc_ld32(trow + kTcS + kTcTok * sbf + 32 * hf, s);
+      if constexpr (TC::NS == 1) {  // the score columns may take the next tile's scores
+        tc_fence_before();
+        tc_mbar_arrive(B_SC);
+      }
       const float4* nk4 = reinterpret_cast<const float4*>(smem + SM::NUK) + (kTcTok * bf + 32 * hf) / 4;
       float mx = kPfFloor;
 #pragma unroll
@@ -888,14 +933,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) mx = fmaxf(mx, s[j]);
-      // the row's maximum over both halves
-      xch[(sbf * 2 + hf) * 128 + r] = mx;
+      // the row's maximum over both halves (two exchange slots by tile parity)
+      xch[((k & 1) * 2 + hf) * 128 + r] = mx;
       asm volatile("bar.sync 2, 256;\n" ::: "memory");
-      const float mn = fmaxf(m, fmaxf(mx, xch[(sbf * 2 + (hf ^ 1)) * 128 + r]));
+      const float mn = fmaxf(m, fmaxf(mx, xch[((k & 1) * 2 + (hf ^ 1)) * 128 + r]));
       const float alpha = pf_ex2(m - mn);
       const float4* nv4 = reinterpret_cast<const float4*>(smem + SM::NUV) + (kTcTok * bf + 32 * hf) / 4;
+      const float4* fv4 = reinterpret_cast<const float4*>(smem + SM::FV) + (kTcTok * bf + 32 * hf) / 4;
       float ps = 0.f;
-      uint32_t pw[16];
+      uint32_t pw[16], pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
         const float4 n = nv4[j / 4];
@@ -904,6 +950,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         ps += (p0 + p1) + (p2 + p3);
         pw[j / 2] = pack_half2(p0 * n.x, p1 * n.y);
         pw[j / 2 + 1] = pack_half2(p2 * n.z, p3 * n.w);
+        if constexpr (VQ) {  // P_sk = p nu_V rho_V
+          const float4 f = fv4[j / 4];
+          pk[j / 2] = pack_half2(p0 * f.x, p1 * f.y);
+          pk[j / 2 + 1] = pack_half2(p2 * f.z, p3 * f.w);
+        }
       }
       l = l * alpha + ps;
       m = mn;
@@ -912,16 +963,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         tc_fence_after();
         if (__any_sync(kFull, alpha != 1.f)) {  // this thread's half of the row's accumulator
 #pragma unroll 1
-          for (int c4 = 0; c4 < 2; ++c4) {
+          for (int c4 = 0; c4 < (VQ ? 4 : 2); ++c4) {  // O's half, then (VQ) O_sk's half
+            const uint32_t col = (c4 < 2 ? kTcO : TC::OSK) + 64 * hf + 32 * (c4 & 1);
             float o[32];
-            tc_ld32(trow + kTcO + 64 * hf + 32 * c4, o);
+            tc_ld32(trow + col, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc_st32(trow + kTcO + 64 * hf + 32 * c4, o);
+            tc_st32(trow + col, o);
           }
         }
       }
-      tc_st16(trow + kTcP + 16 * hf, pw);
+      tc_st16(trow + TC::P + 16 * hf, pw);
+      if constexpr (VQ) tc_st16(trow + TC::PSK + 16 * hf, pk);
       tc_fence_before();
       tc_mbar_arrive(B_P);
     }
@@ -934,7 +987,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     xch[(4 + hf) * 128 + r] = l;
     asm volatile("bar.sync 2, 256;\n" ::: "memory");
     const float lt = l + xch[(4 + (hf ^ 1)) * 128 + r];
-    tc_out_row(p, b, h, rr, ntiles > 0 ? trow + kTcO : 0u, lt > 0.f ? 1.f / lt : 0.f, hf);
+    const float il = lt > 0.f ? 1.f / lt : 0.f;
+    if constexpr (VQ) {
+      if (ntiles > 0) {
+        // c S_V^T O_sk / l: S_V^T as fp16 rows (K-major B, row i, k = j) in the free tile buffers,
+        // c O_sk / l as fp16 pairs (the A operand) in the free score columns, one MMA chain into
+        // O_sk's columns
+        for (int it = 0; it < 8; ++it) {
+          const int item = tid + kTcRowThreads * it, i = item >> 4, cc = item & 15;
+          const float4 x0 = __ldg(reinterpret_cast<const float4*>(p.tab.S_V_T + i * kPfD + 8 * cc));
+          const float4 x1 = __ldg(reinterpret_cast<const float4*>(p.tab.S_V_T + i * kPfD + 8 * cc + 4));
+          *reinterpret_cast<uint4*>(smem + SM::KHI + (i >> 3) * 2048 + cc * 128 + (i & 7) * 16) =
+              make_uint4(pack_half2(x0.x, x0.y), pack_half2(x0.z, x0.w), pack_half2(x1.x, x1.y), pack_half2(x1.z, x1.w));
+        }
+        const float cs = p.qjl_scale * il;
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {
+          float o[32];
+          tc_ld32(trow + TC::OSK + 64 * hf + 32 * c2, o);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pack_half2(o[2 * i] * cs, o[2 * i + 1] * cs);
+          tc_st16(trow + kTcS + 32 * hf + 16 * c2, w);
+        }
+        tc_fence_smem();
+        tc_fence_before();
+        asm volatile("bar.sync 2, 256;\n" ::: "memory");
+        if (tid == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_f16_ta(tmem + TC::OSK, tmem + kTcS + 8 * kk, tc_sdesc(sb + SM::KHI + 256 * kk, 128, 2048),
+                          tc_idesc_f16(128, kPfD), kk > 0 ? 1u : 0u);
+          tc_commit(B_E);
+        }
+        if (!mbar_wait(B_E, 0, kPfWaitLimit)) timed_out = true;
+        tc_fence_after();
+      }
+    }
+    tc_out_row(p, b, h, rr, ntiles > 0 ? trow + kTcO : 0u, il, hf, (VQ && ntiles > 0) ? trow + TC::OSK : 0u);
   }
 
   tc_fence_before();
@@ -961,9 +1052,11 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
 // butterflies over coordinate bits 0 .. 4 within each 32-column piece (written back), then over
 // bits 5 and 6 across the four pieces, 8 columns at a time -- stored to out.  The row's two
 // threads (hf = 0, 1) split the work: pieces 2 hf, 2 hf + 1, then columns 16 hf .. 16 hf + 15 of
-// every piece, with the row owners' barrier between.  Every thread of the 8 row-owner warps
+// every piece, with the row owners' barrier between.  t_add (when not 0): 128 more columns added
+// to O il before the transform (the value sketch's term).  Every thread of the 8 row-owner warps
 // calls (tensor-memory loads are warp-wide); rows past the chunk store nothing.
-__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf) {
+__device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf,
+                                           uint32_t t_add) {
   const bool store = rr < p.rows;
   const int Hq = p.Hkv * p.G;
   float* dst = store ? p.out + (((long long)b * p.nq + rr / p.G) * Hq + h * p.G + rr % p.G) * kPfD : nullptr;
@@ -974,6 +1067,12 @@ __device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h,
     if (have) tc_ld32(t_o + 32 * c4, v);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = have ? v[i] * il : 0.f;
+    if (t_add != 0u && have) {
+      float a[32];
+      tc_ld32(t_add + 32 * c4, a);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += a[i];
+    }
     if (p.v_rotate) {
 #pragma unroll
       for (int hb = 1; hb < 32; hb <<= 1) {
@@ -1059,25 +1158,36 @@ cudaError_t launch_pf(const PrefillParams& p, dim3 grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <bool VQ>
+int pf_tc_smem(const PrefillParams& p) {  // the packed stages: kTcNB of kTcBlk K blocks and kTcBlk V blocks each
+  return std::max(TcSmem<VQ>::STG + kTcNB * kTcBlk * (int)(p.kblk + p.vblk), kTcSmemMin);
+}
+
+template <bool VQ>
 cudaError_t launch_pf_tc(const PrefillParams& p, dim3 grid, cudaStream_t s) {
-  // the packed stages: kTcNB of kTcBlk K blocks and kTcBlk V blocks each
-  const int smem = std::max(TcSmem::STG + kTcNB * kTcBlk * (int)(p.kblk + p.vblk), kTcSmemMin);
+  const int smem = pf_tc_smem<VQ>(p);
   auto go = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kTcThreads, smem, s>>>(p);
     return cudaGetLastError();
   };
-  // one code width on both sides (Plain-KV, TQ-KV) has its own variant
-  if (p.kbits == p.vbits) {
-    switch (p.kbits) {
-      case 4: return go(prefill_tc_kernel<4, 4>);
-      case 3: return go(prefill_tc_kernel<3, 3>);
-      case 2: return go(prefill_tc_kernel<2, 2>);
-      case 1: return go(prefill_tc_kernel<1, 1>);
+  if constexpr (VQ) {  // KQV at n = 4 / 3 / 2 (keys one bit wider than the value codes)
+    if (p.kbits == 4 && p.vbits == 3) return go(prefill_tc_kernel<4, 3, true>);
+    if (p.kbits == 3 && p.vbits == 2) return go(prefill_tc_kernel<3, 2, true>);
+    if (p.kbits == 2 && p.vbits == 1) return go(prefill_tc_kernel<2, 1, true>);
+    return go(prefill_tc_kernel<0, 0, true>);
+  } else {  // one code width on both sides (Plain-KV, TQ-KV)
+    if (p.kbits == p.vbits) {
+      switch (p.kbits) {
+        case 4: return go(prefill_tc_kernel<4, 4, false>);
+        case 3: return go(prefill_tc_kernel<3, 3, false>);
+        case 2: return go(prefill_tc_kernel<2, 2, false>);
+        case 1: return go(prefill_tc_kernel<1, 1, false>);
+      }
     }
+    return go(prefill_tc_kernel<0, 0, false>);
   }
-  return go(prefill_tc_kernel<0, 0>);
 }
 
 }  // namespace
@@ -1159,8 +1269,9 @@ tq_status launch_prefill(const tq_context* ctx, const void* cache, const float* 
   const bool kq = ctx->cfg.k.qjl != 0, vq = ctx->cfg.v.qjl != 0;
   if (kq && vq) e = launch_pf<true, true>(p, grid, s);
   else if (kq) e = launch_pf<true, false>(p, grid, s);
+  else if (vq && pf_tc_smem<true>(p) <= kTcSmemMax) e = launch_pf_tc<true>(p, grid, s);  // value sketch: tcgen05
   else if (vq) e = launch_pf<false, true>(p, grid, s);
-  else e = launch_pf_tc(p, grid, s);  // no sketch: the tcgen05 kernel
+  else e = launch_pf_tc<false>(p, grid, s);  // no sketch: the tcgen05 kernel
   if (e != cudaSuccess) return tqd::pf_fail("prefill", e);
   return TQ_OK;
 }
