@@ -617,17 +617,20 @@ constexpr int kTcSmemMax = 227 * 1024;  // a block's shared memory
 // Shared-memory plan.  Tiles are token-major core matrices: element (token j, dim d) at
 // (j / 8) * 2048 + (d / 8) * 128 + (j % 8) * 16 + (d % 8) * 2 -- a K-major B operand for the
 // scores (LBO 128, SBO 2048) and an MN-major B operand for the readout (LBO 2048, SBO 128).
-template <bool VQ>
+template <bool VQ, bool KQ>
 struct TcSmem {
+  static constexpr int NB = KQ ? 2 : kTcNB;                       // tile buffers (the key sketch's tiles need the room)
   static constexpr int TILE = kTcTok * kPfD * 2;                 // 16 KiB
-  static constexpr int KHI = 0, KLO = kTcNB * TILE, VV = 2 * kTcNB * TILE;  // kTcNB buffers each
-  static constexpr int VS = 3 * kTcNB * TILE;                     // value signs 2 sigma - 1 (VQ)
-  static constexpr int NUK = (VQ ? 4 : 3) * kTcNB * TILE;         // float [kTcNB][kTcTok]
-  static constexpr int NUV = NUK + kTcNB * kTcTok * 4;            // float [kTcNB][kTcTok]
-  static constexpr int FV = NUV + kTcNB * kTcTok * 4;             // nu_V rho_V, float [kTcNB][kTcTok] (VQ)
-  static constexpr int CENT = FV + (VQ ? kTcNB * kTcTok * 4 : 0); // [16] (K hi | K lo << 16), [16] V fp16
+  static constexpr int KHI = 0, KLO = NB * TILE, VV = 2 * NB * TILE;  // NB buffers each
+  static constexpr int VS = 3 * NB * TILE;                        // value signs 2 sigma - 1 (VQ)
+  static constexpr int KS = (VQ ? 4 : 3) * NB * TILE;             // key sketch rows rho (2 sigma - 1) (KQ)
+  static constexpr int QSK = ((VQ ? 4 : 3) + (KQ ? 1 : 0)) * NB * TILE;  // c S_K q_rot, 128 rows (KQ), K-major A
+  static constexpr int NUK = QSK + (KQ ? kPfRows * kPfD * 2 : 0); // float [NB][kTcTok]
+  static constexpr int NUV = NUK + NB * kTcTok * 4;               // float [NB][kTcTok]
+  static constexpr int FV = NUV + NB * kTcTok * 4;                // nu_V rho_V, float [NB][kTcTok] (VQ)
+  static constexpr int CENT = FV + (VQ ? NB * kTcTok * 4 : 0);    // [16] (K hi | K lo << 16), [16] V fp16
   static constexpr int XCH = CENT + 128;  // float [3][2 halves][128 rows]: maxima (by tile parity), then l
-  static constexpr int STG = (XCH + 3 * 2 * 128 * 4 + 127) / 128 * 128;  // kTcNB packed stages
+  static constexpr int STG = (XCH + 3 * 2 * 128 * 4 + 127) / 128 * 128;  // NB packed stages
 };
 
 // Spread the 2-bit fields of a 16-bit value into the low bits of 8 nibbles, and the 8 bits of a
@@ -673,10 +676,11 @@ __device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h,
 // KB, VB: the key and value code widths as compile-time constants (0: read from the parameters).
 // VQ: a QJL value side -- its sketch readout O_sk += P_sk (2 sigma_V - 1), P_sk = p nu_V rho_V,
 // rides beside the code readout, and the epilogue adds c S_V^T O_sk / l as one more MMA.
-template <int KB, int VB, bool VQ>
+template <int KB, int VB, bool VQ, bool KQ>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const PrefillParams p) {
-  using SM = TcSmem<VQ>;
+  using SM = TcSmem<VQ, KQ>;
   using TC = TcCols<VQ>;
+  constexpr int NB = SM::NB;
   extern __shared__ __align__(128) unsigned char smem[];
   // mbarriers: packed stages [3], unpacked tiles U [3], scores S [2], readouts O [3], P, scores
   // consumed (one score buffer), the epilogue's sketch product
@@ -701,7 +705,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
 
   if (warp == kTcIssueWarp) tc_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kTcCols);
   if (tid == 0) {
-    for (int i = 0; i < kTcNB; ++i) {
+    for (int i = 0; i < NB; ++i) {
       mbar_init(B_STG + 8 * i, 1);
       mbar_init(B_U + 8 * i, kTcUnpack);
       mbar_init(B_O + 8 * i, 1);
@@ -712,7 +716,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     mbar_init(B_SC, kTcRowThreads);
     mbar_init(B_E, 1);
     fence_mbar_init();
-    for (int k = 0; k < kTcNB && k < ntiles; ++k) {
+    for (int k = 0; k < NB && k < ntiles; ++k) {
       const uint32_t dst = sb + SM::STG + k * SB;
       pf_issue_stage(C, b, h, k, kTcBlk, kblk, vblk, dst, B_STG + 8 * k);
     }
@@ -757,6 +761,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       tc_st32(trow + kTcQlo + c0, v);
     }
   }
+  if constexpr (KQ) {
+    if (warp < 8) {  // c S_K q_rot of the block's rows: a K-major A operand in shared memory
+#pragma unroll 1
+      for (int it = 0; it < 8; ++it) {
+        const int item = tid + kTcRowThreads * it, rw = item >> 4, cc = item & 15;
+        const uint4 x = *reinterpret_cast<const uint4*>(p.qsk + ((long long)slab * p.R_pad + r0 + rw) * kPfD + 8 * cc);
+        *reinterpret_cast<uint4*>(smem + SM::QSK + (rw >> 3) * 2048 + cc * 128 + (rw & 7) * 16) = x;
+      }
+      tc_fence_smem();
+    }
+  }
   tc_fence_before();
   __syncthreads();  // the queries are in tensor memory before the first score MMA
   tc_fence_after();
@@ -770,16 +785,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     const unsigned kc_off = C.off[tqi::R_K_CODES], kc_rec = C.rec[tqi::R_K_CODES];
     const unsigned kn_off = C.off[tqi::R_K_NORM], vc_off = C.off[tqi::R_V_CODES], vn_off = C.off[tqi::R_V_NORM];
     const unsigned vs_off = C.off[tqi::R_V_SIGNS], vr_off = C.off[tqi::R_V_RHO];
+    const unsigned ks_off = C.off[tqi::R_K_SIGNS], ks_rec = C.rec[tqi::R_K_SIGNS], kr_off = C.off[tqi::R_K_RHO];
     const int kbyte = kbits == 1 ? c : kbits == 4 ? 4 * c : 2 * c;  // the chunk's first code byte in a key record
     const float kscale = p.score_scale;
     const uint32_t* kcent = reinterpret_cast<const uint32_t*>(smem + SM::CENT);
     const unsigned short* vcent = reinterpret_cast<const unsigned short*>(smem + SM::CENT + 64);
     const int g = c >> 1, hv = c & 1;  // the chunk's 16-coordinate value group and half of it
     for (int k = 0; k < ntiles; ++k) {
-      const int bf = k % kTcNB, t0 = k * kTcTok;
-      // the tile kTcNB back has been read out: its buffers are free
-      if (k >= kTcNB && !mbar_wait(B_O + 8 * bf, (uint32_t)(k / kTcNB - 1) & 1u, kPfWaitLimit)) timed_out = true;
-      if (!mbar_wait(B_STG + 8 * bf, (uint32_t)(k / kTcNB) & 1u, kPfWaitLimit)) timed_out = true;
+      const int bf = k % NB, t0 = k * kTcTok;
+      // the tile NB back has been read out: its buffers are free
+      if (k >= NB && !mbar_wait(B_O + 8 * bf, (uint32_t)(k / NB - 1) & 1u, kPfWaitLimit)) timed_out = true;
+      if (!mbar_wait(B_STG + 8 * bf, (uint32_t)(k / NB) & 1u, kPfWaitLimit)) timed_out = true;
       const unsigned char* stg = smem + SM::STG + bf * SB;
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
@@ -812,6 +828,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
           nk = ok ? *reinterpret_cast<const float*>(kp + kn_off + 4 * pos) * kscale : 0.f;  // nu_K log2(e) / sqrt(d)
           nv = ok ? *reinterpret_cast<const float*>(vp + vn_off + 4 * pos) : 0.f;
         }
+        if constexpr (KQ) {  // the key sketch's rows rho_K (2 sigma - 1): token-major 16-byte sign records
+          const uint32_t sgb = kp[ks_off + pos * ks_rec + c];
+          const uint32_t rh = (uint32_t)__half_as_ushort(*reinterpret_cast<const __half*>(kp + kr_off + 2 * pos));
+          uint32_t sw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sw[e] = ((rh | rh << 16) | ((~sgb >> (2 * e)) & 1u) << 15 | ((~sgb >> (2 * e + 1)) & 1u) << 31) &
+                    (ok ? 0xffffffffu : 0u);
+          const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
+          *reinterpret_cast<uint4*>(smem + SM::KS + bf * SM::TILE + off) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+        }
         if constexpr (VQ) {  // the value sketch's signs as +-1 (stream by 16-coordinate groups) and nu_V rho_V
           const uint32_t sgb = vp[vs_off + g * 32 + pos * 2 + hv];
           uint32_t sw[4];
@@ -837,10 +864,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       tc_fence_smem();  // the tile's rows are visible to the tensor cores' operand reads
       tc_mbar_arrive(B_U + 8 * bf);
       asm volatile("bar.sync 1, 256;\n" ::: "memory");  // every unpacking thread is done with the stage
-      if (pt == 0 && k + kTcNB < ntiles) {
+      if (pt == 0 && k + NB < ntiles) {
         fence_proxy_async_shared();
         const uint32_t dst = sb + SM::STG + bf * SB;
-        pf_issue_stage(C, b, h, k + kTcNB, kTcBlk, kblk, vblk, dst, B_STG + 8 * bf);
+        pf_issue_stage(C, b, h, k + NB, kTcBlk, kblk, vblk, dst, B_STG + 8 * bf);
       }
     }
   }
@@ -857,27 +884,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       bool moved = false;
       if (kr < ks && tc_mbar_test(B_P, (uint32_t)kr & 1u)) {
         tc_fence_after();
-        const uint32_t vb = sb + SM::VV + (kr % kTcNB) * SM::TILE;
+        const uint32_t vb = sb + SM::VV + (kr % NB) * SM::TILE;
 #pragma unroll
         for (int kk = 0; kk < kTcTok / 16; ++kk)
           tc_mma_f16_ta(tmem + kTcO, tmem + TC::P + 8 * kk, tc_sdesc(vb + 4096 * kk, 2048, 128), idO,
                         (kr > 0 || kk > 0) ? 1u : 0u);
         if constexpr (VQ) {
-          const uint32_t vsb = sb + SM::VS + (kr % kTcNB) * SM::TILE;
+          const uint32_t vsb = sb + SM::VS + (kr % NB) * SM::TILE;
 #pragma unroll
           for (int kk = 0; kk < kTcTok / 16; ++kk)
             tc_mma_f16_ta(tmem + TC::OSK, tmem + TC::PSK + 8 * kk, tc_sdesc(vsb + 4096 * kk, 2048, 128), idO,
                           (kr > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(B_O + 8 * (kr % kTcNB));
+        tc_commit(B_O + 8 * (kr % NB));
         ++kr;
         moved = true;
       }
       // one score buffer: S(ks) only after the rows have read S(ks - 1)
       if (ks < ntiles && ks <= kr + 1 && (TC::NS == 2 || ks == 0 || tc_mbar_test(B_SC, (uint32_t)(ks - 1) & 1u)) &&
-          tc_mbar_test(B_U + 8 * (ks % kTcNB), (uint32_t)(ks / kTcNB) & 1u)) {
+          tc_mbar_test(B_U + 8 * (ks % NB), (uint32_t)(ks / NB) & 1u)) {
         tc_fence_after();
-        const int bf = ks % kTcNB;
+        const int bf = ks % NB;
         const uint32_t kh = sb + SM::KHI + bf * SM::TILE, kl = sb + SM::KLO + bf * SM::TILE;
         const uint32_t dS = tmem + kTcS + kTcTok * (TC::NS == 2 ? (ks & 1) : 0);
 #pragma unroll
@@ -885,6 +912,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
           tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, kk > 0 ? 1u : 0u);
           tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, 1u);
           tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kl + 256 * kk, 128, 2048), idS, 1u);
+        }
+        if constexpr (KQ) {  // + (c S_K q_rot) (rho_K (2 sigma - 1))^T, A from shared memory
+          const uint32_t kss = sb + SM::KS + bf * SM::TILE;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_f16(dS, tc_sdesc(sb + SM::QSK + 256 * kk, 128, 2048), tc_sdesc(kss + 256 * kk, 128, 2048), idS, 1u);
         }
         tc_commit(B_S + 8 * (TC::NS == 2 ? (ks & 1) : 0));
         ++ks;
@@ -910,9 +943,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     float* xch = reinterpret_cast<float*>(smem + SM::XCH);  // [tile parity][half][row]
     float m = kPfFloor, l = 0.f;  // l: this thread's share of the row sum
     for (int k = 0; k < ntiles; ++k) {
-      const int bf = k % kTcNB, sbf = TC::NS == 2 ? (k & 1) : 0, t0 = k * kTcTok + 32 * hf;
+      const int bf = k % NB, sbf = TC::NS == 2 ? (k & 1) : 0, t0 = k * kTcTok + 32 * hf;
       if (!mbar_wait(B_S + 8 * sbf, (uint32_t)(TC::NS == 2 ? (k >> 1) : k) & 1u, kPfWaitLimit)) timed_out = true;
-      if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k / kTcNB) & 1u, kPfWaitLimit)) timed_out = true;  // the norms
+      if (!mbar_wait(B_U + 8 * bf, (uint32_t)(k / NB) & 1u, kPfWaitLimit)) timed_out = true;  // the norms
       tc_fence_after();
       float s[32];
       tc_ld32(trow + kTcS + kTcTok * sbf + 32 * hf, s);
@@ -959,7 +992,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       l = l * alpha + ps;
       m = mn;
       if (k >= 1) {  // the readout of tile k - 1 is done: O is settled and P's columns are free
-        if (!mbar_wait(B_O + 8 * ((k - 1) % kTcNB), (uint32_t)((k - 1) / kTcNB) & 1u, kPfWaitLimit)) timed_out = true;
+        if (!mbar_wait(B_O + 8 * ((k - 1) % NB), (uint32_t)((k - 1) / NB) & 1u, kPfWaitLimit)) timed_out = true;
         tc_fence_after();
         if (__any_sync(kFull, alpha != 1.f)) {  // this thread's half of the row's accumulator
 #pragma unroll 1
@@ -979,7 +1012,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       tc_mbar_arrive(B_P);
     }
     if (ntiles > 0) {
-      if (!mbar_wait(B_O + 8 * ((ntiles - 1) % kTcNB), (uint32_t)((ntiles - 1) / kTcNB) & 1u, kPfWaitLimit))
+      if (!mbar_wait(B_O + 8 * ((ntiles - 1) % NB), (uint32_t)((ntiles - 1) / NB) & 1u, kPfWaitLimit))
         timed_out = true;
       tc_fence_after();
     }
@@ -1158,35 +1191,45 @@ cudaError_t launch_pf(const PrefillParams& p, dim3 grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <bool VQ>
-int pf_tc_smem(const PrefillParams& p) {  // the packed stages: kTcNB of kTcBlk K blocks and kTcBlk V blocks each
-  return std::max(TcSmem<VQ>::STG + kTcNB * kTcBlk * (int)(p.kblk + p.vblk), kTcSmemMin);
+template <bool VQ, bool KQ>
+int pf_tc_smem(const PrefillParams& p) {  // the packed stages: NB of kTcBlk K blocks and kTcBlk V blocks each
+  using SM = TcSmem<VQ, KQ>;
+  return std::max(SM::STG + SM::NB * kTcBlk * (int)(p.kblk + p.vblk), kTcSmemMin);
 }
 
-template <bool VQ>
+template <bool VQ, bool KQ>
 cudaError_t launch_pf_tc(const PrefillParams& p, dim3 grid, cudaStream_t s) {
-  const int smem = pf_tc_smem<VQ>(p);
+  const int smem = pf_tc_smem<VQ, KQ>(p);
   auto go = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kTcThreads, smem, s>>>(p);
     return cudaGetLastError();
   };
-  if constexpr (VQ) {  // KQV at n = 4 / 3 / 2 (keys one bit wider than the value codes)
-    if (p.kbits == 4 && p.vbits == 3) return go(prefill_tc_kernel<4, 3, true>);
-    if (p.kbits == 3 && p.vbits == 2) return go(prefill_tc_kernel<3, 2, true>);
-    if (p.kbits == 2 && p.vbits == 1) return go(prefill_tc_kernel<2, 1, true>);
-    return go(prefill_tc_kernel<0, 0, true>);
+  if constexpr (KQ) {  // QKQV at n = 4 / 3 / 2 (one code width on both sides)
+    if (p.kbits == p.vbits) {
+      switch (p.kbits) {
+        case 3: return go(prefill_tc_kernel<3, 3, VQ, true>);
+        case 2: return go(prefill_tc_kernel<2, 2, VQ, true>);
+        case 1: return go(prefill_tc_kernel<1, 1, VQ, true>);
+      }
+    }
+    return go(prefill_tc_kernel<0, 0, VQ, true>);
+  } else if constexpr (VQ) {  // KQV at n = 4 / 3 / 2 (keys one bit wider than the value codes)
+    if (p.kbits == 4 && p.vbits == 3) return go(prefill_tc_kernel<4, 3, true, false>);
+    if (p.kbits == 3 && p.vbits == 2) return go(prefill_tc_kernel<3, 2, true, false>);
+    if (p.kbits == 2 && p.vbits == 1) return go(prefill_tc_kernel<2, 1, true, false>);
+    return go(prefill_tc_kernel<0, 0, true, false>);
   } else {  // one code width on both sides (Plain-KV, TQ-KV)
     if (p.kbits == p.vbits) {
       switch (p.kbits) {
-        case 4: return go(prefill_tc_kernel<4, 4, false>);
-        case 3: return go(prefill_tc_kernel<3, 3, false>);
-        case 2: return go(prefill_tc_kernel<2, 2, false>);
-        case 1: return go(prefill_tc_kernel<1, 1, false>);
+        case 4: return go(prefill_tc_kernel<4, 4, false, false>);
+        case 3: return go(prefill_tc_kernel<3, 3, false, false>);
+        case 2: return go(prefill_tc_kernel<2, 2, false, false>);
+        case 1: return go(prefill_tc_kernel<1, 1, false, false>);
       }
     }
-    return go(prefill_tc_kernel<0, 0, false>);
+    return go(prefill_tc_kernel<0, 0, false, false>);
   }
 }
 
@@ -1267,11 +1310,12 @@ tq_status launch_prefill(const tq_context* ctx, const void* cache, const float* 
   for (int b = 0; b < TQ_MAX_BATCH; ++b) p.seq_len[b] = b < B ? seq_len[b] : 0;
   const dim3 grid(R_pad / kPfRows, B * Hkv);
   const bool kq = ctx->cfg.k.qjl != 0, vq = ctx->cfg.v.qjl != 0;
-  if (kq && vq) e = launch_pf<true, true>(p, grid, s);
+  if (kq && vq && pf_tc_smem<true, true>(p) <= kTcSmemMax) e = launch_pf_tc<true, true>(p, grid, s);  // tcgen05
+  else if (kq && vq) e = launch_pf<true, true>(p, grid, s);
   else if (kq) e = launch_pf<true, false>(p, grid, s);
-  else if (vq && pf_tc_smem<true>(p) <= kTcSmemMax) e = launch_pf_tc<true>(p, grid, s);  // value sketch: tcgen05
+  else if (vq && pf_tc_smem<true, false>(p) <= kTcSmemMax) e = launch_pf_tc<true, false>(p, grid, s);  // tcgen05
   else if (vq) e = launch_pf<false, true>(p, grid, s);
-  else e = launch_pf_tc<false>(p, grid, s);  // no sketch: the tcgen05 kernel
+  else e = launch_pf_tc<false, false>(p, grid, s);  // no sketch: the tcgen05 kernel
   if (e != cudaSuccess) return tqd::pf_fail("prefill", e);
   return TQ_OK;
 }
