@@ -5,20 +5,20 @@
 // value sum; [TQ-KV] "Contribuciones Clave" 1 the QJL estimate of a residual inner product.
 //
 // The rows of one (batch, KV head) slab are the chunk's (query, head) pairs, r = i G + g, and
-// row r attends to the first L - nq + 1 + r / G tokens.  A block takes 128 rows (8 warps x 16)
-// and walks the slab's tokens in 32-token tiles.  Each tile's packed K and V are unpacked once
-// per block into shared memory as fp16 rows of the rotated domain -- C[c], and on a QJL side
-// rho (2 sigma - 1) (keys) or 2 sigma - 1 (values) -- so the scores and the readout are dense
-// tensor-core products (mma.sync m16n8k16, fp32 accumulation):
-//   S[16 rows x 32 tok]  = Q_hi K_hi^T + Q_lo K_hi^T + Q_hi K_lo^T (+ (c S_K q_rot) (rho (2 sigma - 1))^T)
-//   acc[16 x 128]       += (p nu_V) V_hat,   acc_sk[16 x 128] += (p nu_V rho_V) (2 sigma_V - 1)
+// row r attends to the first L - nq + 1 + r / G tokens.  A block takes 128 rows and walks the
+// slab's tokens in 64-token tiles.  Each tile's packed K and V are unpacked once per block into
+// shared memory as fp16 rows of the rotated domain -- C[c], and on a QJL side rho (2 sigma - 1)
+// (keys) or 2 sigma - 1 (values) -- so the scores and the readout are dense products on the
+// 5th-generation tensor cores (tcgen05.mma, fp16 operands, fp32 accumulators in tensor memory):
+//   S[128 rows x 64 tok] = Q_hi K_hi^T + Q_lo K_hi^T + Q_hi K_lo^T (+ (c S_K q_rot) (rho (2 sigma - 1))^T)
+//   O[128 x 128]        += (p nu_V) V_hat,   O_sk[128 x 128] += (p nu_V rho_V) (2 sigma_V - 1)
 // with an online softmax (log2 domain) in between.  The epilogue forms
-// o = R_V^T (acc + c S_V^T acc_sk) / l in the accumulator layout: the sketch product is one more
-// MMA against S_V^T staged as fp16, and the inverse Walsh-Hadamard transform's stages run in
-// registers (two of its seven stages cross lanes).  The queries and the key centroids enter as
-// fp16 hi + lo terms: a single rounding of q is a score error common to every token of a row,
-// and one of a centroid an error common to every token with that code; with peaked attention
-// (outlier channels) either reaches the output undiluted.
+// o = R_V^T (O + c S_V^T O_sk) / l: the sketch product is one more MMA against S_V^T staged as
+// fp16, and the inverse Walsh-Hadamard transform runs on 32-column pieces of the accumulator.
+// The queries and the key centroids enter as fp16 hi + lo terms: a single rounding of q is a
+// score error common to every token of a row, and one of a centroid an error common to every
+// token with that code; with peaked attention (outlier channels) either reaches the output
+// undiluted.
 #include <algorithm>
 #include <string>
 
@@ -28,10 +28,7 @@
 namespace tqd {
 namespace {
 
-constexpr int kPfWarps = 8;
-constexpr int kPfRows = 16 * kPfWarps;  // rows per block
-constexpr int kPfTok = 32;              // tokens per tile
-constexpr int kPfPitch = 272;           // bytes per fp16 row of 128 (+ 8 halves: ldmatrix rows on distinct banks)
+constexpr int kPfRows = 128;            // rows per block (one per tensor-memory lane)
 constexpr int kPfD = 128;
 constexpr float kPfLog2e = 1.4426950408889634f;
 constexpr float kPfFloor = -1e30f;      // running maximum of a row that has seen no token yet
@@ -65,96 +62,10 @@ struct PrefillParams {
   int seq_len[TQ_MAX_BATCH];
 };
 
-// Shared-memory plan of a prefill block: the block's query rows (hi, lo, and the key-sketch
-// products), the tile's unpacked key and value rows, and per-token scalars.
-template <bool KQ, bool VQ>
-struct PfSmem {
-  static constexpr int QHI = 0;
-  static constexpr int QLO = QHI + kPfRows * kPfPitch;
-  static constexpr int QSK = QLO + kPfRows * kPfPitch;
-  static constexpr int KC = QSK + (KQ ? kPfRows * kPfPitch : 0);
-  static constexpr int KL = KC + kPfTok * kPfPitch;
-  static constexpr int KS = KL + kPfTok * kPfPitch;
-  static constexpr int VC = KS + (KQ ? kPfTok * kPfPitch : 0);
-  static constexpr int VS = VC + kPfTok * kPfPitch;
-  static constexpr int NUK = VS + (VQ ? kPfTok * kPfPitch : 0);
-  static constexpr int NUV = NUK + kPfTok * 4;
-  static constexpr int FV = NUV + kPfTok * 4;
-  // two stages of packed tiles (bulk copies of two 16-token blocks per side) follow
-  static constexpr int STG = (FV + kPfTok * 4 + 127) / 128 * 128;
-  // the epilogue's S_V^T (fp16, 128 rows) reuses the query rows
-  static_assert(QLO >= 0 && kPfD * kPfPitch <= KC, "S_V^T staging overlaps the tile");
-};
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
 __device__ __forceinline__ float pf_ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
-}
-
-// The 4 W bits of coordinates 4 lane .. 4 lane + 3 of a W-bit stream (W = 1, 2, 4): a whole
-// record at src (pos < 0), or a value-side stream stored by 16-coordinate groups at block
-// position pos.
-template <int W>
-__device__ __forceinline__ uint32_t lane_bits(const unsigned char* src, int pos) {
-  const unsigned lane = threadIdx.x & 31;
-  if constexpr (W == 4) {
-    const unsigned j = 2 * lane;  // even, and so is its grouped position
-    return *reinterpret_cast<const unsigned short*>(pos < 0 ? src + j : src + grouped_byte(j, (unsigned)pos, 4));
-  } else if constexpr (W == 2) {
-    return pos < 0 ? src[lane] : src[grouped_byte(lane, (unsigned)pos, 2)];
-  } else {
-    const unsigned j = lane >> 1;
-    const uint32_t byte = pos < 0 ? src[j] : src[grouped_byte(j, (unsigned)pos, 1)];
-    return (byte >> (4 * (lane & 1))) & 0xFu;
-  }
-}
-
-// Centroids C[c] of this lane's four coordinates of one code record (sign-magnitude symbols: a
-// sign bit s and a magnitude rank k give c = s ? 2^(b-1) + k : 2^(b-1) - 1 - k).
-__device__ __forceinline__ void unpack_codes(const unsigned char* codes, int bits, int pos, int second,
-                                             const float* cent, float (&y)[4]) {
-  uint32_t mag = 0, sgn = 0;
-  if (bits == 4) {
-    const uint32_t v = lane_bits<4>(codes, pos);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sgn |= ((v >> (4 * e + 3)) & 1u) << e;
-      mag |= ((v >> (4 * e)) & 7u) << (4 * e);
-    }
-  } else if (bits == 3) {
-    const uint32_t v = lane_bits<2>(codes, pos);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) mag |= ((v >> (2 * e)) & 3u) << (4 * e);
-    sgn = lane_bits<1>(codes + second, pos);
-  } else if (bits == 2) {
-    const uint32_t v = lane_bits<2>(codes, pos);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sgn |= ((v >> (2 * e + 1)) & 1u) << e;
-      mag |= ((v >> (2 * e)) & 1u) << (4 * e);
-    }
-  } else {
-    sgn = lane_bits<1>(codes, pos);
-  }
-  const uint32_t half = 1u << (bits - 1);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t k = (mag >> (4 * e)) & 7u;
-    const uint32_t c = ((sgn >> e) & 1u) ? half + k : half - 1u - k;
-    y[e] = __ldg(cent + c);
-  }
 }
 
 // The packed blocks of tile `tile` of slab (b, h) -- nb 16-token blocks from block nb * tile --
@@ -229,373 +140,19 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const PrefillPrepPara
   }
 }
 
-template <bool KQ, bool VQ>
-__global__ void __launch_bounds__(kPfWarps * 32, 1) prefill_kernel(const PrefillParams p) {
-  using SM = PfSmem<KQ, VQ>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int slab = blockIdx.y;
-  const int b = slab / p.Hkv, h = slab % p.Hkv;
-  const int r0 = blockIdx.x * kPfRows;
-  const int L = p.seq_len[b];
-  const int Lmin = L - p.nq + 1;  // causal end of the chunk's first query
-  const int rlast = min(r0 + kPfRows, p.rows) - 1;
-  const int eblk = max(0, min(L, Lmin + rlast / p.G));  // tokens any row of the block sees
-  const uint32_t sb = (uint32_t)__cvta_generic_to_shared(smem);
-
-  // ---- the block's query rows into shared memory (16-byte pieces)
-  {
-    const long long row0 = (long long)slab * p.R_pad + r0;
-    const int n16 = kPfRows * (kPfD * 2 / 16);
-    for (int i = threadIdx.x; i < n16; i += blockDim.x) {
-      const int rr = i >> 4, c = i & 15;
-      const long long src = (row0 + rr) * kPfD + 8 * c;
-      *reinterpret_cast<uint4*>(smem + SM::QHI + rr * kPfPitch + 16 * c) = *reinterpret_cast<const uint4*>(p.qhi + src);
-      *reinterpret_cast<uint4*>(smem + SM::QLO + rr * kPfPitch + 16 * c) = *reinterpret_cast<const uint4*>(p.qlo + src);
-      if constexpr (KQ)
-        *reinterpret_cast<uint4*>(smem + SM::QSK + rr * kPfPitch + 16 * c) = *reinterpret_cast<const uint4*>(p.qsk + src);
-    }
-  }
-
-  // ---- this warp's rows: lane rows g (A) and g + 8 (B) of the warp's 16
-  const int rw0 = r0 + 16 * warp;
-  const int rA = rw0 + g, rB = rA + 8;
-  const int eA = rA < p.rows ? Lmin + rA / p.G : 0;
-  const int eB = rB < p.rows ? Lmin + rB / p.G : 0;
-  const int ew = rw0 < p.rows ? max(0, min(L, Lmin + (min(rw0 + 15, p.rows - 1)) / p.G)) : 0;
-  float mA = kPfFloor, mB = kPfFloor, lA = 0.f, lB = 0.f;
-  float acc[16][4], accs[VQ ? 16 : 1][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      acc[n][e] = 0.f;
-      if constexpr (VQ) accs[n][e] = 0.f;
-    }
-  const Cache& C = p.cache;
-  const float* kcent = p.tab.k_c;
-  const float* vcent = p.tab.v_c;
-  float* nuK = reinterpret_cast<float*>(smem + SM::NUK);
-  float* nuV = reinterpret_cast<float*>(smem + SM::NUV);
-  float* fV = reinterpret_cast<float*>(smem + SM::FV);
-  // ldmatrix lane addressing: matrix mi = lane / 8, row lane % 8 of it
-  const int mi = lane >> 3, mr = lane & 7;
-
-  // packed tiles stream through two shared-memory stages: one bulk copy per side brings the
-  // tile's two 16-token blocks (adjacent in the slab), completing on the stage's mbarrier
-  __shared__ __align__(8) unsigned long long s_bars[2];
-  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&s_bars[0]);
-  const unsigned kblk = p.kblk, vblk = p.vblk, SB = 2 * (kblk + vblk);
-  const int ntiles = (eblk + kPfTok - 1) / kPfTok;
-  if (threadIdx.x == 0) {
-    mbar_init(bar0, 1);
-    mbar_init(bar0 + 8, 1);
-    fence_mbar_init();
-    for (int k = 0; k < 2 && k < ntiles; ++k) {
-      const uint32_t dst = sb + SM::STG + k * SB;
-      pf_issue_stage(C, b, h, k, 2, kblk, vblk, dst, bar0 + 8 * k);
-    }
-  }
-  bool timed_out = false;
-
-  for (int k = 0; k < ntiles; ++k) {
-    const int t0 = k * kPfTok, stage = k & 1;
-    __syncthreads();  // the previous tile's rows are consumed (and the queries are in place)
-    if (!mbar_wait(bar0 + 8 * stage, (uint32_t)(k >> 1) & 1u, kPfWaitLimit)) timed_out = true;
-    const unsigned char* stg = smem + SM::STG + stage * SB;
-    // ---- unpack the tile: warp w takes token rows 4 w .. 4 w + 3 of each side
-#pragma unroll 1
-    for (int jj = 0; jj < 4; ++jj) {
-      const int j = 4 * warp + jj, tok = t0 + j;
-      const bool ok = tok < L;
-      const int pos = j & (tqi::kTileTokens - 1);
-      const unsigned char* kp = stg + (j >> 4) * kblk;             // the token's K block
-      const unsigned char* vp = stg + 2 * kblk + (j >> 4) * vblk;  // and V block
-      float y[4] = {0.f, 0.f, 0.f, 0.f};
-      float nu = 0.f;
-      if (ok) {
-        unpack_codes(kp + C.off[tqi::R_K_CODES] + pos * C.rec[tqi::R_K_CODES], p.kbits, -1, kPfD / 4, kcent, y);
-        nu = *reinterpret_cast<const float*>(kp + C.off[tqi::R_K_NORM] + 4 * pos);
-      }
-      float yl[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float hi = __half2float(__float2half_rn(y[e]));
-        yl[e] = y[e] - hi;
-      }
-      st_half4(smem + SM::KC + j * kPfPitch + 8 * lane, y);
-      st_half4(smem + SM::KL + j * kPfPitch + 8 * lane, yl);
-      if (lane == 0) nuK[j] = nu;
-      if constexpr (KQ) {
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        if (ok) {
-          const uint32_t sg = lane_bits<1>(kp + C.off[tqi::R_K_SIGNS] + pos * C.rec[tqi::R_K_SIGNS], -1);
-          const float rho = __half2float(*reinterpret_cast<const __half*>(kp + C.off[tqi::R_K_RHO] + 2 * pos));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[e] = ((sg >> e) & 1u) ? rho : -rho;
-        }
-        st_half4(smem + SM::KS + j * kPfPitch + 8 * lane, s);
-      }
-      // value row: streams by coordinate groups at block position pos
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      float nv = 0.f, fv = 0.f;
-      if (ok) {
-        unpack_codes(vp + C.off[tqi::R_V_CODES], p.vbits, pos, tqi::kTileTokens * (kPfD / 4), vcent, v);
-        nv = *reinterpret_cast<const float*>(vp + C.off[tqi::R_V_NORM] + 4 * pos);
-        if constexpr (VQ) fv = nv * __half2float(*reinterpret_cast<const __half*>(vp + C.off[tqi::R_V_RHO] + 2 * pos));
-      }
-      st_half4(smem + SM::VC + j * kPfPitch + 8 * lane, v);
-      if (lane == 0) {
-        nuV[j] = nv;
-        fV[j] = fv;
-      }
-      if constexpr (VQ) {
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        if (ok) {
-          const uint32_t sg = lane_bits<1>(vp + C.off[tqi::R_V_SIGNS], pos);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[e] = ((sg >> e) & 1u) ? 1.f : -1.f;
-        }
-        st_half4(smem + SM::VS + j * kPfPitch + 8 * lane, s);
-      }
-    }
-    __syncthreads();
-    // the stage is read: refill it with tile k + 2
-    if (threadIdx.x == 0 && k + 2 < ntiles) {
-      fence_proxy_async_shared();
-      const uint32_t dst = sb + SM::STG + stage * SB;
-      pf_issue_stage(C, b, h, k + 2, 2, kblk, vblk, dst, bar0 + 8 * stage);
-    }
-    if (t0 >= ew) continue;  // every row of this warp is past its causal end (warp-uniform)
-
-    // ---- scores of the warp's 16 rows against the tile's 32 tokens (4 n-tiles of 8)
-    float s[4][4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
-    const uint32_t qa = sb + (16 * warp + mr + 8 * (mi & 1)) * kPfPitch + 16 * (mi >> 1);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
-      ldsm_x4(qa + SM::QHI + 32 * ks, a0, a1, a2, a3);
-      ldsm_x4(qa + SM::QLO + 32 * ks, l0, l1, l2, l3);
-      uint32_t z0, z1, z2, z3;
-      if constexpr (KQ) ldsm_x4(qa + SM::QSK + 32 * ks, z0, z1, z2, z3);
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const uint32_t kb = sb + (16 * np + mr + 8 * (mi >> 1)) * kPfPitch + 32 * ks + 16 * (mi & 1);
-        uint32_t b0, b1, b2, b3, d0, d1, d2, d3;
-        ldsm_x4(kb + SM::KC, b0, b1, b2, b3);
-        ldsm_x4(kb + SM::KL, d0, d1, d2, d3);
-        mma16816(s[2 * np], a0, a1, a2, a3, b0, b1);
-        mma16816(s[2 * np], l0, l1, l2, l3, b0, b1);
-        mma16816(s[2 * np], a0, a1, a2, a3, d0, d1);
-        mma16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
-        mma16816(s[2 * np + 1], l0, l1, l2, l3, b2, b3);
-        mma16816(s[2 * np + 1], a0, a1, a2, a3, d2, d3);
-        if constexpr (KQ) {
-          uint32_t c0, c1, c2, c3;
-          ldsm_x4(kb + SM::KS, c0, c1, c2, c3);
-          mma16816(s[2 * np], z0, z1, z2, z3, c0, c1);
-          mma16816(s[2 * np + 1], z0, z1, z2, z3, c2, c3);
-        }
-      }
-    }
-    // ---- key norms, causal masks, online softmax (log2 domain)
-    float mxA = kPfFloor, mxB = kPfFloor;
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = 8 * n + 2 * t + e, tok = t0 + j;
-        const float nu = nuK[j] * p.score_scale;
-        s[n][e] = tok < eA ? s[n][e] * nu : -INFINITY;
-        s[n][2 + e] = tok < eB ? s[n][2 + e] * nu : -INFINITY;
-        mxA = fmaxf(mxA, s[n][e]);
-        mxB = fmaxf(mxB, s[n][2 + e]);
-      }
-#pragma unroll
-    for (int m = 1; m <= 2; m <<= 1) {
-      mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, m));
-      mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, m));
-    }
-    const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
-    const float aA = pf_ex2(mA - nA), aB = pf_ex2(mB - nB);
-    mA = nA;
-    mB = nB;
-    lA *= aA;
-    lB *= aB;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      acc[n][0] *= aA; acc[n][1] *= aA; acc[n][2] *= aB; acc[n][3] *= aB;
-      if constexpr (VQ) {
-        accs[n][0] *= aA; accs[n][1] *= aA; accs[n][2] *= aB; accs[n][3] *= aB;
-      }
-    }
-    // ---- readout: per 16-token chunk, P (times nu_V, and nu_V rho_V for the sketch) as the A
-    // operand straight from the score layout; V_hat rows transposed by ldmatrix
-#pragma unroll
-    for (int kc = 0; kc < 2; ++kc) {
-      float pw[2][4], ps[2][4];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int n = 2 * kc + hh;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int j = 8 * n + 2 * t + e;
-          const float pa = pf_ex2(s[n][e] - nA), pb = pf_ex2(s[n][2 + e] - nB);
-          lA += pa;
-          lB += pb;
-          const float nv = nuV[j];
-          pw[hh][e] = pa * nv;
-          pw[hh][2 + e] = pb * nv;
-          if constexpr (VQ) {
-            const float f = fV[j];
-            ps[hh][e] = pa * f;
-            ps[hh][2 + e] = pb * f;
-          }
-        }
-      }
-      const uint32_t p0 = pack_half2(pw[0][0], pw[0][1]), p1 = pack_half2(pw[0][2], pw[0][3]);
-      const uint32_t p2 = pack_half2(pw[1][0], pw[1][1]), p3 = pack_half2(pw[1][2], pw[1][3]);
-      uint32_t q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-      if constexpr (VQ) {
-        q0 = pack_half2(ps[0][0], ps[0][1]); q1 = pack_half2(ps[0][2], ps[0][3]);
-        q2 = pack_half2(ps[1][0], ps[1][1]); q3 = pack_half2(ps[1][2], ps[1][3]);
-      }
-      const uint32_t vb0 = sb + (16 * kc + mr + 8 * (mi & 1)) * kPfPitch + 16 * (mi >> 1);
-#pragma unroll
-      for (int dt = 0; dt < 8; ++dt) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb0 + SM::VC + 32 * dt, b0, b1, b2, b3);
-        mma16816(acc[2 * dt], p0, p1, p2, p3, b0, b1);
-        mma16816(acc[2 * dt + 1], p0, p1, p2, p3, b2, b3);
-        if constexpr (VQ) {
-          uint32_t c0, c1, c2, c3;
-          ldsm_x4_t(vb0 + SM::VS + 32 * dt, c0, c1, c2, c3);
-          mma16816(accs[2 * dt], q0, q1, q2, q3, c0, c1);
-          mma16816(accs[2 * dt + 1], q0, q1, q2, q3, c2, c3);
-        }
-      }
-    }
-  }
-
-  // ---- epilogue: o = R_V^T (acc + c S_V^T acc_sk) / l, in the accumulator layout
-#pragma unroll
-  for (int m = 1; m <= 2; m <<= 1) {
-    lA += __shfl_xor_sync(kFull, lA, m);
-    lB += __shfl_xor_sync(kFull, lB, m);
-  }
-  const float iA = lA > 0.f ? 1.f / lA : 0.f, iB = lB > 0.f ? 1.f / lB : 0.f;
-#pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    acc[n][0] *= iA; acc[n][1] *= iA; acc[n][2] *= iB; acc[n][3] *= iB;
-  }
-  if constexpr (VQ) {
-    // S_V^T [128 i][128 j] as fp16 rows over the query rows (every warp is past its last tile)
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kPfD * kPfD / 4; idx += blockDim.x) {
-      const int i = idx >> 5, c4 = idx & 31;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(p.tab.S_V_T + i * kPfD + 4 * c4));
-      const float vv[4] = {v.x, v.y, v.z, v.w};
-      st_half4(smem + i * kPfPitch + 8 * c4, vv);
-    }
-    __syncthreads();
-    // acc[r][i] += sum_j (c acc_sk[r][j] / l_r) S_V^T[i][j]: A = the scaled sketch accumulator
-    // (score layout -> A operand, as P above), B = S_V^T rows (n = i, k = j)
-    const float cA = iA * p.qjl_scale, cB = iB * p.qjl_scale;
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-      const uint32_t a0 = pack_half2(accs[2 * kc][0] * cA, accs[2 * kc][1] * cA);
-      const uint32_t a1 = pack_half2(accs[2 * kc][2] * cB, accs[2 * kc][3] * cB);
-      const uint32_t a2 = pack_half2(accs[2 * kc + 1][0] * cA, accs[2 * kc + 1][1] * cA);
-      const uint32_t a3 = pack_half2(accs[2 * kc + 1][2] * cB, accs[2 * kc + 1][3] * cB);
-#pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        const uint32_t sa = sb + (16 * np + mr + 8 * (mi >> 1)) * kPfPitch + 32 * kc + 16 * (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sa, b0, b1, b2, b3);
-        mma16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-        mma16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-      }
-    }
-  }
-  // inverse rotation x = D_V H o_rot / sqrt(d).  Lane (g, t) holds, for each of its two rows,
-  // coordinates 8 n + 2 t + e (n = 0..15, e = 0..1): butterflies over bit 0 (e) and bits 3-6 (n)
-  // are local, over bits 1-2 (t) lane shuffles
-  if (p.v_rotate) {
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      float x0 = acc[n][0], x1 = acc[n][1];
-      acc[n][0] = x0 + x1; acc[n][1] = x0 - x1;
-      x0 = acc[n][2]; x1 = acc[n][3];
-      acc[n][2] = x0 + x1; acc[n][3] = x0 - x1;
-    }
-#pragma unroll
-    for (int m = 1; m <= 2; m <<= 1) {
-#pragma unroll
-      for (int n = 0; n < 16; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float o = __shfl_xor_sync(kFull, acc[n][e], m);
-          acc[n][e] = (t & m) ? (o - acc[n][e]) : (acc[n][e] + o);
-        }
-    }
-#pragma unroll
-    for (int hb = 1; hb < 16; hb <<= 1) {
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        if ((n & hb) == 0) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = acc[n][e], x1 = acc[n + hb][e];
-            acc[n][e] = x0 + x1;
-            acc[n + hb][e] = x0 - x1;
-          }
-        }
-      }
-    }
-    const float rs = 1.f / sqrtf((float)kPfD);
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float sg = __ldg(p.tab.v_sign + 8 * n + 2 * t + e) * rs;
-        acc[n][e] *= sg;
-        acc[n][2 + e] *= sg;
-      }
-  }
-  const int Hq = p.Hkv * p.G;
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int r = rr ? rB : rA;
-    if (r >= p.rows) continue;
-    const int i = r / p.G, gg = r % p.G;
-    float* dst = p.out + (((long long)b * p.nq + i) * Hq + h * p.G + gg) * kPfD;
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<float2*>(dst + 8 * n + 2 * t) = make_float2(acc[n][2 * rr], acc[n][2 * rr + 1]);
-  }
-  if (timed_out) atomicExch(p.err, TQ_DEVERR_WAIT_TIMEOUT);
-}
-
-// ---- The same product on the 5th-generation tensor cores (sides without a QJL sketch) ------
-// A block takes 128 rows, one per tensor-memory lane, and the slab's tokens in 64-token tiles:
-//   S[128 x 64]   = Q_hi K_hi^T + Q_lo K_hi^T + Q_hi K_lo^T      (tcgen05.mma, M = 128, N = 64)
-//   O[128 x 128] += P V,  P = 2^(s - m) nu_V as fp16               (tcgen05.mma, M = 128, N = 128)
-// Q_hi, Q_lo, S (two buffers), P and O live in tensor memory; the unpacked K and V tiles in
-// shared memory (three buffers).  Warps 0-7 own the rows: warp w takes the rows of tensor-memory
+// ---- The prefill kernel ---------------------------------------------------------------------
+// Q_hi, Q_lo, S, P and O (and with a QJL value side P_sk and O_sk) live in tensor memory; the
+// unpacked tiles in shared memory (three buffers, two with a QJL key side, whose c S_K q_rot is a
+// shared-memory A operand).  Warps 0-7 own the rows: warp w takes the rows of tensor-memory
 // lanes 32 (w % 4) .. + 31 and tokens 32 (w / 4) .. + 31 of every tile.  They load the queries
 // into tensor memory, run the online softmax on S (the two threads of a row share their maxima
-// through shared memory) and write P, rescale O when a row's maximum rises, and finish
-// o = R_V^T O / l.  Warps 8-15 unpack the tiles, which bulk copies bring into packed stages; with
-// three tile buffers the unpacking runs up to two tiles ahead.  One thread of warp 16 issues the
-// MMAs, each as soon as its inputs are ready: a tile's scores when it is unpacked, its readout
-// when its P is written.  The stages hand
-// over through mbarriers: a tile unpacked (U), its scores done (S), its P written (P), its
-// readout done (O, which frees the tile's buffers and P).
+// through shared memory) and write P, rescale the accumulators when a row's maximum rises, and
+// finish o.  Warps 8-15 unpack the tiles, which bulk copies bring into packed stages; with three
+// tile buffers the unpacking runs up to two tiles ahead.  One thread of warp 16 issues the MMAs,
+// each as soon as its inputs are ready: a tile's scores when it is unpacked, its readout when its
+// P is written.  The stages hand over through mbarriers: a tile unpacked (U), its scores done
+// (S), its scores read (one score buffer), its P written (P), its readout done (O, which frees
+// the tile's buffers and P).
 constexpr int kTcTok = 64;                       // tokens per tile
 constexpr int kTcBlk = kTcTok / 16;              // 16-token cache blocks per tile
 constexpr int kTcNB = 3;                         // tile buffers (and packed stages): unpacking runs two tiles ahead
@@ -610,6 +167,7 @@ constexpr uint32_t kTcQhi = 0, kTcQlo = 64, kTcS = 128, kTcO = 256;  // tensor-m
 template <bool VQ> struct TcCols {
   static constexpr int NS = VQ ? 1 : 2;  // score buffers
   static constexpr uint32_t P = VQ ? 192 : 384, PSK = 224, OSK = 384;
+  static_assert(!VQ || (PSK == P + 32 && OSK == kTcO + 128), "tensor-memory plan");
 };
 constexpr int kTcSmemMin = 116 * 1024;  // asking for more than half the shared memory keeps one block per SM
 constexpr int kTcSmemMax = 227 * 1024;  // a block's shared memory
@@ -631,6 +189,7 @@ struct TcSmem {
   static constexpr int CENT = FV + (VQ ? NB * kTcTok * 4 : 0);    // [16] (K hi | K lo << 16), [16] V fp16
   static constexpr int XCH = CENT + 128;  // float [3][2 halves][128 rows]: maxima (by tile parity), then l
   static constexpr int STG = (XCH + 3 * 2 * 128 * 4 + 127) / 128 * 128;  // NB packed stages
+  static_assert(VS == VV + NB * TILE && KS >= VS && QSK >= KS, "shared-memory plan");
 };
 
 // Spread the 2-bit fields of a 16-bit value into the low bits of 8 nibbles, and the 8 bits of a
@@ -1182,15 +741,6 @@ int pf_rows_padded(const tq_context* ctx, int nq) {
   return (rows + kPfRows - 1) / kPfRows * kPfRows;
 }
 
-template <bool KQ, bool VQ>
-cudaError_t launch_pf(const PrefillParams& p, dim3 grid, cudaStream_t s) {
-  const int smem = PfSmem<KQ, VQ>::STG + 4 * (int)(p.kblk + p.vblk);
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<KQ, VQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  prefill_kernel<KQ, VQ><<<grid, kPfWarps * 32, smem, s>>>(p);
-  return cudaGetLastError();
-}
-
 template <bool VQ, bool KQ>
 int pf_tc_smem(const PrefillParams& p) {  // the packed stages: NB of kTcBlk K blocks and kTcBlk V blocks each
   using SM = TcSmem<VQ, KQ>;
@@ -1207,11 +757,13 @@ cudaError_t launch_pf_tc(const PrefillParams& p, dim3 grid, cudaStream_t s) {
     return cudaGetLastError();
   };
   if constexpr (KQ) {  // QKQV at n = 4 / 3 / 2 (one code width on both sides)
-    if (p.kbits == p.vbits) {
-      switch (p.kbits) {
-        case 3: return go(prefill_tc_kernel<3, 3, VQ, true>);
-        case 2: return go(prefill_tc_kernel<2, 2, VQ, true>);
-        case 1: return go(prefill_tc_kernel<1, 1, VQ, true>);
+    if constexpr (VQ) {
+      if (p.kbits == p.vbits) {
+        switch (p.kbits) {
+          case 3: return go(prefill_tc_kernel<3, 3, true, true>);
+          case 2: return go(prefill_tc_kernel<2, 2, true, true>);
+          case 1: return go(prefill_tc_kernel<1, 1, true, true>);
+        }
       }
     }
     return go(prefill_tc_kernel<0, 0, VQ, true>);
@@ -1256,6 +808,18 @@ tq_status launch_prefill(const tq_context* ctx, const void* cache, const float* 
   int* err = (int*)ws;
   unsigned char* base = (unsigned char*)ws + 256;
 
+  const bool kq = ctx->cfg.k.qjl != 0, vq = ctx->cfg.v.qjl != 0;
+  {  // the kernel's packed stages must fit next to its tiles (they do for every record of head dim 128)
+    PrefillParams q0;
+    q0.kblk = (unsigned)ctx->layout.block[0];
+    q0.vblk = (unsigned)ctx->layout.block[1];
+    const int need = kq ? (vq ? pf_tc_smem<true, true>(q0) : pf_tc_smem<false, true>(q0))
+                        : (vq ? pf_tc_smem<true, false>(q0) : pf_tc_smem<false, false>(q0));
+    if (need > kTcSmemMax) {
+      set_error("prefill: the cache records are too large for the prefill kernel's shared memory");
+      return TQ_ERR_UNSUPPORTED;
+    }
+  }
   PrefillPrepParams pp;
   pp.tab = make_tables(ctx);
   pp.q = q;
@@ -1309,13 +873,10 @@ tq_status launch_prefill(const tq_context* ctx, const void* cache, const float* 
   p.qjl_scale = pp.qjl_scale;
   for (int b = 0; b < TQ_MAX_BATCH; ++b) p.seq_len[b] = b < B ? seq_len[b] : 0;
   const dim3 grid(R_pad / kPfRows, B * Hkv);
-  const bool kq = ctx->cfg.k.qjl != 0, vq = ctx->cfg.v.qjl != 0;
-  if (kq && vq && pf_tc_smem<true, true>(p) <= kTcSmemMax) e = launch_pf_tc<true, true>(p, grid, s);  // tcgen05
-  else if (kq && vq) e = launch_pf<true, true>(p, grid, s);
-  else if (kq) e = launch_pf<true, false>(p, grid, s);
-  else if (vq && pf_tc_smem<true, false>(p) <= kTcSmemMax) e = launch_pf_tc<true, false>(p, grid, s);  // tcgen05
-  else if (vq) e = launch_pf<false, true>(p, grid, s);
-  else e = launch_pf_tc<false, false>(p, grid, s);  // no sketch: the tcgen05 kernel
+  if (kq && vq) e = launch_pf_tc<true, true>(p, grid, s);
+  else if (kq) e = launch_pf_tc<false, true>(p, grid, s);
+  else if (vq) e = launch_pf_tc<true, false>(p, grid, s);
+  else e = launch_pf_tc<false, false>(p, grid, s);
   if (e != cudaSuccess) return tqd::pf_fail("prefill", e);
   return TQ_OK;
 }
