@@ -162,8 +162,9 @@ size_t tq_tables_bytes(const tq_context* ctx);
  * [H_kv][d][r] (zeros until tq_headq_set_basis); when d > 128 and V has QJL, fp32
  * S_V R_V [m][d] (R_V = H D_V / sqrt(d), each row rounded once from a float64 transform), which
  * maps the value sketch accumulator straight to the output domain; when d = m = 128, for each
- * side with QJL (K, then V), S as fp16 in 128 rows of 136 halves (272-byte pitch), the terms
- * fp16(S) then fp16(S - fp16(S)) (the tensor-core residual sketch's operands); fp32 c1[2], the 1-bit
+ * side with QJL (K, then V), S as fp16 -- the terms fp16(S), then fp16(S - fp16(S)), 32 KiB each, element
+ * (i, j) at byte (i / 8) * 2048 + (j / 8) * 128 + (i % 8) * 16 + (j % 8) * 2 (8 x 8 core matrices:
+ * the tensor-core residual sketch's operand layout); fp32 c1[2], the 1-bit
  * codebook's upper centroid (a spectral side's floor); and for each spectral side (K, then V)
  * its basis E and E^T [H_kv][d][d] and scales s [H_kv][d] in storage order (zeros until
  * tq_spectral_set_basis).  A spectral side's centroid / threshold slots hold the 4-bit codebook.

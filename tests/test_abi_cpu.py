@@ -146,14 +146,17 @@ def test_host_rotation_and_sketch_bit_exact(seed):
     assert np.array_equal(f("S_V", d * d).reshape(d, d), SV)
     assert np.array_equal(f("S_V_T", d * d).reshape(d, d), SV.T)
     assert b.tq_tables_bytes(ctx) >= off["S_V_T"] + 4 * d * d
-    # the fp16 hi / lo rows of S_K then S_V (272-byte pitch) for the tensor-core sketch
+    # the fp16 hi / lo terms of S_K then S_V for the tensor-core sketch, 8 x 8 core matrices:
+    # element (i, j) at byte (i / 8) 2048 + (j / 8) 128 + (i % 8) 16 + (j % 8) 2 of each table
     start = (off["S_V_T"] + 4 * d * d + 255) // 256 * 256
+    ii, jj = np.meshgrid(np.arange(128), np.arange(128), indexing="ij")
+    pos = ((ii >> 3) * 2048 + (jj >> 3) * 128 + (ii & 7) * 16 + (jj & 7) * 2) // 2
     for k, S in enumerate((SK, SV)):
-        o = start + k * ((2 * 128 * 136 * 2 + 255) // 256 * 256)
-        h16 = blob[o:o + 2 * 128 * 136 * 2].view(np.float16).reshape(2, 128, 136)
+        o = start + k * 65536
+        h16 = blob[o:o + 65536].view(np.float16).reshape(2, 128 * 128)
         hi = S.astype(np.float16)
         lo = (S - hi.astype(np.float32)).astype(np.float16)
-        assert np.array_equal(h16[0, :, :128], hi) and np.array_equal(h16[1, :, :128], lo)
+        assert np.array_equal(h16[0][pos], hi) and np.array_equal(h16[1][pos], lo)
     b.tq_context_destroy(ctx)
 
 

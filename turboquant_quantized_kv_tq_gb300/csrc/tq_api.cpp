@@ -171,17 +171,17 @@ tq_status tq_context_create(const tq_config* cfg, tq_context** out) {
   };
   if (cfg->k.qjl) put_sketch(3, ctx->tab.s_k, ctx->tab.s_k_t);
   if (cfg->v.qjl) put_sketch(4, ctx->tab.s_v, ctx->tab.s_v_t);
-  for (int side = 0; side < 2; ++side) {  // fp16 hi / lo rows of S for the tensor-core sketch
+  for (int side = 0; side < 2; ++side) {  // fp16 hi / lo terms of S for the tensor-core sketch
     if (!ctx->tab.s_h16[side]) continue;
     const float* S = (const float*)(base + (side ? ctx->tab.s_v : ctx->tab.s_k));
-    __half* hi = (__half*)(base + ctx->tab.s_h16[side]);
-    __half* lo = hi + 128 * kSketchPitch;
+    unsigned char* hi = base + ctx->tab.s_h16[side];
+    unsigned char* lo = hi + kSketchH16Bytes / 2;
     for (int i = 0; i < 128; ++i)
       for (int j = 0; j < 128; ++j) {
         const float x = S[i * 128 + j];
         const __half h = __float2half_rn(x);
-        hi[i * kSketchPitch + j] = h;
-        lo[i * kSketchPitch + j] = __float2half_rn(x - __half2float(h));
+        *(__half*)(hi + sketch_cm_offset(i, j)) = h;
+        *(__half*)(lo + sketch_cm_offset(i, j)) = __float2half_rn(x - __half2float(h));
       }
   }
   if (ctx->tab.s_v_r) {

@@ -13,6 +13,7 @@
 #include <type_traits>
 
 #include "tq_device.cuh"
+#include "tq_tc05.cuh"
 
 namespace tqd {
 
@@ -850,21 +851,14 @@ constexpr uint32_t kStageWaitLimit = 1u << 20;  // polls of a table copy's mbarr
 constexpr int kQjlWarps = 8;
 constexpr int kQjlBlockVec = 64;        // vectors per block of a large append: 4 MMA row tiles of 16
 constexpr int kQjlSmallVec = 16;        // vectors per block of a small append: one row tile
-constexpr int kSRow = 136;              // fp16 row pitch: 272 B keeps ldmatrix rows on distinct banks
 constexpr float kQjlUp = 256.f;         // residual scale before the fp16 split
 constexpr float kSignRecheck = 2e-5f;   // in units of S r
 constexpr long long kQjlMmaMin = 256;   // vectors per side from which 64-vector blocks are used
 constexpr int kRecheckMax = 256;        // listed near-zero products per block
 
-template <int VEC>
-struct QjlSmem {
-  static constexpr int table = 128 * kSRow * 2;             // one fp16 table (hi or lo)
-  static constexpr int resid = VEC * kSRow * 2;             // one fp16 residual array (hi or lo)
-  static constexpr int signs = VEC * 16;                    // sign records of the block
-  static constexpr int flags = VEC * 4;
-  static constexpr int list = kRecheckMax * 4 + 16;         // listed products + their count
-  static constexpr int bytes = 2 * table + 2 * resid + signs + flags + list;
-};
+// Operands in 8 x 8 fp16 core matrices (the tensor cores' no-swizzle K-major layout): element
+// (row r, coordinate k) of a 128-coordinate operand at byte cm_off(r, k).
+__host__ __device__ constexpr int cm_off(int r, int k) { return (r >> 3) * 2048 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2; }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -878,6 +872,16 @@ __device__ __forceinline__ uint32_t spread4(uint32_t n) {
   return (n | (n << 1)) & 0x55u;
 }
 
+template <int VEC>
+struct QjlSmem {
+  static constexpr int table = 128 * 128 * 2;               // one fp16 table (hi or lo): S, 128 rows
+  static constexpr int resid = VEC * 128 * 2;               // one fp16 residual array (hi or lo): VEC rows
+  static constexpr int signs = VEC * 16;                    // sign records of the block
+  static constexpr int flags = VEC * 4;
+  static constexpr int list = kRecheckMax * 4 + 16;         // listed products + their count
+  static constexpr int bytes = 2 * table + 2 * resid + signs + flags + list;
+};
+
 // BITS: the code width of the QJL side(s) as a compile-time constant (one encode variant in the
 // kernel's code), or 0 when two QJL sides differ (chosen at run time).  HQ: the key side carries
 // a HeadQ side code (its vectors take encode_vectors); only that variant holds that code.
@@ -885,9 +889,8 @@ template <typename Tin, int BITS, bool HQ, int VEC = kQjlBlockVec>
 __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const AppendParams p) {
   constexpr int D = 128, E = 4;
   using QjlSmem = tqd::QjlSmem<VEC>;
-  // MMA row tiles of the block, warps per row tile, n-tiles (8 sketch rows) per warp
-  constexpr int RT = VEC / 16, WPR = kQjlWarps / RT, NTW = 16 / WPR;
   static_assert(VEC == kQjlBlockVec || VEC == kQjlSmallVec, "block sizes");
+  constexpr uint32_t kCols = VEC < 32 ? 32 : VEC;  // tensor-memory columns: one per vector
   extern __shared__ __align__(16) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int side = (p.qjl[0] && p.qjl[1]) ? (int)blockIdx.y : (p.qjl[0] ? 0 : 1);
@@ -907,12 +910,16 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
 
   // ---- (0) S as fp16 hi / lo rows: the table blob holds them in this layout, so bulk copies
   // bring them in while the vectors are encoded; cleared flags
-  static_assert(2 * QjlSmem::table == (int)tqi::kSketchH16Bytes && kSRow == tqi::kSketchPitch, "table layout");
-  __shared__ __align__(8) unsigned long long s_bar;
-  const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(&s_bar);
+  static_assert(2 * QjlSmem::table == (int)tqi::kSketchH16Bytes, "table layout");
+  __shared__ __align__(8) unsigned long long s_bar, s_mma;
+  __shared__ uint32_t s_tmem;
+  const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(&s_bar), smma = (uint32_t)__cvta_generic_to_shared(&s_mma);
+  // S r: [128 sketch rows][VEC] in tensor memory (64-vector blocks)
+  if (VEC == kQjlBlockVec && warp == 0) tc_alloc((uint32_t)__cvta_generic_to_shared(&s_tmem), kCols);
   if (threadIdx.x == 0) {
     constexpr uint32_t kPiece = (uint32_t)tqi::kSketchH16Bytes / 4;
     mbar_init(sbar, 1);
+    mbar_init(smma, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(sbar, (uint32_t)tqi::kSketchH16Bytes);
     const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem);
@@ -943,8 +950,10 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
         hi[e] = __float2half_rn(x);
         lo[e] = __float2half_rn(x - __half2float(hi[e]));
       }
-      *reinterpret_cast<uint4*>(Rhi + vl * kSRow + kQE * q + i) = *reinterpret_cast<const uint4*>(hi);
-      *reinterpret_cast<uint4*>(Rlo + vl * kSRow + kQE * q + i) = *reinterpret_cast<const uint4*>(lo);
+      *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(Rhi) + cm_off(vl, kQE * q + i)) =
+          *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(Rlo) + cm_off(vl, kQE * q + i)) =
+          *reinterpret_cast<const uint4*>(lo);
     }
   } else {
   constexpr int NV = 2;
@@ -967,8 +976,10 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
         hi[e] = __float2half_rn(x);
         lo[e] = __float2half_rn(x - __half2float(hi[e]));
       }
-      *reinterpret_cast<uint2*>(Rhi + (vb + u) * kSRow + lane * E) = *reinterpret_cast<const uint2*>(hi);
-      *reinterpret_cast<uint2*>(Rlo + (vb + u) * kSRow + lane * E) = *reinterpret_cast<const uint2*>(lo);
+      *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(Rhi) + cm_off(vb + u, lane * E)) =
+          *reinterpret_cast<const uint2*>(hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(Rlo) + cm_off(vb + u, lane * E)) =
+          *reinterpret_cast<const uint2*>(lo);
     }
   }
   }
@@ -986,25 +997,16 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
         hi[e] = __float2half_rn(xs[e]);
         lo[e] = __float2half_rn(xs[e] - __half2float(hi[e]));
       }
-      *reinterpret_cast<uint2*>(Shi + i * kSRow + jj) = *reinterpret_cast<const uint2*>(hi);
-      *reinterpret_cast<uint2*>(Slo + i * kSRow + jj) = *reinterpret_cast<const uint2*>(lo);
+      *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(Shi) + cm_off(i, jj)) = *reinterpret_cast<const uint2*>(hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(Slo) + cm_off(i, jj)) = *reinterpret_cast<const uint2*>(lo);
     }
   }
   __syncthreads();
 
-  // ---- (2) S r: warp w takes row tile w / WPR (vectors 16 (w / WPR) ..) and the NTW n-tiles
-  // (8 sketch rows each) from NTW (w % WPR)
-  const int rt = warp / WPR, nt0 = NTW * (warp % WPR);
-  const uint32_t rhi_s = (uint32_t)__cvta_generic_to_shared(Rhi), rlo_s = (uint32_t)__cvta_generic_to_shared(Rlo);
-  const uint32_t shi_s = (uint32_t)__cvta_generic_to_shared(Shi), slo_s = (uint32_t)__cvta_generic_to_shared(Slo);
-  const int mi = lane >> 3, mr = lane & 7;
-  uint32_t ah[8][4], al[8][4];
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint32_t off = (uint32_t)(((16 * rt + mr + 8 * (mi & 1)) * kSRow + 16 * ks + 8 * (mi >> 1)) * 2);
-    ldsm_x4(rhi_s + off, ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3]);
-    ldsm_x4(rlo_s + off, al[ks][0], al[ks][1], al[ks][2], al[ks][3]);
-  }
+  // ---- (2) S r on the tensor cores, transposed: D[128 sketch rows x VEC vectors] = S R^T, with
+  // D in tensor memory (row i in lane i, vector v in column v).  A = S (hi, lo) and B = the
+  // residuals (hi, lo) are K-major core-matrix operands in shared memory: 8 k-steps of 16
+  // coordinates, passes hi.hi, hi.lo, lo.hi into one fp32 accumulator.
   const float thr = kSignRecheck * kQjlUp;
   // a product too close to zero goes on the block's list (or, past its end, flags the vector)
   auto near_zero = [&](float sv, int v, int row) {
@@ -1014,12 +1016,70 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
       else atomicOr(unc + v, 1u);
     }
   };
+  if constexpr (VEC == kQjlBlockVec) {
+  tc_fence_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  if (threadIdx.x == 0) {
+    const uint32_t sh = (uint32_t)__cvta_generic_to_shared(Shi), sl = (uint32_t)__cvta_generic_to_shared(Slo);
+    const uint32_t rh = (uint32_t)__cvta_generic_to_shared(Rhi), rl = (uint32_t)__cvta_generic_to_shared(Rlo);
+    constexpr uint32_t id = tc_idesc_f16(128, VEC);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      tc_mma_f16(tmem, tc_sdesc(sh + 256 * kk, 128, 2048), tc_sdesc(rh + 256 * kk, 128, 2048), id, kk > 0 ? 1u : 0u);
+      tc_mma_f16(tmem, tc_sdesc(sh + 256 * kk, 128, 2048), tc_sdesc(rl + 256 * kk, 128, 2048), id, 1u);
+      tc_mma_f16(tmem, tc_sdesc(sl + 256 * kk, 128, 2048), tc_sdesc(rh + 256 * kk, 128, 2048), id, 1u);
+    }
+    tc_commit(smma);
+  }
+  // signs: warp w reads lanes 32 (w % 4) .. + 31 (sketch rows) and, for VEC = 64, the vectors
+  // 32 (w / 4) .. + 31; a ballot per vector gives 32 sign bits of its record (bit k of word q =
+  // sketch row 32 q + k)
+  const bool mma_ok = mbar_wait(smma, 0, kStageWaitLimit);
+  tc_fence_after();
+  {
+    const int q = warp & 3, vh = warp >> 2;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    uint32_t* sgw = reinterpret_cast<uint32_t*>(sg);
+    if (mma_ok && (VEC == kQjlBlockVec || vh == 0)) {
+      float val[VEC == kQjlBlockVec ? 32 : 16];
+      if constexpr (VEC == kQjlBlockVec) tc_ld32(trow + 32 * vh, val);
+      else tc_ld16(trow, val);
+#pragma unroll
+      for (int c = 0; c < (VEC == kQjlBlockVec ? 32 : 16); ++c) {
+        const int v = (VEC == kQjlBlockVec ? 32 * vh : 0) + c;
+        const uint32_t word = __ballot_sync(kFull, val[c] >= 0.f);
+        if (lane == c) sgw[v * 4 + q] = word;
+        if (__any_sync(kFull, fabsf(val[c]) < thr)) near_zero(val[c], v, 32 * q + lane);
+      }
+    } else if (!mma_ok) {
+      // the product did not complete within the poll limit: every vector takes the FFMA path
+      for (int v = threadIdx.x; v < VEC; v += blockDim.x) unc[v] = 1u;
+    }
+  }
+  } else {
+  // 16-vector blocks (small appends): warp-level MMAs, whose latency is lower than a tensor-memory
+  // round trip at this size.  Warp w takes sketch rows 16 w .. 16 w + 15 (two n-tiles of 8) for
+  // the block's 16 vectors (one row tile); fragments by ldmatrix from the core matrices, hi*hi in
+  // one fp32 chain and hi*lo + lo*hi in another
+  const uint32_t rhi_s = (uint32_t)__cvta_generic_to_shared(Rhi), rlo_s = (uint32_t)__cvta_generic_to_shared(Rlo);
+  const uint32_t shi_s = (uint32_t)__cvta_generic_to_shared(Shi), slo_s = (uint32_t)__cvta_generic_to_shared(Slo);
+  const int mi = lane >> 3, mr = lane & 7;
+  uint32_t ah[8][4], al[8][4];
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = (uint32_t)cm_off(mr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1));
+    ldsm_x4(rhi_s + off, ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3]);
+    ldsm_x4(rlo_s + off, al[ks][0], al[ks][1], al[ks][2], al[ks][3]);
+  }
 #pragma unroll 1
-  for (int nt = nt0; nt < nt0 + NTW; ++nt) {
+  for (int nt = 2 * warp; nt < 2 * warp + 2; ++nt) {
     float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kp = 0; kp < 4; ++kp) {
-      const uint32_t off = (uint32_t)(((8 * nt + mr) * kSRow + 16 * (2 * kp + (mi >> 1)) + 8 * (mi & 1)) * 2);
+      const uint32_t off = (uint32_t)cm_off(8 * nt + mr, 16 * (2 * kp + (mi >> 1)) + 8 * (mi & 1));
       uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
       ldsm_x4(shi_s + off, h0, h1, h2, h3);
       ldsm_x4(slo_s + off, l0, l1, l2, l3);
@@ -1036,17 +1096,18 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     const uint32_t b0 = __ballot_sync(kFull, s0 >= 0.f), b1 = __ballot_sync(kFull, s1 >= 0.f);
     const uint32_t b2 = __ballot_sync(kFull, s2 >= 0.f), b3 = __ballot_sync(kFull, s3 >= 0.f);
     if (__any_sync(kFull, fminf(fminf(fabsf(s0), fabsf(s1)), fminf(fabsf(s2), fabsf(s3))) < thr)) {
-      const int vg = 16 * rt + (lane >> 2), rw = 8 * nt + 2 * (lane & 3);
+      const int vg = lane >> 2, rw = 8 * nt + 2 * (lane & 3);
       near_zero(s0, vg, rw);
       near_zero(s1, vg, rw + 1);
       near_zero(s2, vg + 8, rw);
       near_zero(s3, vg + 8, rw + 1);
     }
-    if (lane < 16) {  // byte nt of vector 16 rt + lane: bit 2t from b0 / b2, bit 2t + 1 from b1 / b3
+    if (lane < 16) {  // byte nt of vector lane: bit 2t from b0 / b2, bit 2t + 1 from b1 / b3
       const int sh = 4 * (lane & 7);
       const uint32_t lo = ((lane < 8 ? b0 : b2) >> sh) & 0xFu, hi = ((lane < 8 ? b1 : b3) >> sh) & 0xFu;
-      sg[(16 * rt + lane) * 16 + nt] = (unsigned char)(spread4(lo) | (spread4(hi) << 1));
+      sg[lane * 16 + nt] = (unsigned char)(spread4(lo) | (spread4(hi) << 1));
     }
+  }
   }
   __syncthreads();
 
@@ -1060,8 +1121,8 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
       const int v = (int)(e >> 7), row = (int)(e & 127u);
       if (unc[v]) continue;  // the whole vector is taken again below
       const float4 s4 = __ldg(reinterpret_cast<const float4*>(S + row * D + 4 * lane));
-      const uint2 h4 = *reinterpret_cast<const uint2*>(Rhi + v * kSRow + 4 * lane);
-      const uint2 l4 = *reinterpret_cast<const uint2*>(Rlo + v * kSRow + 4 * lane);
+      const uint2 h4 = *reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned char*>(Rhi) + cm_off(v, 4 * lane));
+      const uint2 l4 = *reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned char*>(Rlo) + cm_off(v, 4 * lane));
       const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&h4.x));
       const float2 h23 = __half22float2(*reinterpret_cast<const __half2*>(&h4.y));
       const float2 l01 = __half22float2(*reinterpret_cast<const __half2*>(&l4.x));
@@ -1114,6 +1175,14 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     float res[E];
     encode_vector<D, Tin>(p, side, b, h, j, t, res);
     sketch_signs_ffma<D>(p, side, b, h, t, res, side ? p.tab.S_V_T : p.tab.S_K_T);
+  }
+  if constexpr (VEC == kQjlBlockVec) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      tc_dealloc(s_tmem, kCols);
+    }
   }
 }
 

@@ -39,11 +39,13 @@ struct Layout {
   uint64_t total;
 };
 constexpr int kTileTokens = TQ_TILE_TOKENS;
-// fp16 copies of a 128 x 128 sketch matrix for the tensor-core residual sketch: rows of 136
-// halves (the 272-byte pitch the kernel's shared-memory tables use), the hi terms fp16(S) then
-// the lo terms fp16(S - hi)
-constexpr int kSketchPitch = 136;
-constexpr size_t kSketchH16Bytes = 2 * 128 * kSketchPitch * 2;
+// fp16 copies of a 128 x 128 sketch matrix for the tensor-core residual sketch, the hi terms
+// fp16(S) then the lo terms fp16(S - hi), each in 8 x 8 core matrices (the operand layout of the
+// tensor cores): element (i, j) at byte sketch_cm_offset(i, j) of its 32 KiB table
+constexpr size_t kSketchH16Bytes = 2 * 128 * 128 * 2;
+inline size_t sketch_cm_offset(int i, int j) {
+  return (size_t)(i >> 3) * 2048 + (size_t)(j >> 3) * 128 + (size_t)(i & 7) * 16 + (size_t)(j & 7) * 2;
+}
 inline int region_side(int r) { return r >= R_V_CODES ? 1 : 0; }
 
 // Host tables: Beta Lloyd-Max codebook (float64) and SplitMix64-driven D and S.
