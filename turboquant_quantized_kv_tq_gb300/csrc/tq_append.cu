@@ -840,9 +840,11 @@ constexpr uint32_t kStageWaitLimit = 1u << 20;  // polls of a table copy's mbarr
 // vector for VEC = 64, a warp per vector (two at a time) for VEC = 16, where the latency of one
 // vector matters more than the throughput -- and r, scaled by 256, is kept in shared memory as
 // two fp16 terms (hi, lo = fp16(256 r - hi)).  (2) S r for the block is a [VEC x 128] x
-// [128 x 128] product on the tensor cores: mma.sync m16n8k16 with ldmatrix fragments, S split
-// the same way and bulk-copied from the table blob once per block, hi*hi in one fp32 chain and
-// hi*lo + lo*hi in another; warp ballots turn the signs into bytes of the 1-bit stream.
+// [128 x 128] product on the tensor cores, S split the same way and bulk-copied from the table
+// blob once per block.  VEC = 64: tcgen05, D[128 sketch rows x 64 vectors] = S R^T accumulated
+// in tensor memory from hi*hi, hi*lo and lo*hi (24 MMAs of K = 16), one ballot per vector column
+// for 32 of its sign bits.  VEC = 16: mma.sync m16n8k16 with ldmatrix fragments, hi*hi in one
+// fp32 chain and hi*lo + lo*hi in another, warp ballots for the sign bytes.
 // (3) Every product with |S r| below kSignRecheck is listed and taken again as an fp32 FFMA dot
 // product of the row of S with hi + lo (a warp per listed product), so decisions near zero have
 // fp32 accuracy; the sign bits are patched.  (If more than kRecheckMax products of a block are
@@ -1017,48 +1019,45 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     }
   };
   if constexpr (VEC == kQjlBlockVec) {
-  tc_fence_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  if (threadIdx.x == 0) {
-    const uint32_t sh = (uint32_t)__cvta_generic_to_shared(Shi), sl = (uint32_t)__cvta_generic_to_shared(Slo);
-    const uint32_t rh = (uint32_t)__cvta_generic_to_shared(Rhi), rl = (uint32_t)__cvta_generic_to_shared(Rlo);
-    constexpr uint32_t id = tc_idesc_f16(128, VEC);
+    tc_fence_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    if (threadIdx.x == 0) {
+      const uint32_t sh = (uint32_t)__cvta_generic_to_shared(Shi), sl = (uint32_t)__cvta_generic_to_shared(Slo);
+      const uint32_t rh = (uint32_t)__cvta_generic_to_shared(Rhi), rl = (uint32_t)__cvta_generic_to_shared(Rlo);
+      constexpr uint32_t id = tc_idesc_f16(128, VEC);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      tc_mma_f16(tmem, tc_sdesc(sh + 256 * kk, 128, 2048), tc_sdesc(rh + 256 * kk, 128, 2048), id, kk > 0 ? 1u : 0u);
-      tc_mma_f16(tmem, tc_sdesc(sh + 256 * kk, 128, 2048), tc_sdesc(rl + 256 * kk, 128, 2048), id, 1u);
-      tc_mma_f16(tmem, tc_sdesc(sl + 256 * kk, 128, 2048), tc_sdesc(rh + 256 * kk, 128, 2048), id, 1u);
+      for (int kk = 0; kk < 8; ++kk) {
+        tc_mma_f16(tmem, tc_sdesc(sh + 256 * kk, 128, 2048), tc_sdesc(rh + 256 * kk, 128, 2048), id, kk > 0 ? 1u : 0u);
+        tc_mma_f16(tmem, tc_sdesc(sh + 256 * kk, 128, 2048), tc_sdesc(rl + 256 * kk, 128, 2048), id, 1u);
+        tc_mma_f16(tmem, tc_sdesc(sl + 256 * kk, 128, 2048), tc_sdesc(rh + 256 * kk, 128, 2048), id, 1u);
+      }
+      tc_commit(smma);
     }
-    tc_commit(smma);
-  }
-  // signs: warp w reads lanes 32 (w % 4) .. + 31 (sketch rows) and, for VEC = 64, the vectors
-  // 32 (w / 4) .. + 31; a ballot per vector gives 32 sign bits of its record (bit k of word q =
-  // sketch row 32 q + k)
-  const bool mma_ok = mbar_wait(smma, 0, kStageWaitLimit);
-  tc_fence_after();
-  {
+    // signs: warp w reads lanes 32 (w % 4) .. + 31 (sketch rows) of the columns of vectors
+    // 32 (w / 4) .. + 31; a ballot per vector gives 32 sign bits of its record (bit k of word q =
+    // sketch row 32 q + k)
+    // warp-uniform: the tensor-memory load below is a warp-collective instruction
+    const bool mma_ok = __all_sync(kFull, mbar_wait(smma, 0, kStageWaitLimit));
+    tc_fence_after();
     const int q = warp & 3, vh = warp >> 2;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
     uint32_t* sgw = reinterpret_cast<uint32_t*>(sg);
-    if (mma_ok && (VEC == kQjlBlockVec || vh == 0)) {
-      float val[VEC == kQjlBlockVec ? 32 : 16];
-      if constexpr (VEC == kQjlBlockVec) tc_ld32(trow + 32 * vh, val);
-      else tc_ld16(trow, val);
+    if (mma_ok) {
+      float val[32];
+      tc_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * vh, val);
 #pragma unroll
-      for (int c = 0; c < (VEC == kQjlBlockVec ? 32 : 16); ++c) {
-        const int v = (VEC == kQjlBlockVec ? 32 * vh : 0) + c;
+      for (int c = 0; c < 32; ++c) {
+        const int v = 32 * vh + c;
         const uint32_t word = __ballot_sync(kFull, val[c] >= 0.f);
         if (lane == c) sgw[v * 4 + q] = word;
         if (__any_sync(kFull, fabsf(val[c]) < thr)) near_zero(val[c], v, 32 * q + lane);
       }
-    } else if (!mma_ok) {
+    } else {
       // the product did not complete within the poll limit: every vector takes the FFMA path
       for (int v = threadIdx.x; v < VEC; v += blockDim.x) unc[v] = 1u;
     }
-  }
   } else {
   // 16-vector blocks (small appends): warp-level MMAs, whose latency is lower than a tensor-memory
   // round trip at this size.  Warp w takes sketch rows 16 w .. 16 w + 15 (two n-tiles of 8) for
@@ -1180,6 +1179,9 @@ __global__ void __launch_bounds__(kQjlWarps * 32) append_qjl_mma_kernel(const Ap
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
+      // a product still in flight after the poll limit gets one more bounded wait before its
+      // accumulator is freed (returns at once when it has completed)
+      mbar_wait(smma, 0, kStageWaitLimit);
       tc_fence_after();
       tc_dealloc(s_tmem, kCols);
     }
