@@ -217,7 +217,12 @@ def run_gpu(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_dec)]
 
     def step(timed_events=None):
+        # per scheme: the append of the step's token, then the decode; as one library call (the
+        # query preparation overlaps the append), or, to time the decode calls alone, as two
         for i, kv in enumerate(caches):
+            if timed_events is None and not args.split_step:
+                kv.append_decode(k_new, v_new, q, seq, out=outs[i])
+                continue
             kv.append(k_new, v_new, start)
             if timed_events is not None:
                 timed_events[i][0].record(stream)
@@ -315,7 +320,9 @@ def run_gpu(args):
                    "l2": "inputs larger than L2: four caches of 285-294 MB visited per step",
                    "arith": "append fp32; decode scores/readout fp16 MMA operands, fp32 accumulation",
                    "parallelism": f"independent replicas x{world}",
-                   "step_launch": "CUDA graph replay of the captured step" if graph is not None else "eager"},
+                   "step_launch": "CUDA graph replay of the captured step" if graph is not None else "eager",
+                   "step_calls": ("tq_quantize_append + tq_decode_attention per scheme" if args.split_step
+                                  else "tq_append_decode_attention per scheme")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": decode_traffic(SCHEMES),
                      "kernel": "decode (query prep + fused split-K decode), all four schemes",
@@ -364,8 +371,11 @@ def run_e2e(args, caches, inp, device, seq, start):
     def work():  # copy in, append + decode per scheme, copy out
         in_dev.copy_(in_host, non_blocking=True)
         for i, kv in enumerate(caches):
-            kv.append(k_dev, v_dev, start)
-            kv.decode(q_dev, seq, out=outs[i])
+            if args.split_step:
+                kv.append(k_dev, v_dev, start)
+                kv.decode(q_dev, seq, out=outs[i])
+            else:
+                kv.append_decode(k_dev, v_dev, q_dev, seq, out=outs[i])
         out_host.copy_(outs, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -814,6 +824,9 @@ def main():
     ap.add_argument("--skip-long-context", action="store_true",
                     help="leave out the 128k-context (cfg4) decode leg")
     ap.add_argument("--eager", action="store_true", help="time eager steps instead of a captured graph")
+    ap.add_argument("--split-step", action="store_true",
+                    help="append and decode as two library calls (no overlap of the query preparation "
+                         "with the append)")
     ap.add_argument("--schemes", default=None,
                     help="comma-separated subset of plain4,tq4,kqv4,qkqv4 (default: all four)")
     ap.add_argument("--workload", default=None, choices=["cfg1", "cfg3", "cfg4", "cfg5", "sq", "paged", "append"],

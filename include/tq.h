@@ -216,6 +216,20 @@ tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, cons
                               const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
                               tq_stream stream);
 
+/* One decode step: tq_quantize_append of the step's n_new tokens at positions
+ * host_seq_len[b] - n_new .. host_seq_len[b] - 1 of each sequence, then tq_decode_attention of q
+ * over the first host_seq_len[b] tokens (the new ones included).  The cache and out hold exactly
+ * what those two calls give.  Arguments as there (k, v: device [B][H_kv][n_new][d] of dtype; q,
+ * out: device fp32 [B][H_q][d]); every host_seq_len[b] must be >= n_new (else
+ * TQ_ERR_INVALID_ARG, nothing launched).  At head dim 128 the query preparation runs while the
+ * append's kernels do, and the decode starts on the tokens the append does not write; the
+ * decode reads the new tokens only after the append has completed.  n_new = 0 is
+ * tq_decode_attention. */
+tq_status tq_append_decode_attention(const tq_context* ctx, void* dev_cache, const void* k, const void* v,
+                                     tq_dtype dtype, int32_t n_new, const float* q,
+                                     const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
+                                     tq_stream stream);
+
 /* Several queries per sequence in one pass over the cache (speculative-decode drafts, prefill
  * chunks; [ABL] "Recomendações Práticas" names prefill workloads): the nq queries of sequence b
  * are the chunk's last nq positions, and query i attends causally to the first

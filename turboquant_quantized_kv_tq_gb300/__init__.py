@@ -140,6 +140,24 @@ class QuantizedKVCache(_Codec):
                                      out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream)))
         return out
 
+    def append_decode(self, k, v, q, seq_len, out=None, stream=None):
+        """One decode step: append k, v ([batch][num_kv_heads][n_new][head_dim]) as the last n_new
+        tokens of each sequence (positions seq_len[b] - n_new ..), then decode q over the first
+        seq_len[b] tokens.  The same cache and output as append then decode; the library overlaps
+        the query preparation with the append."""
+        import torch
+        k, v, q = k.contiguous(), v.contiguous(), q.contiguous()
+        if k.shape != v.shape or k.dtype != v.dtype:
+            raise ValueError("k and v must have the same shape and dtype")
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(max(int(x) for x in seq_len))
+        check(_b.tq_append_decode_attention(self._ctx, self.cache.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            _dtype_code(k), int(k.shape[2]), q.data_ptr(),
+                                            _b.int_array(seq_len), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                            _stream_handle(stream)))
+        return out
+
     def decode_multi(self, q, seq_len, out=None, stream=None):
         """q: float32 CUDA tensor [batch][nq][num_q_heads][head_dim]: the last nq positions of each
         sequence, query i attending to the first seq_len[b] - nq + 1 + i tokens."""

@@ -100,6 +100,9 @@ DECLARATIONS = [
     ("tq_decode_workspace_bytes", c_size_t, [c_void_p, c_int32]),
     ("tq_decode_attention", c_int32, [c_void_p, c_void_p, c_void_p, ctypes.POINTER(c_int32), c_void_p,
                                       c_void_p, c_size_t, c_void_p]),
+    ("tq_append_decode_attention", c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
+                                             c_void_p, ctypes.POINTER(c_int32), c_void_p, c_void_p, c_size_t,
+                                             c_void_p]),
     ("tq_prefill_workspace_bytes", c_size_t, [c_void_p, c_int32]),
     ("tq_prefill_attention", c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(c_int32),
                                        c_void_p, c_void_p, c_size_t, c_void_p]),

@@ -388,6 +388,41 @@ tq_status tq_decode_attention(const tq_context* ctx, const void* dev_cache, cons
   return launch_decode(ctx, dev_cache, q, host_seq_len, out, ws, ws_bytes, stream);
 }
 
+tq_status tq_append_decode_attention(const tq_context* ctx, void* dev_cache, const void* k, const void* v,
+                                     tq_dtype dtype, int32_t n_new, const float* q,
+                                     const int32_t* host_seq_len, float* out, void* ws, size_t ws_bytes,
+                                     tq_stream stream) {
+  tq_status s = ready(ctx);
+  if (s != TQ_OK) return s;
+  if (n_new < 0) return fail(TQ_ERR_INVALID_ARG, "n_new must be >= 0");
+  if (!dev_cache || !q || !host_seq_len || !out || !ws) return fail(TQ_ERR_INVALID_ARG, "null argument");
+  if (n_new > 0) {
+    if (!k || !v) return fail(TQ_ERR_INVALID_ARG, "null argument");
+    if (dtype != TQ_F32 && dtype != TQ_BF16 && dtype != TQ_F16) return fail(TQ_ERR_INVALID_ARG, "bad dtype");
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(TQ_ERR_INVALID_ARG, "k, v must be 16-byte aligned");
+  }
+  if (!aligned(dev_cache, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 256))
+    return fail(TQ_ERR_INVALID_ARG, "misaligned pointer (cache/ws 256 B, q/out 16 B)");
+  int max_seq;
+  s = check_lengths(ctx, host_seq_len, &max_seq);
+  if (s != TQ_OK) return s;
+  if (ws_bytes < decode_workspace_bytes(ctx, max_seq)) return fail(TQ_ERR_WORKSPACE, "workspace too small");
+  if (n_new == 0) return launch_decode(ctx, dev_cache, q, host_seq_len, out, ws, ws_bytes, stream);
+  std::vector<int32_t> start((size_t)ctx->cfg.batch);
+  for (int b = 0; b < ctx->cfg.batch; ++b) {
+    if (host_seq_len[b] < n_new) return fail(TQ_ERR_INVALID_ARG, "seq_len must be >= n_new");
+    start[(size_t)b] = host_seq_len[b] - n_new;
+  }
+  if (ctx->cfg.head_dim != 128) {  // the two calls in stream order
+    s = launch_append(ctx, dev_cache, k, v, dtype, n_new, start.data(), stream);
+    if (s != TQ_OK) return s;
+    return launch_decode(ctx, dev_cache, q, host_seq_len, out, ws, ws_bytes, stream);
+  }
+  s = launch_append_early(ctx, dev_cache, k, v, dtype, n_new, start.data(), stream);
+  if (s != TQ_OK) return s;
+  return launch_decode_after_append(ctx, dev_cache, q, host_seq_len, n_new, out, ws, stream);
+}
+
 tq_status tq_decode_attention_multi(const tq_context* ctx, const void* dev_cache, const float* q,
                                     int32_t nq, const int32_t* host_seq_len, float* out, void* ws,
                                     size_t ws_bytes, tq_stream stream) {

@@ -35,6 +35,7 @@ struct AppendParams {
   int qjl_mma;   // QJL sides go to append_qjl_mma_kernel (head dim 128)
   int side_base;     // append_kernel: side of blockIdx.y = 0 (the other, if any, is side_base + 1)
   int wait_primary;  // append_kernel runs as the dependent launch of append_qjl_mma_kernel
+  int release_early; // append_kernel / append_quad_kernel let their dependents launch at once
   int start[TQ_MAX_BATCH];
   const int* dev_start;  // set: start positions from device memory (paged pool)
   // n / n_new and n / Hkv for 0 <= n < 2^31 as (umulhi(n, mul) + n) >> shift
@@ -586,9 +587,11 @@ __device__ __forceinline__ void append_body(const AppendParams& p) {
 // above 128 takes its sketch on the FFMA path, S^T from L2).  Launched right after
 // append_qjl_mma_kernel as its programmatic dependent (the other, non-QJL side), its blocks fill
 // that kernel's last wave; each waits for it before exiting, so this grid's completion still
-// implies the whole append's.
+// implies the whole append's.  With release_early it lets its own dependent (a decode step's
+// query preparation, which waits for it before exiting) launch at once.
 template <int D, typename Tin>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+  if (p.release_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   append_body<D, Tin>(p);
   if (p.wait_primary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
@@ -817,9 +820,10 @@ __device__ __forceinline__ void encode_quad_bits(const AppendParams& p, int side
 // append_qjl_mma_kernel): 32 vectors per block of 4 warps, four lanes per vector; seven blocks
 // per SM (at most 73 registers) put a 4096-token chunk of eight heads in one wave.  As the
 // programmatic dependent of append_qjl_mma_kernel (wait_primary) it waits for that kernel
-// before exiting, as append_kernel does.
+// before exiting, as append_kernel does, and release_early has the same meaning.
 template <typename Tin>
 __global__ void __launch_bounds__(kQuadWarps * 32, 7) append_quad_kernel(const AppendParams p) {
+  if (p.release_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int side = p.side_base + (int)blockIdx.y;
   if (!(p.qjl[side] && p.qjl_mma)) {
     const long long per_side = (long long)p.B * p.Hkv * p.n_new;
@@ -1392,7 +1396,7 @@ struct PagedAppend {
 
 static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, const void* v,
                              tq_dtype dtype, int n_new, const int32_t* start, const PagedAppend* pg,
-                             Stream stream) {
+                             Stream stream, bool release_early = false) {
   using namespace tqd;
   AppendParams p;
   p.tab = make_tables(ctx);
@@ -1407,6 +1411,7 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
   p.bits[0] = ctx->cfg.k.bits; p.rotate[0] = ctx->cfg.k.rotate; p.qjl[0] = ctx->cfg.k.qjl;
   p.bits[1] = ctx->cfg.v.bits; p.rotate[1] = ctx->cfg.v.rotate; p.qjl[1] = ctx->cfg.v.qjl;
   p.headq_rank = ctx->cfg.headq_rank;
+  p.release_early = release_early ? 1 : 0;  // (append_qjl_mma_kernel always releases at its start)
   for (int b = 0; b < TQ_MAX_BATCH; ++b) p.start[b] = (!pg && b < ctx->cfg.batch) ? start[b] : 0;
   const int nv = ctx->cfg.head_dim == 128 ? AppendNV<128>::value : 1;
   const long long per_side = (long long)p.B * p.Hkv * n_new;
@@ -1518,6 +1523,11 @@ static tq_status append_impl(const tq_context* ctx, void* cache, const void* k, 
 tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
                         tq_dtype dtype, int n_new, const int32_t* start, Stream stream) {
   return append_impl(ctx, cache, k, v, dtype, n_new, start, nullptr, stream);
+}
+
+tq_status launch_append_early(const tq_context* ctx, void* cache, const void* k, const void* v,
+                              tq_dtype dtype, int n_new, const int32_t* start, Stream stream) {
+  return append_impl(ctx, cache, k, v, dtype, n_new, start, nullptr, stream, true);
 }
 
 tq_status launch_append_paged(const tq_context* ctx, void* pool, const tq_page_table* pt, const void* k,

@@ -68,6 +68,7 @@ struct PrepParams {
   float* out;
   float* sk_final;  // zeroed for empty sequences (head dim > 128 with a QJL value side)
   int n_tickets, n_heads, Hq, Hkv, G, Gc, nq, k_rotate, kq, kh, m, B;
+  int after_append;  // launched as the programmatic dependent of a decode step's append
   int seq_len[TQ_MAX_BATCH];
   const int* dev_seq_len;  // set: lengths from device memory, clamped to [0, lmax]; the work
   int lmax;                // split is then computed into *plan
@@ -145,12 +146,9 @@ __device__ __forceinline__ void store_hi_lo(uint32_t* hi, uint32_t* lo, const fl
 // pairs.  Block 0 also clears the split tickets and the error word; queries of empty sequences
 // get a zero output (no decode block writes them).
 template <int D>
-__global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
+__device__ __forceinline__ void prep_body(const PrepParams& p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
-  // the decode launched after this kernel may start its own setup now (it waits for this
-  // kernel's results before reading them)
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   extern __shared__ __align__(16) float skt_smem[];
   const float* SKT = p.tab.S_K_T;
   if (D == kDecD && p.kq) {  // S_K^T (64 KiB) into shared memory: 128 dependent rows per head
@@ -253,6 +251,18 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   }
 }
 
+// The decode launched after this kernel may start its own setup at once: it waits for this
+// kernel's results before reading them.  In a decode step (after_append) this kernel is itself
+// the programmatic dependent of the step's append, whose output it never reads: it waits for the
+// append only before exiting, so its completion -- what the decode waits for -- implies the
+// append's.
+template <int D>
+__global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  prep_body<D>(p);
+  if (p.after_append) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
 tq_status cuda_fail(const char* what, cudaError_t e) {
   tqi::set_error(std::string(what) + ": " + cudaGetErrorString(e));
   return TQ_ERR_CUDA;
@@ -306,9 +316,11 @@ struct PagedDecode {
   const int32_t* dev_seq_len;
 };
 
+// n_fresh > 0: a decode step right after launch_append_early on the same stream (head dim 128,
+// contiguous cache), whose tokens are each sequence's last n_fresh.
 static tq_status decode_impl(const tq_context* ctx, const void* cache, const float* q, int nq,
                              const int32_t* seq_len, const PagedDecode* pg, float* out, void* ws,
-                             Stream stream) {
+                             Stream stream, int n_fresh = 0) {
   using namespace tqd;
   const int D = ctx->cfg.head_dim;
   const WsLayout w = ws_layout(ctx);
@@ -360,6 +372,11 @@ static tq_status decode_impl(const tq_context* ctx, const void* cache, const flo
   pp.dev_seq_len = pg ? pg->dev_seq_len : nullptr;
   pp.lmax = pg ? kTile * pg->pt->max_blocks_per_seq : 0;
   pp.plan = pg ? (DevPlan*)(base + w.plan) : nullptr;
+  pp.after_append = n_fresh > 0 ? 1 : 0;
+  if (n_fresh > 0 && (pg || D != kDecD)) {
+    set_error("the overlapped decode step is built for a contiguous cache at head dim 128");
+    return TQ_ERR_UNSUPPORTED;
+  }
   if (pg && D != kDecD) {
     set_error("the paged decode is built for head dim 128");
     return TQ_ERR_UNSUPPORTED;
@@ -370,7 +387,20 @@ static tq_status decode_impl(const tq_context* ctx, const void* cache, const flo
     cudaError_t ae = cudaFuncSetAttribute(prep_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
     if (ae != cudaSuccess) return cuda_fail("decode prep", ae);
   }
-  switch (D) {
+  if (pp.after_append) {  // the programmatic dependent of the step's append (head dim 128)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = pgrid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = (size_t)psmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, prep_kernel<128>, pp);
+    if (le != cudaSuccess) return cuda_fail("decode prep", le);
+  } else switch (D) {
     case 128: prep_kernel<128><<<pgrid, 256, psmem, s>>>(pp); break;
     case 256: prep_kernel<256><<<pgrid, 256, 0, s>>>(pp); break;
     case 512: prep_kernel<512><<<pgrid, 256, 0, s>>>(pp); break;
@@ -401,6 +431,7 @@ static tq_status decode_impl(const tq_context* ctx, const void* cache, const flo
   p.score_scale = kLog2e / sqrtf((float)D);
   p.qjl_scale = (float)(1.2533141373155003 / ctx->m);
   p.err = pp.err;
+  p.n_fresh = n_fresh;
   long long W = 0;  // 16-token tiles over all slabs
   for (int b = 0; b < TQ_MAX_BATCH; ++b) {
     p.seq_len[b] = pp.seq_len[b];
@@ -432,6 +463,12 @@ tq_status launch_decode_multi(const tq_context* ctx, const void* cache, const fl
                               Stream stream) {
   (void)ws_bytes;
   return decode_impl(ctx, cache, q, nq, seq_len, nullptr, out, ws, stream);
+}
+
+tq_status launch_decode_after_append(const tq_context* ctx, const void* cache, const float* q,
+                                     const int32_t* seq_len, int n_fresh, float* out, void* ws,
+                                     Stream stream) {
+  return decode_impl(ctx, cache, q, 1, seq_len, nullptr, out, ws, stream, n_fresh);
 }
 
 tq_status launch_decode_paged(const tq_context* ctx, const void* pool, const tq_page_table* pt,

@@ -82,6 +82,8 @@ struct DecodeParams {
   int B, Hkv, G, v_rotate, nblocks;
   int nq, Gc;             // queries per sequence (query i sees tokens [0, seq_len - nq + 1 + i))
   int lo_xor;             // lo columns: lane xor to add them back (Gc / 2), -1 when Gc = 1
+  int n_fresh;            // each sequence's last n_fresh tokens are being written by the step's
+                          // append until grid_dependency_wait returns (0: none)
   long long W;            // number of 16-token tiles over all (batch, KV head) slabs
   float score_scale;      // log2(e) / sqrt(d)
   float qjl_scale;        // sqrt(pi/2) / m
@@ -1101,6 +1103,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
   const long long x_end = (long long)(blockIdx.x + 1) * W / N;
   unsigned seq = 0;  // tile pairs this warp has streamed so far: stage seq % S, phase (seq / S) & 1
   bool timed_out = false;
+  bool waited = PAGED;  // grid_dependency_wait has returned (the paged decode waits above)
 
   while (x < x_end) {
     // ---- locate the slab segment that starts at tile x
@@ -1136,18 +1139,30 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     // registers, before the pair is computed
     constexpr uint32_t KBL = SG::VC, VBL = SG::bytes - SG::VC, PB = 2 * SG::bytes;
     const int npairs = (nt + 1) >> 1;
-#pragma unroll
-    for (int k = 0; k < kPairStages; ++k) {
-      if (k < npairs) {
-        const unsigned sl = (seq + k) % kPairStages;
-        issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
-                                       min(2, nt - 2 * k), lane, p.cache, b, kvh);
-      }
+    const int n_first = npairs < kPairStages ? npairs : kPairStages;
+    // before the first wait, only pair stages whose tiles hold none of the step's new tokens
+    int n_early = n_first;
+    if (p.n_fresh > 0 && !waited) {
+      const int fresh_tile = (L - p.n_fresh) / kTile;  // first tile with a new token
+      for (int k = 0; k < n_first; ++k)
+        if (m0t + 2 * k + min(2, nt - 2 * k) > fresh_tile) { n_early = k; break; }
+    }
+    for (int k = 0; k < n_early; ++k) {
+      const unsigned sl = (seq + k) % kPairStages;
+      issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
+                                     min(2, nt - 2 * k), lane, p.cache, b, kvh);
     }
     // the query prep kernel runs just before this one: its outputs (query fragments, tickets,
     // error word) are read only from here on, so the table build and the first bulk copies above
-    // overlap it (programmatic dependent launch; a no-op without one)
+    // overlap it (programmatic dependent launch; a no-op without one).  In a decode step its
+    // completion also covers the append's, so the deferred stages are issued after it.
     grid_dependency_wait();
+    waited = true;
+    for (int k = n_early; k < n_first; ++k) {
+      const unsigned sl = (seq + k) % kPairStages;
+      issue_pair<KB, KQ, KH, VB, VQ, PAGED>(my_stages_s + sl * PB, my_bars + 8 * sl, sp, m0t + 2 * k,
+                                     min(2, nt - 2 * k), lane, p.cache, b, kvh);
+    }
 
     // ---- query fragments: column lg of KV head kvh, dims [32 lt, 32 lt + 32); columns Gc ..
     // 2 Gc - 1 hold the lo terms when they ride in the same MMA

@@ -78,6 +78,10 @@ namespace tqi {
 typedef struct CUstream_st* Stream;
 tq_status launch_append(const tq_context* ctx, void* cache, const void* k, const void* v,
                         tq_dtype dtype, int n_new, const int32_t* start, Stream stream);
+// The same append with its last kernel releasing its programmatic dependents at its start, so
+// that a decode step's query preparation (launch_decode_after_append) runs beside it.
+tq_status launch_append_early(const tq_context* ctx, void* cache, const void* k, const void* v,
+                              tq_dtype dtype, int n_new, const int32_t* start, Stream stream);
 tq_status launch_append_paged(const tq_context* ctx, void* pool, const tq_page_table* pt, const void* k,
                               const void* v, tq_dtype dtype, int n_new, const int32_t* dev_start,
                               int32_t* dev_error, Stream stream);
@@ -95,6 +99,12 @@ tq_status launch_decode_paged(const tq_context* ctx, const void* pool, const tq_
 tq_status launch_decode(const tq_context* ctx, const void* cache, const float* q,
                         const int32_t* seq_len, float* out, void* ws, size_t ws_bytes,
                         Stream stream);
+// The decode right after launch_append_early on the same stream (head dim 128): the query
+// preparation is the append's programmatic dependent and waits for it before it exits; the decode
+// reads each sequence's last n_fresh tokens only after its own wait for the preparation.
+tq_status launch_decode_after_append(const tq_context* ctx, const void* cache, const float* q,
+                                     const int32_t* seq_len, int n_fresh, float* out, void* ws,
+                                     Stream stream);
 size_t prefill_workspace_bytes(const tq_context* ctx, int nq);
 tq_status launch_prefill(const tq_context* ctx, const void* cache, const float* q, int nq,
                          const int32_t* seq_len, float* out, void* ws, Stream stream);
