@@ -71,12 +71,14 @@ def test_static_scratch_wide_value_sketch_against_oracle():
     ref = pair.orc.decode(buf, inp.q, seq)
     q = torch.from_numpy(inp.q).cuda()
     stream = torch.cuda.current_stream().cuda_stream
+    ws_out = pair.gpu.decode(q, seq).cpu().numpy()  # the same kernels and split on a workspace
     for _ in range(2):
         out = torch.full_like(q, float("nan"))
         b.check(b.tq_decode_attention_static(pair.gpu._ctx, pair.gpu.cache.data_ptr(), q.data_ptr(),
                                              b.int_array(seq), out.data_ptr(), stream))
         torch.cuda.synchronize()
         assert _static_error_word(stream) == (b.TQ_OK, 0)
+        assert np.array_equal(out.cpu().numpy(), ws_out)
         got = out.cpu().numpy().astype(np.float64)
         assert rel_err(got, ref) <= ATTN_TOL, rel_err(got, ref)
 

@@ -12,7 +12,7 @@ constexpr int kLogitsTokensPerBlock = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct WsLayout {
-  size_t err, tickets, q_rot, q_sk, q_u, q_rot_lo, q_sk_lo, part, sk_final, sk_part, plan, total;
+  size_t err, tickets, q_rot, q_sk, q_u, q_rot_lo, q_sk_lo, part, sk_final, sk_part, total;
   int ps;
 };
 
@@ -42,7 +42,6 @@ WsLayout ws_layout(const tq_context* ctx) {
   const bool wide_vq = D > kDecD && ctx->cfg.v.qjl;  // acc_sk / l per head for the sketch pass
   w.sk_final = off; off = align256(off + (wide_vq ? (size_t)B * Hq * ctx->m * sizeof(float) : 0));
   w.sk_part = off; off = align256(off + (wide_vq ? (size_t)(ctx->m / kSkRows) * B * Hq * D * sizeof(float) : 0));
-  w.plan = off; off = align256(off + (D == kDecD ? sizeof(DevPlan) : 0));  // device lengths (paged)
   w.total = off;
   return w;
 }
@@ -70,57 +69,14 @@ struct PrepParams {
   int n_tickets, n_heads, Hq, Hkv, G, Gc, nq, k_rotate, kq, kh, m, B;
   int after_append;  // launched as the programmatic dependent of a decode step's append
   int seq_len[TQ_MAX_BATCH];
-  const int* dev_seq_len;  // set: lengths from device memory, clamped to [0, lmax]; the work
-  int lmax;                // split is then computed into *plan
-  DevPlan* plan;
+  const int* dev_seq_len;  // set: lengths from device memory, clamped to [0, lmax] (the decode
+  int lmax;                // blocks compute the work split from them)
   __device__ __forceinline__ int len(int b) const {
     if (!dev_seq_len) return seq_len[b];
     const int L = __ldg(dev_seq_len + b);
     return L < 0 ? 0 : (L > lmax ? lmax : L);
   }
 };
-
-// Work split of the decode from device lengths, by block 0 of prep_kernel (256 threads, two
-// batch entries each): plan->seq_len = the clamped lengths, plan->batch_start = the exclusive
-// prefix sum of H_kv * ceil(len / 16), plan->W = the total.  A length outside [0, lmax] is
-// recorded as TQ_DEVERR_BAD_LENGTH (after the error word's reset).
-__device__ void build_plan(const PrepParams& p) {
-  static_assert(TQ_MAX_BATCH == 512, "two batch entries per thread of a 256-thread block");
-  __shared__ long long wtot[8];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long v[2];
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int b = 2 * threadIdx.x + i;
-    int L = 0;
-    if (b < p.B) {
-      const int raw = __ldg(p.dev_seq_len + b);
-      bad |= raw < 0 || raw > p.lmax;
-      L = p.len(b);
-    }
-    p.plan->seq_len[b] = L;
-    v[i] = (long long)p.Hkv * ((L + kTile - 1) / kTile);
-  }
-  long long t = v[0] + v[1];  // inclusive scan over the block
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long n = __shfl_up_sync(kFull, t, o);
-    if (lane >= o) t += n;
-  }
-  if (lane == 31) wtot[warp] = t;
-  __syncthreads();
-  long long before = 0;
-  for (int w = 0; w < warp; ++w) before += wtot[w];
-  const long long ex = before + t - v[0] - v[1];
-  p.plan->batch_start[2 * threadIdx.x] = ex;
-  p.plan->batch_start[2 * threadIdx.x + 1] = ex + v[0];
-  if (threadIdx.x == blockDim.x - 1) {
-    p.plan->batch_start[TQ_MAX_BATCH] = before + t;
-    p.plan->W = before + t;
-  }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicExch(p.err, TQ_DEVERR_BAD_LENGTH);
-}
 
 // E values as fp16 pairs at hi and their fp16 remainders (x - hi) at lo.
 template <int E>
@@ -159,10 +115,6 @@ __device__ __forceinline__ void prep_body(const PrepParams& p) {
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < p.n_tickets; i += blockDim.x) p.tickets[i] = 0;
     if (threadIdx.x == 0) p.err[0] = 0;
-    if (p.plan) {
-      __syncthreads();  // the reset above comes before any error the plan records
-      build_plan(p);
-    }
   }
   const int head = blockIdx.x * 8 + (threadIdx.x >> 5);  // flat column index
   if (head >= p.n_heads) return;
@@ -371,7 +323,6 @@ static tq_status decode_impl(const tq_context* ctx, const void* cache, const flo
   for (int b = 0; b < TQ_MAX_BATCH; ++b) pp.seq_len[b] = (!pg && b < B) ? seq_len[b] : 0;
   pp.dev_seq_len = pg ? pg->dev_seq_len : nullptr;
   pp.lmax = pg ? kTile * pg->pt->max_blocks_per_seq : 0;
-  pp.plan = pg ? (DevPlan*)(base + w.plan) : nullptr;
   pp.after_append = n_fresh > 0 ? 1 : 0;
   if (n_fresh > 0 && (pg || D != kDecD)) {
     set_error("the overlapped decode step is built for a contiguous cache at head dim 128");
@@ -411,7 +362,8 @@ static tq_status decode_impl(const tq_context* ctx, const void* cache, const flo
 
   p.tab = tab;
   p.cache = pg ? make_paged_cache(ctx, cache, *pg->pt, pp.err) : make_cache(ctx, cache);
-  p.plan = pp.plan;
+  p.dev_seq_len = pp.dev_seq_len;
+  p.lmax = pp.lmax;
   p.q_rot = pp.q_rot;
   p.q_sk = pp.q_sk;
   p.q_u = pp.q_u;

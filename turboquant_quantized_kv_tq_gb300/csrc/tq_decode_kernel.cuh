@@ -52,14 +52,6 @@ constexpr int kPairStages = 2;  // per-warp ring of 32-token (two-tile) stages
 constexpr int kMaxBlocks = 256;  // partial slots reserved for blocks (>= SM count)
 constexpr int kLutStride = 256;  // bytes between table entries
 
-// The work split when sequence lengths live in device memory: written by prep_kernel from the
-// lengths (clamped to the block table) and read by the decode in place of the DecodeParams copies.
-struct DevPlan {
-  long long W;
-  long long batch_start[TQ_MAX_BATCH + 1];
-  int seq_len[TQ_MAX_BATCH];
-};
-
 struct DecodeParams {
   Tables tab;
   Cache cache;
@@ -89,14 +81,10 @@ struct DecodeParams {
   float qjl_scale;        // sqrt(pi/2) / m
   int seq_len[TQ_MAX_BATCH];
   long long batch_start[TQ_MAX_BATCH + 1];  // first tile of batch b: Hkv * sum of ceil(len/16)
-  const DevPlan* plan;    // paged pool: W, seq_len and batch_start come from here (device lengths)
-  template <bool DEV> __device__ __forceinline__ long long tiles() const { return DEV ? __ldcg(&plan->W) : W; }
-  template <bool DEV> __device__ __forceinline__ long long bstart(int b) const {
-    return DEV ? __ldcg(plan->batch_start + b) : batch_start[b];
-  }
-  template <bool DEV> __device__ __forceinline__ int len(int b) const {
-    return DEV ? __ldcg(plan->seq_len + b) : seq_len[b];
-  }
+  // paged pool: lengths in device memory (clamped to [0, lmax]); each block then computes W,
+  // seq_len and batch_start itself (paged_plan) in place of the copies above
+  const int* dev_seq_len;
+  int lmax;
 };
 
 template <int B>
@@ -498,22 +486,24 @@ struct SlabPtrs {
     kbytes = C.block[0];
     vbytes = C.block[1];
   }
-  __device__ __forceinline__ static int load_page(const Cache& C, int b, int t, int t_end) {
-    return t < t_end ? C.page_of(b, t) : 0;
+  int* err;  // where a bad table entry is recorded
+  __device__ __forceinline__ int load_page(const Cache& C, int b, int t) const {
+    return t < t_end ? C.page_of(b, t, err) : 0;
   }
-  __device__ __forceinline__ void init_pages(const Cache& C, int b, int m0t, int m1t, int lane) {
+  __device__ __forceinline__ void init_pages(const Cache& C, int b, int m0t, int m1t, int lane, int* e) {
     t_base = m0t;
     t_end = m1t;
-    pg0 = load_page(C, b, m0t + lane, m1t);
-    pg1 = load_page(C, b, m0t + 32 + lane, m1t);
+    err = e;
+    pg0 = load_page(C, b, m0t + lane);
+    pg1 = load_page(C, b, m0t + 32 + lane);
   }
   // page of `tile` (warp-uniform and non-decreasing from call to call; every lane calls)
   __device__ __forceinline__ int page(const Cache& C, int b, int tile, int lane) {
     const int w = (tile - t_base) >> 5;
     if (w != 0) {  // a later window: shift (the next one is in pg1) and load the one after it
-      pg0 = w == 1 ? pg1 : load_page(C, b, t_base + 32 * w + lane, t_end);
+      pg0 = w == 1 ? pg1 : load_page(C, b, t_base + 32 * w + lane);
       t_base += 32 * w;
-      pg1 = load_page(C, b, t_base + 32 + lane, t_end);
+      pg1 = load_page(C, b, t_base + 32 + lane);
     }
     return __shfl_sync(kFull, pg0, (tile - t_base) & 31);
   }
@@ -1048,6 +1038,53 @@ __device__ __forceinline__ int owner_block(long long x, long long W, int N) {
   return (int)(((x + 1) * N - 1) / W);
 }
 
+// Paged pool: the stream-K split from the lengths in device memory, computed by every decode
+// block into shared memory after its barriers (kPagedPlanBytes more dynamic shared memory):
+// len[b] = the length clamped to [0, lmax], bs[b] = H_kv * sum over b' < b of ceil(len[b'] / 16),
+// bs[TQ_MAX_BATCH] = W.  The lengths, like the cache and the block table, were complete before
+// the query prep started, so nothing here waits for it.  Returns, block-uniformly, whether a
+// length lay outside [0, lmax] (recorded after the first wait, once prep has cleared the word).
+constexpr uint32_t kPlanLenOff = 8 * (TQ_MAX_BATCH + 2);       // after bs[TQ_MAX_BATCH + 1]
+constexpr uint32_t kPlanSumOff = kPlanLenOff + 4 * TQ_MAX_BATCH;
+constexpr uint32_t kPagedPlanBytes = kPlanSumOff + 8 * 32;    // + per-warp scan totals
+template <int NW>
+__device__ __forceinline__ bool paged_plan(const DecodeParams& p, unsigned char* area) {
+  static_assert(NW * 64 >= TQ_MAX_BATCH && NW <= 32, "two batch entries per thread");
+  long long* const bs = reinterpret_cast<long long*>(area);
+  int* const len = reinterpret_cast<int*>(area + kPlanLenOff);
+  long long* const wsum = reinterpret_cast<long long*>(area + kPlanSumOff);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long v[2];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int b = 2 * (int)threadIdx.x + i;
+    int L = 0;
+    if (b < p.B) {
+      const int raw = __ldg(p.dev_seq_len + b);
+      bad |= raw < 0 || raw > p.lmax;
+      L = raw < 0 ? 0 : (raw > p.lmax ? p.lmax : raw);
+    }
+    if (b < TQ_MAX_BATCH) len[b] = L;
+    v[i] = (long long)p.Hkv * ((L + kTile - 1) / kTile);
+  }
+  long long t = v[0] + v[1];  // inclusive scan over the block
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(kFull, t, o);
+    if (lane >= o) t += n;
+  }
+  if (lane == 31) wsum[warp] = t;
+  __syncthreads();
+  long long before = 0;
+  for (int w = 0; w < warp; ++w) before += wsum[w];
+  const long long ex = before + t - v[0] - v[1];
+  if (2 * (int)threadIdx.x < TQ_MAX_BATCH) bs[2 * threadIdx.x] = ex;
+  if (2 * (int)threadIdx.x + 1 < TQ_MAX_BATCH) bs[2 * threadIdx.x + 1] = ex + v[0];
+  if ((int)threadIdx.x == NW * 32 - 1) bs[TQ_MAX_BATCH] = before + t;
+  return __syncthreads_or(bad) != 0;  // (also makes the plan visible to the whole block)
+}
+
 // Programmatic dependent launch: wait until the preceding kernel of the stream has completed and
 // its memory is visible (returns at once when the launch had no programmatic dependency).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
@@ -1063,6 +1100,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
   constexpr int PS = SM::PS;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_last;
+  __shared__ int s_page_err[SM::NW];  // paged: a bad table entry met before the first wait
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane >> 2, lt = lane & 3;
 
@@ -1093,29 +1131,44 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
   const int G = p.G;          // query heads per KV head
   const int Gc = p.Gc;        // query columns per KV head (G nq)
   const int Hq = p.Hkv * G;
-  if constexpr (PAGED) grid_dependency_wait();  // the work split itself comes from the prep kernel
-  const long long W = p.tiles<PAGED>();
+  unsigned char* const plan = win + SM::bytes;  // paged: the split (paged_plan)
+  bool bad_len = false;
+  if constexpr (PAGED) {
+    if (lane == 0) s_page_err[warp] = 0;
+    bad_len = paged_plan<SM::NW>(p, plan);
+  }
+  const long long* const pl_bs = reinterpret_cast<const long long*>(plan);
+  const int* const pl_len = reinterpret_cast<const int*>(plan + kPlanLenOff);
+  auto bstart = [&](int b) -> long long { return PAGED ? pl_bs[b] : p.batch_start[b]; };
+  auto slen = [&](int b) -> int { return PAGED ? pl_len[b] : p.seq_len[b]; };
+  const long long W = PAGED ? pl_bs[TQ_MAX_BATCH] : p.W;
   // with host lengths nblocks = min(W, #SMs); with device lengths (paged) the grid is #SMs and the
   // same min is taken here, so every working block has a non-empty range (the merge counts on it)
   const int N = PAGED ? (int)(W < p.nblocks ? W : p.nblocks) : p.nblocks;
-  if ((int)blockIdx.x >= N) return;
+  if ((int)blockIdx.x >= N) {
+    if (PAGED && bad_len && blockIdx.x == 0) {  // no block works: block 0 records it
+      grid_dependency_wait();
+      if (threadIdx.x == 0) atomicExch(p.err, TQ_DEVERR_BAD_LENGTH);
+    }
+    return;
+  }
   long long x = (long long)blockIdx.x * W / N;
   const long long x_end = (long long)(blockIdx.x + 1) * W / N;
   unsigned seq = 0;  // tile pairs this warp has streamed so far: stage seq % S, phase (seq / S) & 1
   bool timed_out = false;
-  bool waited = PAGED;  // grid_dependency_wait has returned (the paged decode waits above)
+  bool waited = false;  // grid_dependency_wait has returned
 
   while (x < x_end) {
     // ---- locate the slab segment that starts at tile x
     int lo = 0, hi = p.B - 1;  // largest b with batch_start[b] <= x
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.bstart<PAGED>(mid) <= x) lo = mid; else hi = mid - 1;
+      if (bstart(mid) <= x) lo = mid; else hi = mid - 1;
     }
     const int b = lo;
-    const int L = p.len<PAGED>(b);
+    const int L = slen(b);
     const int ntb = (L + kTile - 1) / kTile;  // tiles per slab of batch b
-    const long long bs = p.bstart<PAGED>(b);
+    const long long bs = bstart(b);
     const long long off = x - bs;
     const int kvh = (int)(off / ntb);
     const int ts = (int)(off % ntb);  // first tile of the segment
@@ -1132,7 +1185,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     const int nt = m1t - m0t;
     SlabPtrs sp;
     if constexpr (!PAGED) sp.init(p.cache, b, kvh);
-    else sp.init_pages(p.cache, b, m0t, m1t, lane);
+    else sp.init_pages(p.cache, b, m0t, m1t, lane, waited ? p.err : s_page_err + warp);
     WarpState<VQ && QLO> st;
     st.reset();
     // both pair stages in flight; a pair stage is refilled as soon as its operands are in
@@ -1157,6 +1210,14 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     // overlap it (programmatic dependent launch; a no-op without one).  In a decode step its
     // completion also covers the append's, so the deferred stages are issued after it.
     grid_dependency_wait();
+    if constexpr (PAGED) {
+      if (!waited) {  // prep has cleared the error word: record what the split and the early
+        __syncwarp();  // table reads met, and record directly from here on
+        if (lane == 0 && s_page_err[warp] != 0) atomicExch(p.err, s_page_err[warp]);
+        if (threadIdx.x == 0 && bad_len) atomicExch(p.err, TQ_DEVERR_BAD_LENGTH);
+        sp.err = p.err;
+      }
+    }
     waited = true;
     for (int k = n_early; k < n_first; ++k) {
       const unsigned sl = (seq + k) % kPairStages;
@@ -1654,17 +1715,19 @@ cudaError_t check_dyn_base(K kernel) {
 template <int KB, bool KQ, bool KH, int VB, bool VQ, bool QLO, bool PAGED>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t s) {
   using SM = DecodeSmem<KB, KQ, KH, VB, VQ, QLO>;
-  static_assert(SM::bytes <= 227 * 1024, "decode shared memory exceeds the per-block limit");
+  constexpr uint32_t bytes = SM::bytes + (PAGED ? kPagedPlanBytes : 0u);
+  static_assert(SM::bytes % 8 == 0, "the paged plan area needs 8-byte alignment");
+  static_assert(bytes <= 227 * 1024, "decode shared memory exceeds the per-block limit");
   auto kern = decode_kernel<KB, KQ, KH, VB, VQ, QLO, PAGED>;
   cudaError_t e = check_dyn_base(kern);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::bytes);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   // may start while the query prep kernel still runs (it waits in grid_dependency_wait)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(SM::NW * 32);
-  cfg.dynamicSmemBytes = SM::bytes;
+  cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

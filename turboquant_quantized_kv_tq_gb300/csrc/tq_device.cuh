@@ -53,15 +53,17 @@ struct Cache {
   int num_pages;
   int* err;
 
-  __device__ __forceinline__ int page_of(int b, int tile) const {
+  // (e: where a bad entry is recorded, when not null)
+  __device__ __forceinline__ int page_of(int b, int tile, int* e) const {
     int page = -1;
     if ((unsigned)tile < (unsigned)max_blocks) page = __ldg(block_table + (long long)b * max_blocks + tile);
     if ((unsigned)page >= (unsigned)num_pages) {
-      if (err) atomicExch(err, TQ_DEVERR_BAD_PAGE);
+      if (e) atomicExch(e, TQ_DEVERR_BAD_PAGE);
       page = num_pages;
     }
     return page;
   }
+  __device__ __forceinline__ int page_of(int b, int tile) const { return page_of(b, tile, err); }
   // block `tile` of slab (b, h) on side 0 (K) or 1 (V)
   __device__ __forceinline__ unsigned char* blockp(int side, int b, int h, int tile) const {
     const unsigned long long blk =
