@@ -443,16 +443,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       bool moved = false;
       if (kr < ks && tc_mbar_test(B_P, (uint32_t)kr & 1u)) {
         tc_fence_after();
-        const uint32_t vb = sb + SM::VV + (kr % NB) * SM::TILE;
+        // each batch's descriptors from one base: a step of 256 (4096) bytes adds 16 (256) to the
+        // address field, which stays below 2^14 for every shared-memory address
+        const uint64_t dv = tc_sdesc(sb + SM::VV + (kr % NB) * SM::TILE, 2048, 128);
 #pragma unroll
         for (int kk = 0; kk < kTcTok / 16; ++kk)
-          tc_mma_f16_ta(tmem + kTcO, tmem + TC::P + 8 * kk, tc_sdesc(vb + 4096 * kk, 2048, 128), idO,
-                        (kr > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ta(tmem + kTcO, tmem + TC::P + 8 * kk, dv + 256u * kk, idO, (kr > 0 || kk > 0) ? 1u : 0u);
         if constexpr (VQ) {
-          const uint32_t vsb = sb + SM::VS + (kr % NB) * SM::TILE;
+          const uint64_t dvs = tc_sdesc(sb + SM::VS + (kr % NB) * SM::TILE, 2048, 128);
 #pragma unroll
           for (int kk = 0; kk < kTcTok / 16; ++kk)
-            tc_mma_f16_ta(tmem + TC::OSK, tmem + TC::PSK + 8 * kk, tc_sdesc(vsb + 4096 * kk, 2048, 128), idO,
+            tc_mma_f16_ta(tmem + TC::OSK, tmem + TC::PSK + 8 * kk, dvs + 256u * kk, idO,
                           (kr > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(B_O + 8 * (kr % NB));
@@ -464,19 +465,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
           tc_mbar_test(B_U + 8 * (ks % NB), (uint32_t)(ks / NB) & 1u)) {
         tc_fence_after();
         const int bf = ks % NB;
-        const uint32_t kh = sb + SM::KHI + bf * SM::TILE, kl = sb + SM::KLO + bf * SM::TILE;
+        const uint64_t dkh = tc_sdesc(sb + SM::KHI + bf * SM::TILE, 128, 2048);
+        const uint64_t dkl = tc_sdesc(sb + SM::KLO + bf * SM::TILE, 128, 2048);
         const uint32_t dS = tmem + kTcS + kTcTok * (TC::NS == 2 ? (ks & 1) : 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, kk > 0 ? 1u : 0u);
-          tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * kk, tc_sdesc(kh + 256 * kk, 128, 2048), idS, 1u);
-          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, tc_sdesc(kl + 256 * kk, 128, 2048), idS, 1u);
+          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, dkh + 16u * kk, idS, kk > 0 ? 1u : 0u);
+          tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * kk, dkh + 16u * kk, idS, 1u);
+          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, dkl + 16u * kk, idS, 1u);
         }
         if constexpr (KQ) {  // + (c S_K q_rot) (rho_K (2 sigma - 1))^T, A from shared memory
-          const uint32_t kss = sb + SM::KS + bf * SM::TILE;
+          const uint64_t dq = tc_sdesc(sb + SM::QSK, 128, 2048), dks = tc_sdesc(sb + SM::KS + bf * SM::TILE, 128, 2048);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc_mma_f16(dS, tc_sdesc(sb + SM::QSK + 256 * kk, 128, 2048), tc_sdesc(kss + 256 * kk, 128, 2048), idS, 1u);
+          for (int kk = 0; kk < 8; ++kk) tc_mma_f16(dS, dq + 16u * kk, dks + 16u * kk, idS, 1u);
         }
         tc_commit(B_S + 8 * (TC::NS == 2 ? (ks & 1) : 0));
         ++ks;
