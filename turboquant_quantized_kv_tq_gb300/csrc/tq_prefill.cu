@@ -431,38 +431,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     }
   }
 
-  if (warp == kTcIssueWarp && lane == 0) {
+  // The issue form per variant (measured): with a key sketch (both operands of its MMAs in shared
+  // memory) the whole warp runs the issue loop and one elected lane issues, which keeps every
+  // descriptor warp-uniform (QKQV n=4 11.27 -> 10.08 ms); without one a single lane issues
+  // (warp-wide was 0.8 % slower for Plain / TQ and 5 % for KQV).
+  constexpr bool kWarpIssue = KQ;
+  if (warp == kTcIssueWarp && (kWarpIssue || lane == 0)) {
     // ---- MMA issue, each as soon as its inputs are ready: the readout of tile kr once its P is
     // written (checked first: it is what the rows wait for), the scores of tile ks once it is
     // unpacked and at most one tile ahead of the readouts (S(ks) reuses S(ks - 2)'s columns, free
     // once P(ks - 2) has been read).  A tile's 24 score MMAs go back to back.
+    // Warp-wide (kWarpIssue): one elected lane issues each MMA and commit, and every poll takes
+    // lane 0's answer, so the warp never diverges.
     constexpr uint32_t idS = tc_idesc_f16(128, kTcTok), idO = tc_idesc_f16(128, kPfD, true);
+    auto test = [&](uint32_t bar, uint32_t parity) {
+      if constexpr (kWarpIssue) return __shfl_sync(kFull, tc_mbar_test(bar, parity) ? 1 : 0, 0) != 0;
+      else return tc_mbar_test(bar, parity);
+    };
+    auto mma_ta = [&](uint32_t d, uint32_t a, uint64_t bd, uint32_t id, uint32_t acc) {
+      if constexpr (kWarpIssue) tc_mma_f16_ta_w(d, a, bd, id, acc);
+      else tc_mma_f16_ta(d, a, bd, id, acc);
+    };
+    auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
+      if constexpr (kWarpIssue) tc_mma_f16_w(d, ad, bd, id, acc);
+      else tc_mma_f16(d, ad, bd, id, acc);
+    };
+    auto commit = [&](uint32_t bar) {
+      if constexpr (kWarpIssue) tc_commit_w(bar);
+      else tc_commit(bar);
+    };
     int ks = 0, kr = 0;
     uint32_t idle = 0;
     while (kr < ntiles) {
       bool moved = false;
-      if (kr < ks && tc_mbar_test(B_P, (uint32_t)kr & 1u)) {
+      if (kr < ks && test(B_P, (uint32_t)kr & 1u)) {
         tc_fence_after();
         // each batch's descriptors from one base: a step of 256 (4096) bytes adds 16 (256) to the
         // address field, which stays below 2^14 for every shared-memory address
         const uint64_t dv = tc_sdesc(sb + SM::VV + (kr % NB) * SM::TILE, 2048, 128);
 #pragma unroll
         for (int kk = 0; kk < kTcTok / 16; ++kk)
-          tc_mma_f16_ta(tmem + kTcO, tmem + TC::P + 8 * kk, dv + 256u * kk, idO, (kr > 0 || kk > 0) ? 1u : 0u);
+          mma_ta(tmem + kTcO, tmem + TC::P + 8 * kk, dv + 256u * kk, idO, (kr > 0 || kk > 0) ? 1u : 0u);
         if constexpr (VQ) {
           const uint64_t dvs = tc_sdesc(sb + SM::VS + (kr % NB) * SM::TILE, 2048, 128);
 #pragma unroll
           for (int kk = 0; kk < kTcTok / 16; ++kk)
-            tc_mma_f16_ta(tmem + TC::OSK, tmem + TC::PSK + 8 * kk, dvs + 256u * kk, idO,
+            mma_ta(tmem + TC::OSK, tmem + TC::PSK + 8 * kk, dvs + 256u * kk, idO,
                           (kr > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(B_O + 8 * (kr % NB));
+        commit(B_O + 8 * (kr % NB));
         ++kr;
         moved = true;
       }
       // one score buffer: S(ks) only after the rows have read S(ks - 1)
-      if (ks < ntiles && ks <= kr + 1 && (TC::NS == 2 || ks == 0 || tc_mbar_test(B_SC, (uint32_t)(ks - 1) & 1u)) &&
-          tc_mbar_test(B_U + 8 * (ks % NB), (uint32_t)(ks / NB) & 1u)) {
+      if (ks < ntiles && ks <= kr + 1 && (TC::NS == 2 || ks == 0 || test(B_SC, (uint32_t)(ks - 1) & 1u)) &&
+          test(B_U + 8 * (ks % NB), (uint32_t)(ks / NB) & 1u)) {
         tc_fence_after();
         const int bf = ks % NB;
         const uint64_t dkh = tc_sdesc(sb + SM::KHI + bf * SM::TILE, 128, 2048);
@@ -470,16 +493,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         const uint32_t dS = tmem + kTcS + kTcTok * (TC::NS == 2 ? (ks & 1) : 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, dkh + 16u * kk, idS, kk > 0 ? 1u : 0u);
-          tc_mma_f16_ta(dS, tmem + kTcQlo + 8 * kk, dkh + 16u * kk, idS, 1u);
-          tc_mma_f16_ta(dS, tmem + kTcQhi + 8 * kk, dkl + 16u * kk, idS, 1u);
+          mma_ta(dS, tmem + kTcQhi + 8 * kk, dkh + 16u * kk, idS, kk > 0 ? 1u : 0u);
+          mma_ta(dS, tmem + kTcQlo + 8 * kk, dkh + 16u * kk, idS, 1u);
+          mma_ta(dS, tmem + kTcQhi + 8 * kk, dkl + 16u * kk, idS, 1u);
         }
         if constexpr (KQ) {  // + (c S_K q_rot) (rho_K (2 sigma - 1))^T, A from shared memory
           const uint64_t dq = tc_sdesc(sb + SM::QSK, 128, 2048), dks = tc_sdesc(sb + SM::KS + bf * SM::TILE, 128, 2048);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) tc_mma_f16(dS, dq + 16u * kk, dks + 16u * kk, idS, 1u);
+          for (int kk = 0; kk < 8; ++kk) mma(dS, dq + 16u * kk, dks + 16u * kk, idS, 1u);
         }
-        tc_commit(B_S + 8 * (TC::NS == 2 ? (ks & 1) : 0));
+        commit(B_S + 8 * (TC::NS == 2 ? (ks & 1) : 0));
         ++ks;
         moved = true;
       }
