@@ -164,10 +164,17 @@ constexpr uint32_t kTcCols = 512;  // the whole tensor memory: one block per SM
 constexpr uint32_t kTcQhi = 0, kTcQlo = 64, kTcS = 128, kTcO = 256;  // tensor-memory columns
 // Without a value sketch: S in two buffers (128 .. 255), P at 384 (32 columns).  With one: S in
 // one buffer (128 .. 191), P at 192, P_sk at 224, O at 256 and O_sk at 384 (the whole memory).
+// One score buffer.  Without a value sketch it is 128 columns wide (WIDE): a tile's K_hi and K_lo
+// rows sit side by side in shared memory, so Q_hi [K_hi | K_lo]^T is one N = 128 MMA per k-step
+// (full tensor rate, where N = 64 runs at about 70 %) and Q_lo K_hi^T one N = 64 MMA into the first
+// half; the rows add the halves.  With a value sketch the columns hold P_sk and O_sk instead, and
+// the three products run as N = 64 MMAs into a 64-column buffer.
 template <bool VQ> struct TcCols {
-  static constexpr int NS = VQ ? 1 : 2;  // score buffers
+  static constexpr int NS = 1;  // score buffers
+  static constexpr bool WIDE = !VQ;
   static constexpr uint32_t P = VQ ? 192 : 384, PSK = 224, OSK = 384;
   static_assert(!VQ || (PSK == P + 32 && OSK == kTcO + 128), "tensor-memory plan");
+  static_assert(VQ || kTcS + 128 <= kTcO, "tensor-memory plan");
 };
 constexpr int kTcSmemMin = 116 * 1024;  // asking for more than half the shared memory keeps one block per SM
 constexpr int kTcSmemMax = 227 * 1024;  // a block's shared memory
@@ -179,7 +186,8 @@ template <bool VQ, bool KQ>
 struct TcSmem {
   static constexpr int NB = KQ ? 2 : kTcNB;                       // tile buffers (the key sketch's tiles need the room)
   static constexpr int TILE = kTcTok * kPfD * 2;                 // 16 KiB
-  static constexpr int KHI = 0, KLO = NB * TILE, VV = 2 * NB * TILE;  // NB buffers each
+  // buffer bf: K hi at KHI + bf KSTR, K lo right after it (the wide score operand), V at VV + bf TILE
+  static constexpr int KSTR = 2 * TILE, KHI = 0, KLO = TILE, VV = 2 * NB * TILE;
   static constexpr int VS = 3 * NB * TILE;                        // value signs 2 sigma - 1 (VQ)
   static constexpr int KS = (VQ ? 4 : 3) * NB * TILE;             // key sketch rows rho (2 sigma - 1) (KQ)
   static constexpr int QSK = ((VQ ? 4 : 3) + (KQ ? 1 : 0)) * NB * TILE;  // c S_K q_rot, 128 rows (KQ), K-major A
@@ -412,8 +420,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
                 ok ? nv * __half2float(*reinterpret_cast<const __half*>(vp + vr_off + 2 * pos)) : 0.f;
         }
         const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
-        *reinterpret_cast<uint4*>(smem + SM::KHI + bf * SM::TILE + off) = khi;
-        *reinterpret_cast<uint4*>(smem + SM::KLO + bf * SM::TILE + off) = klo;
+        *reinterpret_cast<uint4*>(smem + SM::KHI + bf * SM::KSTR + off) = khi;
+        *reinterpret_cast<uint4*>(smem + SM::KLO + bf * SM::KSTR + off) = klo;
         *reinterpret_cast<uint4*>(smem + SM::VV + bf * SM::TILE + off) = vv;
         if (c == 0) {
           reinterpret_cast<float*>(smem + SM::NUK)[kTcTok * bf + j] = nk;
@@ -439,11 +447,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
   if (warp == kTcIssueWarp && (kWarpIssue || lane == 0)) {
     // ---- MMA issue, each as soon as its inputs are ready: the readout of tile kr once its P is
     // written (checked first: it is what the rows wait for), the scores of tile ks once it is
-    // unpacked and at most one tile ahead of the readouts (S(ks) reuses S(ks - 2)'s columns, free
-    // once P(ks - 2) has been read).  A tile's 24 score MMAs go back to back.
+    // unpacked, at most one tile ahead of the readouts, and once the rows have read S(ks - 1) (one
+    // score buffer).  A tile's score MMAs go back to back.
     // Warp-wide (kWarpIssue): one elected lane issues each MMA and commit, and every poll takes
     // lane 0's answer, so the warp never diverges.
     constexpr uint32_t idS = tc_idesc_f16(128, kTcTok), idO = tc_idesc_f16(128, kPfD, true);
+    constexpr uint32_t idS2 = tc_idesc_f16(128, 2 * kTcTok);
     auto test = [&](uint32_t bar, uint32_t parity) {
       if constexpr (kWarpIssue) return __shfl_sync(kFull, tc_mbar_test(bar, parity) ? 1 : 0, 0) != 0;
       else return tc_mbar_test(bar, parity);
@@ -488,14 +497,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
           test(B_U + 8 * (ks % NB), (uint32_t)(ks / NB) & 1u)) {
         tc_fence_after();
         const int bf = ks % NB;
-        const uint64_t dkh = tc_sdesc(sb + SM::KHI + bf * SM::TILE, 128, 2048);
-        const uint64_t dkl = tc_sdesc(sb + SM::KLO + bf * SM::TILE, 128, 2048);
+        const uint64_t dkh = tc_sdesc(sb + SM::KHI + bf * SM::KSTR, 128, 2048);
+        const uint64_t dkl = tc_sdesc(sb + SM::KLO + bf * SM::KSTR, 128, 2048);
         const uint32_t dS = tmem + kTcS + kTcTok * (TC::NS == 2 ? (ks & 1) : 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_ta(dS, tmem + kTcQhi + 8 * kk, dkh + 16u * kk, idS, kk > 0 ? 1u : 0u);
-          mma_ta(dS, tmem + kTcQlo + 8 * kk, dkh + 16u * kk, idS, 1u);
-          mma_ta(dS, tmem + kTcQhi + 8 * kk, dkl + 16u * kk, idS, 1u);
+          if constexpr (TC::WIDE) {  // [K_hi | K_lo]: 128 rows from dkh
+            mma_ta(dS, tmem + kTcQhi + 8 * kk, dkh + 16u * kk, idS2, kk > 0 ? 1u : 0u);
+            mma_ta(dS, tmem + kTcQlo + 8 * kk, dkh + 16u * kk, idS, 1u);
+          } else {
+            mma_ta(dS, tmem + kTcQhi + 8 * kk, dkh + 16u * kk, idS, kk > 0 ? 1u : 0u);
+            mma_ta(dS, tmem + kTcQlo + 8 * kk, dkh + 16u * kk, idS, 1u);
+            mma_ta(dS, tmem + kTcQhi + 8 * kk, dkl + 16u * kk, idS, 1u);
+          }
         }
         if constexpr (KQ) {  // + (c S_K q_rot) (rho_K (2 sigma - 1))^T, A from shared memory
           const uint64_t dq = tc_sdesc(sb + SM::QSK, 128, 2048), dks = tc_sdesc(sb + SM::KS + bf * SM::TILE, 128, 2048);
@@ -532,6 +546,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       tc_fence_after();
       float s[32];
       tc_ld32(trow + kTcS + kTcTok * sbf + 32 * hf, s);
+      if constexpr (TC::WIDE) {  // + Q_hi K_lo^T from the second half
+        float s2[32];
+        tc_ld32(trow + kTcS + kTcTok + 32 * hf, s2);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[j] += s2[j];
+      }
       if constexpr (TC::NS == 1) {  // the score columns may take the next tile's scores
         tc_fence_before();
         tc_mbar_arrive(B_SC);
