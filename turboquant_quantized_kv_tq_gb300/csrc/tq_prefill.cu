@@ -195,7 +195,8 @@ struct TcSmem {
   static constexpr int NUV = NUK + NB * kTcTok * 4;               // float [NB][kTcTok]
   static constexpr int FV = NUV + NB * kTcTok * 4;                // nu_V rho_V, float [NB][kTcTok] (VQ)
   static constexpr int CENT = FV + (VQ ? NB * kTcTok * 4 : 0);    // [16] (K hi | K lo << 16), [16] V fp16
-  static constexpr int XCH = CENT + 128;  // float [3][2 halves][128 rows]: maxima (by tile parity), then l
+  static constexpr int SGN = CENT + 128;  // uint2 [16]: the fp16 sign fields of four signs (a nibble)
+  static constexpr int XCH = SGN + 128;   // float [3][2 halves][128 rows]: maxima (by tile parity), then l
   static constexpr int STG = (XCH + 3 * 2 * 128 * 4 + 127) / 128 * 128;  // NB packed stages
   static_assert(VS == VV + NB * TILE && KS >= VS && QSK >= KS, "shared-memory plan");
 };
@@ -297,6 +298,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
   } else if (tid < 32) {
     reinterpret_cast<__half*>(smem + SM::CENT + 64)[tid - 16] = __float2half_rn(__ldg(p.tab.v_c + tid - 16));
+  } else if (tid < 48) {  // nibble n: signs 0..3 (a set bit is +) as the sign fields of two fp16 pairs
+    const uint32_t n = (uint32_t)tid - 32;
+    reinterpret_cast<uint2*>(smem + SM::SGN)[n] =
+        make_uint2((~n & 1u) << 15 | ((~n >> 1) & 1u) << 31, ((~n >> 2) & 1u) << 15 | ((~n >> 3) & 1u) << 31);
   }
   tc_fence_before();
   __syncthreads();
@@ -356,6 +361,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     const int kbyte = kbits == 1 ? c : kbits == 4 ? 4 * c : 2 * c;  // the chunk's first code byte in a key record
     const float kscale = p.score_scale;
     const uint32_t* kcent = reinterpret_cast<const uint32_t*>(smem + SM::CENT);
+    const uint2* sgn = reinterpret_cast<const uint2*>(smem + SM::SGN);
     const unsigned short* vcent = reinterpret_cast<const unsigned short*>(smem + SM::CENT + 64);
     const int g = c >> 1, hv = c & 1;  // the chunk's 16-coordinate value group and half of it
     for (int k = 0; k < ntiles; ++k) {
@@ -395,26 +401,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
           nk = ok ? *reinterpret_cast<const float*>(kp + kn_off + 4 * pos) * kscale : 0.f;  // nu_K log2(e) / sqrt(d)
           nv = ok ? *reinterpret_cast<const float*>(vp + vn_off + 4 * pos) : 0.f;
         }
+        // the sign fields of a byte of sketch signs: two table entries, one per nibble
+        auto sign_fields = [&](uint32_t sgb, uint32_t mag2) {
+          const uint2 a = sgn[sgb & 15u], bq = sgn[sgb >> 4];
+          const uint32_t z = ok ? 0xffffffffu : 0u;
+          return make_uint4((a.x | mag2) & z, (a.y | mag2) & z, (bq.x | mag2) & z, (bq.y | mag2) & z);
+        };
         if constexpr (KQ) {  // the key sketch's rows rho_K (2 sigma - 1): token-major 16-byte sign records
           const uint32_t sgb = kp[ks_off + pos * ks_rec + c];
           const uint32_t rh = (uint32_t)__half_as_ushort(*reinterpret_cast<const __half*>(kp + kr_off + 2 * pos));
-          uint32_t sw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            sw[e] = ((rh | rh << 16) | ((~sgb >> (2 * e)) & 1u) << 15 | ((~sgb >> (2 * e + 1)) & 1u) << 31) &
-                    (ok ? 0xffffffffu : 0u);
           const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
-          *reinterpret_cast<uint4*>(smem + SM::KS + bf * SM::TILE + off) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+          *reinterpret_cast<uint4*>(smem + SM::KS + bf * SM::TILE + off) = sign_fields(sgb, rh | rh << 16);
         }
         if constexpr (VQ) {  // the value sketch's signs as +-1 (stream by 16-coordinate groups) and nu_V rho_V
           const uint32_t sgb = vp[vs_off + g * 32 + pos * 2 + hv];
-          uint32_t sw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            sw[e] = (0x3C003C00u | ((~sgb >> (2 * e)) & 1u) << 15 | ((~sgb >> (2 * e + 1)) & 1u) << 31) &
-                    (ok ? 0xffffffffu : 0u);
           const int off = (j >> 3) * 2048 + c * 128 + (j & 7) * 16;
-          *reinterpret_cast<uint4*>(smem + SM::VS + bf * SM::TILE + off) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+          *reinterpret_cast<uint4*>(smem + SM::VS + bf * SM::TILE + off) = sign_fields(sgb, 0x3C003C00u);
           if (c == 0)
             reinterpret_cast<float*>(smem + SM::FV)[kTcTok * bf + j] =
                 ok ? nv * __half2float(*reinterpret_cast<const __half*>(vp + vr_off + 2 * pos)) : 0.f;
