@@ -21,6 +21,7 @@
 // undiluted.
 #include <algorithm>
 #include <string>
+#include <type_traits>
 
 #include "tq_device.cuh"
 #include "tq_tc05.cuh"
@@ -370,10 +371,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
       if (k >= NB && !mbar_wait(B_O + 8 * bf, (uint32_t)(k / NB - 1) & 1u, kPfWaitLimit)) timed_out = true;
       if (!mbar_wait(B_STG + 8 * bf, (uint32_t)(k / NB) & 1u, kPfWaitLimit)) timed_out = true;
       const unsigned char* stg = smem + SM::STG + bf * SB;
+      // FULL: every token of the tile is inside the sequence (all but a sequence's last tile), so
+      // nothing is masked
+      auto unpack_tile = [&](auto full_c) {
+      constexpr bool FULL = decltype(full_c)::value;
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         const int j = 8 * (jg0 + 2 * it) + t8, pos = j & (tqi::kTileTokens - 1);
-        const bool ok = t0 + j < L;
+        const bool ok = FULL || t0 + j < L;
         const unsigned char* kp = stg + (j >> 4) * kblk;             // the token's K block
         const unsigned char* vp = stg + kTcBlk * kblk + (j >> 4) * vblk;  // and V block
         // (tokens past the sequence: the stage holds stale bytes there, read but replaced by zeros)
@@ -430,6 +435,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
           reinterpret_cast<float*>(smem + SM::NUV)[kTcTok * bf + j] = nv;
         }
       }
+      };
+      if (t0 + kTcTok <= L) unpack_tile(std::true_type());
+      else unpack_tile(std::false_type());
       tc_fence_smem();  // the tile's rows are visible to the tensor cores' operand reads
       tc_mbar_arrive(B_U + 8 * bf);
       asm volatile("bar.sync 1, 256;\n" ::: "memory");  // every unpacking thread is done with the stage
