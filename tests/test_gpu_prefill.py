@@ -59,13 +59,13 @@ def _run(scheme, n, nq, G, lens, T, seed, name="cfg2"):
     return pair, qm, got
 
 
-@pytest.mark.parametrize("scheme,n", [("plain", 4), ("tq", 4), ("tq", 2), ("kqv", 4), ("kqv", 2),
+@pytest.mark.parametrize("scheme,n", [("plain", 4), ("tq", 4), ("tq", 2), ("kqv", 4), ("kqv", 3), ("kqv", 2),
                                       ("qkqv", 4), ("qkqv", 3), ("plain", 1), ("tq", 3)])
 def test_prefill_schemes_nq128(scheme, n):
     _run(scheme, n, nq=128, G=4, lens=[700, 311], T=700, seed=70)
 
 
-# KQV runs the mma.sync kernel (a QJL value side), TQ-KV the tcgen05 one (no sketch)
+# KQV (a QJL value side: 64-column scores, the value sketch readout) and TQ-KV (no sketch: wide scores)
 @pytest.mark.parametrize("scheme", ["kqv", "tq"])
 @pytest.mark.parametrize("nq,G,lens", [(16, 4, [333, 16, 9]), (512, 4, [900, 600]), (512, 1, [777, 513]),
                                        (128, 8, [640, 129])])

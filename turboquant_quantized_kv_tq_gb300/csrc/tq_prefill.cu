@@ -242,6 +242,16 @@ __device__ __forceinline__ uint32_t codes8(const unsigned char* src, const unsig
 __device__ __forceinline__ void tc_out_row(const PrefillParams& p, int b, int h, int rr, uint32_t t_o, float il, int hf,
                                            uint32_t t_add);
 
+// 3-bit codes without shared-memory lookups: a pair's two 2-bit magnitudes select its two fp16
+// magnitudes from a four-entry table held in two registers (t0 = mag0 | mag1 << 16, t1 = mag2 |
+// mag3 << 16) with one byte permute.  m: spread2 of the chunk's magnitude bytes (coordinate i's
+// magnitude in bits 4 i, 4 i + 1); the selector of pair e has nibbles 2 m0, 2 m0 + 1, 2 m1, 2 m1 + 1.
+__device__ __forceinline__ uint32_t mag_pair(uint32_t t0, uint32_t t1, uint32_t m, int e) {
+  const uint32_t t = (m >> (8 * e)) & 0x33u;            // m0 in bits 0-1, m1 in bits 4-5
+  const uint32_t u = (t & 0x3u) | ((t & 0x30u) << 4);   // m1 to bits 8-9
+  return __byte_perm(t0, t1, u * 0x22u + 0x1010u);
+}
+
 // KB, VB: the key and value code widths as compile-time constants (0: read from the parameters).
 // VQ: a QJL value side -- its sketch readout O_sk += P_sk (2 sigma_V - 1), P_sk = p nu_V rho_V,
 // rides beside the code readout, and the epilogue adds c S_V^T O_sk / l as one more MMA.
@@ -362,6 +372,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
     const int kbyte = kbits == 1 ? c : kbits == 4 ? 4 * c : 2 * c;  // the chunk's first code byte in a key record
     const float kscale = p.score_scale;
     const uint32_t* kcent = reinterpret_cast<const uint32_t*>(smem + SM::CENT);
+    // 3-bit sides: the upper half of the symmetric codebook (the magnitudes) in registers, fp16 hi
+    // and lo terms for the keys, fp16 for the values
+    auto mag2 = [&](const float* cent, int m0, bool lo_term) {
+      const float a = __ldg(cent + 4 + m0), b2 = __ldg(cent + 5 + m0);
+      const __half ha = __float2half_rn(a), hb = __float2half_rn(b2);
+      const __half xa = lo_term ? __float2half_rn(a - __half2float(ha)) : ha;
+      const __half xb = lo_term ? __float2half_rn(b2 - __half2float(hb)) : hb;
+      return (uint32_t)__half_as_ushort(xa) | ((uint32_t)__half_as_ushort(xb) << 16);
+    };
+    uint32_t kmh0 = 0, kmh1 = 0, kml0 = 0, kml1 = 0, vm0 = 0, vm1 = 0;
+    if constexpr (KB == 3) {
+      kmh0 = mag2(p.tab.k_c, 0, false); kmh1 = mag2(p.tab.k_c, 2, false);
+      kml0 = mag2(p.tab.k_c, 0, true);  kml1 = mag2(p.tab.k_c, 2, true);
+    }
+    if constexpr (VB == 3) {
+      vm0 = mag2(p.tab.v_c, 0, false); vm1 = mag2(p.tab.v_c, 2, false);
+    }
     const uint2* sgn = reinterpret_cast<const uint2*>(smem + SM::SGN);
     const unsigned short* vcent = reinterpret_cast<const unsigned short*>(smem + SM::CENT + 64);
     const int g = c >> 1, hv = c & 1;  // the chunk's 16-coordinate value group and half of it
@@ -386,18 +413,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const Prefill
         float nk, nv;
         {
           const unsigned char* kr = kp + kc_off + pos * kc_rec;
-          const uint32_t kc = codes8<KB>(kr + kbyte, kr + kPfD / 4 + c, kbits);
           // value streams by 16-coordinate groups: W bytes of the W-bit stream per chunk
           const unsigned char* vr = vp + vc_off;
-          const uint32_t vc = codes8<VB>(vr + g * 32 * vW + pos * 2 * vW + hv * vW,
-                                         vr + tqi::kTileTokens * (kPfD / 4) + g * 32 + pos * 2 + hv, vbits);
+          const unsigned char* vsrc = vr + g * 32 * vW + pos * 2 * vW + hv * vW;
+          const unsigned char* vsgn = vr + tqi::kTileTokens * (kPfD / 4) + g * 32 + pos * 2 + hv;
           uint32_t kh[4], kl[4], vw[4];
+          if constexpr (KB == 3) {  // magnitudes from registers, signs (a set bit is +) by nibble table
+            const uint32_t m = spread2(*reinterpret_cast<const unsigned short*>(kr + kbyte));
+            const uint32_t sb = kr[kPfD / 4 + c];
+            const uint2 s0 = sgn[sb & 15u], s1 = sgn[sb >> 4];
+            const uint32_t sf[4] = {s0.x, s0.y, s1.x, s1.y};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t a = kcent[(kc >> (8 * e)) & 15u], bq = kcent[(kc >> (8 * e + 4)) & 15u];
-            kh[e] = __byte_perm(a, bq, 0x5410);
-            kl[e] = __byte_perm(a, bq, 0x7632);
-            vw[e] = (uint32_t)vcent[(vc >> (8 * e)) & 15u] | ((uint32_t)vcent[(vc >> (8 * e + 4)) & 15u] << 16);
+            for (int e = 0; e < 4; ++e) {  // (the lo term of -c is -lo(c): the sign flips both)
+              kh[e] = mag_pair(kmh0, kmh1, m, e) ^ sf[e];
+              kl[e] = mag_pair(kml0, kml1, m, e) ^ sf[e];
+            }
+          } else {
+            const uint32_t kc = codes8<KB>(kr + kbyte, kr + kPfD / 4 + c, kbits);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t a = kcent[(kc >> (8 * e)) & 15u], bq = kcent[(kc >> (8 * e + 4)) & 15u];
+              kh[e] = __byte_perm(a, bq, 0x5410);
+              kl[e] = __byte_perm(a, bq, 0x7632);
+            }
+          }
+          if constexpr (VB == 3) {
+            const uint32_t m = spread2(*reinterpret_cast<const unsigned short*>(vsrc));
+            const uint32_t sb = *vsgn;
+            const uint2 s0 = sgn[sb & 15u], s1 = sgn[sb >> 4];
+            vw[0] = mag_pair(vm0, vm1, m, 0) ^ s0.x;
+            vw[1] = mag_pair(vm0, vm1, m, 1) ^ s0.y;
+            vw[2] = mag_pair(vm0, vm1, m, 2) ^ s1.x;
+            vw[3] = mag_pair(vm0, vm1, m, 3) ^ s1.y;
+          } else {
+            const uint32_t vc = codes8<VB>(vsrc, vsgn, vbits);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              vw[e] = (uint32_t)vcent[(vc >> (8 * e)) & 15u] | ((uint32_t)vcent[(vc >> (8 * e + 4)) & 15u] << 16);
           }
           const uint32_t z = ok ? 0xffffffffu : 0u;
           khi = make_uint4(kh[0] & z, kh[1] & z, kh[2] & z, kh[3] & z);
