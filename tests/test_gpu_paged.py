@@ -126,6 +126,30 @@ def test_paged_many_tiles_matches_contiguous_bitwise():
     assert rel_err(out, ref) <= ATTN_TOL, rel_err(out, ref)
 
 
+def test_paged_split_with_boundary_allowance_matches_contiguous_bitwise():
+    # the lengths of the contiguous split test: the device-computed split (with its boundary
+    # allowance above zero and blocks whose ranges hold no real tile) equals the host one
+    import torch
+    from turboquant_quantized_kv_tq_gb300 import QuantizedKVCache
+    lens = [8192] + [0] * 6 + [5000, 8192, 16] + [0] * 6
+    inp = small_inputs("cfg2", B=16, T=8192, Hkv=2, seed=43)
+    pp = PagedPair(inp, "kqv", 4, max_blocks=512, seed=44)
+    for s in range(0, inp.T, 4096):
+        assert pp.append(s, s + 4096) == 0
+    kc, vc = scheme_codecs("kqv", 4)
+    flat = QuantizedKVCache(inp.d, inp.Hq, inp.Hkv, inp.B, 8192, scheme=None, seed=inp.seed,
+                            k_codec=(kc.bits, int(kc.rotate), int(kc.qjl)),
+                            v_codec=(vc.bits, int(vc.rotate), int(vc.qjl)))
+    for s in range(0, inp.T, 4096):
+        flat.append(to_torch(inp.K[:, :, s:s + 4096], inp.dtype).cuda(),
+                    to_torch(inp.V[:, :, s:s + 4096], inp.dtype).cuda(), [s] * inp.B)
+    out = pp.decode(inp.q, lens)
+    ref_flat = flat.decode(torch.from_numpy(inp.q).cuda(), lens).cpu().numpy().astype(np.float64)
+    assert np.array_equal(out, ref_flat)
+    ref = pp.orc.decode(pp.gathered(), inp.q, lens)
+    assert rel_err(out, ref) <= ATTN_TOL, rel_err(out, ref)
+
+
 def test_paged_per_sequence_starts_and_multi_query():
     # each sequence appends at its own device start; the chunk's last two positions decode at once
     import torch

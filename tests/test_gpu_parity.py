@@ -119,6 +119,26 @@ def test_sequence_length_edge_cases(lens):
     assert rel_err(out, ref) <= ATTN_TOL
 
 
+# Lengths whose tile count gives the decode's split a boundary allowance above zero (at least 8
+# tiles per block on a 152-SM GPU), runs of empty sequences long enough that some blocks' ranges
+# hold no real tile, a one-tile sequence, and slab boundaries inside block ranges.
+SPLIT_LENS = [8192] + [0] * 6 + [5000, 8192, 16] + [0] * 6
+
+
+@pytest.mark.parametrize("scheme,n", [("tq", 4), ("kqv", 4), ("qkqv", 3)])
+def test_split_with_boundary_allowance(scheme, n):
+    inp = small_inputs("cfg2", B=16, T=8192, Hkv=2, seed=11)
+    pair = Pair(inp, scheme, n)
+    pair.append_gpu(chunk=4096)
+    buf = pair.gpu_bytes()
+    out = pair.decode_gpu(SPLIT_LENS)
+    ref = pair.orc.decode(buf, inp.q, SPLIT_LENS)
+    for b, L in enumerate(SPLIT_LENS):
+        if L == 0:
+            assert np.all(out[b] == 0)
+    assert rel_err(out, ref) <= ATTN_TOL, rel_err(out, ref)
+
+
 def test_ragged_starts_and_full_capacity():
     inp = small_inputs("cfg2", B=3, T=128, Hkv=2, seed=6)
     pair = Pair(inp, "tq", 3, capacity=128)

@@ -12,8 +12,10 @@
 // o = R_V^T (acc + sqrt(pi/2)/m S_V^T acc_sk) / l once per head.
 //
 // Work split (balanced, "stream-K"): the (batch, KV head, token) positions of all sequences are
-// laid end to end and cut into one equal contiguous range per block, one block per SM.  A block
-// walks the slab segments of its range; for each, its warps stream contiguous sub-ranges in
+// laid end to end and cut into one equal contiguous range per block, one block per SM, counting
+// a fixed allowance of virtual tiles before each slab so that a block whose range crosses a slab
+// boundary takes fewer real tiles.  A block walks the slab segments of its range; for each, its
+// warps stream contiguous sub-ranges in
 // tiles of 16 tokens and the block merges them into one partial per (slab, block).  The last
 // block to finish a slab (atomic ticket) merges that slab's partials in block order and writes
 // the output.  Per tile:
@@ -1100,6 +1102,9 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
   constexpr int PS = SM::PS;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_last;
+  __shared__ float s_wscale[SM::NW][kHeadsPad];  // block merge: 2^(m_w - M) of warp w, column h
+  __shared__ float s_wmax[kHeadsPad];            // block merge: M of column h
+  __shared__ long long s_split[2];               // the split's P and virtual tile count
   __shared__ int s_page_err[SM::NW];  // paged: a bad table entry met before the first wait
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lg = lane >> 2, lt = lane & 3;
@@ -1152,8 +1157,40 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     }
     return;
   }
-  long long x = (long long)blockIdx.x * W / N;
-  const long long x_end = (long long)(blockIdx.x + 1) * W / N;
+  // The split runs over virtual tiles: every slab counts P tiles before its first real one, and
+  // the virtual space is cut into N equal ranges.  A block whose range crosses into a slab so
+  // gets P real tiles fewer for each crossing, which pays for what a segment boundary costs it
+  // (the ring drained and refilled, a partial written, the per-warp split rounded once more).
+  // With P = 0 the virtual and the real tiles coincide.  A range that lies inside a slab's P
+  // virtual tiles holds no real tile; such a block owns no tile of any slab and does nothing.
+  // (P and the virtual count go to shared memory for the merges, so no register holds them
+  // through the streaming loop.)  The variants with separate query lo terms or a HeadQ side
+  // keep the plain equal split (EQS): their register allocation is at its limit.
+  constexpr bool EQS = QLO || KH;
+  long long x, x_end;
+  {
+    const long long P = EQS ? 0 : W / N / 8;
+    const long long Wv = W + P * p.Hkv * p.B;
+    if (threadIdx.x == 0) { s_split[0] = P; s_split[1] = Wv; }
+    auto real_tile = [&](long long v) -> long long {  // the first real tile at or after virtual v
+      int lo = 0, hi = p.B - 1;  // largest b with its virtual start <= v
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (bstart(mid) + P * p.Hkv * mid <= v) lo = mid; else hi = mid - 1;
+      }
+      const long long nt = (slen(lo) + kTile - 1) / kTile;
+      if (nt == 0) return bstart(lo);
+      const long long off = v - (bstart(lo) + P * p.Hkv * lo), k = off / (nt + P), o = off % (nt + P);
+      return bstart(lo) + k * nt + (o > P ? o - P : 0);
+    };
+    if constexpr (EQS) {
+      x = (long long)blockIdx.x * W / N;
+      x_end = (long long)(blockIdx.x + 1) * W / N;
+    } else {
+      x = real_tile((long long)blockIdx.x * Wv / N);
+      x_end = real_tile((long long)(blockIdx.x + 1) * Wv / N);
+    }
+  }
   unsigned seq = 0;  // tile pairs this warp has streamed so far: stage seq % S, phase (seq / S) & 1
   bool timed_out = false;
   bool waited = false;  // grid_dependency_wait has returned
@@ -1384,33 +1421,44 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
       }
     }
     __syncthreads();
-    float* part_out = p.part + ((long long)(pair + blockIdx.x) * Gc) * PS;
-    for (int idx = threadIdx.x; idx < Gc * PS; idx += blockDim.x) {
-      const int h = idx / PS, e = idx % PS;
+    // each column's maximum over the warps and each warp's scale, once per column
+    if (threadIdx.x < Gc) {
+      const int h = threadIdx.x;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < SM::NW; ++w) M = fmaxf(M, reinterpret_cast<const float*>(win + SM::region(w))[h * PS]);
-      float v;
-      if (e == 0) {
-        v = M;
-      } else if (!MV && (e == 2 || e == 3)) {
-        v = 0.f;
-      } else {
-        v = 0.f;
-        if (M != -INFINITY) {
+      s_wmax[h] = M;
 #pragma unroll
-          for (int w = 0; w < SM::NW; ++w) {
-            const float* mbw = reinterpret_cast<const float*>(win + SM::region(w)) + h * PS;
-            v = fmaf(exp2f(mbw[0] - M), mbw[e], v);
-          }
-        }
+      for (int w = 0; w < SM::NW; ++w)
+        s_wscale[w][h] = M != -INFINITY ? exp2f(reinterpret_cast<const float*>(win + SM::region(w))[h * PS] - M) : 0.f;
+    }
+    __syncthreads();
+    float* part_out = p.part + ((long long)(pair + blockIdx.x) * Gc) * PS;
+    for (int idx = threadIdx.x; idx < Gc * PS; idx += blockDim.x) {
+      const int h = idx / PS, e = idx % PS;
+      float v = 0.f;
+      if (e == 0) {
+        v = s_wmax[h];
+      } else if (MV || (e != 2 && e != 3)) {
+#pragma unroll
+        for (int w = 0; w < SM::NW; ++w)
+          v = fmaf(s_wscale[w][h], reinterpret_cast<const float*>(win + SM::region(w))[h * PS + e], v);
       }
       part_out[h * PS + e] = v;
     }
 
     // ---- the last block of this slab merges all its partials
-    const int c_first = owner_block(slab_start, W, N);
-    const int c_last = owner_block(slab_start + ntb - 1, W, N);
+    int c_first, c_last;
+    if constexpr (EQS) {
+      c_first = owner_block(slab_start, W, N);
+      c_last = owner_block(slab_start + ntb - 1, W, N);
+    } else {
+      const long long P = *reinterpret_cast<volatile long long*>(s_split);
+      const long long Wv = *reinterpret_cast<volatile long long*>(s_split + 1);
+      const long long vslab = slab_start + P * (pair + 1);  // its first real tile, slab pair
+      c_first = owner_block(vslab, Wv, N);
+      c_last = owner_block(vslab + ntb - 1, Wv, N);
+    }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1433,23 +1481,27 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accs = make_float4(0.f, 0.f, 0.f, 0.f);
         float Wc = 0.f, Ws = 0.f;  // weight sums of the masked operands (MV)
         if constexpr (MV) {
-          // the partials' maxima, denominators and weight sums are read lane-parallel (lane s
-          // takes partial s, 32 at a time): a slab spread over many blocks (long contexts, few
-          // slabs) would otherwise pay one dependent L2 round trip per partial
-          for (int s0 = 0; s0 < ns; s0 += 32)
+          // the partials' maxima, denominators and weight sums (a partial's first four floats)
+          // are read lane-parallel as one float4 (lane s takes partial s, 32 at a time): a slab
+          // spread over many blocks (long contexts, few slabs) would otherwise pay one dependent
+          // L2 round trip per partial
+          auto header = [&](int s) {
+            return s < ns ? __ldcg(reinterpret_cast<const float4*>(base + (long long)s * sstride))
+                          : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+          };
+          float4 hd = header(lane);
+          M = hd.x;
+          for (int s0 = 32; s0 < ns; s0 += 32)
             if (s0 + lane < ns) M = fmaxf(M, __ldcg(base + (s0 + lane) * sstride));
           M = warp_max(M);
           if (M != -INFINITY) {
             for (int s0 = 0; s0 < ns; s0 += 32) {
               const int nn = min(32, ns - s0);
-              float wl = 0.f;
-              if (lane < nn) {
-                const float* ps = base + (s0 + lane) * sstride;
-                wl = exp2f(__ldcg(ps) - M);
-                L2 = fmaf(wl, __ldcg(ps + 1), L2);
-                Wc = fmaf(wl, __ldcg(ps + 2), Wc);
-                Ws = fmaf(wl, __ldcg(ps + 3), Ws);
-              }
+              if (s0 > 0) hd = header(s0 + lane);
+              const float wl = lane < nn ? exp2f(hd.x - M) : 0.f;
+              L2 = fmaf(wl, hd.y, L2);
+              Wc = fmaf(wl, hd.z, Wc);
+              Ws = fmaf(wl, hd.w, Ws);
 #pragma unroll 4
               for (int i = 0; i < nn; ++i) {
                 const float w = __shfl_sync(kFull, wl, i);
