@@ -1,7 +1,8 @@
 """GPU parity on the method's edge cases, through the C ABI against the oracle:
 
 * zero K / V vectors (norm 0, every code by the tie rule, residual -C[c] with its signs and
-  rho), on both sketch paths (FFMA for small appends, tensor cores for large ones);
+  rho), on both sketch paths (16-vector `mma.sync` blocks for small appends, 64-vector
+  `tcgen05` blocks for large ones; each re-takes near-zero products in fp32 FFMA);
 * coordinates exactly on an fp32 decision threshold (Plain-KV with exact unit-norm fp32
   vectors, so y = x on both sides): a tie is a decision both sides must take the same way
   (the lower cell), so these codes are compared with no exemption;
@@ -22,8 +23,8 @@ from workloads import Inputs
 
 pytestmark = pytest.mark.gpu
 
-SMALL_CHUNK = 16   # 2 x 2 slabs x 16 tokens = 64 vectors per side: the FFMA sketch path
-LARGE_CHUNK = 150  # 600 vectors per side: the tensor-core sketch path
+SMALL_CHUNK = 16   # 2 x 2 slabs x 16 tokens = 64 vectors per side: the 16-vector mma.sync sketch
+LARGE_CHUNK = 150  # 600 vectors per side: the 64-vector tcgen05 sketch
 
 
 def _all_slabs(pair, T):
