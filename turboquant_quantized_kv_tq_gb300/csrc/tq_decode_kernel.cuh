@@ -1468,6 +1468,16 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
     __syncthreads();
     if (s_last) {
       __threadfence();
+      // (2)'s rows of S_V, requested now so that their latency overlaps (1)
+      constexpr int RPW = (kDecD + SM::NW - 1) / SM::NW;  // sketch rows per warp
+      const int j0 = warp * RPW;
+      float4 srow[VQ ? RPW : 1];
+      if constexpr (VQ) {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+          srow[r] = j0 + r < kDecD ? __ldg(reinterpret_cast<const float4*>(p.tab.S_V + (j0 + r) * kDecD + 4 * lane))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       // (1) warp h < Gc merges query column h's partials; with a QJL value side the merged
       // acc_sk goes to shared memory for (2)
       const int h = warp;  // query column
@@ -1502,7 +1512,7 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
               L2 = fmaf(wl, hd.y, L2);
               Wc = fmaf(wl, hd.z, Wc);
               Ws = fmaf(wl, hd.w, Ws);
-#pragma unroll 4
+#pragma unroll 8
               for (int i = 0; i < nn; ++i) {
                 const float w = __shfl_sync(kFull, wl, i);
                 const float* ps = base + (s0 + i) * sstride;
@@ -1557,13 +1567,6 @@ __global__ void __launch_bounds__(DecWarps<KQ, VQ, QLO>::value * 32, 1) decode_k
         // rows, so each loads its rows of S_V once (all in flight) and applies them to every
         // column; partial sums go to shared memory and (3) adds them up
         __syncthreads();
-        constexpr int RPW = (kDecD + SM::NW - 1) / SM::NW;  // sketch rows per warp
-        const int j0 = warp * RPW;
-        float4 srow[RPW];
-#pragma unroll
-        for (int r = 0; r < RPW; ++r)
-          srow[r] = j0 + r < kDecD ? __ldg(reinterpret_cast<const float4*>(p.tab.S_V + (j0 + r) * kDecD + 4 * lane))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         float* part_sum = reinterpret_cast<float*>(win + SM::region(warp));
         for (int c = 0; c < Gc; ++c) {
           const float* a = reinterpret_cast<const float*>(win + SM::region(c) + kSkA);
